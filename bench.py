@@ -1,0 +1,482 @@
+#!/usr/bin/env python3
+"""Benchmark of libgdn on GB300: one JSON line on rank 0.
+
+Workloads (synthetic, seeded; see gated_deltanet_mixer_gb300/inputs.py):
+  prefill  Qwen3.5-4B-shaped GDN layer: B=4, T=8192, Hk=16, Hv=32, Dk=Dv=128,
+           bf16 io, fp32 state.  `value` = prefill tokens/s over all ranks.
+  decode   Qwen3.8-27B-shaped batched decode: B=256, Hk=16, Hv=48; one bench
+           step = 64 consecutive gdn_decode_step calls.  Reported under
+           "decode" as state GB/s and total GB/s against HBM.
+
+--impl reference times the fp64 CPU oracle instead, on a bounded sample of the
+same prefill workload, with the same metric and unit.
+
+Multi-GPU (torchrun): every rank runs its own full prefill batch (weak
+scaling, no collective on the data path); the max over ranks of the timed
+region sets the time.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GDN prefill tokens/s (4B/27B shapes) + decode state GB/s vs HBM peak, 1×GB300"
+D = 128
+PREFILL_KERNELS_PER_CALL = 1   # gdn_prefill launches one kernel
+DECODE_KERNELS_PER_CALL = 1    # gdn_decode_step launches one kernel
+DECODE_CALLS_PER_STEP = 64
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ------------------------------------------------------------ work counts
+def conv_channels(Hk, Hv):
+    return (2 * Hk + Hv) * D
+
+
+def prefill_bytes(B, T, Hk, Hv, io=2):
+    """Algorithmic HBM bytes of one prefill call: every input read once,
+    every output written once."""
+    C = conv_channels(Hk, Hv)
+    per_token = io * C + 2 * io * Hv * D + 8 * Hv          # qkv, z, o, g+beta
+    per_seq = 2 * Hv * D * D * 4 + 2 * 3 * C * io          # S0 + S_T, conv0 + conv_T
+    weights = C * 4 * io + D * io
+    return B * T * per_token + B * per_seq + weights
+
+
+def prefill_flops(B, T, Hk, Hv, chunk=64):
+    """Dense-contraction flops of the chunked (WY) form per call: per key
+    head Q K^T and K K^T; per value head U, W, the masked (QK^T) Delta, and
+    the three state products W S, Q S, K^T Delta."""
+    per_token = Hk * 4 * chunk * D + Hv * (3 * 2 * chunk * D + 6 * D * D)
+    return B * T * per_token
+
+
+def decode_bytes(B, Hk, Hv, io=2):
+    """Algorithmic HBM bytes of one decode call."""
+    C = conv_channels(Hk, Hv)
+    per_seq = 8 * Hv * D * D + 2 * 3 * C * io + io * C + 2 * io * Hv * D + 8 * Hv
+    return B * per_seq + C * 4 * io + D * io
+
+
+def decode_state_bytes(B, Hv):
+    return B * 8 * Hv * D * D
+
+
+# ----------------------------------------------------------------- helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {k: float(pk[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_sha(relpath):
+    with open(os.path.join(ROOT, relpath), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def recorded_traffic(kernel_key, source_relpath):
+    """DRAM bytes per launch recorded from an ncu capture, if the kernel's
+    source is unchanged since; otherwise None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(kernel_key)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("source_sha256") != source_sha(source_relpath):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+    QUERY = ("index,uuid,utilization.gpu,clocks.sm,clocks.max.sm,power.draw,"
+             "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid=None):
+        self.uuid = uuid
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        cmd = ["nvidia-smi", "--query-gpu=" + self.QUERY, "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [ln.split(", ") for ln in self.file.read().splitlines() if ln.strip()]
+        self.file.close()
+        os.unlink(self.file.name)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        load, reasons, maxes = [], set(), []
+        for r in rows:
+            if len(r) < 11:
+                continue
+            try:
+                util, sm, smax = float(r[2]), float(r[3]), float(r[4])
+            except ValueError:
+                continue
+            maxes.append(smax)
+            if util >= 50:
+                load.append(sm)
+                for n, v in zip(names, r[7:11]):
+                    if v.strip().lower() == "active":
+                        reasons.add(n)
+        return {"sm_mhz": statistics.median(load) if load else None,
+                "sm_max_mhz": max(maxes) if maxes else None,
+                "reasons": sorted(reasons), "samples_under_load": len(load),
+                "samples": len(rows)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ----------------------------------------------------------- oracle timing
+def oracle_tokens_per_s(p, budget_s, threads):
+    """Time the oracle as it stands on the first sequence of `p`, all value
+    heads, over as many leading tokens as fit in about `budget_s` seconds."""
+    from oracle import oracle as O
+
+    a = p.arrays
+
+    def run(T):
+        t0 = time.perf_counter()
+        O.gdn_prefill(a["qkv_pre"][:1, :T], a["z"][:1, :T], a["g"][:1, :T], a["beta"][:1, :T],
+                      a["conv_w"], a["norm_w"], None if a["S0"] is None else a["S0"][:1],
+                      None if a["conv0"] is None else a["conv0"][:1], Hk=p.Hk, Hv=p.Hv,
+                      threads=threads, want_conv=False)
+        return time.perf_counter() - t0
+
+    probe_T = min(p.T, 128)
+    rate = probe_T / max(run(probe_T), 1e-6)
+    T = int(max(probe_T, min(p.T, rate * budget_s)))
+    return T, run(T)
+
+
+# --------------------------------------------------------------- GPU arm
+def gdn_arm(args, world, rank, local):
+    import torch
+
+    from gated_deltanet_mixer_gb300 import build as gdn_build
+    from gated_deltanet_mixer_gb300 import gdn
+    from gated_deltanet_mixer_gb300 import inputs as I
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    gdn_build.build()
+    gdn.lib()
+    peaks, peak_src = load_peaks()
+
+    # ---- prefill inputs (each rank its own batch)
+    spec = dict(I.CASES[args.workload])
+    spec["case"] = spec["case"] + 1000 * rank
+    p = I.prefill_problem(**spec)
+    t_io = torch.bfloat16 if p.io == "bf16" else torch.float32
+    a = p.arrays
+
+    def dev(x, dt=torch.float32):
+        return None if x is None else torch.from_numpy(x).to("cuda").to(dt)
+
+    x = dict(qkv_pre=dev(a["qkv_pre"], t_io), z=dev(a["z"], t_io), g=dev(a["g"]),
+             beta=dev(a["beta"]), conv_w=dev(a["conv_w"], t_io), norm_w=dev(a["norm_w"], t_io),
+             S0=dev(a["S0"]), conv0=dev(a["conv0"], t_io))
+    o, S_T, conv_T = gdn.alloc_prefill_outputs(p.B, p.T, p.Hk, p.Hv, t_io)
+    stream = torch.cuda.current_stream()
+
+    def prefill_call(xx, oo, ss, cc):
+        gdn.gdn_prefill(xx["qkv_pre"], xx["z"], xx["g"], xx["beta"], xx["conv_w"], xx["norm_w"],
+                        xx["S0"], xx["conv0"], oo, ss, cc, Hk=p.Hk, Hv=p.Hv, stream=stream)
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(local).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        uuid = None
+    clocks = ClockSampler(uuid)
+    clocks.start()
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        prefill_call(x, o, S_T, conv_T)
+    barrier()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    t_beg, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_beg.record(stream)
+    for k in range(args.steps):
+        ev[k][0].record(stream)
+        prefill_call(x, o, S_T, conv_T)
+        ev[k][1].record(stream)
+    t_end.record(stream)
+    barrier()
+    if gdn.gdn_device_status(stream) != 0:
+        raise RuntimeError("device status not OK after the prefill timing")
+    total_ms = t_beg.elapsed_time(t_end)
+    launch_ms = float(np.mean([s.elapsed_time(e) for s, e in ev]))
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_per_step = total_ms / args.steps
+    tokens = p.B * p.T
+    value = world * tokens / (ms_per_step * 1e-3)
+
+    # ---- decode: 64 consecutive calls per step, inputs resident
+    dec = None
+    if not args.no_decode:
+        dp = I.decode_problem(**dict(I.DECODE_CASE, case=I.DECODE_CASE["case"] + 1000 * rank))
+        S = dev(dp.S)
+        conv = [dev(dp.conv, t_io), dev(dp.conv, t_io)]
+        cw, nw = dev(dp.conv_w, t_io), dev(dp.norm_w, t_io)
+        q_all = dev(dp.qkv_pre, t_io)
+        z_all = dev(dp.z, t_io)
+        g_all, b_all = dev(dp.g), dev(dp.beta)
+        od = torch.empty(dp.B, dp.Hv * D, device="cuda", dtype=t_io)
+
+        def decode_step_block():
+            for s in range(DECODE_CALLS_PER_STEP):
+                gdn.gdn_decode_step(q_all[s], z_all[s], g_all[s], b_all[s], cw, nw, S,
+                                    conv[s % 2], conv[(s + 1) % 2], od, Hk=dp.Hk, Hv=dp.Hv,
+                                    stream=stream)
+
+        for _ in range(args.warmup):
+            decode_step_block()
+        barrier()
+        d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        d0.record(stream)
+        for _ in range(args.steps):
+            decode_step_block()
+        d1.record(stream)
+        barrier()
+        if gdn.gdn_device_status(stream) != 0:
+            raise RuntimeError("device status not OK after the decode timing")
+        dec_ms = d0.elapsed_time(d1)
+        if world > 1:
+            import torch.distributed as dist
+            tt = torch.tensor([dec_ms], device="cuda")
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            dec_ms = float(tt.item())
+        call_ms = dec_ms / (args.steps * DECODE_CALLS_PER_STEP)
+        dbytes = decode_bytes(dp.B, dp.Hk, dp.Hv)
+        sbytes = decode_state_bytes(dp.B, dp.Hv)
+        dach = dbytes / (call_ms * 1e-3) / 1e9
+        dec = {
+            "workload": "Qwen3.8-27B-shaped GDN decode: B=256 sequences x 1 token, Hk=16, Hv=48, "
+                        "Dk=Dv=128, bf16 io, fp32 state; one step = 64 consecutive calls",
+            "value": world * sbytes / (call_ms * 1e-3) / 1e9, "unit": "state GB/s",
+            "total_gbs": world * dach, "ms_per_call": call_ms,
+            "ms_per_step": dec_ms / args.steps,
+            "tokens_per_s": world * dp.B / (call_ms * 1e-3),
+            "gpu_launches": args.steps * DECODE_CALLS_PER_STEP * DECODE_KERNELS_PER_CALL,
+            "roofline": {"bound": "hbm", "achieved": dach, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": dach / peaks["hbm_gbs"],
+                         "traffic": recorded_traffic("decode_kernel",
+                                                     "gated_deltanet_mixer_gb300/csrc/decode.cu"),
+                         "algorithmic_bytes_per_launch": dbytes,
+                         "peak_source": peak_src + " hbm_gbs (burst copy)"},
+        }
+        del S, conv, q_all, z_all, g_all, b_all, od
+    clk = clocks.stop()
+
+    # ---- end to end through the public API with host buffers
+    pin = {k: (None if v is None else v.cpu().pin_memory()) for k, v in x.items()}
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hS = torch.empty(S_T.shape, dtype=S_T.dtype).pin_memory()
+    hc = torch.empty(conv_T.shape, dtype=conv_T.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in pin.values() if v is not None)
+    d2h = sum(t.numel() * t.element_size() for t in (ho, hS, hc))
+    e2e_steps = max(2, min(args.steps, 5))
+
+    def e2e_step():
+        xx = {k: (None if v is None else x[k].copy_(v, non_blocking=True)) for k, v in pin.items()}
+        prefill_call(xx, o, S_T, conv_T)
+        ho.copy_(o, non_blocking=True)
+        hS.copy_(S_T, non_blocking=True)
+        hc.copy_(conv_T, non_blocking=True)
+
+    e2e_step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+
+    # ---- roofline of the prefill kernel
+    pbytes = prefill_bytes(p.B, p.T, p.Hk, p.Hv, 2 if p.io == "bf16" else 4)
+    pflops = prefill_flops(p.B, p.T, p.Hk, p.Hv)
+    ach = pbytes / (launch_ms * 1e-3) / 1e9
+    tfl = pflops / (launch_ms * 1e-3) / 1e12
+    result = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic (seeded; model-shaped random inputs, no weights needed)",
+        "config": {"workload": "Qwen3.5-4B-shaped GDN layer prefill: B=%d, T=%d, Hk=%d, Hv=%d, "
+                               "Dk=Dv=128, bf16 io, fp32 state" % (p.B, p.T, p.Hk, p.Hv),
+                   "io_dtype": p.io, "state_dtype": "f32",
+                   "l2": "inputs larger than L2 (%.2f GB read+written per step; L2 129 MB)"
+                         % (pbytes / 1e9),
+                   "parallelism": "one GPU per rank, each rank its own batch (weak scaling)"},
+        "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": ach / peaks["hbm_gbs"],
+                     "traffic": recorded_traffic("prefill_kernel", PREFILL_SOURCE),
+                     "algorithmic_bytes_per_launch": pbytes, "launch_ms": launch_ms,
+                     "peak_source": peak_src + " hbm_gbs (burst copy)"},
+        "roofline_tensor": {"bound": "tensor", "achieved": tfl, "peak": peaks["bf16_tflops"],
+                            "unit": "TFLOP/s", "frac": tfl / peaks["bf16_tflops"],
+                            "algorithmic_flops_per_launch": pflops,
+                            "peak_source": peak_src + " bf16_tflops (burst)"},
+        "e2e": {"value": world * tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps * PREFILL_KERNELS_PER_CALL,
+        "clocks": clk,
+        "decode": dec,
+    }
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    # ---- CPU baseline: the oracle as it stands, rank 0, single GPU only
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle import oracle as O
+        threads = O.default_threads()
+        T_s, secs = oracle_tokens_per_s(p, args.cpu_budget, threads)
+        result["cpu_baseline"] = {
+            "value": T_s / secs, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": "fp64 oracle on sequence 0 of the workload, all %d value heads, first %d "
+                      "of %d tokens (%.1f s)" % (p.Hv, T_s, p.T, secs)}
+    if rank == 0:
+        print(json.dumps(result))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+PREFILL_SOURCE = "gated_deltanet_mixer_gb300/csrc/prefill_recurrent.cu"
+
+
+# --------------------------------------------------------- reference arm
+def reference_arm(args, world, rank):
+    """The oracle, as it stands, timed on the host cores: rank 0 only."""
+    if rank != 0:
+        return
+    from gated_deltanet_mixer_gb300 import inputs as I
+    from oracle import oracle as O
+
+    threads = O.default_threads()
+    p = I.case_problem(args.workload)
+    a = p.arrays
+    # Size one step's sample so that warmup + steps fit in about args.ref_budget seconds.
+    per_step = args.ref_budget / max(1, args.steps + args.warmup)
+    T_s, _ = oracle_tokens_per_s(p, per_step, threads)
+
+    def step():
+        O.gdn_prefill(a["qkv_pre"][:1, :T_s], a["z"][:1, :T_s], a["g"][:1, :T_s],
+                      a["beta"][:1, :T_s], a["conv_w"], a["norm_w"],
+                      None if a["S0"] is None else a["S0"][:1],
+                      None if a["conv0"] is None else a["conv0"][:1], Hk=p.Hk, Hv=p.Hv,
+                      threads=threads, want_conv=False)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    secs = (time.perf_counter() - t0) / args.steps
+    value = T_s / secs
+    sample = ("fp64 oracle on sequence 0 of the workload, all %d value heads, first %d of %d "
+              "tokens per step" % (p.Hv, T_s, p.T))
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; model-shaped random inputs, no weights needed)",
+        "config": {"workload": "Qwen3.5-4B-shaped GDN layer prefill: B=%d, T=%d, Hk=%d, Hv=%d, "
+                               "Dk=Dv=128, bf16 io, fp32 state" % (p.B, p.T, p.Hk, p.Hv),
+                   "io_dtype": p.io, "state_dtype": "f32"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
+    ap.add_argument("--workload", default="4b_prefill",
+                    choices=["4b_prefill", "0.8b_prefill", "27b_prefill"])
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0,
+                    help="seconds of oracle work for the cpu_baseline sample")
+    ap.add_argument("--ref-budget", type=float, default=120.0,
+                    help="seconds of oracle work for the whole reference arm")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        reference_arm(args, world, rank)
+    else:
+        gdn_arm(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,79 @@
+// gdn_device.cuh -- device helpers shared by the libgdn kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gdn {
+
+constexpr int kD = 128;  // Dk = Dv: the only head width the kernels take
+
+// ---- io element access (io tensors are fp32 or bf16; math is fp32) --------
+__device__ __forceinline__ float ld_io(const float *p) { return *p; }
+__device__ __forceinline__ float ld_io(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+__device__ __forceinline__ void st_io(float *p, float v) { *p = v; }
+__device__ __forceinline__ void st_io(__nv_bfloat16 *p, float v) { *p = __float2bfloat16_rn(v); }
+
+// Four consecutive io elements (8- or 16-byte aligned by construction).
+__device__ __forceinline__ float4 ld_io4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ float4 ld_io4(const __nv_bfloat16 *p) {
+  uint2 u = *reinterpret_cast<const uint2 *>(p);
+  float4 f;
+  f.x = __uint_as_float(u.x << 16);
+  f.y = __uint_as_float(u.x & 0xffff0000u);
+  f.z = __uint_as_float(u.y << 16);
+  f.w = __uint_as_float(u.y & 0xffff0000u);
+  return f;
+}
+__device__ __forceinline__ void st_io4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
+__device__ __forceinline__ void st_io4(__nv_bfloat16 *p, float4 v) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
+  __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t *>(&a);
+  u.y = *reinterpret_cast<uint32_t *>(&b);
+  *reinterpret_cast<uint2 *>(p) = u;
+}
+
+// silu(x) = x * sigmoid(x)
+__device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
+
+__device__ __forceinline__ float dot4(float4 a, float4 b) {
+  return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
+// One halving stage of the transposed warp reduction below.
+template <int HALF>
+__device__ __forceinline__ void tr_stage(float (&a)[32], int lane) {
+  const bool upper = (lane & HALF) != 0;
+#pragma unroll
+  for (int i = 0; i < HALF; ++i) {
+    float send = upper ? a[i] : a[i + HALF];
+    float keep = upper ? a[i + HALF] : a[i];
+    a[i] = keep + __shfl_xor_sync(0xffffffffu, send, HALF);
+  }
+}
+
+// 32 partial sums per lane -> lane L returns the warp-wide total of a[L].
+// 31 shuffles instead of 160 for 32 separate butterfly reductions.
+__device__ __forceinline__ float transpose_reduce32(float (&a)[32], int lane) {
+  tr_stage<16>(a, lane);
+  tr_stage<8>(a, lane);
+  tr_stage<4>(a, lane);
+  tr_stage<2>(a, lane);
+  tr_stage<1>(a, lane);
+  return a[0];
+}
+
+// Streaming (evict-first) 16-byte global access for state rows touched once.
+__device__ __forceinline__ float4 ld_stream(const float *p) { return __ldcs(reinterpret_cast<const float4 *>(p)); }
+__device__ __forceinline__ void st_stream(float *p, float4 v) { __stcs(reinterpret_cast<float4 *>(p), v); }
+
+}  // namespace gdn

@@ -1,0 +1,150 @@
+"""ctypes binding of libgdn (``include/gdn.h``): argument marshalling only.
+
+Each function has the name of its C entry point and takes torch CUDA tensors
+(device memory from PyTorch); all computation happens in libgdn's kernels.
+There is no fallback: if ``libgdn.so`` is missing, loading it raises.
+"""
+import ctypes
+import math
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgdn.so")
+
+GDN_OK = 0
+STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED_SHAPE",
+                3: "GDN_ERR_ALIGNMENT", 4: "GDN_ERR_ALIAS", 5: "GDN_ERR_CUDA",
+                6: "GDN_ERR_TIMEOUT", 7: "GDN_ERR_NO_DEVICE"}
+GDN_F32, GDN_BF16 = 0, 1
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__("%s: %s (%s)" % (where, STATUS_NAMES.get(status, status),
+                                          gdn_status_str(status)))
+
+
+class gdn_shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("Hk", ctypes.c_int),
+                ("Hv", ctypes.c_int), ("Dk", ctypes.c_int), ("Dv", ctypes.c_int),
+                ("io_dtype", ctypes.c_int), ("eps_l2", ctypes.c_float),
+                ("eps_norm", ctypes.c_float), ("q_scale", ctypes.c_float)]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libgdn (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libgdn.so is not built (%s); run "
+                               "`python -m gated_deltanet_mixer_gb300.build`" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        vp = ctypes.c_void_p
+        L.gdn_abi_version.restype = ctypes.c_int
+        L.gdn_abi_version.argtypes = []
+        L.gdn_status_str.restype = ctypes.c_char_p
+        L.gdn_status_str.argtypes = [ctypes.c_int]
+        L.gdn_prefill.restype = ctypes.c_int
+        L.gdn_prefill.argtypes = [ctypes.POINTER(gdn_shape)] + [vp] * 12
+        L.gdn_decode_step.restype = ctypes.c_int
+        L.gdn_decode_step.argtypes = [ctypes.POINTER(gdn_shape)] + [vp] * 11
+        L.gdn_device_status.restype = ctypes.c_int
+        L.gdn_device_status.argtypes = [vp, ctypes.c_int]
+        _lib = L
+    return _lib
+
+
+def gdn_abi_version():
+    return lib().gdn_abi_version()
+
+
+def gdn_status_str(status):
+    return lib().gdn_status_str(int(status)).decode()
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _io_code(dtype):
+    if dtype == torch.bfloat16:
+        return GDN_BF16
+    if dtype == torch.float32:
+        return GDN_F32
+    raise TypeError("io tensors must be bfloat16 or float32, not %s" % dtype)
+
+
+def _head_width(C, Hk, Hv):
+    D, rem = divmod(C, 2 * Hk + Hv)
+    if rem:
+        raise ValueError("channel count %d is not (2*Hk + Hv) * D" % C)
+    return D
+
+
+def make_shape(B, T, Hk, Hv, D, io_dtype, eps_l2=1e-6, eps_norm=1e-6, q_scale=0.0):
+    return gdn_shape(B, T, Hk, Hv, D, D, io_dtype, eps_l2, eps_norm, q_scale)
+
+
+def gdn_prefill(qkv_pre, z, g, beta, conv_w, norm_w, S0, conv0, o, S_T, conv_T, *, Hk, Hv,
+                eps_l2=1e-6, eps_norm=1e-6, q_scale=0.0, stream=None):
+    """Prefill T tokens of B sequences (layouts as in gdn.h).  S0 / conv0 may
+    be None (zeros); S_T may be S0 itself.  Raises GdnError on a non-OK status."""
+    B, T, C = qkv_pre.shape
+    sh = make_shape(B, T, Hk, Hv, _head_width(C, Hk, Hv), _io_code(qkv_pre.dtype),
+                    eps_l2, eps_norm, q_scale)
+    st = lib().gdn_prefill(ctypes.byref(sh), _ptr(qkv_pre), _ptr(z), _ptr(g), _ptr(beta),
+                           _ptr(conv_w), _ptr(norm_w), _ptr(S0), _ptr(conv0), _ptr(o),
+                           _ptr(S_T), _ptr(conv_T), _stream(stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_prefill")
+
+
+def gdn_decode_step(qkv_pre, z, g, beta, conv_w, norm_w, S, conv_in, conv_out, o, *, Hk, Hv,
+                    eps_l2=1e-6, eps_norm=1e-6, q_scale=0.0, stream=None):
+    """One decode token for B sequences; S is updated in place, the new conv
+    window goes to conv_out (distinct from conv_in)."""
+    B, C = qkv_pre.shape
+    sh = make_shape(B, 1, Hk, Hv, _head_width(C, Hk, Hv), _io_code(qkv_pre.dtype),
+                    eps_l2, eps_norm, q_scale)
+    st = lib().gdn_decode_step(ctypes.byref(sh), _ptr(qkv_pre), _ptr(z), _ptr(g), _ptr(beta),
+                               _ptr(conv_w), _ptr(norm_w), _ptr(S), _ptr(conv_in),
+                               _ptr(conv_out), _ptr(o), _stream(stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_decode_step")
+
+
+def gdn_device_status(stream=None, reset=False):
+    """Synchronise and return the device-side status code (0 = OK)."""
+    return lib().gdn_device_status(_stream(stream), int(bool(reset)))
+
+
+# ---------------------------------------------------------------- helpers
+def alloc_prefill_outputs(B, T, Hk, Hv, dtype, device="cuda", D=128):
+    """Fresh (o, S_T, conv_T) buffers for a prefill call."""
+    C = (2 * Hk + Hv) * D
+    o = torch.empty(B, T, Hv * D, dtype=dtype, device=device)
+    S_T = torch.empty(B, Hv, D, D, dtype=torch.float32, device=device)
+    conv_T = torch.empty(B, 3, C, dtype=dtype, device=device)
+    return o, S_T, conv_T
+
+
+def default_q_scale(D=128):
+    return 1.0 / math.sqrt(D)

@@ -4,9 +4,11 @@ This module only draws random numbers; it holds none of the mixer's
 arithmetic.  The tests, the benchmark and the smoke check feed the same
 arrays to the CUDA library and to the CPU oracle.
 
-Every tensor is drawn from its own ``numpy.random.Generator(PCG64(seed))``
-with ``seed = 1000 * case + tensor_id`` (decode steps add ``100 * step``),
-drawn in float64, then rounded to the I/O dtype (round to nearest even).
+Every tensor has its own seed, ``seed = 1000 * case + tensor_id`` (decode
+steps add ``100 * step``); large tensors are drawn in slabs of 2^24 values,
+slab i from ``Generator(PCG64(SeedSequence([seed, i])))`` so that slabs can be
+drawn in parallel and the values do not depend on the thread count.  Values
+are drawn in float64, then rounded to the I/O dtype (round to nearest even).
 Values come back as float32 arrays that hold exactly the rounded values, so a
 bf16 copy made from them is exact.
 
@@ -16,6 +18,8 @@ Distributions (the workload recipe of the Qwen3.5 / Qwen3.8 shapes):
                                          the long-horizon 27B prefill)
   norm_w = 1 + N(0, 0.1^2)               S0 = 0 (tiny case) or N(0, 0.02^2)
 """
+import concurrent.futures as cf
+import os
 from dataclasses import dataclass, field
 from typing import Dict, Optional
 
@@ -29,22 +33,41 @@ _SLAB = 1 << 24  # values drawn per call, to bound peak host memory
 
 def round_to_bf16(x: np.ndarray) -> np.ndarray:
     """Round float values to bfloat16 (nearest, ties to even); return float32."""
-    x32 = np.ascontiguousarray(x, dtype=np.float32)
-    u = x32.view(np.uint32).astype(np.uint64)
-    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
-    return (u.astype(np.uint32) << 16).view(np.float32)
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    u = (u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))) & np.uint32(0xFFFF0000)
+    return u.view(np.float32)
+
+
+def _slab(seed, i, m, mean, std, io):
+    gen = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, i])))
+    x = gen.standard_normal(m) * std + mean
+    return round_to_bf16(x) if io == "bf16" else x.astype(np.float32)
 
 
 def _normal(seed: int, shape, mean=0.0, std=1.0, io="f32") -> np.ndarray:
     """N(mean, std^2) drawn in float64 slab by slab, rounded to ``io``."""
-    gen = np.random.Generator(np.random.PCG64(seed))
     n = int(np.prod(shape))
     out = np.empty(n, dtype=np.float32)
-    for s in range(0, n, _SLAB):
+    starts = list(range(0, n, _SLAB))
+
+    def fill(j):
+        s = starts[j]
         m = min(_SLAB, n - s)
-        x = gen.standard_normal(m) * std + mean
-        out[s:s + m] = round_to_bf16(x) if io == "bf16" else x.astype(np.float32)
+        out[s:s + m] = _slab(seed, j, m, mean, std, io)
+
+    if len(starts) > 1:
+        with cf.ThreadPoolExecutor(max_workers=min(len(starts), _threads())) as ex:
+            list(ex.map(fill, range(len(starts))))
+    elif starts:
+        fill(0)
     return out.reshape(shape)
+
+
+def _threads():
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
 
 
 def _sigmoid(x):
@@ -152,8 +175,11 @@ def decode_problem(B=256, Hk=16, Hv=48, io="bf16", steps=64, case=4, g_mu=3.0,
     p.norm_w = _normal(base + 6, (Dv,), mean=1.0, std=0.1, io=io)
     p.S = _normal(base + 7, (B, Hv, Dv, Dk), std=0.02)
     p.conv = _normal(base + 8, (B, 3, C), io=io)
-    p.qkv_pre = np.stack([_normal(base + 1 + 100 * s, (B, C), io=io) for s in range(steps)])
-    p.z = np.stack([_normal(base + 2 + 100 * s, (B, Hv * Dv), io=io) for s in range(steps)])
+    with cf.ThreadPoolExecutor(max_workers=_threads()) as ex:
+        p.qkv_pre = np.stack(list(ex.map(
+            lambda s: _normal(base + 1 + 100 * s, (B, C), io=io), range(steps))))
+        p.z = np.stack(list(ex.map(
+            lambda s: _normal(base + 2 + 100 * s, (B, Hv * Dv), io=io), range(steps))))
     p.beta = np.stack([_beta(base + 3 + 100 * s, (B, Hv)) for s in range(steps)])
     p.g = np.stack([_log_decay(base + 4 + 100 * s, (B, Hv), g_mu) for s in range(steps)])
     return p

@@ -1,0 +1,138 @@
+/*
+ * gdn.h -- C ABI of libgdn, the Gated DeltaNet token mixer on one GB300 GPU.
+ *
+ * The mixer is the linear-attention layer of the Qwen3.5 / Qwen3.8 hybrid
+ * decoders.  Per sequence b, per value head h, per token t it computes
+ *
+ *   1. u = silu(causal depthwise conv, width 4) on the q|k|v channels
+ *        page "Qwen3.8-27B" (docs.theformalera.com), node gdn.conv:
+ *        y[t,c] = silu( sum_{j<4} w[c,j] * x[t+j-3, c] ); tokens before the
+ *        first come from the carried conv window.
+ *   2. q^ = q / sqrt(sum q^2 + eps_l2) * q_scale,  k^ = k / sqrt(sum k^2 + eps_l2)
+ *        page "How Qwen3.5 works" (azmle112.github.io), section 9.4; value
+ *        head h reads key head h / (Hv / Hk) (integer division).
+ *   3. S_t = e^{g_t} S_{t-1} (I - beta_t k^_t k^_t^T) + beta_t v_t k^_t^T,
+ *      o_t = S_t q^_t
+ *        node gdn.core of the same spec (S is Dv x Dk, "value rows");
+ *        "How Qwen3.5 works" section 9.6 gives the decay -> predict ->
+ *        correct -> read order, section 9.11 the chunked form used by
+ *        gdn_prefill.
+ *   4. y_t = norm_w * o_t / sqrt(mean(o_t^2) + eps_norm) * silu(z_t), per head
+ *        node gdn.norm; "How Qwen3.5 works" section 9.9.
+ *
+ * Layouts (row-major, innermost last; C = 2*Hk*Dk + Hv*Dv conv channels,
+ * ordered q (Hk heads) | k (Hk heads) | v (Hv heads)):
+ *   qkv_pre [B][T][C]       z, o [B][T][Hv*Dv]      g, beta [B][T][Hv] (fp32)
+ *   conv_w  [C][4]          norm_w [Dv]             S [B][Hv][Dv][Dk] (fp32)
+ *   conv window [B][3][C]   raw (pre-conv) rows of the three previous tokens,
+ *                           oldest first
+ * "io" tensors (qkv_pre, z, o, conv windows, conv_w, norm_w) all have the
+ * dtype shape->io_dtype; g, beta and the state are always fp32.
+ *
+ * Ownership and execution: every pointer is a device pointer owned by the
+ * caller; the library allocates no memory, keeps no state between calls
+ * (apart from a per-device error word, see gdn_device_status), and enqueues
+ * its kernels on `stream` (a cudaStream_t; NULL = the legacy default stream)
+ * without synchronising.  Calls on different streams do not share buffers.
+ *
+ * Errors: arguments are checked on the host before anything is launched; a
+ * non-zero status means nothing was enqueued, except GDN_ERR_CUDA from the
+ * launch itself.  Values are not checked: g must be <= 0 (finite, or -inf
+ * for a reset) and beta in [0, 1]; other values give unspecified results
+ * but stay within the buffers.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GDN_ABI_VERSION 1
+
+typedef enum {
+  GDN_OK = 0,
+  GDN_ERR_INVALID_ARG = 1,       /* null pointer, B < 1, T < 1, bad dtype or eps */
+  GDN_ERR_UNSUPPORTED_SHAPE = 2, /* Dk or Dv != 128, Hv % Hk != 0, too large */
+  GDN_ERR_ALIGNMENT = 3,         /* a pointer not 16-byte aligned */
+  GDN_ERR_ALIAS = 4,             /* two buffers overlap where that is forbidden */
+  GDN_ERR_CUDA = 5,              /* a CUDA runtime call failed */
+  GDN_ERR_TIMEOUT = 6,           /* a device-side wait gave up (see gdn_device_status) */
+  GDN_ERR_NO_DEVICE = 7          /* the current device is not an sm_103 GPU */
+} gdn_status;
+
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
+
+typedef struct {
+  int B;          /* sequences */
+  int T;          /* tokens per sequence in this call (decode: 1) */
+  int Hk, Hv;     /* key heads, value heads; Hv % Hk == 0 */
+  int Dk, Dv;     /* head widths; the GPU kernels take 128 only */
+  int io_dtype;   /* gdn_dtype of the io tensors */
+  float eps_l2;   /* epsilon inside the q/k L2 root (1e-6 in the models) */
+  float eps_norm; /* epsilon of the gated RMSNorm (1e-6 in the models) */
+  float q_scale;  /* query scale after normalising; 0 means 1/sqrt(Dk) */
+} gdn_shape;
+
+/* GDN_ABI_VERSION of the loaded library. */
+int gdn_abi_version(void);
+
+/* A static, human-readable name for a status code. */
+const char *gdn_status_str(int status);
+
+/*
+ * Prefill: run T tokens of B sequences through the mixer, carrying the state.
+ *
+ *   qkv_pre, z, g, beta      this call's tokens, layouts above
+ *   conv_w, norm_w           layer weights
+ *   S0     [B][Hv][Dv][Dk]   incoming state, or NULL for zeros
+ *   conv0  [B][3][C]         incoming conv window, or NULL for zeros
+ *   o      [B][T][Hv*Dv]     out: the mixer output (after the gated norm)
+ *   S_T    [B][Hv][Dv][Dk]   out: final state; may be exactly S0 (in place),
+ *                            must not otherwise overlap any buffer
+ *   conv_T [B][3][C]         out: the last three raw rows of conv0 ++ qkv_pre;
+ *                            must not overlap conv0 or qkv_pre
+ *   o must not overlap any input.  All pointers 16-byte aligned.
+ *
+ * The chunked form ("How Qwen3.5 works" section 9.11, chunk 64) is used:
+ * it is the same recurrence reorganised, so results match the token loop up
+ * to rounding.  Continuing a prefill from (S_T, conv_T) equals one longer
+ * prefill; a decode step is a prefill of one token.
+ */
+gdn_status gdn_prefill(const gdn_shape *shape, const void *qkv_pre, const void *z,
+                       const float *g, const float *beta, const void *conv_w,
+                       const void *norm_w, const float *S0, const void *conv0, void *o,
+                       float *S_T, void *conv_T, void *stream);
+
+/*
+ * Decode: one new token for each of B sequences ("How Qwen3.5 works"
+ * section 13.3: each linear layer updates its conv window and does one
+ * recurrent step on the cached state).  shape->T must be 1.
+ *
+ *   qkv_pre [B][C], z [B][Hv*Dv], g and beta [B][Hv]    the new token
+ *   S       [B][Hv][Dv][Dk]   the cached state, updated in place
+ *   conv_in [B][3][C]         the cached window
+ *   conv_out[B][3][C]         out: the new window; must not overlap conv_in
+ *                             (callers ping-pong two buffers)
+ *   o       [B][Hv*Dv]        out: the mixer output for the token
+ */
+gdn_status gdn_decode_step(const gdn_shape *shape, const void *qkv_pre, const void *z,
+                           const float *g, const float *beta, const void *conv_w,
+                           const void *norm_w, float *S, const void *conv_in, void *conv_out,
+                           void *o, void *stream);
+
+/*
+ * Synchronise `stream` and report device-side failures recorded since the
+ * last reset: GDN_ERR_TIMEOUT if a kernel's bounded wait gave up (the kernel
+ * then returned early and its outputs are incomplete), GDN_ERR_CUDA if the
+ * synchronisation itself failed, GDN_OK otherwise.  reset != 0 clears the
+ * record afterwards.  The record is one word per device, shared by all
+ * streams.
+ */
+gdn_status gdn_device_status(void *stream, int reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

@@ -1,0 +1,102 @@
+"""Shared plumbing of the GPU parity tests: upload seeded inputs, call libgdn
+through its C ABI, call the oracle on the same values, compare.
+
+Tolerances (bf16 io, fp32 state):
+  o   : max |o_gpu - o_ref| <= 2e-2 * rms(o_ref) + q(o_ref), where q is the
+        rounding of the stored output (half a bf16 ulp, <= 2^-8 |o_ref|; zero
+        for fp32 io) -- the arithmetic error bound plus the output's own
+        quantisation, which no implementation can avoid.
+  S_T : max |S_gpu - S_ref| <= 1e-2 * rms(S_ref)
+  conv windows: bit-exact (they are raw copies).
+"""
+import numpy as np
+import torch
+
+from gated_deltanet_mixer_gb300 import gdn
+from oracle import oracle as O
+
+O_TOL = 2e-2
+S_TOL = 1e-2
+
+
+def torch_io(io):
+    return torch.bfloat16 if io == "bf16" else torch.float32
+
+
+def dev(a, dtype=torch.float32):
+    if a is None:
+        return None
+    return torch.from_numpy(np.ascontiguousarray(a)).to("cuda").to(dtype)
+
+
+def to_np(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def quantum(ref, io):
+    return (2.0 ** -8) * np.abs(ref) if io == "bf16" else 0.0
+
+
+def check_o(got, ref, io, what="o"):
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    excess = np.abs(got - ref) - quantum(ref, io)
+    worst = float(np.max(excess)) if excess.size else 0.0
+    assert np.all(np.isfinite(got)), "%s: non-finite values" % what
+    assert worst <= O_TOL * rms, "%s: max excess error %.3e > %.3e (rms %.3e)" % (
+        what, worst, O_TOL * rms, rms)
+    return worst / rms if rms > 0 else 0.0
+
+
+def check_S(got, ref, what="S_T"):
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    err = float(np.max(np.abs(got - ref)))
+    assert np.all(np.isfinite(got)), "%s: non-finite values" % what
+    assert err <= S_TOL * rms, "%s: max error %.3e > %.3e (rms %.3e)" % (what, err, S_TOL * rms, rms)
+    return err / rms if rms > 0 else 0.0
+
+
+def upload_prefill(p):
+    """Device copies of a Problem's inputs."""
+    t = torch_io(p.io)
+    a = p.arrays
+    return dict(qkv_pre=dev(a["qkv_pre"], t), z=dev(a["z"], t), g=dev(a["g"]),
+                beta=dev(a["beta"]), conv_w=dev(a["conv_w"], t), norm_w=dev(a["norm_w"], t),
+                S0=dev(a["S0"]), conv0=dev(a["conv0"], t))
+
+
+def gpu_prefill(p, inputs=None, in_place=False):
+    x = inputs or upload_prefill(p)
+    o, S_T, conv_T = gdn.alloc_prefill_outputs(p.B, p.T, p.Hk, p.Hv, torch_io(p.io))
+    if in_place:
+        assert x["S0"] is not None
+        S_T = x["S0"]
+    gdn.gdn_prefill(x["qkv_pre"], x["z"], x["g"], x["beta"], x["conv_w"], x["norm_w"],
+                    x["S0"], x["conv0"], o, S_T, conv_T, Hk=p.Hk, Hv=p.Hv)
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_status() == 0
+    return o, S_T, conv_T
+
+
+def oracle_prefill(p, units=None, threads=0):
+    a = p.arrays
+    return O.gdn_prefill(a["qkv_pre"], a["z"], a["g"], a["beta"], a["conv_w"], a["norm_w"],
+                         a["S0"], a["conv0"], Hk=p.Hk, Hv=p.Hv, units=units,
+                         threads=threads or O.default_threads())
+
+
+def compare_prefill(p, got, units=None):
+    """Compare GPU outputs with the oracle on all units or on a sample."""
+    o, S_T, conv_T = got
+    ref = oracle_prefill(p, units)
+    np.testing.assert_array_equal(to_np(conv_T), ref["conv_T"])
+    if units is None:
+        eo = check_o(to_np(o), ref["o"], p.io)
+        es = check_S(to_np(S_T), ref["S_T"])
+    else:
+        D = 128
+        o4 = o.view(p.B, p.T, p.Hv, D)
+        got_o = np.stack([to_np(o4[u // p.Hv, :, u % p.Hv]) for u in units])
+        got_S = np.stack([to_np(S_T[u // p.Hv, u % p.Hv]) for u in units])
+        eo = check_o(got_o, ref["o_units"], p.io)
+        es = check_S(got_S, ref["S_T"])
+    return eo, es

@@ -1,0 +1,114 @@
+"""libgdn host-side tests that need no GPU: the library loads, exports every
+entry point declared in include/gdn.h, and rejects bad arguments on the host
+before touching the device (fake, never dereferenced pointers)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from gated_deltanet_mixer_gb300 import build as gdn_build
+from gated_deltanet_mixer_gb300 import gdn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdn.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    gdn_build.build()
+    return gdn.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("gdn_prefill", "gdn_decode_step", "gdn_status_str", "gdn_device_status",
+              "gdn_abi_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+    out = os.popen("nm -D --defined-only %s" % gdn.LIB_PATH).read()
+    for name in declared_functions():
+        assert re.search(r"\bT %s\b" % name, out), name
+
+
+def test_abi_version_and_status_strings(L):
+    hdr = open(HEADER).read()
+    ver = int(re.search(r"#define GDN_ABI_VERSION (\d+)", hdr).group(1))
+    assert gdn.gdn_abi_version() == ver
+    for code in range(8):
+        assert gdn.gdn_status_str(code) != "unknown status"
+    assert gdn.gdn_status_str(99) == "unknown status"
+
+
+# Fake device addresses, 16-byte aligned and far apart; never dereferenced
+# because every case below fails its host-side check first.
+BASE = 0x7F0000000000
+STEP = 1 << 36
+
+
+def fake(i, offset=0):
+    return BASE + i * STEP + offset
+
+
+def prefill(L, shape, **over):
+    args = dict(qkv=fake(0), z=fake(1), g=fake(2), beta=fake(3), conv_w=fake(4), norm_w=fake(5),
+                S0=fake(6), conv0=fake(7), o=fake(8), S_T=fake(9), conv_T=fake(10))
+    args.update(over)
+    return L.gdn_prefill(None if shape is None else ctypes.byref(shape),
+                         *[args[k] for k in ("qkv", "z", "g", "beta", "conv_w", "norm_w", "S0",
+                                             "conv0", "o", "S_T", "conv_T")], None)
+
+
+def decode(L, shape, **over):
+    args = dict(qkv=fake(0), z=fake(1), g=fake(2), beta=fake(3), conv_w=fake(4), norm_w=fake(5),
+                S=fake(6), conv_in=fake(7), conv_out=fake(8), o=fake(9))
+    args.update(over)
+    return L.gdn_decode_step(ctypes.byref(shape), *[args[k] for k in (
+        "qkv", "z", "g", "beta", "conv_w", "norm_w", "S", "conv_in", "conv_out", "o")], None)
+
+
+def shape(B=2, T=8, Hk=2, Hv=4, D=128, io=gdn.GDN_BF16, **kw):
+    return gdn.make_shape(B, T, Hk, Hv, D, io, **kw)
+
+
+def test_shape_errors(L):
+    assert prefill(L, None) == 1
+    assert prefill(L, shape(T=0)) == 1            # empty sequence is an error
+    assert prefill(L, shape(B=0)) == 1
+    assert prefill(L, shape(io=7)) == 1
+    assert prefill(L, shape(eps_l2=-1.0)) == 1
+    assert prefill(L, shape(q_scale=float("nan"))) == 1
+    assert prefill(L, shape(D=64)) == 2           # only 128-wide heads on the GPU
+    assert prefill(L, shape(Hk=3, Hv=4)) == 2     # Hv must be a multiple of Hk
+    assert prefill(L, shape(Hv=5000, Hk=5000)) == 2
+    assert decode(L, shape(T=2)) == 1             # decode is one token
+
+
+def test_null_and_alignment_errors(L):
+    assert prefill(L, shape(), qkv=None) == 1
+    assert prefill(L, shape(), o=None) == 1
+    assert prefill(L, shape(), z=fake(1, 8)) == 3
+    assert prefill(L, shape(), S_T=fake(9, 4)) == 3
+    assert decode(L, shape(T=1), S=None) == 1
+    assert decode(L, shape(T=1), conv_out=fake(8, 2)) == 3
+
+
+def test_alias_rules(L):
+    # conv_T may never overlap conv0; o may never overlap an input.
+    assert prefill(L, shape(), conv_T=fake(7)) == 4
+    assert prefill(L, shape(), o=fake(0, 64)) == 4
+    # S_T may be exactly S0 (in place) but not partly overlap it.
+    assert prefill(L, shape(), S_T=fake(6, 4096)) == 4
+    # decode: conv_out must differ from conv_in; S must not overlap o.
+    assert decode(L, shape(T=1), conv_out=fake(7)) == 4
+    assert decode(L, shape(T=1), o=fake(6, 1024)) == 4
