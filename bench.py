@@ -104,7 +104,7 @@ def recorded_traffic(kernel_key, source_relpath):
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks / throttle reasons sampled every 50 ms."""
     QUERY = ("index,uuid,utilization.gpu,clocks.sm,clocks.max.sm,power.draw,"
              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -118,7 +118,7 @@ class ClockSampler:
     def start(self):
         self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
         cmd = ["nvidia-smi", "--query-gpu=" + self.QUERY, "--format=csv,noheader,nounits",
-               "-lms", "200"]
+               "-lms", "50"]
         if self.uuid:
             cmd += ["-i", self.uuid]
         try:
@@ -168,25 +168,32 @@ def dist_env():
 
 
 # ----------------------------------------------------------- oracle timing
-def oracle_tokens_per_s(p, budget_s, threads):
-    """Time the oracle as it stands on the first sequence of `p`, all value
-    heads, over as many leading tokens as fit in about `budget_s` seconds."""
+def oracle_run(p, n_tok, threads):
+    """The oracle, as it stands, on the workload's first `n_tok` tokens: whole
+    sequences first (all value heads), then a prefix of the next.  Seconds."""
     from oracle import oracle as O
 
     a = p.arrays
-
-    def run(T):
-        t0 = time.perf_counter()
-        O.gdn_prefill(a["qkv_pre"][:1, :T], a["z"][:1, :T], a["g"][:1, :T], a["beta"][:1, :T],
-                      a["conv_w"], a["norm_w"], None if a["S0"] is None else a["S0"][:1],
-                      None if a["conv0"] is None else a["conv0"][:1], Hk=p.Hk, Hv=p.Hv,
+    nb, rem = divmod(n_tok, p.T)
+    t0 = time.perf_counter()
+    for b0, b1, T in ((0, nb, p.T), (nb, nb + 1, rem)):
+        if b1 <= b0 or T == 0:
+            continue
+        O.gdn_prefill(a["qkv_pre"][b0:b1, :T], a["z"][b0:b1, :T], a["g"][b0:b1, :T],
+                      a["beta"][b0:b1, :T], a["conv_w"], a["norm_w"],
+                      None if a["S0"] is None else a["S0"][b0:b1],
+                      None if a["conv0"] is None else a["conv0"][b0:b1], Hk=p.Hk, Hv=p.Hv,
                       threads=threads, want_conv=False)
-        return time.perf_counter() - t0
+    return time.perf_counter() - t0
 
-    probe_T = min(p.T, 128)
-    rate = probe_T / max(run(probe_T), 1e-6)
-    T = int(max(probe_T, min(p.T, rate * budget_s)))
-    return T, run(T)
+
+def oracle_tokens_per_s(p, budget_s, threads):
+    """Size a sample to about `budget_s` seconds of oracle work (capped at the
+    whole workload) and time it.  Returns (tokens, seconds)."""
+    probe = min(p.T, 256)
+    rate = probe / max(oracle_run(p, probe, threads), 1e-6)
+    n = int(max(probe, min(p.B * p.T, rate * budget_s)))
+    return n, oracle_run(p, n, threads)
 
 
 # --------------------------------------------------------------- GPU arm
@@ -396,8 +403,8 @@ def gdn_arm(args, world, rank, local):
         T_s, secs = oracle_tokens_per_s(p, args.cpu_budget, threads)
         result["cpu_baseline"] = {
             "value": T_s / secs, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-            "sample": "fp64 oracle on sequence 0 of the workload, all %d value heads, first %d "
-                      "of %d tokens (%.1f s)" % (p.Hv, T_s, p.T, secs)}
+            "sample": "fp64 oracle on the first %d of the workload's %d tokens (%d sequences "
+                      "x %d), all %d value heads, %.1f s" % (T_s, p.B * p.T, p.B, p.T, p.Hv, secs)}
     if rank == 0:
         print(json.dumps(result))
     if world > 1:
@@ -418,17 +425,13 @@ def reference_arm(args, world, rank):
 
     threads = O.default_threads()
     p = I.case_problem(args.workload)
-    a = p.arrays
+
     # Size one step's sample so that warmup + steps fit in about args.ref_budget seconds.
     per_step = args.ref_budget / max(1, args.steps + args.warmup)
     T_s, _ = oracle_tokens_per_s(p, per_step, threads)
 
     def step():
-        O.gdn_prefill(a["qkv_pre"][:1, :T_s], a["z"][:1, :T_s], a["g"][:1, :T_s],
-                      a["beta"][:1, :T_s], a["conv_w"], a["norm_w"],
-                      None if a["S0"] is None else a["S0"][:1],
-                      None if a["conv0"] is None else a["conv0"][:1], Hk=p.Hk, Hv=p.Hv,
-                      threads=threads, want_conv=False)
+        oracle_run(p, T_s, threads)
 
     for _ in range(args.warmup):
         step()
@@ -437,8 +440,8 @@ def reference_arm(args, world, rank):
         step()
     secs = (time.perf_counter() - t0) / args.steps
     value = T_s / secs
-    sample = ("fp64 oracle on sequence 0 of the workload, all %d value heads, first %d of %d "
-              "tokens per step" % (p.Hv, T_s, p.T))
+    sample = ("fp64 oracle on the first %d of the workload's %d tokens per step (%d sequences "
+              "x %d), all %d value heads" % (T_s, p.B * p.T, p.B, p.T, p.Hv))
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3,
@@ -457,7 +460,7 @@ def reference_arm(args, world, rank):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
     ap.add_argument("--workload", default="4b_prefill",

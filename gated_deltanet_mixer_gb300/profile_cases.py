@@ -1,0 +1,67 @@
+"""Small, self-contained launches of the libgdn kernels, for profilers.
+
+    python -m gated_deltanet_mixer_gb300.profile_cases decode --B 48 --calls 3
+    python -m gated_deltanet_mixer_gb300.profile_cases prefill --B 1 --T 2048 --calls 2
+
+Inputs are the seeded synthetic ones of ``inputs.py``; each case is sized so
+that its working set is larger than L2 (129 MB) but only a few GB at most.
+"""
+import argparse
+
+import numpy as np
+import torch
+
+from . import gdn
+from . import inputs as I
+
+
+def _dev(x, dt=torch.float32):
+    return None if x is None else torch.from_numpy(np.ascontiguousarray(x)).cuda().to(dt)
+
+
+def decode(B, Hk, Hv, calls):
+    dp = I.decode_problem(B=B, Hk=Hk, Hv=Hv, steps=1, case=200)
+    t = torch.bfloat16
+    S = _dev(dp.S)
+    conv = [_dev(dp.conv, t), _dev(dp.conv, t)]
+    q, z, g, b = _dev(dp.qkv_pre[0], t), _dev(dp.z[0], t), _dev(dp.g[0]), _dev(dp.beta[0])
+    cw, nw = _dev(dp.conv_w, t), _dev(dp.norm_w, t)
+    o = torch.empty(B, Hv * 128, device="cuda", dtype=t)
+    for s in range(calls):
+        gdn.gdn_decode_step(q, z, g, b, cw, nw, S, conv[s % 2], conv[(s + 1) % 2], o, Hk=Hk, Hv=Hv)
+
+
+def prefill(B, T, Hk, Hv, calls):
+    p = I.prefill_problem(B, T, Hk, Hv, io="bf16", case=201)
+    t = torch.bfloat16
+    a = p.arrays
+    x = [_dev(a["qkv_pre"], t), _dev(a["z"], t), _dev(a["g"]), _dev(a["beta"]),
+         _dev(a["conv_w"], t), _dev(a["norm_w"], t), _dev(a["S0"]), _dev(a["conv0"], t)]
+    o, S_T, conv_T = gdn.alloc_prefill_outputs(B, T, Hk, Hv, t)
+    for _ in range(calls):
+        gdn.gdn_prefill(*x, o, S_T, conv_T, Hk=Hk, Hv=Hv)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("kernel", choices=["decode", "prefill"])
+    ap.add_argument("--B", type=int, default=None)
+    ap.add_argument("--T", type=int, default=2048)
+    ap.add_argument("--Hk", type=int, default=16)
+    ap.add_argument("--Hv", type=int, default=None)
+    ap.add_argument("--calls", type=int, default=3)
+    a = ap.parse_args()
+    gdn.lib()
+    if a.kernel == "decode":
+        decode(a.B or 48, a.Hk, a.Hv or 48, a.calls)
+    else:
+        prefill(a.B or 4, a.T, a.Hk, a.Hv or 32, a.calls)
+    torch.cuda.synchronize()
+    st = gdn.gdn_device_status()
+    if st != 0:
+        raise SystemExit("device status %d" % st)
+    print("ok")
+
+
+if __name__ == "__main__":
+    main()
