@@ -371,7 +371,7 @@ def gdn_arm(args, world, rank, local):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic (seeded; model-shaped random inputs, no weights needed)",
+        "dtype": "f16", "data": "synthetic (seeded; model-shaped random inputs, no weights needed)",
         "config": {"workload": "Qwen3.5-4B-shaped GDN layer prefill: B=%d, T=%d, Hk=%d, Hv=%d, "
                                "Dk=Dv=128, bf16 io, fp32 state" % (p.B, p.T, p.Hk, p.Hv),
                    "io_dtype": p.io, "state_dtype": "f32",
@@ -412,7 +412,7 @@ def gdn_arm(args, world, rank, local):
         dist.destroy_process_group()
 
 
-PREFILL_SOURCE = "gated_deltanet_mixer_gb300/csrc/prefill_recurrent.cu"
+PREFILL_SOURCE = "gated_deltanet_mixer_gb300/csrc/prefill_chunked.cu"
 
 
 # --------------------------------------------------------- reference arm

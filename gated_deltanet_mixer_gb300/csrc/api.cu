@@ -124,7 +124,7 @@ gdn_status gdn_prefill(const gdn_shape *shape, const void *qkv_pre, const void *
   if (st != GDN_OK) return st;
 
   gdn::PrefillArgs a{d, qkv_pre, z, g, beta, conv_w, norm_w, S0, conv0, o, S_T, conv_T, err};
-  cudaError_t e = gdn::launch_prefill(a, shape->io_dtype == GDN_BF16, (cudaStream_t)stream);
+  cudaError_t e = gdn::launch_prefill_chunked(a, shape->io_dtype == GDN_BF16, (cudaStream_t)stream);
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

@@ -42,7 +42,8 @@ struct DecodeArgs {
 
 // Each returns the cudaGetLastError() of its launch.
 cudaError_t launch_decode(const DecodeArgs &a, bool bf16, cudaStream_t s);
-cudaError_t launch_prefill(const PrefillArgs &a, bool bf16, cudaStream_t s);
+cudaError_t launch_prefill(const PrefillArgs &a, bool bf16, cudaStream_t s);          // token-serial
+cudaError_t launch_prefill_chunked(const PrefillArgs &a, bool bf16, cudaStream_t s);  // chunked WY, tcgen05
 
 // Device error bits (the error word is OR-ed).
 constexpr unsigned int kErrTimeout = 1u;

@@ -48,9 +48,11 @@ def test_prefill_in_place_state():
 
 
 def test_prefill_continuation_on_gpu():
-    """Prefill(a ++ b) equals prefill(b) started from prefill(a)'s state and
-    window (the carried cache of 'How Qwen3.5 works' section 13)."""
+    """Prefill(a ++ b) and prefill(b) started from prefill(a)'s state and window
+    (the carried cache of 'How Qwen3.5 works' section 13) both match the
+    oracle's single pass; the carried windows agree bit for bit."""
     p = I.prefill_problem(2, 200, 2, 4, io="bf16", case=62)
+    ref = oracle_prefill(p)
     whole = gpu_prefill(p)
     cut = 77
     seq = ("qkv_pre", "z", "g", "beta")
@@ -62,9 +64,11 @@ def test_prefill_continuation_on_gpu():
     xb = upload_prefill(pb)
     xb["S0"], xb["conv0"] = first[1], first[2]
     second = gpu_prefill(pb, xb)
-    ref_o = to_np(whole[0])[:, cut:]
-    check_o(to_np(second[0]), ref_o, "bf16")
-    check_S(to_np(second[1]), to_np(whole[1]))
+    check_o(to_np(whole[0]), ref["o"], "bf16")
+    check_o(to_np(first[0]), ref["o"][:, :cut], "bf16")
+    check_o(to_np(second[0]), ref["o"][:, cut:], "bf16")
+    check_S(to_np(whole[1]), ref["S_T"])
+    check_S(to_np(second[1]), ref["S_T"])
     np.testing.assert_array_equal(to_np(second[2]), to_np(whole[2]))
 
 
