@@ -124,7 +124,10 @@ gdn_status gdn_prefill(const gdn_shape *shape, const void *qkv_pre, const void *
   if (st != GDN_OK) return st;
 
   gdn::PrefillArgs a{d, qkv_pre, z, g, beta, conv_w, norm_w, S0, conv0, o, S_T, conv_T, err};
-  cudaError_t e = gdn::launch_prefill_chunked(a, shape->io_dtype == GDN_BF16, (cudaStream_t)stream);
+  // bf16 io: the chunked tensor-core kernel; fp32 io: the exact token-serial kernel.
+  const bool bf16 = shape->io_dtype == GDN_BF16;
+  cudaError_t e = bf16 ? gdn::launch_prefill_chunked(a, true, (cudaStream_t)stream)
+                       : gdn::launch_prefill(a, false, (cudaStream_t)stream);
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

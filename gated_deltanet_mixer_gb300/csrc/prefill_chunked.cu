@@ -1,5 +1,5 @@
 // prefill_chunked.cu -- the chunked (WY) form of the gated delta rule on the
-// tcgen05 tensor cores.
+// tcgen05 tensor cores (bf16 io).
 //
 // Page "How Qwen3.5 works" (azmle112.github.io), section 9.11, writes one
 // chunk of n = 64 tokens with incoming state S (k x v there) as
@@ -17,25 +17,32 @@
 // decays G (never a division of two small products); g is clamped at -80.
 //
 // One CTA per (sequence b, value head h), 12 warps, a sequential loop over the
-// chunks.  The fp32 state lives in TMEM for the whole sequence; an fp16 copy
-// in shared memory is the MMA operand.  All MMA operands are fp16 (11-bit
-// significand; bf16's 8 bits cost several percent of the output's rms at the
-// heavy tail of the gated norm) with fp32 accumulation.  The operands that
-// feed the state, V and T B (through U) and both factors of the state update,
-// are carried as hi + lo fp16 pairs (three MMAs for hi*hi + hi*lo + lo*hi), which
-// keeps the state within about 1e-3 of its rms where single fp16 gives 2e-2
-// on short, heavy-tailed updates.  Per chunk, in order:
-//   A  conv + SiLU + L2 norms (front end), operand tiles to shared memory
+// chunks.  The fp32 state lives in TMEM for the whole sequence; its fp16 copy,
+// the MMA operand, lives in TMEM too (tcgen05.mma reads A from TMEM), as do
+// the fp16 Delta^T tiles.  The raw q|k|v rows of a chunk (with the three rows
+// before it) and its z rows arrive by TMA into shared memory, a chunk ahead.
+// All MMA operands are fp16 (11-bit significand; bf16's 8 bits cost several
+// percent of the output's rms at the heavy tail of the gated norm) with fp32
+// accumulation.  The operands that feed the state, V and T B (through U) and
+// both factors of the state update, are carried as hi + lo fp16 pairs (three
+// MMAs for hi*hi + hi*lo + lo*hi), which keeps the state within about 1e-3
+// of its rms where single fp16 gives 2e-2 on short, heavy-tailed updates.
+// Per chunk, in order:
+//   A  conv + SiLU + L2 norms (front end) from the staged raw rows
 //   B  MMA1  [K;Q] K^T                        -> K K^T, Q K^T
 //   C  decayed lower-triangular L (fp32) and M (fp16)
 //   D  T = (I + L)^{-1} in 16 x 16 blocks (fp32, CUDA cores) -> T B, T B D
-//   E  MMA2  U^T = V^T (T B)^T (split);  MMA3  W^T = K^T (T B D)^T
+//   E  MMA2  U^T = V^T (T B)^T (split);  MMA3  W^T = K^T (T B D)^T;
+//      the next chunk's raw rows are requested (TMA)
 //   F  -W^T to shared memory
 //   G  MMA4  Delta^T = U^T - S W^T;  MMA5  S Q^T
-//   H  Delta^T (hi, lo) to shared memory
+//   H  Delta^T (hi, lo) to TMEM
 //   I  MMA6  Delta^T M^T;            MMA7  S += Delta^T (Gamma K) (split)
 //   J  O = d (S Q^T) + Delta^T M^T, gated RMSNorm (node gdn.norm) -> o;
-//      S -> fp16 copy, rescaled for the next chunk (or S_T after the last)
+//      S -> fp16 copy, rescaled for the next chunk (or S_T after the last);
+//      then the next chunk's z rows are requested (TMA)
+#include <cuda.h>
+
 #include "gdn_device.cuh"
 #include "launch.h"
 #include "umma.cuh"
@@ -44,11 +51,14 @@ namespace gdn {
 namespace {
 
 using namespace umma;
+using bf16 = __nv_bfloat16;
 
-constexpr int kC = 64;  // chunk length
+constexpr int kC = 64;          // chunk length
 constexpr int kThreads = 384;   // 12 warps
 constexpr int kTmemWarps = 8;   // warps 0..7 do the TMEM <-> register passes (two per lane quadrant)
 constexpr float kGMin = -80.0f;
+constexpr int kRawRows = kC + 3;                  // a chunk's rows plus the three before it
+constexpr uint32_t kRawBlock = kRawRows * kD * 2;  // one of q | k | v, bytes (17152)
 
 // Shared memory map (byte offsets from a 1024-aligned base).  fp16 tiles.
 constexpr uint32_t OFF_KQ = 0;          // [K;Q] K-major, 128 rows x 128       32 KB
@@ -60,30 +70,33 @@ constexpr uint32_t OFF_TU = 98304;      // T diag(beta)      K-major [i][j]     
 constexpr uint32_t OFF_TW = 106496;     // T diag(beta d)    K-major [i][j]     8 KB
 constexpr uint32_t OFF_M = 114688;      // M         K-major [i][j]             8 KB
 constexpr uint32_t OFF_NW = 122880;     // -W^T      MN-major [k][i]           16 KB
-constexpr uint32_t OFF_S = 139264;      // S         K-major [v][k]            32 KB
-constexpr uint32_t OFF_DT = 172032;     // Delta^T hi K-major [v][j]           16 KB
-constexpr uint32_t OFF_DTL = 188416;    // Delta^T lo                          16 KB
-constexpr uint32_t OFF_TUL = 204800;    // T diag(beta), low part               8 KB
-constexpr uint32_t OFF_VEC = 212992;    // per-token vectors and flags          2 KB
+constexpr uint32_t OFF_TUL = 139264;    // T diag(beta), low part               8 KB
+constexpr uint32_t OFF_RAW = 147456;    // raw q | k | v rows, bf16 [3][67][128] 50.25 KB
+constexpr uint32_t OFF_Z = OFF_RAW + 3 * kRawBlock;  // z rows, bf16 [64][128]  16 KB
+constexpr uint32_t OFF_VEC = OFF_Z + kC * kD * 2;     // per-token vectors, flags, barriers
 // Scratch that lives only between two uses of the tiles it overlays:
-constexpr int kLs = 68;                 // padded row stride of L (floats)
-constexpr uint32_t OFF_L = OFF_DT;      // L fp32 [64][68], phases C-D (DT and the start of DTL)
-constexpr uint32_t OFF_PB = OFF_DT + 64 * kLs * 4;  // block products fp32 [3][16][16], phase D
-constexpr uint32_t OFF_TF = OFF_NW;     // T fp32 [64][64], phase D
-constexpr uint32_t OFF_OST = OFF_VH;    // O^T staging fp32 [64][128] (VH + VL), phase J
+constexpr int kLs = 68;                              // padded row stride of L (floats)
+constexpr uint32_t OFF_L = OFF_RAW;                  // L fp32 [64][68], phases C-D
+constexpr uint32_t OFF_PB = OFF_RAW + 64 * kLs * 4;  // block products fp32 [3][16][16], phase D
+constexpr uint32_t OFF_TF = OFF_NW;                  // T fp32 [64][64], phase D
+constexpr uint32_t OFF_OST = OFF_VH;                 // O^T staging fp32 [64][128] (VH + VL), phase J
 constexpr uint32_t kSmemUsed = OFF_VEC + 2048;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // + alignment slack
+static_assert(OFF_PB + 3 * 256 * 4 <= OFF_Z, "solve scratch fits in the raw rows");
+static_assert(OFF_RAW % 128 == 0 && OFF_Z % 128 == 0 && kRawBlock % 128 == 0, "TMA destinations");
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 // TMEM columns (512 allocated).
-constexpr uint32_t TM_S = 0;      // state, fp32 [v][k]           128 columns
-constexpr uint32_t TM_O1 = 128;   // S Q^T [v][i]                 64
-constexpr uint32_t TM_O2 = 192;   // Delta^T M^T [v][i]           64
-constexpr uint32_t TM_U = 256;    // U^T, then Delta^T [v][j]     64
-constexpr uint32_t TM_W = 320;    // W^T [k][i]                   64
-constexpr uint32_t TM_KQ = 384;   // [K K^T; Q K^T]               64
+constexpr uint32_t TM_S = 0;      // state, fp32 [v][k]                         128 columns
+constexpr uint32_t TM_O1 = 128;   // S Q^T [v][i]                               64
+constexpr uint32_t TM_O2 = 192;   // Delta^T M^T [v][i]                         64
+constexpr uint32_t TM_U = 256;    // U^T, then Delta^T [v][j]                   64
+constexpr uint32_t TM_W = 320;    // W^T [k][i]                                 64
+constexpr uint32_t TM_KQ = 384;   // [K K^T; Q K^T]; then Delta^T fp16 hi | lo  64
+constexpr uint32_t TM_S16 = 448;  // state, fp16 pairs [v][k/2]                 64
 constexpr uint32_t kTmemCols = 512;
 
-struct Vecs {  // per-token chunk vectors in shared memory
+struct __align__(16) Vecs {  // per-token chunk vectors in shared memory
   float G[kC];     // chunk-local cumulative log decay
   float d[kC];     // e^{G_i}
   float dinv[kC];  // e^{-G_j} (only when the chunk's decay is mild)
@@ -95,16 +108,32 @@ struct Vecs {  // per-token chunk vectors in shared memory
   int mild;        // G_last >= -40: ratios as d_i * dinv_j
   int abort;
   uint32_t tmem;
-  uint64_t bar;
+  uint64_t bar;      // MMA completion
+  uint64_t bar_raw;  // raw rows landed
+  uint64_t bar_z;    // z rows landed
 };
 static_assert(sizeof(Vecs) <= 2048, "vector area");
 
-__device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
-
-// e^{G_i - G_j} for j <= i
-__device__ __forceinline__ float ratio(const Vecs &V, bool mild, int i, int j) {
-  return mild ? V.d[i] * V.dinv[j] : __expf(V.G[i] - V.G[j]);
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// silu(x) = x / (1 + 2^(-x log2 e)) for a pair, on the paired fp32 pipes plus
+// one ex2 and one rcp per value.  x -> -inf gives 2^inf = inf, rcp -> 0, -0.
+__device__ __forceinline__ float2 silu2(float2 x) {
+  float2 e = __fmul2_rn(x, make_float2(-1.4426950408889634f, -1.4426950408889634f));
+  e = make_float2(ex2_approx(e.x), ex2_approx(e.y));
+  float2 dn = __fadd2_rn(e, make_float2(1.0f, 1.0f));
+  return __fmul2_rn(x, make_float2(rcp_approx(dn.x), rcp_approx(dn.y)));
+}
+
+__device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
 
 // Chunk vectors from g and beta (one warp).  Padded tokens get g = 0, beta = 0.
 __device__ void chunk_vectors(Vecs &V, const float *g, const float *beta, long long gstride,
@@ -154,70 +183,51 @@ __device__ float chunk_decay(const float *g, long long gstride, int t0, int T, i
   return __expf(warp_sum(s));
 }
 
-// Eight consecutive raw io values of one row, as loaded (not yet widened).
-template <typename IO>
-struct Raw8;
-template <>
-struct Raw8<__nv_bfloat16> {
-  uint4 u;
-};
-template <>
-struct Raw8<float> {
-  float4 a, b;
-};
-
-// Raw conv input x~[t] (token t; t < 0 reads the carried window, t >= T reads 0).
-template <typename IO>
-__device__ __forceinline__ Raw8<IO> ld_raw8(const IO *x, const IO *conv0, long long C, int t,
-                                            int T, long long c) {
-  Raw8<IO> r;
-  const IO *p = nullptr;
-  if (t >= 0 && t < T) p = x + (long long)t * C + c;
-  else if (t < 0 && conv0) p = conv0 + (long long)(3 + t) * C + c;
-  if constexpr (sizeof(IO) == 2) {
-    r.u = p ? *reinterpret_cast<const uint4 *>(p) : make_uint4(0, 0, 0, 0);
-  } else {
-    r.a = p ? reinterpret_cast<const float4 *>(p)[0] : make_float4(0.f, 0.f, 0.f, 0.f);
-    r.b = p ? reinterpret_cast<const float4 *>(p)[1] : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  return r;
-}
-// Widen to four channel pairs.
-__device__ __forceinline__ void widen(const Raw8<__nv_bfloat16> &r, float2 (&v)[4]) {
-  const uint32_t w[4] = {r.u.x, r.u.y, r.u.z, r.u.w};
+// Widen 8 bf16 (one 16-byte chunk) to four channel pairs.
+__device__ __forceinline__ void widen(uint4 u, float2 (&v)[4]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) v[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
 }
-__device__ __forceinline__ void widen(const Raw8<float> &r, float2 (&v)[4]) {
-  v[0] = make_float2(r.a.x, r.a.y);
-  v[1] = make_float2(r.a.z, r.a.w);
-  v[2] = make_float2(r.b.x, r.b.y);
-  v[3] = make_float2(r.b.z, r.b.w);
-}
 
-// 16 bytes of fp16 (8 values, packed conversions, no range clamp: the caller
-// guarantees finite fp16 range) to shared memory.
-__device__ __forceinline__ void st_h8_fast(uint8_t *p, const float *v) {
+// 8 values held as 4 pairs -> one 16-byte fp16 chunk (no range clamp: the
+// caller guarantees finite fp16 range).
+__device__ __forceinline__ void st_h8_pairs(uint8_t *p, const float2 (&v)[4]) {
   uint32_t w[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    __half2 t = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+    __half2 t = __floats2half2_rn(v[i].x, v[i].y);
     w[i] = *reinterpret_cast<uint32_t *>(&t);
   }
   *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
 }
+// hi = fp16(v) and lo = fp16(v - hi) of a clamped pair, as two packed words.
+__device__ __forceinline__ void split2(float a, float b, uint32_t &whi, uint32_t &wlo) {
+  a = fminf(fmaxf(a, -kHalfMax), kHalfMax);
+  b = fminf(fmaxf(b, -kHalfMax), kHalfMax);
+  __half2 th = __floats2half2_rn(a, b);
+  const float2 back = __half22float2(th);
+  __half2 tl = __floats2half2_rn(a - back.x, b - back.y);
+  whi = *reinterpret_cast<uint32_t *>(&th);
+  wlo = *reinterpret_cast<uint32_t *>(&tl);
+}
+// The same as a hi/lo pair of 16-byte chunks.
+__device__ __forceinline__ void st_h8_split_pairs(uint8_t *phi, uint8_t *plo, const float2 (&v)[4]) {
+  uint32_t wh[4], wl[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) split2(v[i].x, v[i].y, wh[i], wl[i]);
+  *reinterpret_cast<uint4 *>(phi) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+  *reinterpret_cast<uint4 *>(plo) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+}
 
-// A: front end for one chunk.  All 12 warps: warp w handles block w / 4
-// (q, k, v), two 8-token eighths (one per half-warp) and, per lane, one
-// 8-channel group; each thread slides the conv window over its 8 tokens, four
-// at a time, with the next four rows already in flight.  Every warp runs the
-// same code; what differs per block (norm, outputs) is warp-uniform data.
+// A: front end for one chunk, from the staged raw rows (row r of a block is
+// token t0 - 3 + r).  All 12 warps: warp w handles block w / 4 (q, k, v), two
+// 8-token eighths (one per half-warp) and, per lane, one 8-channel group, and
+// slides the conv window over its 8 tokens.  Every warp runs the same code;
+// what differs per block (norm, outputs) is warp-uniform data.
 // Writes: q^ and k^ (fp16) into [K;Q]; Gamma k^ (hi, lo); v (hi, lo).
-template <typename IO>
-__device__ void front_end(uint8_t *sm, const Vecs &V, const PrefillArgs &a, const IO *x,
-                          const IO *conv0, int h, int kh, int t0, int tid) {
-  const Dims &d = a.d;
-  const long long C = d.C;
+__device__ void front_end(uint8_t *sm, const Vecs &V, const Dims &d, const bf16 *conv_w,
+                          int h, int kh, int t0, int tid) {
   const int warp = tid >> 5, lane = tid & 31;
   const int blk = warp >> 2, eighth = 2 * (warp & 3) + (lane >> 4), grp = lane & 15;
   const long long c = blk == 0   ? (long long)kh * kD + 8 * grp
@@ -229,88 +239,85 @@ __device__ void front_end(uint8_t *sm, const Vecs &V, const PrefillArgs &a, cons
   const float scale = blk == 0 ? d.q_scale : 1.0f;
   uint8_t *const dhi = sm + (blk == 1 ? OFF_GK : OFF_VH);
   uint8_t *const dlo = sm + (blk == 1 ? OFF_GKL : OFF_VL);
-  const IO *cw = static_cast<const IO *>(a.conv_w);
+  const uint8_t *raw = sm + OFF_RAW + blk * kRawBlock + 16 * grp;  // + 256 * row
   float2 w[4][4];  // [channel pair][tap]
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float4 a0 = ld_io4(cw + 4 * (c + 2 * i)), a1 = ld_io4(cw + 4 * (c + 2 * i + 1));
+    const float4 a0 = ld_io4(conv_w + 4 * (c + 2 * i)), a1 = ld_io4(conv_w + 4 * (c + 2 * i + 1));
     w[i][0] = make_float2(a0.x, a1.x);
     w[i][1] = make_float2(a0.y, a1.y);
     w[i][2] = make_float2(a0.z, a1.z);
     w[i][3] = make_float2(a0.w, a1.w);
   }
-  const int tb = t0 + 8 * eighth;
+  const int r0 = 8 * eighth;  // raw row of token t0 + 8 eighth - 3
   float2 x0[4], x1[4], x2[4];
-  {
-    const Raw8<IO> h0 = ld_raw8(x, conv0, C, tb - 3, d.T, c), h1 = ld_raw8(x, conv0, C, tb - 2, d.T, c),
-                   h2 = ld_raw8(x, conv0, C, tb - 1, d.T, c);
-    widen(h0, x0);
-    widen(h1, x1);
-    widen(h2, x2);
-  }
-  Raw8<IO> nx[4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) nx[e] = ld_raw8(x, conv0, C, tb + e, d.T, c);
-
-  auto token = [&](const Raw8<IO> &raw, int tt) {
-    const int t = tb + tt;
-    const int row = 8 * eighth + tt;  // token index within the chunk
-    float2 x3[4];
-    widen(raw, x3);
-    float u[8];
-    float ss = 0.f;
+  widen(*reinterpret_cast<const uint4 *>(raw + 256 * (r0 + 0)), x0);
+  widen(*reinterpret_cast<const uint4 *>(raw + 256 * (r0 + 1)), x1);
+  widen(*reinterpret_cast<const uint4 *>(raw + 256 * (r0 + 2)), x2);
+#pragma unroll 4
+  for (int tt = 0; tt < 8; ++tt) {
+    const int row = r0 + tt;  // token index within the chunk
+    const int t = t0 + row;
+    float2 x3[4], u[4];
+    widen(*reinterpret_cast<const uint4 *>(raw + 256 * (row + 3)), x3);
+    float2 ss2 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       float2 acc = __fmul2_rn(w[i][0], x0[i]);
       acc = __ffma2_rn(w[i][1], x1[i], acc);
       acc = __ffma2_rn(w[i][2], x2[i], acc);
       acc = __ffma2_rn(w[i][3], x3[i], acc);
-      u[2 * i] = t < d.T ? silu_fast(acc.x) : 0.f;
-      u[2 * i + 1] = t < d.T ? silu_fast(acc.y) : 0.f;
-      ss = fmaf(u[2 * i], u[2 * i], fmaf(u[2 * i + 1], u[2 * i + 1], ss));
+      u[i] = silu2(acc);
+      ss2 = __ffma2_rn(u[i], u[i], ss2);
       x0[i] = x1[i];
       x1[i] = x2[i];
       x2[i] = x3[i];
     }
+    if (t >= d.T) {  // padding beyond the sequence
+#pragma unroll
+      for (int i = 0; i < 4; ++i) u[i] = make_float2(0.f, 0.f);
+      ss2 = make_float2(0.f, 0.f);
+    }
+    float ss = ss2.x + ss2.y;
     // sum of squares over the 16 groups of this eighth: one half-warp
 #pragma unroll
     for (int off = 1; off < 16; off <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
     const float f = has_norm ? rsqrtf(ss + d.eps_l2) * scale : 1.0f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) u[i] *= f;
-    if (has_single) st_h8_fast(sm + OFF_KQ + kmaj(row_off + row, 8 * grp, 128), u);
+    for (int i = 0; i < 4; ++i) u[i] = __fmul2_rn(u[i], make_float2(f, f));
+    if (has_single) st_h8_pairs(sm + OFF_KQ + kmaj(row_off + row, 8 * grp, 128), u);
     if (has_split) {
       const float gm = has_gamma ? V.gam[row] : 1.0f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) u[i] *= gm;
+      for (int i = 0; i < 4; ++i) u[i] = __fmul2_rn(u[i], make_float2(gm, gm));
       const uint32_t o = mnmaj(8 * grp, row, kC);
-      st_h8_split(dhi + o, dlo + o, u);
+      st_h8_split_pairs(dhi + o, dlo + o, u);
     }
-  };
-
-#pragma unroll 1
-  for (int g4 = 0; g4 < 8; g4 += 4) {
-    Raw8<IO> cur[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) cur[e] = nx[e];
-    if (g4 + 4 < 8) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) nx[e] = ld_raw8(x, conv0, C, tb + g4 + 4 + e, d.T, c);
-    }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) token(cur[e], g4 + e);
   }
 }
 
-// D: T = (I + L)^{-1} in 16 x 16 blocks (all threads).  The diagonal blocks
-// by forward substitution, one column per thread; then, block row by block
-// row, T_IJ = -T_II sum_{K=J}^{I-1} L_IK T_KJ.  fp32 throughout; the result is
+// T scratch: fp32 [64][64], float4 groups XOR-swizzled by row, so that reads of
+// one row by eight threads (eight rows) and broadcast reads stay conflict free.
+__device__ __forceinline__ int tfi(int row, int col) {
+  return row * kC + ((((col >> 2) ^ (row & 15)) << 2) | (col & 3));
+}
+__device__ __forceinline__ void fma4(float4 &acc, float s, const float4 t) {
+  acc.x = fmaf(s, t.x, acc.x);
+  acc.y = fmaf(s, t.y, acc.y);
+  acc.z = fmaf(s, t.z, acc.z);
+  acc.w = fmaf(s, t.w, acc.w);
+}
+
+// D: T = (I + L)^{-1} in 16 x 16 blocks.  The diagonal blocks by forward
+// substitution, one column per thread; then, block row by block row,
+// T_IJ = -T_II sum_{K=J}^{I-1} L_IK T_KJ, each thread one row and four
+// columns of a block (16-byte shared loads).  fp32 throughout; the result is
 // written as the fp16 K-major tiles T diag(beta) (hi, lo) and T diag(beta d).
-// L is [64][kLs] (padded rows), T is [64][64].
+// L is [64][kLs] (padded rows), T is [64][64] swizzled (tfi).
 __device__ void solve_T(uint8_t *sm, const Vecs &V, int tid) {
   const float *L = reinterpret_cast<const float *>(sm + OFF_L);
   float *Tf = reinterpret_cast<float *>(sm + OFF_TF);
-  float *P = reinterpret_cast<float *>(sm + OFF_PB);
+  float *P = reinterpret_cast<float *>(sm + OFF_PB);  // [3][16][16]
   if (tid < kC) {
     const int base = 16 * (tid >> 4), c = tid & 15;
     const float *Lb = L + base * kLs + base;
@@ -321,65 +328,74 @@ __device__ void solve_T(uint8_t *sm, const Vecs &V, int tid) {
     for (int i = 1; i < 16; ++i) {
       float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-      for (int j = 0; j < i; ++j) {
-        if (j & 1) a1 = fmaf(Lb[i * kLs + j], xv[j], a1);
-        else a0 = fmaf(Lb[i * kLs + j], xv[j], a0);
+      for (int j4 = 0; j4 < i; j4 += 4) {
+        const float4 l = ld4(Lb + i * kLs + j4);
+        a0 = fmaf(l.x, xv[j4], a0);
+        if (j4 + 1 < i) a1 = fmaf(l.y, xv[j4 + 1], a1);
+        if (j4 + 2 < i) a0 = fmaf(l.z, xv[j4 + 2], a0);
+        if (j4 + 3 < i) a1 = fmaf(l.w, xv[j4 + 3], a1);
       }
       xv[i] -= a0 + a1;
     }
 #pragma unroll
-    for (int i = 0; i < 16; ++i) Tf[(base + i) * kC + base + c] = xv[i];
+    for (int i = 0; i < 16; ++i) Tf[tfi(base + i, base + c)] = xv[i];
   }
   __syncthreads();
-  const bool worker = tid < 256;
-  const int r = (tid >> 4) & 15, c = tid & 15;
 #pragma unroll 1
   for (int I = 1; I < 4; ++I) {
-    const float *Lr = L + (16 * I + r) * kLs;
-#pragma unroll 1
-    for (int J = 0; J < (worker ? I : 0); ++J) {
-      float a0 = 0.f, a1 = 0.f;
-#pragma unroll 1
+    // work item e < 64 I: block J = e / 64, row r, column group c4
+    const int e = tid, J = e >> 6, r = (e >> 2) & 15, c4 = e & 3;
+    const bool active = e < 64 * I;
+    if (active) {
+      const float *Lr = L + (16 * I + r) * kLs;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int K = J; K < I; ++K) {
-        const float *l = Lr + 16 * K;
-        const float *t = Tf + 16 * K * kC + 16 * J + c;
 #pragma unroll
-        for (int k = 0; k < 16; k += 2) {
-          a0 = fmaf(l[k], t[k * kC], a0);
-          a1 = fmaf(l[k + 1], t[(k + 1) * kC], a1);
+        for (int k4 = 0; k4 < 16; k4 += 4) {
+          const float4 l = ld4(Lr + 16 * K + k4);
+          const int row = 16 * K + k4, col = 16 * J + 4 * c4;
+          fma4(acc, l.x, ld4(Tf + tfi(row + 0, col)));
+          fma4(acc, l.y, ld4(Tf + tfi(row + 1, col)));
+          fma4(acc, l.z, ld4(Tf + tfi(row + 2, col)));
+          fma4(acc, l.w, ld4(Tf + tfi(row + 3, col)));
         }
       }
-      P[J * 256 + r * 16 + c] = a0 + a1;
+      *reinterpret_cast<float4 *>(P + J * 256 + r * 16 + 4 * c4) = acc;
     }
     __syncthreads();
-    const float *Tii = Tf + (16 * I + r) * kC + 16 * I;
-#pragma unroll 1
-    for (int J = 0; J < (worker ? I : 0); ++J) {
-      const float *pj = P + J * 256 + c;
-      float s0 = 0.f, s1 = 0.f;
+    if (active) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      const int row = 16 * I + r;
 #pragma unroll
-      for (int k = 0; k < 16; k += 2) {
-        s0 = fmaf(Tii[k], pj[k * 16], s0);
-        s1 = fmaf(Tii[k + 1], pj[(k + 1) * 16], s1);
+      for (int k4 = 0; k4 < 16; k4 += 4) {
+        const float4 t = ld4(Tf + tfi(row, 16 * I + k4));
+        fma4(acc, t.x, ld4(P + J * 256 + (k4 + 0) * 16 + 4 * c4));
+        fma4(acc, t.y, ld4(P + J * 256 + (k4 + 1) * 16 + 4 * c4));
+        fma4(acc, t.z, ld4(P + J * 256 + (k4 + 2) * 16 + 4 * c4));
+        fma4(acc, t.w, ld4(P + J * 256 + (k4 + 3) * 16 + 4 * c4));
       }
-      Tf[(16 * I + r) * kC + 16 * J + c] = -(s0 + s1);
+      *reinterpret_cast<float4 *>(Tf + tfi(row, 16 * J + 4 * c4)) =
+          make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
     }
     __syncthreads();
   }
-  // fp16 tiles: 512 chunks of 8 each, two per thread; blocks above the diagonal are zero
+  // fp16 tiles: 512 chunks of 8 each, two per thread (256 threads); blocks above the diagonal are zero
+  if (tid < 256) {
 #pragma unroll 1
-  for (int m = 0; m < (worker ? 2 : 0); ++m) {
-    const int q = tid + 256 * m, i = q >> 3, j0 = (q & 7) * 8;
-    const bool below = (j0 >> 4) <= (i >> 4);
-    float tb[8], tw[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const float t = below ? Tf[i * kC + j0 + u] : 0.f;
-      tb[u] = t * V.beta[j0 + u];
-      tw[u] = t * V.bd[j0 + u];
+    for (int m = 0; m < 2; ++m) {
+      const int q = tid + 256 * m, i = q >> 3, j0 = (q & 7) * 8;
+      const bool below = (j0 >> 4) <= (i >> 4);
+      const float4 t0 = below ? ld4(Tf + tfi(i, j0)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 t1 = below ? ld4(Tf + tfi(i, j0 + 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 b0 = ld4(V.beta + j0), b1 = ld4(V.beta + j0 + 4);
+      const float4 e0 = ld4(V.bd + j0), e1 = ld4(V.bd + j0 + 4);
+      const float tb[8] = {t0.x * b0.x, t0.y * b0.y, t0.z * b0.z, t0.w * b0.w,
+                           t1.x * b1.x, t1.y * b1.y, t1.z * b1.z, t1.w * b1.w};
+      const float tw[8] = {t0.x * e0.x, t0.y * e0.y, t0.z * e0.z, t0.w * e0.w,
+                           t1.x * e1.x, t1.y * e1.y, t1.z * e1.z, t1.w * e1.w};
+      st_h8_split(sm + OFF_TU + kmaj(i, j0, kC), sm + OFF_TUL + kmaj(i, j0, kC), tb);
+      st_h8(sm + OFF_TW + kmaj(i, j0, kC), tw);
     }
-    st_h8_split(sm + OFF_TU + kmaj(i, j0, kC), sm + OFF_TUL + kmaj(i, j0, kC), tb);
-    st_h8(sm + OFF_TW + kmaj(i, j0, kC), tw);
   }
 }
 
@@ -388,9 +404,25 @@ template <typename FA, typename FB>
 __device__ __forceinline__ void issue(uint32_t d, uint32_t id, int nk, bool accumulate_first, FA da, FB db) {
   for (int ks = 0; ks < nk; ++ks) mma(d, da(ks), db(ks), id, (accumulate_first || ks > 0) ? 1u : 0u);
 }
+// The same with A in TMEM at column a0 (8 columns per K step).
+template <typename FB>
+__device__ __forceinline__ void issue_ta(uint32_t d, uint32_t a0, uint32_t id, int nk, bool accumulate_first,
+                                         FB db) {
+  for (int ks = 0; ks < nk; ++ks) mma_ta(d, a0 + 8 * ks, db(ks), id, (accumulate_first || ks > 0) ? 1u : 0u);
+}
 
-template <typename IO>
-__global__ void __launch_bounds__(kThreads, 1) prefill_chunked_kernel(PrefillArgs a) {
+// Pack 32 fp32 values into 16 fp16-pair words (clamped to the fp16 range).
+__device__ __forceinline__ void pack_h16(const float (&v)[32], uint32_t (&w)[16]) {
+#pragma unroll
+  for (int q = 0; q < 16; ++q) {
+    __half2 t = __halves2half2(to_h(v[2 * q]), to_h(v[2 * q + 1]));
+    w[q] = *reinterpret_cast<uint32_t *>(&t);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_chunked_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tm_qkv,
+                           const __grid_constant__ CUtensorMap tm_z) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   Vecs &V = *reinterpret_cast<Vecs *>(sm + OFF_VEC);
@@ -401,14 +433,30 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunked_kernel(PrefillArg
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int T = d.T;
   const long long C = d.C;
-  const IO *x = static_cast<const IO *>(a.qkv_pre) + (long long)b * T * C;
-  const IO *conv0 = a.conv0 ? static_cast<const IO *>(a.conv0) + (long long)b * 3 * C : nullptr;
+  const bf16 *x = static_cast<const bf16 *>(a.qkv_pre) + (long long)b * T * C;
+  const bf16 *conv0 = a.conv0 ? static_cast<const bf16 *>(a.conv0) + (long long)b * 3 * C : nullptr;
+  const bf16 *conv_w = static_cast<const bf16 *>(a.conv_w);
   const float *gp = a.g + (long long)b * T * d.Hv + h;
   const float *bp = a.beta + (long long)b * T * d.Hv + h;
   const long long unit_off = ((long long)b * d.Hv + h) * kD * kD;
+  const uint32_t sbase = smem_u32(sm);
+  const int cq = kh * kD, ck = d.Hk * kD + kh * kD, cv = 2 * d.Hk * kD + h * kD;
+
+  auto request_raw = [&](int t0) {  // one thread: the raw rows t0-3 .. t0+63 of q, k, v
+    bar_expect_tx(&V.bar_raw, 3 * kRawBlock);
+    tma_load_3d(sbase + OFF_RAW + 0 * kRawBlock, &tm_qkv, cq, t0 - 3, b, &V.bar_raw);
+    tma_load_3d(sbase + OFF_RAW + 1 * kRawBlock, &tm_qkv, ck, t0 - 3, b, &V.bar_raw);
+    tma_load_3d(sbase + OFF_RAW + 2 * kRawBlock, &tm_qkv, cv, t0 - 3, b, &V.bar_raw);
+  };
+  auto request_z = [&](int t0) {  // one thread: the z rows t0 .. t0+63 of head h
+    bar_expect_tx(&V.bar_z, kC * kD * 2);
+    tma_load_3d(sbase + OFF_Z, &tm_z, h * kD, t0, b, &V.bar_z);
+  };
 
   if (tid == 0) {
     bar_init(&V.bar, 1);
+    bar_init(&V.bar_raw, 1);
+    bar_init(&V.bar_z, 1);
     V.abort = 0;
   }
   if (warp == 0) tmem_alloc(&V.tmem, kTmemCols);
@@ -419,13 +467,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunked_kernel(PrefillArg
   fence_before();
   __syncthreads();
   fence_after();
+  if (tid == 0) {
+    request_raw(0);
+    request_z(0);
+  }
   const uint32_t tmem = V.tmem;
   // TMEM lane quadrant and column half of this warp for the 32x32b accesses.
   const int quad = warp & 3, half = warp >> 2;
   const int lrow = 32 * quad + lane;  // TMEM lane (row) this thread reads
   const uint32_t tl = tmem + ((uint32_t)(32 * quad) << 16);
 
-  // Initial state: TMEM <- dC(chunk 0) * S0, shared fp16 copy <- S0.
+  // Initial state: TMEM fp32 <- dC(chunk 0) * S0, TMEM fp16 copy <- S0.
   if (warp < kTmemWarps) {
     const float dc0 = V.dC_next;
     float v[32];
@@ -443,26 +495,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunked_kernel(PrefillArg
 #pragma unroll
         for (int q = 0; q < 32; ++q) v[q] = 0.f;
       }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) st_h8(sm + OFF_S + kmaj(lrow, k0 + 8 * q, 128), v + 8 * q);
+      uint32_t w16[16];
+      pack_h16(v, w16);
+      tmem_st16w(tl + TM_S16 + k0 / 2, w16);
 #pragma unroll
       for (int q = 0; q < 32; ++q) v[q] *= dc0;
       tmem_st32(tl + TM_S + k0, v);
     }
   }
 
-  uint32_t phase = 0;
+  uint32_t phase = 0, phase_raw = 0, phase_z = 0;
+  bool raw_pending = true, z_pending = true;  // a requested TMA not yet consumed
   const int nchunks = (T + kC - 1) / kC;
   const uint32_t id_kk = idesc(128, 64, 0, 0);
   const uint32_t id_mk = idesc(128, 64, 1, 0);
   const uint32_t id_km = idesc(128, 64, 0, 1);
   const uint32_t id_km128 = idesc(128, 128, 0, 1);
-  const uint32_t sbase = smem_u32(sm);
 
-  auto mma_sync = [&]() -> bool {
-    // all threads: wait for the committed MMAs; uniform abort decision
-    bool ok = bar_wait(&V.bar, phase);
-    phase ^= 1u;
+  // All threads: wait on an mbarrier phase; a uniform decision to abort.
+  auto wait_all = [&](uint64_t *bar, uint32_t &ph) -> bool {
+    bool ok = bar_wait(bar, ph);
+    ph ^= 1u;
     fence_after();
     const int bad = __syncthreads_or(!ok);
     if (bad && tid == 0) {
@@ -471,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunked_kernel(PrefillArg
     }
     return !bad;
   };
-  auto smem_ready = [&]() {  // shared-memory operands written -> visible to the MMA unit
+  auto smem_ready = [&]() {  // operands written (shared memory or TMEM) -> visible to the MMA unit
     fence_smem_to_async();
     fence_before();
     __syncthreads();
@@ -485,9 +538,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunked_kernel(PrefillArg
       const float dcn = n + 1 < nchunks ? chunk_decay(gp, d.Hv, t0 + kC, T, lane) : 1.f;
       if (lane == 0) V.dC_next = dcn;
     }
-    __syncthreads();
+    if (!wait_all(&V.bar_raw, phase_raw)) break;
+    raw_pending = false;
+    if (n == 0 && conv0) {  // rows before the first token come from the carried window
+      for (int idx = tid; idx < 3 * 3 * 16; idx += kThreads) {
+        const int blk = idx / 48, rw = (idx / 16) % 3, g8 = idx % 16;
+        const int cc = blk == 0 ? cq : blk == 1 ? ck : cv;
+        *reinterpret_cast<uint4 *>(sm + OFF_RAW + blk * kRawBlock + 256 * rw + 16 * g8) =
+            *reinterpret_cast<const uint4 *>(conv0 + (long long)rw * C + cc + 8 * g8);
+      }
+      __syncthreads();
+    }
     // A: front end
-    front_end<IO>(sm, V, a, x, conv0, h, kh, t0, tid);
+    front_end(sm, V, d, conv_w, h, kh, t0, tid);
     smem_ready();
     // B: MMA1  [K;Q] K^T
     if (tid == 0) {
@@ -496,34 +559,43 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunked_kernel(PrefillArg
             [&](int ks) { return desc_k(sbase + OFF_KQ, ks, 128); });
       commit(&V.bar);
     }
-    if (!mma_sync()) break;
+    if (!wait_all(&V.bar, phase)) break;
     // C: L (fp32, strictly lower, decayed beta K K^T) and M (fp16, decayed Q K^T incl. diagonal)
     if (warp < kTmemWarps) {
-      float v[32];
+      float v[32], rr[32];
       tmem_ld32(tl + TM_KQ + 32 * half, v);
       const int j0 = 32 * half;
-      const bool mild = V.mild != 0;
-      if (lrow < kC) {
-        const int i = lrow;
-        const float bi = V.beta[i];
-        float *L = reinterpret_cast<float *>(sm + OFF_L);
+      const int i = lrow < kC ? lrow : lrow - kC;
+      if (V.mild) {
+        const float di = V.d[i];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          float4 f;
-          const int j = j0 + 4 * q;
-          f.x = (j + 0 < i) ? bi * v[4 * q + 0] * ratio(V, mild, i, j + 0) : 0.f;
-          f.y = (j + 1 < i) ? bi * v[4 * q + 1] * ratio(V, mild, i, j + 1) : 0.f;
-          f.z = (j + 2 < i) ? bi * v[4 * q + 2] * ratio(V, mild, i, j + 2) : 0.f;
-          f.w = (j + 3 < i) ? bi * v[4 * q + 3] * ratio(V, mild, i, j + 3) : 0.f;
-          *reinterpret_cast<float4 *>(L + i * kLs + j) = f;
+        for (int q = 0; q < 32; q += 4) {
+          const float4 dv = ld4(V.dinv + j0 + q);
+          rr[q] = di * dv.x;
+          rr[q + 1] = di * dv.y;
+          rr[q + 2] = di * dv.z;
+          rr[q + 3] = di * dv.w;
         }
       } else {
-        const int i = lrow - kC;
+        const float gi = V.G[i];
 #pragma unroll
-        for (int q = 0; q < 32; ++q) {
-          const int j = j0 + q;
-          v[q] = (j <= i) ? v[q] * ratio(V, mild, i, j) : 0.f;
+        for (int q = 0; q < 32; ++q) rr[q] = __expf(gi - V.G[j0 + q]);
+      }
+      if (lrow < kC) {
+        const float bi = V.beta[i];
+        float *L = reinterpret_cast<float *>(sm + OFF_L) + i * kLs + j0;
+#pragma unroll
+        for (int q = 0; q < 32; q += 4) {
+          float4 f;
+          f.x = (j0 + q + 0 < i) ? bi * v[q + 0] * rr[q + 0] : 0.f;
+          f.y = (j0 + q + 1 < i) ? bi * v[q + 1] * rr[q + 1] : 0.f;
+          f.z = (j0 + q + 2 < i) ? bi * v[q + 2] * rr[q + 2] : 0.f;
+          f.w = (j0 + q + 3 < i) ? bi * v[q + 3] * rr[q + 3] : 0.f;
+          *reinterpret_cast<float4 *>(L + q) = f;
         }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 32; ++q) v[q] = (j0 + q <= i) ? v[q] * rr[q] : 0.f;
 #pragma unroll
         for (int q = 0; q < 4; ++q) st_h8(sm + OFF_M + kmaj(i, j0 + 8 * q, kC), v + 8 * q);
       }
@@ -533,7 +605,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunked_kernel(PrefillArg
     solve_T(sm, V, tid);
     smem_ready();
     // E: MMA2 U^T = V^T (T B)^T, hi*hi + lo*hi + hi*lo; MMA3 W^T = K^T (T B D)^T
-    // (K^ read from [K;Q] as an MN-major operand)
+    // (K^ read from [K;Q] as an MN-major operand).  The raw rows are free now:
+    // request the next chunk's.
     if (tid == 0) {
       fence_after();
       auto a_vh = [&](int ks) { return desc_mn(sbase + OFF_VH, ks, kC); };
@@ -545,8 +618,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunked_kernel(PrefillArg
             [&](int ks) { return desc(sbase + OFF_KQ + (uint32_t)(ks * 2048), 128 * 128, 1024); },
             [&](int ks) { return desc_k(sbase + OFF_TW, ks, kC); });
       commit(&V.bar);
+      if (n + 1 < nchunks) request_raw(t0 + kC);
     }
-    if (!mma_sync()) break;
+    if (n + 1 < nchunks) raw_pending = true;
+    if (!wait_all(&V.bar, phase)) break;
     // F: -W^T (lanes k, columns i) -> MN-major [k][i]
     if (warp < kTmemWarps) {
       float v[32];
@@ -557,47 +632,52 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunked_kernel(PrefillArg
       for (int q = 0; q < 4; ++q) st_h8(sm + OFF_NW + mnmaj(32 * half + 8 * q, lrow, kD), v + 8 * q);
     }
     smem_ready();
-    // G: MMA4 Delta^T = U^T - S W^T;  MMA5 S Q^T (Q^ = rows 64..127 of [K;Q])
+    // G: MMA4 Delta^T = U^T - S W^T;  MMA5 S Q^T (Q^ = rows 64..127 of [K;Q]); S from TMEM
     if (tid == 0) {
       fence_after();
-      auto a_s = [&](int ks) { return desc_k(sbase + OFF_S, ks, 128); };
-      issue(tmem + TM_U, id_km, 8, true, a_s, [&](int ks) { return desc_mn(sbase + OFF_NW, ks, kD); });
-      issue(tmem + TM_O1, id_kk, 8, false, a_s, [&](int ks) { return desc_k(sbase + OFF_KQ + 64 * 128, ks, 128); });
+      issue_ta(tmem + TM_U, tmem + TM_S16, id_km, 8, true, [&](int ks) { return desc_mn(sbase + OFF_NW, ks, kD); });
+      issue_ta(tmem + TM_O1, tmem + TM_S16, id_kk, 8, false,
+               [&](int ks) { return desc_k(sbase + OFF_KQ + 64 * 128, ks, 128); });
       commit(&V.bar);
     }
-    if (!mma_sync()) break;
-    // H: Delta^T (lanes v, columns j) -> K-major [v][j], hi and lo
+    if (!wait_all(&V.bar, phase)) break;
+    // H: Delta^T (lanes v, columns j) -> fp16 hi and lo pairs in TMEM
     if (warp < kTmemWarps) {
       float v[32];
       tmem_ld32(tl + TM_U + 32 * half, v);
+      uint32_t wh[16], wl[16];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint32_t o = kmaj(lrow, 32 * half + 8 * q, 128);
-        st_h8_split(sm + OFF_DT + o, sm + OFF_DTL + o, v + 8 * q);
-      }
+      for (int q = 0; q < 16; ++q) split2(v[2 * q], v[2 * q + 1], wh[q], wl[q]);
+      tmem_st16w(tl + TM_KQ + 16 * half, wh);
+      tmem_st16w(tl + TM_KQ + 32 + 16 * half, wl);
     }
     smem_ready();
     // I: MMA6 Delta^T M^T;  MMA7 S += Delta^T (Gamma K), hi*hi + hi*lo + lo*hi
     if (tid == 0) {
       fence_after();
-      auto a_dt = [&](int ks) { return desc_k(sbase + OFF_DT, ks, 128); };
       auto b_gk = [&](int ks) { return desc_mn(sbase + OFF_GK, ks, kC); };
-      issue(tmem + TM_O2, id_kk, 4, false, a_dt, [&](int ks) { return desc_k(sbase + OFF_M, ks, kC); });
-      issue(tmem + TM_S, id_km128, 4, true, a_dt, b_gk);
-      issue(tmem + TM_S, id_km128, 4, true, a_dt, [&](int ks) { return desc_mn(sbase + OFF_GKL, ks, kC); });
-      issue(tmem + TM_S, id_km128, 4, true, [&](int ks) { return desc_k(sbase + OFF_DTL, ks, 128); }, b_gk);
+      issue_ta(tmem + TM_O2, tmem + TM_KQ, id_kk, 4, false, [&](int ks) { return desc_k(sbase + OFF_M, ks, kC); });
+      issue_ta(tmem + TM_S, tmem + TM_KQ, id_km128, 4, true, b_gk);
+      issue_ta(tmem + TM_S, tmem + TM_KQ, id_km128, 4, true, [&](int ks) { return desc_mn(sbase + OFF_GKL, ks, kC); });
+      issue_ta(tmem + TM_S, tmem + TM_KQ + 32, id_km128, 4, true, b_gk);
       commit(&V.bar);
     }
-    if (!mma_sync()) break;
+    if (!wait_all(&V.bar, phase)) break;
     // J1: O^T = d (S Q^T) + Delta^T M^T -> staging [i][v]; S -> fp16 copy and
-    // rescaled TMEM state (or S_T after the last chunk)
+    // rescaled state (or S_T after the last chunk), all in TMEM
     if (warp < kTmemWarps) {
       float *ost = reinterpret_cast<float *>(sm + OFF_OST);
       float v[32], w2[32];
       tmem_ld32(tl + TM_O1 + 32 * half, v);
       tmem_ld32(tl + TM_O2 + 32 * half, w2);
 #pragma unroll
-      for (int q = 0; q < 32; ++q) ost[(32 * half + q) * kD + lrow] = fmaf(V.d[32 * half + q], v[q], w2[q]);
+      for (int q = 0; q < 32; q += 4) {
+        const float4 dq = ld4(V.d + 32 * half + q);
+        ost[(32 * half + q + 0) * kD + lrow] = fmaf(dq.x, v[q + 0], w2[q + 0]);
+        ost[(32 * half + q + 1) * kD + lrow] = fmaf(dq.y, v[q + 1], w2[q + 1]);
+        ost[(32 * half + q + 2) * kD + lrow] = fmaf(dq.z, v[q + 2], w2[q + 2]);
+        ost[(32 * half + q + 3) * kD + lrow] = fmaf(dq.w, v[q + 3], w2[q + 3]);
+      }
       const bool last = n + 1 == nchunks;
       const float dcn = V.dC_next;
 #pragma unroll
@@ -609,8 +689,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunked_kernel(PrefillArg
 #pragma unroll
           for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
         } else {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) st_h8(sm + OFF_S + kmaj(lrow, k0 + 8 * q, 128), v + 8 * q);
+          uint32_t w16[16];
+          pack_h16(v, w16);
+          tmem_st16w(tl + TM_S16 + k0 / 2, w16);
 #pragma unroll
           for (int q = 0; q < 32; ++q) v[q] *= dcn;
           tmem_st32(tl + TM_S + k0, v);
@@ -618,57 +699,58 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunked_kernel(PrefillArg
       }
     }
     fence_before();
-    __syncthreads();
-    // J2: gated RMSNorm per token, one warp per token (z rows loaded first)
+    if (!wait_all(&V.bar_z, phase_z)) break;  // also the barrier after J1
+    z_pending = false;
+    // J2: gated RMSNorm per token, one warp per token, z from the staged rows
     {
       const float *ost = reinterpret_cast<const float *>(sm + OFF_OST);
-      const float4 w4 = ld_io4(static_cast<const IO *>(a.norm_w) + 4 * lane);
+      const float4 w4 = ld_io4(static_cast<const bf16 *>(a.norm_w) + 4 * lane);
       const int nv = min(kC, T - t0);
-      const IO *zb = static_cast<const IO *>(a.z) + (((long long)b * T + t0) * d.Hv + h) * kD + 4 * lane;
-      const long long zstride = (long long)d.Hv * kD;
-      constexpr int kNW = kThreads / 32, kPer = (kC + kNW - 1) / kNW;
-      float4 z4[kPer];
-#pragma unroll
-      for (int m = 0; m < kPer; ++m) {
-        const int i = warp + kNW * m;
-        z4[m] = i < nv ? ld_io4(zb + i * zstride) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-      IO *ob = static_cast<IO *>(a.o) + (((long long)b * T + t0) * d.Hv + h) * kD + 4 * lane;
-#pragma unroll
-      for (int m = 0; m < kPer; ++m) {
-        const int i = warp + kNW * m;
-        if (i < nv) {
-          const float4 o4 = reinterpret_cast<const float4 *>(ost + i * kD)[lane];
-          const float rstd = rsqrtf(warp_sum(dot4(o4, o4)) * (1.0f / kD) + d.eps_norm);
-          float4 y;
-          y.x = w4.x * (o4.x * rstd) * silu_fast(z4[m].x);
-          y.y = w4.y * (o4.y * rstd) * silu_fast(z4[m].y);
-          y.z = w4.z * (o4.z * rstd) * silu_fast(z4[m].z);
-          y.w = w4.w * (o4.w * rstd) * silu_fast(z4[m].w);
-          st_io4(ob + i * zstride, y);
-        }
+      bf16 *ob = static_cast<bf16 *>(a.o) + (((long long)b * T + t0) * d.Hv + h) * kD + 4 * lane;
+      const long long ostride = (long long)d.Hv * kD;
+#pragma unroll 2
+      for (int i = warp; i < nv; i += kThreads / 32) {
+        const float4 o4 = reinterpret_cast<const float4 *>(ost + i * kD)[lane];
+        const float4 z4 = ld_io4(reinterpret_cast<const bf16 *>(sm + OFF_Z) + i * kD + 4 * lane);
+        const float rstd = rsqrtf(warp_sum(dot4(o4, o4)) * (1.0f / kD) + d.eps_norm);
+        const float2 s01 = silu2(make_float2(z4.x, z4.y)), s23 = silu2(make_float2(z4.z, z4.w));
+        float4 y;
+        y.x = w4.x * (o4.x * rstd) * s01.x;
+        y.y = w4.y * (o4.y * rstd) * s01.y;
+        y.z = w4.z * (o4.z * rstd) * s23.x;
+        y.w = w4.w * (o4.w * rstd) * s23.y;
+        st_io4(ob + i * ostride, y);
       }
     }
+    fence_smem_to_async();  // z and the staging were read: order before the next TMA writes
     __syncthreads();
+    if (n + 1 < nchunks) {
+      if (tid == 0) request_z(t0 + kC);
+      z_pending = true;
+    }
   }
 
   // Carried conv window: the last three raw rows of the channels this CTA owns.
   {
-    IO *cT = static_cast<IO *>(a.conv_T) + (long long)b * 3 * C;
+    bf16 *cT = static_cast<bf16 *>(a.conv_T) + (long long)b * 3 * C;
     const bool own_qk = (h % r) == 0;
     for (int idx = tid; idx < 3 * 3 * kD; idx += kThreads) {
       const int e = idx / (3 * kD), rem = idx % (3 * kD), blk = rem / kD, ch = rem % kD;
       if (blk < 2 && !own_qk) continue;
-      const long long c = blk == 0   ? (long long)kh * kD + ch
-                          : blk == 1 ? (long long)d.Hk * kD + (long long)kh * kD + ch
-                                     : 2LL * d.Hk * kD + (long long)h * kD + ch;
+      const long long c = (blk == 0 ? cq : blk == 1 ? ck : cv) + ch;
       const int t = T - 3 + e;
-      IO val;
+      bf16 val;
       if (t >= 0) val = x[(long long)t * C + c];
       else if (conv0) val = conv0[(long long)(3 + t) * C + c];
-      else val = IO(0.f);
+      else val = bf16(0.f);
       cT[(long long)e * C + c] = val;
     }
+  }
+  // After an early exit, no requested copy may still be landing in shared
+  // memory when the CTA ends: wait (bounded) for any that was not consumed.
+  if (tid == 0) {
+    if (raw_pending) bar_wait(&V.bar_raw, phase_raw);
+    if (z_pending) bar_wait(&V.bar_z, phase_z);
   }
   fence_before();
   __syncthreads();
@@ -678,22 +760,48 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunked_kernel(PrefillArg
   }
 }
 
+// cuTensorMapEncodeTiled, found once through the runtime (no libcuda link).
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                 const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiled encoder() {
+  static EncodeTiled fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(p);
+  }
+  return fn;
+}
+
+// A [B][T][width] bf16 tensor as a 3-d map with boxes of 128 columns x `rows` rows.
+bool encode_rows(CUtensorMap *m, const void *base, long long width, int T, int B, int rows) {
+  EncodeTiled enc = encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)T, (cuuint64_t)B};
+  const cuuint64_t strides[2] = {(cuuint64_t)width * 2, (cuuint64_t)width * 2 * T};
+  const cuuint32_t box[3] = {(cuuint32_t)kD, (cuuint32_t)rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
-cudaError_t launch_prefill_chunked(const PrefillArgs &a, bool bf16, cudaStream_t s) {
-  dim3 grid((unsigned)(a.d.B * a.d.Hv)), block(kThreads);
-  cudaError_t e;
-  if (bf16) {
-    e = cudaFuncSetAttribute(prefill_chunked_kernel<__nv_bfloat16>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
-    prefill_chunked_kernel<__nv_bfloat16><<<grid, block, kSmemBytes, s>>>(a);
-  } else {
-    e = cudaFuncSetAttribute(prefill_chunked_kernel<float>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
-    prefill_chunked_kernel<float><<<grid, block, kSmemBytes, s>>>(a);
-  }
+cudaError_t launch_prefill_chunked(const PrefillArgs &a, bool bf16_io, cudaStream_t s) {
+  if (!bf16_io) return cudaErrorInvalidValue;  // the chunked kernel stages bf16 rows
+  CUtensorMap tm_qkv, tm_z;
+  if (!encode_rows(&tm_qkv, a.qkv_pre, a.d.C, a.d.T, a.d.B, kRawRows) ||
+      !encode_rows(&tm_z, a.z, (long long)a.d.Hv * kD, a.d.T, a.d.B, kC))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(prefill_chunked_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
+  prefill_chunked_kernel<<<dim3((unsigned)(a.d.B * a.d.Hv)), dim3(kThreads), kSmemBytes, s>>>(a, tm_qkv, tm_z);
   return cudaGetLastError();
 }
 
