@@ -29,13 +29,13 @@
 // of its rms where single fp16 gives 2e-2 on short, heavy-tailed updates.
 // Per chunk, in order:
 //   A  conv + SiLU + L2 norms (front end) from the staged raw rows
-//   B  MMA1  [K;Q] K^T                        -> K K^T, Q K^T
+//   B  MMA1  [K;Q] K^T -> K K^T, Q K^T;  MMA5  S Q^T
 //   C  decayed lower-triangular L (fp32) and M (fp16)
 //   D  T = (I + L)^{-1} in 16 x 16 blocks (fp32, CUDA cores) -> T B, T B D
 //   E  MMA2  U^T = V^T (T B)^T (split);  MMA3  W^T = K^T (T B D)^T;
 //      the next chunk's raw rows are requested (TMA)
 //   F  -W^T to shared memory
-//   G  MMA4  Delta^T = U^T - S W^T;  MMA5  S Q^T
+//   G  MMA4  Delta^T = U^T - S W^T
 //   H  Delta^T (hi, lo) to TMEM
 //   I  MMA6  Delta^T M^T;            MMA7  S += Delta^T (Gamma K) (split)
 //   J  O = d (S Q^T) + Delta^T M^T, gated RMSNorm (node gdn.norm) -> o;
@@ -135,16 +135,21 @@ __device__ __forceinline__ float2 silu2(float2 x) {
 
 __device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
 
-// Chunk vectors from g and beta (one warp).  Padded tokens get g = 0, beta = 0.
-__device__ void chunk_vectors(Vecs &V, const float *g, const float *beta, long long gstride,
-                              int T, int lane) {
-  float gv[2], bv[2];
+// g and beta of the chunk starting at t0 (one warp: tokens lane, lane + 32),
+// loaded a chunk ahead of use.  Padded tokens get g = 0, beta = 0; g is
+// clamped at kGMin.
+__device__ __forceinline__ void load_gb(const float *g, const float *beta, long long gstride, int t0,
+                                        int T, int lane, float (&gv)[2], float (&bv)[2]) {
 #pragma unroll
   for (int u = 0; u < 2; ++u) {
-    const int t = lane + 32 * u;
+    const int t = t0 + lane + 32 * u;
     gv[u] = t < T ? fmaxf(g[(long long)t * gstride], kGMin) : 0.f;
     bv[u] = t < T ? beta[(long long)t * gstride] : 0.f;
   }
+}
+
+// Chunk vectors from the chunk's g and beta (one warp).
+__device__ void chunk_vectors(Vecs &V, float (&gv)[2], const float (&bv)[2], int lane) {
 #pragma unroll
   for (int u = 0; u < 2; ++u)
 #pragma unroll
@@ -170,17 +175,6 @@ __device__ void chunk_vectors(Vecs &V, const float *g, const float *beta, long l
     V.dC = __expf(Glast);
     V.mild = mild ? 1 : 0;
   }
-}
-
-// e^{sum of the chunk's clamped g} for the chunk starting at t0 (one warp).
-__device__ float chunk_decay(const float *g, long long gstride, int t0, int T, int lane) {
-  float s = 0.f;
-#pragma unroll
-  for (int u = 0; u < 2; ++u) {
-    const int t = t0 + lane + 32 * u;
-    s += t < T ? fmaxf(g[(long long)t * gstride], kGMin) : 0.f;
-  }
-  return __expf(warp_sum(s));
 }
 
 // Widen 8 bf16 (one 16-byte chunk) to four channel pairs.
@@ -460,8 +454,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     V.abort = 0;
   }
   if (warp == 0) tmem_alloc(&V.tmem, kTmemCols);
+  float g_cur[2], b_cur[2], g_nxt[2], b_nxt[2];  // warp 11: g, beta of this and the next chunk
   if (warp == 11) {
-    const float dc0 = chunk_decay(gp, d.Hv, 0, T, lane);
+    load_gb(gp, bp, d.Hv, 0, T, lane, g_cur, b_cur);
+    const float dc0 = __expf(warp_sum(g_cur[0] + g_cur[1]));
     if (lane == 0) V.dC_next = dc0;
   }
   fence_before();
@@ -532,11 +528,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   for (int n = 0; n < nchunks; ++n) {
     const int t0 = n * kC;
-    // A0: chunk vectors; the next chunk's total decay
+    // A0: chunk vectors; the next chunk's g and beta requested
     if (warp == 11) {
-      chunk_vectors(V, gp + (long long)t0 * d.Hv, bp + (long long)t0 * d.Hv, d.Hv, T - t0, lane);
-      const float dcn = n + 1 < nchunks ? chunk_decay(gp, d.Hv, t0 + kC, T, lane) : 1.f;
-      if (lane == 0) V.dC_next = dcn;
+      chunk_vectors(V, g_cur, b_cur, lane);
+      if (n + 1 < nchunks) load_gb(gp, bp, d.Hv, t0 + kC, T, lane, g_nxt, b_nxt);
     }
     if (!wait_all(&V.bar_raw, phase_raw)) break;
     raw_pending = false;
@@ -552,11 +547,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // A: front end
     front_end(sm, V, d, conv_w, h, kh, t0, tid);
     smem_ready();
-    // B: MMA1  [K;Q] K^T
+    // B: MMA1  [K;Q] K^T;  MMA5 S Q^T (Q^ = rows 64..127 of [K;Q], S from TMEM)
     if (tid == 0) {
       fence_after();
       issue(tmem + TM_KQ, id_kk, 8, false, [&](int ks) { return desc_k(sbase + OFF_KQ, ks, 128); },
             [&](int ks) { return desc_k(sbase + OFF_KQ, ks, 128); });
+      issue_ta(tmem + TM_O1, tmem + TM_S16, id_kk, 8, false,
+               [&](int ks) { return desc_k(sbase + OFF_KQ + 64 * 128, ks, 128); });
       commit(&V.bar);
     }
     if (!wait_all(&V.bar, phase)) break;
@@ -622,6 +619,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (n + 1 < nchunks) raw_pending = true;
     if (!wait_all(&V.bar, phase)) break;
+    if (warp == 11) {  // the next chunk's total decay (its g arrived meanwhile)
+      const float dcn = n + 1 < nchunks ? __expf(warp_sum(g_nxt[0] + g_nxt[1])) : 1.f;
+      if (lane == 0) V.dC_next = dcn;
+    }
     // F: -W^T (lanes k, columns i) -> MN-major [k][i]
     if (warp < kTmemWarps) {
       float v[32];
@@ -632,12 +633,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int q = 0; q < 4; ++q) st_h8(sm + OFF_NW + mnmaj(32 * half + 8 * q, lrow, kD), v + 8 * q);
     }
     smem_ready();
-    // G: MMA4 Delta^T = U^T - S W^T;  MMA5 S Q^T (Q^ = rows 64..127 of [K;Q]); S from TMEM
+    // G: MMA4 Delta^T = U^T - S W^T (S from TMEM)
     if (tid == 0) {
       fence_after();
       issue_ta(tmem + TM_U, tmem + TM_S16, id_km, 8, true, [&](int ks) { return desc_mn(sbase + OFF_NW, ks, kD); });
-      issue_ta(tmem + TM_O1, tmem + TM_S16, id_kk, 8, false,
-               [&](int ks) { return desc_k(sbase + OFF_KQ + 64 * 128, ks, 128); });
       commit(&V.bar);
     }
     if (!wait_all(&V.bar, phase)) break;
@@ -727,6 +726,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (n + 1 < nchunks) {
       if (tid == 0) request_z(t0 + kC);
       z_pending = true;
+      if (warp == 11) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          g_cur[u] = g_nxt[u];
+          b_cur[u] = b_nxt[u];
+        }
+      }
     }
   }
 
