@@ -25,23 +25,24 @@ bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi && a.lo != a.
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct Sizes {
-  size_t io;     // bytes per io element
-  size_t qkv, zo, gb, S, conv, conv_w, norm_w;  // bytes of each tensor
+  size_t io;                                                     // bytes per io element
+  size_t qkv, zo, gb, gio, S, conv, conv_w, norm_w, head, snap;  // bytes of each tensor
 };
 
-gdn_status check_shape(const gdn_shape *sh, bool decode, gdn::Dims *d, Sizes *z) {
+// tokens: rows of the token-major tensors (B*T fixed length, T packed).
+gdn_status check_shape(const gdn_shape *sh, long long tokens, gdn::Dims *d, Sizes *z) {
   if (!sh) return GDN_ERR_INVALID_ARG;
   if (sh->B < 1 || sh->T < 1 || sh->Hk < 1 || sh->Hv < 1 || sh->Dk < 1 || sh->Dv < 1)
     return GDN_ERR_INVALID_ARG;
-  if (decode && sh->T != 1) return GDN_ERR_INVALID_ARG;
   if (sh->io_dtype != GDN_F32 && sh->io_dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
   if (!std::isfinite(sh->eps_l2) || sh->eps_l2 < 0.f || !std::isfinite(sh->eps_norm) ||
       sh->eps_norm < 0.f || !std::isfinite(sh->q_scale))
     return GDN_ERR_INVALID_ARG;
   if (sh->Dk != gdn::kDHead || sh->Dv != gdn::kDHead) return GDN_ERR_UNSUPPORTED_SHAPE;
   if (sh->Hv % sh->Hk != 0) return GDN_ERR_UNSUPPORTED_SHAPE;
-  // Limits that keep every size product inside 64 bits and the grid legal.
-  if (sh->Hk > 4096 || sh->Hv > 4096 || sh->B > 65536 || (long long)sh->B * sh->T > (1LL << 34))
+  // Limits that keep every size product inside 64 bits, the grid legal and
+  // token row indices (TMA coordinates) inside 31 bits.
+  if (sh->Hk > 4096 || sh->Hv > 4096 || sh->B > 65536 || tokens > (1LL << 30))
     return GDN_ERR_UNSUPPORTED_SHAPE;
   d->B = sh->B;
   d->T = sh->T;
@@ -51,15 +52,18 @@ gdn_status check_shape(const gdn_shape *sh, bool decode, gdn::Dims *d, Sizes *z)
   d->eps_l2 = sh->eps_l2;
   d->eps_norm = sh->eps_norm;
   d->q_scale = sh->q_scale != 0.f ? sh->q_scale : 1.0f / std::sqrt((float)gdn::kDHead);
-  const size_t BT = (size_t)sh->B * sh->T;
+  const size_t N = (size_t)tokens;
   z->io = sh->io_dtype == GDN_BF16 ? 2 : 4;
-  z->qkv = BT * (size_t)d->C * z->io;
-  z->zo = BT * (size_t)sh->Hv * gdn::kDHead * z->io;
-  z->gb = BT * (size_t)sh->Hv * sizeof(float);
+  z->qkv = N * (size_t)d->C * z->io;
+  z->zo = N * (size_t)sh->Hv * gdn::kDHead * z->io;
+  z->gb = N * (size_t)sh->Hv * sizeof(float);
+  z->gio = N * (size_t)sh->Hv * z->io;
   z->S = (size_t)sh->B * sh->Hv * gdn::kDHead * gdn::kDHead * sizeof(float);
   z->conv = (size_t)sh->B * 3 * (size_t)d->C * z->io;
   z->conv_w = (size_t)d->C * 4 * z->io;
   z->norm_w = (size_t)gdn::kDHead * z->io;
+  z->head = (size_t)sh->Hv * sizeof(float);
+  z->snap = N * (size_t)sh->Hv * gdn::kDHead * gdn::kDHead * sizeof(float);
   return GDN_OK;
 }
 
@@ -73,6 +77,145 @@ gdn_status check_device(unsigned int **err) {
   if (cudaGetSymbolAddress(reinterpret_cast<void **>(err), g_err_word) != cudaSuccess)
     return GDN_ERR_CUDA;
   return GDN_OK;
+}
+
+// The gate source: (g, beta) or the raw projections, never both.
+gdn_status gate_source(const float *g, const float *beta, const gdn_raw_gates *raw, gdn::GateSrc *out) {
+  if (raw) {
+    if (g || beta || !raw->a || !raw->b || !raw->A_log || !raw->dt_bias) return GDN_ERR_INVALID_ARG;
+    *out = gdn::GateSrc{nullptr, nullptr, raw->a, raw->b, raw->A_log, raw->dt_bias};
+  } else {
+    if (!g || !beta) return GDN_ERR_INVALID_ARG;
+    *out = gdn::GateSrc{g, beta, nullptr, nullptr, nullptr, nullptr};
+  }
+  return GDN_OK;
+}
+
+// The gate tensors of either source, as input ranges; returns how many.
+int gate_ranges(const gdn::GateSrc &gs, const Sizes &sz, Range *out) {
+  if (gs.g) {
+    out[0] = range_of(gs.g, sz.gb);
+    out[1] = range_of(gs.beta, sz.gb);
+    return 2;
+  }
+  out[0] = range_of(gs.a, sz.gio);
+  out[1] = range_of(gs.b, sz.gio);
+  out[2] = range_of(gs.A_log, sz.head);
+  out[3] = range_of(gs.dt_bias, sz.head);
+  return 4;
+}
+
+bool all_aligned(const void *const *ptrs, int n) {
+  for (int i = 0; i < n; ++i)
+    if (ptrs[i] && !aligned16(ptrs[i])) return false;
+  return true;
+}
+
+gdn_status prefill_impl(const gdn_shape *shape, const gdn_prefill_io *io, void *stream) {
+  if (!shape || !io) return GDN_ERR_INVALID_ARG;
+  if (shape->B < 1 || shape->T < 1) return GDN_ERR_INVALID_ARG;
+  const bool packed = io->cu_seqlens != nullptr;
+  const long long tokens = packed ? (long long)shape->T : (long long)shape->B * shape->T;
+  gdn::Dims d;
+  Sizes sz;
+  gdn_status st = check_shape(shape, tokens, &d, &sz);
+  if (st != GDN_OK) return st;
+  gdn::GateSrc gs;
+  st = gate_source(io->g, io->beta, io->raw_gates, &gs);
+  if (st != GDN_OK) return st;
+  if (!io->qkv_pre || !io->z || !io->conv_w || !io->norm_w || !io->o || !io->S_T || !io->conv_T)
+    return GDN_ERR_INVALID_ARG;
+  const void *ptrs[] = {io->qkv_pre, io->z,      gs.g,      gs.beta, gs.a,     gs.b,
+                        gs.A_log,    gs.dt_bias, io->conv_w, io->norm_w, io->S0, io->conv0,
+                        io->o,       io->S_T,    io->conv_T, io->cu_seqlens, io->S_snap};
+  if (!all_aligned(ptrs, 17)) return GDN_ERR_ALIGNMENT;
+  Range in[12];
+  int n = 0;
+  in[n++] = range_of(io->qkv_pre, sz.qkv);
+  in[n++] = range_of(io->z, sz.zo);
+  n += gate_ranges(gs, sz, in + n);
+  in[n++] = range_of(io->conv_w, sz.conv_w);
+  in[n++] = range_of(io->norm_w, sz.norm_w);
+  in[n++] = range_of(io->conv0, sz.conv);
+  in[n++] = range_of(io->cu_seqlens, ((size_t)shape->B + 1) * sizeof(int));
+  const int i_S0 = n;
+  in[n++] = range_of(io->S0, sz.S);
+  const Range ro = range_of(io->o, sz.zo), rs = range_of(io->S_T, sz.S), rc = range_of(io->conv_T, sz.conv),
+              rp = range_of(io->S_snap, sz.snap);
+  const bool in_place = io->S0 != nullptr && io->S0 == io->S_T;
+  for (int i = 0; i < n; ++i) {
+    if (overlap(ro, in[i]) || overlap(rc, in[i]) || overlap(rp, in[i])) return GDN_ERR_ALIAS;
+    if (i == i_S0 && in_place) continue;
+    if (overlap(rs, in[i])) return GDN_ERR_ALIAS;
+  }
+  if (overlap(ro, rs) || overlap(ro, rc) || overlap(rs, rc) || overlap(rp, ro) || overlap(rp, rs) ||
+      overlap(rp, rc))
+    return GDN_ERR_ALIAS;
+  unsigned int *err = nullptr;
+  st = check_device(&err);
+  if (st != GDN_OK) return st;
+
+  gdn::PrefillArgs a{d,         io->qkv_pre, io->z,   gs,         io->conv_w,     io->norm_w, io->S0,
+                     io->conv0, io->o,       io->S_T, io->conv_T, io->cu_seqlens, io->S_snap, err};
+  // bf16 io without snapshots: the chunked tensor-core kernel.  fp32 io (fp32
+  // arithmetic throughout) and per-token snapshots: the token-serial kernel.
+  const bool bf16 = shape->io_dtype == GDN_BF16;
+  cudaError_t e = (bf16 && !io->S_snap) ? gdn::launch_prefill_chunked(a, true, (cudaStream_t)stream)
+                                        : gdn::launch_prefill(a, bf16, (cudaStream_t)stream);
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+gdn_status decode_impl(const gdn_shape *shape, const gdn_decode_io *io, void *stream) {
+  if (!shape || !io) return GDN_ERR_INVALID_ARG;
+  if (shape->B < 1 || shape->T < 1) return GDN_ERR_INVALID_ARG;
+  const long long tokens = (long long)shape->B * shape->T;
+  gdn::Dims d;
+  Sizes sz;
+  gdn_status st = check_shape(shape, tokens, &d, &sz);
+  if (st != GDN_OK) return st;
+  gdn::GateSrc gs;
+  st = gate_source(io->g, io->beta, io->raw_gates, &gs);
+  if (st != GDN_OK) return st;
+  if (!io->qkv_pre || !io->z || !io->conv_w || !io->norm_w || !io->S || !io->conv_in || !io->conv_out ||
+      !io->o)
+    return GDN_ERR_INVALID_ARG;
+  const void *ptrs[] = {io->qkv_pre, io->z,        gs.g,       gs.beta,    gs.a,  gs.b,
+                        gs.A_log,    gs.dt_bias,   io->conv_w, io->norm_w, io->S, io->S_snap,
+                        io->conv_in, io->conv_out, io->o};
+  if (!all_aligned(ptrs, 15)) return GDN_ERR_ALIGNMENT;
+  Range in[10];
+  int n = 0;
+  in[n++] = range_of(io->qkv_pre, sz.qkv);
+  in[n++] = range_of(io->z, sz.zo);
+  n += gate_ranges(gs, sz, in + n);
+  in[n++] = range_of(io->conv_w, sz.conv_w);
+  in[n++] = range_of(io->norm_w, sz.norm_w);
+  in[n++] = range_of(io->conv_in, sz.conv);
+  const Range rS = range_of(io->S, sz.S), ro = range_of(io->o, sz.zo), rc = range_of(io->conv_out, sz.conv),
+              rp = range_of(io->S_snap, sz.snap);
+  for (int i = 0; i < n; ++i)
+    if (overlap(rS, in[i]) || overlap(ro, in[i]) || overlap(rc, in[i]) || overlap(rp, in[i]))
+      return GDN_ERR_ALIAS;
+  if (overlap(rS, ro) || overlap(rS, rc) || overlap(ro, rc) || overlap(rp, rS) || overlap(rp, ro) ||
+      overlap(rp, rc))
+    return GDN_ERR_ALIAS;
+  unsigned int *err = nullptr;
+  st = check_device(&err);
+  if (st != GDN_OK) return st;
+
+  const bool bf16 = shape->io_dtype == GDN_BF16;
+  cudaError_t e;
+  if (shape->T == 1 && !io->S_snap) {
+    gdn::DecodeArgs a{d, io->qkv_pre, io->z, gs, io->conv_w, io->norm_w, io->S, io->conv_in, io->conv_out,
+                      io->o, err};
+    e = gdn::launch_decode(a, bf16, (cudaStream_t)stream);
+  } else {
+    // T tokens from the cache = a T-token prefill with the state in place.
+    gdn::PrefillArgs a{d,     io->qkv_pre, io->z,        gs,      io->conv_w, io->norm_w, io->S, io->conv_in,
+                       io->o, io->S,       io->conv_out, nullptr, io->S_snap, err};
+    e = gdn::launch_prefill(a, bf16, (cudaStream_t)stream);
+  }
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
 }  // namespace
@@ -99,64 +242,35 @@ gdn_status gdn_prefill(const gdn_shape *shape, const void *qkv_pre, const void *
                        const float *g, const float *beta, const void *conv_w,
                        const void *norm_w, const float *S0, const void *conv0, void *o,
                        float *S_T, void *conv_T, void *stream) {
-  gdn::Dims d;
-  Sizes sz;
-  gdn_status st = check_shape(shape, false, &d, &sz);
-  if (st != GDN_OK) return st;
-  if (!qkv_pre || !z || !g || !beta || !conv_w || !norm_w || !o || !S_T || !conv_T)
-    return GDN_ERR_INVALID_ARG;
-  const void *ptrs[] = {qkv_pre, z, g, beta, conv_w, norm_w, S0, conv0, o, S_T, conv_T};
-  for (const void *p : ptrs)
-    if (p && !aligned16(p)) return GDN_ERR_ALIGNMENT;
-  const Range in[] = {range_of(qkv_pre, sz.qkv), range_of(z, sz.zo),   range_of(g, sz.gb),
-                      range_of(beta, sz.gb),     range_of(conv_w, sz.conv_w),
-                      range_of(norm_w, sz.norm_w), range_of(S0, sz.S), range_of(conv0, sz.conv)};
-  const Range ro = range_of(o, sz.zo), rs = range_of(S_T, sz.S), rc = range_of(conv_T, sz.conv);
-  const bool in_place = S0 != nullptr && S0 == S_T;
-  for (int i = 0; i < 8; ++i) {
-    if (overlap(ro, in[i]) || overlap(rc, in[i])) return GDN_ERR_ALIAS;
-    if (i == 6 && in_place) continue;
-    if (overlap(rs, in[i])) return GDN_ERR_ALIAS;
-  }
-  if (overlap(ro, rs) || overlap(ro, rc) || overlap(rs, rc)) return GDN_ERR_ALIAS;
-  unsigned int *err = nullptr;
-  st = check_device(&err);
-  if (st != GDN_OK) return st;
+  if (!g || !beta) return GDN_ERR_INVALID_ARG;
+  const gdn_prefill_io io{qkv_pre, z,  g,    beta,   nullptr, conv_w,  norm_w,
+                          S0,      conv0, o, S_T, conv_T, nullptr, nullptr};
+  return prefill_impl(shape, &io, stream);
+}
 
-  gdn::PrefillArgs a{d, qkv_pre, z, g, beta, conv_w, norm_w, S0, conv0, o, S_T, conv_T, err};
-  // bf16 io: the chunked tensor-core kernel; fp32 io: the exact token-serial kernel.
-  const bool bf16 = shape->io_dtype == GDN_BF16;
-  cudaError_t e = bf16 ? gdn::launch_prefill_chunked(a, true, (cudaStream_t)stream)
-                       : gdn::launch_prefill(a, false, (cudaStream_t)stream);
-  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+gdn_status gdn_prefill_ex(const gdn_shape *shape, const gdn_prefill_io *io, void *stream) {
+  return prefill_impl(shape, io, stream);
 }
 
 gdn_status gdn_decode_step(const gdn_shape *shape, const void *qkv_pre, const void *z,
                            const float *g, const float *beta, const void *conv_w,
                            const void *norm_w, float *S, const void *conv_in, void *conv_out,
                            void *o, void *stream) {
-  gdn::Dims d;
-  Sizes sz;
-  gdn_status st = check_shape(shape, true, &d, &sz);
-  if (st != GDN_OK) return st;
-  if (!qkv_pre || !z || !g || !beta || !conv_w || !norm_w || !S || !conv_in || !conv_out || !o)
-    return GDN_ERR_INVALID_ARG;
-  const void *ptrs[] = {qkv_pre, z, g, beta, conv_w, norm_w, S, conv_in, conv_out, o};
-  for (const void *p : ptrs)
-    if (!aligned16(p)) return GDN_ERR_ALIGNMENT;
-  const Range in[] = {range_of(qkv_pre, sz.qkv), range_of(z, sz.zo), range_of(g, sz.gb),
-                      range_of(beta, sz.gb),     range_of(conv_w, sz.conv_w),
-                      range_of(norm_w, sz.norm_w), range_of(conv_in, sz.conv)};
-  const Range rS = range_of(S, sz.S), ro = range_of(o, sz.zo), rc = range_of(conv_out, sz.conv);
-  for (const Range &r : in)
-    if (overlap(rS, r) || overlap(ro, r) || overlap(rc, r)) return GDN_ERR_ALIAS;
-  if (overlap(rS, ro) || overlap(rS, rc) || overlap(ro, rc)) return GDN_ERR_ALIAS;
-  unsigned int *err = nullptr;
-  st = check_device(&err);
-  if (st != GDN_OK) return st;
+  if (!shape || shape->T != 1 || !g || !beta) return GDN_ERR_INVALID_ARG;
+  const gdn_decode_io io{qkv_pre, z, g, beta, nullptr, conv_w, norm_w, S, nullptr, conv_in, conv_out, o};
+  return decode_impl(shape, &io, stream);
+}
 
-  gdn::DecodeArgs a{d, qkv_pre, z, g, beta, conv_w, norm_w, S, conv_in, conv_out, o, err};
-  cudaError_t e = gdn::launch_decode(a, shape->io_dtype == GDN_BF16, (cudaStream_t)stream);
+gdn_status gdn_decode_ex(const gdn_shape *shape, const gdn_decode_io *io, void *stream) {
+  return decode_impl(shape, io, stream);
+}
+
+gdn_status gdn_selftest_wait_timeout(int wait_us, void *stream) {
+  if (wait_us < 1 || wait_us > 1000000) return GDN_ERR_INVALID_ARG;
+  unsigned int *err = nullptr;
+  gdn_status st = check_device(&err);
+  if (st != GDN_OK) return st;
+  cudaError_t e = gdn::launch_wait_selftest(err, 1000ull * (unsigned long long)wait_us, (cudaStream_t)stream);
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
@@ -174,7 +288,9 @@ gdn_status gdn_device_status(void *stream, int reset) {
         cudaStreamSynchronize(s) != cudaSuccess)
       return GDN_ERR_CUDA;
   }
-  return (word & gdn::kErrTimeout) ? GDN_ERR_TIMEOUT : GDN_OK;
+  if (word & gdn::kErrTimeout) return GDN_ERR_TIMEOUT;
+  if (word & gdn::kErrSeqlens) return GDN_ERR_INVALID_ARG;
+  return GDN_OK;
 }
 
 }  // extern "C"

@@ -42,7 +42,7 @@ __device__ __forceinline__ float conv_token(const IO *win, const IO *x, const IO
   return silu(acc);
 }
 
-template <typename IO>
+template <typename IO, bool kRawGates>
 __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
   const Dims d = a.d;
   const int unit = blockIdx.x;
@@ -96,8 +96,14 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
 
   // ---- state pass: each warp streams its 16 rows once
   const long long gi = (long long)b * d.Hv + h;
-  const float alpha = expf(a.g[gi]);
-  const float beta = a.beta[gi];
+  float gt, beta;
+  if (kRawGates) {
+    gate_at<IO>(a.gate, gi, h, gt, beta);
+  } else {
+    gt = a.gate.g[gi];
+    beta = a.gate.beta[gi];
+  }
+  const float alpha = expf(gt);
   const float kq = s_kq;
   const float4 k4 = reinterpret_cast<const float4 *>(s_k)[lane];
   const float4 q4 = reinterpret_cast<const float4 *>(s_q)[lane];
@@ -154,10 +160,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
 
 cudaError_t launch_decode(const DecodeArgs &a, bool bf16, cudaStream_t s) {
   dim3 grid((unsigned)(a.d.B * a.d.Hv)), block(kThreads);
+  const bool raw = a.gate.g == nullptr;
   if (bf16)
-    decode_kernel<__nv_bfloat16><<<grid, block, 0, s>>>(a);
+    (raw ? decode_kernel<__nv_bfloat16, true> : decode_kernel<__nv_bfloat16, false>)<<<grid, block, 0, s>>>(a);
   else
-    decode_kernel<float><<<grid, block, 0, s>>>(a);
+    (raw ? decode_kernel<float, true> : decode_kernel<float, false>)<<<grid, block, 0, s>>>(a);
   return cudaGetLastError();
 }
 

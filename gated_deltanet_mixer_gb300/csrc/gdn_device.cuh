@@ -36,6 +36,22 @@ __device__ __forceinline__ void st_io4(__nv_bfloat16 *p, float4 v) {
   *reinterpret_cast<uint2 *>(p) = u;
 }
 
+// The write gate and log decay of element i (head h) of a [token][Hv] gate
+// tensor: given, or from the raw projections ("How Qwen3.5 works" section
+// 9.5: beta = sigmoid(b), g = -exp(A_log) softplus(a + dt_bias), in fp32).
+template <typename IO, typename Src>
+__device__ __forceinline__ void gate_at(const Src &s, long long i, int h, float &g, float &beta) {
+  if (s.g) {
+    g = s.g[i];
+    beta = s.beta[i];
+  } else {
+    const float x = ld_io(static_cast<const IO *>(s.a) + i) + s.dt_bias[h];
+    const float sp = fmaxf(x, 0.f) + log1pf(expf(-fabsf(x)));  // softplus without overflow
+    g = -expf(s.A_log[h]) * sp;
+    beta = 1.0f / (1.0f + expf(-ld_io(static_cast<const IO *>(s.b) + i)));
+  }
+}
+
 // silu(x) = x * sigmoid(x)
 __device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
 

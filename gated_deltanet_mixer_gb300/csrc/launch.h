@@ -15,23 +15,37 @@ struct Dims {
   float eps_l2, eps_norm, q_scale;
 };
 
+// Where a token's gates come from: g and beta given, or (g == nullptr) the
+// raw projections a, b (io dtype, same [token][Hv] layout) with the per-head
+// parameters A_log, dt_bias [Hv].
+struct GateSrc {
+  const float *g, *beta;
+  const void *a, *b;
+  const float *A_log, *dt_bias;
+};
+
+// Fixed length: sequence b owns tokens b*T .. b*T + T - 1 of the token-major
+// tensors.  Packed (cu_seqlens != nullptr): sequence b owns tokens
+// cu_seqlens[b] .. cu_seqlens[b+1] - 1 and d.T is the total token count.
 struct PrefillArgs {
   Dims d;
   const void *qkv_pre, *z;
-  const float *g, *beta;
+  GateSrc gate;
   const void *conv_w, *norm_w;
   const float *S0;      // may be null (zeros)
   const void *conv0;    // may be null (zeros)
   void *o;
   float *S_T;
   void *conv_T;
-  unsigned int *err;    // device error word
+  const int *cu_seqlens;  // may be null (fixed length)
+  float *S_snap;          // may be null: the state after every token, [token][Hv][128][128]
+  unsigned int *err;      // device error word
 };
 
 struct DecodeArgs {
   Dims d;               // d.T == 1
   const void *qkv_pre, *z;
-  const float *g, *beta;
+  GateSrc gate;
   const void *conv_w, *norm_w;
   float *S;
   const void *conv_in;
@@ -44,8 +58,10 @@ struct DecodeArgs {
 cudaError_t launch_decode(const DecodeArgs &a, bool bf16, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillArgs &a, bool bf16, cudaStream_t s);          // token-serial
 cudaError_t launch_prefill_chunked(const PrefillArgs &a, bool bf16, cudaStream_t s);  // chunked WY, tcgen05
+cudaError_t launch_wait_selftest(unsigned int *err, unsigned long long limit_ns, cudaStream_t s);
 
 // Device error bits (the error word is OR-ed).
-constexpr unsigned int kErrTimeout = 1u;
+constexpr unsigned int kErrTimeout = 1u;  // a bounded wait gave up
+constexpr unsigned int kErrSeqlens = 2u;  // packed-sequence offsets out of order or range
 
 }  // namespace gdn

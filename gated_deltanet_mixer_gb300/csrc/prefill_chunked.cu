@@ -136,15 +136,28 @@ __device__ __forceinline__ float2 silu2(float2 x) {
 __device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
 
 // g and beta of the chunk starting at t0 (one warp: tokens lane, lane + 32),
-// loaded a chunk ahead of use.  Padded tokens get g = 0, beta = 0; g is
-// clamped at kGMin.
-__device__ __forceinline__ void load_gb(const float *g, const float *beta, long long gstride, int t0,
-                                        int T, int lane, float (&gv)[2], float (&bv)[2]) {
+// loaded a chunk ahead of use; gate element of token t is (bos + t) Hv + h.
+// Padded tokens get g = 0, beta = 0; g is clamped at kGMin.
+template <bool kRaw>
+__device__ __forceinline__ void load_gb(const GateSrc &gs, long long bos, int Hv, int h, int t0, int T,
+                                        int lane, float (&gv)[2], float (&bv)[2]) {
 #pragma unroll
   for (int u = 0; u < 2; ++u) {
     const int t = t0 + lane + 32 * u;
-    gv[u] = t < T ? fmaxf(g[(long long)t * gstride], kGMin) : 0.f;
-    bv[u] = t < T ? beta[(long long)t * gstride] : 0.f;
+    gv[u] = 0.f;
+    bv[u] = 0.f;
+    if (t < T) {
+      const long long i = (bos + t) * Hv + h;
+      if (kRaw) {
+        GateSrc raw = gs;
+        raw.g = nullptr;
+        gate_at<__nv_bfloat16>(raw, i, h, gv[u], bv[u]);
+      } else {
+        gv[u] = gs.g[i];
+        bv[u] = gs.beta[i];
+      }
+      gv[u] = fmaxf(gv[u], kGMin);
+    }
   }
 }
 
@@ -221,7 +234,7 @@ __device__ __forceinline__ void st_h8_split_pairs(uint8_t *phi, uint8_t *plo, co
 // what differs per block (norm, outputs) is warp-uniform data.
 // Writes: q^ and k^ (fp16) into [K;Q]; Gamma k^ (hi, lo); v (hi, lo).
 __device__ void front_end(uint8_t *sm, const Vecs &V, const Dims &d, const bf16 *conv_w,
-                          int h, int kh, int t0, int tid) {
+                          int h, int kh, int t0, int T, int tid) {
   const int warp = tid >> 5, lane = tid & 31;
   const int blk = warp >> 2, eighth = 2 * (warp & 3) + (lane >> 4), grp = lane & 15;
   const long long c = blk == 0   ? (long long)kh * kD + 8 * grp
@@ -267,7 +280,7 @@ __device__ void front_end(uint8_t *sm, const Vecs &V, const Dims &d, const bf16 
       x1[i] = x2[i];
       x2[i] = x3[i];
     }
-    if (t >= d.T) {  // padding beyond the sequence
+    if (t >= T) {  // padding beyond the sequence
 #pragma unroll
       for (int i = 0; i < 4; ++i) u[i] = make_float2(0.f, 0.f);
       ss2 = make_float2(0.f, 0.f);
@@ -414,6 +427,7 @@ __device__ __forceinline__ void pack_h16(const float (&v)[32], uint32_t (&w)[16]
   }
 }
 
+template <bool kRawGates>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_chunked_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tm_qkv,
                            const __grid_constant__ CUtensorMap tm_z) {
@@ -425,27 +439,65 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = unit / d.Hv, h = unit % d.Hv;
   const int r = d.Hv / d.Hk, kh = h / r;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int T = d.T;
   const long long C = d.C;
-  const bf16 *x = static_cast<const bf16 *>(a.qkv_pre) + (long long)b * T * C;
+  // This sequence's tokens: rows bos .. bos + T - 1 of the token-major tensors.
+  long long bos;
+  int T;
+  if (a.cu_seqlens) {
+    const int lo = a.cu_seqlens[b], hi = a.cu_seqlens[b + 1];
+    if (lo < 0 || hi < lo || hi > d.T) {  // unusable offsets: leave this sequence untouched
+      if (tid == 0) atomicOr(a.err, kErrSeqlens);
+      return;
+    }
+    bos = lo;
+    T = hi - lo;
+  } else {
+    bos = (long long)b * d.T;
+    T = d.T;
+  }
+  const bf16 *x = static_cast<const bf16 *>(a.qkv_pre) + bos * C;
   const bf16 *conv0 = a.conv0 ? static_cast<const bf16 *>(a.conv0) + (long long)b * 3 * C : nullptr;
   const bf16 *conv_w = static_cast<const bf16 *>(a.conv_w);
-  const float *gp = a.g + (long long)b * T * d.Hv + h;
-  const float *bp = a.beta + (long long)b * T * d.Hv + h;
   const long long unit_off = ((long long)b * d.Hv + h) * kD * kD;
   const uint32_t sbase = smem_u32(sm);
   const int cq = kh * kD, ck = d.Hk * kD + kh * kD, cv = 2 * d.Hk * kD + h * kD;
 
   auto request_raw = [&](int t0) {  // one thread: the raw rows t0-3 .. t0+63 of q, k, v
     bar_expect_tx(&V.bar_raw, 3 * kRawBlock);
-    tma_load_3d(sbase + OFF_RAW + 0 * kRawBlock, &tm_qkv, cq, t0 - 3, b, &V.bar_raw);
-    tma_load_3d(sbase + OFF_RAW + 1 * kRawBlock, &tm_qkv, ck, t0 - 3, b, &V.bar_raw);
-    tma_load_3d(sbase + OFF_RAW + 2 * kRawBlock, &tm_qkv, cv, t0 - 3, b, &V.bar_raw);
+    const int row = (int)(bos + t0 - 3);
+    tma_load_3d(sbase + OFF_RAW + 0 * kRawBlock, &tm_qkv, cq, row, 0, &V.bar_raw);
+    tma_load_3d(sbase + OFF_RAW + 1 * kRawBlock, &tm_qkv, ck, row, 0, &V.bar_raw);
+    tma_load_3d(sbase + OFF_RAW + 2 * kRawBlock, &tm_qkv, cv, row, 0, &V.bar_raw);
   };
   auto request_z = [&](int t0) {  // one thread: the z rows t0 .. t0+63 of head h
     bar_expect_tx(&V.bar_z, kC * kD * 2);
-    tma_load_3d(sbase + OFF_Z, &tm_z, h * kD, t0, b, &V.bar_z);
+    tma_load_3d(sbase + OFF_Z, &tm_z, h * kD, (int)(bos + t0), 0, &V.bar_z);
   };
+
+  // Carried conv window: the last three raw rows of the channels this CTA owns.
+  auto write_conv_T = [&]() {
+    bf16 *cT = static_cast<bf16 *>(a.conv_T) + (long long)b * 3 * C;
+    const bool own_qk = (h % r) == 0;
+    for (int idx = tid; idx < 3 * 3 * kD; idx += kThreads) {
+      const int e = idx / (3 * kD), rem = idx % (3 * kD), blk = rem / kD, ch = rem % kD;
+      if (blk < 2 && !own_qk) continue;
+      const long long c = (blk == 0 ? cq : blk == 1 ? ck : cv) + ch;
+      const int t = T - 3 + e;
+      bf16 val;
+      if (t >= 0) val = x[(long long)t * C + c];
+      else if (conv0) val = conv0[(long long)(3 + t) * C + c];
+      else val = bf16(0.f);
+      cT[(long long)e * C + c] = val;
+    }
+  };
+  if (T == 0) {  // an empty packed sequence: state and window pass through
+    float4 *dst = reinterpret_cast<float4 *>(a.S_T + unit_off);
+    const float4 *src = a.S0 ? reinterpret_cast<const float4 *>(a.S0 + unit_off) : nullptr;
+    if (src != dst)
+      for (int i = tid; i < kD * kD / 4; i += kThreads) dst[i] = src ? src[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    write_conv_T();
+    return;
+  }
 
   if (tid == 0) {
     bar_init(&V.bar, 1);
@@ -456,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) tmem_alloc(&V.tmem, kTmemCols);
   float g_cur[2], b_cur[2], g_nxt[2], b_nxt[2];  // warp 11: g, beta of this and the next chunk
   if (warp == 11) {
-    load_gb(gp, bp, d.Hv, 0, T, lane, g_cur, b_cur);
+    load_gb<kRawGates>(a.gate, bos, d.Hv, h, 0, T, lane, g_cur, b_cur);
     const float dc0 = __expf(warp_sum(g_cur[0] + g_cur[1]));
     if (lane == 0) V.dC_next = dc0;
   }
@@ -531,21 +583,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     // A0: chunk vectors; the next chunk's g and beta requested
     if (warp == 11) {
       chunk_vectors(V, g_cur, b_cur, lane);
-      if (n + 1 < nchunks) load_gb(gp, bp, d.Hv, t0 + kC, T, lane, g_nxt, b_nxt);
+      if (n + 1 < nchunks) load_gb<kRawGates>(a.gate, bos, d.Hv, h, t0 + kC, T, lane, g_nxt, b_nxt);
     }
     if (!wait_all(&V.bar_raw, phase_raw)) break;
     raw_pending = false;
-    if (n == 0 && conv0) {  // rows before the first token come from the carried window
+    if (n == 0) {  // rows before the first token: the carried window, or zeros
       for (int idx = tid; idx < 3 * 3 * 16; idx += kThreads) {
         const int blk = idx / 48, rw = (idx / 16) % 3, g8 = idx % 16;
         const int cc = blk == 0 ? cq : blk == 1 ? ck : cv;
         *reinterpret_cast<uint4 *>(sm + OFF_RAW + blk * kRawBlock + 256 * rw + 16 * g8) =
-            *reinterpret_cast<const uint4 *>(conv0 + (long long)rw * C + cc + 8 * g8);
+            conv0 ? *reinterpret_cast<const uint4 *>(conv0 + (long long)rw * C + cc + 8 * g8)
+                  : make_uint4(0u, 0u, 0u, 0u);
       }
       __syncthreads();
     }
     // A: front end
-    front_end(sm, V, d, conv_w, h, kh, t0, tid);
+    front_end(sm, V, d, conv_w, h, kh, t0, T, tid);
     smem_ready();
     // B: MMA1  [K;Q] K^T;  MMA5 S Q^T (Q^ = rows 64..127 of [K;Q], S from TMEM)
     if (tid == 0) {
@@ -705,7 +758,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float *ost = reinterpret_cast<const float *>(sm + OFF_OST);
       const float4 w4 = ld_io4(static_cast<const bf16 *>(a.norm_w) + 4 * lane);
       const int nv = min(kC, T - t0);
-      bf16 *ob = static_cast<bf16 *>(a.o) + (((long long)b * T + t0) * d.Hv + h) * kD + 4 * lane;
+      bf16 *ob = static_cast<bf16 *>(a.o) + ((bos + t0) * d.Hv + h) * kD + 4 * lane;
       const long long ostride = (long long)d.Hv * kD;
 #pragma unroll 2
       for (int i = warp; i < nv; i += kThreads / 32) {
@@ -736,22 +789,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  // Carried conv window: the last three raw rows of the channels this CTA owns.
-  {
-    bf16 *cT = static_cast<bf16 *>(a.conv_T) + (long long)b * 3 * C;
-    const bool own_qk = (h % r) == 0;
-    for (int idx = tid; idx < 3 * 3 * kD; idx += kThreads) {
-      const int e = idx / (3 * kD), rem = idx % (3 * kD), blk = rem / kD, ch = rem % kD;
-      if (blk < 2 && !own_qk) continue;
-      const long long c = (blk == 0 ? cq : blk == 1 ? ck : cv) + ch;
-      const int t = T - 3 + e;
-      bf16 val;
-      if (t >= 0) val = x[(long long)t * C + c];
-      else if (conv0) val = conv0[(long long)(3 + t) * C + c];
-      else val = bf16(0.f);
-      cT[(long long)e * C + c] = val;
-    }
-  }
+  write_conv_T();
   // After an early exit, no requested copy may still be landing in shared
   // memory when the CTA ends: wait (bounded) for any that was not consumed.
   if (tid == 0) {
@@ -784,7 +822,7 @@ EncodeTiled encoder() {
 }
 
 // A [B][T][width] bf16 tensor as a 3-d map with boxes of 128 columns x `rows` rows.
-bool encode_rows(CUtensorMap *m, const void *base, long long width, int T, int B, int rows) {
+bool encode_rows(CUtensorMap *m, const void *base, long long width, long long T, int B, int rows) {
   EncodeTiled enc = encoder();
   if (!enc) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)T, (cuuint64_t)B};
@@ -801,13 +839,18 @@ bool encode_rows(CUtensorMap *m, const void *base, long long width, int T, int B
 cudaError_t launch_prefill_chunked(const PrefillArgs &a, bool bf16_io, cudaStream_t s) {
   if (!bf16_io) return cudaErrorInvalidValue;  // the chunked kernel stages bf16 rows
   CUtensorMap tm_qkv, tm_z;
-  if (!encode_rows(&tm_qkv, a.qkv_pre, a.d.C, a.d.T, a.d.B, kRawRows) ||
-      !encode_rows(&tm_z, a.z, (long long)a.d.Hv * kD, a.d.T, a.d.B, kC))
+  // The token-major tensors as one run of rows; each CTA addresses its own
+  // sequence's rows (fixed length or packed) and masks the rows past its end.
+  const long long rows = a.cu_seqlens ? (long long)a.d.T : (long long)a.d.B * a.d.T;
+  if (!encode_rows(&tm_qkv, a.qkv_pre, a.d.C, rows, 1, kRawRows) ||
+      !encode_rows(&tm_z, a.z, (long long)a.d.Hv * kD, rows, 1, kC))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(prefill_chunked_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kSmemBytes);
+  const dim3 grid((unsigned)(a.d.B * a.d.Hv)), block(kThreads);
+  const bool raw = a.gate.g == nullptr;
+  auto kern = raw ? prefill_chunked_kernel<true> : prefill_chunked_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  prefill_chunked_kernel<<<dim3((unsigned)(a.d.B * a.d.Hv)), dim3(kThreads), kSmemBytes, s>>>(a, tm_qkv, tm_z);
+  kern<<<grid, block, kSmemBytes, s>>>(a, tm_qkv, tm_z);
   return cudaGetLastError();
 }
 

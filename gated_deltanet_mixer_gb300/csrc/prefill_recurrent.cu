@@ -9,6 +9,9 @@
 //   2. L2 norms of q and k per token (one warp per token),
 //   3. the serial gated delta rule over the block's tokens,
 //   4. the per-head gated RMSNorm of the block's outputs (node gdn.norm).
+// It also serves packed variable-length batches, raw gate projections and
+// per-token state snapshots (each warp stores its rows after every token),
+// and T-token decoding from the cache (S0 == S_T).
 #include "gdn_device.cuh"
 #include "launch.h"
 
@@ -62,7 +65,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_recurrent_kernel(PrefillA
   const int r = d.Hv / d.Hk, kh = h / r;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const long long C = d.C;
-  const int T = d.T;
+  // This sequence's tokens: rows bos .. bos + T - 1 of the token-major tensors.
+  long long bos;
+  int T;
+  if (a.cu_seqlens) {
+    const int lo = a.cu_seqlens[b], hi = a.cu_seqlens[b + 1];
+    if (lo < 0 || hi < lo || hi > d.T) {  // unusable offsets: leave this sequence untouched
+      if (tid == 0) atomicOr(a.err, kErrSeqlens);
+      return;
+    }
+    bos = lo;
+    T = hi - lo;
+  } else {
+    bos = (long long)b * d.T;
+    T = d.T;
+  }
 
   extern __shared__ __align__(16) float smem[];
   float *s_q = smem;              // [kTB][128] normalised, scaled query
@@ -73,7 +90,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_recurrent_kernel(PrefillA
   float *s_beta = s_alpha + kTB;
   float *s_kq = s_beta + kTB;
 
-  const IO *x = static_cast<const IO *>(a.qkv_pre) + (long long)b * T * C;
+  const IO *x = static_cast<const IO *>(a.qkv_pre) + bos * C;
   const IO *cw = static_cast<const IO *>(a.conv_w);
   const IO *conv0 = a.conv0 ? static_cast<const IO *>(a.conv0) + (long long)b * 3 * C : nullptr;
 
@@ -120,9 +137,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_recurrent_kernel(PrefillA
       }
     }
     if (tid < nt) {
-      const long long gi = ((long long)b * T + t0 + tid) * d.Hv + h;
-      s_alpha[tid] = expf(a.g[gi]);
-      s_beta[tid] = a.beta[gi];
+      float gt, bt;
+      gate_at<IO>(a.gate, (bos + t0 + tid) * d.Hv + h, h, gt, bt);
+      s_alpha[tid] = expf(gt);
+      s_beta[tid] = bt;
     }
     __syncthreads();
     // 2. L2 norms
@@ -164,6 +182,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_recurrent_kernel(PrefillA
         s[i].z = fmaf(alpha, s[i].z, di * k4.z);
         s[i].w = fmaf(alpha, s[i].w, di * k4.w);
       }
+      if (a.S_snap) {
+        float *snap = a.S_snap + ((bos + t0 + tt) * d.Hv + h) * (kD * kD);
+#pragma unroll
+        for (int i = 0; i < kRowsPerWarp; ++i) st_stream(snap + (row0 + i) * kD + 4 * lane, s[i]);
+      }
     }
     __syncthreads();
     // 4. gated RMSNorm, one warp per token
@@ -171,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_recurrent_kernel(PrefillA
     for (int tt = warp; tt < nt; tt += kWarps) {
       const float4 o4 = reinterpret_cast<const float4 *>(s_o + tt * kD)[lane];
       const float rstd = rsqrtf(warp_sum(dot4(o4, o4)) * (1.0f / kD) + d.eps_norm);
-      const long long oi = (((long long)b * T + t0 + tt) * d.Hv + h) * kD + 4 * lane;
+      const long long oi = ((bos + t0 + tt) * d.Hv + h) * kD + 4 * lane;
       const float4 z4 = ld_io4(static_cast<const IO *>(a.z) + oi);
       float4 y;
       y.x = w4.x * (o4.x * rstd) * silu(z4.x);

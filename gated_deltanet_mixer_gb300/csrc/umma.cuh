@@ -107,13 +107,15 @@ __device__ __forceinline__ uint64_t global_ns() {
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
   return t;
 }
-// Bounded wait for phase `parity`: false if it has not completed within about
-// one second (the work it waits for takes microseconds).
-__device__ __forceinline__ bool bar_wait(uint64_t *bar, uint32_t parity) {
+// Bounded wait for phase `parity`: false if it has not completed within
+// `limit_ns` (default about one second; the work it waits for takes
+// microseconds).
+__device__ __forceinline__ bool bar_wait(uint64_t *bar, uint32_t parity,
+                                         uint64_t limit_ns = 1000000000ull) {
   if (bar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   while (!bar_try_wait(bar, parity))
-    if (global_ns() - t0 > 1000000000ull) return false;
+    if (global_ns() - t0 > limit_ns) return false;
   return true;
 }
 // Arrive on `bar` announcing `bytes` of asynchronous copies to complete on it.

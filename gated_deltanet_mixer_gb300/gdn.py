@@ -14,6 +14,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libgdn.so")
 
 GDN_OK = 0
+GDN_ERR_INVALID_ARG = 1
+GDN_ERR_TIMEOUT = 6
 STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED_SHAPE",
                 3: "GDN_ERR_ALIGNMENT", 4: "GDN_ERR_ALIAS", 5: "GDN_ERR_CUDA",
                 6: "GDN_ERR_TIMEOUT", 7: "GDN_ERR_NO_DEVICE"}
@@ -32,6 +34,23 @@ class gdn_shape(ctypes.Structure):
                 ("Hv", ctypes.c_int), ("Dk", ctypes.c_int), ("Dv", ctypes.c_int),
                 ("io_dtype", ctypes.c_int), ("eps_l2", ctypes.c_float),
                 ("eps_norm", ctypes.c_float), ("q_scale", ctypes.c_float)]
+
+
+vp = ctypes.c_void_p
+
+
+class gdn_raw_gates(ctypes.Structure):
+    _fields_ = [("a", vp), ("b", vp), ("A_log", vp), ("dt_bias", vp)]
+
+
+class gdn_prefill_io(ctypes.Structure):
+    _fields_ = [(n, vp) for n in ("qkv_pre", "z", "g", "beta", "raw_gates", "conv_w", "norm_w", "S0",
+                                  "conv0", "o", "S_T", "conv_T", "cu_seqlens", "S_snap")]
+
+
+class gdn_decode_io(ctypes.Structure):
+    _fields_ = [(n, vp) for n in ("qkv_pre", "z", "g", "beta", "raw_gates", "conv_w", "norm_w", "S",
+                                  "S_snap", "conv_in", "conv_out", "o")]
 
 
 _lib = None
@@ -56,6 +75,12 @@ def lib():
         L.gdn_decode_step.argtypes = [ctypes.POINTER(gdn_shape)] + [vp] * 11
         L.gdn_device_status.restype = ctypes.c_int
         L.gdn_device_status.argtypes = [vp, ctypes.c_int]
+        L.gdn_prefill_ex.restype = ctypes.c_int
+        L.gdn_prefill_ex.argtypes = [ctypes.POINTER(gdn_shape), ctypes.POINTER(gdn_prefill_io), vp]
+        L.gdn_decode_ex.restype = ctypes.c_int
+        L.gdn_decode_ex.argtypes = [ctypes.POINTER(gdn_shape), ctypes.POINTER(gdn_decode_io), vp]
+        L.gdn_selftest_wait_timeout.restype = ctypes.c_int
+        L.gdn_selftest_wait_timeout.argtypes = [ctypes.c_int, vp]
         _lib = L
     return _lib
 
@@ -131,9 +156,67 @@ def gdn_decode_step(qkv_pre, z, g, beta, conv_w, norm_w, S, conv_in, conv_out, o
         raise GdnError(st, "gdn_decode_step")
 
 
+def _raw(raw_gates):
+    """A gdn_raw_gates struct from dict(a, b, A_log, dt_bias) of tensors, or None."""
+    if raw_gates is None:
+        return None
+    return gdn_raw_gates(*[_ptr(raw_gates[k]) for k in ("a", "b", "A_log", "dt_bias")])
+
+
+def gdn_prefill_ex(qkv_pre, z, g, beta, conv_w, norm_w, S0, conv0, o, S_T, conv_T, *, Hk, Hv,
+                   raw_gates=None, cu_seqlens=None, S_snap=None, eps_l2=1e-6, eps_norm=1e-6,
+                   q_scale=0.0, stream=None):
+    """Prefill with the options of gdn_prefill_ex: raw gate projections
+    (raw_gates = dict(a, b, A_log, dt_bias), g = beta = None), packed
+    sequences (qkv_pre [N, C], z and o [N, Hv*D], cu_seqlens int32 [B+1] on
+    the device), and per-token state snapshots S_snap [tokens, Hv, D, D]."""
+    if cu_seqlens is not None:
+        N, C = qkv_pre.shape
+        B, T = cu_seqlens.numel() - 1, N
+    else:
+        B, T, C = qkv_pre.shape
+    io_dtype = _io_code(qkv_pre.dtype)
+    sh = make_shape(B, T, Hk, Hv, _head_width(C, Hk, Hv), io_dtype, eps_l2, eps_norm, q_scale)
+    rg = _raw(raw_gates)
+    io = gdn_prefill_io(_ptr(qkv_pre), _ptr(z), _ptr(g), _ptr(beta),
+                        None if rg is None else ctypes.addressof(rg), _ptr(conv_w), _ptr(norm_w),
+                        _ptr(S0), _ptr(conv0), _ptr(o), _ptr(S_T), _ptr(conv_T), _ptr(cu_seqlens),
+                        _ptr(S_snap))
+    st = lib().gdn_prefill_ex(ctypes.byref(sh), ctypes.byref(io), _stream(stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_prefill_ex")
+
+
+def gdn_decode_ex(qkv_pre, z, g, beta, conv_w, norm_w, S, conv_in, conv_out, o, *, Hk, Hv,
+                  raw_gates=None, S_snap=None, eps_l2=1e-6, eps_norm=1e-6, q_scale=0.0,
+                  stream=None):
+    """T new tokens per sequence from the cache (qkv_pre [B, T, C], z and o
+    [B, T, Hv*D]); S is updated in place; S_snap [B, T, Hv, D, D] (optional)
+    receives the state after every token; the window after the T tokens goes
+    to conv_out."""
+    B, T, C = qkv_pre.shape
+    sh = make_shape(B, T, Hk, Hv, _head_width(C, Hk, Hv), _io_code(qkv_pre.dtype), eps_l2,
+                    eps_norm, q_scale)
+    rg = _raw(raw_gates)
+    io = gdn_decode_io(_ptr(qkv_pre), _ptr(z), _ptr(g), _ptr(beta),
+                       None if rg is None else ctypes.addressof(rg), _ptr(conv_w), _ptr(norm_w),
+                       _ptr(S), _ptr(S_snap), _ptr(conv_in), _ptr(conv_out), _ptr(o))
+    st = lib().gdn_decode_ex(ctypes.byref(sh), ctypes.byref(io), _stream(stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_decode_ex")
+
+
 def gdn_device_status(stream=None, reset=False):
     """Synchronise and return the device-side status code (0 = OK)."""
     return lib().gdn_device_status(_stream(stream), int(bool(reset)))
+
+
+def gdn_selftest_wait_timeout(wait_us, stream=None):
+    """Enqueue the failure-detection self-test: a kernel whose bounded wait
+    runs out after `wait_us` microseconds and records a timeout."""
+    st = lib().gdn_selftest_wait_timeout(int(wait_us), _stream(stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_selftest_wait_timeout")
 
 
 # ---------------------------------------------------------------- helpers

@@ -17,6 +17,12 @@ Distributions (the workload recipe of the Qwen3.5 / Qwen3.8 shapes):
   beta = sigmoid(N(0, 1))                g = log(sigmoid(N(mu_g, 1))), mu_g = 3 (5 for
                                          the long-horizon 27B prefill)
   norm_w = 1 + N(0, 0.1^2)               S0 = 0 (tiny case) or N(0, 0.02^2)
+Raw gate projections (when the gates are prepared inside the library):
+  a, b ~ N(0, 1) (io dtype)              A_log = log U(1, 16), dt_bias ~ U(-7, -2)
+                                         per value head (fp32)
+so that softplus(a + dt_bias) is mostly 1e-3 .. 0.1 and g spans about
+-1e-3 .. -2 per token.
+Packed (varlen) batches draw their token tensors as one [N, ...] run.
 """
 import concurrent.futures as cf
 import os
@@ -26,7 +32,7 @@ from typing import Dict, Optional
 import numpy as np
 
 TENSOR_IDS = {"qkv_pre": 1, "z": 2, "beta": 3, "g": 4, "conv_w": 5, "norm_w": 6,
-              "S0": 7, "conv0": 8}
+              "S0": 7, "conv0": 8, "a": 9, "b": 10, "A_log": 11, "dt_bias": 12}
 
 _SLAB = 1 << 24  # values drawn per call, to bound peak host memory
 
@@ -182,4 +188,66 @@ def decode_problem(B=256, Hk=16, Hv=48, io="bf16", steps=64, case=4, g_mu=3.0,
             lambda s: _normal(base + 2 + 100 * s, (B, Hv * Dv), io=io), range(steps))))
     p.beta = np.stack([_beta(base + 3 + 100 * s, (B, Hv)) for s in range(steps)])
     p.g = np.stack([_log_decay(base + 4 + 100 * s, (B, Hv), g_mu) for s in range(steps)])
+    return p
+
+
+def raw_gate_arrays(case, lead, Hv, io="bf16"):
+    """Raw gate projections a, b [*lead, Hv] (io-rounded) and the per-head
+    parameters A_log, dt_bias [Hv] (fp32)."""
+    base = 1000 * case
+    gen = np.random.Generator(np.random.PCG64(base + 11))
+    A_log = np.log(gen.uniform(1.0, 16.0, size=Hv)).astype(np.float32)
+    gen = np.random.Generator(np.random.PCG64(base + 12))
+    dt_bias = gen.uniform(-7.0, -2.0, size=Hv).astype(np.float32)
+    return dict(a=_normal(base + 9, tuple(lead) + (Hv,), io=io),
+                b=_normal(base + 10, tuple(lead) + (Hv,), io=io), A_log=A_log, dt_bias=dt_bias)
+
+
+@dataclass
+class PackedProblem:
+    """Sequences of the given lengths packed back to back (cu_seqlens)."""
+    lengths: tuple
+    Hk: int
+    Hv: int
+    io: str
+    Dk: int = 128
+    Dv: int = 128
+    arrays: Dict[str, Optional[np.ndarray]] = field(default_factory=dict)
+
+    @property
+    def C(self) -> int:
+        return 2 * self.Hk * self.Dk + self.Hv * self.Dv
+
+    @property
+    def cu_seqlens(self) -> np.ndarray:
+        return np.concatenate([[0], np.cumsum(self.lengths)]).astype(np.int32)
+
+    @property
+    def N(self) -> int:
+        return int(sum(self.lengths))
+
+    def __getitem__(self, k):
+        return self.arrays[k]
+
+
+def packed_problem(lengths, Hk, Hv, io="bf16", case=0, g_mu=3.0, state=True, raw_gates=False,
+                   Dk=128, Dv=128) -> PackedProblem:
+    """Inputs of one packed prefill call; with ``raw_gates`` the gates come as
+    raw projections (arrays a, b, A_log, dt_bias) instead of g and beta."""
+    p = PackedProblem(tuple(int(n) for n in lengths), Hk, Hv, io, Dk, Dv)
+    B, N, C = len(p.lengths), p.N, p.C
+    base = 1000 * case
+    a = p.arrays
+    a["qkv_pre"] = _normal(base + 1, (N, C), io=io)
+    a["z"] = _normal(base + 2, (N, Hv * Dv), io=io)
+    if raw_gates:
+        a.update(raw_gate_arrays(case, (N,), Hv, io))
+        a["g"] = a["beta"] = None
+    else:
+        a["beta"] = _beta(base + 3, (N, Hv))
+        a["g"] = _log_decay(base + 4, (N, Hv), g_mu)
+    a["conv_w"] = _normal(base + 5, (C, 4), std=0.5, io=io)
+    a["norm_w"] = _normal(base + 6, (Dv,), mean=1.0, std=0.1, io=io)
+    a["S0"] = _normal(base + 7, (B, Hv, Dv, Dk), std=0.02) if state else None
+    a["conv0"] = _normal(base + 8, (B, 3, C), io=io) if state else None
     return p

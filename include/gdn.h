@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define GDN_ABI_VERSION 1
+#define GDN_ABI_VERSION 2
 
 typedef enum {
   GDN_OK = 0,
@@ -122,14 +122,109 @@ gdn_status gdn_decode_step(const gdn_shape *shape, const void *qkv_pre, const vo
                            void *o, void *stream);
 
 /*
+ * Raw gate projections ("How Qwen3.5 works" section 9.5): per token and
+ * value head the library forms, in fp32,
+ *   beta = sigmoid(b),   g = -exp(A_log[h]) * softplus(a + dt_bias[h]).
+ *   a, b            [tokens][Hv], io dtype (the outputs of the a and b
+ *                   projections, same token order as z)
+ *   A_log, dt_bias  [Hv] fp32 layer parameters
+ */
+typedef struct {
+  const void *a, *b;
+  const float *A_log, *dt_bias;
+} gdn_raw_gates;
+
+/*
+ * Arguments of gdn_prefill_ex.  Exactly one gate source: (g, beta) or
+ * raw_gates.  "tokens" is B*T for fixed-length sequences and T for packed
+ * ones (below).
+ *   qkv_pre [tokens][C]   z, o [tokens][Hv*Dv]   g, beta [tokens][Hv]
+ *   S0, S_T, conv0, conv_T per sequence, as for gdn_prefill
+ *   cu_seqlens  device int32 [B+1] or NULL.  When given, the B sequences are
+ *               packed back to back ("varlen"): sequence s owns tokens
+ *               cu_seqlens[s] .. cu_seqlens[s+1]-1 and shape->T is the total
+ *               token count.  Each sequence starts from its own S0[s] and
+ *               conv0[s] (or zeros); nothing flows between sequences.  A
+ *               sequence of length 0 copies its incoming state and window.
+ *               The offsets are read on the device: offsets that decrease
+ *               or leave [0, T] make the kernel skip that sequence (its
+ *               outputs stay untouched) and record GDN_ERR_INVALID_ARG for
+ *               gdn_device_status.
+ *   S_snap      [tokens][Hv][Dv][Dk] fp32 or NULL: the state after every
+ *               token (for rollback; costs one state write per token).
+ * Fixed length without snapshots and with bf16 io runs the chunked
+ * tensor-core kernel; the other cases run the token-serial kernel.
+ */
+typedef struct {
+  const void *qkv_pre, *z;
+  const float *g, *beta;
+  const gdn_raw_gates *raw_gates;
+  const void *conv_w, *norm_w;
+  const float *S0;
+  const void *conv0;
+  void *o;
+  float *S_T;
+  void *conv_T;
+  const int *cu_seqlens;
+  float *S_snap;
+} gdn_prefill_io;
+
+/* Prefill with the options above; aliasing and alignment rules as for
+ * gdn_prefill (raw gates, cu_seqlens and S_snap count as inputs / outputs). */
+gdn_status gdn_prefill_ex(const gdn_shape *shape, const gdn_prefill_io *io, void *stream);
+
+/*
+ * Arguments of gdn_decode_ex: shape->T >= 1 new tokens for each of B
+ * sequences from the cached state, e.g. the draft tokens of speculative
+ * decoding being verified ("How Qwen3.5 works" section 13).
+ *   qkv_pre [B][T][C]   z, o [B][T][Hv*Dv]   g, beta [B][T][Hv] (or raw_gates)
+ *   S        [B][Hv][Dv][Dk]     the cached state, updated in place (final state)
+ *   S_snap   [B][T][Hv][Dv][Dk]  or NULL: the state after each token, so that a
+ *                                caller who accepts only the first m tokens can
+ *                                restore snapshot m-1
+ *   conv_in, conv_out [B][3][C]  cached window in; window after the T tokens out
+ *                                (must not overlap)
+ * T == 1 without snapshots runs the decode kernel of gdn_decode_step; other
+ * cases run the token-serial kernel with the state held in registers.
+ */
+typedef struct {
+  const void *qkv_pre, *z;
+  const float *g, *beta;
+  const gdn_raw_gates *raw_gates;
+  const void *conv_w, *norm_w;
+  float *S;
+  float *S_snap;
+  const void *conv_in;
+  void *conv_out;
+  void *o;
+} gdn_decode_io;
+
+gdn_status gdn_decode_ex(const gdn_shape *shape, const gdn_decode_io *io, void *stream);
+
+/*
  * Synchronise `stream` and report device-side failures recorded since the
  * last reset: GDN_ERR_TIMEOUT if a kernel's bounded wait gave up (the kernel
- * then returned early and its outputs are incomplete), GDN_ERR_CUDA if the
- * synchronisation itself failed, GDN_OK otherwise.  reset != 0 clears the
+ * then returned early and its outputs are incomplete), GDN_ERR_INVALID_ARG
+ * if a kernel met packed-sequence offsets it could not use, GDN_ERR_CUDA if
+ * the synchronisation itself failed, GDN_OK otherwise.  reset != 0 clears the
  * record afterwards.  The record is one word per device, shared by all
  * streams.
  */
 gdn_status gdn_device_status(void *stream, int reset);
+
+/*
+ * Failure-detection self-test; the pages have no counterpart (they describe
+ * no kernels).  Enqueues one CTA that takes the same steps as a prefill
+ * kernel whose awaited work never completes: it allocates TMEM, waits on an
+ * mbarrier that nothing arrives on with the bounded wait the prefill kernel
+ * uses, here limited to `wait_us` microseconds (1 .. 1000000), records the
+ * timeout in the device error word, frees its TMEM and returns.  Afterwards
+ * gdn_device_status reports GDN_ERR_TIMEOUT and the context stays usable.
+ * Nothing is allocated and no caller buffer is touched.
+ * Errors: GDN_ERR_INVALID_ARG for wait_us out of range, GDN_ERR_NO_DEVICE,
+ * GDN_ERR_CUDA from the launch.
+ */
+gdn_status gdn_selftest_wait_timeout(int wait_us, void *stream);
 
 #ifdef __cplusplus
 }

@@ -26,6 +26,9 @@
  *        node gdn.norm: y = w * x / sqrt(mean(x^2) + eps) * silu(z);
  *        section 9.9 of "How Qwen3.5 works" (scale applied directly, SiLU
  *        gate after normalising).
+ *   0. optionally, the gates from their raw projections
+ *        "How Qwen3.5 works" section 9.5: beta = sigmoid(b),
+ *        g = -exp(A_log) * softplus(a + dt_bias), per value head.
  *
  * State layout: S[b][h][i][j], i = value index (row), j = key index
  * (contiguous), i.e. the node gdn.core orientation.  Dimensions are generic
@@ -100,6 +103,19 @@ void oracle_core_recurrent(int T, int Dk, int Dv, const double *q, const double 
                      v + (size_t)t * Dv, g[t], beta[t], o + (size_t)t * Dv);
 }
 
+/* Step 0 ("How Qwen3.5 works" section 9.5): the write gate and the log
+ * decay of one token on one value head from the raw projections a, b and
+ * the head's parameters A_log, dt_bias. */
+double oracle_sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+/* softplus(x) = log(1 + e^x), evaluated without overflow for large x. */
+double oracle_softplus(double x) { return x > 0.0 ? x + log1p(exp(-x)) : log1p(exp(x)); }
+
+void oracle_gates(double a, double b, double A_log, double dt_bias, double *g, double *beta) {
+  *beta = oracle_sigmoid(b);
+  *g = -exp(A_log) * oracle_softplus(a + dt_bias);
+}
+
 /* Step 4 for one head: y = w * x / sqrt(mean(x^2) + eps) * silu(z). */
 void oracle_gated_norm(int n, const double *x, const double *z, const double *w,
                        double eps, double *y) {
@@ -138,27 +154,37 @@ static double conv_at(const oracle_shape *s, const float *qkv_pre, const float *
   return oracle_conv_silu_one(window, taps);
 }
 
+/* Raw gate inputs: a, b [B][T][Hv]; A_log, dt_bias [Hv]. */
+typedef struct {
+  const float *a, *b, *A_log, *dt_bias;
+} oracle_raw_gates;
+
 /*
  * The whole mixer for a list of (b, h) units.
  *
  *   qkv_pre [B][T][C], C = 2*Hk*Dk + Hv*Dv     z [B][T][Hv*Dv]
- *   g, beta [B][T][Hv]                         conv_w [C][4]     norm_w [Dv]
+ *   g, beta [B][T][Hv], or NULL with `raw` giving the gates' projections
+ *   conv_w [C][4]     norm_w [Dv]
  *   S0 [B][Hv][Dv][Dk] or NULL (zeros)         conv0 [B][3][C] or NULL (zeros)
  *   units[n_units] = b*Hv + h, or NULL for all B*Hv units in order
  *   y      [n_units][T][Dv]   gated-norm output (the mixer output)
  *   core_o [n_units][T][Dv]   core output before the norm, or NULL
  *   S_T    [n_units][Dv][Dk]  final state
+ *   S_snap [n_units][T][Dv][Dk] or NULL: the state after each token
  *   conv_T [B][3][C] or NULL  last three raw rows of (conv0 ++ qkv_pre)
  *
  * Returns 0, or -1 for a shape the method does not define (T < 1,
- * Hv not a multiple of Hk, non-positive sizes) or a unit out of range.
+ * Hv not a multiple of Hk, non-positive sizes), a unit out of range, or
+ * neither (g, beta) nor raw gates given.
  */
-int oracle_gdn_prefill(const oracle_shape *s, const float *qkv_pre, const float *z,
-                       const float *g, const float *beta, const float *conv_w,
-                       const float *norm_w, const float *S0, const float *conv0, int n_units,
-                       const int *units, double *y, double *core_o, double *S_T,
-                       double *conv_T, int n_threads) {
+int oracle_gdn_prefill_ex(const oracle_shape *s, const float *qkv_pre, const float *z,
+                          const float *g, const float *beta, const oracle_raw_gates *raw,
+                          const float *conv_w, const float *norm_w, const float *S0,
+                          const float *conv0, int n_units, const int *units, double *y,
+                          double *core_o, double *S_T, double *S_snap, double *conv_T,
+                          int n_threads) {
   if (s->B < 1 || s->T < 1 || s->Hk < 1 || s->Hv < 1 || s->Dk < 1 || s->Dv < 1) return -1;
+  if (!(g && beta) && !(raw && raw->a && raw->b && raw->A_log && raw->dt_bias)) return -1;
   if (s->Hv % s->Hk != 0) return -1;
   int total = s->B * s->Hv;
   if (!units) n_units = total;
@@ -208,7 +234,17 @@ int oracle_gdn_prefill(const oracle_shape *s, const float *qkv_pre, const float 
       oracle_l2norm(Dk, qraw, s->eps_l2, s->q_scale, qh);
       oracle_l2norm(Dk, kraw, s->eps_l2, 1.0, kh_);
       size_t gi = ((size_t)b * T + t) * s->Hv + h;
-      oracle_core_step(Dk, Dv, S, qh, kh_, vv, (double)g[gi], (double)beta[gi], o);
+      double gt, bt;
+      if (g && beta) {
+        gt = (double)g[gi];
+        bt = (double)beta[gi];
+      } else {
+        oracle_gates((double)raw->a[gi], (double)raw->b[gi], (double)raw->A_log[h],
+                     (double)raw->dt_bias[h], &gt, &bt);
+      }
+      oracle_core_step(Dk, Dv, S, qh, kh_, vv, gt, bt, o);
+      if (S_snap)
+        memcpy(S_snap + ((size_t)u * T + t) * Dv * Dk, S, sizeof(double) * (size_t)Dv * Dk);
       if (core_o) memcpy(core_o + ((size_t)u * T + t) * Dv, o, sizeof(double) * Dv);
       const float *zt = z + ((size_t)b * T + t) * ((size_t)s->Hv * Dv) + (size_t)h * Dv;
       for (int i = 0; i < Dv; ++i) zz[i] = (double)zt[i];
@@ -218,4 +254,15 @@ int oracle_gdn_prefill(const oracle_shape *s, const float *qkv_pre, const float 
     free(S);
   }
   return failed ? -1 : 0;
+}
+
+/* The mixer with precomputed gates and no snapshots. */
+int oracle_gdn_prefill(const oracle_shape *s, const float *qkv_pre, const float *z,
+                       const float *g, const float *beta, const float *conv_w,
+                       const float *norm_w, const float *S0, const float *conv0, int n_units,
+                       const int *units, double *y, double *core_o, double *S_T,
+                       double *conv_T, int n_threads) {
+  if (!g || !beta) return -1;
+  return oracle_gdn_prefill_ex(s, qkv_pre, z, g, beta, NULL, conv_w, norm_w, S0, conv0, n_units,
+                               units, y, core_o, S_T, NULL, conv_T, n_threads);
 }

@@ -17,6 +17,11 @@ from . import build as _build
 _lib = None
 
 
+class _RawGates(ctypes.Structure):
+    _fields_ = [("a", ctypes.c_void_p), ("b", ctypes.c_void_p), ("A_log", ctypes.c_void_p),
+                ("dt_bias", ctypes.c_void_p)]
+
+
 class _Shape(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("Hk", ctypes.c_int),
                 ("Hv", ctypes.c_int), ("Dk", ctypes.c_int), ("Dv", ctypes.c_int),
@@ -46,6 +51,16 @@ def lib():
         L.oracle_core_recurrent.argtypes = [ctypes.c_int] * 3 + [dp] * 7
         L.oracle_gated_norm.restype = None
         L.oracle_gated_norm.argtypes = [ctypes.c_int, dp, dp, dp, ctypes.c_double, dp]
+        L.oracle_sigmoid.restype = ctypes.c_double
+        L.oracle_sigmoid.argtypes = [ctypes.c_double]
+        L.oracle_softplus.restype = ctypes.c_double
+        L.oracle_softplus.argtypes = [ctypes.c_double]
+        L.oracle_gates.restype = None
+        L.oracle_gates.argtypes = [ctypes.c_double] * 4 + [dp, dp]
+        L.oracle_gdn_prefill_ex.restype = ctypes.c_int
+        L.oracle_gdn_prefill_ex.argtypes = [ctypes.POINTER(_Shape)] + [ctypes.c_void_p] * 4 + [
+            ctypes.POINTER(_RawGates)] + [ctypes.c_void_p] * 4 + [ctypes.c_int, ctypes.c_void_p] + [
+            ctypes.c_void_p] * 5 + [ctypes.c_int]
         L.oracle_gdn_prefill.restype = ctypes.c_int
         L.oracle_gdn_prefill.argtypes = [ctypes.POINTER(_Shape)] + [ctypes.c_void_p] * 8 + [
             ctypes.c_int, ctypes.c_void_p] + [ctypes.c_void_p] * 4 + [ctypes.c_int]
@@ -81,6 +96,24 @@ def l2norm(x, eps=1e-6, scale=1.0):
     y = np.empty_like(x)
     lib().oracle_l2norm(x.size, xp, eps, scale, y.ctypes.data_as(ctypes.POINTER(ctypes.c_double)))
     return y
+
+
+def sigmoid(x):
+    return lib().oracle_sigmoid(float(x))
+
+
+def softplus(x):
+    return lib().oracle_softplus(float(x))
+
+
+def gates(a, b, A_log, dt_bias):
+    """Write gate and log decay of one token on one head (section 9.5 of
+    "How Qwen3.5 works"): returns (g, beta) as floats."""
+    g = ctypes.c_double()
+    beta = ctypes.c_double()
+    lib().oracle_gates(float(a), float(b), float(A_log), float(dt_bias), ctypes.byref(g),
+                       ctypes.byref(beta))
+    return g.value, beta.value
 
 
 def gated_norm(x, z, w, eps=1e-6):
@@ -120,16 +153,19 @@ def conv_channels(Hk, Hv, Dk=128, Dv=128):
 
 def gdn_prefill(qkv_pre, z, g, beta, conv_w, norm_w, S0=None, conv0=None, *, Hk, Hv,
                 Dk=128, Dv=128, eps_l2=1e-6, eps_norm=1e-6, q_scale=None, units=None,
-                threads=0, want_core=False, want_conv=True):
+                threads=0, want_core=False, want_conv=True, raw_gates=None, want_snap=False):
     """The full mixer on the CPU in fp64.
 
     qkv_pre [B,T,C], z [B,T,Hv*Dv], g and beta [B,T,Hv], conv_w [C,4],
     norm_w [Dv], S0 [B,Hv,Dv,Dk] or None, conv0 [B,3,C] or None.
+    With ``raw_gates`` = dict(a, b [B,T,Hv], A_log, dt_bias [Hv]), g and beta
+    must be None and come from the raw projections (section 9.5).
 
     ``units`` (optional) lists b*Hv + h pairs to compute; the default is all.
     Returns a dict with ``o`` [B,T,Hv*Dv] (all units) or, when ``units`` is
     given, ``o_units`` [n,T,Dv]; ``S_T`` ([B,Hv,Dv,Dk] or [n,Dv,Dk]);
-    ``conv_T`` [B,3,C]; and ``core`` (pre-norm output) when asked.
+    ``conv_T`` [B,3,C]; ``core`` (pre-norm output) and ``S_snap`` (the state
+    after every token, [B,T,Hv,Dv,Dk] or [n,T,Dv,Dk]) when asked.
     """
     qkv_pre = np.asarray(qkv_pre)
     B, T, C = qkv_pre.shape
@@ -137,7 +173,13 @@ def gdn_prefill(qkv_pre, z, g, beta, conv_w, norm_w, S0=None, conv0=None, *, Hk,
         raise ValueError("qkv_pre channel count %d does not match Hk/Hv/Dk/Dv" % C)
     sh = _Shape(B, T, Hk, Hv, Dk, Dv, eps_l2, eps_norm,
                 (1.0 / np.sqrt(Dk)) if q_scale is None else q_scale)
+    if (raw_gates is None) == (g is None or beta is None):
+        raise ValueError("give either g and beta or raw_gates")
     arrs = [_f(qkv_pre), _f(z), _f(g), _f(beta), _f(conv_w), _f(norm_w), _f(S0), _f(conv0)]
+    raw = None
+    if raw_gates is not None:
+        keep = [_f(raw_gates[k]) for k in ("a", "b", "A_log", "dt_bias")]
+        raw = _RawGates(*[k[1] for k in keep])
     if units is None:
         n = B * Hv
         up = None
@@ -150,12 +192,15 @@ def gdn_prefill(qkv_pre, z, g, beta, conv_w, norm_w, S0=None, conv0=None, *, Hk,
     core = np.empty((n, T, Dv)) if want_core else None
     S_T = np.empty((n, Dv, Dk))
     conv_T = np.empty((B, 3, C)) if want_conv else None
-    rc = lib().oracle_gdn_prefill(
-        ctypes.byref(sh), *[a[1] for a in arrs], n, up,
-        y.ctypes.data_as(ctypes.c_void_p),
-        None if core is None else core.ctypes.data_as(ctypes.c_void_p),
-        S_T.ctypes.data_as(ctypes.c_void_p),
-        None if conv_T is None else conv_T.ctypes.data_as(ctypes.c_void_p), int(threads))
+    snap = np.empty((n, T, Dv, Dk)) if want_snap else None
+
+    def ptr(x):
+        return None if x is None else x.ctypes.data_as(ctypes.c_void_p)
+
+    ins = [a[1] for a in arrs]
+    rc = lib().oracle_gdn_prefill_ex(
+        ctypes.byref(sh), *ins[:4], None if raw is None else ctypes.byref(raw), *ins[4:], n, up,
+        ptr(y), ptr(core), ptr(S_T), ptr(snap), ptr(conv_T), int(threads))
     if rc != 0:
         raise ValueError("oracle_gdn_prefill rejected the problem (rc=%d)" % rc)
     out = {"conv_T": conv_T}
@@ -164,11 +209,15 @@ def gdn_prefill(qkv_pre, z, g, beta, conv_w, norm_w, S0=None, conv0=None, *, Hk,
         out["S_T"] = S_T.reshape(B, Hv, Dv, Dk)
         if want_core:
             out["core"] = core.reshape(B, Hv, T, Dv).transpose(0, 2, 1, 3).reshape(B, T, Hv * Dv)
+        if want_snap:
+            out["S_snap"] = snap.reshape(B, Hv, T, Dv, Dk).transpose(0, 2, 1, 3, 4)
     else:
         out["o_units"] = y
         out["S_T"] = S_T
         if want_core:
             out["core_units"] = core
+        if want_snap:
+            out["S_snap"] = snap
     return out
 
 
@@ -182,6 +231,55 @@ def gdn_decode_step(qkv_pre, z, g, beta, conv_w, norm_w, S, conv_in, **kw):
     r = gdn_prefill(qkv_pre[:, None], np.asarray(z)[:, None], np.asarray(g)[:, None],
                     np.asarray(beta)[:, None], conv_w, norm_w, S, conv_in, **kw)
     return {"o": r["o"][:, 0], "S": r["S_T"], "conv_out": r["conv_T"]}
+
+
+def gdn_decode_multi(qkv_pre, z, g, beta, conv_w, norm_w, S, conv_in, **kw):
+    """T consecutive decode tokens for B sequences (speculative verification:
+    "How Qwen3.5 works" section 13), with the state after every token kept
+    for rollback.  qkv_pre [B,T,C], z [B,T,Hv*Dv], g and beta [B,T,Hv] (or
+    raw_gates=...), S [B,Hv,Dv,Dk], conv_in [B,3,C].  The T tokens of a
+    sequence are a prefill of T tokens from the cached state; returns
+    dict(o [B,T,Hv*Dv], S [B,Hv,Dv,Dk], S_snap [B,T,Hv,Dv,Dk], conv_out)."""
+    r = gdn_prefill(qkv_pre, z, g, beta, conv_w, norm_w, S, conv_in, want_snap=True, **kw)
+    return {"o": r["o"], "S": r["S_T"], "S_snap": r["S_snap"], "conv_out": r["conv_T"]}
+
+
+def gdn_prefill_varlen(qkv_pre, z, g, beta, conv_w, norm_w, cu_seqlens, S0=None, conv0=None, *,
+                       Hk, Hv, raw_gates=None, **kw):
+    """Packed variable-length prefill: sequence s owns the tokens
+    cu_seqlens[s] .. cu_seqlens[s+1]-1 of qkv_pre [N,C], z [N,Hv*Dv], g and
+    beta [N,Hv] (or raw_gates with a, b [N,Hv]); each starts from its own
+    S0[s] / conv0[s] (zeros when None), and nothing flows between sequences.
+    By definition that is one independent prefill per sequence, which is
+    what this does.  Returns dict(o [N,Hv*Dv], S_T [nseq,Hv,Dv,Dk],
+    conv_T [nseq,3,C])."""
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    nseq = cu.size - 1
+    N, C = np.asarray(qkv_pre).shape
+    if cu[0] != 0 or cu[-1] != N or np.any(np.diff(cu) < 1):
+        raise ValueError("cu_seqlens must run from 0 to the token count in steps of >= 1")
+    Dv = kw.get("Dv", 128)
+    Dk = kw.get("Dk", 128)
+    o = np.empty((N, Hv * Dv))
+    S_T = np.empty((nseq, Hv, Dv, Dk))
+    conv_T = np.empty((nseq, 3, C))
+    for s in range(nseq):
+        lo, hi = int(cu[s]), int(cu[s + 1])
+        sl = slice(lo, hi)
+        rg = None
+        if raw_gates is not None:
+            rg = dict(a=np.asarray(raw_gates["a"])[None, sl], b=np.asarray(raw_gates["b"])[None, sl],
+                      A_log=raw_gates["A_log"], dt_bias=raw_gates["dt_bias"])
+        r = gdn_prefill(np.asarray(qkv_pre)[None, sl], np.asarray(z)[None, sl],
+                        None if g is None else np.asarray(g)[None, sl],
+                        None if beta is None else np.asarray(beta)[None, sl], conv_w, norm_w,
+                        None if S0 is None else np.asarray(S0)[s:s + 1],
+                        None if conv0 is None else np.asarray(conv0)[s:s + 1],
+                        Hk=Hk, Hv=Hv, raw_gates=rg, **kw)
+        o[sl] = r["o"][0]
+        S_T[s] = r["S_T"][0]
+        conv_T[s] = r["conv_T"][0]
+    return {"o": o, "S_T": S_T, "conv_T": conv_T}
 
 
 def default_threads():

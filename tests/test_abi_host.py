@@ -112,3 +112,52 @@ def test_alias_rules(L):
     # decode: conv_out must differ from conv_in; S must not overlap o.
     assert decode(L, shape(T=1), conv_out=fake(7)) == 4
     assert decode(L, shape(T=1), o=fake(6, 1024)) == 4
+
+
+def test_selftest_limit_checked_on_host(L):
+    for us in (0, -1, 1000001):
+        assert L.gdn_selftest_wait_timeout(us, None) == gdn.GDN_ERR_INVALID_ARG
+
+
+def prefill_ex(L, sh, raw=None, **over):
+    args = dict(qkv_pre=fake(0), z=fake(1), g=fake(2), beta=fake(3), raw_gates=None, conv_w=fake(4),
+                norm_w=fake(5), S0=fake(6), conv0=fake(7), o=fake(8), S_T=fake(9), conv_T=fake(10),
+                cu_seqlens=None, S_snap=None)
+    args.update(over)
+    if raw is not None:
+        args["raw_gates"] = ctypes.addressof(raw)
+    io = gdn.gdn_prefill_io(**args)
+    return L.gdn_prefill_ex(ctypes.byref(sh), ctypes.byref(io), None)
+
+
+def decode_ex(L, sh, raw=None, **over):
+    args = dict(qkv_pre=fake(0), z=fake(1), g=fake(2), beta=fake(3), raw_gates=None, conv_w=fake(4),
+                norm_w=fake(5), S=fake(6), S_snap=None, conv_in=fake(7), conv_out=fake(8), o=fake(9))
+    args.update(over)
+    if raw is not None:
+        args["raw_gates"] = ctypes.addressof(raw)
+    io = gdn.gdn_decode_io(**args)
+    return L.gdn_decode_ex(ctypes.byref(sh), ctypes.byref(io), None)
+
+
+def test_extended_entry_points_check_on_host(L):
+    sh = shape()
+    assert L.gdn_prefill_ex(ctypes.byref(sh), None, None) == 1
+    assert L.gdn_decode_ex(ctypes.byref(sh), None, None) == 1
+    raw = gdn.gdn_raw_gates(fake(11), fake(12), fake(13), fake(14))
+    # exactly one gate source
+    assert prefill_ex(L, sh, raw=raw) == 1
+    assert prefill_ex(L, sh, g=None, beta=None) == 1
+    assert decode_ex(L, shape(T=3), g=None, beta=None) == 1
+    assert prefill_ex(L, sh, raw=gdn.gdn_raw_gates(fake(11), None, fake(13), fake(14)),
+                      g=None, beta=None) == 1
+    # raw gate tensors and offsets are aligned inputs; snapshots are outputs
+    assert prefill_ex(L, sh, raw=gdn.gdn_raw_gates(fake(11, 2), fake(12), fake(13), fake(14)),
+                      g=None, beta=None) == 3
+    assert prefill_ex(L, sh, cu_seqlens=fake(11, 4)) == 3
+    assert prefill_ex(L, sh, S_snap=fake(0)) == 4           # snapshots over an input
+    assert prefill_ex(L, sh, S_snap=fake(9)) == 4           # snapshots over S_T
+    assert prefill_ex(L, sh, o=fake(11), raw=raw, g=None, beta=None) == 4  # o over gate a
+    assert decode_ex(L, shape(T=4), S_snap=fake(6, 256)) == 4  # snapshots over the state
+    assert decode_ex(L, shape(T=4), conv_out=fake(7)) == 4
+    assert prefill_ex(L, shape(T=1 << 29, B=4)) == 2        # token rows beyond 2^30

@@ -49,6 +49,15 @@ MUTANTS = {
                             "conv0[((size_t)b * 3 + (2 - e)) * C + c]"),
     "carried_window_off_by_one": ("xext(s, qkv_pre, conv0, b, T + e, c);",
                                   "xext(s, qkv_pre, conv0, b, T + e - 1, c);"),
+    "sigmoid_sign": ("return 1.0 / (1.0 + exp(-x));", "return 1.0 / (1.0 + exp(x));"),
+    "softplus_drops_linear_term": ("x > 0.0 ? x + log1p(exp(-x))", "x > 0.0 ? log1p(exp(-x))"),
+    "decay_A_log_not_exponentiated": ("*g = -exp(A_log) *", "*g = -A_log *"),
+    "decay_no_dt_bias": ("oracle_softplus(a + dt_bias)", "oracle_softplus(a)"),
+    "write_gate_from_a": ("*beta = oracle_sigmoid(b);", "*beta = oracle_sigmoid(a);"),
+    "gate_parameters_of_head_zero": ("(double)raw->A_log[h],\n                     (double)raw->dt_bias[h]",
+                                     "(double)raw->A_log[0],\n                     (double)raw->dt_bias[0]"),
+    "snapshots_reversed": ("S_snap + ((size_t)u * T + t) * Dv * Dk",
+                           "S_snap + ((size_t)u * T + (T - 1 - t)) * Dv * Dk"),
 }
 
 

@@ -433,3 +433,125 @@ def test_rejects_empty_and_bad_head_ratio():
     p, sh = _small_problem(23, T=2, Hk=3, Hv=4)
     with pytest.raises(ValueError):
         O.gdn_prefill(**p, **sh)
+
+
+# --------------------------------------------------------------- gates ----
+def test_sigmoid_and_softplus():
+    """Section 9.5 of "How Qwen3.5 works" uses the logistic sigmoid and
+    softplus(x) = log(1 + e^x): library values, the reflection identities,
+    and no overflow at large |x|."""
+    assert O.sigmoid(0.0) == 0.5
+    assert O.softplus(0.0) == pytest.approx(math.log(2.0), rel=1e-15)
+    for x in (-30.0, -3.5, -0.25, 0.7, 4.0, 30.0):
+        assert O.sigmoid(x) == pytest.approx(float(expit(x)), rel=1e-14)
+        assert O.softplus(x) == pytest.approx(float(np.logaddexp(0.0, x)), rel=1e-14)
+        assert O.sigmoid(x) + O.sigmoid(-x) == pytest.approx(1.0, rel=1e-15)
+        assert O.softplus(x) - O.softplus(-x) == pytest.approx(x, rel=1e-13)
+    assert O.softplus(800.0) == 800.0
+    assert 0.0 <= O.softplus(-800.0) < 1e-300
+
+
+def test_gates_closed_forms():
+    """beta = sigmoid(b); g = -exp(A_log) softplus(a + dt_bias)."""
+    g, beta = O.gates(0.4, 0.0, math.log(3.0), -0.4)  # a + dt_bias = 0
+    assert g == pytest.approx(-3.0 * math.log(2.0), rel=1e-14)
+    assert beta == 0.5
+    g1, b1 = O.gates(1.0, -2.0, 0.5, 0.2)
+    g2, b2 = O.gates(1.0, 3.0, 0.5, 0.2)
+    assert g1 == g2 and b1 < 0.5 < b2  # b drives only the write gate
+    g, _ = O.gates(40.0, 0.0, 0.0, 2.0)  # softplus(x) -> x for large x
+    assert g == pytest.approx(-42.0, rel=1e-15)
+    rng = _rng(40)
+    for _ in range(20):
+        a, b, A_log, dt = rng.normal(size=4) * (3.0, 2.0, 1.0, 2.0)
+        g, beta = O.gates(a, b, A_log, dt)
+        assert g <= 0.0
+        assert g == pytest.approx(-math.exp(A_log) * float(np.logaddexp(0.0, a + dt)), rel=1e-13)
+        assert beta == pytest.approx(float(expit(b)), rel=1e-14)
+
+
+def _raw_gates(seed, B, T, Hv):
+    rng = _rng(seed)
+    f = np.float32
+    return dict(a=rng.normal(size=(B, T, Hv)).astype(f), b=rng.normal(size=(B, T, Hv)).astype(f),
+                A_log=np.log(rng.uniform(1.0, 16.0, size=Hv)).astype(f),
+                dt_bias=rng.normal(-3.0, 1.0, size=Hv).astype(f))
+
+
+def test_raw_gates_through_the_mixer():
+    """The mixer fed the raw projections equals the mixer fed g and beta
+    computed from them by library routines (per value head parameters)."""
+    p, sh = _small_problem(41, T=6)
+    rg = _raw_gates(42, 2, 6, sh["Hv"])
+    want_g = -np.exp(rg["A_log"].astype(np.float64)) * np.logaddexp(
+        0.0, rg["a"].astype(np.float64) + rg["dt_bias"].astype(np.float64))
+    want_b = expit(rg["b"].astype(np.float64))
+    plain = O.gdn_prefill(**dict(p, g=want_g, beta=want_b), **sh)
+    raw = O.gdn_prefill(**dict(p, g=None, beta=None), raw_gates=rg, **sh)
+    # the plain call carries g and beta in float32
+    np.testing.assert_allclose(raw["o"], plain["o"], rtol=2e-5, atol=1e-6)
+    np.testing.assert_allclose(raw["S_T"], plain["S_T"], rtol=2e-5, atol=1e-7)
+    with pytest.raises(ValueError):
+        O.gdn_prefill(**p, raw_gates=rg, **sh)
+
+
+# ----------------------------------------------- snapshots and packing ----
+def test_state_snapshots_are_prefix_states():
+    """The state kept after token t equals the final state of a prefill of
+    the first t + 1 tokens; the last one is S_T."""
+    p, sh = _small_problem(43, T=4)
+    full = O.gdn_prefill(**p, **sh, want_snap=True)
+    np.testing.assert_array_equal(full["S_snap"][:, -1], full["S_T"])
+    seq = ("qkv_pre", "z", "g", "beta")
+    for t in range(1, 4):
+        pre = O.gdn_prefill(**{k: (v[:, :t] if k in seq else v) for k, v in p.items()}, **sh)
+        np.testing.assert_array_equal(full["S_snap"][:, t - 1], pre["S_T"])
+
+
+def test_multi_token_decode_rollback():
+    """Speculative verification: after T tokens, restoring the snapshot of
+    token m and decoding token m + 1 again reproduces that token's output."""
+    p, sh = _small_problem(44, T=3)
+    r = O.gdn_decode_multi(p["qkv_pre"], p["z"], p["g"], p["beta"], p["conv_w"], p["norm_w"],
+                           p["S0"], p["conv0"], **sh)
+    np.testing.assert_array_equal(r["S_snap"][:, -1], r["S"])
+    m = 0
+    conv_m = np.concatenate([p["conv0"][:, 1:], p["qkv_pre"][:, :1]], axis=1)
+    d = O.gdn_decode_step(p["qkv_pre"][:, 1], p["z"][:, 1], p["g"][:, 1], p["beta"][:, 1],
+                          p["conv_w"], p["norm_w"], r["S_snap"][:, m], conv_m, **sh)
+    np.testing.assert_allclose(d["o"], r["o"][:, 1], rtol=1e-5, atol=1e-7)
+
+
+def _pack(p, keys=("qkv_pre", "z", "g", "beta")):
+    return {k: (v.reshape(-1, v.shape[-1]) if k in keys else v) for k, v in p.items()}
+
+
+def test_varlen_equal_lengths_equals_batched():
+    """Packed sequences of equal length give the batched result exactly."""
+    p, sh = _small_problem(45, T=7, B=3)
+    batched = O.gdn_prefill(**p, **sh)
+    q = _pack(p)
+    packed = O.gdn_prefill_varlen(q["qkv_pre"], q["z"], q["g"], q["beta"], p["conv_w"],
+                                  p["norm_w"], [0, 7, 14, 21], p["S0"], p["conv0"], **sh)
+    np.testing.assert_array_equal(packed["o"], batched["o"].reshape(21, -1))
+    np.testing.assert_array_equal(packed["S_T"], batched["S_T"])
+    np.testing.assert_array_equal(packed["conv_T"], batched["conv_T"])
+
+
+def test_varlen_sequences_do_not_interact():
+    """Changing one packed sequence leaves the others untouched, and a
+    sequence shorter than the conv window carries part of its old window."""
+    p, sh = _small_problem(46, T=5, B=3)
+    q = _pack(p)
+    cu = [0, 5, 6, 15]
+    base = O.gdn_prefill_varlen(q["qkv_pre"], q["z"], q["g"], q["beta"], p["conv_w"], p["norm_w"],
+                                cu, p["S0"], p["conv0"], **sh)
+    x2 = q["qkv_pre"].copy()
+    x2[:5] += 1.0
+    moved = O.gdn_prefill_varlen(x2, q["z"], q["g"], q["beta"], p["conv_w"], p["norm_w"], cu,
+                                 p["S0"], p["conv0"], **sh)
+    assert not np.allclose(moved["o"][:5], base["o"][:5])
+    np.testing.assert_array_equal(moved["o"][5:], base["o"][5:])
+    np.testing.assert_array_equal(moved["S_T"][1:], base["S_T"][1:])
+    np.testing.assert_array_equal(base["conv_T"][1, :2], p["conv0"][1, 1:])
+    np.testing.assert_array_equal(base["conv_T"][1, 2], q["qkv_pre"][5])
