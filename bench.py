@@ -8,6 +8,12 @@ Workloads (synthetic, seeded; see gated_deltanet_mixer_gb300/inputs.py):
            step = 64 consecutive gdn_decode_step calls.  Reported under
            "decode" as state GB/s and total GB/s against HBM.
 
+  next     the extended calls, per GPU, under "next": the 4B prefill with
+           the gates formed from raw projections, a packed batch of 24
+           sequences (log-uniform lengths 100..4000), and 4-token decoding
+           from the cache at the 27B decode shape with and without per-token
+           state snapshots.
+
 --impl reference times the fp64 CPU oracle instead, on a bounded sample of the
 same prefill workload, with the same metric and unit.
 
@@ -71,6 +77,32 @@ def decode_bytes(B, Hk, Hv, io=2):
 
 def decode_state_bytes(B, Hv):
     return B * 8 * Hv * D * D
+
+
+def packed_bytes(lengths, Hk, Hv, io=2, raw_gates=False):
+    """Algorithmic HBM bytes of one packed prefill call."""
+    C = conv_channels(Hk, Hv)
+    N, B = sum(lengths), len(lengths)
+    gates = 2 * io * Hv if raw_gates else 8 * Hv
+    per_token = io * C + 2 * io * Hv * D + gates
+    per_seq = 2 * Hv * D * D * 4 + 2 * 3 * C * io
+    return N * per_token + B * per_seq + C * 4 * io + D * io + (B + 1) * 4 + (8 * Hv if raw_gates else 0)
+
+
+def decode_multi_bytes(B, T, Hk, Hv, io=2, snapshots=True):
+    """Algorithmic HBM bytes of one T-token decode call: the state read and
+    written once, one snapshot per token, the window in and out, the tokens."""
+    C = conv_channels(Hk, Hv)
+    per_seq = 8 * Hv * D * D + (4 * T * Hv * D * D if snapshots else 0) + 2 * 3 * C * io \
+        + T * (io * C + 2 * io * Hv * D + 8 * Hv)
+    return B * per_seq + C * 4 * io + D * io
+
+
+# Packed-batch length mix: 24 sequences, log-uniform lengths in [100, 4000]
+# (a serving batch of prompts), seed 7.
+def varlen_lengths():
+    gen = np.random.Generator(np.random.PCG64(7))
+    return [int(round(x)) for x in np.exp(gen.uniform(np.log(100.0), np.log(4000.0), size=24))]
 
 
 # ----------------------------------------------------------------- helpers
@@ -329,6 +361,9 @@ def gdn_arm(args, world, rank, local):
                          "peak_source": peak_src + " hbm_gbs (burst copy)"},
         }
         del S, conv, q_all, z_all, g_all, b_all, od
+    # ---- the extended calls: raw gates, packed batch, multi-token decode
+    nxt = None if args.no_next else next_rows(args, x, o, S_T, conv_T, p, peaks, peak_src, stream,
+                                              barrier, world, rank)
     clk = clocks.stop()
 
     # ---- end to end through the public API with host buffers
@@ -392,6 +427,7 @@ def gdn_arm(args, world, rank, local):
         "gpu_launches": args.steps * PREFILL_KERNELS_PER_CALL,
         "clocks": clk,
         "decode": dec,
+        "next": nxt,
     }
     if world > 1:
         import torch.distributed as dist
@@ -413,6 +449,105 @@ def gdn_arm(args, world, rank, local):
 
 
 PREFILL_SOURCE = "gated_deltanet_mixer_gb300/csrc/prefill_chunked.cu"
+
+
+def time_launches(fn, steps, warmup, stream, barrier):
+    """Mean device ms per call of fn (one library call), CUDA events on `stream`."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    barrier()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for k in range(steps):
+        ev[k][0].record(stream)
+        fn()
+        ev[k][1].record(stream)
+    barrier()
+    return float(np.mean([s.elapsed_time(e) for s, e in ev]))
+
+
+def next_rows(args, x, o, S_T, conv_T, p, peaks, peak_src, stream, barrier, world, rank):
+    """Throughput of the extended entry points on model-shaped inputs (each
+    input larger than L2), per GPU."""
+    import torch
+
+    from gated_deltanet_mixer_gb300 import gdn
+    from gated_deltanet_mixer_gb300 import inputs as I
+
+    def dev(a, dt=torch.float32):
+        return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to("cuda").to(dt)
+
+    bf = torch.bfloat16
+    hbm = peaks["hbm_gbs"]
+    out = {}
+    steps = max(3, min(args.steps, 10))
+
+    # raw gate projections on the 4B prefill workload
+    rg = I.raw_gate_arrays(60 + 1000 * rank, (p.B, p.T), p.Hv, "bf16")
+    rgd = dict(a=dev(rg["a"], bf), b=dev(rg["b"], bf), A_log=dev(rg["A_log"]),
+               dt_bias=dev(rg["dt_bias"]))
+    ms = time_launches(lambda: gdn.gdn_prefill_ex(
+        x["qkv_pre"], x["z"], None, None, x["conv_w"], x["norm_w"], x["S0"], x["conv0"], o, S_T,
+        conv_T, Hk=p.Hk, Hv=p.Hv, raw_gates=rgd, stream=stream), steps, args.warmup, stream, barrier)
+    nb = packed_bytes([p.T] * p.B, p.Hk, p.Hv, raw_gates=True)
+    out["prefill_raw_gates"] = {
+        "workload": "4B-shaped prefill (B=%d, T=%d) with beta, g formed from raw a, b, A_log, "
+                    "dt_bias inside the kernel" % (p.B, p.T),
+        "value": world * p.B * p.T / (ms * 1e-3), "unit": "tokens/s", "ms_per_launch": ms,
+        "roofline": {"bound": "hbm", "achieved": nb / (ms * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
+                     "frac": nb / (ms * 1e-3) / 1e9 / hbm, "peak_source": peak_src}}
+    del rgd
+
+    # packed variable-length batch at the 4B head shape
+    lens = varlen_lengths()
+    q = I.packed_problem(lens, p.Hk, p.Hv, io="bf16", case=61 + 1000 * rank)
+    qa = q.arrays
+    qx = {k: dev(qa[k], bf if k in ("qkv_pre", "z", "conv_w", "norm_w", "conv0") else torch.float32)
+          for k in ("qkv_pre", "z", "g", "beta", "conv_w", "norm_w", "S0", "conv0")}
+    cu = torch.from_numpy(q.cu_seqlens).to("cuda")
+    qo = torch.empty(q.N, p.Hv * D, device="cuda", dtype=bf)
+    qS = torch.empty(len(lens), p.Hv, D, D, device="cuda")
+    qc = torch.empty(len(lens), 3, q.C, device="cuda", dtype=bf)
+    ms = time_launches(lambda: gdn.gdn_prefill_ex(
+        qx["qkv_pre"], qx["z"], qx["g"], qx["beta"], qx["conv_w"], qx["norm_w"], qx["S0"],
+        qx["conv0"], qo, qS, qc, Hk=p.Hk, Hv=p.Hv, cu_seqlens=cu, stream=stream), steps,
+        args.warmup, stream, barrier)
+    nb = packed_bytes(lens, p.Hk, p.Hv)
+    out["prefill_varlen"] = {
+        "workload": "packed batch of %d sequences (log-uniform lengths 100..4000, %d tokens), "
+                    "Hk=%d, Hv=%d, bf16 io" % (len(lens), q.N, p.Hk, p.Hv),
+        "value": world * q.N / (ms * 1e-3), "unit": "tokens/s", "ms_per_launch": ms,
+        "roofline": {"bound": "hbm", "achieved": nb / (ms * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
+                     "frac": nb / (ms * 1e-3) / 1e9 / hbm, "peak_source": peak_src}}
+    del qx, qo, qS, qc, cu
+
+    # T-token decode from the cache (speculative verification), 27B decode shape
+    T = 4
+    dp = I.decode_problem(**dict(I.DECODE_CASE, steps=T, case=I.DECODE_CASE["case"] + 70 + 1000 * rank))
+    S = dev(dp.S)
+    snap = torch.empty(dp.B, T, dp.Hv, D, D, device="cuda")
+    conv_in, conv_out = dev(dp.conv, bf), torch.empty(dp.B, 3, dp.C, device="cuda", dtype=bf)
+    tq = dev(dp.qkv_pre.transpose(1, 0, 2), bf)
+    tz = dev(dp.z.transpose(1, 0, 2), bf)
+    tg, tb = dev(dp.g.transpose(1, 0, 2)), dev(dp.beta.transpose(1, 0, 2))
+    cw, nw = dev(dp.conv_w, bf), dev(dp.norm_w, bf)
+    od = torch.empty(dp.B, T, dp.Hv * D, device="cuda", dtype=bf)
+    for with_snap in (True, False):
+        ms = time_launches(lambda: gdn.gdn_decode_ex(
+            tq, tz, tg, tb, cw, nw, S, conv_in, conv_out, od, Hk=dp.Hk, Hv=dp.Hv,
+            S_snap=snap if with_snap else None, stream=stream), steps, args.warmup, stream, barrier)
+        nb = decode_multi_bytes(dp.B, T, dp.Hk, dp.Hv, snapshots=with_snap)
+        out["decode_multi%s" % ("_snapshots" if with_snap else "")] = {
+            "workload": "27B-shaped decode of %d tokens per sequence from the cache, B=%d, Hv=%d%s"
+                        % (T, dp.B, dp.Hv, ", state snapshot after every token" if with_snap else ""),
+            "value": world * dp.B * T / (ms * 1e-3), "unit": "tokens/s", "ms_per_launch": ms,
+            "roofline": {"bound": "hbm", "achieved": nb / (ms * 1e-3) / 1e9, "peak": hbm,
+                         "unit": "GB/s", "frac": nb / (ms * 1e-3) / 1e9 / hbm,
+                         "peak_source": peak_src}}
+    if gdn.gdn_device_status(stream) != 0:
+        raise RuntimeError("device status not OK after the extended calls")
+    return out
 
 
 # --------------------------------------------------------- reference arm
@@ -467,6 +602,8 @@ def main():
                     choices=["4b_prefill", "0.8b_prefill", "27b_prefill"])
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-next", action="store_true",
+                    help="skip the extended calls (raw gates, packed batch, multi-token decode)")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--ref-budget", type=float, default=120.0,

@@ -205,9 +205,9 @@ gdn_status decode_impl(const gdn_shape *shape, const gdn_decode_io *io, void *st
 
   const bool bf16 = shape->io_dtype == GDN_BF16;
   cudaError_t e;
-  if (shape->T == 1 && !io->S_snap) {
-    gdn::DecodeArgs a{d, io->qkv_pre, io->z, gs, io->conv_w, io->norm_w, io->S, io->conv_in, io->conv_out,
-                      io->o, err};
+  if (shape->T <= gdn::kDecodeMaxT) {
+    gdn::DecodeArgs a{d,           io->qkv_pre,  io->z, gs, io->conv_w, io->norm_w, io->S, io->S_snap,
+                      io->conv_in, io->conv_out, io->o, err};
     e = gdn::launch_decode(a, bf16, (cudaStream_t)stream);
   } else {
     // T tokens from the cache = a T-token prefill with the state in place.

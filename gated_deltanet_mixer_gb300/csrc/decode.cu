@@ -1,11 +1,15 @@
-// decode.cu -- one decode token for B sequences: the memory-bound step.
+// decode.cu -- new tokens for B sequences from the cache: the memory-bound
+// step.  decode1_kernel takes one token (the common case, no snapshots);
+// decode_kernel takes T <= kDecodeMaxT tokens and can keep the state after
+// every token.
 //
 // One CTA per (sequence b, value head h), 8 warps.  The 128 x 128 fp32 state
 // of the pair is streamed through registers exactly once: each warp owns 16
 // state rows (row = value index i, key index j contiguous), loads them as
-// float4 per lane, forms both S k^ and S q^ in the same pass, and writes the
-// updated rows straight back.  Row i of the update only needs v[i], so no
-// block-wide barrier sits between loading and storing the state.
+// float4 per lane, and per token forms both S k^ and S q^ in the same pass
+// and updates the rows in registers; the final rows (and, when asked, the
+// rows after every token) are written straight back.  Row i of the update
+// only needs v[i], so no block-wide barrier sits inside the state pass.
 //
 // Per token ("How Qwen3.5 works" section 9.6, decay -> predict -> correct ->
 // read; node gdn.core of the Qwen3.8-27B spec for the v x k orientation):
@@ -19,6 +23,7 @@ namespace gdn {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
 constexpr int kRowsPerWarp = 16;
 
 // silu(conv) of channel c for the new token; also shifts the window of c
@@ -43,7 +48,7 @@ __device__ __forceinline__ float conv_token(const IO *win, const IO *x, const IO
 }
 
 template <typename IO, bool kRawGates>
-__global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) decode1_kernel(DecodeArgs a) {
   const Dims d = a.d;
   const int unit = blockIdx.x;
   const int b = unit / d.Hv, h = unit % d.Hv;
@@ -156,15 +161,175 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
   }
 }
 
+template <typename IO, bool kRawGates>
+__global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
+  const Dims d = a.d;
+  const int T = d.T;
+  const int unit = blockIdx.x;
+  const int b = unit / d.Hv, h = unit % d.Hv;
+  const int r = d.Hv / d.Hk, kh = h / r;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const long long C = d.C;
+
+  __shared__ __align__(16) float s_q[kDecodeMaxT][kD];
+  __shared__ __align__(16) float s_k[kDecodeMaxT][kD];
+  __shared__ float s_v[kDecodeMaxT][kD];
+  __shared__ __align__(16) float s_o[kDecodeMaxT][kD];
+  __shared__ float s_kq[kDecodeMaxT];
+
+  const IO *x = static_cast<const IO *>(a.qkv_pre) + (long long)b * T * C;
+  const IO *win = static_cast<const IO *>(a.conv_in) + (long long)b * 3 * C;
+  IO *wout = static_cast<IO *>(a.conv_out) + (long long)b * 3 * C;
+  const IO *cw = static_cast<const IO *>(a.conv_w);
+
+  // ---- front end: conv + SiLU of the T tokens, sliding the window of the
+  // channel(s) this thread owns (q and k of key head kh, or v of head h)
+  {
+    const bool qk = tid < kD;
+    const long long c0 = qk ? (long long)kh * kD + tid : 2LL * d.Hk * kD + (long long)h * kD + (tid - kD);
+    const long long c1 = (long long)d.Hk * kD + (long long)kh * kD + tid;  // k channel (qk threads)
+    float w0[3] = {ld_io(win + c0), ld_io(win + C + c0), ld_io(win + 2 * C + c0)};
+    float w1[3] = {0.f, 0.f, 0.f};
+    const float4 t0 = ld_io4(cw + 4 * c0);
+    float4 t1 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (qk) {
+      w1[0] = ld_io(win + c1);
+      w1[1] = ld_io(win + C + c1);
+      w1[2] = ld_io(win + 2 * C + c1);
+      t1 = ld_io4(cw + 4 * c1);
+    }
+    for (int t = 0; t < T; ++t) {
+      const float x0 = ld_io(x + (long long)t * C + c0);
+      float acc = fmaf(t0.w, x0, fmaf(t0.z, w0[2], fmaf(t0.y, w0[1], t0.x * w0[0])));
+      w0[0] = w0[1];
+      w0[1] = w0[2];
+      w0[2] = x0;
+      if (qk) {
+        s_q[t][tid] = silu(acc);
+        const float x1 = ld_io(x + (long long)t * C + c1);
+        const float acc1 = fmaf(t1.w, x1, fmaf(t1.z, w1[2], fmaf(t1.y, w1[1], t1.x * w1[0])));
+        w1[0] = w1[1];
+        w1[1] = w1[2];
+        w1[2] = x1;
+        s_k[t][tid] = silu(acc1);
+      } else {
+        s_v[t][tid - kD] = silu(acc);
+      }
+    }
+    // the new window: the last three raw rows (one CTA per key head shifts q/k)
+    if (!qk || (h % r) == 0) {
+#pragma unroll
+      for (int e = 0; e < 3; ++e) st_io(wout + e * C + c0, w0[e]);
+      if (qk) {
+#pragma unroll
+        for (int e = 0; e < 3; ++e) st_io(wout + e * C + c1, w1[e]);
+      }
+    }
+  }
+  __syncthreads();
+  // ---- L2 norms of q and k, and k^ . q^, one warp per token
+  for (int t = warp; t < T; t += kWarps) {
+    float4 q4 = reinterpret_cast<const float4 *>(s_q[t])[lane];
+    float4 k4 = reinterpret_cast<const float4 *>(s_k[t])[lane];
+    const float fq = rsqrtf(warp_sum(dot4(q4, q4)) + d.eps_l2) * d.q_scale;
+    const float fk = rsqrtf(warp_sum(dot4(k4, k4)) + d.eps_l2);
+    q4.x *= fq; q4.y *= fq; q4.z *= fq; q4.w *= fq;
+    k4.x *= fk; k4.y *= fk; k4.z *= fk; k4.w *= fk;
+    reinterpret_cast<float4 *>(s_q[t])[lane] = q4;
+    reinterpret_cast<float4 *>(s_k[t])[lane] = k4;
+    const float kq = warp_sum(dot4(q4, k4));
+    if (lane == 0) s_kq[t] = kq;
+  }
+  __syncthreads();
+
+  // ---- state pass: each warp streams its 16 rows once
+  const long long gi = (long long)b * d.Hv + h;
+  float *S = a.S + gi * (kD * kD);
+  const int row0 = warp * kRowsPerWarp;
+  // gates of token t (every thread reads the same element: a broadcast load)
+  auto gates = [&](int t, float &gt, float &bt) {
+    const long long i = ((long long)b * T + t) * d.Hv + h;
+    if (kRawGates) {
+      gate_at<IO>(a.gate, i, h, gt, bt);
+    } else {
+      gt = a.gate.g[i];
+      bt = a.gate.beta[i];
+    }
+  };
+  float g_nx, b_nx;
+  gates(0, g_nx, b_nx);
+  float4 s[kRowsPerWarp];
+#pragma unroll
+  for (int i = 0; i < kRowsPerWarp; ++i) s[i] = ld_stream(S + (row0 + i) * kD + 4 * lane);
+
+  for (int t = 0; t < T; ++t) {
+    const float alpha = expf(g_nx), beta = b_nx, kq = s_kq[t];
+    if (t + 1 < T) gates(t + 1, g_nx, b_nx);
+    const float4 k4 = reinterpret_cast<const float4 *>(s_k[t])[lane];
+    const float4 q4 = reinterpret_cast<const float4 *>(s_q[t])[lane];
+    float part[32];
+#pragma unroll
+    for (int i = 0; i < kRowsPerWarp; ++i) {
+      part[i] = dot4(s[i], k4);
+      part[16 + i] = dot4(s[i], q4);
+    }
+    // lane L < 16: (S k^)[row0 + L];  lane L >= 16: (S q^)[row0 + L - 16]
+    const float red = transpose_reduce32(part, lane);
+    const int myrow = lane & 15;
+    const float Sk = __shfl_sync(0xffffffffu, red, myrow);
+    const float Sq = __shfl_sync(0xffffffffu, red, myrow + 16);
+    const float delta = beta * (s_v[t][row0 + myrow] - alpha * Sk);
+    if (lane < 16) s_o[t][row0 + myrow] = fmaf(alpha, Sq, delta * kq);
+#pragma unroll
+    for (int i = 0; i < kRowsPerWarp; ++i) {
+      const float di = __shfl_sync(0xffffffffu, delta, i);
+      s[i].x = fmaf(alpha, s[i].x, di * k4.x);
+      s[i].y = fmaf(alpha, s[i].y, di * k4.y);
+      s[i].z = fmaf(alpha, s[i].z, di * k4.z);
+      s[i].w = fmaf(alpha, s[i].w, di * k4.w);
+    }
+    if (a.S_snap) {
+      float *snap = a.S_snap + (((long long)b * T + t) * d.Hv + h) * (kD * kD);
+#pragma unroll
+      for (int i = 0; i < kRowsPerWarp; ++i) st_stream(snap + (row0 + i) * kD + 4 * lane, s[i]);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kRowsPerWarp; ++i) st_stream(S + (row0 + i) * kD + 4 * lane, s[i]);
+  __syncthreads();
+
+  // ---- gated RMSNorm over the head's 128 outputs, one warp per token
+  const float4 w4 = ld_io4(static_cast<const IO *>(a.norm_w) + 4 * lane);
+  for (int t = warp; t < T; t += kWarps) {
+    const float4 o4 = reinterpret_cast<const float4 *>(s_o[t])[lane];
+    const float rstd = rsqrtf(warp_sum(dot4(o4, o4)) * (1.0f / kD) + d.eps_norm);
+    const long long oi = (((long long)b * T + t) * d.Hv + h) * kD + 4 * lane;  // [B][T][Hv*Dv]
+    const float4 z4 = ld_io4(static_cast<const IO *>(a.z) + oi);
+    float4 y;
+    y.x = w4.x * (o4.x * rstd) * silu(z4.x);
+    y.y = w4.y * (o4.y * rstd) * silu(z4.y);
+    y.z = w4.z * (o4.z * rstd) * silu(z4.z);
+    y.w = w4.w * (o4.w * rstd) * silu(z4.w);
+    st_io4(static_cast<IO *>(a.o) + oi, y);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_decode(const DecodeArgs &a, bool bf16, cudaStream_t s) {
+  if (a.d.T < 1 || a.d.T > kDecodeMaxT) return cudaErrorInvalidValue;
   dim3 grid((unsigned)(a.d.B * a.d.Hv)), block(kThreads);
   const bool raw = a.gate.g == nullptr;
-  if (bf16)
+  if (a.d.T == 1 && !a.S_snap) {
+    if (bf16)
+      (raw ? decode1_kernel<__nv_bfloat16, true> : decode1_kernel<__nv_bfloat16, false>)<<<grid, block, 0, s>>>(a);
+    else
+      (raw ? decode1_kernel<float, true> : decode1_kernel<float, false>)<<<grid, block, 0, s>>>(a);
+  } else if (bf16) {
     (raw ? decode_kernel<__nv_bfloat16, true> : decode_kernel<__nv_bfloat16, false>)<<<grid, block, 0, s>>>(a);
-  else
+  } else {
     (raw ? decode_kernel<float, true> : decode_kernel<float, false>)<<<grid, block, 0, s>>>(a);
+  }
   return cudaGetLastError();
 }
 

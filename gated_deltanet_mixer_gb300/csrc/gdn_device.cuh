@@ -39,17 +39,51 @@ __device__ __forceinline__ void st_io4(__nv_bfloat16 *p, float4 v) {
 // The write gate and log decay of element i (head h) of a [token][Hv] gate
 // tensor: given, or from the raw projections ("How Qwen3.5 works" section
 // 9.5: beta = sigmoid(b), g = -exp(A_log) softplus(a + dt_bias), in fp32).
+// neg_exp_A = -exp(A_log[h]).
+__device__ __forceinline__ void raw_gate_math(float a, float b, float neg_exp_A, float dt_bias, float &g,
+                                              float &beta) {
+  const float x = a + dt_bias;
+  const float sp = fmaxf(x, 0.f) + log1pf(expf(-fabsf(x)));  // softplus without overflow
+  g = neg_exp_A * sp;
+  beta = 1.0f / (1.0f + expf(-b));
+}
 template <typename IO, typename Src>
 __device__ __forceinline__ void gate_at(const Src &s, long long i, int h, float &g, float &beta) {
   if (s.g) {
     g = s.g[i];
     beta = s.beta[i];
   } else {
-    const float x = ld_io(static_cast<const IO *>(s.a) + i) + s.dt_bias[h];
-    const float sp = fmaxf(x, 0.f) + log1pf(expf(-fabsf(x)));  // softplus without overflow
-    g = -expf(s.A_log[h]) * sp;
-    beta = 1.0f / (1.0f + expf(-ld_io(static_cast<const IO *>(s.b) + i)));
+    raw_gate_math(ld_io(static_cast<const IO *>(s.a) + i), ld_io(static_cast<const IO *>(s.b) + i),
+                  -expf(s.A_log[h]), s.dt_bias[h], g, beta);
   }
+}
+
+// Longest-first placement of packed sequences (cu_seqlens[0..B]): returns
+// the sequence of rank `slot` when the sequences are ordered by length,
+// longest first, ties by index.  CTAs are dispatched in index order, so CTA
+// slots taking sequences in this order start the longest work first.  The
+// order is a permutation even for malformed offsets (their rows are then
+// rejected by the caller).  All threads of the block must call it; `scratch`
+// is shared memory for B + 2 ints; B <= kLongestFirstMax.
+constexpr int kLongestFirstMax = 512;
+__device__ __forceinline__ int longest_first(const int *cu, int B, int slot, int *scratch) {
+  int *len = scratch, *pick = scratch + B;
+  for (int s = threadIdx.x; s < B; s += blockDim.x) len[s] = cu[s + 1] - cu[s];
+  if (threadIdx.x == 0) *pick = slot;  // replaced below; keeps the result defined
+  __syncthreads();
+  for (int s = threadIdx.x; s < B; s += blockDim.x) {
+    const int ls = len[s];
+    int rank = 0;
+    for (int j = 0; j < B; ++j) {
+      const int lj = len[j];
+      rank += (lj > ls) || (lj == ls && j < s);
+    }
+    if (rank == slot) *pick = s;
+  }
+  __syncthreads();
+  const int res = *pick;
+  __syncthreads();
+  return res;
 }
 
 // silu(x) = x * sigmoid(x)

@@ -42,12 +42,16 @@ struct PrefillArgs {
   unsigned int *err;      // device error word
 };
 
+// T = d.T new tokens per sequence from the cache (1 <= T <= kDecodeMaxT):
+// qkv_pre [B][T][C], z and o [B][T][Hv*128], gates [B][T][Hv].
+constexpr int kDecodeMaxT = 16;
 struct DecodeArgs {
-  Dims d;               // d.T == 1
+  Dims d;
   const void *qkv_pre, *z;
   GateSrc gate;
   const void *conv_w, *norm_w;
-  float *S;
+  float *S;             // in place
+  float *S_snap;        // may be null: the state after every token, [B][T][Hv][128][128]
   const void *conv_in;
   void *conv_out;
   void *o;

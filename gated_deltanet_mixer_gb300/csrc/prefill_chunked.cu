@@ -80,7 +80,8 @@ constexpr uint32_t OFF_L = OFF_RAW;                  // L fp32 [64][68], phases 
 constexpr uint32_t OFF_PB = OFF_RAW + 64 * kLs * 4;  // block products fp32 [3][16][16], phase D
 constexpr uint32_t OFF_TF = OFF_NW;                  // T fp32 [64][64], phase D
 constexpr uint32_t OFF_OST = OFF_VH;                 // O^T staging fp32 [64][128] (VH + VL), phase J
-constexpr uint32_t kSmemUsed = OFF_VEC + 2048;
+constexpr uint32_t kVecBytes = 2560;
+constexpr uint32_t kSmemUsed = OFF_VEC + kVecBytes;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // + alignment slack
 static_assert(OFF_PB + 3 * 256 * 4 <= OFF_Z, "solve scratch fits in the raw rows");
 static_assert(OFF_RAW % 128 == 0 && OFF_Z % 128 == 0 && kRawBlock % 128 == 0, "TMA destinations");
@@ -103,6 +104,8 @@ struct __align__(16) Vecs {  // per-token chunk vectors in shared memory
   float gam[kC];   // e^{G_last - G_j}
   float beta[kC];
   float bd[kC];    // beta_j d_j
+  float gn[kC];    // g of the next chunk (clamped), formed during this chunk's solve
+  float bn[kC];    // beta of the next chunk
   float dC;        // e^{G_last} of the current chunk
   float dC_next;   // e^{G_last} of the next chunk
   int mild;        // G_last >= -40: ratios as d_i * dinv_j
@@ -112,7 +115,7 @@ struct __align__(16) Vecs {  // per-token chunk vectors in shared memory
   uint64_t bar_raw;  // raw rows landed
   uint64_t bar_z;    // z rows landed
 };
-static_assert(sizeof(Vecs) <= 2048, "vector area");
+static_assert(sizeof(Vecs) <= kVecBytes, "vector area");
 
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
@@ -136,8 +139,10 @@ __device__ __forceinline__ float2 silu2(float2 x) {
 __device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
 
 // g and beta of the chunk starting at t0 (one warp: tokens lane, lane + 32),
-// loaded a chunk ahead of use; gate element of token t is (bos + t) Hv + h.
-// Padded tokens get g = 0, beta = 0; g is clamped at kGMin.
+// loaded a chunk ahead of use (gate element of token t: (bos + t) Hv + h),
+// as given or as the raw projections a, b; finish_gb, called once the loads
+// have landed, forms the gates from raw values.  Padded tokens get g = 0,
+// beta = 0; g is clamped at kGMin.
 template <bool kRaw>
 __device__ __forceinline__ void load_gb(const GateSrc &gs, long long bos, int Hv, int h, int t0, int T,
                                         int lane, float (&gv)[2], float (&bv)[2]) {
@@ -148,16 +153,25 @@ __device__ __forceinline__ void load_gb(const GateSrc &gs, long long bos, int Hv
     bv[u] = 0.f;
     if (t < T) {
       const long long i = (bos + t) * Hv + h;
-      if (kRaw) {
-        GateSrc raw = gs;
-        raw.g = nullptr;
-        gate_at<__nv_bfloat16>(raw, i, h, gv[u], bv[u]);
+      if (kRaw) {  // the raw bf16 bits, widened only in finish_gb (no wait on the load here)
+        gv[u] = __uint_as_float(static_cast<const unsigned short *>(gs.a)[i]);
+        bv[u] = __uint_as_float(static_cast<const unsigned short *>(gs.b)[i]);
       } else {
         gv[u] = gs.g[i];
         bv[u] = gs.beta[i];
       }
-      gv[u] = fmaxf(gv[u], kGMin);
     }
+  }
+}
+template <bool kRaw>
+__device__ __forceinline__ void finish_gb(float neg_exp_A, float dt_bias, int t0, int T, int lane,
+                                          float (&gv)[2], float (&bv)[2]) {
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    if (kRaw && t0 + lane + 32 * u < T)
+      raw_gate_math(__uint_as_float(__float_as_uint(gv[u]) << 16), __uint_as_float(__float_as_uint(bv[u]) << 16),
+                    neg_exp_A, dt_bias, gv[u], bv[u]);
+    gv[u] = fmaxf(gv[u], kGMin);
   }
 }
 
@@ -436,10 +450,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   Vecs &V = *reinterpret_cast<Vecs *>(sm + OFF_VEC);
   const Dims d = a.d;
   const int unit = blockIdx.x;
-  const int b = unit / d.Hv, h = unit % d.Hv;
+  const int h = unit % d.Hv;
+  int b = unit / d.Hv;
   const int r = d.Hv / d.Hk, kh = h / r;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const long long C = d.C;
+  if (a.cu_seqlens && d.B <= kLongestFirstMax)  // packed: the longest sequences first
+    b = longest_first(a.cu_seqlens, d.B, b, reinterpret_cast<int *>(sm + OFF_RAW));
   // This sequence's tokens: rows bos .. bos + T - 1 of the token-major tensors.
   long long bos;
   int T;
@@ -506,9 +523,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     V.abort = 0;
   }
   if (warp == 0) tmem_alloc(&V.tmem, kTmemCols);
-  float g_cur[2], b_cur[2], g_nxt[2], b_nxt[2];  // warp 11: g, beta of this and the next chunk
+  float g_cur[2], b_cur[2], g_nxt[2] = {0.f, 0.f}, b_nxt[2] = {0.f, 0.f};  // warp 11: this and the next chunk
+  float neg_exp_A = 0.f, dt_bias = 0.f;          // warp 11, raw gates: -exp(A_log[h]), dt_bias[h]
   if (warp == 11) {
     load_gb<kRawGates>(a.gate, bos, d.Hv, h, 0, T, lane, g_cur, b_cur);
+    if (kRawGates) {
+      neg_exp_A = -expf(a.gate.A_log[h]);
+      dt_bias = a.gate.dt_bias[h];
+    }
+    finish_gb<kRawGates>(neg_exp_A, dt_bias, 0, T, lane, g_cur, b_cur);
     const float dc0 = __expf(warp_sum(g_cur[0] + g_cur[1]));
     if (lane == 0) V.dC_next = dc0;
   }
@@ -582,6 +605,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t0 = n * kC;
     // A0: chunk vectors; the next chunk's g and beta requested
     if (warp == 11) {
+      if (n > 0) {  // formed during the previous chunk
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          g_cur[u] = V.gn[lane + 32 * u];
+          b_cur[u] = V.bn[lane + 32 * u];
+        }
+      }
       chunk_vectors(V, g_cur, b_cur, lane);
       if (n + 1 < nchunks) load_gb<kRawGates>(a.gate, bos, d.Hv, h, t0 + kC, T, lane, g_nxt, b_nxt);
     }
@@ -651,7 +681,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncthreads();
-    // D: the triangular inverse, scaled copies T B and T B D
+    // D: the triangular inverse, scaled copies T B and T B D.  Warp 11, idle
+    // in the solve, forms the next chunk's gates and total decay meanwhile
+    // (through shared memory, so that the work stays here).
+    if (warp == 11) {
+      finish_gb<kRawGates>(neg_exp_A, dt_bias, t0 + kC, T, lane, g_nxt, b_nxt);
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        V.gn[lane + 32 * u] = g_nxt[u];
+        V.bn[lane + 32 * u] = b_nxt[u];
+      }
+      const float dcn = n + 1 < nchunks ? __expf(warp_sum(g_nxt[0] + g_nxt[1])) : 1.f;
+      if (lane == 0) V.dC_next = dcn;
+    }
     solve_T(sm, V, tid);
     smem_ready();
     // E: MMA2 U^T = V^T (T B)^T, hi*hi + lo*hi + hi*lo; MMA3 W^T = K^T (T B D)^T
@@ -672,10 +714,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (n + 1 < nchunks) raw_pending = true;
     if (!wait_all(&V.bar, phase)) break;
-    if (warp == 11) {  // the next chunk's total decay (its g arrived meanwhile)
-      const float dcn = n + 1 < nchunks ? __expf(warp_sum(g_nxt[0] + g_nxt[1])) : 1.f;
-      if (lane == 0) V.dC_next = dcn;
-    }
     // F: -W^T (lanes k, columns i) -> MN-major [k][i]
     if (warp < kTmemWarps) {
       float v[32];
@@ -779,13 +817,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (n + 1 < nchunks) {
       if (tid == 0) request_z(t0 + kC);
       z_pending = true;
-      if (warp == 11) {
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          g_cur[u] = g_nxt[u];
-          b_cur[u] = b_nxt[u];
-        }
-      }
     }
   }
 

@@ -61,10 +61,14 @@ template <typename IO>
 __global__ void __launch_bounds__(kThreads, 1) prefill_recurrent_kernel(PrefillArgs a) {
   const Dims d = a.d;
   const int unit = blockIdx.x;
-  const int b = unit / d.Hv, h = unit % d.Hv;
+  const int h = unit % d.Hv;
+  int b = unit / d.Hv;
   const int r = d.Hv / d.Hk, kh = h / r;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const long long C = d.C;
+  extern __shared__ __align__(16) float smem[];
+  if (a.cu_seqlens && d.B <= kLongestFirstMax)  // packed: the longest sequences first
+    b = longest_first(a.cu_seqlens, d.B, b, reinterpret_cast<int *>(smem));
   // This sequence's tokens: rows bos .. bos + T - 1 of the token-major tensors.
   long long bos;
   int T;
@@ -81,7 +85,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_recurrent_kernel(PrefillA
     T = d.T;
   }
 
-  extern __shared__ __align__(16) float smem[];
   float *s_q = smem;              // [kTB][128] normalised, scaled query
   float *s_k = s_q + kTB * kD;    // [kTB][128] normalised key
   float *s_v = s_k + kTB * kD;    // [kTB][128] value

@@ -184,8 +184,9 @@ gdn_status gdn_prefill_ex(const gdn_shape *shape, const gdn_prefill_io *io, void
  *                                restore snapshot m-1
  *   conv_in, conv_out [B][3][C]  cached window in; window after the T tokens out
  *                                (must not overlap)
- * T == 1 without snapshots runs the decode kernel of gdn_decode_step; other
- * cases run the token-serial kernel with the state held in registers.
+ * T <= 16 runs the decode kernel of gdn_decode_step (the state streamed once
+ * through registers for all T tokens); longer runs use the token-serial
+ * prefill kernel with the state in place.
  */
 typedef struct {
   const void *qkv_pre, *z;

@@ -115,7 +115,7 @@ def _check_packed(p, got, raw=False):
     assert cu[-1] == o.shape[0]
 
 
-LENGTHS = [(1, 2, 3, 64, 65, 130, 63), (300, 0, 5, 129), (64,)]
+LENGTHS = [(1, 2, 3, 64, 65, 130, 63), (300, 0, 5, 129), (64,), tuple(range(1, 40))]
 
 
 @pytest.mark.parametrize("lengths", LENGTHS)
@@ -191,7 +191,7 @@ def test_prefill_snapshots(io):
 
 
 @pytest.mark.parametrize("io,T,raw", [("bf16", 2, False), ("bf16", 4, True), ("f32", 3, False),
-                                      ("bf16", 1, False)])
+                                      ("bf16", 1, False), ("bf16", 16, False), ("bf16", 20, True)])
 def test_multi_token_decode(io, T, raw):
     B, Hk, Hv = 5, 2, 6
     dp = I.decode_problem(B=B, Hk=Hk, Hv=Hv, io=io, steps=T, case=140 + T)
