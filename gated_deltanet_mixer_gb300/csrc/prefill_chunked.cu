@@ -38,9 +38,12 @@
 //   G  MMA4  Delta^T = U^T - S W^T
 //   H  Delta^T (hi, lo) to TMEM
 //   I  MMA6  Delta^T M^T;            MMA7  S += Delta^T (Gamma K) (split)
-//   J  O = d (S Q^T) + Delta^T M^T, gated RMSNorm (node gdn.norm) -> o;
-//      S -> fp16 copy, rescaled for the next chunk (or S_T after the last);
-//      then the next chunk's z rows are requested (TMA)
+//   J  O = d (S Q^T) + Delta^T M^T, gated RMSNorm (node gdn.norm) -> o,
+//      while MMA7 runs; then S -> fp16 copy, rescaled for the next chunk
+//      (or S_T after the last), and the next chunk's z rows are requested
+// Each MMA group commits to its own mbarrier, so a phase waits only for the
+// products it reads (C for K K^T, F for W^T, J for O) while the rest of the
+// chain (S Q^T, U^T, the state update) keeps the tensor pipe busy.
 #include <cuda.h>
 
 #include "gdn_device.cuh"
@@ -111,7 +114,12 @@ struct __align__(16) Vecs {  // per-token chunk vectors in shared memory
   int mild;        // G_last >= -40: ratios as d_i * dinv_j
   int abort;
   uint32_t tmem;
-  uint64_t bar;      // MMA completion
+  uint64_t bar_qk;   // MMA1 done (K K^T, Q K^T)
+  uint64_t bar_w;    // MMA3 done (W^T)
+  uint64_t bar_d;    // MMA2, MMA4 done (Delta^T)
+  uint64_t bar_o;    // MMA5, MMA6 done (S Q^T, Delta^T M^T)
+  uint64_t bar_s;    // MMA7 done (state update)
+  uint64_t bar_end;  // every MMA issued, before TMEM is freed
   uint64_t bar_raw;  // raw rows landed
   uint64_t bar_z;    // z rows landed
 };
@@ -517,7 +525,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   if (tid == 0) {
-    bar_init(&V.bar, 1);
+    bar_init(&V.bar_qk, 1);
+    bar_init(&V.bar_w, 1);
+    bar_init(&V.bar_d, 1);
+    bar_init(&V.bar_o, 1);
+    bar_init(&V.bar_s, 1);
+    bar_init(&V.bar_end, 1);
     bar_init(&V.bar_raw, 1);
     bar_init(&V.bar_z, 1);
     V.abort = 0;
@@ -575,7 +588,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  uint32_t phase = 0, phase_raw = 0, phase_z = 0;
+  // Each mbarrier completes once per chunk; its phase bit is tracked here.
+  uint32_t ph_qk = 0, ph_w = 0, ph_d = 0, ph_o = 0, ph_s = 0, phase_raw = 0, phase_z = 0;
   bool raw_pending = true, z_pending = true;  // a requested TMA not yet consumed
   const int nchunks = (T + kC - 1) / kC;
   const uint32_t id_kk = idesc(128, 64, 0, 0);
@@ -635,11 +649,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_after();
       issue(tmem + TM_KQ, id_kk, 8, false, [&](int ks) { return desc_k(sbase + OFF_KQ, ks, 128); },
             [&](int ks) { return desc_k(sbase + OFF_KQ, ks, 128); });
+      commit(&V.bar_qk);
       issue_ta(tmem + TM_O1, tmem + TM_S16, id_kk, 8, false,
                [&](int ks) { return desc_k(sbase + OFF_KQ + 64 * 128, ks, 128); });
-      commit(&V.bar);
     }
-    if (!wait_all(&V.bar, phase)) break;
+    if (!wait_all(&V.bar_qk, ph_qk)) break;  // S Q^T runs on meanwhile
     // C: L (fp32, strictly lower, decayed beta K K^T) and M (fp16, decayed Q K^T incl. diagonal)
     if (warp < kTmemWarps) {
       float v[32], rr[32];
@@ -703,17 +717,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_after();
       auto a_vh = [&](int ks) { return desc_mn(sbase + OFF_VH, ks, kC); };
       auto b_tu = [&](int ks) { return desc_k(sbase + OFF_TU, ks, kC); };
-      issue(tmem + TM_U, id_mk, 4, false, a_vh, b_tu);
-      issue(tmem + TM_U, id_mk, 4, true, [&](int ks) { return desc_mn(sbase + OFF_VL, ks, kC); }, b_tu);
-      issue(tmem + TM_U, id_mk, 4, true, a_vh, [&](int ks) { return desc_k(sbase + OFF_TUL, ks, kC); });
       issue(tmem + TM_W, id_mk, 4, false,
             [&](int ks) { return desc(sbase + OFF_KQ + (uint32_t)(ks * 2048), 128 * 128, 1024); },
             [&](int ks) { return desc_k(sbase + OFF_TW, ks, kC); });
-      commit(&V.bar);
+      commit(&V.bar_w);
+      issue(tmem + TM_U, id_mk, 4, false, a_vh, b_tu);
+      issue(tmem + TM_U, id_mk, 4, true, [&](int ks) { return desc_mn(sbase + OFF_VL, ks, kC); }, b_tu);
+      issue(tmem + TM_U, id_mk, 4, true, a_vh, [&](int ks) { return desc_k(sbase + OFF_TUL, ks, kC); });
       if (n + 1 < nchunks) request_raw(t0 + kC);
     }
     if (n + 1 < nchunks) raw_pending = true;
-    if (!wait_all(&V.bar, phase)) break;
+    if (!wait_all(&V.bar_w, ph_w)) break;  // U^T runs on meanwhile
     // F: -W^T (lanes k, columns i) -> MN-major [k][i]
     if (warp < kTmemWarps) {
       float v[32];
@@ -728,9 +742,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
       fence_after();
       issue_ta(tmem + TM_U, tmem + TM_S16, id_km, 8, true, [&](int ks) { return desc_mn(sbase + OFF_NW, ks, kD); });
-      commit(&V.bar);
+      commit(&V.bar_d);
     }
-    if (!wait_all(&V.bar, phase)) break;
+    if (!wait_all(&V.bar_d, ph_d)) break;
     // H: Delta^T (lanes v, columns j) -> fp16 hi and lo pairs in TMEM
     if (warp < kTmemWarps) {
       float v[32];
@@ -747,14 +761,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_after();
       auto b_gk = [&](int ks) { return desc_mn(sbase + OFF_GK, ks, kC); };
       issue_ta(tmem + TM_O2, tmem + TM_KQ, id_kk, 4, false, [&](int ks) { return desc_k(sbase + OFF_M, ks, kC); });
+      commit(&V.bar_o);
       issue_ta(tmem + TM_S, tmem + TM_KQ, id_km128, 4, true, b_gk);
       issue_ta(tmem + TM_S, tmem + TM_KQ, id_km128, 4, true, [&](int ks) { return desc_mn(sbase + OFF_GKL, ks, kC); });
       issue_ta(tmem + TM_S, tmem + TM_KQ + 32, id_km128, 4, true, b_gk);
-      commit(&V.bar);
+      commit(&V.bar_s);
     }
-    if (!wait_all(&V.bar, phase)) break;
-    // J1: O^T = d (S Q^T) + Delta^T M^T -> staging [i][v]; S -> fp16 copy and
-    // rescaled state (or S_T after the last chunk), all in TMEM
+    if (!wait_all(&V.bar_o, ph_o)) break;  // the state update runs on meanwhile
+    // J1: O^T = d (S Q^T) + Delta^T M^T -> staging [i][v]
     if (warp < kTmemWarps) {
       float *ost = reinterpret_cast<float *>(sm + OFF_OST);
       float v[32], w2[32];
@@ -768,27 +782,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ost[(32 * half + q + 2) * kD + lrow] = fmaf(dq.z, v[q + 2], w2[q + 2]);
         ost[(32 * half + q + 3) * kD + lrow] = fmaf(dq.w, v[q + 3], w2[q + 3]);
       }
-      const bool last = n + 1 == nchunks;
-      const float dcn = V.dC_next;
-#pragma unroll
-      for (int p = 0; p < 2; ++p) {
-        const int k0 = 64 * half + 32 * p;
-        tmem_ld32(tl + TM_S + k0, v);
-        if (last) {
-          float4 *dst = reinterpret_cast<float4 *>(a.S_T + unit_off + (long long)lrow * kD + k0);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-        } else {
-          uint32_t w16[16];
-          pack_h16(v, w16);
-          tmem_st16w(tl + TM_S16 + k0 / 2, w16);
-#pragma unroll
-          for (int q = 0; q < 32; ++q) v[q] *= dcn;
-          tmem_st32(tl + TM_S + k0, v);
-        }
-      }
     }
-    fence_before();
     if (!wait_all(&V.bar_z, phase_z)) break;  // also the barrier after J1
     z_pending = false;
     // J2: gated RMSNorm per token, one warp per token, z from the staged rows
@@ -812,6 +806,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         st_io4(ob + i * ostride, y);
       }
     }
+    // J3: S -> fp16 copy and rescaled state (or S_T after the last chunk), in TMEM
+    if (!wait_all(&V.bar_s, ph_s)) break;
+    if (warp < kTmemWarps) {
+      const bool last = n + 1 == nchunks;
+      const float dcn = V.dC_next;
+      float v[32];
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+        const int k0 = 64 * half + 32 * p;
+        tmem_ld32(tl + TM_S + k0, v);
+        if (last) {
+          float4 *dst = reinterpret_cast<float4 *>(a.S_T + unit_off + (long long)lrow * kD + k0);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        } else {
+          uint32_t w16[16];
+          pack_h16(v, w16);
+          tmem_st16w(tl + TM_S16 + k0 / 2, w16);
+#pragma unroll
+          for (int q = 0; q < 32; ++q) v[q] *= dcn;
+          tmem_st32(tl + TM_S + k0, v);
+        }
+      }
+    }
+    fence_before();
     fence_smem_to_async();  // z and the staging were read: order before the next TMA writes
     __syncthreads();
     if (n + 1 < nchunks) {
@@ -822,10 +841,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   write_conv_T();
   // After an early exit, no requested copy may still be landing in shared
-  // memory when the CTA ends: wait (bounded) for any that was not consumed.
+  // memory, and no MMA still writing TMEM, when the CTA ends: wait (bounded)
+  // for any copy that was not consumed and for every MMA issued.
   if (tid == 0) {
     if (raw_pending) bar_wait(&V.bar_raw, phase_raw);
     if (z_pending) bar_wait(&V.bar_z, phase_z);
+    commit(&V.bar_end);
+    bar_wait(&V.bar_end, 0);
   }
   fence_before();
   __syncthreads();
