@@ -282,6 +282,22 @@ def gdn_prefill_varlen(qkv_pre, z, g, beta, conv_w, norm_w, cu_seqlens, S0=None,
     return {"o": o, "S_T": S_T, "conv_T": conv_T}
 
 
+def linear(x, w):
+    """The projections gdn.in_proj and gdn.out_proj of the page "Qwen3.8-27B"
+    (node table): y[t, n] = sum_k x[t, k] w[n, k], here in fp64 on the values
+    given (the weight in nn.Linear layout [N, K]).  numpy's matmul is the one
+    library step."""
+    return np.asarray(x, dtype=np.float64) @ np.asarray(w, dtype=np.float64).T
+
+
+# Columns of the in_proj output [T, 16480] at the 27B shape, in order:
+# qkv_pre (the 10240 conv channels), z (48 x 128), b (48), a (48).
+def in_proj_split(Hk=16, Hv=48, D=128):
+    C = conv_channels(Hk, Hv, D, D)
+    edges = np.cumsum([0, C, Hv * D, Hv, Hv])
+    return {name: (int(lo), int(hi)) for name, lo, hi in zip(("qkv_pre", "z", "b", "a"), edges[:-1], edges[1:])}
+
+
 def default_threads():
     try:
         return len(os.sched_getaffinity(0))

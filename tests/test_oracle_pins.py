@@ -555,3 +555,32 @@ def test_varlen_sequences_do_not_interact():
     np.testing.assert_array_equal(moved["S_T"][1:], base["S_T"][1:])
     np.testing.assert_array_equal(base["conv_T"][1, :2], p["conv0"][1, 1:])
     np.testing.assert_array_equal(base["conv_T"][1, 2], q["qkv_pre"][5])
+
+
+# ---------------------------------------------------------- projections ----
+def test_linear_brute_force_and_special_cases():
+    """y[t,n] = sum_k x[t,k] w[n,k]: a triple loop on a small case, the
+    identity weight, and a rank-one product."""
+    rng = _rng(50)
+    x, w = rng.normal(size=(3, 7)), rng.normal(size=(5, 7))
+    want = np.zeros((3, 5))
+    for t in range(3):
+        for n in range(5):
+            for k in range(7):
+                want[t, n] += x[t, k] * w[n, k]
+    np.testing.assert_allclose(O.linear(x, w), want, rtol=1e-14, atol=1e-14)
+    np.testing.assert_array_equal(O.linear(x, np.eye(7)), x)
+    u, v = rng.normal(size=4), rng.normal(size=6)
+    np.testing.assert_allclose(O.linear(u[:, None], v[:, None]), np.outer(u, v), rtol=1e-15)
+
+
+def test_in_proj_split_matches_the_spec(golden):
+    """The four column blocks of the 27B in_proj output fill N = 16480 and
+    have the widths the spec's tensor table gives the next nodes."""
+    G = golden("projection_shapes.txt")
+    sp = O.in_proj_split(16, int(G["v_heads"][0]), int(G["head_dim"][0]))
+    assert sp["qkv_pre"] == (0, int(G["conv_channels"][0]))
+    assert sp["z"][1] - sp["z"][0] == G["v_heads"][0] * G["head_dim"][0]
+    assert sp["b"][1] - sp["b"][0] == G["v_heads"][0] == sp["a"][1] - sp["a"][0]
+    assert sp["a"][1] == G["in_proj"][2]
+    assert G["out_proj"][0] == G["v_heads"][0] * G["head_dim"][0]
