@@ -582,5 +582,5 @@ def test_in_proj_split_matches_the_spec(golden):
     assert sp["qkv_pre"] == (0, int(G["conv_channels"][0]))
     assert sp["z"][1] - sp["z"][0] == G["v_heads"][0] * G["head_dim"][0]
     assert sp["b"][1] - sp["b"][0] == G["v_heads"][0] == sp["a"][1] - sp["a"][0]
-    assert sp["a"][1] == G["in_proj"][2]
-    assert G["out_proj"][0] == G["v_heads"][0] * G["head_dim"][0]
+    assert sp["a"][1] == G["in_proj"][3]
+    assert G["out_proj"][1] == G["v_heads"][0] * G["head_dim"][0]
