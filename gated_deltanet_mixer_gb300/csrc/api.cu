@@ -265,6 +265,52 @@ gdn_status gdn_decode_ex(const gdn_shape *shape, const gdn_decode_io *io, void *
   return decode_impl(shape, io, stream);
 }
 
+gdn_status gdn_linear(int M, int N, int K, const void *x, long long ldx, const void *w, long long ldw,
+                      int n_out, const gdn_linear_out *out, void *stream) {
+  if (M < 1 || N < 1 || K < 1 || !x || !w || !out || n_out < 1 || n_out > gdn::kGemmMaxOut)
+    return GDN_ERR_INVALID_ARG;
+  if (ldx < K || ldw < K) return GDN_ERR_INVALID_ARG;
+  if (M > (1 << 30) || N > (1 << 30) || K > (1 << 30) || ldx > (1LL << 32) || ldw > (1LL << 32))
+    return GDN_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(x) || !aligned16(w) || (ldx % 8) != 0 || (ldw % 8) != 0) return GDN_ERR_ALIGNMENT;
+  gdn::GemmArgs a{};
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.x = x;
+  a.w = w;
+  a.ldx = ldx;
+  a.ldw = ldw;
+  a.n_out = n_out;
+  const Range rx = range_of(x, (size_t)(M - 1) * ldx * 2 + (size_t)K * 2);
+  const Range rw = range_of(w, (size_t)(N - 1) * ldw * 2 + (size_t)K * 2);
+  Range ro[gdn::kGemmMaxOut];
+  for (int o = 0; o < n_out; ++o) {
+    const gdn_linear_out &q = out[o];
+    if (!q.ptr || q.col_begin < 0 || q.col_end <= q.col_begin || q.col_end > N || q.ld < q.col_end - q.col_begin)
+      return GDN_ERR_INVALID_ARG;
+    for (int p = 0; p < o; ++p)
+      if (q.col_begin < out[p].col_end && out[p].col_begin < q.col_end) return GDN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(q.ptr) & 1u) != 0) return GDN_ERR_ALIGNMENT;
+    ro[o] = range_of(q.ptr, ((size_t)(M - 1) * q.ld + (size_t)(q.col_end - q.col_begin)) * 2);
+    if (overlap(ro[o], rx) || overlap(ro[o], rw)) return GDN_ERR_ALIAS;
+    for (int p = 0; p < o; ++p)
+      if (overlap(ro[o], ro[p])) return GDN_ERR_ALIAS;
+    a.out[o] = gdn::GemmOut{q.col_begin, q.col_end, q.ptr, q.ld,
+                            aligned16(q.ptr) && (q.ld % 8) == 0 && (q.col_begin % 8) == 0 ? 1 : 0};
+  }
+  unsigned int *err = nullptr;
+  gdn_status st = check_device(&err);
+  if (st != GDN_OK) return st;
+  a.err = err;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    return GDN_ERR_CUDA;
+  cudaError_t e = gdn::launch_gemm(a, sms, (cudaStream_t)stream);
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
 gdn_status gdn_selftest_wait_timeout(int wait_us, void *stream) {
   if (wait_us < 1 || wait_us > 1000000) return GDN_ERR_INVALID_ARG;
   unsigned int *err = nullptr;

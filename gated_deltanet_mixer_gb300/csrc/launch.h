@@ -58,10 +58,29 @@ struct DecodeArgs {
   unsigned int *err;
 };
 
+// y[t, n] = sum_k x[t, k] w[n, k] (bf16 x [M][ldx], w [N][ldw]); columns
+// [col_begin, col_end) of y go to out[o].ptr[row * ld + col - col_begin].
+struct GemmOut {
+  int col_begin, col_end;
+  void *ptr;
+  long long ld;
+  int vec_ok;  // 16-byte stores allowed (ptr, ld and col_begin aligned)
+};
+constexpr int kGemmMaxOut = 4;
+struct GemmArgs {
+  int M, N, K;
+  const void *x, *w;
+  long long ldx, ldw;
+  int n_out;
+  GemmOut out[kGemmMaxOut];
+  unsigned int *err;
+};
+
 // Each returns the cudaGetLastError() of its launch.
 cudaError_t launch_decode(const DecodeArgs &a, bool bf16, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillArgs &a, bool bf16, cudaStream_t s);          // token-serial
 cudaError_t launch_prefill_chunked(const PrefillArgs &a, bool bf16, cudaStream_t s);  // chunked WY, tcgen05
+cudaError_t launch_gemm(const GemmArgs &a, int num_sms, cudaStream_t s);
 cudaError_t launch_wait_selftest(unsigned int *err, unsigned long long limit_ns, cudaStream_t s);
 
 // Device error bits (the error word is OR-ed).

@@ -48,6 +48,7 @@
 
 #include "gdn_device.cuh"
 #include "launch.h"
+#include "tma_host.h"
 #include "umma.cuh"
 
 namespace gdn {
@@ -599,6 +600,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // All threads: wait on an mbarrier phase; a uniform decision to abort.
   auto wait_all = [&](uint64_t *bar, uint32_t &ph) -> bool {
+    // Reconverge first: lane 0 of warp 0 issues the MMAs and TMA copies, and
+    // while its 31 sibling lanes sat in the polling loop (each try_wait may
+    // suspend the warp for a while) that lane lost about a microsecond.
+    __syncwarp();
     bool ok = bar_wait(bar, ph);
     ph ^= 1u;
     fence_after();
@@ -855,23 +860,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-}
-
-// cuTensorMapEncodeTiled, found once through the runtime (no libcuda link).
-using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                 const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-EncodeTiled encoder() {
-  static EncodeTiled fn = nullptr;
-  if (!fn) {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiled>(p);
-  }
-  return fn;
 }
 
 // A [B][T][width] bf16 tensor as a 3-d map with boxes of 128 columns x `rows` rows.

@@ -48,6 +48,10 @@ class gdn_prefill_io(ctypes.Structure):
                                   "conv0", "o", "S_T", "conv_T", "cu_seqlens", "S_snap")]
 
 
+class gdn_linear_out(ctypes.Structure):
+    _fields_ = [("col_begin", ctypes.c_int), ("col_end", ctypes.c_int), ("ptr", vp), ("ld", ctypes.c_longlong)]
+
+
 class gdn_decode_io(ctypes.Structure):
     _fields_ = [(n, vp) for n in ("qkv_pre", "z", "g", "beta", "raw_gates", "conv_w", "norm_w", "S",
                                   "S_snap", "conv_in", "conv_out", "o")]
@@ -79,6 +83,9 @@ def lib():
         L.gdn_prefill_ex.argtypes = [ctypes.POINTER(gdn_shape), ctypes.POINTER(gdn_prefill_io), vp]
         L.gdn_decode_ex.restype = ctypes.c_int
         L.gdn_decode_ex.argtypes = [ctypes.POINTER(gdn_shape), ctypes.POINTER(gdn_decode_io), vp]
+        L.gdn_linear.restype = ctypes.c_int
+        L.gdn_linear.argtypes = [ctypes.c_int] * 3 + [vp, ctypes.c_longlong, vp, ctypes.c_longlong, ctypes.c_int,
+                                                      ctypes.POINTER(gdn_linear_out), vp]
         L.gdn_selftest_wait_timeout.restype = ctypes.c_int
         L.gdn_selftest_wait_timeout.argtypes = [ctypes.c_int, vp]
         _lib = L
@@ -204,6 +211,23 @@ def gdn_decode_ex(qkv_pre, z, g, beta, conv_w, norm_w, S, conv_in, conv_out, o, 
     st = lib().gdn_decode_ex(ctypes.byref(sh), ctypes.byref(io), _stream(stream))
     if st != GDN_OK:
         raise GdnError(st, "gdn_decode_ex")
+
+
+def gdn_linear(x, w, outs, stream=None):
+    """y = x w^T for bf16 x [M, K] and w [N, K] (row strides may exceed K);
+    ``outs`` lists (col_begin, col_end, tensor) with tensor a bf16 [M, >=
+    col_end - col_begin] view (row stride from the tensor) receiving those
+    columns of y."""
+    M, K = x.shape
+    N, K2 = w.shape
+    if K2 != K:
+        raise ValueError("x and w disagree on K")
+    arr = (gdn_linear_out * len(outs))(*[gdn_linear_out(int(b), int(e), _ptr(t), int(t.stride(0)))
+                                         for b, e, t in outs])
+    st = lib().gdn_linear(M, N, K, _ptr(x), int(x.stride(0)), _ptr(w), int(w.stride(0)), len(outs), arr,
+                          _stream(stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_linear")
 
 
 def gdn_device_status(stream=None, reset=False):

@@ -251,3 +251,10 @@ def packed_problem(lengths, Hk, Hv, io="bf16", case=0, g_mu=3.0, state=True, raw
     a["S0"] = _normal(base + 7, (B, Hv, Dv, Dk), std=0.02) if state else None
     a["conv0"] = _normal(base + 8, (B, 3, C), io=io) if state else None
     return p
+
+
+def linear_problem(M, N, K, case=0, w_std=0.02):
+    """Inputs of one projection: x ~ N(0, 1) [M, K] and w ~ N(0, w_std^2)
+    [N, K], both bf16-rounded (tensor ids 13, 14)."""
+    base = 1000 * case
+    return _normal(base + 13, (M, K), io="bf16"), _normal(base + 14, (N, K), std=w_std, io="bf16")

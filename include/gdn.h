@@ -203,6 +203,31 @@ typedef struct {
 gdn_status gdn_decode_ex(const gdn_shape *shape, const gdn_decode_io *io, void *stream);
 
 /*
+ * The projections around the mixer, nodes gdn.in_proj (K=5120 -> N=16480)
+ * and gdn.out_proj (K=6144 -> N=5120) of the page "Qwen3.8-27B":
+ *   y[t, n] = sum_k x[t, k] w[n, k],   t < M, n < N, k < K
+ * bf16 inputs, fp32 accumulation on the tensor cores, bf16 outputs.  The
+ * pages give the formula; the column routing is this library's: columns
+ * [col_begin, col_end) of y are written to ptr[t * ld + (n - col_begin)],
+ * so the in_proj output can land directly in the mixer's qkv_pre, z, b and a
+ * buffers (columns 0-10239, 10240-16383, 16384-16431, 16432-16479 at the 27B
+ * shape).
+ *   x   [M][ldx] bf16, ldx >= K       w [N][ldw] bf16 (nn.Linear layout), ldw >= K
+ *   ldx, ldw multiples of 8 (16-byte rows); x, w 16-byte aligned
+ *   out[0 .. n_out-1], 1 <= n_out <= 4: disjoint column ranges inside [0, N),
+ *   ld >= col_end - col_begin; output rows must not overlap x, w or each other
+ * Columns not covered by any range are computed and dropped.
+ */
+typedef struct {
+  int col_begin, col_end;
+  void *ptr;
+  long long ld;
+} gdn_linear_out;
+
+gdn_status gdn_linear(int M, int N, int K, const void *x, long long ldx, const void *w, long long ldw,
+                      int n_out, const gdn_linear_out *out, void *stream);
+
+/*
  * Synchronise `stream` and report device-side failures recorded since the
  * last reset: GDN_ERR_TIMEOUT if a kernel's bounded wait gave up (the kernel
  * then returned early and its outputs are incomplete), GDN_ERR_INVALID_ARG

@@ -161,3 +161,15 @@ def test_extended_entry_points_check_on_host(L):
     assert decode_ex(L, shape(T=4), S_snap=fake(6, 256)) == 4  # snapshots over the state
     assert decode_ex(L, shape(T=4), conv_out=fake(7)) == 4
     assert prefill_ex(L, shape(T=1 << 29, B=4)) == 2        # token rows beyond 2^30
+
+
+def test_linear_checked_on_host(L):
+    out = (gdn.gdn_linear_out * 2)(gdn.gdn_linear_out(0, 8, fake(2), 8), gdn.gdn_linear_out(8, 16, fake(3), 8))
+    assert L.gdn_linear(0, 16, 64, fake(0), 64, fake(1), 64, 2, out, None) == 1
+    assert L.gdn_linear(4, 16, 64, fake(0), 32, fake(1), 64, 2, out, None) == 1   # ldx < K
+    assert L.gdn_linear(4, 16, 64, fake(0), 68, fake(1), 64, 2, out, None) == 3   # row stride not 16 bytes
+    assert L.gdn_linear(4, 16, 64, fake(0, 8), 64, fake(1), 64, 2, out, None) == 3
+    assert L.gdn_linear(4, 12, 64, fake(0), 64, fake(1), 64, 2, out, None) == 1   # range past N
+    assert L.gdn_linear(4, 16, 64, fake(0), 64, fake(1), 64, 5, out, None) == 1   # too many outputs
+    bad = (gdn.gdn_linear_out * 1)(gdn.gdn_linear_out(0, 8, fake(0, 64), 8))
+    assert L.gdn_linear(4, 16, 64, fake(0), 64, fake(1), 64, 1, bad, None) == 4  # output over x
