@@ -12,7 +12,8 @@ Workloads (synthetic, seeded; see gated_deltanet_mixer_gb300/inputs.py):
            the gates formed from raw projections, a packed batch of 24
            sequences (log-uniform lengths 100..4000), and 4-token decoding
            from the cache at the 27B decode shape with and without per-token
-           state snapshots.
+           state snapshots; and the 27B in_proj / out_proj projections
+           (gdn_linear, 8192 tokens) against the bf16 tensor peak.
 
 --impl reference times the fp64 CPU oracle instead, on a bounded sample of the
 same prefill workload, with the same metric and unit.
@@ -545,6 +546,31 @@ def next_rows(args, x, o, S_T, conv_T, p, peaks, peak_src, stream, barrier, worl
             "roofline": {"bound": "hbm", "achieved": nb / (ms * 1e-3) / 1e9, "peak": hbm,
                          "unit": "GB/s", "frac": nb / (ms * 1e-3) / 1e9 / hbm,
                          "peak_source": peak_src}}
+    del S, snap, conv_in, conv_out, tq, tz, tg, tb, od
+
+    # the projections around the mixer at the 27B shape, 8192 tokens
+    Tp = 8192
+    for name, K, N, split in (("in_proj", 5120, 16480, True), ("out_proj", 6144, 5120, False)):
+        xa, wa = I.linear_problem(Tp, N, K, case=80 + (name == "out_proj") + 1000 * rank)
+        x_, w_ = dev(xa, bf), dev(wa, bf)
+        if split:  # straight into the mixer's input buffers: qkv_pre | z | b | a
+            edges = np.cumsum([0, conv_channels(16, 48), 48 * D, 48, 48])
+            outs = [(int(lo), int(hi), torch.empty(Tp, int(hi - lo), device="cuda", dtype=bf))
+                    for lo, hi in zip(edges[:-1], edges[1:])]
+        else:
+            outs = [(0, N, torch.empty(Tp, N, device="cuda", dtype=bf))]
+        ms = time_launches(lambda: gdn.gdn_linear(x_, w_, outs, stream=stream), steps, args.warmup,
+                           stream, barrier)
+        fl = 2.0 * Tp * N * K
+        tf = fl / (ms * 1e-3) / 1e12
+        out["linear_" + name] = {
+            "workload": "27B %s: %d tokens, K=%d, N=%d, bf16 in/out, fp32 accumulation%s"
+                        % (name, Tp, K, N, ", output split into qkv_pre|z|b|a" if split else ""),
+            "value": world * tf, "unit": "TFLOP/s", "ms_per_launch": ms,
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"],
+                         "peak_source": peak_src + " bf16_tflops (burst)"}}
+        del x_, w_, outs
     if gdn.gdn_device_status(stream) != 0:
         raise RuntimeError("device status not OK after the extended calls")
     return out
