@@ -2,6 +2,7 @@
 
     python -m gated_deltanet_mixer_gb300.profile_cases decode --B 48 --calls 3
     python -m gated_deltanet_mixer_gb300.profile_cases prefill --B 1 --T 2048 --calls 2
+    python -m gated_deltanet_mixer_gb300.profile_cases linear --T 2048 --K 5120 --N 16480 --calls 2
 
 Inputs are the seeded synthetic ones of ``inputs.py``; each case is sized so
 that its working set is larger than L2 (129 MB) but only a few GB at most.
@@ -42,18 +43,30 @@ def prefill(B, T, Hk, Hv, calls):
         gdn.gdn_prefill(*x, o, S_T, conv_T, Hk=Hk, Hv=Hv)
 
 
+def linear(T, K, N, calls):
+    xa, wa = I.linear_problem(T, N, K, case=202)
+    x, w = _dev(xa, torch.bfloat16), _dev(wa, torch.bfloat16)
+    y = torch.empty(T, N, device="cuda", dtype=torch.bfloat16)
+    for _ in range(calls):
+        gdn.gdn_linear(x, w, [(0, N, y)])
+
+
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("kernel", choices=["decode", "prefill"])
+    ap.add_argument("kernel", choices=["decode", "prefill", "linear"])
     ap.add_argument("--B", type=int, default=None)
     ap.add_argument("--T", type=int, default=2048)
     ap.add_argument("--Hk", type=int, default=16)
     ap.add_argument("--Hv", type=int, default=None)
+    ap.add_argument("--K", type=int, default=5120)
+    ap.add_argument("--N", type=int, default=16480)
     ap.add_argument("--calls", type=int, default=3)
     a = ap.parse_args()
     gdn.lib()
     if a.kernel == "decode":
         decode(a.B or 48, a.Hk, a.Hv or 48, a.calls)
+    elif a.kernel == "linear":
+        linear(a.T, a.K, a.N, a.calls)
     else:
         prefill(a.B or 4, a.T, a.Hk, a.Hv or 32, a.calls)
     torch.cuda.synchronize()
