@@ -81,13 +81,13 @@ constexpr uint32_t OFF_VEC = OFF_Z + kC * kD * 2;     // per-token vectors, flag
 // Scratch that lives only between two uses of the tiles it overlays:
 constexpr int kLs = 68;                              // padded row stride of L (floats)
 constexpr uint32_t OFF_L = OFF_RAW;                  // L fp32 [64][68], phases C-D
-constexpr uint32_t OFF_PB = OFF_RAW + 64 * kLs * 4;  // block products fp32 [3][16][16], phase D
+constexpr uint32_t OFF_PB = OFF_RAW + 64 * kLs * 4;  // block products fp32 [32][32], phase D
 constexpr uint32_t OFF_TF = OFF_NW;                  // T fp32 [64][64], phase D
 constexpr uint32_t OFF_OST = OFF_VH;                 // O^T staging fp32 [64][128] (VH + VL), phase J
 constexpr uint32_t kVecBytes = 2560;
 constexpr uint32_t kSmemUsed = OFF_VEC + kVecBytes;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // + alignment slack
-static_assert(OFF_PB + 3 * 256 * 4 <= OFF_Z, "solve scratch fits in the raw rows");
+static_assert(OFF_PB + 32 * 32 * 4 <= OFF_Z, "solve scratch fits in the raw rows");
 static_assert(OFF_RAW % 128 == 0 && OFF_Z % 128 == 0 && kRawBlock % 128 == 0, "TMA destinations");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
@@ -338,16 +338,48 @@ __device__ __forceinline__ void fma4(float4 &acc, float s, const float4 t) {
   acc.w = fmaf(s, t.w, acc.w);
 }
 
-// D: T = (I + L)^{-1} in 16 x 16 blocks.  The diagonal blocks by forward
-// substitution, one column per thread; then, block row by block row,
-// T_IJ = -T_II sum_{K=J}^{I-1} L_IK T_KJ, each thread one row and four
-// columns of a block (16-byte shared loads).  fp32 throughout; the result is
-// written as the fp16 K-major tiles T diag(beta) (hi, lo) and T diag(beta d).
-// L is [64][kLs] (padded rows), T is [64][64] swizzled (tfi).
+// Row i, columns j .. j+3 (j % 4 == 0) of T -> the fp16 K-major tiles
+// T diag(beta) (hi, lo) and T diag(beta d), one 8-byte store each.
+__device__ __forceinline__ void store_T4(uint8_t *sm, const Vecs &V, int i, int j, float4 t) {
+  const float4 b = ld4(V.beta + j), e = ld4(V.bd + j);
+  uint32_t hw[2], lw[2], ww[2];
+  split2(t.x * b.x, t.y * b.y, hw[0], lw[0]);
+  split2(t.z * b.z, t.w * b.w, hw[1], lw[1]);
+  __half2 w0 = __halves2half2(to_h(t.x * e.x), to_h(t.y * e.y));
+  __half2 w1 = __halves2half2(to_h(t.z * e.z), to_h(t.w * e.w));
+  ww[0] = *reinterpret_cast<uint32_t *>(&w0);
+  ww[1] = *reinterpret_cast<uint32_t *>(&w1);
+  const uint32_t o = kmaj(i, j, kC);
+  *reinterpret_cast<uint2 *>(sm + OFF_TU + o) = make_uint2(hw[0], hw[1]);
+  *reinterpret_cast<uint2 *>(sm + OFF_TUL + o) = make_uint2(lw[0], lw[1]);
+  *reinterpret_cast<uint2 *>(sm + OFF_TW + o) = make_uint2(ww[0], ww[1]);
+}
+
+// The fp16 T tiles are zero above the block diagonal (16 x 16 blocks) in
+// every chunk: written once, before the first chunk.
+__device__ void zero_T_upper(uint8_t *sm, int tid) {
+  for (int q = tid; q < 3 * 6 * 32; q += kThreads) {
+    const int tile = q / 192, rem = q % 192, blk = rem / 32, w = rem % 32;
+    const int I = blk < 3 ? 0 : blk < 5 ? 1 : 2;
+    const int J = blk < 3 ? blk + 1 : blk < 5 ? blk - 1 : 3;
+    const int i = 16 * I + (w >> 1), j = 16 * J + 8 * (w & 1);
+    const uint32_t off = tile == 0 ? OFF_TU : tile == 1 ? OFF_TUL : OFF_TW;
+    *reinterpret_cast<uint4 *>(sm + off + kmaj(i, j, kC)) = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// D: T = (I + L)^{-1} (L strictly lower, 64 x 64), fp32, by recursive
+// doubling on 16 x 16 blocks: the four diagonal blocks by forward
+// substitution (one column per thread); the two 32 x 32 halves by
+// T_BA = -T_BB (L_BA T_AA); then the whole by the same identity on the
+// 32 x 32 halves.  Threads idle in a product convert the blocks already
+// final into the fp16 tiles meanwhile; the last product converts its own.
+// L is [64][kLs] (padded rows), T is [64][64] swizzled (tfi); blocks above
+// the diagonal of T are never written (and never read).
 __device__ void solve_T(uint8_t *sm, const Vecs &V, int tid) {
   const float *L = reinterpret_cast<const float *>(sm + OFF_L);
   float *Tf = reinterpret_cast<float *>(sm + OFF_TF);
-  float *P = reinterpret_cast<float *>(sm + OFF_PB);  // [3][16][16]
+  float *P = reinterpret_cast<float *>(sm + OFF_PB);  // [2][16][16], then [32][32]
   if (tid < kC) {
     const int base = 16 * (tid >> 4), c = tid & 15;
     const float *Lb = L + base * kLs + base;
@@ -371,61 +403,73 @@ __device__ void solve_T(uint8_t *sm, const Vecs &V, int tid) {
     for (int i = 0; i < 16; ++i) Tf[tfi(base + i, base + c)] = xv[i];
   }
   __syncthreads();
-#pragma unroll 1
-  for (int I = 1; I < 4; ++I) {
-    // work item e < 64 I: block J = e / 64, row r, column group c4
-    const int e = tid, J = e >> 6, r = (e >> 2) & 15, c4 = e & 3;
-    const bool active = e < 64 * I;
-    if (active) {
-      const float *Lr = L + (16 * I + r) * kLs;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int K = J; K < I; ++K) {
+  // The 32 x 32 halves (A, B) = (0, 1), (2, 3): P = L_BA T_AA, T_BA = -T_BB P.
+  const int h = tid >> 6, r16 = (tid >> 2) & 15, c4 = tid & 3;
+  const int A = 2 * h, Bb = A + 1;
+  if (tid < 128) {
+    const float *Lr = L + (16 * Bb + r16) * kLs + 16 * A;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int k4 = 0; k4 < 16; k4 += 4) {
-          const float4 l = ld4(Lr + 16 * K + k4);
-          const int row = 16 * K + k4, col = 16 * J + 4 * c4;
-          fma4(acc, l.x, ld4(Tf + tfi(row + 0, col)));
-          fma4(acc, l.y, ld4(Tf + tfi(row + 1, col)));
-          fma4(acc, l.z, ld4(Tf + tfi(row + 2, col)));
-          fma4(acc, l.w, ld4(Tf + tfi(row + 3, col)));
-        }
-      }
-      *reinterpret_cast<float4 *>(P + J * 256 + r * 16 + 4 * c4) = acc;
+    for (int k4 = 0; k4 < 16; k4 += 4) {
+      const float4 l = ld4(Lr + k4);
+      const int row = 16 * A + k4, col = 16 * A + 4 * c4;
+      fma4(acc, l.x, ld4(Tf + tfi(row + 0, col)));
+      fma4(acc, l.y, ld4(Tf + tfi(row + 1, col)));
+      fma4(acc, l.z, ld4(Tf + tfi(row + 2, col)));
+      fma4(acc, l.w, ld4(Tf + tfi(row + 3, col)));
     }
-    __syncthreads();
-    if (active) {
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      const int row = 16 * I + r;
-#pragma unroll
-      for (int k4 = 0; k4 < 16; k4 += 4) {
-        const float4 t = ld4(Tf + tfi(row, 16 * I + k4));
-        fma4(acc, t.x, ld4(P + J * 256 + (k4 + 0) * 16 + 4 * c4));
-        fma4(acc, t.y, ld4(P + J * 256 + (k4 + 1) * 16 + 4 * c4));
-        fma4(acc, t.z, ld4(P + J * 256 + (k4 + 2) * 16 + 4 * c4));
-        fma4(acc, t.w, ld4(P + J * 256 + (k4 + 3) * 16 + 4 * c4));
-      }
-      *reinterpret_cast<float4 *>(Tf + tfi(row, 16 * J + 4 * c4)) =
-          make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-    }
-    __syncthreads();
+    *reinterpret_cast<float4 *>(P + h * 256 + r16 * 16 + 4 * c4) = acc;
+  } else {  // the diagonal blocks are final
+    const int q = tid - 128, b = q >> 6, row = 16 * b + ((q >> 2) & 15), col = 16 * b + 4 * (q & 3);
+    store_T4(sm, V, row, col, ld4(Tf + tfi(row, col)));
   }
-  // fp16 tiles: 512 chunks of 8 each, two per thread (256 threads); blocks above the diagonal are zero
-  if (tid < 256) {
-#pragma unroll 1
-    for (int m = 0; m < 2; ++m) {
-      const int q = tid + 256 * m, i = q >> 3, j0 = (q & 7) * 8;
-      const bool below = (j0 >> 4) <= (i >> 4);
-      const float4 t0 = below ? ld4(Tf + tfi(i, j0)) : make_float4(0.f, 0.f, 0.f, 0.f);
-      const float4 t1 = below ? ld4(Tf + tfi(i, j0 + 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
-      const float4 b0 = ld4(V.beta + j0), b1 = ld4(V.beta + j0 + 4);
-      const float4 e0 = ld4(V.bd + j0), e1 = ld4(V.bd + j0 + 4);
-      const float tb[8] = {t0.x * b0.x, t0.y * b0.y, t0.z * b0.z, t0.w * b0.w,
-                           t1.x * b1.x, t1.y * b1.y, t1.z * b1.z, t1.w * b1.w};
-      const float tw[8] = {t0.x * e0.x, t0.y * e0.y, t0.z * e0.z, t0.w * e0.w,
-                           t1.x * e1.x, t1.y * e1.y, t1.z * e1.z, t1.w * e1.w};
-      st_h8_split(sm + OFF_TU + kmaj(i, j0, kC), sm + OFF_TUL + kmaj(i, j0, kC), tb);
-      st_h8(sm + OFF_TW + kmaj(i, j0, kC), tw);
+  __syncthreads();
+  if (tid < 128) {
+    const int row = 16 * Bb + r16;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k4 = 0; k4 < 16; k4 += 4) {
+      const float4 t = ld4(Tf + tfi(row, 16 * Bb + k4));
+      fma4(acc, t.x, ld4(P + h * 256 + (k4 + 0) * 16 + 4 * c4));
+      fma4(acc, t.y, ld4(P + h * 256 + (k4 + 1) * 16 + 4 * c4));
+      fma4(acc, t.z, ld4(P + h * 256 + (k4 + 2) * 16 + 4 * c4));
+      fma4(acc, t.w, ld4(P + h * 256 + (k4 + 3) * 16 + 4 * c4));
     }
+    *reinterpret_cast<float4 *>(Tf + tfi(row, 16 * A + 4 * c4)) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+  }
+  __syncthreads();
+  // The whole: P = L[32:64][0:32] T[0:32][0:32], T[32:64][0:32] = -T[32:64][32:64] P.
+  const int r32 = tid >> 3, col = 4 * (tid & 7);
+  if (tid < 256) {
+    const float *Lr = L + (32 + r32) * kLs;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 2
+    for (int k4 = col >= 16 ? 16 : 0; k4 < 32; k4 += 4) {  // T[0:16][16:32] is zero
+      const float4 l = ld4(Lr + k4);
+      fma4(acc, l.x, ld4(Tf + tfi(k4 + 0, col)));
+      fma4(acc, l.y, ld4(Tf + tfi(k4 + 1, col)));
+      fma4(acc, l.z, ld4(Tf + tfi(k4 + 2, col)));
+      fma4(acc, l.w, ld4(Tf + tfi(k4 + 3, col)));
+    }
+    *reinterpret_cast<float4 *>(P + r32 * 32 + col) = acc;
+  } else {  // the blocks T_10 and T_32 are final
+    const int q = tid - 256, hh = q >> 6;
+    const int row = 16 * (2 * hh + 1) + ((q >> 2) & 15), cc = 32 * hh + 4 * (q & 3);
+    store_T4(sm, V, row, cc, ld4(Tf + tfi(row, cc)));
+  }
+  __syncthreads();
+  if (tid < 256) {
+    const int row = 32 + r32;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 2
+    for (int k4 = 0; k4 < (r32 < 16 ? 16 : 32); k4 += 4) {  // T[32:48][48:64] is zero
+      const float4 t = ld4(Tf + tfi(row, 32 + k4));
+      fma4(acc, t.x, ld4(P + (k4 + 0) * 32 + col));
+      fma4(acc, t.y, ld4(P + (k4 + 1) * 32 + col));
+      fma4(acc, t.z, ld4(P + (k4 + 2) * 32 + col));
+      fma4(acc, t.w, ld4(P + (k4 + 3) * 32 + col));
+    }
+    store_T4(sm, V, row, col, make_float4(-acc.x, -acc.y, -acc.z, -acc.w));
   }
 }
 
@@ -537,6 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     V.abort = 0;
   }
   if (warp == 0) tmem_alloc(&V.tmem, kTmemCols);
+  zero_T_upper(sm, tid);
   float g_cur[2], b_cur[2], g_nxt[2] = {0.f, 0.f}, b_nxt[2] = {0.f, 0.f};  // warp 11: this and the next chunk
   float neg_exp_A = 0.f, dt_bias = 0.f;          // warp 11, raw gates: -exp(A_log[h]), dt_bias[h]
   if (warp == 11) {
