@@ -250,20 +250,14 @@ __device__ __forceinline__ void st_h8_split_pairs(uint8_t *phi, uint8_t *plo, co
   *reinterpret_cast<uint4 *>(plo) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
 }
 
-// A: front end for one chunk, from the staged raw rows (row r of a block is
-// token t0 - 3 + r).  All 12 warps: warp w handles block w / 4 (q, k, v), two
-// 8-token eighths (one per half-warp) and, per lane, one 8-channel group, and
-// slides the conv window over its 8 tokens.  Every warp runs the same code;
-// what differs per block (norm, outputs) is warp-uniform data.
+// One front-end pass: block blk (0 q, 1 k, 2 v) for tokens r0 .. r0+ntok-1 of
+// the chunk (row r of a staged block is token t0 - 3 + r), one 8-channel
+// group per lane, sliding the conv window over the tokens; the L2 norm sums
+// over the 16 lanes of a half-warp, which hold one token's 128 channels.
 // Writes: q^ and k^ (fp16) into [K;Q]; Gamma k^ (hi, lo); v (hi, lo).
-__device__ void front_end(uint8_t *sm, const Vecs &V, const Dims &d, const bf16 *conv_w,
-                          int h, int kh, int t0, int T, int tid) {
-  const int warp = tid >> 5, lane = tid & 31;
-  const int blk = warp >> 2, eighth = 2 * (warp & 3) + (lane >> 4), grp = lane & 15;
-  const long long c = blk == 0   ? (long long)kh * kD + 8 * grp
-                      : blk == 1 ? (long long)d.Hk * kD + (long long)kh * kD + 8 * grp
-                                 : 2LL * d.Hk * kD + (long long)h * kD + 8 * grp;
-  // warp-uniform output plan
+template <int NTOK>
+__device__ __forceinline__ void fe_pass(uint8_t *sm, const Vecs &V, const Dims &d, const bf16 *conv_w, int blk,
+                                        long long c, int r0, int t0, int T, int grp) {
   const bool has_norm = blk < 2, has_single = blk < 2, has_split = blk > 0, has_gamma = blk == 1;
   const int row_off = blk == 0 ? 64 : 0;
   const float scale = blk == 0 ? d.q_scale : 1.0f;
@@ -279,13 +273,12 @@ __device__ void front_end(uint8_t *sm, const Vecs &V, const Dims &d, const bf16 
     w[i][2] = make_float2(a0.z, a1.z);
     w[i][3] = make_float2(a0.w, a1.w);
   }
-  const int r0 = 8 * eighth;  // raw row of token t0 + 8 eighth - 3
   float2 x0[4], x1[4], x2[4];
   widen(*reinterpret_cast<const uint4 *>(raw + 256 * (r0 + 0)), x0);
   widen(*reinterpret_cast<const uint4 *>(raw + 256 * (r0 + 1)), x1);
   widen(*reinterpret_cast<const uint4 *>(raw + 256 * (r0 + 2)), x2);
 #pragma unroll 4
-  for (int tt = 0; tt < 8; ++tt) {
+  for (int tt = 0; tt < NTOK; ++tt) {
     const int row = r0 + tt;  // token index within the chunk
     const int t = t0 + row;
     float2 x3[4], u[4];
@@ -309,7 +302,7 @@ __device__ void front_end(uint8_t *sm, const Vecs &V, const Dims &d, const bf16 
       ss2 = make_float2(0.f, 0.f);
     }
     float ss = ss2.x + ss2.y;
-    // sum of squares over the 16 groups of this eighth: one half-warp
+    // sum of squares over the 16 groups of this token: one half-warp
 #pragma unroll
     for (int off = 1; off < 16; off <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
     const float f = has_norm ? rsqrtf(ss + d.eps_l2) * scale : 1.0f;
@@ -323,6 +316,23 @@ __device__ void front_end(uint8_t *sm, const Vecs &V, const Dims &d, const bf16 
       const uint32_t o = mnmaj(8 * grp, row, kC);
       st_h8_split_pairs(dhi + o, dlo + o, u);
     }
+  }
+}
+
+// A: front end for one chunk, from the staged raw rows.  Work per token is
+// about 78 (q), 127 (k: norm, single and split outputs) and 100 (v: split)
+// units, so warps 0-7 each take q and then k of 4 tokens per half-warp
+// (32 token groups of 4), and warps 8-11 take v of 8 tokens per half-warp.
+__device__ void front_end(uint8_t *sm, const Vecs &V, const Dims &d, const bf16 *conv_w,
+                          int h, int kh, int t0, int T, int tid) {
+  const int warp = tid >> 5, lane = tid & 31, grp = lane & 15;
+  if (warp < 8) {
+    const int r0 = 4 * (2 * warp + (lane >> 4));
+    fe_pass<4>(sm, V, d, conv_w, 0, (long long)kh * kD + 8 * grp, r0, t0, T, grp);
+    fe_pass<4>(sm, V, d, conv_w, 1, (long long)d.Hk * kD + (long long)kh * kD + 8 * grp, r0, t0, T, grp);
+  } else {
+    const int r0 = 8 * (2 * (warp - 8) + (lane >> 4));
+    fe_pass<8>(sm, V, d, conv_w, 2, 2LL * d.Hk * kD + (long long)h * kD + 8 * grp, r0, t0, T, grp);
   }
 }
 
