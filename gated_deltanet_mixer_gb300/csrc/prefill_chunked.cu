@@ -120,7 +120,9 @@ struct __align__(16) Vecs {  // per-token chunk vectors in shared memory
   uint64_t bar_d;    // MMA2, MMA4 done (Delta^T)
   uint64_t bar_o;    // MMA5, MMA6 done (S Q^T, Delta^T M^T)
   uint64_t bar_s;    // MMA7 done (state update)
-  uint64_t bar_end;  // every MMA issued, before TMEM is freed
+  uint64_t bar_sq;   // MMA5 done (S Q^T), issued by the second issuer
+  uint64_t bar_u;    // MMA2 done (U^T), issued by the second issuer
+  uint64_t bar_end;  // every MMA of both issuers, before TMEM is freed
   uint64_t bar_raw;  // raw rows landed
   uint64_t bar_z;    // z rows landed
 };
@@ -585,7 +587,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bar_init(&V.bar_d, 1);
     bar_init(&V.bar_o, 1);
     bar_init(&V.bar_s, 1);
-    bar_init(&V.bar_end, 1);
+    bar_init(&V.bar_sq, 1);
+    bar_init(&V.bar_u, 1);
+    bar_init(&V.bar_end, 2);
     bar_init(&V.bar_raw, 1);
     bar_init(&V.bar_z, 1);
     V.abort = 0;
@@ -645,7 +649,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // Each mbarrier completes once per chunk; its phase bit is tracked here.
-  uint32_t ph_qk = 0, ph_w = 0, ph_d = 0, ph_o = 0, ph_s = 0, phase_raw = 0, phase_z = 0;
+  uint32_t ph_qk = 0, ph_w = 0, ph_d = 0, ph_o = 0, ph_s = 0, ph_sq = 0, ph_u = 0, phase_raw = 0, phase_z = 0;
+  // MMAs off the critical path are issued by lane 0 of warp 11, idle in the
+  // phases where it issues them; the critical ones by thread 0.
+  const bool issuer2 = tid == kThreads - 32;
   bool raw_pending = true, z_pending = true;  // a requested TMA not yet consumed
   const int nchunks = (T + kC - 1) / kC;
   const uint32_t id_kk = idesc(128, 64, 0, 0);
@@ -704,16 +711,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     // A: front end
     front_end(sm, V, d, conv_w, h, kh, t0, T, tid);
     smem_ready();
-    // B: MMA1  [K;Q] K^T;  MMA5 S Q^T (Q^ = rows 64..127 of [K;Q], S from TMEM)
+    // B: MMA1  [K;Q] K^T
     if (tid == 0) {
       fence_after();
       issue(tmem + TM_KQ, id_kk, 8, false, [&](int ks) { return desc_k(sbase + OFF_KQ, ks, 128); },
             [&](int ks) { return desc_k(sbase + OFF_KQ, ks, 128); });
       commit(&V.bar_qk);
+    }
+    if (!wait_all(&V.bar_qk, ph_qk)) break;
+    // MMA5 S Q^T (Q^ = rows 64..127 of [K;Q], S from TMEM), needed only in J
+    if (issuer2) {
+      fence_after();
       issue_ta(tmem + TM_O1, tmem + TM_S16, id_kk, 8, false,
                [&](int ks) { return desc_k(sbase + OFF_KQ + 64 * 128, ks, 128); });
+      commit(&V.bar_sq);
     }
-    if (!wait_all(&V.bar_qk, ph_qk)) break;  // S Q^T runs on meanwhile
     // C: L (fp32, strictly lower, decayed beta K K^T) and M (fp16, decayed Q K^T incl. diagonal)
     if (warp < kTmemWarps) {
       float v[32], rr[32];
@@ -775,19 +787,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     // request the next chunk's.
     if (tid == 0) {
       fence_after();
-      auto a_vh = [&](int ks) { return desc_mn(sbase + OFF_VH, ks, kC); };
-      auto b_tu = [&](int ks) { return desc_k(sbase + OFF_TU, ks, kC); };
       issue(tmem + TM_W, id_mk, 4, false,
             [&](int ks) { return desc(sbase + OFF_KQ + (uint32_t)(ks * 2048), 128 * 128, 1024); },
             [&](int ks) { return desc_k(sbase + OFF_TW, ks, kC); });
       commit(&V.bar_w);
-      issue(tmem + TM_U, id_mk, 4, false, a_vh, b_tu);
-      issue(tmem + TM_U, id_mk, 4, true, [&](int ks) { return desc_mn(sbase + OFF_VL, ks, kC); }, b_tu);
-      issue(tmem + TM_U, id_mk, 4, true, a_vh, [&](int ks) { return desc_k(sbase + OFF_TUL, ks, kC); });
       if (n + 1 < nchunks) request_raw(t0 + kC);
     }
     if (n + 1 < nchunks) raw_pending = true;
-    if (!wait_all(&V.bar_w, ph_w)) break;  // U^T runs on meanwhile
+    if (!wait_all(&V.bar_w, ph_w)) break;
+    // MMA2 U^T, needed only by MMA4
+    if (issuer2) {
+      fence_after();
+      auto a_vh = [&](int ks) { return desc_mn(sbase + OFF_VH, ks, kC); };
+      auto b_tu = [&](int ks) { return desc_k(sbase + OFF_TU, ks, kC); };
+      issue(tmem + TM_U, id_mk, 4, false, a_vh, b_tu);
+      issue(tmem + TM_U, id_mk, 4, true, [&](int ks) { return desc_mn(sbase + OFF_VL, ks, kC); }, b_tu);
+      issue(tmem + TM_U, id_mk, 4, true, a_vh, [&](int ks) { return desc_k(sbase + OFF_TUL, ks, kC); });
+      commit(&V.bar_u);
+    }
     // F: -W^T (lanes k, columns i) -> MN-major [k][i]
     if (warp < kTmemWarps) {
       float v[32];
@@ -798,12 +815,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int q = 0; q < 4; ++q) st_h8(sm + OFF_NW + mnmaj(32 * half + 8 * q, lrow, kD), v + 8 * q);
     }
     smem_ready();
-    // G: MMA4 Delta^T = U^T - S W^T (S from TMEM)
+    // G: MMA4 Delta^T = U^T - S W^T (S from TMEM), after MMA2 (the other issuer)
     if (tid == 0) {
+      bar_wait(&V.bar_u, ph_u);  // bounded; a stall here ends in the timeout below
       fence_after();
       issue_ta(tmem + TM_U, tmem + TM_S16, id_km, 8, true, [&](int ks) { return desc_mn(sbase + OFF_NW, ks, kD); });
       commit(&V.bar_d);
     }
+    ph_u ^= 1u;
     if (!wait_all(&V.bar_d, ph_d)) break;
     // H: Delta^T (lanes v, columns j) -> fp16 hi and lo pairs in TMEM
     if (warp < kTmemWarps) {
@@ -818,16 +837,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     smem_ready();
     // I: MMA6 Delta^T M^T;  MMA7 S += Delta^T (Gamma K), hi*hi + hi*lo + lo*hi
     if (tid == 0) {
+      bar_wait(&V.bar_sq, ph_sq);  // MMA5 (the other issuer) done, so bar_o covers O1 and O2
       fence_after();
-      auto b_gk = [&](int ks) { return desc_mn(sbase + OFF_GK, ks, kC); };
       issue_ta(tmem + TM_O2, tmem + TM_KQ, id_kk, 4, false, [&](int ks) { return desc_k(sbase + OFF_M, ks, kC); });
       commit(&V.bar_o);
+    }
+    ph_sq ^= 1u;
+    if (!wait_all(&V.bar_o, ph_o)) break;
+    // MMA7, needed only in J3: the state update runs while O is normalised
+    if (issuer2) {
+      fence_after();
+      auto b_gk = [&](int ks) { return desc_mn(sbase + OFF_GK, ks, kC); };
       issue_ta(tmem + TM_S, tmem + TM_KQ, id_km128, 4, true, b_gk);
       issue_ta(tmem + TM_S, tmem + TM_KQ, id_km128, 4, true, [&](int ks) { return desc_mn(sbase + OFF_GKL, ks, kC); });
       issue_ta(tmem + TM_S, tmem + TM_KQ + 32, id_km128, 4, true, b_gk);
       commit(&V.bar_s);
     }
-    if (!wait_all(&V.bar_o, ph_o)) break;  // the state update runs on meanwhile
     // J1: O^T = d (S Q^T) + Delta^T M^T -> staging [i][v]
     if (warp < kTmemWarps) {
       float *ost = reinterpret_cast<float *>(sm + OFF_OST);
@@ -909,6 +934,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     commit(&V.bar_end);
     bar_wait(&V.bar_end, 0);
   }
+  if (issuer2) commit(&V.bar_end);  // the second issuer's MMAs (count 2)
   fence_before();
   __syncthreads();
   if (warp == 0) {
