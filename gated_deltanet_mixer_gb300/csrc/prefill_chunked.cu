@@ -831,8 +831,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t wh[16], wl[16];
 #pragma unroll
       for (int q = 0; q < 16; ++q) split2(v[2 * q], v[2 * q + 1], wh[q], wl[q]);
-      tmem_st16w(tl + TM_KQ + 16 * half, wh);
-      tmem_st16w(tl + TM_KQ + 32 + 16 * half, wl);
+      tmem_st16w_nw(tl + TM_KQ + 16 * half, wh);
+      tmem_st16w_nw(tl + TM_KQ + 32 + 16 * half, wl);
+      tmem_wait_st();
     }
     smem_ready();
     // I: MMA6 Delta^T M^T;  MMA7 S += Delta^T (Gamma K), hi*hi + hi*lo + lo*hi
@@ -856,9 +857,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // J1: O^T = d (S Q^T) + Delta^T M^T -> staging [i][v]
     if (warp < kTmemWarps) {
       float *ost = reinterpret_cast<float *>(sm + OFF_OST);
+      uint32_t ra[32], rb[32];
+      tmem_ld32_nw(tl + TM_O1 + 32 * half, ra);
+      tmem_ld32_nw(tl + TM_O2 + 32 * half, rb);
+      tmem_wait_ld();
       float v[32], w2[32];
-      tmem_ld32(tl + TM_O1 + 32 * half, v);
-      tmem_ld32(tl + TM_O2 + 32 * half, w2);
+#pragma unroll
+      for (int q = 0; q < 32; ++q) {
+        v[q] = __uint_as_float(ra[q]);
+        w2[q] = __uint_as_float(rb[q]);
+      }
 #pragma unroll
       for (int q = 0; q < 32; q += 4) {
         const float4 dq = ld4(V.d + 32 * half + q);
@@ -870,25 +878,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!wait_all(&V.bar_z, phase_z)) break;  // also the barrier after J1
     z_pending = false;
-    // J2: gated RMSNorm per token, one warp per token, z from the staged rows
+    // J2: gated RMSNorm per token, one half-warp per token (8 channels per
+    // lane), z from the staged rows
     {
       const float *ost = reinterpret_cast<const float *>(sm + OFF_OST);
-      const float4 w4 = ld_io4(static_cast<const bf16 *>(a.norm_w) + 4 * lane);
+      const int hl = lane & 15;
+      float2 wn[4];
+      widen(*reinterpret_cast<const uint4 *>(static_cast<const bf16 *>(a.norm_w) + 8 * hl), wn);
       const int nv = min(kC, T - t0);
-      bf16 *ob = static_cast<bf16 *>(a.o) + ((bos + t0) * d.Hv + h) * kD + 4 * lane;
+      bf16 *ob = static_cast<bf16 *>(a.o) + ((bos + t0) * d.Hv + h) * kD + 8 * hl;
       const long long ostride = (long long)d.Hv * kD;
-#pragma unroll 2
-      for (int i = warp; i < nv; i += kThreads / 32) {
-        const float4 o4 = reinterpret_cast<const float4 *>(ost + i * kD)[lane];
-        const float4 z4 = ld_io4(reinterpret_cast<const bf16 *>(sm + OFF_Z) + i * kD + 4 * lane);
-        const float rstd = rsqrtf(warp_sum(dot4(o4, o4)) * (1.0f / kD) + d.eps_norm);
-        const float2 s01 = silu2(make_float2(z4.x, z4.y)), s23 = silu2(make_float2(z4.z, z4.w));
-        float4 y;
-        y.x = w4.x * (o4.x * rstd) * s01.x;
-        y.y = w4.y * (o4.y * rstd) * s01.y;
-        y.z = w4.z * (o4.z * rstd) * s23.x;
-        y.w = w4.w * (o4.w * rstd) * s23.y;
-        st_io4(ob + i * ostride, y);
+#pragma unroll
+      for (int m = 0; m < 3; ++m) {
+        const int i = 2 * warp + (lane >> 4) + 24 * m;  // 24 tokens per round
+        const bool valid = i < nv;
+        float4 o0 = make_float4(0.f, 0.f, 0.f, 0.f), o1 = o0;
+        uint4 zr = make_uint4(0u, 0u, 0u, 0u);
+        if (valid) {
+          o0 = ld4(ost + i * kD + 8 * hl);
+          o1 = ld4(ost + i * kD + 8 * hl + 4);
+          zr = *reinterpret_cast<const uint4 *>(sm + OFF_Z + i * kD * 2 + 16 * hl);
+        }
+        float ss = dot4(o0, o0) + dot4(o1, o1);
+#pragma unroll
+        for (int off = 1; off < 16; off <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        const float rstd = rsqrtf(ss * (1.0f / kD) + d.eps_norm);
+        float2 zz[4];
+        widen(zr, zz);
+        const float2 op[4] = {make_float2(o0.x, o0.y), make_float2(o0.z, o0.w), make_float2(o1.x, o1.y),
+                              make_float2(o1.z, o1.w)};
+        uint32_t yw[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 sg = silu2(zz[q]);
+          const float2 y = __fmul2_rn(__fmul2_rn(wn[q], __fmul2_rn(op[q], make_float2(rstd, rstd))), sg);
+          __nv_bfloat162 t = __floats2bfloat162_rn(y.x, y.y);
+          yw[q] = *reinterpret_cast<uint32_t *>(&t);
+        }
+        if (valid) *reinterpret_cast<uint4 *>(ob + i * ostride) = make_uint4(yw[0], yw[1], yw[2], yw[3]);
       }
     }
     // J3: S -> fp16 copy and rescaled state (or S_T after the last chunk), in TMEM
@@ -896,23 +923,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp < kTmemWarps) {
       const bool last = n + 1 == nchunks;
       const float dcn = V.dC_next;
-      float v[32];
+      const int k0 = 64 * half;
+      uint32_t r0[32], r1[32];
+      tmem_ld32_nw(tl + TM_S + k0, r0);
+      tmem_ld32_nw(tl + TM_S + k0 + 32, r1);
+      tmem_wait_ld();
+      if (last) {
+        float4 *dst = reinterpret_cast<float4 *>(a.S_T + unit_off + (long long)lrow * kD + k0);
 #pragma unroll
-      for (int p = 0; p < 2; ++p) {
-        const int k0 = 64 * half + 32 * p;
-        tmem_ld32(tl + TM_S + k0, v);
-        if (last) {
-          float4 *dst = reinterpret_cast<float4 *>(a.S_T + unit_off + (long long)lrow * kD + k0);
+        for (int q = 0; q < 8; ++q)
+          dst[q] = make_float4(__uint_as_float(r0[4 * q]), __uint_as_float(r0[4 * q + 1]),
+                               __uint_as_float(r0[4 * q + 2]), __uint_as_float(r0[4 * q + 3]));
 #pragma unroll
-          for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-        } else {
-          uint32_t w16[16];
-          pack_h16(v, w16);
-          tmem_st16w(tl + TM_S16 + k0 / 2, w16);
+        for (int q = 0; q < 8; ++q)
+          dst[8 + q] = make_float4(__uint_as_float(r1[4 * q]), __uint_as_float(r1[4 * q + 1]),
+                                   __uint_as_float(r1[4 * q + 2]), __uint_as_float(r1[4 * q + 3]));
+      } else {
+        uint32_t w16[16];
 #pragma unroll
-          for (int q = 0; q < 32; ++q) v[q] *= dcn;
-          tmem_st32(tl + TM_S + k0, v);
+        for (int q = 0; q < 16; ++q) {
+          __half2 t = __halves2half2(to_h(__uint_as_float(r0[2 * q])), to_h(__uint_as_float(r0[2 * q + 1])));
+          w16[q] = *reinterpret_cast<uint32_t *>(&t);
         }
+        tmem_st16w_nw(tl + TM_S16 + k0 / 2, w16);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          __half2 t = __halves2half2(to_h(__uint_as_float(r1[2 * q])), to_h(__uint_as_float(r1[2 * q + 1])));
+          w16[q] = *reinterpret_cast<uint32_t *>(&t);
+        }
+        tmem_st16w_nw(tl + TM_S16 + k0 / 2 + 16, w16);
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+          r0[q] = __float_as_uint(__uint_as_float(r0[q]) * dcn);
+          r1[q] = __float_as_uint(__uint_as_float(r1[q]) * dcn);
+        }
+        tmem_st32w_nw(tl + TM_S + k0, r0);
+        tmem_st32w_nw(tl + TM_S + k0 + 32, r1);
+        tmem_wait_st();
       }
     }
     fence_before();
