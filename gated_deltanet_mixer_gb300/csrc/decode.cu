@@ -198,22 +198,36 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
       w1[2] = ld_io(win + 2 * C + c1);
       t1 = ld_io4(cw + 4 * c1);
     }
-    for (int t = 0; t < T; ++t) {
-      const float x0 = ld_io(x + (long long)t * C + c0);
-      float acc = fmaf(t0.w, x0, fmaf(t0.z, w0[2], fmaf(t0.y, w0[1], t0.x * w0[0])));
-      w0[0] = w0[1];
-      w0[1] = w0[2];
-      w0[2] = x0;
-      if (qk) {
-        s_q[t][tid] = silu(acc);
-        const float x1 = ld_io(x + (long long)t * C + c1);
-        const float acc1 = fmaf(t1.w, x1, fmaf(t1.z, w1[2], fmaf(t1.y, w1[1], t1.x * w1[0])));
-        w1[0] = w1[1];
-        w1[1] = w1[2];
-        w1[2] = x1;
-        s_k[t][tid] = silu(acc1);
-      } else {
-        s_v[t][tid - kD] = silu(acc);
+    // Tokens in batches of 8: the batch's loads are all issued before the
+    // first is used, so the T tokens cost about T / 8 load latencies.
+    for (int tb = 0; tb < T; tb += 8) {
+      float xa[8], xb[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const bool in = tb + u < T;
+        xa[u] = in ? ld_io(x + (long long)(tb + u) * C + c0) : 0.f;
+        xb[u] = (in && qk) ? ld_io(x + (long long)(tb + u) * C + c1) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (tb + u >= T) break;
+        const int t = tb + u;
+        const float x0 = xa[u];
+        float acc = fmaf(t0.w, x0, fmaf(t0.z, w0[2], fmaf(t0.y, w0[1], t0.x * w0[0])));
+        w0[0] = w0[1];
+        w0[1] = w0[2];
+        w0[2] = x0;
+        if (qk) {
+          s_q[t][tid] = silu(acc);
+          const float x1 = xb[u];
+          const float acc1 = fmaf(t1.w, x1, fmaf(t1.z, w1[2], fmaf(t1.y, w1[1], t1.x * w1[0])));
+          w1[0] = w1[1];
+          w1[1] = w1[2];
+          w1[2] = x1;
+          s_k[t][tid] = silu(acc1);
+        } else {
+          s_v[t][tid - kD] = silu(acc);
+        }
       }
     }
     // the new window: the last three raw rows (one CTA per key head shifts q/k)
