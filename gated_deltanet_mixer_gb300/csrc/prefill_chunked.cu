@@ -84,7 +84,7 @@ constexpr uint32_t OFF_L = OFF_RAW;                  // L fp32 [64][68], phases 
 constexpr uint32_t OFF_PB = OFF_RAW + 64 * kLs * 4;  // block products fp32 [32][32], phase D
 constexpr uint32_t OFF_TF = OFF_NW;                  // T fp32 [64][64], phase D
 constexpr uint32_t OFF_OST = OFF_VH;                 // O^T staging fp32 [64][128] (VH + VL), phase J
-constexpr uint32_t kVecBytes = 2560;
+constexpr uint32_t kVecBytes = 3584;
 constexpr uint32_t kSmemUsed = OFF_VEC + kVecBytes;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // + alignment slack
 static_assert(OFF_PB + 32 * 32 * 4 <= OFF_Z, "solve scratch fits in the raw rows");
@@ -101,18 +101,18 @@ constexpr uint32_t TM_KQ = 384;   // [K K^T; Q K^T]; then Delta^T fp16 hi | lo  
 constexpr uint32_t TM_S16 = 448;  // state, fp16 pairs [v][k/2]                 64
 constexpr uint32_t kTmemCols = 512;
 
-struct __align__(16) Vecs {  // per-token chunk vectors in shared memory
+struct __align__(16) ChunkVecs {  // per-token vectors of one chunk
   float G[kC];     // chunk-local cumulative log decay
   float d[kC];     // e^{G_i}
   float dinv[kC];  // e^{-G_j} (only when the chunk's decay is mild)
   float gam[kC];   // e^{G_last - G_j}
   float beta[kC];
   float bd[kC];    // beta_j d_j
-  float gn[kC];    // g of the next chunk (clamped), formed during this chunk's solve
-  float bn[kC];    // beta of the next chunk
-  float dC;        // e^{G_last} of the current chunk
-  float dC_next;   // e^{G_last} of the next chunk
   int mild;        // G_last >= -40: ratios as d_i * dinv_j
+};
+struct __align__(16) Vecs {  // shared-memory scalars, vectors and barriers
+  ChunkVecs cv[2];  // chunk n uses cv[n & 1]; chunk n + 1's are formed during chunk n's solve
+  float dC_next;   // e^{G_last} of the next chunk
   int abort;
   uint32_t tmem;
   uint64_t bar_qk;   // MMA1 done (K K^T, Q K^T)
@@ -186,8 +186,8 @@ __device__ __forceinline__ void finish_gb(float neg_exp_A, float dt_bias, int t0
   }
 }
 
-// Chunk vectors from the chunk's g and beta (one warp).
-__device__ void chunk_vectors(Vecs &V, float (&gv)[2], const float (&bv)[2], int lane) {
+// Chunk vectors from the chunk's g and beta (one warp); returns e^{G_last}.
+__device__ float chunk_vectors(ChunkVecs &V, float (&gv)[2], const float (&bv)[2], int lane) {
 #pragma unroll
   for (int u = 0; u < 2; ++u)
 #pragma unroll
@@ -209,10 +209,8 @@ __device__ void chunk_vectors(Vecs &V, float (&gv)[2], const float (&bv)[2], int
     V.beta[i] = bv[u];
     V.bd[i] = bv[u] * di;
   }
-  if (lane == 0) {
-    V.dC = __expf(Glast);
-    V.mild = mild ? 1 : 0;
-  }
+  if (lane == 0) V.mild = mild ? 1 : 0;
+  return __expf(Glast);
 }
 
 // Widen 8 bf16 (one 16-byte chunk) to four channel pairs.
@@ -258,7 +256,7 @@ __device__ __forceinline__ void st_h8_split_pairs(uint8_t *phi, uint8_t *plo, co
 // over the 16 lanes of a half-warp, which hold one token's 128 channels.
 // Writes: q^ and k^ (fp16) into [K;Q]; Gamma k^ (hi, lo); v (hi, lo).
 template <int NTOK>
-__device__ __forceinline__ void fe_pass(uint8_t *sm, const Vecs &V, const Dims &d, const bf16 *conv_w, int blk,
+__device__ __forceinline__ void fe_pass(uint8_t *sm, const ChunkVecs &V, const Dims &d, const bf16 *conv_w, int blk,
                                         long long c, int r0, int t0, int T, int grp) {
   const bool has_norm = blk < 2, has_single = blk < 2, has_split = blk > 0, has_gamma = blk == 1;
   const int row_off = blk == 0 ? 64 : 0;
@@ -325,7 +323,7 @@ __device__ __forceinline__ void fe_pass(uint8_t *sm, const Vecs &V, const Dims &
 // about 78 (q), 127 (k: norm, single and split outputs) and 100 (v: split)
 // units, so warps 0-7 each take q and then k of 4 tokens per half-warp
 // (32 token groups of 4), and warps 8-11 take v of 8 tokens per half-warp.
-__device__ void front_end(uint8_t *sm, const Vecs &V, const Dims &d, const bf16 *conv_w,
+__device__ void front_end(uint8_t *sm, const ChunkVecs &V, const Dims &d, const bf16 *conv_w,
                           int h, int kh, int t0, int T, int tid) {
   const int warp = tid >> 5, lane = tid & 31, grp = lane & 15;
   if (warp < 8) {
@@ -352,7 +350,7 @@ __device__ __forceinline__ void fma4(float4 &acc, float s, const float4 t) {
 
 // Row i, columns j .. j+3 (j % 4 == 0) of T -> the fp16 K-major tiles
 // T diag(beta) (hi, lo) and T diag(beta d), one 8-byte store each.
-__device__ __forceinline__ void store_T4(uint8_t *sm, const Vecs &V, int i, int j, float4 t) {
+__device__ __forceinline__ void store_T4(uint8_t *sm, const ChunkVecs &V, int i, int j, float4 t) {
   const float4 b = ld4(V.beta + j), e = ld4(V.bd + j);
   uint32_t hw[2], lw[2], ww[2];
   split2(t.x * b.x, t.y * b.y, hw[0], lw[0]);
@@ -388,7 +386,7 @@ __device__ void zero_T_upper(uint8_t *sm, int tid) {
 // final into the fp16 tiles meanwhile; the last product converts its own.
 // L is [64][kLs] (padded rows), T is [64][64] swizzled (tfi); blocks above
 // the diagonal of T are never written (and never read).
-__device__ void solve_T(uint8_t *sm, const Vecs &V, int tid) {
+__device__ void solve_T(uint8_t *sm, const ChunkVecs &V, int tid) {
   const float *L = reinterpret_cast<const float *>(sm + OFF_L);
   float *Tf = reinterpret_cast<float *>(sm + OFF_TF);
   float *P = reinterpret_cast<float *>(sm + OFF_PB);  // [2][16][16], then [32][32]
@@ -605,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       dt_bias = a.gate.dt_bias[h];
     }
     finish_gb<kRawGates>(neg_exp_A, dt_bias, 0, T, lane, g_cur, b_cur);
-    const float dc0 = __expf(warp_sum(g_cur[0] + g_cur[1]));
+    const float dc0 = chunk_vectors(V.cv[0], g_cur, b_cur, lane);
     if (lane == 0) V.dC_next = dc0;
   }
   fence_before();
@@ -685,17 +683,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int n = 0; n < nchunks; ++n) {
     const int t0 = n * kC;
     // A0: chunk vectors; the next chunk's g and beta requested
-    if (warp == 11) {
-      if (n > 0) {  // formed during the previous chunk
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          g_cur[u] = V.gn[lane + 32 * u];
-          b_cur[u] = V.bn[lane + 32 * u];
-        }
-      }
-      chunk_vectors(V, g_cur, b_cur, lane);
-      if (n + 1 < nchunks) load_gb<kRawGates>(a.gate, bos, d.Hv, h, t0 + kC, T, lane, g_nxt, b_nxt);
-    }
+    ChunkVecs &CV = V.cv[n & 1];  // formed before the loop or during the previous chunk's solve
+    if (warp == 11 && n + 1 < nchunks) load_gb<kRawGates>(a.gate, bos, d.Hv, h, t0 + kC, T, lane, g_nxt, b_nxt);
     if (!wait_all(&V.bar_raw, phase_raw)) break;
     raw_pending = false;
     if (n == 0) {  // rows before the first token: the carried window, or zeros
@@ -709,7 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncthreads();
     }
     // A: front end
-    front_end(sm, V, d, conv_w, h, kh, t0, T, tid);
+    front_end(sm, CV, d, conv_w, h, kh, t0, T, tid);
     smem_ready();
     // B: MMA1  [K;Q] K^T
     if (tid == 0) {
@@ -732,23 +721,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(tl + TM_KQ + 32 * half, v);
       const int j0 = 32 * half;
       const int i = lrow < kC ? lrow : lrow - kC;
-      if (V.mild) {
-        const float di = V.d[i];
+      if (CV.mild) {
+        const float di = CV.d[i];
 #pragma unroll
         for (int q = 0; q < 32; q += 4) {
-          const float4 dv = ld4(V.dinv + j0 + q);
+          const float4 dv = ld4(CV.dinv + j0 + q);
           rr[q] = di * dv.x;
           rr[q + 1] = di * dv.y;
           rr[q + 2] = di * dv.z;
           rr[q + 3] = di * dv.w;
         }
       } else {
-        const float gi = V.G[i];
+        const float gi = CV.G[i];
 #pragma unroll
-        for (int q = 0; q < 32; ++q) rr[q] = __expf(gi - V.G[j0 + q]);
+        for (int q = 0; q < 32; ++q) rr[q] = __expf(gi - CV.G[j0 + q]);
       }
       if (lrow < kC) {
-        const float bi = V.beta[i];
+        const float bi = CV.beta[i];
         float *L = reinterpret_cast<float *>(sm + OFF_L) + i * kLs + j0;
 #pragma unroll
         for (int q = 0; q < 32; q += 4) {
@@ -770,17 +759,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // D: the triangular inverse, scaled copies T B and T B D.  Warp 11, idle
     // in the solve, forms the next chunk's gates and total decay meanwhile
     // (through shared memory, so that the work stays here).
-    if (warp == 11) {
+    if (warp == 11 && n + 1 < nchunks) {
       finish_gb<kRawGates>(neg_exp_A, dt_bias, t0 + kC, T, lane, g_nxt, b_nxt);
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        V.gn[lane + 32 * u] = g_nxt[u];
-        V.bn[lane + 32 * u] = b_nxt[u];
-      }
-      const float dcn = n + 1 < nchunks ? __expf(warp_sum(g_nxt[0] + g_nxt[1])) : 1.f;
+      const float dcn = chunk_vectors(V.cv[(n + 1) & 1], g_nxt, b_nxt, lane);
       if (lane == 0) V.dC_next = dcn;
     }
-    solve_T(sm, V, tid);
+    solve_T(sm, CV, tid);
     smem_ready();
     // E: MMA2 U^T = V^T (T B)^T, hi*hi + lo*hi + hi*lo; MMA3 W^T = K^T (T B D)^T
     // (K^ read from [K;Q] as an MN-major operand).  The raw rows are free now:
@@ -869,7 +853,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 #pragma unroll
       for (int q = 0; q < 32; q += 4) {
-        const float4 dq = ld4(V.d + 32 * half + q);
+        const float4 dq = ld4(CV.d + 32 * half + q);
         ost[(32 * half + q + 0) * kD + lrow] = fmaf(dq.x, v[q + 0], w2[q + 0]);
         ost[(32 * half + q + 1) * kD + lrow] = fmaf(dq.y, v[q + 1], w2[q + 1]);
         ost[(32 * half + q + 2) * kD + lrow] = fmaf(dq.z, v[q + 2], w2[q + 2]);
