@@ -100,3 +100,18 @@ def test_linear_host_errors_leave_outputs_untouched():
         assert e.value.status in (1, 4)
     torch.cuda.synchronize()
     assert bool((y == 5.0).all())
+
+
+def test_bench_in_proj_8192_tokens_sampled_rows():
+    """The benchmark's 27B in_proj (8192 tokens, split outputs) in its launch
+    configuration; 64 sampled rows against the oracle on every column."""
+    T = 8192
+    xa, wa = I.linear_problem(T, 16480, 5120, case=80)
+    x, w = dev(xa, torch.bfloat16), dev(wa, torch.bfloat16)
+    sp = O.in_proj_split(16, 48, 128)
+    bufs = {k: torch.empty(T, hi - lo, device="cuda", dtype=torch.bfloat16) for k, (lo, hi) in sp.items()}
+    run(x, w, [(sp[k][0], sp[k][1], bufs[k]) for k in ("qkv_pre", "z", "b", "a")])
+    rows = np.random.default_rng(0).choice(T, size=64, replace=False)
+    ref = O.linear(xa[rows], wa)
+    for k, (lo, hi) in sp.items():
+        check_linear(to_np(bufs[k][rows]), ref[:, lo:hi], k)

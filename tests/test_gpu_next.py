@@ -237,3 +237,56 @@ def test_decode_ex_single_token_matches_decode_step():
                       c2, o2, Hk=1, Hv=2)
     torch.cuda.synchronize()
     assert torch.equal(S1, S2) and torch.equal(c1, c2) and torch.equal(o1, o2[:, 0])
+
+
+# ------------------------------ the bench's extended workloads, full size ----
+def test_bench_packed_batch_sampled():
+    """The benchmark's packed batch (24 sequences, log-uniform lengths
+    100..4000, 4B head shape) in its launch configuration; sampled units of
+    the longest, the shortest and a middle sequence against the oracle."""
+    import bench
+    lens = bench.varlen_lengths()
+    p = I.packed_problem(lens, 16, 32, io="bf16", case=61)
+    o, S_T, conv_T, _ = _run_packed(p)
+    a = p.arrays
+    cu = p.cu_seqlens
+    order = np.argsort(lens)
+    for s in (int(order[-1]), int(order[0]), int(order[len(lens) // 2])):
+        lo, hi = int(cu[s]), int(cu[s + 1])
+        units = [s * 32 + 0, s * 32 + 17]
+        ref = O.gdn_prefill(a["qkv_pre"][None, lo:hi], a["z"][None, lo:hi], a["g"][None, lo:hi],
+                            a["beta"][None, lo:hi], a["conv_w"], a["norm_w"], a["S0"][s:s + 1],
+                            a["conv0"][s:s + 1], Hk=16, Hv=32, units=[u - s * 32 for u in units],
+                            threads=O.default_threads())
+        got_o = np.stack([to_np(o[lo:hi].view(hi - lo, 32, D)[:, u - s * 32]) for u in units])
+        check_o(got_o, ref["o_units"], "bf16")
+        check_S(np.stack([to_np(S_T[s, u - s * 32]) for u in units]), ref["S_T"])
+        np.testing.assert_array_equal(to_np(conv_T[s]), ref["conv_T"][0])
+
+
+def test_bench_multi_token_decode_sampled():
+    """The benchmark's 4-token decode with snapshots at the 27B decode shape
+    (B=256, Hv=48), three sequences checked on every output and snapshot."""
+    B, Hk, Hv, T = 256, 16, 48, 4
+    dp = I.decode_problem(B=B, Hk=Hk, Hv=Hv, io="bf16", steps=T, case=74)
+    t = torch.bfloat16
+    qkv = np.ascontiguousarray(dp.qkv_pre.transpose(1, 0, 2))
+    z = np.ascontiguousarray(dp.z.transpose(1, 0, 2))
+    g = np.ascontiguousarray(dp.g.transpose(1, 0, 2))
+    beta = np.ascontiguousarray(dp.beta.transpose(1, 0, 2))
+    S = dev(dp.S)
+    snap = torch.empty(B, T, Hv, D, D, device="cuda")
+    conv_out = torch.empty(B, 3, dp.C, device="cuda", dtype=t)
+    o = torch.empty(B, T, Hv * D, device="cuda", dtype=t)
+    gdn.gdn_decode_ex(dev(qkv, t), dev(z, t), dev(g), dev(beta), dev(dp.conv_w, t), dev(dp.norm_w, t), S,
+                      dev(dp.conv, t), conv_out, o, Hk=Hk, Hv=Hv, S_snap=snap)
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_status() == 0
+    seqs = [0, 131, 255]
+    ref = O.gdn_decode_multi(qkv[seqs], z[seqs], g[seqs], beta[seqs], dp.conv_w, dp.norm_w, dp.S[seqs],
+                             dp.conv[seqs], Hk=Hk, Hv=Hv, threads=O.default_threads())
+    check_o(to_np(o[seqs]), ref["o"], "bf16")
+    check_S(to_np(S[seqs]), ref["S"])
+    for k in range(T):
+        check_S(to_np(snap[seqs, k]), ref["S_snap"][:, k], "S_snap[%d]" % k)
+    np.testing.assert_array_equal(to_np(conv_out[seqs]), ref["conv_out"])
