@@ -27,6 +27,10 @@
 // both factors of the state update, are carried as hi + lo fp16 pairs (three
 // MMAs for hi*hi + hi*lo + lo*hi), which keeps the state within about 1e-3
 // of its rms where single fp16 gives 2e-2 on short, heavy-tailed updates.
+// Operands derived from the inputs (v, the initial state, T) are clamped to
+// the fp16 range; Gamma k^ (|.| <= 1), the state's fp16 copy and Delta are
+// converted without a clamp, so a state or Delta entry beyond 65504 (far
+// outside any model's regime) would overflow to inf.
 // Per chunk, in order:
 //   A  conv + SiLU + L2 norms (front end) from the staged raw rows
 //   B  MMA1  [K;Q] K^T -> K K^T, Q K^T;  MMA5  S Q^T
@@ -241,11 +245,30 @@ __device__ __forceinline__ void split2(float a, float b, uint32_t &whi, uint32_t
   whi = *reinterpret_cast<uint32_t *>(&th);
   wlo = *reinterpret_cast<uint32_t *>(&tl);
 }
+// hi/lo of a pair known to lie well inside the fp16 range (no clamp).
+__device__ __forceinline__ void split2_inrange(float a, float b, uint32_t &whi, uint32_t &wlo) {
+  __half2 th = __floats2half2_rn(a, b);
+  const float2 back = __half22float2(th);
+  __half2 tl = __floats2half2_rn(a - back.x, b - back.y);
+  whi = *reinterpret_cast<uint32_t *>(&th);
+  wlo = *reinterpret_cast<uint32_t *>(&tl);
+}
+// A pair packed to fp16 without a clamp (values well inside the range).
+__device__ __forceinline__ uint32_t pack2_inrange(float a, float b) {
+  __half2 t = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t *>(&t);
+}
 // The same as a hi/lo pair of 16-byte chunks.
+template <bool kClamp>
 __device__ __forceinline__ void st_h8_split_pairs(uint8_t *phi, uint8_t *plo, const float2 (&v)[4]) {
   uint32_t wh[4], wl[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) split2(v[i].x, v[i].y, wh[i], wl[i]);
+  for (int i = 0; i < 4; ++i) {
+    if (kClamp)
+      split2(v[i].x, v[i].y, wh[i], wl[i]);
+    else
+      split2_inrange(v[i].x, v[i].y, wh[i], wl[i]);
+  }
   *reinterpret_cast<uint4 *>(phi) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
   *reinterpret_cast<uint4 *>(plo) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
 }
@@ -314,7 +337,10 @@ __device__ __forceinline__ void fe_pass(uint8_t *sm, const ChunkVecs &V, const D
 #pragma unroll
       for (int i = 0; i < 4; ++i) u[i] = __fmul2_rn(u[i], make_float2(gm, gm));
       const uint32_t o = mnmaj(8 * grp, row, kC);
-      st_h8_split_pairs(dhi + o, dlo + o, u);
+      if (has_gamma)
+        st_h8_split_pairs<false>(dhi + o, dlo + o, u);  // |Gamma k^| <= 1
+      else
+        st_h8_split_pairs<true>(dhi + o, dlo + o, u);
     }
   }
 }
@@ -814,7 +840,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(tl + TM_U + 32 * half, v);
       uint32_t wh[16], wl[16];
 #pragma unroll
-      for (int q = 0; q < 16; ++q) split2(v[2 * q], v[2 * q + 1], wh[q], wl[q]);
+      for (int q = 0; q < 16; ++q) split2_inrange(v[2 * q], v[2 * q + 1], wh[q], wl[q]);
       tmem_st16w_nw(tl + TM_KQ + 16 * half, wh);
       tmem_st16w_nw(tl + TM_KQ + 32 + 16 * half, wl);
       tmem_wait_st();
@@ -926,14 +952,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t w16[16];
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
-          __half2 t = __halves2half2(to_h(__uint_as_float(r0[2 * q])), to_h(__uint_as_float(r0[2 * q + 1])));
-          w16[q] = *reinterpret_cast<uint32_t *>(&t);
+          w16[q] = pack2_inrange(__uint_as_float(r0[2 * q]), __uint_as_float(r0[2 * q + 1]));
         }
         tmem_st16w_nw(tl + TM_S16 + k0 / 2, w16);
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
-          __half2 t = __halves2half2(to_h(__uint_as_float(r1[2 * q])), to_h(__uint_as_float(r1[2 * q + 1])));
-          w16[q] = *reinterpret_cast<uint32_t *>(&t);
+          w16[q] = pack2_inrange(__uint_as_float(r1[2 * q]), __uint_as_float(r1[2 * q + 1]));
         }
         tmem_st16w_nw(tl + TM_S16 + k0 / 2 + 16, w16);
 #pragma unroll
