@@ -474,38 +474,62 @@ __device__ void solve_T(uint8_t *sm, const ChunkVecs &V, int tid) {
     *reinterpret_cast<float4 *>(Tf + tfi(row, 16 * A + 4 * c4)) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
   }
   __syncthreads();
-  // The whole: P = L[32:64][0:32] T[0:32][0:32], T[32:64][0:32] = -T[32:64][32:64] P.
-  const int r32 = tid >> 3, col = 4 * (tid & 7);
-  if (tid < 256) {
-    const float *Lr = L + (32 + r32) * kLs;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  // The whole: P = L[32:64][0:32] T[0:32][0:32], T[32:64][0:32] = -T[32:64][32:64] P,
+  // each thread two rows (r, r + 16) by four columns, so every operand load
+  // feeds eight products.
+  const int r16b = tid >> 3, col = 4 * (tid & 7);
+  if (tid < 128) {
+    const float *La = L + (32 + r16b) * kLs, *Lb = L + (48 + r16b) * kLs;
+    float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
 #pragma unroll 2
     for (int k4 = col >= 16 ? 16 : 0; k4 < 32; k4 += 4) {  // T[0:16][16:32] is zero
-      const float4 l = ld4(Lr + k4);
-      fma4(acc, l.x, ld4(Tf + tfi(k4 + 0, col)));
-      fma4(acc, l.y, ld4(Tf + tfi(k4 + 1, col)));
-      fma4(acc, l.z, ld4(Tf + tfi(k4 + 2, col)));
-      fma4(acc, l.w, ld4(Tf + tfi(k4 + 3, col)));
+      const float4 la = ld4(La + k4), lb = ld4(Lb + k4);
+      const float4 t0 = ld4(Tf + tfi(k4 + 0, col)), t1 = ld4(Tf + tfi(k4 + 1, col));
+      const float4 t2 = ld4(Tf + tfi(k4 + 2, col)), t3 = ld4(Tf + tfi(k4 + 3, col));
+      fma4(acc0, la.x, t0);
+      fma4(acc1, lb.x, t0);
+      fma4(acc0, la.y, t1);
+      fma4(acc1, lb.y, t1);
+      fma4(acc0, la.z, t2);
+      fma4(acc1, lb.z, t2);
+      fma4(acc0, la.w, t3);
+      fma4(acc1, lb.w, t3);
     }
-    *reinterpret_cast<float4 *>(P + r32 * 32 + col) = acc;
-  } else {  // the blocks T_10 and T_32 are final
-    const int q = tid - 256, hh = q >> 6;
+    *reinterpret_cast<float4 *>(P + r16b * 32 + col) = acc0;
+    *reinterpret_cast<float4 *>(P + (16 + r16b) * 32 + col) = acc1;
+  } else if (tid < 256) {  // the blocks T_10 and T_32 are final
+    const int q = tid - 128, hh = q >> 6;
     const int row = 16 * (2 * hh + 1) + ((q >> 2) & 15), cc = 32 * hh + 4 * (q & 3);
     store_T4(sm, V, row, cc, ld4(Tf + tfi(row, cc)));
   }
   __syncthreads();
-  if (tid < 256) {
-    const int row = 32 + r32;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (tid < 128) {  // rows 32 + r (T_BB row has 16 terms) and 48 + r (32 terms); T[32:48][48:64] is zero
+    const int ra = 32 + r16b, rb = 48 + r16b;
+    float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
 #pragma unroll 2
-    for (int k4 = 0; k4 < (r32 < 16 ? 16 : 32); k4 += 4) {  // T[32:48][48:64] is zero
-      const float4 t = ld4(Tf + tfi(row, 32 + k4));
-      fma4(acc, t.x, ld4(P + (k4 + 0) * 32 + col));
-      fma4(acc, t.y, ld4(P + (k4 + 1) * 32 + col));
-      fma4(acc, t.z, ld4(P + (k4 + 2) * 32 + col));
-      fma4(acc, t.w, ld4(P + (k4 + 3) * 32 + col));
+    for (int k4 = 0; k4 < 16; k4 += 4) {
+      const float4 ta = ld4(Tf + tfi(ra, 32 + k4)), tb = ld4(Tf + tfi(rb, 32 + k4));
+      const float4 p0 = ld4(P + (k4 + 0) * 32 + col), p1 = ld4(P + (k4 + 1) * 32 + col);
+      const float4 p2 = ld4(P + (k4 + 2) * 32 + col), p3 = ld4(P + (k4 + 3) * 32 + col);
+      fma4(acc0, ta.x, p0);
+      fma4(acc1, tb.x, p0);
+      fma4(acc0, ta.y, p1);
+      fma4(acc1, tb.y, p1);
+      fma4(acc0, ta.z, p2);
+      fma4(acc1, tb.z, p2);
+      fma4(acc0, ta.w, p3);
+      fma4(acc1, tb.w, p3);
     }
-    store_T4(sm, V, row, col, make_float4(-acc.x, -acc.y, -acc.z, -acc.w));
+#pragma unroll 2
+    for (int k4 = 16; k4 < 32; k4 += 4) {
+      const float4 tb = ld4(Tf + tfi(rb, 32 + k4));
+      fma4(acc1, tb.x, ld4(P + (k4 + 0) * 32 + col));
+      fma4(acc1, tb.y, ld4(P + (k4 + 1) * 32 + col));
+      fma4(acc1, tb.z, ld4(P + (k4 + 2) * 32 + col));
+      fma4(acc1, tb.w, ld4(P + (k4 + 3) * 32 + col));
+    }
+    store_T4(sm, V, ra, col, make_float4(-acc0.x, -acc0.y, -acc0.z, -acc0.w));
+    store_T4(sm, V, rb, col, make_float4(-acc1.x, -acc1.y, -acc1.z, -acc1.w));
   }
 }
 
