@@ -28,9 +28,9 @@
 // MMAs for hi*hi + hi*lo + lo*hi), which keeps the state within about 1e-3
 // of its rms where single fp16 gives 2e-2 on short, heavy-tailed updates.
 // Operands derived from the inputs (v, the initial state, T) are clamped to
-// the fp16 range; Gamma k^ (|.| <= 1), the state's fp16 copy and Delta are
-// converted without a clamp, so a state or Delta entry beyond 65504 (far
-// outside any model's regime) would overflow to inf.
+// the fp16 range; Gamma k^ and M (|.| <= 1), W, the state's fp16 copy and
+// Delta are converted without a clamp, so an entry of those beyond 65504
+// (far outside any model's regime) would overflow to inf.
 // Per chunk, in order:
 //   A  conv + SiLU + L2 norms (front end) from the staged raw rows
 //   B  MMA1  [K;Q] K^T -> K K^T, Q K^T;  MMA5  S Q^T
@@ -257,6 +257,11 @@ __device__ __forceinline__ void split2_inrange(float a, float b, uint32_t &whi, 
 __device__ __forceinline__ uint32_t pack2_inrange(float a, float b) {
   __half2 t = __floats2half2_rn(a, b);
   return *reinterpret_cast<uint32_t *>(&t);
+}
+// 8 values -> one 16-byte fp16 chunk, no clamp.
+__device__ __forceinline__ void st_h8_inrange(uint8_t *p, const float *v) {
+  *reinterpret_cast<uint4 *>(p) = make_uint4(pack2_inrange(v[0], v[1]), pack2_inrange(v[2], v[3]),
+                                             pack2_inrange(v[4], v[5]), pack2_inrange(v[6], v[7]));
 }
 // The same as a hi/lo pair of 16-byte chunks.
 template <bool kClamp>
@@ -802,7 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int q = 0; q < 32; ++q) v[q] = (j0 + q <= i) ? v[q] * rr[q] : 0.f;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) st_h8(sm + OFF_M + kmaj(i, j0 + 8 * q, kC), v + 8 * q);
+        for (int q = 0; q < 4; ++q) st_h8_inrange(sm + OFF_M + kmaj(i, j0 + 8 * q, kC), v + 8 * q);  // |M| <= q_scale
       }
     }
     __syncthreads();
@@ -846,7 +851,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int q = 0; q < 32; ++q) v[q] = -v[q];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) st_h8(sm + OFF_NW + mnmaj(32 * half + 8 * q, lrow, kD), v + 8 * q);
+      for (int q = 0; q < 4; ++q) st_h8_inrange(sm + OFF_NW + mnmaj(32 * half + 8 * q, lrow, kD), v + 8 * q);
     }
     smem_ready();
     // G: MMA4 Delta^T = U^T - S W^T (S from TMEM), after MMA2 (the other issuer)
