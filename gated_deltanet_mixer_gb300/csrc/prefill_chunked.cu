@@ -87,7 +87,8 @@ constexpr int kLs = 68;                              // padded row stride of L (
 constexpr uint32_t OFF_L = OFF_RAW;                  // L fp32 [64][68], phases C-D
 constexpr uint32_t OFF_PB = OFF_RAW + 64 * kLs * 4;  // block products fp32 [32][32], phase D
 constexpr uint32_t OFF_TF = OFF_NW;                  // T fp32 [64][64], phase D
-constexpr uint32_t OFF_OST = OFF_VH;                 // O^T staging fp32 [64][128] (VH + VL), phase J
+constexpr uint32_t OFF_OST = OFF_M;                  // O^T staging fp32 [64][128] (M, NW, TUL), phase J
+static_assert(OFF_NW == OFF_M + 8192 && OFF_TUL == OFF_NW + 16384, "the staging spans M, NW and TUL");
 constexpr uint32_t kVecBytes = 3584;
 constexpr uint32_t kSmemUsed = OFF_VEC + kVecBytes;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // + alignment slack
@@ -397,9 +398,11 @@ __device__ __forceinline__ void store_T4(uint8_t *sm, const ChunkVecs &V, int i,
 }
 
 // The fp16 T tiles are zero above the block diagonal (16 x 16 blocks) in
-// every chunk: written once, before the first chunk.
-__device__ void zero_T_upper(uint8_t *sm, int tid) {
-  for (int q = tid; q < 3 * 6 * 32; q += kThreads) {
+// every chunk: written before the first chunk (tiles 0, 1, 2 = T diag(beta)
+// hi, lo and T diag(beta d); q0 = 0) and, for tile 1, whose space the O
+// staging borrows, again in every solve (q0 = 192, items 192 .. 383).
+__device__ void zero_T_upper(uint8_t *sm, int tid, int q0 = 0, int nthreads = kThreads, int q1 = 3 * 6 * 32) {
+  for (int q = q0 + tid; q < q1; q += nthreads) {
     const int tile = q / 192, rem = q % 192, blk = rem / 32, w = rem % 32;
     const int I = blk < 3 ? 0 : blk < 5 ? 1 : 2;
     const int J = blk < 3 ? blk + 1 : blk < 5 ? blk - 1 : 3;
@@ -535,6 +538,8 @@ __device__ void solve_T(uint8_t *sm, const ChunkVecs &V, int tid) {
     }
     store_T4(sm, V, ra, col, make_float4(-acc0.x, -acc0.y, -acc0.z, -acc0.w));
     store_T4(sm, V, rb, col, make_float4(-acc1.x, -acc1.y, -acc1.z, -acc1.w));
+  } else {
+    zero_T_upper(sm, tid - 128, 192, kThreads - 128, 2 * 192);  // tile 1, overwritten by the O staging
   }
 }
 
