@@ -65,6 +65,26 @@ constexpr int kC = 64;          // chunk length
 constexpr int kThreads = 384;   // 12 warps
 constexpr int kTmemWarps = 8;   // warps 0..7 do the TMEM <-> register passes (two per lane quadrant)
 constexpr float kGMin = -80.0f;
+constexpr int kBarTmem = 1;  // named barrier of warps 0-7 in the epilogue
+constexpr int kBarMma6 = 2;  // warp 0 (MMA6 issued) -> warp 11 (may issue MMA7)
+
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+__device__ __forceinline__ void named_arrive(int id, int nthreads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// bar.red.or over the named barrier's threads: true if any thread passed true.
+__device__ __forceinline__ bool named_sync_or(int id, int nthreads, bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred q, t;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred t, %2, %3, q;\n\tselp.u32 %0, 1, 0, t;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)p), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
 constexpr int kRawRows = kC + 3;                  // a chunk's rows plus the three before it
 constexpr uint32_t kRawBlock = kRawRows * kD * 2;  // one of q | k | v, bytes (17152)
 
@@ -355,17 +375,35 @@ __device__ __forceinline__ void fe_pass(uint8_t *sm, const ChunkVecs &V, const D
 // about 78 (q), 127 (k: norm, single and split outputs) and 100 (v: split)
 // units, so warps 0-7 each take q and then k of 4 tokens per half-warp
 // (32 token groups of 4), and warps 8-11 take v of 8 tokens per half-warp.
+// with_v: the first chunk; later chunks' v tiles are made by warps 8-11
+// during the previous chunk's epilogue (front_end_v), so the others split
+// q and k between all twelve warps: k on warps 0-7 (4 tokens per half-warp),
+// q on warps 8-11 (8 tokens).
 __device__ void front_end(uint8_t *sm, const ChunkVecs &V, const Dims &d, const bf16 *conv_w,
-                          int h, int kh, int t0, int T, int tid) {
+                          int h, int kh, int t0, int T, int tid, bool with_v) {
   const int warp = tid >> 5, lane = tid & 31, grp = lane & 15;
-  if (warp < 8) {
-    const int r0 = 4 * (2 * warp + (lane >> 4));
-    fe_pass<4>(sm, V, d, conv_w, 0, (long long)kh * kD + 8 * grp, r0, t0, T, grp);
-    fe_pass<4>(sm, V, d, conv_w, 1, (long long)d.Hk * kD + (long long)kh * kD + 8 * grp, r0, t0, T, grp);
+  const long long cq = (long long)kh * kD + 8 * grp, ck = (long long)d.Hk * kD + (long long)kh * kD + 8 * grp;
+  if (with_v) {
+    if (warp < 8) {
+      const int r0 = 4 * (2 * warp + (lane >> 4));
+      fe_pass<4>(sm, V, d, conv_w, 0, cq, r0, t0, T, grp);
+      fe_pass<4>(sm, V, d, conv_w, 1, ck, r0, t0, T, grp);
+    } else {
+      const int r0 = 8 * (2 * (warp - 8) + (lane >> 4));
+      fe_pass<8>(sm, V, d, conv_w, 2, 2LL * d.Hk * kD + (long long)h * kD + 8 * grp, r0, t0, T, grp);
+    }
+  } else if (warp < 8) {
+    fe_pass<4>(sm, V, d, conv_w, 1, ck, 4 * (2 * warp + (lane >> 4)), t0, T, grp);
   } else {
-    const int r0 = 8 * (2 * (warp - 8) + (lane >> 4));
-    fe_pass<8>(sm, V, d, conv_w, 2, 2LL * d.Hk * kD + (long long)h * kD + 8 * grp, r0, t0, T, grp);
+    fe_pass<8>(sm, V, d, conv_w, 0, cq, 8 * (2 * (warp - 8) + (lane >> 4)), t0, T, grp);
   }
+}
+// The v tiles of the chunk starting at t0 (warps 8-11, 8 tokens per half-warp).
+__device__ void front_end_v(uint8_t *sm, const ChunkVecs &V, const Dims &d, const bf16 *conv_w, int h, int t0,
+                            int T, int tid) {
+  const int warp = tid >> 5, lane = tid & 31, grp = lane & 15;
+  fe_pass<8>(sm, V, d, conv_w, 2, 2LL * d.Hk * kD + (long long)h * kD + 8 * grp, 8 * (2 * (warp - 8) + (lane >> 4)),
+             t0, T, grp);
 }
 
 // T scratch: fp32 [64][64], float4 groups XOR-swizzled by row, so that reads of
@@ -734,6 +772,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     return !bad;
   };
+  // Warps 0-7 only (named barrier kBarTmem, 256 threads): wait on an mbarrier
+  // phase; a timeout sets the abort flag, seen by all at the end of the chunk.
+  auto wait_tmem = [&](uint64_t *bar, uint32_t &ph) -> bool {
+    __syncwarp();
+    const bool ok = bar_wait(bar, ph);
+    ph ^= 1u;
+    fence_after();
+    __syncwarp();  // the barrier instruction wants the warp converged
+    const bool bad = named_sync_or(kBarTmem, kTmemWarps * 32, !ok);
+    if (bad && tid == 0) {
+      atomicOr(a.err, kErrTimeout);
+      V.abort = 1;
+    }
+    return !bad;
+  };
   auto smem_ready = [&]() {  // operands written (shared memory or TMEM) -> visible to the MMA unit
     fence_smem_to_async();
     fence_before();
@@ -745,8 +798,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // A0: chunk vectors; the next chunk's g and beta requested
     ChunkVecs &CV = V.cv[n & 1];  // formed before the loop or during the previous chunk's solve
     if (warp == 11 && n + 1 < nchunks) load_gb<kRawGates>(a.gate, bos, d.Hv, h, t0 + kC, T, lane, g_nxt, b_nxt);
-    if (!wait_all(&V.bar_raw, phase_raw)) break;
-    raw_pending = false;
+    if (n == 0) {  // later chunks' rows were awaited by warps 8-11 during the previous epilogue
+      if (!wait_all(&V.bar_raw, phase_raw)) break;
+      raw_pending = false;
+    }
     if (n == 0) {  // rows before the first token: the carried window, or zeros
       for (int idx = tid; idx < 3 * 3 * 16; idx += kThreads) {
         const int blk = idx / 48, rw = (idx / 16) % 3, g8 = idx % 16;
@@ -758,7 +813,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncthreads();
     }
     // A: front end
-    front_end(sm, CV, d, conv_w, h, kh, t0, T, tid);
+    front_end(sm, CV, d, conv_w, h, kh, t0, T, tid, n == 0);
     smem_ready();
     // B: MMA1  [K;Q] K^T
     if (tid == 0) {
@@ -880,134 +935,174 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_st();
     }
     smem_ready();
-    // I: MMA6 Delta^T M^T;  MMA7 S += Delta^T (Gamma K), hi*hi + hi*lo + lo*hi
-    if (tid == 0) {
-      bar_wait(&V.bar_sq, ph_sq);  // MMA5 (the other issuer) done, so bar_o covers O1 and O2
-      fence_after();
-      issue_ta(tmem + TM_O2, tmem + TM_KQ, id_kk, 4, false, [&](int ks) { return desc_k(sbase + OFF_M, ks, kC); });
-      commit(&V.bar_o);
+    // The epilogue.  Warps 0-7 (TMEM) finish this chunk and sync among
+    // themselves (named barrier 1); warps 8-11 meanwhile make the next
+    // chunk's v tiles from its staged rows (the V tiles were last read by
+    // MMA2, complete since G).  Everyone meets at the end of the chunk.
+    if (warp < kTmemWarps) {
+      bool ok = true;
+      // I: MMA6 Delta^T M^T (thread 0); then warp 11 may issue MMA7 behind it
+      if (tid == 0) {
+        bar_wait(&V.bar_sq, ph_sq);  // MMA5 (the other issuer) done, so bar_o covers O1 and O2
+        fence_after();
+        issue_ta(tmem + TM_O2, tmem + TM_KQ, id_kk, 4, false, [&](int ks) { return desc_k(sbase + OFF_M, ks, kC); });
+        commit(&V.bar_o);
+      }
+      if (warp == 0) {
+        __syncwarp();
+        named_arrive(kBarMma6, 64);
+      }
+      ok = wait_tmem(&V.bar_o, ph_o);
+      if (ok) {
+      // J1: O^T = d (S Q^T) + Delta^T M^T -> staging [i][v]
+        {
+        float *ost = reinterpret_cast<float *>(sm + OFF_OST);
+        uint32_t ra[32], rb[32];
+        tmem_ld32_nw(tl + TM_O1 + 32 * half, ra);
+        tmem_ld32_nw(tl + TM_O2 + 32 * half, rb);
+        tmem_wait_ld();
+        float v[32], w2[32];
+  #pragma unroll
+        for (int q = 0; q < 32; ++q) {
+          v[q] = __uint_as_float(ra[q]);
+          w2[q] = __uint_as_float(rb[q]);
+        }
+  #pragma unroll
+        for (int q = 0; q < 32; q += 4) {
+          const float4 dq = ld4(CV.d + 32 * half + q);
+          ost[(32 * half + q + 0) * kD + lrow] = fmaf(dq.x, v[q + 0], w2[q + 0]);
+          ost[(32 * half + q + 1) * kD + lrow] = fmaf(dq.y, v[q + 1], w2[q + 1]);
+          ost[(32 * half + q + 2) * kD + lrow] = fmaf(dq.z, v[q + 2], w2[q + 2]);
+          ost[(32 * half + q + 3) * kD + lrow] = fmaf(dq.w, v[q + 3], w2[q + 3]);
+        }
+      }
+      }
+      ok = wait_tmem(&V.bar_z, phase_z) && ok;
+      z_pending = false;
+      if (ok) {
+      // J2: gated RMSNorm per token, one half-warp per token (8 channels per
+      // lane, warps 0-7), z from the staged rows
+      {
+        const float *ost = reinterpret_cast<const float *>(sm + OFF_OST);
+        const int hl = lane & 15;
+        float2 wn[4];
+        widen(*reinterpret_cast<const uint4 *>(static_cast<const bf16 *>(a.norm_w) + 8 * hl), wn);
+        const int nv = min(kC, T - t0);
+        bf16 *ob = static_cast<bf16 *>(a.o) + ((bos + t0) * d.Hv + h) * kD + 8 * hl;
+        const long long ostride = (long long)d.Hv * kD;
+  #pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const int i = 2 * warp + (lane >> 4) + 16 * m;  // 16 tokens per round (warps 0-7)
+          const bool valid = i < nv;
+          float4 o0 = make_float4(0.f, 0.f, 0.f, 0.f), o1 = o0;
+          uint4 zr = make_uint4(0u, 0u, 0u, 0u);
+          if (valid) {
+            o0 = ld4(ost + i * kD + 8 * hl);
+            o1 = ld4(ost + i * kD + 8 * hl + 4);
+            zr = *reinterpret_cast<const uint4 *>(sm + OFF_Z + i * kD * 2 + 16 * hl);
+          }
+          float ss = dot4(o0, o0) + dot4(o1, o1);
+  #pragma unroll
+          for (int off = 1; off < 16; off <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+          const float rstd = rsqrtf(ss * (1.0f / kD) + d.eps_norm);
+          float2 zz[4];
+          widen(zr, zz);
+          const float2 op[4] = {make_float2(o0.x, o0.y), make_float2(o0.z, o0.w), make_float2(o1.x, o1.y),
+                                make_float2(o1.z, o1.w)};
+          uint32_t yw[4];
+  #pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 sg = silu2(zz[q]);
+            const float2 y = __fmul2_rn(__fmul2_rn(wn[q], __fmul2_rn(op[q], make_float2(rstd, rstd))), sg);
+            __nv_bfloat162 t = __floats2bfloat162_rn(y.x, y.y);
+            yw[q] = *reinterpret_cast<uint32_t *>(&t);
+          }
+          if (valid) *reinterpret_cast<uint4 *>(ob + i * ostride) = make_uint4(yw[0], yw[1], yw[2], yw[3]);
+        }
+      }
+      }
+      // J3: S -> fp16 copy and rescaled state (or S_T after the last chunk), in TMEM
+      ok = wait_tmem(&V.bar_s, ph_s) && ok;
+      if (ok) {
+      {
+        const bool last = n + 1 == nchunks;
+        const float dcn = V.dC_next;
+        const int k0 = 64 * half;
+        uint32_t r0[32], r1[32];
+        tmem_ld32_nw(tl + TM_S + k0, r0);
+        tmem_ld32_nw(tl + TM_S + k0 + 32, r1);
+        tmem_wait_ld();
+        if (last) {
+          float4 *dst = reinterpret_cast<float4 *>(a.S_T + unit_off + (long long)lrow * kD + k0);
+  #pragma unroll
+          for (int q = 0; q < 8; ++q)
+            dst[q] = make_float4(__uint_as_float(r0[4 * q]), __uint_as_float(r0[4 * q + 1]),
+                                 __uint_as_float(r0[4 * q + 2]), __uint_as_float(r0[4 * q + 3]));
+  #pragma unroll
+          for (int q = 0; q < 8; ++q)
+            dst[8 + q] = make_float4(__uint_as_float(r1[4 * q]), __uint_as_float(r1[4 * q + 1]),
+                                     __uint_as_float(r1[4 * q + 2]), __uint_as_float(r1[4 * q + 3]));
+        } else {
+          uint32_t w16[16];
+  #pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            w16[q] = pack2_inrange(__uint_as_float(r0[2 * q]), __uint_as_float(r0[2 * q + 1]));
+          }
+          tmem_st16w_nw(tl + TM_S16 + k0 / 2, w16);
+  #pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            w16[q] = pack2_inrange(__uint_as_float(r1[2 * q]), __uint_as_float(r1[2 * q + 1]));
+          }
+          tmem_st16w_nw(tl + TM_S16 + k0 / 2 + 16, w16);
+  #pragma unroll
+          for (int q = 0; q < 32; ++q) {
+            r0[q] = __float_as_uint(__uint_as_float(r0[q]) * dcn);
+            r1[q] = __float_as_uint(__uint_as_float(r1[q]) * dcn);
+          }
+          tmem_st32w_nw(tl + TM_S + k0, r0);
+          tmem_st32w_nw(tl + TM_S + k0 + 32, r1);
+          tmem_wait_st();
+        }
+      }
+      }
+    } else {
+      // MMA7 S += Delta^T (Gamma K), hi*hi + hi*lo + lo*hi: needed only in J3,
+      // issued once MMA6 is in the queue ahead of it
+      if (warp == 11) {
+        __syncwarp();
+        named_sync(kBarMma6, 64);
+      }
+      if (issuer2) {
+        fence_after();
+        auto b_gk = [&](int ks) { return desc_mn(sbase + OFF_GK, ks, kC); };
+        issue_ta(tmem + TM_S, tmem + TM_KQ, id_km128, 4, true, b_gk);
+        issue_ta(tmem + TM_S, tmem + TM_KQ, id_km128, 4, true, [&](int ks) { return desc_mn(sbase + OFF_GKL, ks, kC); });
+        issue_ta(tmem + TM_S, tmem + TM_KQ + 32, id_km128, 4, true, b_gk);
+        commit(&V.bar_s);
+      }
+      ph_o ^= 1u;
+      phase_z ^= 1u;
+      ph_s ^= 1u;
+      if (n + 1 < nchunks) {  // the next chunk's v tiles
+        __syncwarp();
+        const bool got = bar_wait(&V.bar_raw, phase_raw);
+        fence_after();
+        if (__all_sync(0xffffffffu, got)) {
+          front_end_v(sm, V.cv[(n + 1) & 1], d, conv_w, h, t0 + kC, T, tid);
+        } else if (lane == 0) {
+          atomicOr(a.err, kErrTimeout);
+          V.abort = 1;
+        }
+      }
     }
     ph_sq ^= 1u;
-    if (!wait_all(&V.bar_o, ph_o)) break;
-    // MMA7, needed only in J3: the state update runs while O is normalised
-    if (issuer2) {
-      fence_after();
-      auto b_gk = [&](int ks) { return desc_mn(sbase + OFF_GK, ks, kC); };
-      issue_ta(tmem + TM_S, tmem + TM_KQ, id_km128, 4, true, b_gk);
-      issue_ta(tmem + TM_S, tmem + TM_KQ, id_km128, 4, true, [&](int ks) { return desc_mn(sbase + OFF_GKL, ks, kC); });
-      issue_ta(tmem + TM_S, tmem + TM_KQ + 32, id_km128, 4, true, b_gk);
-      commit(&V.bar_s);
-    }
-    // J1: O^T = d (S Q^T) + Delta^T M^T -> staging [i][v]
-    if (warp < kTmemWarps) {
-      float *ost = reinterpret_cast<float *>(sm + OFF_OST);
-      uint32_t ra[32], rb[32];
-      tmem_ld32_nw(tl + TM_O1 + 32 * half, ra);
-      tmem_ld32_nw(tl + TM_O2 + 32 * half, rb);
-      tmem_wait_ld();
-      float v[32], w2[32];
-#pragma unroll
-      for (int q = 0; q < 32; ++q) {
-        v[q] = __uint_as_float(ra[q]);
-        w2[q] = __uint_as_float(rb[q]);
-      }
-#pragma unroll
-      for (int q = 0; q < 32; q += 4) {
-        const float4 dq = ld4(CV.d + 32 * half + q);
-        ost[(32 * half + q + 0) * kD + lrow] = fmaf(dq.x, v[q + 0], w2[q + 0]);
-        ost[(32 * half + q + 1) * kD + lrow] = fmaf(dq.y, v[q + 1], w2[q + 1]);
-        ost[(32 * half + q + 2) * kD + lrow] = fmaf(dq.z, v[q + 2], w2[q + 2]);
-        ost[(32 * half + q + 3) * kD + lrow] = fmaf(dq.w, v[q + 3], w2[q + 3]);
-      }
-    }
-    if (!wait_all(&V.bar_z, phase_z)) break;  // also the barrier after J1
-    z_pending = false;
-    // J2: gated RMSNorm per token, one half-warp per token (8 channels per
-    // lane), z from the staged rows
-    {
-      const float *ost = reinterpret_cast<const float *>(sm + OFF_OST);
-      const int hl = lane & 15;
-      float2 wn[4];
-      widen(*reinterpret_cast<const uint4 *>(static_cast<const bf16 *>(a.norm_w) + 8 * hl), wn);
-      const int nv = min(kC, T - t0);
-      bf16 *ob = static_cast<bf16 *>(a.o) + ((bos + t0) * d.Hv + h) * kD + 8 * hl;
-      const long long ostride = (long long)d.Hv * kD;
-#pragma unroll
-      for (int m = 0; m < 3; ++m) {
-        const int i = 2 * warp + (lane >> 4) + 24 * m;  // 24 tokens per round
-        const bool valid = i < nv;
-        float4 o0 = make_float4(0.f, 0.f, 0.f, 0.f), o1 = o0;
-        uint4 zr = make_uint4(0u, 0u, 0u, 0u);
-        if (valid) {
-          o0 = ld4(ost + i * kD + 8 * hl);
-          o1 = ld4(ost + i * kD + 8 * hl + 4);
-          zr = *reinterpret_cast<const uint4 *>(sm + OFF_Z + i * kD * 2 + 16 * hl);
-        }
-        float ss = dot4(o0, o0) + dot4(o1, o1);
-#pragma unroll
-        for (int off = 1; off < 16; off <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-        const float rstd = rsqrtf(ss * (1.0f / kD) + d.eps_norm);
-        float2 zz[4];
-        widen(zr, zz);
-        const float2 op[4] = {make_float2(o0.x, o0.y), make_float2(o0.z, o0.w), make_float2(o1.x, o1.y),
-                              make_float2(o1.z, o1.w)};
-        uint32_t yw[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float2 sg = silu2(zz[q]);
-          const float2 y = __fmul2_rn(__fmul2_rn(wn[q], __fmul2_rn(op[q], make_float2(rstd, rstd))), sg);
-          __nv_bfloat162 t = __floats2bfloat162_rn(y.x, y.y);
-          yw[q] = *reinterpret_cast<uint32_t *>(&t);
-        }
-        if (valid) *reinterpret_cast<uint4 *>(ob + i * ostride) = make_uint4(yw[0], yw[1], yw[2], yw[3]);
-      }
-    }
-    // J3: S -> fp16 copy and rescaled state (or S_T after the last chunk), in TMEM
-    if (!wait_all(&V.bar_s, ph_s)) break;
-    if (warp < kTmemWarps) {
-      const bool last = n + 1 == nchunks;
-      const float dcn = V.dC_next;
-      const int k0 = 64 * half;
-      uint32_t r0[32], r1[32];
-      tmem_ld32_nw(tl + TM_S + k0, r0);
-      tmem_ld32_nw(tl + TM_S + k0 + 32, r1);
-      tmem_wait_ld();
-      if (last) {
-        float4 *dst = reinterpret_cast<float4 *>(a.S_T + unit_off + (long long)lrow * kD + k0);
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          dst[q] = make_float4(__uint_as_float(r0[4 * q]), __uint_as_float(r0[4 * q + 1]),
-                               __uint_as_float(r0[4 * q + 2]), __uint_as_float(r0[4 * q + 3]));
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          dst[8 + q] = make_float4(__uint_as_float(r1[4 * q]), __uint_as_float(r1[4 * q + 1]),
-                                   __uint_as_float(r1[4 * q + 2]), __uint_as_float(r1[4 * q + 3]));
-      } else {
-        uint32_t w16[16];
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          w16[q] = pack2_inrange(__uint_as_float(r0[2 * q]), __uint_as_float(r0[2 * q + 1]));
-        }
-        tmem_st16w_nw(tl + TM_S16 + k0 / 2, w16);
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          w16[q] = pack2_inrange(__uint_as_float(r1[2 * q]), __uint_as_float(r1[2 * q + 1]));
-        }
-        tmem_st16w_nw(tl + TM_S16 + k0 / 2 + 16, w16);
-#pragma unroll
-        for (int q = 0; q < 32; ++q) {
-          r0[q] = __float_as_uint(__uint_as_float(r0[q]) * dcn);
-          r1[q] = __float_as_uint(__uint_as_float(r1[q]) * dcn);
-        }
-        tmem_st32w_nw(tl + TM_S + k0, r0);
-        tmem_st32w_nw(tl + TM_S + k0 + 32, r1);
-        tmem_wait_st();
-      }
-    }
+    if (n + 1 < nchunks) phase_raw ^= 1u;  // consumed by warps 8-11 above
     fence_before();
-    fence_smem_to_async();  // z and the staging were read: order before the next TMA writes
+    fence_smem_to_async();  // z, the staging and the next v tiles: order before the next TMA and MMA reads
     __syncthreads();
+    if (V.abort) break;
     if (n + 1 < nchunks) {
+      raw_pending = false;
       if (tid == 0) request_z(t0 + kC);
       z_pending = true;
     }
