@@ -67,6 +67,7 @@ constexpr int kTmemWarps = 8;   // warps 0..7 do the TMEM <-> register passes (t
 constexpr float kGMin = -80.0f;
 constexpr int kBarTmem = 1;  // named barrier of warps 0-7 in the epilogue
 constexpr int kBarMma6 = 2;  // warp 0 (MMA6 issued) -> warp 11 (may issue MMA7)
+constexpr int kBarMma3 = 3;  // warp 0 (MMA3 issued) -> warp 11 (may issue MMA2)
 
 __device__ __forceinline__ void named_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -893,27 +894,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (n + 1 < nchunks) request_raw(t0 + kC);
     }
     if (n + 1 < nchunks) raw_pending = true;
-    if (!wait_all(&V.bar_w, ph_w)) break;
-    // MMA2 U^T, needed only by MMA4
-    if (issuer2) {
-      fence_after();
-      auto a_vh = [&](int ks) { return desc_mn(sbase + OFF_VH, ks, kC); };
-      auto b_tu = [&](int ks) { return desc_k(sbase + OFF_TU, ks, kC); };
-      issue(tmem + TM_U, id_mk, 4, false, a_vh, b_tu);
-      issue(tmem + TM_U, id_mk, 4, true, [&](int ks) { return desc_mn(sbase + OFF_VL, ks, kC); }, b_tu);
-      issue(tmem + TM_U, id_mk, 4, true, a_vh, [&](int ks) { return desc_k(sbase + OFF_TUL, ks, kC); });
-      commit(&V.bar_u);
-    }
-    // F: -W^T (lanes k, columns i) -> MN-major [k][i]
     if (warp < kTmemWarps) {
-      float v[32];
-      tmem_ld32(tl + TM_W + 32 * half, v);
+      if (warp == 0) {
+        __syncwarp();
+        named_arrive(kBarMma3, 64);
+      }
+      // F: -W^T (lanes k, columns i) -> MN-major [k][i]
+      if (wait_tmem(&V.bar_w, ph_w)) {
+        float v[32];
+        tmem_ld32(tl + TM_W + 32 * half, v);
 #pragma unroll
-      for (int q = 0; q < 32; ++q) v[q] = -v[q];
+        for (int q = 0; q < 32; ++q) v[q] = -v[q];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) st_h8_inrange(sm + OFF_NW + mnmaj(32 * half + 8 * q, lrow, kD), v + 8 * q);
+        for (int q = 0; q < 4; ++q) st_h8_inrange(sm + OFF_NW + mnmaj(32 * half + 8 * q, lrow, kD), v + 8 * q);
+      }
+    } else {
+      // MMA2 U^T, needed only by MMA4: issued behind MMA3 while F runs
+      if (warp == 11) {
+        __syncwarp();
+        named_sync(kBarMma3, 64);
+      }
+      if (issuer2) {
+        fence_after();
+        auto a_vh = [&](int ks) { return desc_mn(sbase + OFF_VH, ks, kC); };
+        auto b_tu = [&](int ks) { return desc_k(sbase + OFF_TU, ks, kC); };
+        issue(tmem + TM_U, id_mk, 4, false, a_vh, b_tu);
+        issue(tmem + TM_U, id_mk, 4, true, [&](int ks) { return desc_mn(sbase + OFF_VL, ks, kC); }, b_tu);
+        issue(tmem + TM_U, id_mk, 4, true, a_vh, [&](int ks) { return desc_k(sbase + OFF_TUL, ks, kC); });
+        commit(&V.bar_u);
+      }
+      ph_w ^= 1u;
     }
     smem_ready();
+    if (V.abort) break;
     // G: MMA4 Delta^T = U^T - S W^T (S from TMEM), after MMA2 (the other issuer)
     if (tid == 0) {
       bar_wait(&V.bar_u, ph_u);  // bounded; a stall here ends in the timeout below
