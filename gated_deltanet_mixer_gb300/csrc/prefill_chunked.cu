@@ -379,7 +379,9 @@ __device__ __forceinline__ void fe_pass(uint8_t *sm, const ChunkVecs &V, const D
 // with_v: the first chunk; later chunks' v tiles are made by warps 8-11
 // during the previous chunk's epilogue (front_end_v), so the others split
 // q and k between all twelve warps: k on warps 0-7 (4 tokens per half-warp),
-// q on warps 8-11 (8 tokens).
+// q on warps 8-11 (7 tokens) and the last 8 q tokens on warps 0-3 (one per
+// half-warp, before their k): at most 586 units per half-warp, against 624
+// with all of q on warps 8-11.
 __device__ void front_end(uint8_t *sm, const ChunkVecs &V, const Dims &d, const bf16 *conv_w,
                           int h, int kh, int t0, int T, int tid, bool with_v) {
   const int warp = tid >> 5, lane = tid & 31, grp = lane & 15;
@@ -394,9 +396,10 @@ __device__ void front_end(uint8_t *sm, const ChunkVecs &V, const Dims &d, const 
       fe_pass<8>(sm, V, d, conv_w, 2, 2LL * d.Hk * kD + (long long)h * kD + 8 * grp, r0, t0, T, grp);
     }
   } else if (warp < 8) {
+    if (warp < 4) fe_pass<1>(sm, V, d, conv_w, 0, cq, 56 + 2 * warp + (lane >> 4), t0, T, grp);
     fe_pass<4>(sm, V, d, conv_w, 1, ck, 4 * (2 * warp + (lane >> 4)), t0, T, grp);
   } else {
-    fe_pass<8>(sm, V, d, conv_w, 0, cq, 8 * (2 * (warp - 8) + (lane >> 4)), t0, T, grp);
+    fe_pass<7>(sm, V, d, conv_w, 0, cq, 7 * (2 * (warp - 8) + (lane >> 4)), t0, T, grp);
   }
 }
 // The v tiles of the chunk starting at t0 (warps 8-11, 8 tokens per half-warp).
