@@ -36,7 +36,7 @@
 //   B  MMA1  [K;Q] K^T -> K K^T, Q K^T;  MMA5  S Q^T
 //   C  decayed lower-triangular L (fp32) and M (fp16)
 //   D  T = (I + L)^{-1} in 16 x 16 blocks (fp32, CUDA cores) -> T B, T B D
-//   E  MMA2  U^T = V^T (T B)^T (split);  MMA3  W^T = K^T (T B D)^T;
+//   E  MMA2  U^T = V^T (T B)^T (split);  MMA3  -W^T = K^T (-T B D)^T;
 //      the next chunk's raw rows are requested (TMA)
 //   F  -W^T to shared memory
 //   G  MMA4  Delta^T = U^T - S W^T
@@ -96,7 +96,7 @@ constexpr uint32_t OFF_VL = 49152;      // V lo                                1
 constexpr uint32_t OFF_GK = 65536;      // Gamma K hi  MN-major [j][k]         16 KB
 constexpr uint32_t OFF_GKL = 81920;     // Gamma K lo                          16 KB
 constexpr uint32_t OFF_TU = 98304;      // T diag(beta)      K-major [i][j]     8 KB
-constexpr uint32_t OFF_TW = 106496;     // T diag(beta d)    K-major [i][j]     8 KB
+constexpr uint32_t OFF_TW = 106496;     // -T diag(beta d)   K-major [i][j]     8 KB
 constexpr uint32_t OFF_M = 114688;      // M         K-major [i][j]             8 KB
 constexpr uint32_t OFF_NW = 122880;     // -W^T      MN-major [k][i]           16 KB
 constexpr uint32_t OFF_TUL = 139264;    // T diag(beta), low part               8 KB
@@ -423,14 +423,15 @@ __device__ __forceinline__ void fma4(float4 &acc, float s, const float4 t) {
 }
 
 // Row i, columns j .. j+3 (j % 4 == 0) of T -> the fp16 K-major tiles
-// T diag(beta) (hi, lo) and T diag(beta d), one 8-byte store each.
+// T diag(beta) (hi, lo) and -T diag(beta d) (negated, so that MMA3 yields
+// -W^T, the operand MMA4 wants), one 8-byte store each.
 __device__ __forceinline__ void store_T4(uint8_t *sm, const ChunkVecs &V, int i, int j, float4 t) {
   const float4 b = ld4(V.beta + j), e = ld4(V.bd + j);
   uint32_t hw[2], lw[2], ww[2];
   split2(t.x * b.x, t.y * b.y, hw[0], lw[0]);
   split2(t.z * b.z, t.w * b.w, hw[1], lw[1]);
-  __half2 w0 = __halves2half2(to_h(t.x * e.x), to_h(t.y * e.y));
-  __half2 w1 = __halves2half2(to_h(t.z * e.z), to_h(t.w * e.w));
+  __half2 w0 = __halves2half2(to_h(-(t.x * e.x)), to_h(-(t.y * e.y)));
+  __half2 w1 = __halves2half2(to_h(-(t.z * e.z)), to_h(-(t.w * e.w)));
   ww[0] = *reinterpret_cast<uint32_t *>(&w0);
   ww[1] = *reinterpret_cast<uint32_t *>(&w1);
   const uint32_t o = kmaj(i, j, kC);
@@ -885,7 +886,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     solve_T(sm, CV, tid);
     smem_ready();
-    // E: MMA2 U^T = V^T (T B)^T, hi*hi + lo*hi + hi*lo; MMA3 W^T = K^T (T B D)^T
+    // E: MMA2 U^T = V^T (T B)^T, hi*hi + lo*hi + hi*lo; MMA3 -W^T = K^T (-T B D)^T
     // (K^ read from [K;Q] as an MN-major operand).  The raw rows are free now:
     // request the next chunk's.
     if (tid == 0) {
@@ -902,12 +903,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         named_arrive(kBarMma3, 64);
       }
-      // F: -W^T (lanes k, columns i) -> MN-major [k][i]
+      // F: -W^T (lanes k, columns i; the sign comes from the T tile) -> MN-major [k][i]
       if (wait_tmem(&V.bar_w, ph_w)) {
         float v[32];
         tmem_ld32(tl + TM_W + 32 * half, v);
-#pragma unroll
-        for (int q = 0; q < 32; ++q) v[q] = -v[q];
 #pragma unroll
         for (int q = 0; q < 4; ++q) st_h8_inrange(sm + OFF_NW + mnmaj(32 * half + 8 * q, lrow, kD), v + 8 * q);
       }
@@ -986,10 +985,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   #pragma unroll
         for (int q = 0; q < 32; q += 4) {
           const float4 dq = ld4(CV.d + 32 * half + q);
-          ost[(32 * half + q + 0) * kD + lrow] = fmaf(dq.x, v[q + 0], w2[q + 0]);
-          ost[(32 * half + q + 1) * kD + lrow] = fmaf(dq.y, v[q + 1], w2[q + 1]);
-          ost[(32 * half + q + 2) * kD + lrow] = fmaf(dq.z, v[q + 2], w2[q + 2]);
-          ost[(32 * half + q + 3) * kD + lrow] = fmaf(dq.w, v[q + 3], w2[q + 3]);
+          const float2 o01 = __ffma2_rn(make_float2(dq.x, dq.y), make_float2(v[q], v[q + 1]), make_float2(w2[q], w2[q + 1]));
+          const float2 o23 = __ffma2_rn(make_float2(dq.z, dq.w), make_float2(v[q + 2], v[q + 3]),
+                                        make_float2(w2[q + 2], w2[q + 3]));
+          ost[(32 * half + q + 0) * kD + lrow] = o01.x;
+          ost[(32 * half + q + 1) * kD + lrow] = o01.y;
+          ost[(32 * half + q + 2) * kD + lrow] = o23.x;
+          ost[(32 * half + q + 3) * kD + lrow] = o23.y;
         }
       }
       }
@@ -1071,9 +1073,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_st16w_nw(tl + TM_S16 + k0 / 2 + 16, w16);
   #pragma unroll
-          for (int q = 0; q < 32; ++q) {
-            r0[q] = __float_as_uint(__uint_as_float(r0[q]) * dcn);
-            r1[q] = __float_as_uint(__uint_as_float(r1[q]) * dcn);
+          for (int q = 0; q < 32; q += 2) {  // paired fp32 multiplies
+            float2 x0 = __fmul2_rn(make_float2(__uint_as_float(r0[q]), __uint_as_float(r0[q + 1])), make_float2(dcn, dcn));
+            float2 x1 = __fmul2_rn(make_float2(__uint_as_float(r1[q]), __uint_as_float(r1[q + 1])), make_float2(dcn, dcn));
+            r0[q] = __float_as_uint(x0.x);
+            r0[q + 1] = __float_as_uint(x0.y);
+            r1[q] = __float_as_uint(x1.x);
+            r1[q + 1] = __float_as_uint(x1.y);
           }
           tmem_st32w_nw(tl + TM_S + k0, r0);
           tmem_st32w_nw(tl + TM_S + k0 + 32, r1);
