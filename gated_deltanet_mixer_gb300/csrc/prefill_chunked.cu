@@ -262,16 +262,16 @@ __device__ __forceinline__ void split2(float a, float b, uint32_t &whi, uint32_t
   a = fminf(fmaxf(a, -kHalfMax), kHalfMax);
   b = fminf(fmaxf(b, -kHalfMax), kHalfMax);
   __half2 th = __floats2half2_rn(a, b);
-  const float2 back = __half22float2(th);
-  __half2 tl = __floats2half2_rn(a - back.x, b - back.y);
+  const float2 r = __ffma2_rn(__half22float2(th), make_float2(-1.f, -1.f), make_float2(a, b));  // v - hi
+  __half2 tl = __floats2half2_rn(r.x, r.y);
   whi = *reinterpret_cast<uint32_t *>(&th);
   wlo = *reinterpret_cast<uint32_t *>(&tl);
 }
 // hi/lo of a pair known to lie well inside the fp16 range (no clamp).
 __device__ __forceinline__ void split2_inrange(float a, float b, uint32_t &whi, uint32_t &wlo) {
   __half2 th = __floats2half2_rn(a, b);
-  const float2 back = __half22float2(th);
-  __half2 tl = __floats2half2_rn(a - back.x, b - back.y);
+  const float2 r = __ffma2_rn(__half22float2(th), make_float2(-1.f, -1.f), make_float2(a, b));  // v - hi
+  __half2 tl = __floats2half2_rn(r.x, r.y);
   whi = *reinterpret_cast<uint32_t *>(&th);
   wlo = *reinterpret_cast<uint32_t *>(&tl);
 }
@@ -846,10 +846,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int q = 0; q < 32; q += 4) {
           const float4 dv = ld4(CV.dinv + j0 + q);
-          rr[q] = di * dv.x;
-          rr[q + 1] = di * dv.y;
-          rr[q + 2] = di * dv.z;
-          rr[q + 3] = di * dv.w;
+          const float2 r01 = __fmul2_rn(make_float2(di, di), make_float2(dv.x, dv.y));
+          const float2 r23 = __fmul2_rn(make_float2(di, di), make_float2(dv.z, dv.w));
+          rr[q] = r01.x;
+          rr[q + 1] = r01.y;
+          rr[q + 2] = r23.x;
+          rr[q + 3] = r23.y;
         }
       } else {
         const float gi = CV.G[i];
@@ -861,16 +863,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         float *L = reinterpret_cast<float *>(sm + OFF_L) + i * kLs + j0;
 #pragma unroll
         for (int q = 0; q < 32; q += 4) {
+          const float2 p01 = __fmul2_rn(__fmul2_rn(make_float2(bi, bi), make_float2(v[q], v[q + 1])),
+                                        make_float2(rr[q], rr[q + 1]));
+          const float2 p23 = __fmul2_rn(__fmul2_rn(make_float2(bi, bi), make_float2(v[q + 2], v[q + 3])),
+                                        make_float2(rr[q + 2], rr[q + 3]));
           float4 f;
-          f.x = (j0 + q + 0 < i) ? bi * v[q + 0] * rr[q + 0] : 0.f;
-          f.y = (j0 + q + 1 < i) ? bi * v[q + 1] * rr[q + 1] : 0.f;
-          f.z = (j0 + q + 2 < i) ? bi * v[q + 2] * rr[q + 2] : 0.f;
-          f.w = (j0 + q + 3 < i) ? bi * v[q + 3] * rr[q + 3] : 0.f;
+          f.x = (j0 + q + 0 < i) ? p01.x : 0.f;
+          f.y = (j0 + q + 1 < i) ? p01.y : 0.f;
+          f.z = (j0 + q + 2 < i) ? p23.x : 0.f;
+          f.w = (j0 + q + 3 < i) ? p23.y : 0.f;
           *reinterpret_cast<float4 *>(L + q) = f;
         }
       } else {
 #pragma unroll
-        for (int q = 0; q < 32; ++q) v[q] = (j0 + q <= i) ? v[q] * rr[q] : 0.f;
+        for (int q = 0; q < 32; q += 2) {
+          const float2 p = __fmul2_rn(make_float2(v[q], v[q + 1]), make_float2(rr[q], rr[q + 1]));
+          v[q] = (j0 + q <= i) ? p.x : 0.f;
+          v[q + 1] = (j0 + q + 1 <= i) ? p.y : 0.f;
+        }
 #pragma unroll
         for (int q = 0; q < 4; ++q) st_h8_inrange(sm + OFF_M + kmaj(i, j0 + 8 * q, kC), v + 8 * q);  // |M| <= q_scale
       }
