@@ -47,6 +47,24 @@ __device__ __forceinline__ float conv_token(const IO *win, const IO *x, const IO
   return silu(acc);
 }
 
+// s . k for one state row, on the paired fp32 pipes: (x, y) and (z, w) lanes
+// in parallel, then one add.  Used by the T-token kernel, whose serial token
+// steps are arithmetic-bound; the single-token kernel, bound by the state
+// stream, measured faster with the scalar form.
+__device__ __forceinline__ float dot4p(float4 s, float4 k) {
+  const float2 acc = __ffma2_rn(make_float2(s.x, s.y), make_float2(k.x, k.y),
+                                __fmul2_rn(make_float2(s.z, s.w), make_float2(k.z, k.w)));
+  return acc.x + acc.y;
+}
+// alpha s + di k for one state row (fmaf(alpha, s, di * k) per element), paired.
+__device__ __forceinline__ float4 decay_update(float4 s, float alpha, float di, float4 k) {
+  const float2 n01 = __ffma2_rn(make_float2(alpha, alpha), make_float2(s.x, s.y),
+                                __fmul2_rn(make_float2(di, di), make_float2(k.x, k.y)));
+  const float2 n23 = __ffma2_rn(make_float2(alpha, alpha), make_float2(s.z, s.w),
+                                __fmul2_rn(make_float2(di, di), make_float2(k.z, k.w)));
+  return make_float4(n01.x, n01.y, n23.x, n23.y);
+}
+
 template <typename IO, bool kRawGates>
 __global__ void __launch_bounds__(kThreads, 2) decode1_kernel(DecodeArgs a) {
   const Dims d = a.d;
@@ -284,8 +302,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
     float part[32];
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i) {
-      part[i] = dot4(s[i], k4);
-      part[16 + i] = dot4(s[i], q4);
+      part[i] = dot4p(s[i], k4);
+      part[16 + i] = dot4p(s[i], q4);
     }
     // lane L < 16: (S k^)[row0 + L];  lane L >= 16: (S q^)[row0 + L - 16]
     const float red = transpose_reduce32(part, lane);
@@ -297,10 +315,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i) {
       const float di = __shfl_sync(0xffffffffu, delta, i);
-      s[i].x = fmaf(alpha, s[i].x, di * k4.x);
-      s[i].y = fmaf(alpha, s[i].y, di * k4.y);
-      s[i].z = fmaf(alpha, s[i].z, di * k4.z);
-      s[i].w = fmaf(alpha, s[i].w, di * k4.w);
+      s[i] = decay_update(s[i], alpha, di, k4);
     }
     if (a.S_snap) {
       float *snap = a.S_snap + (((long long)b * T + t) * d.Hv + h) * (kD * kD);
