@@ -193,12 +193,35 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
   __shared__ __align__(16) float s_k[kDecodeMaxT][kD];
   __shared__ float s_v[kDecodeMaxT][kD];
   __shared__ __align__(16) float s_o[kDecodeMaxT][kD];
+  __shared__ __align__(16) float s_z[kDecodeMaxT][kD];
   __shared__ float s_kq[kDecodeMaxT];
+  __shared__ float s_g[kDecodeMaxT], s_b[kDecodeMaxT];
 
   const IO *x = static_cast<const IO *>(a.qkv_pre) + (long long)b * T * C;
   const IO *win = static_cast<const IO *>(a.conv_in) + (long long)b * 3 * C;
   IO *wout = static_cast<IO *>(a.conv_out) + (long long)b * 3 * C;
   const IO *cw = static_cast<const IO *>(a.conv_w);
+
+  // The gates of every token and the z rows of the gated norm, fetched now so
+  // that their loads overlap the front end's instead of sitting one after
+  // another inside the token steps.
+  if (tid < T) {
+    const long long i = ((long long)b * T + tid) * d.Hv + h;
+    float gt, bt;
+    if (kRawGates) {
+      gate_at<IO>(a.gate, i, h, gt, bt);
+    } else {
+      gt = a.gate.g[i];
+      bt = a.gate.beta[i];
+    }
+    s_g[tid] = gt;
+    s_b[tid] = bt;
+  }
+  for (int e = tid; e < T * (kD / 4); e += kThreads) {  // four channels per load
+    const int t = e / (kD / 4), c = 4 * (e % (kD / 4));
+    reinterpret_cast<float4 *>(s_z[t])[c / 4] =
+        ld_io4(static_cast<const IO *>(a.z) + (((long long)b * T + t) * d.Hv + h) * kD + c);
+  }
 
   // ---- front end: conv + SiLU of the T tokens, sliding the window of the
   // channel(s) this thread owns (q and k of key head kh, or v of head h)
@@ -278,25 +301,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
   const long long gi = (long long)b * d.Hv + h;
   float *S = a.S + gi * (kD * kD);
   const int row0 = warp * kRowsPerWarp;
-  // gates of token t (every thread reads the same element: a broadcast load)
-  auto gates = [&](int t, float &gt, float &bt) {
-    const long long i = ((long long)b * T + t) * d.Hv + h;
-    if (kRawGates) {
-      gate_at<IO>(a.gate, i, h, gt, bt);
-    } else {
-      gt = a.gate.g[i];
-      bt = a.gate.beta[i];
-    }
-  };
-  float g_nx, b_nx;
-  gates(0, g_nx, b_nx);
   float4 s[kRowsPerWarp];
 #pragma unroll
   for (int i = 0; i < kRowsPerWarp; ++i) s[i] = ld_stream(S + (row0 + i) * kD + 4 * lane);
 
   for (int t = 0; t < T; ++t) {
-    const float alpha = expf(g_nx), beta = b_nx, kq = s_kq[t];
-    if (t + 1 < T) gates(t + 1, g_nx, b_nx);
+    const float alpha = expf(s_g[t]), beta = s_b[t], kq = s_kq[t];
     const float4 k4 = reinterpret_cast<const float4 *>(s_k[t])[lane];
     const float4 q4 = reinterpret_cast<const float4 *>(s_q[t])[lane];
     float part[32];
@@ -333,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
     const float4 o4 = reinterpret_cast<const float4 *>(s_o[t])[lane];
     const float rstd = rsqrtf(warp_sum(dot4(o4, o4)) * (1.0f / kD) + d.eps_norm);
     const long long oi = (((long long)b * T + t) * d.Hv + h) * kD + 4 * lane;  // [B][T][Hv*Dv]
-    const float4 z4 = ld_io4(static_cast<const IO *>(a.z) + oi);
+    const float4 z4 = reinterpret_cast<const float4 *>(s_z[t])[lane];
     float4 y;
     y.x = w4.x * (o4.x * rstd) * silu(z4.x);
     y.y = w4.y * (o4.y * rstd) * silu(z4.y);
