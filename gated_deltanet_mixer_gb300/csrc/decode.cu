@@ -86,6 +86,17 @@ __global__ void __launch_bounds__(kThreads, 2) decode1_kernel(DecodeArgs a) {
   IO *wout = static_cast<IO *>(a.conv_out) + (long long)b * 3 * C;
   const IO *cw = static_cast<const IO *>(a.conv_w);
 
+  // This warp's 16 state rows and this thread's z element, requested first:
+  // their latency overlaps the front end's.  (Requesting the gates here too
+  // measured slower.)
+  const long long gi = (long long)b * d.Hv + h;
+  float *S = a.S + gi * (kD * kD);
+  const int row0 = warp * kRowsPerWarp;
+  float4 s[kRowsPerWarp];
+#pragma unroll
+  for (int i = 0; i < kRowsPerWarp; ++i) s[i] = ld_stream(S + (row0 + i) * kD + 4 * lane);
+  const float zv = tid < kD ? ld_io(static_cast<const IO *>(a.z) + gi * kD + tid) : 0.f;
+
   // ---- front end: conv + SiLU (q, k of key head kh; v of head h), L2 norms
   float qraw = 0.f, kraw = 0.f;
   if (tid < kD) {
@@ -118,7 +129,6 @@ __global__ void __launch_bounds__(kThreads, 2) decode1_kernel(DecodeArgs a) {
   __syncthreads();
 
   // ---- state pass: each warp streams its 16 rows once
-  const long long gi = (long long)b * d.Hv + h;
   float gt, beta;
   if (kRawGates) {
     gate_at<IO>(a.gate, gi, h, gt, beta);
@@ -130,12 +140,6 @@ __global__ void __launch_bounds__(kThreads, 2) decode1_kernel(DecodeArgs a) {
   const float kq = s_kq;
   const float4 k4 = reinterpret_cast<const float4 *>(s_k)[lane];
   const float4 q4 = reinterpret_cast<const float4 *>(s_q)[lane];
-  float *S = a.S + gi * (kD * kD);
-  const int row0 = warp * kRowsPerWarp;
-
-  float4 s[kRowsPerWarp];
-#pragma unroll
-  for (int i = 0; i < kRowsPerWarp; ++i) s[i] = ld_stream(S + (row0 + i) * kD + 4 * lane);
 
   float part[32];
 #pragma unroll
@@ -173,7 +177,6 @@ __global__ void __launch_bounds__(kThreads, 2) decode1_kernel(DecodeArgs a) {
     float tot = s_red[0][0] + s_red[1][0] + s_red[2][0] + s_red[3][0];
     float rstd = rsqrtf(tot * (1.0f / kD) + d.eps_norm);
     const long long oi = gi * kD + tid;  // [B][Hv*Dv]
-    float zv = ld_io(static_cast<const IO *>(a.z) + oi);
     float wv = ld_io(static_cast<const IO *>(a.norm_w) + tid);
     st_io(static_cast<IO *>(a.o) + oi, wv * (ov * rstd) * silu(zv));
   }
