@@ -200,6 +200,22 @@ def dist_env():
     return world, rank, local
 
 
+def rank_case(case, rank):
+    """Input seed of `case` on `rank`: every rank draws its own batch."""
+    return case + 1000 * rank
+
+
+def max_over_ranks(x, world, device="cuda"):
+    """The largest of every rank's `x` (a time in ms); `x` itself at world 1."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ----------------------------------------------------------- oracle timing
 def oracle_run(p, n_tok, threads):
     """The oracle, as it stands, on the workload's first `n_tok` tokens: whole
@@ -247,7 +263,7 @@ def gdn_arm(args, world, rank, local):
 
     # ---- prefill inputs (each rank its own batch)
     spec = dict(I.CASES[args.workload])
-    spec["case"] = spec["case"] + 1000 * rank
+    spec["case"] = rank_case(spec["case"], rank)
     p = I.prefill_problem(**spec)
     t_io = torch.bfloat16 if p.io == "bf16" else torch.float32
     a = p.arrays
@@ -298,11 +314,7 @@ def gdn_arm(args, world, rank, local):
         raise RuntimeError("device status not OK after the prefill timing")
     total_ms = t_beg.elapsed_time(t_end)
     launch_ms = float(np.mean([s.elapsed_time(e) for s, e in ev]))
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(total_ms, world)
     ms_per_step = total_ms / args.steps
     tokens = p.B * p.T
     value = world * tokens / (ms_per_step * 1e-3)
@@ -310,7 +322,7 @@ def gdn_arm(args, world, rank, local):
     # ---- decode: 64 consecutive calls per step, inputs resident
     dec = None
     if not args.no_decode:
-        dp = I.decode_problem(**dict(I.DECODE_CASE, case=I.DECODE_CASE["case"] + 1000 * rank))
+        dp = I.decode_problem(**dict(I.DECODE_CASE, case=rank_case(I.DECODE_CASE["case"], rank)))
         S = dev(dp.S)
         conv = [dev(dp.conv, t_io), dev(dp.conv, t_io)]
         cw, nw = dev(dp.conv_w, t_io), dev(dp.norm_w, t_io)
@@ -337,11 +349,7 @@ def gdn_arm(args, world, rank, local):
         if gdn.gdn_device_status(stream) != 0:
             raise RuntimeError("device status not OK after the decode timing")
         dec_ms = d0.elapsed_time(d1)
-        if world > 1:
-            import torch.distributed as dist
-            tt = torch.tensor([dec_ms], device="cuda")
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            dec_ms = float(tt.item())
+        dec_ms = max_over_ranks(dec_ms, world)
         call_ms = dec_ms / (args.steps * DECODE_CALLS_PER_STEP)
         dbytes = decode_bytes(dp.B, dp.Hk, dp.Hv)
         sbytes = decode_state_bytes(dp.B, dp.Hv)
@@ -419,11 +427,7 @@ def gdn_arm(args, world, rank, local):
     e1.record(s_out)
     barrier()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e2e_ms, world)
 
     # ---- roofline of the prefill kernel
     pbytes = prefill_bytes(p.B, p.T, p.Hk, p.Hv, 2 if p.io == "bf16" else 4)
@@ -480,8 +484,9 @@ def gdn_arm(args, world, rank, local):
 PREFILL_SOURCE = "gated_deltanet_mixer_gb300/csrc/prefill_chunked.cu"
 
 
-def time_launches(fn, steps, warmup, stream, barrier):
-    """Mean device ms per call of fn (one library call), CUDA events on `stream`."""
+def time_launches(fn, steps, warmup, stream, barrier, world=1):
+    """Mean device ms per call of fn (one library call), CUDA events on
+    `stream`; the largest over the ranks."""
     import torch
     for _ in range(warmup):
         fn()
@@ -493,7 +498,7 @@ def time_launches(fn, steps, warmup, stream, barrier):
         fn()
         ev[k][1].record(stream)
     barrier()
-    return float(np.mean([s.elapsed_time(e) for s, e in ev]))
+    return max_over_ranks(float(np.mean([s.elapsed_time(e) for s, e in ev])), world)
 
 
 def next_rows(args, x, o, S_T, conv_T, p, peaks, peak_src, stream, barrier, world, rank):
@@ -513,12 +518,12 @@ def next_rows(args, x, o, S_T, conv_T, p, peaks, peak_src, stream, barrier, worl
     steps = max(3, min(args.steps, 10))
 
     # raw gate projections on the 4B prefill workload
-    rg = I.raw_gate_arrays(60 + 1000 * rank, (p.B, p.T), p.Hv, "bf16")
+    rg = I.raw_gate_arrays(rank_case(60, rank), (p.B, p.T), p.Hv, "bf16")
     rgd = dict(a=dev(rg["a"], bf), b=dev(rg["b"], bf), A_log=dev(rg["A_log"]),
                dt_bias=dev(rg["dt_bias"]))
     ms = time_launches(lambda: gdn.gdn_prefill_ex(
         x["qkv_pre"], x["z"], None, None, x["conv_w"], x["norm_w"], x["S0"], x["conv0"], o, S_T,
-        conv_T, Hk=p.Hk, Hv=p.Hv, raw_gates=rgd, stream=stream), steps, args.warmup, stream, barrier)
+        conv_T, Hk=p.Hk, Hv=p.Hv, raw_gates=rgd, stream=stream), steps, args.warmup, stream, barrier, world)
     nb = packed_bytes([p.T] * p.B, p.Hk, p.Hv, raw_gates=True)
     out["prefill_raw_gates"] = {
         "workload": "4B-shaped prefill (B=%d, T=%d) with beta, g formed from raw a, b, A_log, "
@@ -530,7 +535,7 @@ def next_rows(args, x, o, S_T, conv_T, p, peaks, peak_src, stream, barrier, worl
 
     # packed variable-length batch at the 4B head shape
     lens = varlen_lengths()
-    q = I.packed_problem(lens, p.Hk, p.Hv, io="bf16", case=61 + 1000 * rank)
+    q = I.packed_problem(lens, p.Hk, p.Hv, io="bf16", case=rank_case(61, rank))
     qa = q.arrays
     qx = {k: dev(qa[k], bf if k in ("qkv_pre", "z", "conv_w", "norm_w", "conv0") else torch.float32)
           for k in ("qkv_pre", "z", "g", "beta", "conv_w", "norm_w", "S0", "conv0")}
@@ -541,7 +546,7 @@ def next_rows(args, x, o, S_T, conv_T, p, peaks, peak_src, stream, barrier, worl
     ms = time_launches(lambda: gdn.gdn_prefill_ex(
         qx["qkv_pre"], qx["z"], qx["g"], qx["beta"], qx["conv_w"], qx["norm_w"], qx["S0"],
         qx["conv0"], qo, qS, qc, Hk=p.Hk, Hv=p.Hv, cu_seqlens=cu, stream=stream), steps,
-        args.warmup, stream, barrier)
+        args.warmup, stream, barrier, world)
     nb = packed_bytes(lens, p.Hk, p.Hv)
     out["prefill_varlen"] = {
         "workload": "packed batch of %d sequences (log-uniform lengths 100..4000, %d tokens), "
@@ -553,7 +558,7 @@ def next_rows(args, x, o, S_T, conv_T, p, peaks, peak_src, stream, barrier, worl
 
     # T-token decode from the cache (speculative verification), 27B decode shape
     T = 4
-    dp = I.decode_problem(**dict(I.DECODE_CASE, steps=T, case=I.DECODE_CASE["case"] + 70 + 1000 * rank))
+    dp = I.decode_problem(**dict(I.DECODE_CASE, steps=T, case=rank_case(I.DECODE_CASE["case"] + 70, rank)))
     S = dev(dp.S)
     snap = torch.empty(dp.B, T, dp.Hv, D, D, device="cuda")
     conv_in, conv_out = dev(dp.conv, bf), torch.empty(dp.B, 3, dp.C, device="cuda", dtype=bf)
@@ -565,7 +570,7 @@ def next_rows(args, x, o, S_T, conv_T, p, peaks, peak_src, stream, barrier, worl
     for with_snap in (True, False):
         ms = time_launches(lambda: gdn.gdn_decode_ex(
             tq, tz, tg, tb, cw, nw, S, conv_in, conv_out, od, Hk=dp.Hk, Hv=dp.Hv,
-            S_snap=snap if with_snap else None, stream=stream), steps, args.warmup, stream, barrier)
+            S_snap=snap if with_snap else None, stream=stream), steps, args.warmup, stream, barrier, world)
         nb = decode_multi_bytes(dp.B, T, dp.Hk, dp.Hv, snapshots=with_snap)
         out["decode_multi%s" % ("_snapshots" if with_snap else "")] = {
             "workload": "27B-shaped decode of %d tokens per sequence from the cache, B=%d, Hv=%d%s"
@@ -579,7 +584,7 @@ def next_rows(args, x, o, S_T, conv_T, p, peaks, peak_src, stream, barrier, worl
     # the projections around the mixer at the 27B shape, 8192 tokens
     Tp = 8192
     for name, K, N, split in (("in_proj", 5120, 16480, True), ("out_proj", 6144, 5120, False)):
-        xa, wa = I.linear_problem(Tp, N, K, case=80 + (name == "out_proj") + 1000 * rank)
+        xa, wa = I.linear_problem(Tp, N, K, case=rank_case(80 + (name == "out_proj"), rank))
         x_, w_ = dev(xa, bf), dev(wa, bf)
         if split:  # straight into the mixer's input buffers: qkv_pre | z | b | a
             edges = np.cumsum([0, conv_channels(16, 48), 48 * D, 48, 48])
@@ -588,7 +593,7 @@ def next_rows(args, x, o, S_T, conv_T, p, peaks, peak_src, stream, barrier, worl
         else:
             outs = [(0, N, torch.empty(Tp, N, device="cuda", dtype=bf))]
         ms = time_launches(lambda: gdn.gdn_linear(x_, w_, outs, stream=stream), steps, args.warmup,
-                           stream, barrier)
+                           stream, barrier, world)
         fl = 2.0 * Tp * N * K
         tf = fl / (ms * 1e-3) / 1e12
         out["linear_" + name] = {
