@@ -27,10 +27,11 @@
 // both factors of the state update, are carried as hi + lo fp16 pairs (three
 // MMAs for hi*hi + hi*lo + lo*hi), which keeps the state within about 1e-3
 // of its rms where single fp16 gives 2e-2 on short, heavy-tailed updates.
-// Operands derived from the inputs (v, the initial state, T) are clamped to
-// the fp16 range; Gamma k^ and M (|.| <= 1), W, the state's fp16 copy and
-// Delta are converted without a clamp, so an entry of those beyond 65504
-// (far outside any model's regime) would overflow to inf.
+// Operands derived from the inputs (v, the initial state, T) are saturated to
+// the finite fp16 range in the conversion (cvt .satfinite); Gamma k^ and M
+// (|.| <= 1), W, the state's fp16 copy and Delta are converted without it, so
+// an entry of those beyond 65504 (far outside any model's regime) would
+// overflow to inf.
 // Per chunk, in order:
 //   A  conv + SiLU + L2 norms (front end) from the staged raw rows
 //   B  MMA1  [K;Q] K^T -> K K^T, Q K^T;  MMA5  S Q^T
@@ -257,15 +258,14 @@ __device__ __forceinline__ void st_h8_pairs(uint8_t *p, const float2 (&v)[4]) {
   }
   *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
 }
-// hi = fp16(v) and lo = fp16(v - hi) of a clamped pair, as two packed words.
+// hi = fp16(v) and lo = fp16(v - hi) of a pair, as two packed words, both
+// saturated to the finite fp16 range (an entry beyond it cannot be carried;
+// saturation keeps it finite).
 __device__ __forceinline__ void split2(float a, float b, uint32_t &whi, uint32_t &wlo) {
-  a = fminf(fmaxf(a, -kHalfMax), kHalfMax);
-  b = fminf(fmaxf(b, -kHalfMax), kHalfMax);
-  __half2 th = __floats2half2_rn(a, b);
+  whi = pack2_sat(a, b);
+  __half2 th = *reinterpret_cast<__half2 *>(&whi);
   const float2 r = __ffma2_rn(__half22float2(th), make_float2(-1.f, -1.f), make_float2(a, b));  // v - hi
-  __half2 tl = __floats2half2_rn(r.x, r.y);
-  whi = *reinterpret_cast<uint32_t *>(&th);
-  wlo = *reinterpret_cast<uint32_t *>(&tl);
+  wlo = pack2_sat(r.x, r.y);
 }
 // hi/lo of a pair known to lie well inside the fp16 range (no clamp).
 __device__ __forceinline__ void split2_inrange(float a, float b, uint32_t &whi, uint32_t &wlo) {
@@ -430,10 +430,8 @@ __device__ __forceinline__ void store_T4(uint8_t *sm, const ChunkVecs &V, int i,
   uint32_t hw[2], lw[2], ww[2];
   split2(t.x * b.x, t.y * b.y, hw[0], lw[0]);
   split2(t.z * b.z, t.w * b.w, hw[1], lw[1]);
-  __half2 w0 = __halves2half2(to_h(-(t.x * e.x)), to_h(-(t.y * e.y)));
-  __half2 w1 = __halves2half2(to_h(-(t.z * e.z)), to_h(-(t.w * e.w)));
-  ww[0] = *reinterpret_cast<uint32_t *>(&w0);
-  ww[1] = *reinterpret_cast<uint32_t *>(&w1);
+  ww[0] = pack2_sat(-(t.x * e.x), -(t.y * e.y));
+  ww[1] = pack2_sat(-(t.z * e.z), -(t.w * e.w));
   const uint32_t o = kmaj(i, j, kC);
   *reinterpret_cast<uint2 *>(sm + OFF_TU + o) = make_uint2(hw[0], hw[1]);
   *reinterpret_cast<uint2 *>(sm + OFF_TUL + o) = make_uint2(lw[0], lw[1]);
@@ -598,13 +596,10 @@ __device__ __forceinline__ void issue_ta(uint32_t d, uint32_t a0, uint32_t id, i
   for (int ks = 0; ks < nk; ++ks) mma_ta(d, a0 + 8 * ks, db(ks), id, (accumulate_first || ks > 0) ? 1u : 0u);
 }
 
-// Pack 32 fp32 values into 16 fp16-pair words (clamped to the fp16 range).
+// Pack 32 fp32 values into 16 fp16-pair words (saturated to the fp16 range).
 __device__ __forceinline__ void pack_h16(const float (&v)[32], uint32_t (&w)[16]) {
 #pragma unroll
-  for (int q = 0; q < 16; ++q) {
-    __half2 t = __halves2half2(to_h(v[2 * q]), to_h(v[2 * q + 1]));
-    w[q] = *reinterpret_cast<uint32_t *>(&t);
-  }
+  for (int q = 0; q < 16; ++q) w[q] = pack2_sat(v[2 * q], v[2 * q + 1]);
 }
 
 template <bool kRawGates>

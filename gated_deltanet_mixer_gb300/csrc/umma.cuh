@@ -224,6 +224,14 @@ constexpr float kHalfMax = 65504.0f;
 __device__ __forceinline__ __half to_h(float x) {
   return __float2half_rn(fminf(fmaxf(x, -kHalfMax), kHalfMax));
 }
+// A pair of floats as packed fp16 (a in the low half), rounded to nearest and
+// saturated to the finite range (+-65504) in the conversion itself; NaN stays
+// NaN.  Finite values inside the range convert exactly as __floats2half2_rn.
+__device__ __forceinline__ uint32_t pack2_sat(float a, float b) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));  // first source -> high half
+  return r;
+}
 // Pack 8 floats into one 16-byte chunk of fp16 and store it to shared memory.
 __device__ __forceinline__ void st_h8(uint8_t *p, const float *v) {
   uint32_t w[4];
