@@ -111,6 +111,11 @@ bool all_aligned(const void *const *ptrs, int n) {
   return true;
 }
 
+// Workspace of the staged q^ / k^: 3 fp16 values per (token row, key head, channel).
+size_t qk_workspace_bytes(const gdn::Dims &d, long long tokens) {
+  return 3 * (size_t)tokens * (size_t)d.Hk * gdn::kDHead * 2;
+}
+
 gdn_status prefill_impl(const gdn_shape *shape, const gdn_prefill_io *io, void *stream) {
   if (!shape || !io) return GDN_ERR_INVALID_ARG;
   if (shape->B < 1 || shape->T < 1) return GDN_ERR_INVALID_ARG;
@@ -151,17 +156,34 @@ gdn_status prefill_impl(const gdn_shape *shape, const gdn_prefill_io *io, void *
   if (overlap(ro, rs) || overlap(ro, rc) || overlap(rs, rc) || overlap(rp, ro) || overlap(rp, rs) ||
       overlap(rp, rc))
     return GDN_ERR_ALIAS;
+  // bf16 io without snapshots: the chunked tensor-core kernel, with q^ and k^
+  // staged through the workspace when one is given.  fp32 io (fp32
+  // arithmetic throughout) and per-token snapshots: the token-serial kernel.
+  const bool bf16 = shape->io_dtype == GDN_BF16;
+  const bool chunked = bf16 && !io->S_snap;
+  void *ws = nullptr;
+  if (chunked && io->workspace) {
+    const size_t need = qk_workspace_bytes(d, tokens);
+    if ((reinterpret_cast<uintptr_t>(io->workspace) & 255u) != 0) return GDN_ERR_ALIGNMENT;
+    if (io->workspace_bytes < need) return GDN_ERR_INVALID_ARG;
+    const Range rw = range_of(io->workspace, need);
+    for (int i = 0; i < n; ++i)
+      if (overlap(rw, in[i])) return GDN_ERR_ALIAS;
+    if (overlap(rw, ro) || overlap(rw, rs) || overlap(rw, rc)) return GDN_ERR_ALIAS;
+    ws = io->workspace;
+  }
   unsigned int *err = nullptr;
   st = check_device(&err);
   if (st != GDN_OK) return st;
-
   gdn::PrefillArgs a{d,         io->qkv_pre, io->z,   gs,         io->conv_w,     io->norm_w, io->S0,
-                     io->conv0, io->o,       io->S_T, io->conv_T, io->cu_seqlens, io->S_snap, err};
-  // bf16 io without snapshots: the chunked tensor-core kernel.  fp32 io (fp32
-  // arithmetic throughout) and per-token snapshots: the token-serial kernel.
-  const bool bf16 = shape->io_dtype == GDN_BF16;
-  cudaError_t e = (bf16 && !io->S_snap) ? gdn::launch_prefill_chunked(a, true, (cudaStream_t)stream)
-                                        : gdn::launch_prefill(a, bf16, (cudaStream_t)stream);
+                     io->conv0, io->o,       io->S_T, io->conv_T, io->cu_seqlens, io->S_snap, ws,  err};
+  cudaError_t e;
+  if (!chunked) {
+    e = gdn::launch_prefill(a, bf16, (cudaStream_t)stream);
+  } else {
+    e = ws ? gdn::launch_prefill_qk(a, (cudaStream_t)stream) : cudaSuccess;
+    if (e == cudaSuccess) e = gdn::launch_prefill_chunked(a, true, (cudaStream_t)stream);
+  }
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
@@ -212,7 +234,7 @@ gdn_status decode_impl(const gdn_shape *shape, const gdn_decode_io *io, void *st
   } else {
     // T tokens from the cache = a T-token prefill with the state in place.
     gdn::PrefillArgs a{d,     io->qkv_pre, io->z,        gs,      io->conv_w, io->norm_w, io->S, io->conv_in,
-                       io->o, io->S,       io->conv_out, nullptr, io->S_snap, err};
+                       io->o, io->S,       io->conv_out, nullptr, io->S_snap, nullptr, err};
     e = gdn::launch_prefill(a, bf16, (cudaStream_t)stream);
   }
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
@@ -250,6 +272,15 @@ gdn_status gdn_prefill(const gdn_shape *shape, const void *qkv_pre, const void *
 
 gdn_status gdn_prefill_ex(const gdn_shape *shape, const gdn_prefill_io *io, void *stream) {
   return prefill_impl(shape, io, stream);
+}
+
+size_t gdn_prefill_workspace_bytes(const gdn_shape *shape, int packed) {
+  if (!shape || shape->B < 1 || shape->T < 1 || shape->io_dtype != GDN_BF16) return 0;
+  const long long tokens = packed ? (long long)shape->T : (long long)shape->B * shape->T;
+  gdn::Dims d;
+  Sizes sz;
+  if (check_shape(shape, tokens, &d, &sz) != GDN_OK) return 0;
+  return qk_workspace_bytes(d, tokens);
 }
 
 gdn_status gdn_decode_step(const gdn_shape *shape, const void *qkv_pre, const void *z,

@@ -39,6 +39,8 @@ struct PrefillArgs {
   void *conv_T;
   const int *cu_seqlens;  // may be null (fixed length)
   float *S_snap;          // may be null: the state after every token, [token][Hv][128][128]
+  void *qk_ws;            // may be null: staged q^ / k^, fp16 [3][token rows][Hk][128]
+                          // (q^, k^ hi, k^ lo), written by launch_prefill_qk
   unsigned int *err;      // device error word
 };
 
@@ -80,6 +82,7 @@ struct GemmArgs {
 cudaError_t launch_decode(const DecodeArgs &a, bool bf16, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillArgs &a, bool bf16, cudaStream_t s);          // token-serial
 cudaError_t launch_prefill_chunked(const PrefillArgs &a, bool bf16, cudaStream_t s);  // chunked WY, tcgen05
+cudaError_t launch_prefill_qk(const PrefillArgs &a, cudaStream_t s);  // q^ / k^ into a.qk_ws (bf16 io)
 cudaError_t launch_gemm(const GemmArgs &a, int num_sms, cudaStream_t s);
 cudaError_t launch_wait_selftest(unsigned int *err, unsigned long long limit_ns, cudaStream_t s);
 

@@ -110,6 +110,8 @@ constexpr uint32_t OFF_L = OFF_RAW;                  // L fp32 [64][68], phases 
 constexpr uint32_t OFF_PB = OFF_RAW + 64 * kLs * 4;  // block products fp32 [32][32], phase D
 constexpr uint32_t OFF_TF = OFF_NW;                  // T fp32 [64][64], phase D
 constexpr uint32_t OFF_OST = OFF_M;                  // O^T staging fp32 [64][128] (M, NW, TUL), phase J
+constexpr uint32_t OFF_KLO = OFF_RAW;                // staged path: k^ lo, K-major [64][128] fp16, phase A
+static_assert(OFF_KLO % 1024 == 0 && kC * kD * 2 <= 2 * kRawBlock, "k^ lo fills the q and k row blocks");
 static_assert(OFF_NW == OFF_M + 8192 && OFF_TUL == OFF_NW + 16384, "the staging spans M, NW and TUL");
 constexpr uint32_t kVecBytes = 3584;
 constexpr uint32_t kSmemUsed = OFF_VEC + kVecBytes;
@@ -152,6 +154,7 @@ struct __align__(16) Vecs {  // shared-memory scalars, vectors and barriers
   uint64_t bar_end;  // every MMA of both issuers, before TMEM is freed
   uint64_t bar_raw;  // raw rows landed
   uint64_t bar_z;    // z rows landed
+  uint64_t bar_kq;   // staged q^ and k^ hi landed in [K;Q] (staged path)
 };
 static_assert(sizeof(Vecs) <= kVecBytes, "vector area");
 
@@ -410,6 +413,40 @@ __device__ void front_end_v(uint8_t *sm, const ChunkVecs &V, const Dims &d, cons
              t0, T, grp);
 }
 
+// A, staged path: Gamma k^ for the chunk from k^'s fp16 hi part (in [K;Q])
+// and lo part (staged), as the fp16 hi/lo tiles the state update reads.
+// Items (token j, 8-channel group g) are spread over `nthreads` threads.
+__device__ __forceinline__ void gamma_k_pass(uint8_t *sm, const ChunkVecs &V, int i0, int nthreads) {
+  for (int q = i0; q < kC * 16; q += nthreads) {
+    const int j = q >> 4, g = q & 15;
+    const uint4 hi = *reinterpret_cast<const uint4 *>(sm + OFF_KQ + kmaj(j, 8 * g, 128));
+    const uint4 lo = *reinterpret_cast<const uint4 *>(sm + OFF_KLO + kmaj(j, 8 * g, kC));
+    const float gm = V.gam[j];
+    const uint32_t hw[4] = {hi.x, hi.y, hi.z, hi.w}, lw[4] = {lo.x, lo.y, lo.z, lo.w};
+    float2 u[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 kh = __half22float2(*reinterpret_cast<const __half2 *>(&hw[i]));
+      const float2 kl = __half22float2(*reinterpret_cast<const __half2 *>(&lw[i]));
+      u[i] = __fmul2_rn(__fadd2_rn(kh, kl), make_float2(gm, gm));
+    }
+    const uint32_t o = mnmaj(8 * g, j, kC);
+    st_h8_split_pairs<false>(sm + OFF_GK + o, sm + OFF_GKL + o, u);  // |Gamma k^| <= 1
+  }
+}
+// A, staged path: q^ and k^ arrived by TMA, so the front end is the Gamma k^
+// pass (all warps), plus, for the first chunk, the v tiles on warps 8-11.
+__device__ void front_end_staged(uint8_t *sm, const ChunkVecs &V, const Dims &d, const bf16 *conv_w, int h,
+                                 int t0, int T, int tid, bool with_v) {
+  if (!with_v) {
+    gamma_k_pass(sm, V, tid, kThreads);
+  } else if ((tid >> 5) < 8) {
+    gamma_k_pass(sm, V, tid, 256);
+  } else {
+    front_end_v(sm, V, d, conv_w, h, t0, T, tid);
+  }
+}
+
 // T scratch: fp32 [64][64], float4 groups XOR-swizzled by row, so that reads of
 // one row by eight threads (eight rows) and broadcast reads stay conflict free.
 __device__ __forceinline__ int tfi(int row, int col) {
@@ -602,10 +639,10 @@ __device__ __forceinline__ void pack_h16(const float (&v)[32], uint32_t (&w)[16]
   for (int q = 0; q < 16; ++q) w[q] = pack2_sat(v[2 * q], v[2 * q + 1]);
 }
 
-template <bool kRawGates>
+template <bool kRawGates, bool kStagedQK>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_chunked_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tm_qkv,
-                           const __grid_constant__ CUtensorMap tm_z) {
+                           const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_qk) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   Vecs &V = *reinterpret_cast<Vecs *>(sm + OFF_VEC);
@@ -640,12 +677,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = smem_u32(sm);
   const int cq = kh * kD, ck = d.Hk * kD + kh * kD, cv = 2 * d.Hk * kD + h * kD;
 
-  auto request_raw = [&](int t0) {  // one thread: the raw rows t0-3 .. t0+63 of q, k, v
-    bar_expect_tx(&V.bar_raw, 3 * kRawBlock);
+  // One thread: the raw rows t0-3 .. t0+63 of q, k, v; in the staged path
+  // the raw v rows and k^ lo of tokens t0 .. t0+63 (two 64-column boxes).
+  auto request_raw = [&](int t0) {
     const int row = (int)(bos + t0 - 3);
-    tma_load_3d(sbase + OFF_RAW + 0 * kRawBlock, &tm_qkv, cq, row, 0, &V.bar_raw);
-    tma_load_3d(sbase + OFF_RAW + 1 * kRawBlock, &tm_qkv, ck, row, 0, &V.bar_raw);
+    if (kStagedQK) {
+      bar_expect_tx(&V.bar_raw, kRawBlock + kC * kD * 2);
+      tma_load_3d(sbase + OFF_KLO, &tm_qk, kh * kD, (int)(bos + t0), 2, &V.bar_raw);
+      tma_load_3d(sbase + OFF_KLO + kC * 128, &tm_qk, kh * kD + 64, (int)(bos + t0), 2, &V.bar_raw);
+    } else {
+      bar_expect_tx(&V.bar_raw, 3 * kRawBlock);
+      tma_load_3d(sbase + OFF_RAW + 0 * kRawBlock, &tm_qkv, cq, row, 0, &V.bar_raw);
+      tma_load_3d(sbase + OFF_RAW + 1 * kRawBlock, &tm_qkv, ck, row, 0, &V.bar_raw);
+    }
     tma_load_3d(sbase + OFF_RAW + 2 * kRawBlock, &tm_qkv, cv, row, 0, &V.bar_raw);
+  };
+  // Staged path, one thread: q^ (rows 64..127) and k^ hi (rows 0..63) of tokens
+  // t0 .. t0+63 straight into the [K;Q] tile, two 64-column boxes each.
+  auto request_kq = [&](int t0) {
+    bar_expect_tx(&V.bar_kq, 2 * kC * kD * 2);
+#pragma unroll
+    for (int at = 0; at < 2; ++at) {
+      tma_load_3d(sbase + OFF_KQ + at * 16384 + 64 * 128, &tm_qk, kh * kD + 64 * at, (int)(bos + t0), 0, &V.bar_kq);
+      tma_load_3d(sbase + OFF_KQ + at * 16384, &tm_qk, kh * kD + 64 * at, (int)(bos + t0), 1, &V.bar_kq);
+    }
   };
   auto request_z = [&](int t0) {  // one thread: the z rows t0 .. t0+63 of head h
     bar_expect_tx(&V.bar_z, kC * kD * 2);
@@ -688,6 +743,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bar_init(&V.bar_end, 2);
     bar_init(&V.bar_raw, 1);
     bar_init(&V.bar_z, 1);
+    bar_init(&V.bar_kq, 1);
     V.abort = 0;
   }
   if (warp == 0) tmem_alloc(&V.tmem, kTmemCols);
@@ -709,6 +765,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   fence_after();
   if (tid == 0) {
     request_raw(0);
+    if (kStagedQK) request_kq(0);
     request_z(0);
   }
   const uint32_t tmem = V.tmem;
@@ -745,11 +802,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // Each mbarrier completes once per chunk; its phase bit is tracked here.
-  uint32_t ph_qk = 0, ph_w = 0, ph_d = 0, ph_o = 0, ph_s = 0, ph_sq = 0, ph_u = 0, phase_raw = 0, phase_z = 0;
+  uint32_t ph_qk = 0, ph_w = 0, ph_d = 0, ph_o = 0, ph_s = 0, ph_sq = 0, ph_u = 0, phase_raw = 0, phase_z = 0,
+           phase_kq = 0;
   // MMAs off the critical path are issued by lane 0 of warp 11, idle in the
   // phases where it issues them; the critical ones by thread 0.
   const bool issuer2 = tid == kThreads - 32;
-  bool raw_pending = true, z_pending = true;  // a requested TMA not yet consumed
+  bool raw_pending = true, z_pending = true, kq_pending = kStagedQK;  // a requested TMA not yet consumed
   const int nchunks = (T + kC - 1) / kC;
   const uint32_t id_kk = idesc(128, 64, 0, 0);
   const uint32_t id_mk = idesc(128, 64, 1, 0);
@@ -802,8 +860,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!wait_all(&V.bar_raw, phase_raw)) break;
       raw_pending = false;
     }
+    if (kStagedQK) {  // q^ and k^ hi of this chunk in [K;Q]
+      if (!wait_all(&V.bar_kq, phase_kq)) break;
+      kq_pending = false;
+    }
     if (n == 0) {  // rows before the first token: the carried window, or zeros
-      for (int idx = tid; idx < 3 * 3 * 16; idx += kThreads) {
+      for (int idx = kStagedQK ? 2 * 48 + tid : tid; idx < 3 * 3 * 16; idx += kThreads) {
         const int blk = idx / 48, rw = (idx / 16) % 3, g8 = idx % 16;
         const int cc = blk == 0 ? cq : blk == 1 ? ck : cv;
         *reinterpret_cast<uint4 *>(sm + OFF_RAW + blk * kRawBlock + 256 * rw + 16 * g8) =
@@ -813,7 +875,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncthreads();
     }
     // A: front end
-    front_end(sm, CV, d, conv_w, h, kh, t0, T, tid, n == 0);
+    if (kStagedQK)
+      front_end_staged(sm, CV, d, conv_w, h, t0, T, tid, n == 0);
+    else
+      front_end(sm, CV, d, conv_w, h, kh, t0, T, tid, n == 0);
     smem_ready();
     // B: MMA1  [K;Q] K^T
     if (tid == 0) {
@@ -964,6 +1029,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // I: MMA6 Delta^T M^T (thread 0); then warp 11 may issue MMA7 behind it
       if (tid == 0) {
         bar_wait(&V.bar_sq, ph_sq);  // MMA5 (the other issuer) done, so bar_o covers O1 and O2
+        if (kStagedQK && n + 1 < nchunks) {  // [K;Q]'s last readers (MMA1, MMA3, MMA5) are done
+          request_kq(t0 + kC);
+          kq_pending = true;
+        }
         fence_after();
         issue_ta(tmem + TM_O2, tmem + TM_KQ, id_kk, 4, false, [&](int ks) { return desc_k(sbase + OFF_M, ks, kC); });
         commit(&V.bar_o);
@@ -1142,6 +1211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     if (raw_pending) bar_wait(&V.bar_raw, phase_raw);
     if (z_pending) bar_wait(&V.bar_z, phase_z);
+    if (kStagedQK && kq_pending) bar_wait(&V.bar_kq, phase_kq);
     commit(&V.bar_end);
     bar_wait(&V.bar_end, 0);
   }
@@ -1155,6 +1225,140 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // A [B][T][width] bf16 tensor as a 3-d map with boxes of 128 columns x `rows` rows.
+// The q^ / k^ front end of the staged path, once per key head rather than
+// once per value head: conv + SiLU + L2 norm of q and k for 64 token rows,
+// written as fp16 q^ and as an fp16 hi/lo pair for k^ (hi = fp16(k^),
+// lo = fp16(k^ - hi)) into qk_ws [3][rows][Hk][128].  The arithmetic is
+// fe_pass's, so q^ and k^'s hi part equal the fused kernel's operands bit
+// for bit.  Half-warps 0-7 take q, 8-15 take k, a run of 8 tokens each: the
+// run's 11 rows are loaded up front and the window slides over them; a token
+// within three rows of its sequence's start takes those rows from the
+// carried window (or zeros) instead.
+__global__ void __launch_bounds__(256) prefill_qk_kernel(const PrefillArgs a) {
+  const Dims d = a.d;
+  // Key heads vary fastest across the grid, so the CTAs running together read
+  // neighbouring slices of the same rows.
+  const int kh = (int)(blockIdx.x % (unsigned)d.Hk);
+  const long long tile = blockIdx.x / (unsigned)d.Hk;
+  const long long rows = a.cu_seqlens ? (long long)d.T : (long long)d.B * d.T;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, grp = lane & 15;
+  const int hw = 2 * warp + (lane >> 4);  // half-warp 0..15
+  const int blk = hw >> 3;                // 0: q, 1: k
+  const long long C = d.C;
+  const long long c = (blk == 0 ? 0LL : (long long)d.Hk * kD) + (long long)kh * kD + 8 * grp;
+  const float scale = blk == 0 ? d.q_scale : 1.0f;
+  const bf16 *x = static_cast<const bf16 *>(a.qkv_pre);
+  const bf16 *conv_w = static_cast<const bf16 *>(a.conv_w);
+  const bf16 *conv0 = static_cast<const bf16 *>(a.conv0);
+  __half *ws = static_cast<__half *>(a.qk_ws);
+  const long long plane = rows * d.Hk * kD;  // elements of each of q^, k^ hi, k^ lo
+  const long long tb = tile * kC + 8 * (hw & 7);
+  uint4 rr[11];  // rows tb-3 .. tb+7
+#pragma unroll
+  for (int j = 0; j < 11; ++j) {
+    const long long r = tb - 3 + j;
+    rr[j] = (r >= 0 && r < rows) ? *reinterpret_cast<const uint4 *>(x + r * C + c) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  float2 w[4][4];  // [channel pair][tap]
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 a0 = ld_io4(conv_w + 4 * (c + 2 * i)), a1 = ld_io4(conv_w + 4 * (c + 2 * i + 1));
+    w[i][0] = make_float2(a0.x, a1.x);
+    w[i][1] = make_float2(a0.y, a1.y);
+    w[i][2] = make_float2(a0.z, a1.z);
+    w[i][3] = make_float2(a0.w, a1.w);
+  }
+  // The sequence of the run's first token, advanced along the run.
+  int b = 0;
+  long long bos = 0, eos = rows;
+  if (tb < rows) {
+    if (a.cu_seqlens) {  // the last sequence starting at or before tb
+      int lo = 0, hi = d.B - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.cu_seqlens[mid] <= tb) lo = mid; else hi = mid - 1;
+      }
+      b = lo;
+      bos = a.cu_seqlens[b];
+      eos = a.cu_seqlens[b + 1];
+    } else {
+      b = (int)(tb / d.T);
+      bos = (long long)b * d.T;
+      eos = bos + d.T;
+    }
+  }
+#pragma unroll
+  for (int u8 = 0; u8 < 8; ++u8) {
+    const long long t = tb + u8;
+    const bool valid = t < rows;  // the shuffles below run on every lane regardless
+    if (valid) {
+      while (t >= eos && b + 1 < d.B) {  // the run crossed into the next sequence
+        ++b;
+        bos = eos;
+        eos = a.cu_seqlens ? (long long)a.cu_seqlens[b + 1] : bos + d.T;
+      }
+    }
+    float2 x0[4], x1[4], x2[4], x3[4];
+    uint4 w0 = rr[u8], w1 = rr[u8 + 1], w2 = rr[u8 + 2];
+    if (valid && t - bos < 3) {  // rows before the sequence: the carried window, or zeros
+      const bf16 *cw0 = conv0 ? conv0 + (long long)b * 3 * C + c : nullptr;
+      const long long k0 = t - 3 - bos;  // window row of tap 0: -3 .. -1 -> carried rows 0 .. 2
+      const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
+      if (k0 < 0) w0 = cw0 ? *reinterpret_cast<const uint4 *>(cw0 + (3 + k0) * C) : z4;
+      if (k0 + 1 < 0) w1 = cw0 ? *reinterpret_cast<const uint4 *>(cw0 + (4 + k0) * C) : z4;
+      if (k0 + 2 < 0) w2 = cw0 ? *reinterpret_cast<const uint4 *>(cw0 + (5 + k0) * C) : z4;
+    }
+    widen(w0, x0);
+    widen(w1, x1);
+    widen(w2, x2);
+    widen(rr[u8 + 3], x3);
+    float2 u[4], ss2 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float2 acc = __fmul2_rn(w[i][0], x0[i]);
+      acc = __ffma2_rn(w[i][1], x1[i], acc);
+      acc = __ffma2_rn(w[i][2], x2[i], acc);
+      acc = __ffma2_rn(w[i][3], x3[i], acc);
+      u[i] = silu2(acc);
+      ss2 = __ffma2_rn(u[i], u[i], ss2);
+    }
+    float ss = ss2.x + ss2.y;
+#pragma unroll
+    for (int off = 1; off < 16; off <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    const float f = rsqrtf(ss + d.eps_l2) * scale;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) u[i] = __fmul2_rn(u[i], make_float2(f, f));
+    if (valid) {
+      const long long off = (t * d.Hk + kh) * kD + 8 * grp;
+      uint32_t wh[4], wl[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) split2_inrange(u[i].x, u[i].y, wh[i], wl[i]);  // |k^|, |q^| <= 1
+      if (blk == 0) {
+        *reinterpret_cast<uint4 *>(ws + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+      } else {
+        *reinterpret_cast<uint4 *>(ws + plane + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+        *reinterpret_cast<uint4 *>(ws + 2 * plane + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+      }
+    }
+  }
+}
+
+// The staged q^ / k^ of qk_ws as a 3-d map {Hk*128 columns, rows, 3 tensors}
+// of fp16 with 128-byte-swizzled 64 x 64 boxes: the layout of the K-major
+// [K;Q] tile.
+bool encode_qk(CUtensorMap *m, void *base, int Hk, long long rows) {
+  EncodeTiled enc = encoder();
+  if (!enc) return false;
+  const long long width = (long long)Hk * kD;
+  const cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)rows, 3};
+  const cuuint64_t strides[2] = {(cuuint64_t)width * 2, (cuuint64_t)width * 2 * rows};
+  const cuuint32_t box[3] = {64, (cuuint32_t)kC, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_rows(CUtensorMap *m, const void *base, long long width, long long T, int B, int rows) {
   EncodeTiled enc = encoder();
   if (!enc) return false;
@@ -1178,12 +1382,25 @@ cudaError_t launch_prefill_chunked(const PrefillArgs &a, bool bf16_io, cudaStrea
   if (!encode_rows(&tm_qkv, a.qkv_pre, a.d.C, rows, 1, kRawRows) ||
       !encode_rows(&tm_z, a.z, (long long)a.d.Hv * kD, rows, 1, kC))
     return cudaErrorInvalidValue;
+  CUtensorMap tm_qk = tm_z;  // unread by the fused variant
+  if (a.qk_ws && !encode_qk(&tm_qk, a.qk_ws, a.d.Hk, rows)) return cudaErrorInvalidValue;
   const dim3 grid((unsigned)(a.d.B * a.d.Hv)), block(kThreads);
   const bool raw = a.gate.g == nullptr;
-  auto kern = raw ? prefill_chunked_kernel<true> : prefill_chunked_kernel<false>;
+  auto kern = a.qk_ws ? (raw ? prefill_chunked_kernel<true, true> : prefill_chunked_kernel<false, true>)
+                      : (raw ? prefill_chunked_kernel<true, false> : prefill_chunked_kernel<false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  kern<<<grid, block, kSmemBytes, s>>>(a, tm_qkv, tm_z);
+  kern<<<grid, block, kSmemBytes, s>>>(a, tm_qkv, tm_z, tm_qk);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_qk(const PrefillArgs &a, cudaStream_t s) {
+  if (!a.qk_ws) return cudaErrorInvalidValue;
+  const long long rows = a.cu_seqlens ? (long long)a.d.T : (long long)a.d.B * a.d.T;
+  if (rows <= 0) return cudaSuccess;
+  const long long ctas = (rows + kC - 1) / kC * a.d.Hk;
+  if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
+  prefill_qk_kernel<<<(unsigned)ctas, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -45,7 +45,8 @@ class gdn_raw_gates(ctypes.Structure):
 
 class gdn_prefill_io(ctypes.Structure):
     _fields_ = [(n, vp) for n in ("qkv_pre", "z", "g", "beta", "raw_gates", "conv_w", "norm_w", "S0",
-                                  "conv0", "o", "S_T", "conv_T", "cu_seqlens", "S_snap")]
+                                  "conv0", "o", "S_T", "conv_T", "cu_seqlens", "S_snap", "workspace")] + \
+               [("workspace_bytes", ctypes.c_size_t)]
 
 
 class gdn_linear_out(ctypes.Structure):
@@ -88,6 +89,8 @@ def lib():
                                                       ctypes.POINTER(gdn_linear_out), vp]
         L.gdn_selftest_wait_timeout.restype = ctypes.c_int
         L.gdn_selftest_wait_timeout.argtypes = [ctypes.c_int, vp]
+        L.gdn_prefill_workspace_bytes.restype = ctypes.c_size_t
+        L.gdn_prefill_workspace_bytes.argtypes = [ctypes.POINTER(gdn_shape), ctypes.c_int]
         _lib = L
     return _lib
 
@@ -171,12 +174,14 @@ def _raw(raw_gates):
 
 
 def gdn_prefill_ex(qkv_pre, z, g, beta, conv_w, norm_w, S0, conv0, o, S_T, conv_T, *, Hk, Hv,
-                   raw_gates=None, cu_seqlens=None, S_snap=None, eps_l2=1e-6, eps_norm=1e-6,
-                   q_scale=0.0, stream=None):
+                   raw_gates=None, cu_seqlens=None, S_snap=None, workspace=None, eps_l2=1e-6,
+                   eps_norm=1e-6, q_scale=0.0, stream=None):
     """Prefill with the options of gdn_prefill_ex: raw gate projections
     (raw_gates = dict(a, b, A_log, dt_bias), g = beta = None), packed
     sequences (qkv_pre [N, C], z and o [N, Hv*D], cu_seqlens int32 [B+1] on
-    the device), and per-token state snapshots S_snap [tokens, Hv, D, D]."""
+    the device), per-token state snapshots S_snap [tokens, Hv, D, D], and a
+    device workspace (any tensor of at least gdn_prefill_workspace_bytes()
+    bytes) for the staged q^ / k^ path."""
     if cu_seqlens is not None:
         N, C = qkv_pre.shape
         B, T = cu_seqlens.numel() - 1, N
@@ -188,10 +193,17 @@ def gdn_prefill_ex(qkv_pre, z, g, beta, conv_w, norm_w, S0, conv0, o, S_T, conv_
     io = gdn_prefill_io(_ptr(qkv_pre), _ptr(z), _ptr(g), _ptr(beta),
                         None if rg is None else ctypes.addressof(rg), _ptr(conv_w), _ptr(norm_w),
                         _ptr(S0), _ptr(conv0), _ptr(o), _ptr(S_T), _ptr(conv_T), _ptr(cu_seqlens),
-                        _ptr(S_snap))
+                        _ptr(S_snap), _ptr(workspace),
+                        0 if workspace is None else workspace.numel() * workspace.element_size())
     st = lib().gdn_prefill_ex(ctypes.byref(sh), ctypes.byref(io), _stream(stream))
     if st != GDN_OK:
         raise GdnError(st, "gdn_prefill_ex")
+
+
+def gdn_prefill_workspace_bytes(B, T, Hk, Hv, packed=False, D=128, io_dtype=None):
+    """Workspace bytes of the staged q^ / k^ path (gdn_prefill_workspace_bytes)."""
+    sh = make_shape(B, T, Hk, Hv, D, GDN_BF16 if io_dtype is None else io_dtype)
+    return lib().gdn_prefill_workspace_bytes(ctypes.byref(sh), 1 if packed else 0)
 
 
 def gdn_decode_ex(qkv_pre, z, g, beta, conv_w, norm_w, S, conv_in, conv_out, o, *, Hk, Hv,

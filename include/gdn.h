@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define GDN_ABI_VERSION 2
+#define GDN_ABI_VERSION 3
 
 typedef enum {
   GDN_OK = 0,
@@ -152,8 +152,18 @@ typedef struct {
  *               gdn_device_status.
  *   S_snap      [tokens][Hv][Dv][Dk] fp32 or NULL: the state after every
  *               token (for rollback; costs one state write per token).
- * Fixed length without snapshots and with bf16 io runs the chunked
- * tensor-core kernel; the other cases run the token-serial kernel.
+ *   workspace   device scratch of at least gdn_prefill_workspace_bytes()
+ *               bytes (workspace_bytes says how many were given), 256-byte
+ *               aligned, overlapping no other argument; or NULL.  Owned by
+ *               the caller; its contents are undefined after the call and
+ *               it must not be shared by calls that may run concurrently.
+ *               When given, and the call runs the chunked kernel, the
+ *               normalised q and k of each key head are formed once by a
+ *               separate kernel into the workspace and read back by TMA,
+ *               instead of once per value head inside the chunked kernel.
+ * bf16 io without snapshots (fixed length or packed) runs the chunked
+ * tensor-core kernel; fp32 io and snapshots run the token-serial kernel,
+ * which ignores the workspace.
  */
 typedef struct {
   const void *qkv_pre, *z;
@@ -167,7 +177,16 @@ typedef struct {
   void *conv_T;
   const int *cu_seqlens;
   float *S_snap;
+  void *workspace;
+  size_t workspace_bytes;
 } gdn_prefill_io;
+
+/* Bytes of workspace the chunked prefill can use for this shape (packed: the
+ * call passes cu_seqlens, so the token rows are shape->T, else B*T): the
+ * staged q^ and k^ of every token row and key head, 3 fp16 values per
+ * element (q^, and k^ as a hi/lo pair).  0 when the shape is invalid or
+ * the call would not run the chunked kernel (fp32 io). */
+size_t gdn_prefill_workspace_bytes(const gdn_shape *shape, int packed);
 
 /* Prefill with the options above; aliasing and alignment rules as for
  * gdn_prefill (raw gates, cu_seqlens and S_snap count as inputs / outputs). */

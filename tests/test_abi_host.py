@@ -122,7 +122,7 @@ def test_selftest_limit_checked_on_host(L):
 def prefill_ex(L, sh, raw=None, **over):
     args = dict(qkv_pre=fake(0), z=fake(1), g=fake(2), beta=fake(3), raw_gates=None, conv_w=fake(4),
                 norm_w=fake(5), S0=fake(6), conv0=fake(7), o=fake(8), S_T=fake(9), conv_T=fake(10),
-                cu_seqlens=None, S_snap=None)
+                cu_seqlens=None, S_snap=None, workspace=None, workspace_bytes=0)
     args.update(over)
     if raw is not None:
         args["raw_gates"] = ctypes.addressof(raw)
@@ -161,6 +161,20 @@ def test_extended_entry_points_check_on_host(L):
     assert decode_ex(L, shape(T=4), S_snap=fake(6, 256)) == 4  # snapshots over the state
     assert decode_ex(L, shape(T=4), conv_out=fake(7)) == 4
     assert prefill_ex(L, shape(T=1 << 29, B=4)) == 2        # token rows beyond 2^30
+
+
+def test_workspace_checked_on_host(L):
+    sh = shape(B=2, T=8, Hk=2, Hv=4)
+    need = L.gdn_prefill_workspace_bytes(ctypes.byref(sh), 0)
+    assert need == 3 * 2 * 8 * 2 * 128 * 2
+    assert L.gdn_prefill_workspace_bytes(ctypes.byref(sh), 1) == 3 * 8 * 2 * 128 * 2   # packed: T rows
+    assert L.gdn_prefill_workspace_bytes(ctypes.byref(shape(io=gdn.GDN_F32)), 0) == 0  # no chunked kernel
+    assert L.gdn_prefill_workspace_bytes(None, 0) == 0
+    ws = fake(11)
+    assert prefill_ex(L, sh, workspace=fake(11, 16), workspace_bytes=need) == 3     # not 256-byte aligned
+    assert prefill_ex(L, sh, workspace=ws, workspace_bytes=need - 1) == 1           # too small
+    assert prefill_ex(L, sh, workspace=fake(0), workspace_bytes=need) == 4          # over qkv_pre
+    assert prefill_ex(L, sh, workspace=fake(8), workspace_bytes=need) == 4          # over o
 
 
 def test_linear_checked_on_host(L):
