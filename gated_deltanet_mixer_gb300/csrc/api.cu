@@ -274,6 +274,20 @@ gdn_status gdn_prefill_ex(const gdn_shape *shape, const gdn_prefill_io *io, void
   return prefill_impl(shape, io, stream);
 }
 
+gdn_status gdn_prefill_static(const gdn_shape *shape, const gdn_prefill_io *io, void *stream) {
+  if (!shape || !io || io->workspace) return GDN_ERR_INVALID_ARG;
+  const size_t need = gdn_prefill_workspace_bytes(shape, io->cu_seqlens != nullptr ? 1 : 0);
+  if (need > GDN_STATIC_SCRATCH_BYTES) return GDN_ERR_UNSUPPORTED_SHAPE;
+  gdn_prefill_io staged = *io;
+  if (need > 0 && shape->io_dtype == GDN_BF16 && !io->S_snap) {  // the chunked kernel: stage q^ / k^
+    void *p = nullptr;
+    if (gdn::static_scratch(&p) != cudaSuccess) return GDN_ERR_CUDA;
+    staged.workspace = p;
+    staged.workspace_bytes = GDN_STATIC_SCRATCH_BYTES;
+  }
+  return prefill_impl(shape, &staged, stream);
+}
+
 size_t gdn_prefill_workspace_bytes(const gdn_shape *shape, int packed) {
   if (!shape || shape->B < 1 || shape->T < 1 || shape->io_dtype != GDN_BF16) return 0;
   const long long tokens = packed ? (long long)shape->T : (long long)shape->B * shape->T;

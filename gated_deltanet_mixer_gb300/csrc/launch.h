@@ -83,6 +83,10 @@ cudaError_t launch_decode(const DecodeArgs &a, bool bf16, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillArgs &a, bool bf16, cudaStream_t s);          // token-serial
 cudaError_t launch_prefill_chunked(const PrefillArgs &a, bool bf16, cudaStream_t s);  // chunked WY, tcgen05
 cudaError_t launch_prefill_qk(const PrefillArgs &a, cudaStream_t s);  // q^ / k^ into a.qk_ws (bf16 io)
+
+// The library's device scratch (GDN_STATIC_SCRATCH_BYTES) on the current
+// device; its address is looked up once per device.
+cudaError_t static_scratch(void **ptr);
 cudaError_t launch_gemm(const GemmArgs &a, int num_sms, cudaStream_t s);
 cudaError_t launch_wait_selftest(unsigned int *err, unsigned long long limit_ns, cudaStream_t s);
 

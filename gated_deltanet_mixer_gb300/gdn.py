@@ -20,6 +20,7 @@ STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED_S
                 3: "GDN_ERR_ALIGNMENT", 4: "GDN_ERR_ALIAS", 5: "GDN_ERR_CUDA",
                 6: "GDN_ERR_TIMEOUT", 7: "GDN_ERR_NO_DEVICE"}
 GDN_F32, GDN_BF16 = 0, 1
+GDN_STATIC_SCRATCH_BYTES = 512 << 20  # include/gdn.h: the scratch of gdn_prefill_static
 
 
 class GdnError(RuntimeError):
@@ -89,6 +90,8 @@ def lib():
                                                       ctypes.POINTER(gdn_linear_out), vp]
         L.gdn_selftest_wait_timeout.restype = ctypes.c_int
         L.gdn_selftest_wait_timeout.argtypes = [ctypes.c_int, vp]
+        L.gdn_prefill_static.restype = ctypes.c_int
+        L.gdn_prefill_static.argtypes = [ctypes.POINTER(gdn_shape), ctypes.POINTER(gdn_prefill_io), vp]
         L.gdn_prefill_workspace_bytes.restype = ctypes.c_size_t
         L.gdn_prefill_workspace_bytes.argtypes = [ctypes.POINTER(gdn_shape), ctypes.c_int]
         _lib = L
@@ -175,7 +178,7 @@ def _raw(raw_gates):
 
 def gdn_prefill_ex(qkv_pre, z, g, beta, conv_w, norm_w, S0, conv0, o, S_T, conv_T, *, Hk, Hv,
                    raw_gates=None, cu_seqlens=None, S_snap=None, workspace=None, eps_l2=1e-6,
-                   eps_norm=1e-6, q_scale=0.0, stream=None):
+                   eps_norm=1e-6, q_scale=0.0, stream=None, _entry="gdn_prefill_ex"):
     """Prefill with the options of gdn_prefill_ex: raw gate projections
     (raw_gates = dict(a, b, A_log, dt_bias), g = beta = None), packed
     sequences (qkv_pre [N, C], z and o [N, Hv*D], cu_seqlens int32 [B+1] on
@@ -195,9 +198,18 @@ def gdn_prefill_ex(qkv_pre, z, g, beta, conv_w, norm_w, S0, conv0, o, S_T, conv_
                         _ptr(S0), _ptr(conv0), _ptr(o), _ptr(S_T), _ptr(conv_T), _ptr(cu_seqlens),
                         _ptr(S_snap), _ptr(workspace),
                         0 if workspace is None else workspace.numel() * workspace.element_size())
-    st = lib().gdn_prefill_ex(ctypes.byref(sh), ctypes.byref(io), _stream(stream))
+    st = getattr(lib(), _entry)(ctypes.byref(sh), ctypes.byref(io), _stream(stream))
     if st != GDN_OK:
-        raise GdnError(st, "gdn_prefill_ex")
+        raise GdnError(st, _entry)
+
+
+def gdn_prefill_static(qkv_pre, z, g, beta, conv_w, norm_w, S0, conv0, o, S_T, conv_T, *, Hk, Hv, **kw):
+    """gdn_prefill_ex in the library's own device scratch (gdn_prefill_static):
+    no workspace argument, no allocation; calls that overlap in time race."""
+    if kw.get("workspace") is not None:
+        raise ValueError("gdn_prefill_static takes no workspace")
+    gdn_prefill_ex(qkv_pre, z, g, beta, conv_w, norm_w, S0, conv0, o, S_T, conv_T, Hk=Hk, Hv=Hv,
+                   _entry="gdn_prefill_static", **kw)
 
 
 def gdn_prefill_workspace_bytes(B, T, Hk, Hv, packed=False, D=128, io_dtype=None):

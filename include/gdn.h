@@ -193,6 +193,25 @@ size_t gdn_prefill_workspace_bytes(const gdn_shape *shape, int packed);
 gdn_status gdn_prefill_ex(const gdn_shape *shape, const gdn_prefill_io *io, void *stream);
 
 /*
+ * gdn_prefill_ex with no caller workspace and no allocation: the staged
+ * q^ / k^ path runs in a device scratch array that the library owns, one
+ * per device, GDN_STATIC_SCRATCH_BYTES large.  The pages have no
+ * counterpart; this is a serving convenience of the library.
+ *   io->workspace must be NULL (GDN_ERR_INVALID_ARG otherwise).
+ *   A call whose workspace need (gdn_prefill_workspace_bytes) exceeds the
+ *   scratch returns GDN_ERR_UNSUPPORTED_SHAPE before any launch.
+ *   Nothing in the scratch has to start at zero: every byte the chunked
+ *   kernel reads is written first by the q/k kernel of the same call.
+ *   The scratch is shared by every call on the device: calls that overlap in
+ *   time (different streams, or unordered host threads) race on it and give
+ *   undefined results.  Issue them on one stream, or order them.
+ *   The array is device memory of the library's own module; with lazy
+ *   module loading (the CUDA default) it is allocated at the first call.
+ */
+#define GDN_STATIC_SCRATCH_BYTES (512ull << 20)
+gdn_status gdn_prefill_static(const gdn_shape *shape, const gdn_prefill_io *io, void *stream);
+
+/*
  * Arguments of gdn_decode_ex: shape->T >= 1 new tokens for each of B
  * sequences from the cached state, e.g. the draft tokens of speculative
  * decoding being verified ("How Qwen3.5 works" section 13).

@@ -177,6 +177,17 @@ def test_workspace_checked_on_host(L):
     assert prefill_ex(L, sh, workspace=fake(8), workspace_bytes=need) == 4          # over o
 
 
+def test_static_entry_checked_on_host(L):
+    sh = shape(B=2, T=8, Hk=2, Hv=4)
+    io = gdn.gdn_prefill_io(*[fake(i) for i in range(4)], None, fake(4), fake(5), fake(6), fake(7), fake(8),
+                            fake(9), fake(10), None, None, fake(11), 1 << 20)
+    assert L.gdn_prefill_static(ctypes.byref(sh), ctypes.byref(io), None) == 1   # a workspace is given
+    big = shape(B=1, T=1 << 20, Hk=2, Hv=4)   # 3 x 2^20 rows x 2 heads x 256 B = 1.5 GiB > the scratch
+    io.workspace, io.workspace_bytes = None, 0
+    assert L.gdn_prefill_static(ctypes.byref(big), ctypes.byref(io), None) == 2
+    assert L.gdn_prefill_static(None, ctypes.byref(io), None) == 1
+
+
 def test_linear_checked_on_host(L):
     out = (gdn.gdn_linear_out * 2)(gdn.gdn_linear_out(0, 8, fake(2), 8), gdn.gdn_linear_out(8, 16, fake(3), 8))
     assert L.gdn_linear(0, 16, 64, fake(0), 64, fake(1), 64, 2, out, None) == 1
