@@ -1237,27 +1237,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 __global__ void __launch_bounds__(256) prefill_qk_kernel(const PrefillArgs a) {
   const Dims d = a.d;
   // Key heads vary fastest across the grid, so the CTAs running together read
-  // neighbouring slices of the same rows.
+  // neighbouring slices of the same rows.  Token rows fit in 31 bits.
   const int kh = (int)(blockIdx.x % (unsigned)d.Hk);
-  const long long tile = blockIdx.x / (unsigned)d.Hk;
-  const long long rows = a.cu_seqlens ? (long long)d.T : (long long)d.B * d.T;
+  const int tile = (int)(blockIdx.x / (unsigned)d.Hk);
+  const int rows = a.cu_seqlens ? d.T : d.B * d.T;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, grp = lane & 15;
   const int hw = 2 * warp + (lane >> 4);  // half-warp 0..15
   const int blk = hw >> 3;                // 0: q, 1: k
   const long long C = d.C;
-  const long long c = (blk == 0 ? 0LL : (long long)d.Hk * kD) + (long long)kh * kD + 8 * grp;
+  const int c = (blk == 0 ? 0 : d.Hk * kD) + kh * kD + 8 * grp;
   const float scale = blk == 0 ? d.q_scale : 1.0f;
-  const bf16 *x = static_cast<const bf16 *>(a.qkv_pre);
   const bf16 *conv_w = static_cast<const bf16 *>(a.conv_w);
   const bf16 *conv0 = static_cast<const bf16 *>(a.conv0);
-  __half *ws = static_cast<__half *>(a.qk_ws);
-  const long long plane = rows * d.Hk * kD;  // elements of each of q^, k^ hi, k^ lo
-  const long long tb = tile * kC + 8 * (hw & 7);
-  uint4 rr[11];  // rows tb-3 .. tb+7
+  const int tb = tile * kC + 8 * (hw & 7);  // this half-warp's run: tokens tb .. tb+7
+  // rows tb-3 .. tb+7 of this lane's 8 channels
+  const bf16 *xr = static_cast<const bf16 *>(a.qkv_pre) + ((long long)tb - 3) * C + c;
+  uint4 rr[11];
+  if (tb >= 3 && tb + 8 <= rows) {
 #pragma unroll
-  for (int j = 0; j < 11; ++j) {
-    const long long r = tb - 3 + j;
-    rr[j] = (r >= 0 && r < rows) ? *reinterpret_cast<const uint4 *>(x + r * C + c) : make_uint4(0u, 0u, 0u, 0u);
+    for (int j = 0; j < 11; ++j) rr[j] = *reinterpret_cast<const uint4 *>(xr + j * C);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 11; ++j) {
+      const int r = tb - 3 + j;
+      rr[j] = (r >= 0 && r < rows) ? *reinterpret_cast<const uint4 *>(xr + j * C) : make_uint4(0u, 0u, 0u, 0u);
+    }
   }
   float2 w[4][4];  // [channel pair][tap]
 #pragma unroll
@@ -1269,8 +1273,7 @@ __global__ void __launch_bounds__(256) prefill_qk_kernel(const PrefillArgs a) {
     w[i][3] = make_float2(a0.w, a1.w);
   }
   // The sequence of the run's first token, advanced along the run.
-  int b = 0;
-  long long bos = 0, eos = rows;
+  int b = 0, bos = 0, eos = rows;
   if (tb < rows) {
     if (a.cu_seqlens) {  // the last sequence starting at or before tb
       int lo = 0, hi = d.B - 1;
@@ -1282,36 +1285,53 @@ __global__ void __launch_bounds__(256) prefill_qk_kernel(const PrefillArgs a) {
       bos = a.cu_seqlens[b];
       eos = a.cu_seqlens[b + 1];
     } else {
-      b = (int)(tb / d.T);
-      bos = (long long)b * d.T;
+      b = tb / d.T;
+      bos = b * d.T;
       eos = bos + d.T;
     }
   }
+  // Outputs: q^ (plane 0), k^ hi and lo (planes 1, 2), row stride Hk * 128.
+  const long long rstride = (long long)d.Hk * kD;
+  const long long plane = (long long)rows * rstride;
+  __half *dst = static_cast<__half *>(a.qk_ws) + (blk == 0 ? 0 : plane) + (long long)tb * rstride + kh * kD +
+                8 * grp;
+  float2 s0[4], s1[4], s2[4];  // the sliding window: rows t-3, t-2, t-1, widened once each
+  widen(rr[0], s0);
+  widen(rr[1], s1);
+  widen(rr[2], s2);
 #pragma unroll
   for (int u8 = 0; u8 < 8; ++u8) {
-    const long long t = tb + u8;
+    const int t = tb + u8;
     const bool valid = t < rows;  // the shuffles below run on every lane regardless
     if (valid) {
       while (t >= eos && b + 1 < d.B) {  // the run crossed into the next sequence
         ++b;
         bos = eos;
-        eos = a.cu_seqlens ? (long long)a.cu_seqlens[b + 1] : bos + d.T;
+        eos = a.cu_seqlens ? a.cu_seqlens[b + 1] : bos + d.T;
       }
     }
     float2 x0[4], x1[4], x2[4], x3[4];
-    uint4 w0 = rr[u8], w1 = rr[u8 + 1], w2 = rr[u8 + 2];
+    widen(rr[u8 + 3], x3);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x0[i] = s0[i];
+      x1[i] = s1[i];
+      x2[i] = s2[i];
+    }
     if (valid && t - bos < 3) {  // rows before the sequence: the carried window, or zeros
       const bf16 *cw0 = conv0 ? conv0 + (long long)b * 3 * C + c : nullptr;
-      const long long k0 = t - 3 - bos;  // window row of tap 0: -3 .. -1 -> carried rows 0 .. 2
+      const int k0 = t - 3 - bos;  // window row of tap 0: -3 .. -1 -> carried rows 0 .. 2
       const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
-      if (k0 < 0) w0 = cw0 ? *reinterpret_cast<const uint4 *>(cw0 + (3 + k0) * C) : z4;
-      if (k0 + 1 < 0) w1 = cw0 ? *reinterpret_cast<const uint4 *>(cw0 + (4 + k0) * C) : z4;
-      if (k0 + 2 < 0) w2 = cw0 ? *reinterpret_cast<const uint4 *>(cw0 + (5 + k0) * C) : z4;
+      if (k0 < 0) widen(cw0 ? *reinterpret_cast<const uint4 *>(cw0 + (3 + k0) * C) : z4, x0);
+      if (k0 + 1 < 0) widen(cw0 ? *reinterpret_cast<const uint4 *>(cw0 + (4 + k0) * C) : z4, x1);
+      if (k0 + 2 < 0) widen(cw0 ? *reinterpret_cast<const uint4 *>(cw0 + (5 + k0) * C) : z4, x2);
     }
-    widen(w0, x0);
-    widen(w1, x1);
-    widen(w2, x2);
-    widen(rr[u8 + 3], x3);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {  // slide (the raw rows, not the substituted ones)
+      s0[i] = s1[i];
+      s1[i] = s2[i];
+      s2[i] = x3[i];
+    }
     float2 u[4], ss2 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -1329,17 +1349,13 @@ __global__ void __launch_bounds__(256) prefill_qk_kernel(const PrefillArgs a) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) u[i] = __fmul2_rn(u[i], make_float2(f, f));
     if (valid) {
-      const long long off = (t * d.Hk + kh) * kD + 8 * grp;
       uint32_t wh[4], wl[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) split2_inrange(u[i].x, u[i].y, wh[i], wl[i]);  // |k^|, |q^| <= 1
-      if (blk == 0) {
-        *reinterpret_cast<uint4 *>(ws + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-      } else {
-        *reinterpret_cast<uint4 *>(ws + plane + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-        *reinterpret_cast<uint4 *>(ws + 2 * plane + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-      }
+      *reinterpret_cast<uint4 *>(dst) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+      if (blk == 1) *reinterpret_cast<uint4 *>(dst + plane) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
     }
+    dst += rstride;
   }
 }
 
