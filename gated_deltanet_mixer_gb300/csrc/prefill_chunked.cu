@@ -874,18 +874,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncthreads();
     }
-    // A: front end
-    if (kStagedQK)
-      front_end_staged(sm, CV, d, conv_w, h, t0, T, tid, n == 0);
-    else
-      front_end(sm, CV, d, conv_w, h, kh, t0, T, tid, n == 0);
-    smem_ready();
-    // B: MMA1  [K;Q] K^T
-    if (tid == 0) {
+    auto issue_mma1 = [&]() {  // B: MMA1  [K;Q] K^T
       fence_after();
       issue(tmem + TM_KQ, id_kk, 8, false, [&](int ks) { return desc_k(sbase + OFF_KQ, ks, 128); },
             [&](int ks) { return desc_k(sbase + OFF_KQ, ks, 128); });
       commit(&V.bar_qk);
+    };
+    if (kStagedQK) {
+      // [K;Q] arrived by TMA: MMA1 goes first, and the front end (the Gamma k^
+      // pass, read only by MMA7; for the first chunk also the v tiles) runs
+      // while it executes.
+      if (tid == 0) issue_mma1();
+      front_end_staged(sm, CV, d, conv_w, h, t0, T, tid, n == 0);
+    } else {
+      // A: front end
+      front_end(sm, CV, d, conv_w, h, kh, t0, T, tid, n == 0);
+      smem_ready();
+      if (tid == 0) issue_mma1();
     }
     if (!wait_all(&V.bar_qk, ph_qk)) break;
     // MMA5 S Q^T (Q^ = rows 64..127 of [K;Q], S from TMEM), needed only in J
