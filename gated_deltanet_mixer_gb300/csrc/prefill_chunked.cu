@@ -984,6 +984,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tl + TM_W + 32 * half, v);
 #pragma unroll
         for (int q = 0; q < 4; ++q) st_h8_inrange(sm + OFF_NW + mnmaj(32 * half + 8 * q, lrow, kD), v + 8 * q);
+        // [K;Q]'s last readers (MMA1, MMA3, MMA5) are done: the next chunk's
+        // q^ and k^ may land there
+        if (kStagedQK && tid == 0 && n + 1 < nchunks && bar_wait(&V.bar_sq, ph_sq)) {  // else: a timeout at I
+          request_kq(t0 + kC);
+          kq_pending = true;
+        }
       }
     } else {
       // MMA2 U^T, needed only by MMA4: issued behind MMA3 while F runs
@@ -1034,10 +1040,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       // I: MMA6 Delta^T M^T (thread 0); then warp 11 may issue MMA7 behind it
       if (tid == 0) {
         bar_wait(&V.bar_sq, ph_sq);  // MMA5 (the other issuer) done, so bar_o covers O1 and O2
-        if (kStagedQK && n + 1 < nchunks) {  // [K;Q]'s last readers (MMA1, MMA3, MMA5) are done
-          request_kq(t0 + kC);
-          kq_pending = true;
-        }
         fence_after();
         issue_ta(tmem + TM_O2, tmem + TM_KQ, id_kk, 4, false, [&](int ks) { return desc_k(sbase + OFF_M, ks, kC); });
         commit(&V.bar_o);
