@@ -435,11 +435,12 @@ __device__ __forceinline__ void gamma_k_pass(uint8_t *sm, const ChunkVecs &V, in
   }
 }
 // A, staged path: q^ and k^ arrived by TMA, so the front end is the Gamma k^
-// pass (all warps), plus, for the first chunk, the v tiles on warps 8-11.
+// pass (warps 1-11: warp 0 issues the first MMA meanwhile), or, for the first
+// chunk, that pass on warps 0-7 and the v tiles on warps 8-11.
 __device__ void front_end_staged(uint8_t *sm, const ChunkVecs &V, const Dims &d, const bf16 *conv_w, int h,
                                  int t0, int T, int tid, bool with_v) {
   if (!with_v) {
-    gamma_k_pass(sm, V, tid, kThreads);
+    if (tid >= 32) gamma_k_pass(sm, V, tid - 32, kThreads - 32);
   } else if ((tid >> 5) < 8) {
     gamma_k_pass(sm, V, tid, 256);
   } else {
@@ -632,6 +633,18 @@ __device__ __forceinline__ void issue_ta(uint32_t d, uint32_t a0, uint32_t id, i
                                          FB db) {
   for (int ks = 0; ks < nk; ++ks) mma_ta(d, a0 + 8 * ks, db(ks), id, (accumulate_first || ks > 0) ? 1u : 0u);
 }
+// Both, called by a whole converged warp (lane 0 issues).
+template <typename FA, typename FB>
+__device__ __forceinline__ void issue_w(uint32_t d, uint32_t id, int nk, bool accumulate_first, FA da, FB db) {
+#pragma unroll
+  for (int ks = 0; ks < nk; ++ks) mma_w(d, da(ks), db(ks), id, (accumulate_first || ks > 0) ? 1u : 0u);
+}
+template <typename FB>
+__device__ __forceinline__ void issue_ta_w(uint32_t d, uint32_t a0, uint32_t id, int nk, bool accumulate_first,
+                                           FB db) {
+#pragma unroll
+  for (int ks = 0; ks < nk; ++ks) mma_ta_w(d, a0 + 8 * ks, db(ks), id, (accumulate_first || ks > 0) ? 1u : 0u);
+}
 
 // Pack 32 fp32 values into 16 fp16-pair words (saturated to the fp16 range).
 __device__ __forceinline__ void pack_h16(const float (&v)[32], uint32_t (&w)[16]) {
@@ -804,9 +817,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Each mbarrier completes once per chunk; its phase bit is tracked here.
   uint32_t ph_qk = 0, ph_w = 0, ph_d = 0, ph_o = 0, ph_s = 0, ph_sq = 0, ph_u = 0, phase_raw = 0, phase_z = 0,
            phase_kq = 0;
-  // MMAs off the critical path are issued by lane 0 of warp 11, idle in the
-  // phases where it issues them; the critical ones by thread 0.
+  // MMAs off the critical path are issued by warp 11 (its lane 0), idle in the
+  // phases where it issues them; the critical ones by warp 0 (thread 0).  A
+  // whole converged warp runs the issue code.  Warp 10 (lane 0) requests the
+  // raw rows and the staged q^ / k^ of the next chunk.
   const bool issuer2 = tid == kThreads - 32;
+  const bool loader = tid == kThreads - 64;
   bool raw_pending = true, z_pending = true, kq_pending = kStagedQK;  // a requested TMA not yet consumed
   const int nchunks = (T + kC - 1) / kC;
   const uint32_t id_kk = idesc(128, 64, 0, 0);
@@ -860,8 +876,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!wait_all(&V.bar_raw, phase_raw)) break;
       raw_pending = false;
     }
-    if (kStagedQK) {  // q^ and k^ hi of this chunk in [K;Q]
-      if (!wait_all(&V.bar_kq, phase_kq)) break;
+    if (kStagedQK) {  // q^ and k^ hi of this chunk in [K;Q]: one thread waits, the rest meet it
+      if (tid == 0 && !bar_wait(&V.bar_kq, phase_kq)) { atomicOr(a.err, kErrTimeout); V.abort = 1; }
+      phase_kq ^= 1u;
+      fence_after();
+      __syncthreads();
+      if (V.abort) break;
       kq_pending = false;
     }
     if (n == 0) {  // rows before the first token: the carried window, or zeros
@@ -874,31 +894,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncthreads();
     }
-    auto issue_mma1 = [&]() {  // B: MMA1  [K;Q] K^T
+    auto issue_mma1 = [&]() {  // B: MMA1  [K;Q] K^T (warp 0)
+      __syncwarp();
       fence_after();
-      issue(tmem + TM_KQ, id_kk, 8, false, [&](int ks) { return desc_k(sbase + OFF_KQ, ks, 128); },
-            [&](int ks) { return desc_k(sbase + OFF_KQ, ks, 128); });
-      commit(&V.bar_qk);
+      issue_w(tmem + TM_KQ, id_kk, 8, false, [&](int ks) { return desc_k(sbase + OFF_KQ, ks, 128); },
+              [&](int ks) { return desc_k(sbase + OFF_KQ, ks, 128); });
+      commit_w(&V.bar_qk);
     };
     if (kStagedQK) {
       // [K;Q] arrived by TMA: MMA1 goes first, and the front end (the Gamma k^
       // pass, read only by MMA7; for the first chunk also the v tiles) runs
       // while it executes.
-      if (tid == 0) issue_mma1();
+      if (warp == 0) issue_mma1();
       front_end_staged(sm, CV, d, conv_w, h, t0, T, tid, n == 0);
     } else {
       // A: front end
       front_end(sm, CV, d, conv_w, h, kh, t0, T, tid, n == 0);
       smem_ready();
-      if (tid == 0) issue_mma1();
+      if (warp == 0) issue_mma1();
     }
     if (!wait_all(&V.bar_qk, ph_qk)) break;
     // MMA5 S Q^T (Q^ = rows 64..127 of [K;Q], S from TMEM), needed only in J
-    if (issuer2) {
+    if (warp == 11) {
       fence_after();
-      issue_ta(tmem + TM_O1, tmem + TM_S16, id_kk, 8, false,
-               [&](int ks) { return desc_k(sbase + OFF_KQ + 64 * 128, ks, 128); });
-      commit(&V.bar_sq);
+      issue_ta_w(tmem + TM_O1, tmem + TM_S16, id_kk, 8, false,
+                 [&](int ks) { return desc_k(sbase + OFF_KQ + 64 * 128, ks, 128); });
+      commit_w(&V.bar_sq);
     }
     // C: L (fp32, strictly lower, decayed beta K K^T) and M (fp16, decayed Q K^T incl. diagonal)
     if (warp < kTmemWarps) {
@@ -963,18 +984,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     smem_ready();
     // E: MMA2 U^T = V^T (T B)^T, hi*hi + lo*hi + hi*lo; MMA3 -W^T = K^T (-T B D)^T
     // (K^ read from [K;Q] as an MN-major operand).  The raw rows are free now:
-    // request the next chunk's.
-    if (tid == 0) {
-      fence_after();
-      issue(tmem + TM_W, id_mk, 4, false,
-            [&](int ks) { return desc(sbase + OFF_KQ + (uint32_t)(ks * 2048), 128 * 128, 1024); },
-            [&](int ks) { return desc_k(sbase + OFF_TW, ks, kC); });
-      commit(&V.bar_w);
-      if (n + 1 < nchunks) request_raw(t0 + kC);
+    // the loader requests the next chunk's (and, once MMA3 and MMA5 are done,
+    // its q^ and k^).
+    if (n + 1 < nchunks) {
+      raw_pending = true;
+      kq_pending = kStagedQK;
     }
-    if (n + 1 < nchunks) raw_pending = true;
     if (warp < kTmemWarps) {
       if (warp == 0) {
+        fence_after();
+        issue_w(tmem + TM_W, id_mk, 4, false,
+                [&](int ks) { return desc(sbase + OFF_KQ + (uint32_t)(ks * 2048), 128 * 128, 1024); },
+                [&](int ks) { return desc_k(sbase + OFF_TW, ks, kC); });
+        commit_w(&V.bar_w);
         __syncwarp();
         named_arrive(kBarMma3, 64);
       }
@@ -984,38 +1006,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tl + TM_W + 32 * half, v);
 #pragma unroll
         for (int q = 0; q < 4; ++q) st_h8_inrange(sm + OFF_NW + mnmaj(32 * half + 8 * q, lrow, kD), v + 8 * q);
-        // [K;Q]'s last readers (MMA1, MMA3, MMA5) are done: the next chunk's
-        // q^ and k^ may land there
-        if (kStagedQK && tid == 0 && n + 1 < nchunks && bar_wait(&V.bar_sq, ph_sq)) {  // else: a timeout at I
-          request_kq(t0 + kC);
-          kq_pending = true;
-        }
       }
     } else {
       // MMA2 U^T, needed only by MMA4: issued behind MMA3 while F runs
       if (warp == 11) {
         __syncwarp();
         named_sync(kBarMma3, 64);
-      }
-      if (issuer2) {
         fence_after();
         auto a_vh = [&](int ks) { return desc_mn(sbase + OFF_VH, ks, kC); };
         auto b_tu = [&](int ks) { return desc_k(sbase + OFF_TU, ks, kC); };
-        issue(tmem + TM_U, id_mk, 4, false, a_vh, b_tu);
-        issue(tmem + TM_U, id_mk, 4, true, [&](int ks) { return desc_mn(sbase + OFF_VL, ks, kC); }, b_tu);
-        issue(tmem + TM_U, id_mk, 4, true, a_vh, [&](int ks) { return desc_k(sbase + OFF_TUL, ks, kC); });
-        commit(&V.bar_u);
+        issue_w(tmem + TM_U, id_mk, 4, false, a_vh, b_tu);
+        issue_w(tmem + TM_U, id_mk, 4, true, [&](int ks) { return desc_mn(sbase + OFF_VL, ks, kC); }, b_tu);
+        issue_w(tmem + TM_U, id_mk, 4, true, a_vh, [&](int ks) { return desc_k(sbase + OFF_TUL, ks, kC); });
+        commit_w(&V.bar_u);
+      }
+      if (loader && n + 1 < nchunks) {
+        request_raw(t0 + kC);
+        // [K;Q]'s last readers (MMA1, MMA3, MMA5) done: the next chunk's q^
+        // and k^ may land there (a timeout here ends in one at the next chunk)
+        if (kStagedQK && bar_wait(&V.bar_w, ph_w) && bar_wait(&V.bar_sq, ph_sq)) request_kq(t0 + kC);
       }
       ph_w ^= 1u;
     }
     smem_ready();
     if (V.abort) break;
     // G: MMA4 Delta^T = U^T - S W^T (S from TMEM), after MMA2 (the other issuer)
-    if (tid == 0) {
+    if (warp == 0) {
       bar_wait(&V.bar_u, ph_u);  // bounded; a stall here ends in the timeout below
+      __syncwarp();
       fence_after();
-      issue_ta(tmem + TM_U, tmem + TM_S16, id_km, 8, true, [&](int ks) { return desc_mn(sbase + OFF_NW, ks, kD); });
-      commit(&V.bar_d);
+      issue_ta_w(tmem + TM_U, tmem + TM_S16, id_km, 8, true, [&](int ks) { return desc_mn(sbase + OFF_NW, ks, kD); });
+      commit_w(&V.bar_d);
     }
     ph_u ^= 1u;
     if (!wait_all(&V.bar_d, ph_d)) break;
@@ -1038,13 +1059,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp < kTmemWarps) {
       bool ok = true;
       // I: MMA6 Delta^T M^T (thread 0); then warp 11 may issue MMA7 behind it
-      if (tid == 0) {
-        bar_wait(&V.bar_sq, ph_sq);  // MMA5 (the other issuer) done, so bar_o covers O1 and O2
-        fence_after();
-        issue_ta(tmem + TM_O2, tmem + TM_KQ, id_kk, 4, false, [&](int ks) { return desc_k(sbase + OFF_M, ks, kC); });
-        commit(&V.bar_o);
-      }
       if (warp == 0) {
+        bar_wait(&V.bar_sq, ph_sq);  // MMA5 (the other issuer) done, so bar_o covers O1 and O2
+        __syncwarp();
+        fence_after();
+        issue_ta_w(tmem + TM_O2, tmem + TM_KQ, id_kk, 4, false, [&](int ks) { return desc_k(sbase + OFF_M, ks, kC); });
+        commit_w(&V.bar_o);
         __syncwarp();
         named_arrive(kBarMma6, 64);
       }
@@ -1174,14 +1194,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (warp == 11) {
         __syncwarp();
         named_sync(kBarMma6, 64);
-      }
-      if (issuer2) {
         fence_after();
         auto b_gk = [&](int ks) { return desc_mn(sbase + OFF_GK, ks, kC); };
-        issue_ta(tmem + TM_S, tmem + TM_KQ, id_km128, 4, true, b_gk);
-        issue_ta(tmem + TM_S, tmem + TM_KQ, id_km128, 4, true, [&](int ks) { return desc_mn(sbase + OFF_GKL, ks, kC); });
-        issue_ta(tmem + TM_S, tmem + TM_KQ + 32, id_km128, 4, true, b_gk);
-        commit(&V.bar_s);
+        issue_ta_w(tmem + TM_S, tmem + TM_KQ, id_km128, 4, true, b_gk);
+        issue_ta_w(tmem + TM_S, tmem + TM_KQ, id_km128, 4, true,
+                   [&](int ks) { return desc_mn(sbase + OFF_GKL, ks, kC); });
+        issue_ta_w(tmem + TM_S, tmem + TM_KQ + 32, id_km128, 4, true, b_gk);
+        commit_w(&V.bar_s);
       }
       ph_o ^= 1u;
       phase_z ^= 1u;
