@@ -33,19 +33,22 @@
 // an entry of those beyond 65504 (far outside any model's regime) would
 // overflow to inf.
 // Per chunk, in order:
-//   A  conv + SiLU + L2 norms (front end) from the staged raw rows
+//   A  conv + SiLU + L2 norms of q and k (front end) from the staged raw rows
+//      (staged path: q^ and k^ come by TMA; only Gamma k^ is formed)
 //   B  MMA1  [K;Q] K^T -> K K^T, Q K^T;  MMA5  S Q^T
 //   C  decayed lower-triangular L (fp32) and M (fp16)
-//   D  T = (I + L)^{-1} in 16 x 16 blocks (fp32, CUDA cores) -> T B, T B D
+//   D  T = (I + L)^{-1} in 16 x 16 blocks (fp32, CUDA cores, warps 0-7) ->
+//      T B, T B D; meanwhile the v tiles (conv + SiLU of v, warps 8-11)
 //   E  MMA2  U^T = V^T (T B)^T (split);  MMA3  -W^T = K^T (-T B D)^T;
-//      the next chunk's raw rows are requested (TMA)
+//      the next chunk's raw rows are requested (TMA), and its q^ and k^
 //   F  -W^T to shared memory
 //   G  MMA4  Delta^T = U^T - S W^T
 //   H  Delta^T (hi, lo) to TMEM
 //   I  MMA6  Delta^T M^T;            MMA7  S += Delta^T (Gamma K) (split)
-//   J  O = d (S Q^T) + Delta^T M^T, gated RMSNorm (node gdn.norm) -> o,
-//      while MMA7 runs; then S -> fp16 copy, rescaled for the next chunk
-//      (or S_T after the last), and the next chunk's z rows are requested
+//   J  O = d (S Q^T) + Delta^T M^T, gated RMSNorm (node gdn.norm) -> o on
+//      warps 0-7; on warps 8-11, once MMA7 is done, S -> fp16 copy, rescaled
+//      for the next chunk (or S_T after the last); then the next chunk's z
+//      rows are requested
 // Each MMA group commits to its own mbarrier, so a phase waits only for the
 // products it reads (C for K K^T, F for W^T, J for O) while the rest of the
 // chain (S Q^T, U^T, the state update) keeps the tensor pipe busy.
@@ -69,6 +72,8 @@ constexpr float kGMin = -80.0f;
 constexpr int kBarTmem = 1;  // named barrier of warps 0-7 in the epilogue
 constexpr int kBarMma6 = 2;  // warp 0 (MMA6 issued) -> warp 11 (may issue MMA7)
 constexpr int kBarMma3 = 3;  // warp 0 (MMA3 issued) -> warp 11 (may issue MMA2)
+constexpr int kBarSolve = 4;  // warps 0-7 in the solve
+constexpr int kBarEpi = 5;    // warps 8-11 in the epilogue (the next chunk's decay formed)
 
 __device__ __forceinline__ void named_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -375,30 +380,17 @@ __device__ __forceinline__ void fe_pass(uint8_t *sm, const ChunkVecs &V, const D
   }
 }
 
-// A: front end for one chunk, from the staged raw rows.  Work per token is
-// about 78 (q), 127 (k: norm, single and split outputs) and 100 (v: split)
-// units, so warps 0-7 each take q and then k of 4 tokens per half-warp
-// (32 token groups of 4), and warps 8-11 take v of 8 tokens per half-warp.
-// with_v: the first chunk; later chunks' v tiles are made by warps 8-11
-// during the previous chunk's epilogue (front_end_v), so the others split
-// q and k between all twelve warps: k on warps 0-7 (4 tokens per half-warp),
-// q on warps 8-11 (7 tokens) and the last 8 q tokens on warps 0-3 (one per
-// half-warp, before their k): at most 586 units per half-warp, against 624
-// with all of q on warps 8-11.
-__device__ void front_end(uint8_t *sm, const ChunkVecs &V, const Dims &d, const bf16 *conv_w,
-                          int h, int kh, int t0, int T, int tid, bool with_v) {
+// A: front end for one chunk (q and k), from the staged raw rows; the v tiles
+// are made during the solve (front_end_v).  Work per token is about 78 (q)
+// and 127 (k: norm, single and split outputs) units, so k goes to warps 0-7
+// (4 tokens per half-warp), q to warps 8-11 (7 tokens) and the last 8 q
+// tokens to warps 0-3 (one per half-warp, before their k): at most 586 units
+// per half-warp, against 624 with all of q on warps 8-11.
+__device__ void front_end(uint8_t *sm, const ChunkVecs &V, const Dims &d, const bf16 *conv_w, int kh, int t0,
+                          int T, int tid) {
   const int warp = tid >> 5, lane = tid & 31, grp = lane & 15;
   const long long cq = (long long)kh * kD + 8 * grp, ck = (long long)d.Hk * kD + (long long)kh * kD + 8 * grp;
-  if (with_v) {
-    if (warp < 8) {
-      const int r0 = 4 * (2 * warp + (lane >> 4));
-      fe_pass<4>(sm, V, d, conv_w, 0, cq, r0, t0, T, grp);
-      fe_pass<4>(sm, V, d, conv_w, 1, ck, r0, t0, T, grp);
-    } else {
-      const int r0 = 8 * (2 * (warp - 8) + (lane >> 4));
-      fe_pass<8>(sm, V, d, conv_w, 2, 2LL * d.Hk * kD + (long long)h * kD + 8 * grp, r0, t0, T, grp);
-    }
-  } else if (warp < 8) {
+  if (warp < 8) {
     if (warp < 4) fe_pass<1>(sm, V, d, conv_w, 0, cq, 56 + 2 * warp + (lane >> 4), t0, T, grp);
     fe_pass<4>(sm, V, d, conv_w, 1, ck, 4 * (2 * warp + (lane >> 4)), t0, T, grp);
   } else {
@@ -435,17 +427,9 @@ __device__ __forceinline__ void gamma_k_pass(uint8_t *sm, const ChunkVecs &V, in
   }
 }
 // A, staged path: q^ and k^ arrived by TMA, so the front end is the Gamma k^
-// pass (warps 1-11: warp 0 issues the first MMA meanwhile), or, for the first
-// chunk, that pass on warps 0-7 and the v tiles on warps 8-11.
-__device__ void front_end_staged(uint8_t *sm, const ChunkVecs &V, const Dims &d, const bf16 *conv_w, int h,
-                                 int t0, int T, int tid, bool with_v) {
-  if (!with_v) {
-    if (tid >= 32) gamma_k_pass(sm, V, tid - 32, kThreads - 32);
-  } else if ((tid >> 5) < 8) {
-    gamma_k_pass(sm, V, tid, 256);
-  } else {
-    front_end_v(sm, V, d, conv_w, h, t0, T, tid);
-  }
+// pass (warps 1-11: warp 0 issues the first MMA meanwhile).
+__device__ void front_end_staged(uint8_t *sm, const ChunkVecs &V, int tid) {
+  if (tid >= 32) gamma_k_pass(sm, V, tid - 32, kThreads - 32);
 }
 
 // T scratch: fp32 [64][64], float4 groups XOR-swizzled by row, so that reads of
@@ -491,7 +475,7 @@ __device__ void zero_T_upper(uint8_t *sm, int tid, int q0 = 0, int nthreads = kT
   }
 }
 
-// D: T = (I + L)^{-1} (L strictly lower, 64 x 64), fp32, by recursive
+// D (warps 0-7): T = (I + L)^{-1} (L strictly lower, 64 x 64), fp32, by recursive
 // doubling on 16 x 16 blocks: the four diagonal blocks by forward
 // substitution (one column per thread); the two 32 x 32 halves by
 // T_BA = -T_BB (L_BA T_AA); then the whole by the same identity on the
@@ -525,7 +509,8 @@ __device__ void solve_T(uint8_t *sm, const ChunkVecs &V, int tid) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) Tf[tfi(base + i, base + c)] = xv[i];
   }
-  __syncthreads();
+  __syncwarp();
+  named_sync(kBarSolve, kTmemWarps * 32);
   // The 32 x 32 halves (A, B) = (0, 1), (2, 3): P = L_BA T_AA, T_BA = -T_BB P.
   const int h = tid >> 6, r16 = (tid >> 2) & 15, c4 = tid & 3;
   const int A = 2 * h, Bb = A + 1;
@@ -542,11 +527,15 @@ __device__ void solve_T(uint8_t *sm, const ChunkVecs &V, int tid) {
       fma4(acc, l.w, ld4(Tf + tfi(row + 3, col)));
     }
     *reinterpret_cast<float4 *>(P + h * 256 + r16 * 16 + 4 * c4) = acc;
-  } else {  // the diagonal blocks are final
-    const int q = tid - 128, b = q >> 6, row = 16 * b + ((q >> 2) & 15), col = 16 * b + 4 * (q & 3);
-    store_T4(sm, V, row, col, ld4(Tf + tfi(row, col)));
+  } else {  // the diagonal blocks are final (two items per thread)
+#pragma unroll
+    for (int q = tid - 128; q < 256; q += 128) {
+      const int b = q >> 6, row = 16 * b + ((q >> 2) & 15), col = 16 * b + 4 * (q & 3);
+      store_T4(sm, V, row, col, ld4(Tf + tfi(row, col)));
+    }
   }
-  __syncthreads();
+  __syncwarp();
+  named_sync(kBarSolve, kTmemWarps * 32);
   if (tid < 128) {
     const int row = 16 * Bb + r16;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -560,7 +549,8 @@ __device__ void solve_T(uint8_t *sm, const ChunkVecs &V, int tid) {
     }
     *reinterpret_cast<float4 *>(Tf + tfi(row, 16 * A + 4 * c4)) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
   }
-  __syncthreads();
+  __syncwarp();
+  named_sync(kBarSolve, kTmemWarps * 32);
   // The whole: P = L[32:64][0:32] T[0:32][0:32], T[32:64][0:32] = -T[32:64][32:64] P,
   // each thread two rows (r, r + 16) by four columns, so every operand load
   // feeds eight products.
@@ -589,7 +579,8 @@ __device__ void solve_T(uint8_t *sm, const ChunkVecs &V, int tid) {
     const int row = 16 * (2 * hh + 1) + ((q >> 2) & 15), cc = 32 * hh + 4 * (q & 3);
     store_T4(sm, V, row, cc, ld4(Tf + tfi(row, cc)));
   }
-  __syncthreads();
+  __syncwarp();
+  named_sync(kBarSolve, kTmemWarps * 32);
   if (tid < 128) {  // rows 32 + r (T_BB row has 16 terms) and 48 + r (32 terms); T[32:48][48:64] is zero
     const int ra = 32 + r16b, rb = 48 + r16b;
     float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
@@ -618,7 +609,7 @@ __device__ void solve_T(uint8_t *sm, const ChunkVecs &V, int tid) {
     store_T4(sm, V, ra, col, make_float4(-acc0.x, -acc0.y, -acc0.z, -acc0.w));
     store_T4(sm, V, rb, col, make_float4(-acc1.x, -acc1.y, -acc1.z, -acc1.w));
   } else {
-    zero_T_upper(sm, tid - 128, 192, kThreads - 128, 2 * 192);  // tile 1, overwritten by the O staging
+    zero_T_upper(sm, tid - 128, 192, 128, 2 * 192);  // tile 1, overwritten by the O staging
   }
 }
 
@@ -872,18 +863,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     // A0: chunk vectors; the next chunk's g and beta requested
     ChunkVecs &CV = V.cv[n & 1];  // formed before the loop or during the previous chunk's solve
     if (warp == 11 && n + 1 < nchunks) load_gb<kRawGates>(a.gate, bos, d.Hv, h, t0 + kC, T, lane, g_nxt, b_nxt);
-    if (n == 0) {  // later chunks' rows were awaited by warps 8-11 during the previous epilogue
-      if (!wait_all(&V.bar_raw, phase_raw)) break;
-      raw_pending = false;
+    // This chunk's staged rows (and q^, k^ hi in [K;Q]): one thread waits, the
+    // rest meet it.
+    if (tid == 0) {
+      bool ok = bar_wait(&V.bar_raw, phase_raw);
+      if (kStagedQK) ok = bar_wait(&V.bar_kq, phase_kq) && ok;
+      if (!ok) {
+        atomicOr(a.err, kErrTimeout);
+        V.abort = 1;
+      }
     }
-    if (kStagedQK) {  // q^ and k^ hi of this chunk in [K;Q]: one thread waits, the rest meet it
-      if (tid == 0 && !bar_wait(&V.bar_kq, phase_kq)) { atomicOr(a.err, kErrTimeout); V.abort = 1; }
+    phase_raw ^= 1u;
+    raw_pending = false;
+    if (kStagedQK) {
       phase_kq ^= 1u;
-      fence_after();
-      __syncthreads();
-      if (V.abort) break;
       kq_pending = false;
     }
+    fence_after();
+    __syncthreads();
+    if (V.abort) break;
     if (n == 0) {  // rows before the first token: the carried window, or zeros
       for (int idx = kStagedQK ? 2 * 48 + tid : tid; idx < 3 * 3 * 16; idx += kThreads) {
         const int blk = idx / 48, rw = (idx / 16) % 3, g8 = idx % 16;
@@ -906,10 +904,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // pass, read only by MMA7; for the first chunk also the v tiles) runs
       // while it executes.
       if (warp == 0) issue_mma1();
-      front_end_staged(sm, CV, d, conv_w, h, t0, T, tid, n == 0);
+      front_end_staged(sm, CV, tid);
     } else {
       // A: front end
-      front_end(sm, CV, d, conv_w, h, kh, t0, T, tid, n == 0);
+      front_end(sm, CV, d, conv_w, kh, t0, T, tid);
       smem_ready();
       if (warp == 0) issue_mma1();
     }
@@ -972,15 +970,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncthreads();
-    // D: the triangular inverse, scaled copies T B and T B D.  Warp 11, idle
-    // in the solve, forms the next chunk's gates and total decay meanwhile
-    // (through shared memory, so that the work stays here).
-    if (warp == 11 && n + 1 < nchunks) {
-      finish_gb<kRawGates>(neg_exp_A, dt_bias, t0 + kC, T, lane, g_nxt, b_nxt);
-      const float dcn = chunk_vectors(V.cv[(n + 1) & 1], g_nxt, b_nxt, lane);
-      if (lane == 0) V.dC_next = dcn;
-    }
-    solve_T(sm, CV, tid);
+    // D: the triangular inverse, scaled copies T B and T B D (warps 0-7);
+    // meanwhile warps 8-11 make this chunk's v tiles from its staged rows (the
+    // V tiles were last read by MMA2 of the previous chunk; the raw v rows do
+    // not share space with the solve's scratch).
+    if (warp < kTmemWarps)
+      solve_T(sm, CV, tid);
+    else
+      front_end_v(sm, CV, d, conv_w, h, t0, T, tid);
     smem_ready();
     // E: MMA2 U^T = V^T (T B)^T, hi*hi + lo*hi + hi*lo; MMA3 -W^T = K^T (-T B D)^T
     // (K^ read from [K;Q] as an MN-major operand).  The raw rows are free now:
@@ -1052,10 +1049,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_st();
     }
     smem_ready();
-    // The epilogue.  Warps 0-7 (TMEM) finish this chunk and sync among
-    // themselves (named barrier 1); warps 8-11 meanwhile make the next
-    // chunk's v tiles from its staged rows (the V tiles were last read by
-    // MMA2, complete since G).  Everyone meets at the end of the chunk.
+    // The epilogue.  Warps 0-7 (TMEM) form and store the output and sync
+    // among themselves (named barrier 1); warps 8-11 meanwhile issue the state
+    // update and pass the state on.  Everyone meets at the end of the chunk.
     if (warp < kTmemWarps) {
       bool ok = true;
       // I: MMA6 Delta^T M^T (thread 0); then warp 11 may issue MMA7 behind it
@@ -1140,57 +1136,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       }
-      // J3: S -> fp16 copy and rescaled state (or S_T after the last chunk), in TMEM
-      ok = wait_tmem(&V.bar_s, ph_s) && ok;
-      if (ok) {
-      {
-        const bool last = n + 1 == nchunks;
-        const float dcn = V.dC_next;
-        const int k0 = 64 * half;
-        uint32_t r0[32], r1[32];
-        tmem_ld32_nw(tl + TM_S + k0, r0);
-        tmem_ld32_nw(tl + TM_S + k0 + 32, r1);
-        tmem_wait_ld();
-        if (last) {
-          float4 *dst = reinterpret_cast<float4 *>(a.S_T + unit_off + (long long)lrow * kD + k0);
-  #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            dst[q] = make_float4(__uint_as_float(r0[4 * q]), __uint_as_float(r0[4 * q + 1]),
-                                 __uint_as_float(r0[4 * q + 2]), __uint_as_float(r0[4 * q + 3]));
-  #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            dst[8 + q] = make_float4(__uint_as_float(r1[4 * q]), __uint_as_float(r1[4 * q + 1]),
-                                     __uint_as_float(r1[4 * q + 2]), __uint_as_float(r1[4 * q + 3]));
-        } else {
-          uint32_t w16[16];
-  #pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            w16[q] = pack2_inrange(__uint_as_float(r0[2 * q]), __uint_as_float(r0[2 * q + 1]));
-          }
-          tmem_st16w_nw(tl + TM_S16 + k0 / 2, w16);
-  #pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            w16[q] = pack2_inrange(__uint_as_float(r1[2 * q]), __uint_as_float(r1[2 * q + 1]));
-          }
-          tmem_st16w_nw(tl + TM_S16 + k0 / 2 + 16, w16);
-  #pragma unroll
-          for (int q = 0; q < 32; q += 2) {  // paired fp32 multiplies
-            float2 x0 = __fmul2_rn(make_float2(__uint_as_float(r0[q]), __uint_as_float(r0[q + 1])), make_float2(dcn, dcn));
-            float2 x1 = __fmul2_rn(make_float2(__uint_as_float(r1[q]), __uint_as_float(r1[q + 1])), make_float2(dcn, dcn));
-            r0[q] = __float_as_uint(x0.x);
-            r0[q + 1] = __float_as_uint(x0.y);
-            r1[q] = __float_as_uint(x1.x);
-            r1[q + 1] = __float_as_uint(x1.y);
-          }
-          tmem_st32w_nw(tl + TM_S + k0, r0);
-          tmem_st32w_nw(tl + TM_S + k0 + 32, r1);
-          tmem_wait_st();
-        }
-      }
-      }
+      ph_s ^= 1u;
     } else {
-      // MMA7 S += Delta^T (Gamma K), hi*hi + hi*lo + lo*hi: needed only in J3,
-      // issued once MMA6 is in the queue ahead of it
+      // MMA7 S += Delta^T (Gamma K), hi*hi + hi*lo + lo*hi, issued once MMA6 is
+      // in the queue ahead of it; while it runs, warp 11 forms the next
+      // chunk's gates and chunk vectors (through shared memory).
       if (warp == 11) {
         __syncwarp();
         named_sync(kBarMma6, 64);
@@ -1201,30 +1151,74 @@ __global__ void __launch_bounds__(kThreads, 1)
                    [&](int ks) { return desc_mn(sbase + OFF_GKL, ks, kC); });
         issue_ta_w(tmem + TM_S, tmem + TM_KQ + 32, id_km128, 4, true, b_gk);
         commit_w(&V.bar_s);
+        if (n + 1 < nchunks) {
+          finish_gb<kRawGates>(neg_exp_A, dt_bias, t0 + kC, T, lane, g_nxt, b_nxt);
+          const float dcn = chunk_vectors(V.cv[(n + 1) & 1], g_nxt, b_nxt, lane);
+          if (lane == 0) V.dC_next = dcn;
+        }
       }
       ph_o ^= 1u;
       phase_z ^= 1u;
+      // J3 (warps 8-11, all 128 state columns each, alongside J2 on warps
+      // 0-7): S -> fp16 copy and rescaled state (or S_T after the last
+      // chunk), in TMEM
+      __syncwarp();
+      named_sync(kBarEpi, 128);  // the next chunk's total decay is formed
+      bool ok = bar_wait(&V.bar_s, ph_s);
       ph_s ^= 1u;
-      if (n + 1 < nchunks) {  // the next chunk's v tiles
-        __syncwarp();
-        const bool got = bar_wait(&V.bar_raw, phase_raw);
-        fence_after();
-        if (__all_sync(0xffffffffu, got)) {
-          front_end_v(sm, V.cv[(n + 1) & 1], d, conv_w, h, t0 + kC, T, tid);
-        } else if (lane == 0) {
-          atomicOr(a.err, kErrTimeout);
-          V.abort = 1;
+      fence_after();
+      if (__all_sync(0xffffffffu, ok)) {
+        const bool last = n + 1 == nchunks;
+        const float dcn = V.dC_next;
+#pragma unroll 1
+        for (int k0 = 0; k0 < kD; k0 += 64) {
+          uint32_t r0[32], r1[32];
+          tmem_ld32_nw(tl + TM_S + k0, r0);
+          tmem_ld32_nw(tl + TM_S + k0 + 32, r1);
+          tmem_wait_ld();
+          if (last) {
+            float4 *dst = reinterpret_cast<float4 *>(a.S_T + unit_off + (long long)lrow * kD + k0);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              dst[q] = make_float4(__uint_as_float(r0[4 * q]), __uint_as_float(r0[4 * q + 1]),
+                                   __uint_as_float(r0[4 * q + 2]), __uint_as_float(r0[4 * q + 3]));
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              dst[8 + q] = make_float4(__uint_as_float(r1[4 * q]), __uint_as_float(r1[4 * q + 1]),
+                                       __uint_as_float(r1[4 * q + 2]), __uint_as_float(r1[4 * q + 3]));
+          } else {
+            uint32_t w16[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) w16[q] = pack2_inrange(__uint_as_float(r0[2 * q]), __uint_as_float(r0[2 * q + 1]));
+            tmem_st16w_nw(tl + TM_S16 + k0 / 2, w16);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) w16[q] = pack2_inrange(__uint_as_float(r1[2 * q]), __uint_as_float(r1[2 * q + 1]));
+            tmem_st16w_nw(tl + TM_S16 + k0 / 2 + 16, w16);
+#pragma unroll
+            for (int q = 0; q < 32; q += 2) {  // paired fp32 multiplies
+              float2 x0 = __fmul2_rn(make_float2(__uint_as_float(r0[q]), __uint_as_float(r0[q + 1])), make_float2(dcn, dcn));
+              float2 x1 = __fmul2_rn(make_float2(__uint_as_float(r1[q]), __uint_as_float(r1[q + 1])), make_float2(dcn, dcn));
+              r0[q] = __float_as_uint(x0.x);
+              r0[q + 1] = __float_as_uint(x0.y);
+              r1[q] = __float_as_uint(x1.x);
+              r1[q + 1] = __float_as_uint(x1.y);
+            }
+            tmem_st32w_nw(tl + TM_S + k0, r0);
+            tmem_st32w_nw(tl + TM_S + k0 + 32, r1);
+            tmem_wait_st();
+          }
         }
+      } else if (lane == 0) {
+        atomicOr(a.err, kErrTimeout);
+        V.abort = 1;
       }
     }
     ph_sq ^= 1u;
-    if (n + 1 < nchunks) phase_raw ^= 1u;  // consumed by warps 8-11 above
     fence_before();
-    fence_smem_to_async();  // z, the staging and the next v tiles: order before the next TMA and MMA reads
+    fence_smem_to_async();  // z and the staging: order before the next TMA and MMA reads
     __syncthreads();
     if (V.abort) break;
     if (n + 1 < nchunks) {
-      raw_pending = false;
       if (tid == 0) request_z(t0 + kC);
       z_pending = true;
     }
