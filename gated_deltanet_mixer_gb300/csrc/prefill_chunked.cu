@@ -145,7 +145,7 @@ struct __align__(16) ChunkVecs {  // per-token vectors of one chunk
   int mild;        // G_last >= -40: ratios as d_i * dinv_j
 };
 struct __align__(16) Vecs {  // shared-memory scalars, vectors and barriers
-  ChunkVecs cv[2];  // chunk n uses cv[n & 1]; chunk n + 1's are formed during chunk n's solve
+  ChunkVecs cv[2];  // chunk n uses cv[n & 1]; chunk n + 1's are formed during chunk n's epilogue
   float dC_next;   // e^{G_last} of the next chunk
   int abort;
   uint32_t tmem;
@@ -869,7 +869,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int n = 0; n < nchunks; ++n) {
     const int t0 = n * kC;
     // A0: chunk vectors; the next chunk's g and beta requested
-    ChunkVecs &CV = V.cv[n & 1];  // formed before the loop or during the previous chunk's solve
+    ChunkVecs &CV = V.cv[n & 1];  // formed before the loop or during the previous chunk's epilogue
     if (warp == 11 && n + 1 < nchunks) load_gb<kRawGates>(a.gate, bos, d.Hv, h, t0 + kC, T, lane, g_nxt, b_nxt);
     // This chunk's staged rows (and q^, k^ hi in [K;Q]): one thread waits, the
     // rest meet it.
@@ -1062,7 +1062,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // update and pass the state on.  Everyone meets at the end of the chunk.
     if (warp < kTmemWarps) {
       bool ok = true;
-      // I: MMA6 Delta^T M^T (thread 0); then warp 11 may issue MMA7 behind it
+      // I: MMA6 Delta^T M^T (warp 0); then warp 11 may issue MMA7 behind it
       if (warp == 0) {
         bar_wait(&V.bar_sq, ph_sq);  // MMA5 (the other issuer) done, so bar_o covers O1 and O2
         __syncwarp();
