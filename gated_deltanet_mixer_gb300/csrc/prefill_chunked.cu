@@ -1266,21 +1266,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // A [B][T][width] bf16 tensor as a 3-d map with boxes of 128 columns x `rows` rows.
 // The q^ / k^ front end of the staged path, once per key head rather than
-// once per value head: conv + SiLU + L2 norm of q and k for 64 token rows,
-// written as fp16 q^ and as an fp16 hi/lo pair for k^ (hi = fp16(k^),
-// lo = fp16(k^ - hi)) into qk_ws [3][rows][Hk][128].  The arithmetic is
-// fe_pass's, so q^ and k^'s hi part equal the fused kernel's operands bit
-// for bit.  Half-warps 0-7 take q, 8-15 take k, a run of 8 tokens each: the
-// run's 11 rows are loaded up front and the window slides over them; a token
-// within three rows of its sequence's start takes those rows from the
-// carried window (or zeros) instead.
-__global__ void __launch_bounds__(256) prefill_qk_kernel(const PrefillArgs a) {
+// once per value head: conv + SiLU + L2 norm of q and k, written as fp16 q^
+// and as an fp16 hi/lo pair for k^ (hi = fp16(k^), lo = fp16(k^ - hi)) into
+// qk_ws [3][rows][Hk][128].  The arithmetic is fe_pass's, so q^ and k^'s hi
+// part equal the fused kernel's operands bit for bit.
+// Persistent: a CTA keeps one key head and takes every nslots-th 64-token
+// tile.  A tile's raw q and k rows, with the three before it, arrive by TMA
+// in one of two stages, the next tile's while this one is computed.
+// Half-warps 0-7 take q, 8-15 take k, a run of 8 tokens each, the window
+// sliding over the staged rows; a token within three rows of its sequence's
+// start takes those rows from the carried window (or zeros) instead.
+constexpr int kQkThreads = 256;
+constexpr uint32_t kQkStage = 2 * kRawBlock;            // raw q | k rows of one tile
+constexpr uint32_t kQkSmem = 2 * kQkStage + 64 + 128;   // two stages, two mbarriers, alignment slack
+static_assert(kQkStage % 128 == 0, "TMA stage alignment");
+
+__global__ void __launch_bounds__(kQkThreads, 2)
+    prefill_qk_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tm_qkv) {
+  extern __shared__ uint8_t qk_smem_raw[];
+  uint8_t *sm = qk_smem_raw + ((128 - (smem_u32(qk_smem_raw) & 127)) & 127);
+  const uint32_t sbase = smem_u32(sm);
+  uint64_t *full = reinterpret_cast<uint64_t *>(sm + 2 * kQkStage);  // a stage's rows landed
   const Dims d = a.d;
-  // Key heads vary fastest across the grid, so the CTAs running together read
-  // neighbouring slices of the same rows.  Token rows fit in 31 bits.
   const int kh = (int)(blockIdx.x % (unsigned)d.Hk);
-  const int tile = (int)(blockIdx.x / (unsigned)d.Hk);
-  const int rows = a.cu_seqlens ? d.T : d.B * d.T;
+  const int slot = (int)(blockIdx.x / (unsigned)d.Hk), nslots = (int)(gridDim.x / (unsigned)d.Hk);
+  const int rows = a.cu_seqlens ? d.T : d.B * d.T;  // token rows fit in 31 bits
+  const int ntiles = (rows + kC - 1) / kC;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, grp = lane & 15;
   const int hw = 2 * warp + (lane >> 4);  // half-warp 0..15
   const int blk = hw >> 3;                // 0: q, 1: k
@@ -1289,19 +1300,24 @@ __global__ void __launch_bounds__(256) prefill_qk_kernel(const PrefillArgs a) {
   const float scale = blk == 0 ? d.q_scale : 1.0f;
   const bf16 *conv_w = static_cast<const bf16 *>(a.conv_w);
   const bf16 *conv0 = static_cast<const bf16 *>(a.conv0);
-  const int tb = tile * kC + 8 * (hw & 7);  // this half-warp's run: tokens tb .. tb+7
-  // rows tb-3 .. tb+7 of this lane's 8 channels
-  const bf16 *xr = static_cast<const bf16 *>(a.qkv_pre) + ((long long)tb - 3) * C + c;
-  uint4 rr[11];
-  if (tb >= 3 && tb + 8 <= rows) {
-#pragma unroll
-    for (int j = 0; j < 11; ++j) rr[j] = *reinterpret_cast<const uint4 *>(xr + j * C);
-  } else {
-#pragma unroll
-    for (int j = 0; j < 11; ++j) {
-      const int r = tb - 3 + j;
-      rr[j] = (r >= 0 && r < rows) ? *reinterpret_cast<const uint4 *>(xr + j * C) : make_uint4(0u, 0u, 0u, 0u);
-    }
+  if (tid == 0) {
+    bar_init(&full[0], 1);
+    bar_init(&full[1], 1);
+  }
+  __syncthreads();
+  // Thread 0: a tile's rows tile*64-3 .. tile*64+63 of this head's q and k
+  // channels into a stage (rows outside the tensor read as zeros).
+  uint32_t issued0 = 0u, issued1 = 0u;  // uses of stage 0 and 1 requested (thread 0)
+  auto request = [&](int tile, int stage) {
+    bar_expect_tx(&full[stage], kQkStage);
+    const int row = tile * kC - 3;
+    tma_load_3d(sbase + stage * kQkStage, &tm_qkv, kh * kD, row, 0, &full[stage]);
+    tma_load_3d(sbase + stage * kQkStage + kRawBlock, &tm_qkv, d.Hk * kD + kh * kD, row, 0, &full[stage]);
+    if (stage) ++issued1; else ++issued0;
+  };
+  if (tid == 0) {
+    if (slot < ntiles) request(slot, 0);
+    if (slot + nslots < ntiles) request(slot + nslots, 1);
   }
   float2 w[4][4];  // [channel pair][tap]
 #pragma unroll
@@ -1312,90 +1328,111 @@ __global__ void __launch_bounds__(256) prefill_qk_kernel(const PrefillArgs a) {
     w[i][2] = make_float2(a0.z, a1.z);
     w[i][3] = make_float2(a0.w, a1.w);
   }
-  // The sequence of the run's first token, advanced along the run.
-  int b = 0, bos = 0, eos = rows;
-  if (tb < rows) {
-    if (a.cu_seqlens) {  // the last sequence starting at or before tb
-      int lo = 0, hi = d.B - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (a.cu_seqlens[mid] <= tb) lo = mid; else hi = mid - 1;
-      }
-      b = lo;
-      bos = a.cu_seqlens[b];
-      eos = a.cu_seqlens[b + 1];
-    } else {
-      b = tb / d.T;
-      bos = b * d.T;
-      eos = bos + d.T;
-    }
-  }
   // Outputs: q^ (plane 0), k^ hi and lo (planes 1, 2), row stride Hk * 128.
   const long long rstride = (long long)d.Hk * kD;
   const long long plane = (long long)rows * rstride;
-  __half *dst = static_cast<__half *>(a.qk_ws) + (blk == 0 ? 0 : plane) + (long long)tb * rstride + kh * kD +
-                8 * grp;
-  float2 s0[4], s1[4], s2[4];  // the sliding window: rows t-3, t-2, t-1, widened once each
-  widen(rr[0], s0);
-  widen(rr[1], s1);
-  widen(rr[2], s2);
-#pragma unroll
-  for (int u8 = 0; u8 < 8; ++u8) {
-    const int t = tb + u8;
-    const bool valid = t < rows;  // the shuffles below run on every lane regardless
-    if (valid) {
-      while (t >= eos && b + 1 < d.B) {  // the run crossed into the next sequence
-        ++b;
-        bos = eos;
-        eos = a.cu_seqlens ? a.cu_seqlens[b + 1] : bos + d.T;
+  int n = 0;
+  for (int tile = slot; tile < ntiles; tile += nslots, ++n) {
+    const int stage = n & 1;
+    __syncwarp();
+    const bool got = bar_wait(&full[stage], (uint32_t)(n >> 1) & 1u);
+    if (__syncthreads_or(!got)) {
+      if (tid == 0) atomicOr(a.err, kErrTimeout);
+      break;
+    }
+    const int tb = tile * kC + 8 * (hw & 7);  // this half-warp's run: tokens tb .. tb+7
+    // this run's window rows tb-3 .. tb+7 in the stage: 256 bytes per row
+    const uint8_t *xr = sm + stage * kQkStage + blk * kRawBlock + 256 * (8 * (hw & 7)) + 16 * grp;
+    // The sequence of the run's first token, advanced along the run.
+    int b = 0, bos = 0, eos = rows;
+    if (tb < rows) {
+      if (a.cu_seqlens) {  // the last sequence starting at or before tb
+        int lo = 0, hi = d.B - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (a.cu_seqlens[mid] <= tb) lo = mid; else hi = mid - 1;
+        }
+        b = lo;
+        bos = a.cu_seqlens[b];
+        eos = a.cu_seqlens[b + 1];
+      } else {
+        b = tb / d.T;
+        bos = b * d.T;
+        eos = bos + d.T;
       }
     }
-    float2 x0[4], x1[4], x2[4], x3[4];
-    widen(rr[u8 + 3], x3);
+    __half *dst = static_cast<__half *>(a.qk_ws) + (blk == 0 ? 0 : plane) + (long long)tb * rstride + kh * kD +
+                  8 * grp;
+    float2 s0[4], s1[4], s2[4];  // the sliding window: rows t-3, t-2, t-1, widened once each
+    widen(*reinterpret_cast<const uint4 *>(xr), s0);
+    widen(*reinterpret_cast<const uint4 *>(xr + 256), s1);
+    widen(*reinterpret_cast<const uint4 *>(xr + 512), s2);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      x0[i] = s0[i];
-      x1[i] = s1[i];
-      x2[i] = s2[i];
+    for (int u8 = 0; u8 < 8; ++u8) {
+      const int t = tb + u8;
+      const bool valid = t < rows;  // the shuffles below run on every lane regardless
+      if (valid) {
+        while (t >= eos && b + 1 < d.B) {  // the run crossed into the next sequence
+          ++b;
+          bos = eos;
+          eos = a.cu_seqlens ? a.cu_seqlens[b + 1] : bos + d.T;
+        }
+      }
+      float2 x0[4], x1[4], x2[4], x3[4];
+      widen(*reinterpret_cast<const uint4 *>(xr + 256 * (u8 + 3)), x3);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        x0[i] = s0[i];
+        x1[i] = s1[i];
+        x2[i] = s2[i];
+      }
+      if (valid && t - bos < 3) {  // rows before the sequence: the carried window, or zeros
+        const bf16 *cw0 = conv0 ? conv0 + (long long)b * 3 * C + c : nullptr;
+        const int k0 = t - 3 - bos;  // window row of tap 0: -3 .. -1 -> carried rows 0 .. 2
+        const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
+        if (k0 < 0) widen(cw0 ? *reinterpret_cast<const uint4 *>(cw0 + (3 + k0) * C) : z4, x0);
+        if (k0 + 1 < 0) widen(cw0 ? *reinterpret_cast<const uint4 *>(cw0 + (4 + k0) * C) : z4, x1);
+        if (k0 + 2 < 0) widen(cw0 ? *reinterpret_cast<const uint4 *>(cw0 + (5 + k0) * C) : z4, x2);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {  // slide (the raw rows, not the substituted ones)
+        s0[i] = s1[i];
+        s1[i] = s2[i];
+        s2[i] = x3[i];
+      }
+      float2 u[4], ss2 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float2 acc = __fmul2_rn(w[i][0], x0[i]);
+        acc = __ffma2_rn(w[i][1], x1[i], acc);
+        acc = __ffma2_rn(w[i][2], x2[i], acc);
+        acc = __ffma2_rn(w[i][3], x3[i], acc);
+        u[i] = silu2(acc);
+        ss2 = __ffma2_rn(u[i], u[i], ss2);
+      }
+      float ss = ss2.x + ss2.y;
+#pragma unroll
+      for (int off = 1; off < 16; off <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+      const float f = rsqrtf(ss + d.eps_l2) * scale;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) u[i] = __fmul2_rn(u[i], make_float2(f, f));
+      if (valid) {
+        uint32_t wh[4], wl[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) split2_inrange(u[i].x, u[i].y, wh[i], wl[i]);  // |k^|, |q^| <= 1
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+        if (blk == 1) *reinterpret_cast<uint4 *>(dst + plane) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+      }
+      dst += rstride;
     }
-    if (valid && t - bos < 3) {  // rows before the sequence: the carried window, or zeros
-      const bf16 *cw0 = conv0 ? conv0 + (long long)b * 3 * C + c : nullptr;
-      const int k0 = t - 3 - bos;  // window row of tap 0: -3 .. -1 -> carried rows 0 .. 2
-      const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
-      if (k0 < 0) widen(cw0 ? *reinterpret_cast<const uint4 *>(cw0 + (3 + k0) * C) : z4, x0);
-      if (k0 + 1 < 0) widen(cw0 ? *reinterpret_cast<const uint4 *>(cw0 + (4 + k0) * C) : z4, x1);
-      if (k0 + 2 < 0) widen(cw0 ? *reinterpret_cast<const uint4 *>(cw0 + (5 + k0) * C) : z4, x2);
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {  // slide (the raw rows, not the substituted ones)
-      s0[i] = s1[i];
-      s1[i] = s2[i];
-      s2[i] = x3[i];
-    }
-    float2 u[4], ss2 = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float2 acc = __fmul2_rn(w[i][0], x0[i]);
-      acc = __ffma2_rn(w[i][1], x1[i], acc);
-      acc = __ffma2_rn(w[i][2], x2[i], acc);
-      acc = __ffma2_rn(w[i][3], x3[i], acc);
-      u[i] = silu2(acc);
-      ss2 = __ffma2_rn(u[i], u[i], ss2);
-    }
-    float ss = ss2.x + ss2.y;
-#pragma unroll
-    for (int off = 1; off < 16; off <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-    const float f = rsqrtf(ss + d.eps_l2) * scale;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) u[i] = __fmul2_rn(u[i], make_float2(f, f));
-    if (valid) {
-      uint32_t wh[4], wl[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) split2_inrange(u[i].x, u[i].y, wh[i], wl[i]);  // |k^|, |q^| <= 1
-      *reinterpret_cast<uint4 *>(dst) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-      if (blk == 1) *reinterpret_cast<uint4 *>(dst + plane) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-    }
-    dst += rstride;
+    __syncthreads();  // the stage is read: it may take the tile after next
+    if (tid == 0 && tile + 2 * nslots < ntiles) request(tile + 2 * nslots, stage);
+  }
+  // After an early exit no copy may still be landing in shared memory when the
+  // CTA ends: wait (bounded) for every stage use requested.
+  if (tid == 0) {
+    if (issued0 > 0) bar_wait(&full[0], (issued0 - 1) & 1u);
+    if (issued1 > 0) bar_wait(&full[1], (issued1 - 1) & 1u);
   }
 }
 
@@ -1454,9 +1491,21 @@ cudaError_t launch_prefill_qk(const PrefillArgs &a, cudaStream_t s) {
   if (!a.qk_ws) return cudaErrorInvalidValue;
   const long long rows = a.cu_seqlens ? (long long)a.d.T : (long long)a.d.B * a.d.T;
   if (rows <= 0) return cudaSuccess;
-  const long long ctas = (rows + kC - 1) / kC * a.d.Hk;
-  if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
-  prefill_qk_kernel<<<(unsigned)ctas, 256, 0, s>>>(a);
+  if (rows > 0x7fffffffLL - 2 * kC) return cudaErrorInvalidValue;  // token rows in 31 bits
+  CUtensorMap tm_qkv;
+  if (!encode_rows(&tm_qkv, a.qkv_pre, a.d.C, rows, 1, kRawRows)) return cudaErrorInvalidValue;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  // Two resident CTAs per SM, each keeping one key head.
+  const long long ntiles = (rows + kC - 1) / kC;
+  long long nslots = (2LL * sms) / a.d.Hk;
+  if (nslots > ntiles) nslots = ntiles;
+  if (nslots < 1) nslots = 1;
+  e = cudaFuncSetAttribute(prefill_qk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kQkSmem);
+  if (e != cudaSuccess) return e;
+  prefill_qk_kernel<<<(unsigned)(nslots * a.d.Hk), kQkThreads, kQkSmem, s>>>(a, tm_qkv);
   return cudaGetLastError();
 }
 
