@@ -1272,13 +1272,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 // part equal the fused kernel's operands bit for bit.
 // Persistent: a CTA keeps one key head and takes every nslots-th 64-token
 // tile.  A tile's raw q and k rows, with the three before it, arrive by TMA
-// in one of two stages, the next tile's while this one is computed.
+// in one of kQkStages stages, the next tiles' while this one is computed.
 // Half-warps 0-7 take q, 8-15 take k, a run of 8 tokens each, the window
 // sliding over the staged rows; a token within three rows of its sequence's
 // start takes those rows from the carried window (or zeros) instead.
 constexpr int kQkThreads = 256;
-constexpr uint32_t kQkStage = 2 * kRawBlock;            // raw q | k rows of one tile
-constexpr uint32_t kQkSmem = 2 * kQkStage + 64 + 128;   // two stages, two mbarriers, alignment slack
+constexpr int kQkStages = 2;
+constexpr uint32_t kQkStage = 2 * kRawBlock;  // raw q | k rows of one tile
+constexpr uint32_t kQkSmem = kQkStages * kQkStage + 64 + 128;  // stages, mbarriers, alignment slack
 static_assert(kQkStage % 128 == 0, "TMA stage alignment");
 
 __global__ void __launch_bounds__(kQkThreads, 2)
@@ -1286,7 +1287,7 @@ __global__ void __launch_bounds__(kQkThreads, 2)
   extern __shared__ uint8_t qk_smem_raw[];
   uint8_t *sm = qk_smem_raw + ((128 - (smem_u32(qk_smem_raw) & 127)) & 127);
   const uint32_t sbase = smem_u32(sm);
-  uint64_t *full = reinterpret_cast<uint64_t *>(sm + 2 * kQkStage);  // a stage's rows landed
+  uint64_t *full = reinterpret_cast<uint64_t *>(sm + kQkStages * kQkStage);  // a stage's rows landed
   const Dims d = a.d;
   const int kh = (int)(blockIdx.x % (unsigned)d.Hk);
   const int slot = (int)(blockIdx.x / (unsigned)d.Hk), nslots = (int)(gridDim.x / (unsigned)d.Hk);
@@ -1300,25 +1301,19 @@ __global__ void __launch_bounds__(kQkThreads, 2)
   const float scale = blk == 0 ? d.q_scale : 1.0f;
   const bf16 *conv_w = static_cast<const bf16 *>(a.conv_w);
   const bf16 *conv0 = static_cast<const bf16 *>(a.conv0);
-  if (tid == 0) {
-    bar_init(&full[0], 1);
-    bar_init(&full[1], 1);
-  }
+  if (tid == 0)
+    for (int st = 0; st < kQkStages; ++st) bar_init(&full[st], 1);
   __syncthreads();
   // Thread 0: a tile's rows tile*64-3 .. tile*64+63 of this head's q and k
   // channels into a stage (rows outside the tensor read as zeros).
-  uint32_t issued0 = 0u, issued1 = 0u;  // uses of stage 0 and 1 requested (thread 0)
   auto request = [&](int tile, int stage) {
     bar_expect_tx(&full[stage], kQkStage);
     const int row = tile * kC - 3;
     tma_load_3d(sbase + stage * kQkStage, &tm_qkv, kh * kD, row, 0, &full[stage]);
     tma_load_3d(sbase + stage * kQkStage + kRawBlock, &tm_qkv, d.Hk * kD + kh * kD, row, 0, &full[stage]);
-    if (stage) ++issued1; else ++issued0;
   };
-  if (tid == 0) {
-    if (slot < ntiles) request(slot, 0);
-    if (slot + nslots < ntiles) request(slot + nslots, 1);
-  }
+  if (tid == 0)
+    for (int j = 0; j < kQkStages && slot + j * nslots < ntiles; ++j) request(slot + j * nslots, j);
   float2 w[4][4];  // [channel pair][tap]
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -1333,9 +1328,9 @@ __global__ void __launch_bounds__(kQkThreads, 2)
   const long long plane = (long long)rows * rstride;
   int n = 0;
   for (int tile = slot; tile < ntiles; tile += nslots, ++n) {
-    const int stage = n & 1;
+    const int stage = n % kQkStages;
     __syncwarp();
-    const bool got = bar_wait(&full[stage], (uint32_t)(n >> 1) & 1u);
+    const bool got = bar_wait(&full[stage], (uint32_t)(n / kQkStages) & 1u);
     if (__syncthreads_or(!got)) {
       if (tid == 0) atomicOr(a.err, kErrTimeout);
       break;
@@ -1425,15 +1420,15 @@ __global__ void __launch_bounds__(kQkThreads, 2)
       }
       dst += rstride;
     }
-    __syncthreads();  // the stage is read: it may take the tile after next
-    if (tid == 0 && tile + 2 * nslots < ntiles) request(tile + 2 * nslots, stage);
+    __syncthreads();  // the stage is read: it may take the tile kQkStages on
+    if (tid == 0 && tile + kQkStages * nslots < ntiles) request(tile + kQkStages * nslots, stage);
   }
   // After an early exit no copy may still be landing in shared memory when the
-  // CTA ends: wait (bounded) for every stage use requested.
-  if (tid == 0) {
-    if (issued0 > 0) bar_wait(&full[0], (issued0 - 1) & 1u);
-    if (issued1 > 0) bar_wait(&full[1], (issued1 - 1) & 1u);
-  }
+  // CTA ends: wait (bounded) for the requests of the tiles not consumed (on a
+  // normal exit there are none).
+  if (tid == 0)
+    for (int j = n; j < n + kQkStages; ++j)
+      if (slot + j * nslots < ntiles) bar_wait(&full[j % kQkStages], (uint32_t)(j / kQkStages) & 1u);
 }
 
 // The staged q^ / k^ of qk_ws as a 3-d map {Hk*128 columns, rows, 3 tensors}
