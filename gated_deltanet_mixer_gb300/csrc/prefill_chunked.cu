@@ -313,7 +313,7 @@ __device__ __forceinline__ void st_h8_split_pairs(uint8_t *phi, uint8_t *plo, co
 // group per lane, sliding the conv window over the tokens; the L2 norm sums
 // over the 16 lanes of a half-warp, which hold one token's 128 channels.
 // Writes: q^ and k^ (fp16) into [K;Q]; Gamma k^ (hi, lo); v (hi, lo).
-template <int NTOK, int UNROLL = 4>
+template <int NTOK>
 __device__ __forceinline__ void fe_pass(uint8_t *sm, const ChunkVecs &V, const Dims &d, const bf16 *conv_w, int blk,
                                         long long c, int r0, int t0, int T, int grp) {
   const bool has_norm = blk < 2, has_single = blk < 2, has_split = blk > 0, has_gamma = blk == 1;
@@ -335,7 +335,7 @@ __device__ __forceinline__ void fe_pass(uint8_t *sm, const ChunkVecs &V, const D
   widen(*reinterpret_cast<const uint4 *>(raw + 256 * (r0 + 0)), x0);
   widen(*reinterpret_cast<const uint4 *>(raw + 256 * (r0 + 1)), x1);
   widen(*reinterpret_cast<const uint4 *>(raw + 256 * (r0 + 2)), x2);
-#pragma unroll UNROLL
+#pragma unroll 4
   for (int tt = 0; tt < NTOK; ++tt) {
     const int row = r0 + tt;  // token index within the chunk
     const int t = t0 + row;
@@ -397,20 +397,12 @@ __device__ void front_end(uint8_t *sm, const ChunkVecs &V, const Dims &d, const 
     fe_pass<7>(sm, V, d, conv_w, 0, cq, 7 * (2 * (warp - 8) + (lane >> 4)), t0, T, grp);
   }
 }
-// The v tiles of the chunk starting at t0 (warps 8-11, 8 tokens per
-// half-warp): all of them (part 0), or the first 2 (part 1) or last 6 (part 2)
-// tokens of each half-warp's run.
+// The v tiles of the chunk starting at t0 (warps 8-11, 8 tokens per half-warp).
 __device__ void front_end_v(uint8_t *sm, const ChunkVecs &V, const Dims &d, const bf16 *conv_w, int h, int t0,
-                            int T, int tid, int part) {
+                            int T, int tid) {
   const int warp = tid >> 5, lane = tid & 31, grp = lane & 15;
-  const long long c = 2LL * d.Hk * kD + (long long)h * kD + 8 * grp;
-  const int r0 = 8 * (2 * (warp - 8) + (lane >> 4));
-  if (part == 0)
-    fe_pass<8>(sm, V, d, conv_w, 2, c, r0, t0, T, grp);
-  else if (part == 1)
-    fe_pass<2, 2>(sm, V, d, conv_w, 2, c, r0, t0, T, grp);
-  else
-    fe_pass<6, 6>(sm, V, d, conv_w, 2, c, r0 + 2, t0, T, grp);
+  fe_pass<8>(sm, V, d, conv_w, 2, 2LL * d.Hk * kD + (long long)h * kD + 8 * grp, 8 * (2 * (warp - 8) + (lane >> 4)),
+             t0, T, grp);
 }
 
 // A, staged path: Gamma k^ for the chunk from k^'s fp16 hi part (in [K;Q])
@@ -976,16 +968,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int q = 0; q < 4; ++q) st_h8_inrange(sm + OFF_M + kmaj(i, j0 + 8 * q, kC), v + 8 * q);  // |M| <= q_scale
       }
+      __syncwarp();
+      named_sync(kBarSolve, kTmemWarps * 32);  // L written: the solve may read it (warps 8-11 go on)
     }
-    __syncthreads();
     // D: the triangular inverse, scaled copies T B and T B D (warps 0-7);
-    // meanwhile warps 8-11 make this chunk's v tiles from its staged rows, all
-    // of them for the first chunk, else those not made in the previous
-    // epilogue (the raw v rows do not share space with the solve's scratch).
+    // warps 8-11 make this chunk's v tiles from its staged rows meanwhile,
+    // from the end of B on (the V tiles were last read by MMA2 of the previous
+    // chunk; the raw v rows do not share space with the solve's scratch).
     if (warp < kTmemWarps)
       solve_T(sm, CV, tid);
     else
-      front_end_v(sm, CV, d, conv_w, h, t0, T, tid, n == 0 ? 0 : 2);
+      front_end_v(sm, CV, d, conv_w, h, t0, T, tid);
     smem_ready();
     // E: MMA2 U^T = V^T (T B)^T, hi*hi + lo*hi + hi*lo; MMA3 -W^T = K^T (-T B D)^T
     // (K^ read from [K;Q] as an MN-major operand).  The raw rows are free now:
@@ -1219,18 +1212,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if (lane == 0) {
         atomicOr(a.err, kErrTimeout);
         V.abort = 1;
-      }
-      // The first tokens of the next chunk's v tiles (the V tiles were last
-      // read by MMA2, complete since G), once its raw rows have landed.
-      if (n + 1 < nchunks) {
-        __syncwarp();
-        const bool got = bar_wait(&V.bar_raw, phase_raw);
-        if (__all_sync(0xffffffffu, got)) {
-          front_end_v(sm, V.cv[(n + 1) & 1], d, conv_w, h, t0 + kC, T, tid, 1);
-        } else if (lane == 0) {
-          atomicOr(a.err, kErrTimeout);
-          V.abort = 1;
-        }
       }
     }
     ph_sq ^= 1u;
