@@ -45,10 +45,11 @@
 //   G  MMA4  Delta^T = U^T - S W^T
 //   H  Delta^T (hi, lo) to TMEM
 //   I  MMA6  Delta^T M^T;            MMA7  S += Delta^T (Gamma K) (split)
-//   J  O = d (S Q^T) + Delta^T M^T, gated RMSNorm (node gdn.norm) -> o on
-//      warps 0-7; on warps 8-11, once MMA7 is done, S -> fp16 copy, rescaled
-//      for the next chunk (or S_T after the last); then the next chunk's z
-//      rows are requested
+//   J  O = d (S Q^T) + Delta^T M^T (warps 0-7) and the gated RMSNorm (node
+//      gdn.norm) -> o, tokens 0-47 on warps 0-7 and 48-63 on warps 8-11,
+//      which first, once MMA7 is done, pass S on (fp16 copy and rescaled
+//      state for the next chunk, or S_T after the last); then the next
+//      chunk's z rows are requested
 // Each MMA group commits to its own mbarrier, so a phase waits only for the
 // products it reads (C for K K^T, F for W^T, J for O) while the rest of the
 // chain (S Q^T, U^T, the state update) keeps the tensor pipe busy.
@@ -74,6 +75,7 @@ constexpr int kBarMma6 = 2;  // warp 0 (MMA6 issued) -> warp 11 (may issue MMA7)
 constexpr int kBarMma3 = 3;  // warp 0 (MMA3 issued) -> warp 11 (may issue MMA2)
 constexpr int kBarSolve = 4;  // warps 0-7 in the solve
 constexpr int kBarEpi = 5;    // warps 8-11 in the epilogue (the next chunk's decay formed)
+constexpr int kBarJ1 = 6;     // warps 0-7 (O staged) -> warps 8-11 (may read it)
 
 __device__ __forceinline__ void named_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -613,6 +615,50 @@ __device__ void solve_T(uint8_t *sm, const ChunkVecs &V, int tid) {
   }
 }
 
+// J: the gated RMSNorm (node gdn.norm) of NR tokens i0, i0 + di, ... of the
+// chunk, one half-warp per token (8 channels per lane), from the O staging
+// and the staged z rows, to o.
+template <int NR>
+__device__ __forceinline__ void gated_norm(const uint8_t *sm, const bf16 *norm_w, bf16 *o, const Dims &d,
+                                           long long bos, int h, int t0, int T, int i0, int di, int lane) {
+  const float *ost = reinterpret_cast<const float *>(sm + OFF_OST);
+  const int hl = lane & 15;
+  float2 wn[4];
+  widen(*reinterpret_cast<const uint4 *>(norm_w + 8 * hl), wn);
+  const int nv = min(kC, T - t0);
+  bf16 *ob = o + ((bos + t0) * d.Hv + h) * kD + 8 * hl;
+  const long long ostride = (long long)d.Hv * kD;
+#pragma unroll
+  for (int m = 0; m < NR; ++m) {
+    const int i = i0 + di * m;
+    const bool valid = i < nv;
+    float4 o0 = make_float4(0.f, 0.f, 0.f, 0.f), o1 = o0;
+    uint4 zr = make_uint4(0u, 0u, 0u, 0u);
+    if (valid) {
+      o0 = ld4(ost + i * kD + 8 * hl);
+      o1 = ld4(ost + i * kD + 8 * hl + 4);
+      zr = *reinterpret_cast<const uint4 *>(sm + OFF_Z + i * kD * 2 + 16 * hl);
+    }
+    float ss = dot4(o0, o0) + dot4(o1, o1);
+#pragma unroll
+    for (int off = 1; off < 16; off <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    const float rstd = rsqrtf(ss * (1.0f / kD) + d.eps_norm);
+    float2 zz[4];
+    widen(zr, zz);
+    const float2 op[4] = {make_float2(o0.x, o0.y), make_float2(o0.z, o0.w), make_float2(o1.x, o1.y),
+                          make_float2(o1.z, o1.w)};
+    uint32_t yw[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 sg = silu2(zz[q]);
+      const float2 y = __fmul2_rn(__fmul2_rn(wn[q], __fmul2_rn(op[q], make_float2(rstd, rstd))), sg);
+      __nv_bfloat162 t = __floats2bfloat162_rn(y.x, y.y);
+      yw[q] = *reinterpret_cast<uint32_t *>(&t);
+    }
+    if (valid) *reinterpret_cast<uint4 *>(ob + i * ostride) = make_uint4(yw[0], yw[1], yw[2], yw[3]);
+  }
+}
+
 // K steps of one MMA family; descriptors built by the caller's lambdas.
 template <typename FA, typename FB>
 __device__ __forceinline__ void issue(uint32_t d, uint32_t id, int nk, bool accumulate_first, FA da, FB db) {
@@ -1052,7 +1098,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     smem_ready();
     // The epilogue.  Warps 0-7 (TMEM) form and store the output and sync
     // among themselves (named barrier 1); warps 8-11 meanwhile issue the state
-    // update and pass the state on.  Everyone meets at the end of the chunk.
+    // update, pass the state on and take the last 16 tokens of the gated norm.
+    // Everyone meets at the end of the chunk.
     if (warp < kTmemWarps) {
       bool ok = true;
       // I: MMA6 Delta^T M^T (warp 0); then warp 11 may issue MMA7 behind it
@@ -1093,49 +1140,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       }
+      __syncwarp();
+      named_arrive(kBarJ1, kThreads);  // the O staging is written
       ok = wait_tmem(&V.bar_z, phase_z) && ok;
       z_pending = false;
       if (ok) {
-      // J2: gated RMSNorm per token, one half-warp per token (8 channels per
-      // lane, warps 0-7), z from the staged rows
-      {
-        const float *ost = reinterpret_cast<const float *>(sm + OFF_OST);
-        const int hl = lane & 15;
-        float2 wn[4];
-        widen(*reinterpret_cast<const uint4 *>(static_cast<const bf16 *>(a.norm_w) + 8 * hl), wn);
-        const int nv = min(kC, T - t0);
-        bf16 *ob = static_cast<bf16 *>(a.o) + ((bos + t0) * d.Hv + h) * kD + 8 * hl;
-        const long long ostride = (long long)d.Hv * kD;
-  #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          const int i = 2 * warp + (lane >> 4) + 16 * m;  // 16 tokens per round (warps 0-7)
-          const bool valid = i < nv;
-          float4 o0 = make_float4(0.f, 0.f, 0.f, 0.f), o1 = o0;
-          uint4 zr = make_uint4(0u, 0u, 0u, 0u);
-          if (valid) {
-            o0 = ld4(ost + i * kD + 8 * hl);
-            o1 = ld4(ost + i * kD + 8 * hl + 4);
-            zr = *reinterpret_cast<const uint4 *>(sm + OFF_Z + i * kD * 2 + 16 * hl);
-          }
-          float ss = dot4(o0, o0) + dot4(o1, o1);
-  #pragma unroll
-          for (int off = 1; off < 16; off <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-          const float rstd = rsqrtf(ss * (1.0f / kD) + d.eps_norm);
-          float2 zz[4];
-          widen(zr, zz);
-          const float2 op[4] = {make_float2(o0.x, o0.y), make_float2(o0.z, o0.w), make_float2(o1.x, o1.y),
-                                make_float2(o1.z, o1.w)};
-          uint32_t yw[4];
-  #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float2 sg = silu2(zz[q]);
-            const float2 y = __fmul2_rn(__fmul2_rn(wn[q], __fmul2_rn(op[q], make_float2(rstd, rstd))), sg);
-            __nv_bfloat162 t = __floats2bfloat162_rn(y.x, y.y);
-            yw[q] = *reinterpret_cast<uint32_t *>(&t);
-          }
-          if (valid) *reinterpret_cast<uint4 *>(ob + i * ostride) = make_uint4(yw[0], yw[1], yw[2], yw[3]);
-        }
-      }
+      // J2: gated RMSNorm of tokens 0-47 (warps 0-7; 48-63 on warps 8-11)
+      gated_norm<3>(sm, static_cast<const bf16 *>(a.norm_w), static_cast<bf16 *>(a.o), d, bos, h, t0, T,
+                    2 * warp + (lane >> 4), 16, lane);
       }
       ph_s ^= 1u;
     } else {
@@ -1159,7 +1171,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       ph_o ^= 1u;
-      phase_z ^= 1u;
       // J3 (warps 8-11, all 128 state columns each, alongside J2 on warps
       // 0-7): S -> fp16 copy and rescaled state (or S_T after the last
       // chunk), in TMEM
@@ -1209,6 +1220,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_st();
           }
         }
+      } else if (lane == 0) {
+        atomicOr(a.err, kErrTimeout);
+        V.abort = 1;
+      }
+      // J2 of tokens 48-63, once warps 0-7 have staged O and the z rows landed
+      __syncwarp();
+      named_sync(kBarJ1, kThreads);
+      const bool zok = bar_wait(&V.bar_z, phase_z);
+      phase_z ^= 1u;
+      if (__all_sync(0xffffffffu, zok)) {
+        gated_norm<2>(sm, static_cast<const bf16 *>(a.norm_w), static_cast<bf16 *>(a.o), d, bos, h, t0, T,
+                      48 + 2 * (warp - 8) + (lane >> 4), 8, lane);
       } else if (lane == 0) {
         atomicOr(a.err, kErrTimeout);
         V.abort = 1;
