@@ -868,7 +868,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t id_km128 = idesc(128, 128, 0, 1);
 
   // All threads: wait on an mbarrier phase; a uniform decision to abort.
-  auto wait_all = [&](uint64_t *bar, uint32_t &ph) -> bool {
+  // ok_in: an earlier wait of this thread that is voted on here too.
+  auto wait_all = [&](uint64_t *bar, uint32_t &ph, bool ok_in = true) -> bool {
     // Reconverge first: lane 0 of warp 0 issues the MMAs and TMA copies, and
     // while its 31 sibling lanes sat in the polling loop (each try_wait may
     // suspend the warp for a while) that lane lost about a microsecond.
@@ -876,7 +877,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = bar_wait(bar, ph);
     ph ^= 1u;
     fence_after();
-    const int bad = __syncthreads_or(!ok);
+    const int bad = __syncthreads_or(!(ok && ok_in));
     if (bad && tid == 0) {
       atomicOr(a.err, kErrTimeout);
       V.abort = 1;
@@ -909,25 +910,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // A0: chunk vectors; the next chunk's g and beta requested
     ChunkVecs &CV = V.cv[n & 1];  // formed before the loop or during the previous chunk's epilogue
     if (warp == 11 && n + 1 < nchunks) load_gb<kRawGates>(a.gate, bos, d.Hv, h, t0 + kC, T, lane, g_nxt, b_nxt);
-    // This chunk's staged rows (and q^, k^ hi in [K;Q]): one thread waits, the
-    // rest meet it.
-    if (tid == 0) {
-      bool ok = bar_wait(&V.bar_raw, phase_raw);
-      if (kStagedQK) ok = bar_wait(&V.bar_kq, phase_kq) && ok;
-      if (!ok) {
-        atomicOr(a.err, kErrTimeout);
-        V.abort = 1;
-      }
-    }
+    // This chunk's staged rows (and q^, k^ hi in [K;Q]): every warp waits for
+    // them itself (the previous chunk ended on a barrier); a timeout is voted
+    // on at the barrier after the first MMA.
+    __syncwarp();
+    bool start_ok = bar_wait(&V.bar_raw, phase_raw);
+    if (kStagedQK) start_ok = bar_wait(&V.bar_kq, phase_kq) && start_ok;
     phase_raw ^= 1u;
     raw_pending = false;
     if (kStagedQK) {
       phase_kq ^= 1u;
       kq_pending = false;
     }
-    fence_after();
-    __syncthreads();
-    if (V.abort) break;
     if (n == 0) {  // rows before the first token: the carried window, or zeros
       for (int idx = kStagedQK ? 2 * 48 + tid : tid; idx < 3 * 3 * 16; idx += kThreads) {
         const int blk = idx / 48, rw = (idx / 16) % 3, g8 = idx % 16;
@@ -957,7 +951,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       smem_ready();
       if (warp == 0) issue_mma1();
     }
-    if (!wait_all(&V.bar_qk, ph_qk)) break;
+    if (!wait_all(&V.bar_qk, ph_qk, start_ok)) break;
     // MMA5 S Q^T (Q^ = rows 64..127 of [K;Q], S from TMEM), needed only in J
     if (warp == 11) {
       fence_after();
