@@ -101,8 +101,9 @@ constexpr uint32_t kRawBlock = kRawRows * kD * 2;  // one of q | k | v, bytes (1
 constexpr uint32_t OFF_KQ = 0;          // [K;Q] K-major, 128 rows x 128       32 KB
 constexpr uint32_t OFF_VH = 32768;      // V hi      MN-major [j][v]           16 KB
 constexpr uint32_t OFF_VL = 49152;      // V lo                                16 KB
-constexpr uint32_t OFF_GK = 65536;      // Gamma K hi  MN-major [j][k]         16 KB
-constexpr uint32_t OFF_GKL = 81920;     // Gamma K lo                          16 KB
+constexpr uint32_t OFF_GK = 65536;      // Gamma K hi  MN-major [j][k]         16 KB (fused path)
+constexpr uint32_t OFF_GKL = 81920;     // Gamma K lo                          16 KB (fused path)
+constexpr uint32_t OFF_KQ2 = OFF_GK;    // staged path: the second [K;Q] buffer  32 KB
 constexpr uint32_t OFF_TU = 98304;      // T diag(beta)      K-major [i][j]     8 KB
 constexpr uint32_t OFF_TW = 106496;     // -T diag(beta d)   K-major [i][j]     8 KB
 constexpr uint32_t OFF_M = 114688;      // M         K-major [i][j]             8 KB
@@ -114,16 +115,18 @@ constexpr uint32_t OFF_VEC = OFF_Z + kC * kD * 2;     // per-token vectors, flag
 // Scratch that lives only between two uses of the tiles it overlays:
 constexpr int kLs = 68;                              // padded row stride of L (floats)
 constexpr uint32_t OFF_L = OFF_RAW;                  // L fp32 [64][68], phases C-D
-constexpr uint32_t OFF_PB = OFF_RAW + 64 * kLs * 4;  // block products fp32 [32][32], phase D
 constexpr uint32_t OFF_TF = OFF_NW;                  // T fp32 [64][64], phase D
 constexpr uint32_t OFF_OST = OFF_M;                  // O^T staging fp32 [64][128] (M, NW, TUL), phase J
-constexpr uint32_t OFF_KLO = OFF_RAW;                // staged path: k^ lo, K-major [64][128] fp16, phase A
-static_assert(OFF_KLO % 1024 == 0 && kC * kD * 2 <= 2 * kRawBlock, "k^ lo fills the q and k row blocks");
+// staged path: k^ lo, K-major [64][128] fp16, from before MMA7 of the previous
+// chunk completes to MMA7 of this one: beside L in the q and k row blocks
+constexpr uint32_t OFF_KLO = OFF_L + 64 * kLs * 4;
+static_assert(OFF_KLO % 1024 == 0 && OFF_KLO + kC * kD * 2 <= OFF_RAW + 2 * kRawBlock, "L and k^ lo share the q and k row blocks");
+static_assert(OFF_KQ2 % 1024 == 0 && OFF_GKL == OFF_GK + 16384, "the second [K;Q] buffer spans Gamma K hi and lo");
 static_assert(OFF_NW == OFF_M + 8192 && OFF_TUL == OFF_NW + 16384, "the staging spans M, NW and TUL");
 constexpr uint32_t kVecBytes = 3584;
-constexpr uint32_t kSmemUsed = OFF_VEC + kVecBytes;
+constexpr uint32_t OFF_PB = OFF_VEC + kVecBytes;  // block products fp32 [32][32], phase D
+constexpr uint32_t kSmemUsed = OFF_PB + 32 * 32 * 4;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // + alignment slack
-static_assert(OFF_PB + 32 * 32 * 4 <= OFF_Z, "solve scratch fits in the raw rows");
 static_assert(OFF_RAW % 128 == 0 && OFF_Z % 128 == 0 && kRawBlock % 128 == 0, "TMA destinations");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
@@ -161,7 +164,8 @@ struct __align__(16) Vecs {  // shared-memory scalars, vectors and barriers
   uint64_t bar_end;  // every MMA of both issuers, before TMEM is freed
   uint64_t bar_raw;  // raw rows landed
   uint64_t bar_z;    // z rows landed
-  uint64_t bar_kq;   // staged q^ and k^ hi landed in [K;Q] (staged path)
+  uint64_t bar_kq[2];  // staged path: q^ and k^ hi landed in [K;Q] buffer 0 / 1
+  uint64_t bar_klo;    // staged path: k^ lo landed
 };
 static_assert(sizeof(Vecs) <= kVecBytes, "vector area");
 
@@ -405,33 +409,6 @@ __device__ void front_end_v(uint8_t *sm, const ChunkVecs &V, const Dims &d, cons
   const int warp = tid >> 5, lane = tid & 31, grp = lane & 15;
   fe_pass<8>(sm, V, d, conv_w, 2, 2LL * d.Hk * kD + (long long)h * kD + 8 * grp, 8 * (2 * (warp - 8) + (lane >> 4)),
              t0, T, grp);
-}
-
-// A, staged path: Gamma k^ for the chunk from k^'s fp16 hi part (in [K;Q])
-// and lo part (staged), as the fp16 hi/lo tiles the state update reads.
-// Items (token j, 8-channel group g) are spread over `nthreads` threads.
-__device__ __forceinline__ void gamma_k_pass(uint8_t *sm, const ChunkVecs &V, int i0, int nthreads) {
-  for (int q = i0; q < kC * 16; q += nthreads) {
-    const int j = q >> 4, g = q & 15;
-    const uint4 hi = *reinterpret_cast<const uint4 *>(sm + OFF_KQ + kmaj(j, 8 * g, 128));
-    const uint4 lo = *reinterpret_cast<const uint4 *>(sm + OFF_KLO + kmaj(j, 8 * g, kC));
-    const float gm = V.gam[j];
-    const uint32_t hw[4] = {hi.x, hi.y, hi.z, hi.w}, lw[4] = {lo.x, lo.y, lo.z, lo.w};
-    float2 u[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 kh = __half22float2(*reinterpret_cast<const __half2 *>(&hw[i]));
-      const float2 kl = __half22float2(*reinterpret_cast<const __half2 *>(&lw[i]));
-      u[i] = __fmul2_rn(__fadd2_rn(kh, kl), make_float2(gm, gm));
-    }
-    const uint32_t o = mnmaj(8 * g, j, kC);
-    st_h8_split_pairs<false>(sm + OFF_GK + o, sm + OFF_GKL + o, u);  // |Gamma k^| <= 1
-  }
-}
-// A, staged path: q^ and k^ arrived by TMA, so the front end is the Gamma k^
-// pass (warps 1-11: warp 0 issues the first MMA meanwhile).
-__device__ void front_end_staged(uint8_t *sm, const ChunkVecs &V, int tid) {
-  if (tid >= 32) gamma_k_pass(sm, V, tid - 32, kThreads - 32);
 }
 
 // T scratch: fp32 [64][64], float4 groups XOR-swizzled by row, so that reads of
@@ -727,14 +704,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = smem_u32(sm);
   const int cq = kh * kD, ck = d.Hk * kD + kh * kD, cv = 2 * d.Hk * kD + h * kD;
 
-  // One thread: the raw rows t0-3 .. t0+63 of q, k, v; in the staged path
-  // the raw v rows and k^ lo of tokens t0 .. t0+63 (two 64-column boxes).
+  // One thread: the raw rows t0-3 .. t0+63 of q, k, v (staged path: of v).
   auto request_raw = [&](int t0) {
     const int row = (int)(bos + t0 - 3);
     if (kStagedQK) {
-      bar_expect_tx(&V.bar_raw, kRawBlock + kC * kD * 2);
-      tma_load_3d(sbase + OFF_KLO, &tm_qk, kh * kD, (int)(bos + t0), 2, &V.bar_raw);
-      tma_load_3d(sbase + OFF_KLO + kC * 128, &tm_qk, kh * kD + 64, (int)(bos + t0), 2, &V.bar_raw);
+      bar_expect_tx(&V.bar_raw, kRawBlock);
     } else {
       bar_expect_tx(&V.bar_raw, 3 * kRawBlock);
       tma_load_3d(sbase + OFF_RAW + 0 * kRawBlock, &tm_qkv, cq, row, 0, &V.bar_raw);
@@ -743,14 +717,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_load_3d(sbase + OFF_RAW + 2 * kRawBlock, &tm_qkv, cv, row, 0, &V.bar_raw);
   };
   // Staged path, one thread: q^ (rows 64..127) and k^ hi (rows 0..63) of tokens
-  // t0 .. t0+63 straight into the [K;Q] tile, two 64-column boxes each.
-  auto request_kq = [&](int t0) {
-    bar_expect_tx(&V.bar_kq, 2 * kC * kD * 2);
+  // t0 .. t0+63 straight into [K;Q] buffer `buf`, two 64-column boxes each.
+  auto request_kq = [&](int t0, int buf) {
+    const uint32_t kqb = sbase + (buf ? OFF_KQ2 : OFF_KQ);
+    bar_expect_tx(&V.bar_kq[buf], 2 * kC * kD * 2);
 #pragma unroll
     for (int at = 0; at < 2; ++at) {
-      tma_load_3d(sbase + OFF_KQ + at * 16384 + 64 * 128, &tm_qk, kh * kD + 64 * at, (int)(bos + t0), 0, &V.bar_kq);
-      tma_load_3d(sbase + OFF_KQ + at * 16384, &tm_qk, kh * kD + 64 * at, (int)(bos + t0), 1, &V.bar_kq);
+      tma_load_3d(kqb + at * 16384 + 64 * 128, &tm_qk, kh * kD + 64 * at, (int)(bos + t0), 0, &V.bar_kq[buf]);
+      tma_load_3d(kqb + at * 16384, &tm_qk, kh * kD + 64 * at, (int)(bos + t0), 1, &V.bar_kq[buf]);
     }
+  };
+  // Staged path, one thread: k^ lo of tokens t0 .. t0+63 (two 64-column boxes).
+  auto request_klo = [&](int t0) {
+    bar_expect_tx(&V.bar_klo, kC * kD * 2);
+    tma_load_3d(sbase + OFF_KLO, &tm_qk, kh * kD, (int)(bos + t0), 2, &V.bar_klo);
+    tma_load_3d(sbase + OFF_KLO + kC * 128, &tm_qk, kh * kD + 64, (int)(bos + t0), 2, &V.bar_klo);
   };
   auto request_z = [&](int t0) {  // one thread: the z rows t0 .. t0+63 of head h
     bar_expect_tx(&V.bar_z, kC * kD * 2);
@@ -793,7 +774,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bar_init(&V.bar_end, 2);
     bar_init(&V.bar_raw, 1);
     bar_init(&V.bar_z, 1);
-    bar_init(&V.bar_kq, 1);
+    bar_init(&V.bar_kq[0], 1);
+    bar_init(&V.bar_kq[1], 1);
+    bar_init(&V.bar_klo, 1);
     V.abort = 0;
   }
   if (warp == 0) tmem_alloc(&V.tmem, kTmemCols);
@@ -815,9 +798,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   fence_after();
   if (tid == 0) {
     request_raw(0);
-    if (kStagedQK) request_kq(0);
+    if (kStagedQK) {
+      request_kq(0, 0);
+      if (T > kC) request_kq(kC, 1);
+      request_klo(0);
+    }
     request_z(0);
   }
+  // Staged path: [K;Q] buffer and k^ lo copies requested and consumed so far
+  // (chunk n reads buffer n & 1, its (n >> 1)-th use; k^ lo's n-th use).
+  int kq_next = kStagedQK ? (T > kC ? 2 : 1) : 0, kq_used = 0;
+  int klo_next = kStagedQK ? 1 : 0, klo_used = 0;
   const uint32_t tmem = V.tmem;
   // TMEM lane quadrant and column half of this warp for the 32x32b accesses.
   const int quad = warp & 3, half = warp >> 2;
@@ -852,15 +843,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // Each mbarrier completes once per chunk; its phase bit is tracked here.
-  uint32_t ph_qk = 0, ph_w = 0, ph_d = 0, ph_o = 0, ph_s = 0, ph_sq = 0, ph_u = 0, phase_raw = 0, phase_z = 0,
-           phase_kq = 0;
+  uint32_t ph_qk = 0, ph_w = 0, ph_d = 0, ph_o = 0, ph_s = 0, ph_sq = 0, ph_u = 0, phase_raw = 0, phase_z = 0;
   // MMAs off the critical path are issued by warp 11 (its lane 0), idle in the
   // phases where it issues them; the critical ones by warp 0 (thread 0).  A
   // whole converged warp runs the issue code.  Warp 10 (lane 0) requests the
   // raw rows and the staged q^ / k^ of the next chunk.
   const bool issuer2 = tid == kThreads - 32;
   const bool loader = tid == kThreads - 64;
-  bool raw_pending = true, z_pending = true, kq_pending = kStagedQK;  // a requested TMA not yet consumed
+  bool raw_pending = true, z_pending = true;  // a requested TMA not yet consumed
   const int nchunks = (T + kC - 1) / kC;
   const uint32_t id_kk = idesc(128, 64, 0, 0);
   const uint32_t id_mk = idesc(128, 64, 1, 0);
@@ -910,54 +900,73 @@ __global__ void __launch_bounds__(kThreads, 1)
     // A0: chunk vectors; the next chunk's g and beta requested
     ChunkVecs &CV = V.cv[n & 1];  // formed before the loop or during the previous chunk's epilogue
     if (warp == 11 && n + 1 < nchunks) load_gb<kRawGates>(a.gate, bos, d.Hv, h, t0 + kC, T, lane, g_nxt, b_nxt);
-    // This chunk's staged rows (and q^, k^ hi in [K;Q]): every warp waits for
-    // them itself (the previous chunk ended on a barrier); a timeout is voted
-    // on at the barrier after the first MMA.
+    // This chunk's staged rows (fused path: every warp; staged path: warps
+    // 8-11, which read only the v rows, while warp 0 waits for q^ and k^ hi
+    // in [K;Q]): each warp waits itself (the previous chunk ended on a
+    // barrier); a timeout is voted on at the next barrier.
+    const uint32_t kqb = sbase + ((kStagedQK && (n & 1)) ? OFF_KQ2 : OFF_KQ);  // this chunk's [K;Q]
+    bool start_ok = true;
     __syncwarp();
-    bool start_ok = bar_wait(&V.bar_raw, phase_raw);
-    if (kStagedQK) start_ok = bar_wait(&V.bar_kq, phase_kq) && start_ok;
+    if (!kStagedQK || warp >= kTmemWarps) start_ok = bar_wait(&V.bar_raw, phase_raw);
+    if (kStagedQK && warp == 0) start_ok = bar_wait(&V.bar_kq[n & 1], (uint32_t)(n >> 1) & 1u);
     phase_raw ^= 1u;
     raw_pending = false;
     if (kStagedQK) {
-      phase_kq ^= 1u;
-      kq_pending = false;
+      ++kq_used;
+      // the other buffer's last readers (the previous chunk's MMAs) are done:
+      // the next chunk's q^ and k^ may land there
+      if (n >= 1 && n + 1 < nchunks) {
+        if (loader) request_kq(t0 + kC, (n + 1) & 1);
+        ++kq_next;
+      }
+      if (!start_ok) {  // no barrier votes here: the abort flag is read after F
+        atomicOr(a.err, kErrTimeout);
+        V.abort = 1;
+      }
     }
     if (n == 0) {  // rows before the first token: the carried window, or zeros
-      for (int idx = kStagedQK ? 2 * 48 + tid : tid; idx < 3 * 3 * 16; idx += kThreads) {
-        const int blk = idx / 48, rw = (idx / 16) % 3, g8 = idx % 16;
-        const int cc = blk == 0 ? cq : blk == 1 ? ck : cv;
-        *reinterpret_cast<uint4 *>(sm + OFF_RAW + blk * kRawBlock + 256 * rw + 16 * g8) =
-            conv0 ? *reinterpret_cast<const uint4 *>(conv0 + (long long)rw * C + cc + 8 * g8)
-                  : make_uint4(0u, 0u, 0u, 0u);
+      if (!kStagedQK || warp >= kTmemWarps) {  // staged path: the v rows, by warps 8-11 (they waited)
+        const int i0 = kStagedQK ? 2 * 48 + tid - kTmemWarps * 32 : tid;
+        const int nth = kStagedQK ? kThreads - kTmemWarps * 32 : kThreads;
+        for (int idx = i0; idx < 3 * 3 * 16; idx += nth) {
+          const int blk = idx / 48, rw = (idx / 16) % 3, g8 = idx % 16;
+          const int cc = blk == 0 ? cq : blk == 1 ? ck : cv;
+          *reinterpret_cast<uint4 *>(sm + OFF_RAW + blk * kRawBlock + 256 * rw + 16 * g8) =
+              conv0 ? *reinterpret_cast<const uint4 *>(conv0 + (long long)rw * C + cc + 8 * g8)
+                    : make_uint4(0u, 0u, 0u, 0u);
+        }
       }
       __syncthreads();
     }
     auto issue_mma1 = [&]() {  // B: MMA1  [K;Q] K^T (warp 0)
       __syncwarp();
       fence_after();
-      issue_w(tmem + TM_KQ, id_kk, 8, false, [&](int ks) { return desc_k(sbase + OFF_KQ, ks, 128); },
-              [&](int ks) { return desc_k(sbase + OFF_KQ, ks, 128); });
+      issue_w(tmem + TM_KQ, id_kk, 8, false, [&](int ks) { return desc_k(kqb, ks, 128); },
+              [&](int ks) { return desc_k(kqb, ks, 128); });
       commit_w(&V.bar_qk);
     };
+    // MMA5 S Q^T (Q^ = rows 64..127 of [K;Q], S from TMEM), needed only in J
+    auto issue_mma5 = [&]() {
+      fence_after();
+      issue_ta_w(tmem + TM_O1, tmem + TM_S16, id_kk, 8, false, [&](int ks) { return desc_k(kqb + 64 * 128, ks, 128); });
+      commit_w(&V.bar_sq);
+    };
     if (kStagedQK) {
-      // [K;Q] arrived by TMA: MMA1 goes first, and the front end (the Gamma k^
-      // pass, read only by MMA7; for the first chunk also the v tiles) runs
-      // while it executes.
-      if (warp == 0) issue_mma1();
-      front_end_staged(sm, CV, tid);
+      // [K;Q] arrived by TMA: warp 0 issues MMA1 and MMA5 behind it; warps
+      // 0-7 wait for MMA1 alone, warps 8-11 go on to the v tiles.
+      if (warp == 0) {
+        issue_mma1();
+        issue_mma5();
+      }
+      if (warp < kTmemWarps) wait_tmem(&V.bar_qk, ph_qk);  // a timeout sets the abort flag, read after F
+      else ph_qk ^= 1u;
     } else {
       // A: front end
       front_end(sm, CV, d, conv_w, kh, t0, T, tid);
       smem_ready();
       if (warp == 0) issue_mma1();
-    }
-    if (!wait_all(&V.bar_qk, ph_qk, start_ok)) break;
-    // MMA5 S Q^T (Q^ = rows 64..127 of [K;Q], S from TMEM), needed only in J
-    if (warp == 11) {
-      fence_after();
-      issue_ta_w(tmem + TM_O1, tmem + TM_S16, id_kk, 8, false,
-                 [&](int ks) { return desc_k(sbase + OFF_KQ + 64 * 128, ks, 128); });
-      commit_w(&V.bar_sq);
+      if (!wait_all(&V.bar_qk, ph_qk, start_ok)) break;
+      if (warp == 11) issue_mma5();
     }
     // C: L (fp32, strictly lower, decayed beta K K^T) and M (fp16, decayed Q K^T incl. diagonal)
     if (warp < kTmemWarps) {
@@ -1022,17 +1031,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     smem_ready();
     // E: MMA2 U^T = V^T (T B)^T, hi*hi + lo*hi + hi*lo; MMA3 -W^T = K^T (-T B D)^T
     // (K^ read from [K;Q] as an MN-major operand).  The raw rows are free now:
-    // the loader requests the next chunk's (and, once MMA3 and MMA5 are done,
-    // its q^ and k^).
-    if (n + 1 < nchunks) {
-      raw_pending = true;
-      kq_pending = kStagedQK;
-    }
+    // the loader requests the next chunk's.
+    if (n + 1 < nchunks) raw_pending = true;
     if (warp < kTmemWarps) {
       if (warp == 0) {
         fence_after();
         issue_w(tmem + TM_W, id_mk, 4, false,
-                [&](int ks) { return desc(sbase + OFF_KQ + (uint32_t)(ks * 2048), 128 * 128, 1024); },
+                [&](int ks) { return desc(kqb + (uint32_t)(ks * 2048), 128 * 128, 1024); },
                 [&](int ks) { return desc_k(sbase + OFF_TW, ks, kC); });
         commit_w(&V.bar_w);
         __syncwarp();
@@ -1058,12 +1063,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         issue_w(tmem + TM_U, id_mk, 4, true, a_vh, [&](int ks) { return desc_k(sbase + OFF_TUL, ks, kC); });
         commit_w(&V.bar_u);
       }
-      if (loader && n + 1 < nchunks) {
-        request_raw(t0 + kC);
-        // [K;Q]'s last readers (MMA1, MMA3, MMA5) done: the next chunk's q^
-        // and k^ may land there (a timeout here ends in one at the next chunk)
-        if (kStagedQK && bar_wait(&V.bar_w, ph_w) && bar_wait(&V.bar_sq, ph_sq)) request_kq(t0 + kC);
-      }
+      if (loader && n + 1 < nchunks) request_raw(t0 + kC);
       ph_w ^= 1u;
     }
     smem_ready();
@@ -1078,7 +1078,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ph_u ^= 1u;
     if (!wait_all(&V.bar_d, ph_d)) break;
-    // H: Delta^T (lanes v, columns j) -> fp16 hi and lo pairs in TMEM
+    // H: Delta^T (lanes v, columns j) -> fp16 hi and lo pairs in TMEM; in the
+    // staged path also (Delta Gamma)^T, the state update's A operand (W^T's
+    // columns are free since F), so that MMA7 reads k^ straight from its tiles
     if (warp < kTmemWarps) {
       float v[32];
       tmem_ld32(tl + TM_U + 32 * half, v);
@@ -1087,6 +1089,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int q = 0; q < 16; ++q) split2_inrange(v[2 * q], v[2 * q + 1], wh[q], wl[q]);
       tmem_st16w_nw(tl + TM_KQ + 16 * half, wh);
       tmem_st16w_nw(tl + TM_KQ + 32 + 16 * half, wl);
+      if (kStagedQK) {
+#pragma unroll
+        for (int q = 0; q < 32; q += 4) {  // column j = 32 half + q: times e^{G_last - G_j} <= 1
+          const float4 g = ld4(CV.gam + 32 * half + q);
+          const float2 p01 = __fmul2_rn(make_float2(v[q], v[q + 1]), make_float2(g.x, g.y));
+          const float2 p23 = __fmul2_rn(make_float2(v[q + 2], v[q + 3]), make_float2(g.z, g.w));
+          v[q] = p01.x;
+          v[q + 1] = p01.y;
+          v[q + 2] = p23.x;
+          v[q + 3] = p23.y;
+        }
+#pragma unroll
+        for (int q = 0; q < 16; ++q) split2_inrange(v[2 * q], v[2 * q + 1], wh[q], wl[q]);
+        tmem_st16w_nw(tl + TM_W + 16 * half, wh);
+        tmem_st16w_nw(tl + TM_W + 32 + 16 * half, wl);
+      }
       tmem_wait_st();
     }
     smem_ready();
@@ -1151,12 +1169,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (warp == 11) {
         __syncwarp();
         named_sync(kBarMma6, 64);
+        if (kStagedQK) {  // this chunk's k^ lo (requested once the previous MMA7 was done)
+          if (!bar_wait(&V.bar_klo, (uint32_t)n & 1u) && lane == 0) {
+            atomicOr(a.err, kErrTimeout);
+            V.abort = 1;
+          }
+          __syncwarp();
+        }
         fence_after();
-        auto b_gk = [&](int ks) { return desc_mn(sbase + OFF_GK, ks, kC); };
-        issue_ta_w(tmem + TM_S, tmem + TM_KQ, id_km128, 4, true, b_gk);
-        issue_ta_w(tmem + TM_S, tmem + TM_KQ, id_km128, 4, true,
-                   [&](int ks) { return desc_mn(sbase + OFF_GKL, ks, kC); });
-        issue_ta_w(tmem + TM_S, tmem + TM_KQ + 32, id_km128, 4, true, b_gk);
+        if (kStagedQK) {  // S += (Delta Gamma)^T K: A from TMEM (W^T's columns), k^ hi in [K;Q], k^ lo staged
+          auto b_kh = [&](int ks) { return desc(kqb + (uint32_t)(ks * 2048), 128 * 128, 1024); };
+          issue_ta_w(tmem + TM_S, tmem + TM_W, id_km128, 4, true, b_kh);
+          issue_ta_w(tmem + TM_S, tmem + TM_W, id_km128, 4, true,
+                     [&](int ks) { return desc(sbase + OFF_KLO + (uint32_t)(ks * 2048), kC * 128, 1024); });
+          issue_ta_w(tmem + TM_S, tmem + TM_W + 32, id_km128, 4, true, b_kh);
+        } else {
+          auto b_gk = [&](int ks) { return desc_mn(sbase + OFF_GK, ks, kC); };
+          issue_ta_w(tmem + TM_S, tmem + TM_KQ, id_km128, 4, true, b_gk);
+          issue_ta_w(tmem + TM_S, tmem + TM_KQ, id_km128, 4, true,
+                     [&](int ks) { return desc_mn(sbase + OFF_GKL, ks, kC); });
+          issue_ta_w(tmem + TM_S, tmem + TM_KQ + 32, id_km128, 4, true, b_gk);
+        }
         commit_w(&V.bar_s);
         if (n + 1 < nchunks) {
           finish_gb<kRawGates>(neg_exp_A, dt_bias, t0 + kC, T, lane, g_nxt, b_nxt);
@@ -1173,6 +1206,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = bar_wait(&V.bar_s, ph_s);
       ph_s ^= 1u;
       fence_after();
+      // MMA7 is done with k^ lo (staged path): the next chunk's may land
+      if (kStagedQK && loader && ok && n + 1 < nchunks) request_klo(t0 + kC);
       if (__all_sync(0xffffffffu, ok)) {
         const bool last = n + 1 == nchunks;
         const float dcn = V.dC_next;
@@ -1232,6 +1267,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     ph_sq ^= 1u;
+    if (kStagedQK) {
+      ++klo_used;
+      if (n + 1 < nchunks) ++klo_next;
+    }
     fence_before();
     fence_smem_to_async();  // z, the staging and the v tiles: order before the next TMA and MMA reads
     __syncthreads();
@@ -1249,7 +1288,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     if (raw_pending) bar_wait(&V.bar_raw, phase_raw);
     if (z_pending) bar_wait(&V.bar_z, phase_z);
-    if (kStagedQK && kq_pending) bar_wait(&V.bar_kq, phase_kq);
+    for (int j = kq_used; j < kq_next; ++j) bar_wait(&V.bar_kq[j & 1], (uint32_t)(j >> 1) & 1u);
+    for (int j = klo_used; j < klo_next; ++j) bar_wait(&V.bar_klo, (uint32_t)j & 1u);
     commit(&V.bar_end);
     bar_wait(&V.bar_end, 0);
   }
