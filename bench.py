@@ -99,6 +99,21 @@ def decode_multi_bytes(B, T, Hk, Hv, io=2, snapshots=True):
     return B * per_seq + C * 4 * io + D * io
 
 
+WORKLOAD_LABEL = {
+    "4b_prefill": "Qwen3.5-4B-shaped GDN layer prefill",
+    "0.8b_prefill": "Qwen3.5-0.8B-shaped GDN layer prefill",
+    "27b_prefill": "Qwen3.8-27B-shaped GDN long prefill",
+}
+# What the path computes in: io is bf16, the tensor-core operands fp16 (the
+# state path's as hi/lo pairs), the state and every accumulation fp32.
+DTYPE = "bf16 io, fp16 MMA operands (hi/lo pairs on the state path), fp32 state and accumulation"
+
+
+def workload_name(name, p):
+    return "%s: B=%d, T=%d, Hk=%d, Hv=%d, Dk=Dv=128, bf16 io, fp32 state" % (
+        WORKLOAD_LABEL[name], p.B, p.T, p.Hk, p.Hv)
+
+
 # Packed-batch length mix: 24 sequences, log-uniform lengths in [100, 4000]
 # (a serving batch of prompts), seed 7.
 def varlen_lengths():
@@ -375,6 +390,8 @@ def gdn_arm(args, world, rank, local):
                          "peak_source": peak_src + " hbm_gbs (burst copy)"},
         }
         del S, conv, q_all, z_all, g_all, b_all, od
+    # ---- the other prefill shapes of the metric (0.8B, 27B), one call each
+    shapes = None if args.no_shapes else shape_rows(args, peaks, peak_src, stream, barrier, world, rank)
     # ---- the extended calls: raw gates, packed batch, multi-token decode
     nxt = None if args.no_next else next_rows(args, x, o, S_T, conv_T, p, peaks, peak_src, stream,
                                               barrier, world, rank)
@@ -443,9 +460,8 @@ def gdn_arm(args, world, rank, local):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f16", "data": "synthetic (seeded; model-shaped random inputs, no weights needed)",
-        "config": {"workload": "Qwen3.5-4B-shaped GDN layer prefill: B=%d, T=%d, Hk=%d, Hv=%d, "
-                               "Dk=Dv=128, bf16 io, fp32 state" % (p.B, p.T, p.Hk, p.Hv),
+        "dtype": DTYPE, "data": "synthetic (seeded; model-shaped random inputs, no weights needed)",
+        "config": {"workload": workload_name(args.workload, p),
                    "io_dtype": p.io, "state_dtype": "f32",
                    "l2": "inputs larger than L2 (%.2f GB read+written per step; L2 129 MB)"
                          % (pbytes / 1e9),
@@ -468,6 +484,7 @@ def gdn_arm(args, world, rank, local):
         "gpu_launches": args.steps * PREFILL_KERNELS_PER_CALL,
         "clocks": clk,
         "decode": dec,
+        "prefill_shapes": shapes,
         "next": nxt,
     }
     if world > 1:
@@ -507,6 +524,60 @@ def time_launches(fn, steps, warmup, stream, barrier, world=1):
         ev[k][1].record(stream)
     barrier()
     return max_over_ranks(float(np.mean([s.elapsed_time(e) for s, e in ev])), world)
+
+
+def shape_rows(args, peaks, peak_src, stream, barrier, world, rank):
+    """The prefill shapes the metric names besides the main workload: one
+    gdn_prefill_ex call each (the benchmarked path: a workspace given), inputs
+    resident, tokens/s with the call's HBM and bf16 tensor rooflines."""
+    import torch
+
+    from gated_deltanet_mixer_gb300 import gdn
+    from gated_deltanet_mixer_gb300 import inputs as I
+
+    out = {}
+    for name in ("0.8b_prefill", "27b_prefill"):
+        if name == args.workload:
+            continue
+        spec = dict(I.CASES[name])
+        spec["case"] = rank_case(spec["case"], rank)
+        q = I.prefill_problem(**spec)
+        a = q.arrays
+        bf = torch.bfloat16
+
+        def dev(v, dt=torch.float32):
+            return None if v is None else torch.from_numpy(v).to("cuda").to(dt)
+
+        qx = dict(qkv_pre=dev(a["qkv_pre"], bf), z=dev(a["z"], bf), g=dev(a["g"]), beta=dev(a["beta"]),
+                  conv_w=dev(a["conv_w"], bf), norm_w=dev(a["norm_w"], bf), S0=dev(a["S0"]),
+                  conv0=dev(a["conv0"], bf))
+        del q.arrays
+        qo, qS, qc = gdn.alloc_prefill_outputs(q.B, q.T, q.Hk, q.Hv, bf)
+        qws = torch.empty(gdn.gdn_prefill_workspace_bytes(q.B, q.T, q.Hk, q.Hv), dtype=torch.uint8,
+                          device="cuda")
+        steps = max(3, min(args.steps, 10))
+        ms = time_launches(lambda: gdn.gdn_prefill_ex(
+            qx["qkv_pre"], qx["z"], qx["g"], qx["beta"], qx["conv_w"], qx["norm_w"], qx["S0"], qx["conv0"],
+            qo, qS, qc, Hk=q.Hk, Hv=q.Hv, workspace=qws, stream=stream), steps, args.warmup, stream, barrier,
+            world)
+        nb = prefill_bytes(q.B, q.T, q.Hk, q.Hv)
+        fl = prefill_flops(q.B, q.T, q.Hk, q.Hv)
+        ach, tf = nb / (ms * 1e-3) / 1e9, fl / (ms * 1e-3) / 1e12
+        out[name] = {
+            "workload": workload_name(name, q), "value": world * q.B * q.T / (ms * 1e-3),
+            "unit": "tokens/s", "ms_per_launch": ms, "launches_timed": steps,
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": ach / peaks["hbm_gbs"], "algorithmic_bytes_per_launch": nb,
+                         "peak_source": peak_src + " hbm_gbs (burst copy)"},
+            "roofline_tensor": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"],
+                                "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"],
+                                "algorithmic_flops_per_launch": fl,
+                                "peak_source": peak_src + " bf16_tflops (burst)"}}
+        del qx, qo, qS, qc, qws
+        torch.cuda.empty_cache()
+    if gdn.gdn_device_status(stream) != 0:
+        raise RuntimeError("device status not OK after the prefill shapes")
+    return out
 
 
 def next_rows(args, x, o, S_T, conv_T, p, peaks, peak_src, stream, barrier, world, rank):
@@ -653,8 +724,7 @@ def reference_arm(args, world, rank):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded; model-shaped random inputs, no weights needed)",
-        "config": {"workload": "Qwen3.5-4B-shaped GDN layer prefill: B=%d, T=%d, Hk=%d, Hv=%d, "
-                               "Dk=Dv=128, bf16 io, fp32 state" % (p.B, p.T, p.Hk, p.Hv),
+        "config": {"workload": workload_name(args.workload, p),
                    "io_dtype": p.io, "state_dtype": "f32"},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
@@ -673,6 +743,8 @@ def main():
                     choices=["4b_prefill", "0.8b_prefill", "27b_prefill"])
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-shapes", action="store_true",
+                    help="skip the other prefill shapes of the metric (0.8B, 27B)")
     ap.add_argument("--no-next", action="store_true",
                     help="skip the extended calls (raw gates, packed batch, multi-token decode)")
     ap.add_argument("--cpu-budget", type=float, default=15.0,

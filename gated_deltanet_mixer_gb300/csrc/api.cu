@@ -278,6 +278,11 @@ gdn_status gdn_prefill_static(const gdn_shape *shape, const gdn_prefill_io *io, 
   if (!shape || !io || io->workspace) return GDN_ERR_INVALID_ARG;
   const size_t need = gdn_prefill_workspace_bytes(shape, io->cu_seqlens != nullptr ? 1 : 0);
   if (need > GDN_STATIC_SCRATCH_BYTES) return GDN_ERR_UNSUPPORTED_SHAPE;
+  // The device is checked before the scratch is looked up (which loads the
+  // module), so that a wrong device reports GDN_ERR_NO_DEVICE as elsewhere.
+  unsigned int *err = nullptr;
+  const gdn_status dev_st = check_device(&err);
+  if (dev_st != GDN_OK) return dev_st;
   gdn_prefill_io staged = *io;
   if (need > 0 && shape->io_dtype == GDN_BF16 && !io->S_snap) {  // the chunked kernel: stage q^ / k^
     void *p = nullptr;

@@ -4,6 +4,8 @@
     python -m gated_deltanet_mixer_gb300.profile_cases prefill --B 1 --T 2048 --calls 2
     python -m gated_deltanet_mixer_gb300.profile_cases prefill --B 4 --T 2048 --calls 2 --staged
     python -m gated_deltanet_mixer_gb300.profile_cases linear --T 2048 --K 5120 --N 16480 --calls 2
+    python -m gated_deltanet_mixer_gb300.profile_cases decode_multi --B 64 --T 4 --calls 2 [--snap]
+    python -m gated_deltanet_mixer_gb300.profile_cases serial --B 4 --T 1024 --Hv 32 --calls 2
 
 Inputs are the seeded synthetic ones of ``inputs.py``; each case is sized so
 that its working set is larger than L2 (129 MB) but only a few GB at most.
@@ -50,6 +52,33 @@ def prefill(B, T, Hk, Hv, calls, staged=False):
             gdn.gdn_prefill(*x, o, S_T, conv_T, Hk=Hk, Hv=Hv)
 
 
+def decode_multi(B, T, Hk, Hv, calls, snap):
+    """T tokens per sequence from the cache (the T-token decode kernel)."""
+    dp = I.decode_problem(B=B, Hk=Hk, Hv=Hv, steps=T, case=203)
+    t = torch.bfloat16
+    S = _dev(dp.S)
+    q = _dev(dp.qkv_pre.transpose(1, 0, 2), t)
+    z = _dev(dp.z.transpose(1, 0, 2), t)
+    g, b = _dev(dp.g.transpose(1, 0, 2)), _dev(dp.beta.transpose(1, 0, 2))
+    cw, nw = _dev(dp.conv_w, t), _dev(dp.norm_w, t)
+    conv_in = _dev(dp.conv, t)
+    conv_out = torch.empty_like(conv_in)
+    o = torch.empty(B, T, Hv * 128, device="cuda", dtype=t)
+    S_snap = torch.empty(B, T, Hv, 128, 128, device="cuda") if snap else None
+    for _ in range(calls):
+        gdn.gdn_decode_ex(q, z, g, b, cw, nw, S, conv_in, conv_out, o, Hk=Hk, Hv=Hv, S_snap=S_snap)
+
+
+def serial(B, T, Hk, Hv, calls):
+    """fp32 io prefill: the token-serial kernel."""
+    p = I.prefill_problem(B, T, Hk, Hv, io="f32", case=204)
+    a = p.arrays
+    x = [_dev(a[k]) for k in ("qkv_pre", "z", "g", "beta", "conv_w", "norm_w", "S0", "conv0")]
+    o, S_T, conv_T = gdn.alloc_prefill_outputs(B, T, Hk, Hv, torch.float32)
+    for _ in range(calls):
+        gdn.gdn_prefill(*x, o, S_T, conv_T, Hk=Hk, Hv=Hv)
+
+
 def linear(T, K, N, calls):
     xa, wa = I.linear_problem(T, N, K, case=202)
     x, w = _dev(xa, torch.bfloat16), _dev(wa, torch.bfloat16)
@@ -60,7 +89,7 @@ def linear(T, K, N, calls):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("kernel", choices=["decode", "prefill", "linear"])
+    ap.add_argument("kernel", choices=["decode", "prefill", "linear", "decode_multi", "serial"])
     ap.add_argument("--B", type=int, default=None)
     ap.add_argument("--T", type=int, default=2048)
     ap.add_argument("--Hk", type=int, default=16)
@@ -69,12 +98,17 @@ def main():
     ap.add_argument("--N", type=int, default=16480)
     ap.add_argument("--calls", type=int, default=3)
     ap.add_argument("--staged", action="store_true", help="prefill through a workspace (two kernels)")
+    ap.add_argument("--snap", action="store_true", help="decode_multi: a state snapshot after every token")
     a = ap.parse_args()
     gdn.lib()
     if a.kernel == "decode":
         decode(a.B or 48, a.Hk, a.Hv or 48, a.calls)
     elif a.kernel == "linear":
         linear(a.T, a.K, a.N, a.calls)
+    elif a.kernel == "decode_multi":
+        decode_multi(a.B or 64, a.T, a.Hk, a.Hv or 48, a.calls, a.snap)
+    elif a.kernel == "serial":
+        serial(a.B or 4, a.T, a.Hk, a.Hv or 32, a.calls)
     else:
         prefill(a.B or 4, a.T, a.Hk, a.Hv or 32, a.calls, a.staged)
     torch.cuda.synchronize()

@@ -36,3 +36,21 @@ def read_golden(name):
 @pytest.fixture
 def golden():
     return read_golden
+
+
+def pytest_terminal_summary(terminalreporter):
+    """The o error yardsticks over every GPU comparison of the run (see
+    gpu_harness.REPORT): the largest of each, relative to rms(o_ref)."""
+    h = sys.modules.get("gpu_harness")
+    rep = getattr(h, "REPORT", None) if h else None
+    if not rep:
+        return
+    tr = terminalreporter
+    tr.write_sep("-", "o error over %d comparisons (max, relative to rms(o_ref))" % len(rep))
+    for key, label in (("excess", "asserted: |o_gpu - o_ref| - bf16 quantum"),
+                       ("plain", "plain: |o_gpu - o_ref|"),
+                       ("rne", "against bf16_rne(o_ref): |o_gpu - rne(o_ref)|"),
+                       ("rne_ulps", "the same in bf16 ulps, where |o_ref| >= rms/16")):
+        vals = [r[key] for r in rep if key in r]
+        if vals:
+            tr.write_line("  %-52s %.3e" % (label, max(vals)))

@@ -13,10 +13,19 @@ import numpy as np
 import torch
 
 from gated_deltanet_mixer_gb300 import gdn
+from gated_deltanet_mixer_gb300 import inputs as I
 from oracle import oracle as O
 
 O_TOL = 2e-2
 S_TOL = 1e-2
+
+# Every o comparison of the session, by yardstick (printed at the end of the
+# run by conftest.py): the asserted excess over the output's rounding, the
+# plain max |o_gpu - o_ref| / rms, the same against the oracle's output
+# rounded to bf16 (round to nearest even), and that difference in bf16 ulps
+# of the rounded reference where |o_ref| >= rms/16 (0 = every stored value is
+# the correctly rounded one, 1 = off by one rounding step at most).
+REPORT = []
 
 
 def torch_io(io):
@@ -37,10 +46,33 @@ def quantum(ref, io):
     return (2.0 ** -8) * np.abs(ref) if io == "bf16" else 0.0
 
 
+def bf16_ulp(x):
+    """The spacing of bf16 values at |x| (normals; 2^-133 below them)."""
+    e = np.floor(np.log2(np.maximum(np.abs(x), 2.0 ** -126)))
+    return 2.0 ** (e - 7)
+
+
+def yardsticks(got, ref, io):
+    """The o error measures of REPORT, relative to rms(ref)."""
+    rms = float(np.sqrt(np.mean(ref * ref))) or 1.0
+    out = {"excess": float(np.max(np.abs(got - ref) - quantum(ref, io))) / rms,
+           "plain": float(np.max(np.abs(got - ref))) / rms}
+    if io == "bf16":
+        rne = I.round_to_bf16(ref).astype(np.float64)
+        d = np.abs(got - rne)
+        out["rne"] = float(np.max(d)) / rms
+        big = np.abs(rne) >= rms / 16  # ulps are meaningful where |o| is not tiny against rms
+        if np.any(big):
+            out["rne_ulps"] = float(np.max(d[big] / bf16_ulp(rne[big])))
+    return out
+
+
 def check_o(got, ref, io, what="o"):
     rms = float(np.sqrt(np.mean(ref * ref)))
     excess = np.abs(got - ref) - quantum(ref, io)
     worst = float(np.max(excess)) if excess.size else 0.0
+    if excess.size:
+        REPORT.append(yardsticks(got, ref, io))
     assert np.all(np.isfinite(got)), "%s: non-finite values" % what
     assert worst <= O_TOL * rms, "%s: max excess error %.3e > %.3e (rms %.3e)" % (
         what, worst, O_TOL * rms, rms)
