@@ -40,6 +40,25 @@
  * launch itself.  Values are not checked: g must be <= 0 (finite, or -inf
  * for a reset) and beta in [0, 1]; other values give unspecified results
  * but stay within the buffers.
+ *
+ * Numeric domain of the bf16-io prefill (the chunked tensor-core kernels).
+ * The products run on the tensor cores with fp16 operands and fp32
+ * accumulation; the state itself stays fp32.
+ *   - g below -80 acts as -80: a decay of e^-80 (about 1.8e-35) stands in for
+ *     any smaller one, the reset g = -inf included.  Decode and the fp32-io
+ *     kernels use e^g as given (e^-inf = 0).
+ *   - Overflow: the fp16 copy of the state that multiplies W and q^, the
+ *     chunk's Delta = U - W S (and Delta scaled by decay ratios <= 1) and W
+ *     are converted without a range clamp, so |S|, |Delta| and |W| must stay
+ *     below 65504; entries beyond it become inf.  Inputs (v, S0, the inverse
+ *     T) are saturated to +-65504 instead.  Normalised q^ and k^ are <= 1.
+ *   - Underflow: entries below 6.1e-5 in magnitude are fp16 subnormals
+ *     (absolute spacing 6.0e-8), so where the state's entries are of order
+ *     1e-4 and smaller, the products S W^T and S q^ carry them with fewer
+ *     significant bits (the fp32 state and its update keep full precision).
+ *   Tested against the fp64 oracle within the tolerances: qkv_pre scaled by
+ *   1e-3 and by 30, initial states of rms 1e-4 and 10, g = -inf anywhere in
+ *   a chunk, g down to -1e4, runs of beta = 0 and beta = 1.
  */
 #ifndef GDN_H
 #define GDN_H
