@@ -115,6 +115,22 @@ bool all_aligned(const void *const *ptrs, int n) {
 size_t qk_workspace_bytes(const gdn::Dims &d, long long tokens) {
   return 3 * (size_t)tokens * (size_t)d.Hk * gdn::kDHead * 2;
 }
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+// Workspace of the chunk-parallel / sequential prefill: the staged q^ / k^,
+// then kSplitItemBytes per (chunk slot, value head); 0 when the work items
+// exceed what the kernels index (TMA row coordinates in 31 bits).
+size_t split_workspace_bytes(const gdn::Dims &d, long long tokens, bool packed, gdn::SplitArgs *sa = nullptr) {
+  int nslots = 0, nch = 0;
+  const long long items = gdn::split_items(d, tokens, packed, &nslots, &nch);
+  if (items < 1 || items * gdn::kDHead >= (1LL << 31)) return 0;
+  if (sa) {
+    sa->B = d.B;
+    sa->T = d.T;
+    sa->nch = nch;
+    sa->nslots = nslots;
+  }
+  return align256(qk_workspace_bytes(d, tokens)) + (size_t)items * gdn::kSplitItemBytes;
+}
 
 gdn_status prefill_impl(const gdn_shape *shape, const gdn_prefill_io *io, void *stream) {
   if (!shape || !io) return GDN_ERR_INVALID_ARG;
@@ -161,16 +177,32 @@ gdn_status prefill_impl(const gdn_shape *shape, const gdn_prefill_io *io, void *
   // arithmetic throughout) and per-token snapshots: the token-serial kernel.
   const bool bf16 = shape->io_dtype == GDN_BF16;
   const bool chunked = bf16 && !io->S_snap;
+  // With a workspace the chunked path takes the fastest form that fits it:
+  // the chunk-parallel / sequential split (split_workspace_bytes), else the
+  // staged q^ / k^ form (qk_workspace_bytes).
   void *ws = nullptr;
+  bool split = false;
+  gdn::SplitArgs sa{};
   if (chunked && io->workspace) {
-    const size_t need = qk_workspace_bytes(d, tokens);
+    const size_t need_qk = qk_workspace_bytes(d, tokens);
+    const size_t need_split = split_workspace_bytes(d, tokens, packed, &sa);
     if ((reinterpret_cast<uintptr_t>(io->workspace) & 255u) != 0) return GDN_ERR_ALIGNMENT;
-    if (io->workspace_bytes < need) return GDN_ERR_INVALID_ARG;
-    const Range rw = range_of(io->workspace, need);
+    if (io->workspace_bytes < need_qk) return GDN_ERR_INVALID_ARG;
+    split = need_split > 0 && io->workspace_bytes >= need_split;
+    const Range rw = range_of(io->workspace, split ? need_split : need_qk);
     for (int i = 0; i < n; ++i)
       if (overlap(rw, in[i])) return GDN_ERR_ALIAS;
     if (overlap(rw, ro) || overlap(rw, rs) || overlap(rw, rc)) return GDN_ERR_ALIAS;
     ws = io->workspace;
+    if (split) {
+      const long long items = (long long)sa.nslots * d.Hv;
+      uint8_t *base = static_cast<uint8_t *>(ws) + align256(need_qk);
+      sa.cu = io->cu_seqlens;
+      sa.ws_u = reinterpret_cast<float *>(base);
+      sa.ws_nw = base + (size_t)items * 32768;
+      sa.ws_m = base + (size_t)items * (32768 + 16384);
+      sa.ws_vec = reinterpret_cast<float *>(base + (size_t)items * (32768 + 16384 + 8192));
+    }
   }
   unsigned int *err = nullptr;
   st = check_device(&err);
@@ -182,7 +214,9 @@ gdn_status prefill_impl(const gdn_shape *shape, const gdn_prefill_io *io, void *
     e = gdn::launch_prefill(a, bf16, (cudaStream_t)stream);
   } else {
     e = ws ? gdn::launch_prefill_qk(a, (cudaStream_t)stream) : cudaSuccess;
-    if (e == cudaSuccess) e = gdn::launch_prefill_chunked(a, true, (cudaStream_t)stream);
+    if (e == cudaSuccess)
+      e = split ? gdn::launch_prefill_split(a, sa, (cudaStream_t)stream)
+                : gdn::launch_prefill_chunked(a, true, (cudaStream_t)stream);
   }
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
@@ -276,7 +310,7 @@ gdn_status gdn_prefill_ex(const gdn_shape *shape, const gdn_prefill_io *io, void
 
 gdn_status gdn_prefill_static(const gdn_shape *shape, const gdn_prefill_io *io, void *stream) {
   if (!shape || !io || io->workspace) return GDN_ERR_INVALID_ARG;
-  const size_t need = gdn_prefill_workspace_bytes(shape, io->cu_seqlens != nullptr ? 1 : 0);
+  const size_t need = gdn_prefill_staged_bytes(shape, io->cu_seqlens != nullptr ? 1 : 0);
   if (need > GDN_STATIC_SCRATCH_BYTES) return GDN_ERR_UNSUPPORTED_SHAPE;
   // The device is checked before the scratch is looked up (which loads the
   // module), so that a wrong device reports GDN_ERR_NO_DEVICE as elsewhere.
@@ -294,6 +328,16 @@ gdn_status gdn_prefill_static(const gdn_shape *shape, const gdn_prefill_io *io, 
 }
 
 size_t gdn_prefill_workspace_bytes(const gdn_shape *shape, int packed) {
+  if (!shape || shape->B < 1 || shape->T < 1 || shape->io_dtype != GDN_BF16) return 0;
+  const long long tokens = packed ? (long long)shape->T : (long long)shape->B * shape->T;
+  gdn::Dims d;
+  Sizes sz;
+  if (check_shape(shape, tokens, &d, &sz) != GDN_OK) return 0;
+  const size_t split = split_workspace_bytes(d, tokens, packed != 0);
+  return split ? split : qk_workspace_bytes(d, tokens);
+}
+
+size_t gdn_prefill_staged_bytes(const gdn_shape *shape, int packed) {
   if (!shape || shape->B < 1 || shape->T < 1 || shape->io_dtype != GDN_BF16) return 0;
   const long long tokens = packed ? (long long)shape->T : (long long)shape->B * shape->T;
   gdn::Dims d;

@@ -84,6 +84,28 @@ cudaError_t launch_prefill(const PrefillArgs &a, bool bf16, cudaStream_t s);    
 cudaError_t launch_prefill_chunked(const PrefillArgs &a, bool bf16, cudaStream_t s);  // chunked WY, tcgen05
 cudaError_t launch_prefill_qk(const PrefillArgs &a, cudaStream_t s);  // q^ / k^ into a.qk_ws (bf16 io)
 
+// The chunk-parallel / sequential prefill (prefill_split.cu).  Chunk slots
+// index the workspace: fixed length, slot = b * nch + n; packed sequences,
+// slot = (cu[b] >> 6) + b + n.  A work item is (slot, value head), item =
+// slot * Hv + h, and owns kSplitItemBytes of workspace across four arrays:
+//   ws_u   [items][128 v][64 j]  fp32   U^T
+//   ws_nw  [items][128 k][64 j]  fp16   -W^T
+//   ws_m   [items][64 i][64 j]   fp16   M = (Q K^T) o R (lower, diagonal included)
+//   ws_vec [items][2][64]        fp32   d_i = e^{G_i}, Gamma_j = e^{G_last - G_j}
+// The staged q^ / k^ (qk_ws, from launch_prefill_qk) must be in place first.
+struct SplitArgs {
+  int B, T;        // sequences; tokens per sequence (fixed length) or in total (packed)
+  int nch, nslots; // chunks per sequence (fixed length); chunk slots
+  const int *cu;   // cu_seqlens or null
+  float *ws_u;
+  void *ws_nw, *ws_m;
+  float *ws_vec;
+};
+constexpr size_t kSplitItemBytes = 32768 + 16384 + 8192 + 512;
+// Work items of a call (tokens: B*T fixed length, T packed); sets nslots, nch.
+long long split_items(const Dims &d, long long tokens, bool packed, int *nslots, int *nch);
+cudaError_t launch_prefill_split(const PrefillArgs &a, const SplitArgs &s, cudaStream_t st);
+
 // The library's device scratch (GDN_STATIC_SCRATCH_BYTES) on the current
 // device; its address is looked up once per device.
 cudaError_t static_scratch(void **ptr);

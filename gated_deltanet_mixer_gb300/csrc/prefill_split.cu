@@ -1,0 +1,950 @@
+// prefill_split.cu -- the chunked (WY) prefill split into a chunk-parallel
+// part and a sequential part, so that only the state recurrence is serial.
+//
+// Page "How Qwen3.5 works" (azmle112.github.io), section 9.11: within a chunk
+// of 64 tokens, A = I + tril((B K K^T) o R, -1), T = A^{-1}, U = T B V and
+// W = T B D K depend on the chunk alone; only Delta = U - W S, the output
+// O = D Q S + ((Q K^T) o R) Delta and the state update
+// S <- d_n S + K^T diag(d_n / d_j) Delta need the carried state S.  Kept
+// value-major (S[v][k], node gdn.core of the Qwen3.8-27B spec):
+//   Delta^T = U^T - S W^T,  O^T = (S Q^T) D + Delta^T M^T,  M = (Q K^T) o R,
+//   S <- d_n S + (Delta Gamma)^T K,  Gamma = diag(d_n / d_j).
+//
+// prefill_prep_kernel, one work item per (chunk, value head), every chunk of
+// every sequence at once (persistent CTAs, two per SM): from the staged q^ and
+// k^ of the chunk (written once per key head by prefill_qk_kernel) and its raw
+// v rows and gates it forms the chunk vectors, [K;Q] K^T on the tensor cores,
+// L and M, the inverse T (fp32, CUDA cores), the v tiles (conv + SiLU, into
+// TMEM as fp16 hi/lo), U^T = V^T (T B)^T and -W^T = K^T (-T B D)^T on the
+// tensor cores, and writes U^T (fp32), -W^T (fp16), M (fp16) and the vectors
+// d, Gamma to a workspace.
+//
+// prefill_seq_kernel, one CTA per (sequence, value head): walks the chunks
+// with the fp32 state resident in TMEM.  Per chunk four groups of MMAs:
+//   MMA4  D = S (-W^T)        MMA5  O1 = S Q^T
+//   MMA6  O2 = Delta^T M^T    MMA7  S += (Delta Gamma)^T K (hi/lo split)
+// and three passes on the CUDA cores: Delta = D + U^T to fp16 (hi, and
+// Gamma-scaled hi/lo); the state pass (fp16 copy, rescale by the next chunk's
+// decay); the epilogue O = d O1 + O2 and the gated RMSNorm (node gdn.norm)
+// on other warps, overlapping the next chunk's chain.  The chunk tiles arrive
+// by TMA two chunks ahead.
+//
+// Rows of a chunk past its sequence's end carry beta = 0 and g = 0, so their
+// columns of T B, T B D are zero: they add nothing to U, W, Delta or the state,
+// whatever finite values the staged rows hold there.
+#include <cuda.h>
+
+#include "chunk_math.cuh"
+#include "gdn_device.cuh"
+#include "launch.h"
+#include "tma_host.h"
+#include "umma.cuh"
+
+namespace gdn {
+namespace {
+
+using namespace umma;
+using namespace chunk;
+using bf16 = __nv_bfloat16;
+
+constexpr int kRawRows = kC + 3;                   // a chunk's rows plus the three before it
+constexpr uint32_t kRawBlock = kRawRows * kD * 2;  // 17152 bytes
+
+// ---- work geometry -----------------------------------------------------------
+// Chunk slots index the workspace: fixed length, slot = b * nch + n; packed
+// sequences, slot = (cu[b] >> 6) + b + n, which never collides (a sequence
+// starting at token s with L tokens uses slots (s >> 6) + b .. (s >> 6) + b +
+// ceil(L/64) - 1, below the next sequence's first slot).
+struct ChunkLoc {
+  int b, n, bos, len;
+  bool ok;
+};
+
+__device__ __forceinline__ ChunkLoc locate(const SplitArgs &s, int slot) {
+  ChunkLoc c{0, 0, 0, 0, false};
+  if (!s.cu) {
+    c.b = slot / s.nch;
+    c.n = slot - c.b * s.nch;
+    c.bos = c.b * s.T;
+    c.len = s.T;
+    c.ok = c.b < s.B;
+    return c;
+  }
+  int lo = 0, hi = s.B - 1;  // the last sequence whose first slot is <= slot
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if ((s.cu[mid] >> 6) + mid <= slot) lo = mid; else hi = mid - 1;
+  }
+  const int s0 = s.cu[lo], s1 = s.cu[lo + 1];
+  if (s0 < 0 || s1 < s0 || s1 > s.T) return c;  // unusable offsets: the sequential kernel reports them
+  c.b = lo;
+  c.bos = s0;
+  c.len = s1 - s0;
+  c.n = slot - ((s0 >> 6) + lo);
+  c.ok = c.n >= 0 && kC * c.n < c.len;
+  return c;
+}
+__device__ __forceinline__ int slot_of(const SplitArgs &s, int b, int bos, int n) {
+  return s.cu ? (bos >> 6) + b + n : b * s.nch + n;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// A plain bulk copy global -> shared completing on `bar` (16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+// =============================================================================
+// prefill_prep_kernel
+// =============================================================================
+constexpr int kPrepThreads = 256;
+// Shared memory (offsets from a 1024-aligned base).
+constexpr uint32_t P_KQ = 0;        // [K;Q] K-major 128 x 128 fp16 (k^ hi rows 0-63, q^ rows 64-127)  32 KB
+constexpr uint32_t P_TU = 32768;    // T diag(beta) hi  K-major [i][j]                                      8 KB
+constexpr uint32_t P_TUL = 40960;   // T diag(beta) lo                                                      8 KB
+constexpr uint32_t P_TW = 49152;    // -T diag(beta d)                                                      8 KB
+constexpr uint32_t P_NW = P_TU;     // after MMA U / W: -W^T fp16 MN-major [k][j] over TU + TUL            16 KB
+constexpr uint32_t P_M = 57344;     // M fp16 K-major [i][j]                                                8 KB
+constexpr uint32_t P_RAW = 65536;   // raw v rows bf16 [67][128]; then L fp32 [64][68]; then U^T box 0  17 KB
+constexpr uint32_t P_TF = P_RAW + 64 * kLs * 4;  // T fp32 [64][64] (tfi); then U^T box 1                16 KB
+constexpr uint32_t P_PB = P_TF + 16384;          // solve block products                                 4 KB
+constexpr uint32_t P_VEC = P_PB + 4096;
+struct PrepShared {
+  ChunkVecs cv;
+  uint64_t bar_ld, bar_qk, bar_uw;
+  uint32_t tmem;
+  int abort;
+};
+constexpr uint32_t kPrepSmem = P_VEC + ((sizeof(PrepShared) + 127) / 128) * 128 + 1024;
+static_assert(64 * kLs * 4 >= kRawBlock && 64 * kLs * 4 >= 16384, "the raw v region holds L and U^T box 0");
+static_assert(P_TF % 1024 == 0 && P_PB % 16 == 0 && P_VEC % 16 == 0, "alignment (U^T boxes: 1024)");
+static_assert(kPrepSmem <= 113 * 1024, "two CTAs per SM");
+// TMEM columns (256 allocated).
+constexpr uint32_t TP_KQ = 0;    // [K K^T; Q K^T]                    64
+constexpr uint32_t TP_V = 64;    // V^T fp16 pairs: hi 64..95, lo 96..127
+constexpr uint32_t TP_U = 128;   // U^T [v][i]                        64
+constexpr uint32_t TP_W = 192;   // -W^T [k][i]                       64
+constexpr uint32_t kPrepTmem = 256;
+constexpr int kBarSolve = 1;
+
+template <bool kRawGates>
+__global__ void __launch_bounds__(kPrepThreads, 2)
+    prefill_prep_kernel(const PrefillArgs a, const SplitArgs s, const __grid_constant__ CUtensorMap tm_qkv,
+                        const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ CUtensorMap tm_u,
+                        const __grid_constant__ CUtensorMap tm_nw, const __grid_constant__ CUtensorMap tm_m) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  PrepShared &V = *reinterpret_cast<PrepShared *>(sm + P_VEC);
+  const Dims d = a.d;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int quad = warp & 3, half = warp >> 2;
+  const int lrow = 32 * quad + lane;  // TMEM lane of this thread
+  const uint32_t sbase = smem_u32(sm);
+  const SolveSmem ss{reinterpret_cast<const float *>(sm + P_RAW), reinterpret_cast<float *>(sm + P_TF),
+                     reinterpret_cast<float *>(sm + P_PB), sm + P_TU, sm + P_TUL, sm + P_TW};
+  const bf16 *conv_w = static_cast<const bf16 *>(a.conv_w);
+  const bf16 *conv0 = static_cast<const bf16 *>(a.conv0);
+  const int r = d.Hv / d.Hk;
+  const long long C = d.C;
+  const long long nitems = (long long)s.nslots * d.Hv;
+
+  if (tid == 0) {
+    bar_init(&V.bar_ld, 1);
+    bar_init(&V.bar_qk, 1);
+    bar_init(&V.bar_uw, 1);
+    V.abort = 0;
+  }
+  if (warp == 0) tmem_alloc(&V.tmem, kPrepTmem);
+  zero_T_upper(ss, tid, kPrepThreads, 0, 3 * 192);
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = V.tmem;
+  const uint32_t tl = tmem + ((uint32_t)(32 * quad) << 16);
+  const uint32_t id_kk = idesc(128, 64, 0, 0), id_mk = idesc(128, 64, 1, 0);
+  uint32_t ph_ld = 0, ph_qk = 0, ph_uw = 0;
+  bool ld_pending = false, stores = false;  // thread 0's bookkeeping
+
+  for (long long item = blockIdx.x; item < nitems; item += gridDim.x) {
+    const int slot = (int)(item / d.Hv), h = (int)(item % d.Hv);
+    const ChunkLoc c = locate(s, slot);
+    if (!c.ok) continue;  // the same decision in every thread
+    const int kh = h / r, t0 = kC * c.n, T = c.len;
+    const long long bos = c.bos;
+    const long long cv = 2LL * d.Hk * kD + (long long)h * kD;
+    // The previous item's TMA stores must have read their shared-memory sources.
+    if (tid == 0 && stores) bulk_wait_read();
+    __syncthreads();
+    if (tid == 0) {
+      bar_expect_tx(&V.bar_ld, 2 * kC * kD * 2 + kRawBlock);
+#pragma unroll
+      for (int at = 0; at < 2; ++at) {
+        tma_load_3d(sbase + P_KQ + at * 16384 + 64 * 128, &tm_qk, kh * kD + 64 * at, (int)(bos + t0), 0, &V.bar_ld);
+        tma_load_3d(sbase + P_KQ + at * 16384, &tm_qk, kh * kD + 64 * at, (int)(bos + t0), 1, &V.bar_ld);
+      }
+      tma_load_3d(sbase + P_RAW, &tm_qkv, (int)cv, (int)(bos + t0 - 3), 0, &V.bar_ld);
+      ld_pending = true;
+    }
+    if (warp == 7) {  // the chunk's gates and vectors
+      float gv[2], bv[2];
+      load_gb<kRawGates>(a.gate, bos, d.Hv, h, t0, T, lane, gv, bv);
+      float nea = 0.f, dtb = 0.f;
+      if (kRawGates) {
+        nea = -expf(a.gate.A_log[h]);
+        dtb = a.gate.dt_bias[h];
+      }
+      finish_gb<kRawGates>(nea, dtb, t0, T, lane, gv, bv);
+      chunk_vectors(V.cv, gv, bv, lane);
+    }
+    __syncwarp();
+    bool ok = bar_wait(&V.bar_ld, ph_ld);
+    ph_ld ^= 1u;
+    if (__syncthreads_or(!ok)) {
+      if (tid == 0) {
+        atomicOr(a.err, kErrTimeout);
+        V.abort = 1;
+      }
+      break;
+    }
+    if (tid == 0) ld_pending = false;
+    if (c.n == 0) {  // rows before the sequence's first token: the carried window, or zeros
+      if (tid < 48) {
+        const int rw = tid >> 4, g8 = tid & 15;
+        *reinterpret_cast<uint4 *>(sm + P_RAW + 256 * rw + 16 * g8) =
+            conv0 ? *reinterpret_cast<const uint4 *>(conv0 + ((long long)c.b * 3 + rw) * C + cv + 8 * g8)
+                  : make_uint4(0u, 0u, 0u, 0u);
+      }
+      __syncthreads();
+    }
+    // MMA1 (warp 0): [K;Q] K^T -> K K^T (lanes 0-63), Q K^T (lanes 64-127)
+    const uint32_t kq = sbase + P_KQ;
+    if (warp == 0) {
+      fence_after();
+      issue_w(tmem + TP_KQ, id_kk, 8, false, [&](int ks) { return desc_k(kq, ks, 128); },
+              [&](int ks) { return desc_k(kq, ks, 128); });
+      commit_w(&V.bar_qk);
+    }
+    // The v tiles (every warp): row v = lrow, tokens 32 half .. 32 half + 31;
+    // conv + SiLU, zero past the sequence, fp16 hi/lo pairs into TMEM (the A
+    // operand of MMA U: lane = v, column c = tokens 2c, 2c + 1).
+    {
+      const bf16 *raw = reinterpret_cast<const bf16 *>(sm + P_RAW);
+      const float4 w4 = ld_io4(conv_w + 4 * (cv + lrow));
+      const int j0 = 32 * half;
+      float x0 = __bfloat162float(raw[(j0 + 0) * kD + lrow]);
+      float x1 = __bfloat162float(raw[(j0 + 1) * kD + lrow]);
+      float x2 = __bfloat162float(raw[(j0 + 2) * kD + lrow]);
+      uint32_t wh[16], wl[16];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        float u[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int j = j0 + 2 * q + e;
+          const float x3 = __bfloat162float(raw[(j + 3) * kD + lrow]);
+          float acc = w4.x * x0;
+          acc = fmaf(w4.y, x1, acc);
+          acc = fmaf(w4.z, x2, acc);
+          acc = fmaf(w4.w, x3, acc);
+          u[e] = t0 + j < T ? silu1(acc) : 0.f;
+          x0 = x1;
+          x1 = x2;
+          x2 = x3;
+        }
+        split2(u[0], u[1], wh[q], wl[q]);
+      }
+      tmem_st16w_nw(tl + TP_V + 16 * half, wh);
+      tmem_st16w_nw(tl + TP_V + 32 + 16 * half, wl);
+      tmem_wait_st();
+    }
+    fence_before();
+    __syncthreads();  // the v rows are read: L may take their space
+    ok = bar_wait(&V.bar_qk, ph_qk);
+    ph_qk ^= 1u;
+    fence_after();
+    if (__syncthreads_or(!ok)) {
+      if (tid == 0) {
+        atomicOr(a.err, kErrTimeout);
+        V.abort = 1;
+      }
+      break;
+    }
+    // L (fp32, strictly lower, decayed beta K K^T) and M (fp16, decayed Q K^T incl. the diagonal)
+    {
+      const ChunkVecs &CV = V.cv;
+      float v[32], rr[32];
+      tmem_ld32(tl + TP_KQ + 32 * half, v);
+      const int j0 = 32 * half;
+      const int i = lrow < kC ? lrow : lrow - kC;
+      if (CV.mild) {
+        const float di = CV.d[i];
+#pragma unroll
+        for (int q = 0; q < 32; q += 4) {
+          const float4 dv = ld4(CV.dinv + j0 + q);
+          const float2 r01 = __fmul2_rn(make_float2(di, di), make_float2(dv.x, dv.y));
+          const float2 r23 = __fmul2_rn(make_float2(di, di), make_float2(dv.z, dv.w));
+          rr[q] = r01.x;
+          rr[q + 1] = r01.y;
+          rr[q + 2] = r23.x;
+          rr[q + 3] = r23.y;
+        }
+      } else {
+        const float gi = CV.G[i];
+#pragma unroll
+        for (int q = 0; q < 32; ++q) rr[q] = __expf(gi - CV.G[j0 + q]);
+      }
+      if (lrow < kC) {
+        const float bi = CV.beta[i];
+        float *L = reinterpret_cast<float *>(sm + P_RAW) + i * kLs + j0;
+#pragma unroll
+        for (int q = 0; q < 32; q += 4) {
+          const float2 p01 =
+              __fmul2_rn(__fmul2_rn(make_float2(bi, bi), make_float2(v[q], v[q + 1])), make_float2(rr[q], rr[q + 1]));
+          const float2 p23 = __fmul2_rn(__fmul2_rn(make_float2(bi, bi), make_float2(v[q + 2], v[q + 3])),
+                                        make_float2(rr[q + 2], rr[q + 3]));
+          float4 f;
+          f.x = (j0 + q + 0 < i) ? p01.x : 0.f;
+          f.y = (j0 + q + 1 < i) ? p01.y : 0.f;
+          f.z = (j0 + q + 2 < i) ? p23.x : 0.f;
+          f.w = (j0 + q + 3 < i) ? p23.y : 0.f;
+          *reinterpret_cast<float4 *>(L + q) = f;
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 32; q += 2) {
+          const float2 p = __fmul2_rn(make_float2(v[q], v[q + 1]), make_float2(rr[q], rr[q + 1]));
+          v[q] = (j0 + q <= i) ? p.x : 0.f;
+          v[q + 1] = (j0 + q + 1 <= i) ? p.y : 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) st_h8_inrange(sm + P_M + kmaj(i, j0 + 8 * q, kC), v + 8 * q);  // |M| <= q_scale
+      }
+    }
+    fence_smem_to_async();
+    __syncthreads();  // L and M written; MMA1 is done with [K;Q]'s q^ rows (the T scratch goes there)
+    if (tid == 0) {
+      tma_store_2d(&tm_m, sbase + P_M, 0, (int)(item * kC));
+      bulk_commit();
+      stores = true;
+    }
+    // T = (I + L)^{-1} and the fp16 tiles (the upper blocks of T B hi / lo are
+    // zeroed again: the -W^T staging of the previous item used their space)
+    solve_T(ss, V.cv, tid, kBarSolve, true);
+    fence_smem_to_async();
+    fence_before();
+    __syncthreads();
+    // MMA U (hi*hi + lo*hi + hi*lo, A = V^T from TMEM) and MMA W (warp 0)
+    if (warp == 0) {
+      fence_after();
+      auto b_tu = [&](int ks) { return desc_k(sbase + P_TU, ks, kC); };
+      issue_ta_w(tmem + TP_U, tmem + TP_V, id_kk, 4, false, b_tu);
+      issue_ta_w(tmem + TP_U, tmem + TP_V + 32, id_kk, 4, true, b_tu);
+      issue_ta_w(tmem + TP_U, tmem + TP_V, id_kk, 4, true, [&](int ks) { return desc_k(sbase + P_TUL, ks, kC); });
+      issue_w(tmem + TP_W, id_mk, 4, false, [&](int ks) { return desc(kq + (uint32_t)(ks * 2048), 128 * 128, 1024); },
+              [&](int ks) { return desc_k(sbase + P_TW, ks, kC); });
+      commit_w(&V.bar_uw);
+    }
+    if (tid < 2 * kC) {  // the chunk vectors d and Gamma, fp32 [2][64]
+      float *vec = s.ws_vec + item * (2 * kC);
+      vec[tid] = tid < kC ? V.cv.d[tid] : V.cv.gam[tid - kC];
+    }
+    __syncwarp();
+    ok = bar_wait(&V.bar_uw, ph_uw);
+    ph_uw ^= 1u;
+    fence_after();
+    if (__syncthreads_or(!ok)) {
+      if (tid == 0) {
+        atomicOr(a.err, kErrTimeout);
+        V.abort = 1;
+      }
+      break;
+    }
+    {
+      // U^T [v][i] fp32 -> staging box `half` (rows v, 32 values of 4 bytes, 128-byte swizzle)
+      float v[32];
+      tmem_ld32(tl + TP_U + 32 * half, v);
+      uint8_t *box = sm + (half == 0 ? P_RAW : P_TF) + lrow * 128;
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        *reinterpret_cast<float4 *>(box + ((q ^ (lrow & 7)) << 4)) =
+            make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      // -W^T [k][i] -> fp16 MN-major (the B operand layout of MMA4)
+      tmem_ld32(tl + TP_W + 32 * half, v);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) st_h8_inrange(sm + P_NW + mnmaj(32 * half + 8 * q, lrow, kD), v + 8 * q);
+    }
+    fence_smem_to_async();
+    fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      tma_store_2d(&tm_u, sbase + P_RAW, 0, (int)(item * kD));
+      tma_store_2d(&tm_u, sbase + P_TF, 32, (int)(item * kD));
+      tma_store_2d(&tm_nw, sbase + P_NW, 0, (int)(item * kD));
+      bulk_commit();
+    }
+  }
+  // Before the CTA ends: the stores complete, no load still lands, and no MMA
+  // still writes TMEM (after an early exit).
+  if (tid == 0) {
+    bulk_wait_all();
+    if (ld_pending) bar_wait(&V.bar_ld, ph_ld);
+  }
+  fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    fence_after();
+    tmem_dealloc(tmem, kPrepTmem);
+  }
+}
+
+// =============================================================================
+// prefill_seq_kernel
+// =============================================================================
+constexpr int kSeqThreads = 384;
+// One stage (a chunk's tiles), offsets within the stage; fp16, 128-byte swizzle.
+constexpr uint32_t Q_Q = 0;         // q^ K-major [i][k] (64 rows, k halves 8 KB apart)   16 KB
+constexpr uint32_t Q_KH = 16384;    // k^ hi [j][k]                                       16 KB
+constexpr uint32_t Q_KL = 32768;    // k^ lo [j][k]                                       16 KB
+constexpr uint32_t Q_NW = 49152;    // -W^T MN-major [k][j]                               16 KB
+constexpr uint32_t Q_M = 65536;     // M K-major [i][j]                                    8 KB
+constexpr uint32_t kStage = 73728;
+constexpr uint32_t kStageTx = 3 * 16384 + 16384 + 8192 + 2 * kC * 4;  // tiles + the vectors
+constexpr uint32_t S_U = 2 * kStage;          // U^T fp32, two boxes [128 v][32] (128-byte swizzle)  32 KB
+constexpr uint32_t S_Z = S_U + 32768;         // z rows bf16 [64][128]                                16 KB
+constexpr uint32_t S_OST = S_Z + 16384;       // O staging fp32 [64 i][128 v]                         32 KB
+constexpr uint32_t S_VEC = S_OST + 32768;     // d, Gamma of the two stages, fp32 [2][2][64]            1 KB
+constexpr uint32_t S_BAR = S_VEC + 1024;
+struct SeqShared {
+  uint64_t full[2];  // a stage's tiles and vectors landed
+  uint64_t bar_u;    // U^T landed
+  uint64_t bar_z;    // z rows landed
+  uint64_t bar_d;    // MMA4 done
+  uint64_t bar_o;    // MMA5 and MMA6 done
+  uint64_t bar_s;    // MMA7 done
+  uint64_t bar_ofree;  // the epilogue has read O1, O2 (one arrival per chunk)
+  uint64_t bar_end;
+  uint32_t tmem;
+  int abort;
+  int req_full[2], req_u, req_z;  // requests issued (each completes one phase)
+};
+constexpr uint32_t kSeqSmem = S_BAR + ((sizeof(SeqShared) + 127) / 128) * 128 + 1024;
+static_assert(kSeqSmem <= 232448, "shared memory per CTA");
+static_assert(S_U % 1024 == 0 && S_Z % 128 == 0 && kStage % 1024 == 0, "TMA destinations");
+// TMEM columns (512 allocated).
+constexpr uint32_t TS_S = 0;      // state fp32 [v][k]                  128
+constexpr uint32_t TS_O1 = 128;   // S Q^T [v][i]                        64
+constexpr uint32_t TS_O2 = 192;   // Delta^T M^T [v][i]                  64
+constexpr uint32_t TS_D = 256;    // S (-W^T) [v][j]                     64
+constexpr uint32_t TS_DG = 320;   // (Delta Gamma)^T fp16: hi 320..351, lo 352..383
+constexpr uint32_t TS_DH = 384;   // Delta^T fp16 hi                     32
+constexpr uint32_t TS_S16 = 448;  // state fp16 pairs [v][k/2]           64
+constexpr uint32_t kSeqTmem = 512;
+constexpr int kBarChain = 2;  // warps 8-11
+constexpr int kBarEpi = 3;    // warps 0-7
+
+// The gated RMSNorm (node gdn.norm) of NR tokens i0, i0 + di, ... of the chunk,
+// one half-warp per token (8 channels per lane), from the O staging and the
+// staged z rows, to o (valid tokens only).
+template <int NR>
+__device__ __forceinline__ void gated_norm(const uint8_t *sm, const bf16 *norm_w, bf16 *o, const Dims &d, long long bos,
+                                           int h, int t0, int T, int i0, int di, int lane) {
+  const float *ost = reinterpret_cast<const float *>(sm + S_OST);
+  const int hl = lane & 15;
+  float2 wn[4];
+  widen(*reinterpret_cast<const uint4 *>(norm_w + 8 * hl), wn);
+  const int nv = min(kC, T - t0);
+  bf16 *ob = o + ((bos + t0) * d.Hv + h) * kD + 8 * hl;
+  const long long ostride = (long long)d.Hv * kD;
+#pragma unroll
+  for (int m = 0; m < NR; ++m) {
+    const int i = i0 + di * m;
+    const bool valid = i < nv;
+    float4 o0 = make_float4(0.f, 0.f, 0.f, 0.f), o1 = o0;
+    uint4 zr = make_uint4(0u, 0u, 0u, 0u);
+    if (valid) {
+      o0 = ld4(ost + i * kD + 8 * hl);
+      o1 = ld4(ost + i * kD + 8 * hl + 4);
+      zr = *reinterpret_cast<const uint4 *>(sm + S_Z + i * kD * 2 + 16 * hl);
+    }
+    float ss = dot4(o0, o0) + dot4(o1, o1);
+#pragma unroll
+    for (int off = 1; off < 16; off <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    const float rstd = rsqrtf(ss * (1.0f / kD) + d.eps_norm);
+    float2 zz[4];
+    widen(zr, zz);
+    const float2 op[4] = {make_float2(o0.x, o0.y), make_float2(o0.z, o0.w), make_float2(o1.x, o1.y),
+                          make_float2(o1.z, o1.w)};
+    uint32_t yw[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 sg = silu2(zz[q]);
+      const float2 y = __fmul2_rn(__fmul2_rn(wn[q], __fmul2_rn(op[q], make_float2(rstd, rstd))), sg);
+      __nv_bfloat162 t = __floats2bfloat162_rn(y.x, y.y);
+      yw[q] = *reinterpret_cast<uint32_t *>(&t);
+    }
+    if (valid) *reinterpret_cast<uint4 *>(ob + i * ostride) = make_uint4(yw[0], yw[1], yw[2], yw[3]);
+  }
+}
+
+__global__ void __launch_bounds__(kSeqThreads, 1)
+    prefill_seq_kernel(const PrefillArgs a, const SplitArgs s, const __grid_constant__ CUtensorMap tm_qk,
+                       const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_u,
+                       const __grid_constant__ CUtensorMap tm_nw, const __grid_constant__ CUtensorMap tm_m) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  SeqShared &V = *reinterpret_cast<SeqShared *>(sm + S_BAR);
+  const Dims d = a.d;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int h = blockIdx.x % d.Hv;
+  int b = blockIdx.x / d.Hv;
+  const int r = d.Hv / d.Hk, kh = h / r;
+  const long long C = d.C;
+  const uint32_t sbase = smem_u32(sm);
+  if (a.cu_seqlens && d.B <= kLongestFirstMax)  // packed: the longest sequences first
+    b = longest_first(a.cu_seqlens, d.B, b, reinterpret_cast<int *>(sm + S_OST));
+  long long bos;
+  int T;
+  if (a.cu_seqlens) {
+    const int lo = a.cu_seqlens[b], hi = a.cu_seqlens[b + 1];
+    if (lo < 0 || hi < lo || hi > d.T) {  // unusable offsets: leave this sequence untouched
+      if (tid == 0) atomicOr(a.err, kErrSeqlens);
+      return;
+    }
+    bos = lo;
+    T = hi - lo;
+  } else {
+    bos = (long long)b * d.T;
+    T = d.T;
+  }
+  const long long unit_off = ((long long)b * d.Hv + h) * kD * kD;
+  const bf16 *x = static_cast<const bf16 *>(a.qkv_pre) + bos * C;
+  const bf16 *conv0 = a.conv0 ? static_cast<const bf16 *>(a.conv0) + (long long)b * 3 * C : nullptr;
+  const int cq = kh * kD, ck = d.Hk * kD + kh * kD, cvv = 2 * d.Hk * kD + h * kD;
+
+  // The carried conv window: the last three raw rows of the channels this CTA owns.
+  auto write_conv_T = [&]() {
+    bf16 *cT = static_cast<bf16 *>(a.conv_T) + (long long)b * 3 * C;
+    const bool own_qk = (h % r) == 0;
+    for (int idx = tid; idx < 3 * 3 * kD; idx += kSeqThreads) {
+      const int e = idx / (3 * kD), rem = idx % (3 * kD), blk = rem / kD, ch = rem % kD;
+      if (blk < 2 && !own_qk) continue;
+      const long long cc = (blk == 0 ? cq : blk == 1 ? ck : cvv) + ch;
+      const int t = T - 3 + e;
+      bf16 val;
+      if (t >= 0) val = x[(long long)t * C + cc];
+      else if (conv0) val = conv0[(long long)(3 + t) * C + cc];
+      else val = bf16(0.f);
+      cT[(long long)e * C + cc] = val;
+    }
+  };
+  if (T == 0) {  // an empty packed sequence: state and window pass through
+    float4 *dst = reinterpret_cast<float4 *>(a.S_T + unit_off);
+    const float4 *src = a.S0 ? reinterpret_cast<const float4 *>(a.S0 + unit_off) : nullptr;
+    if (src != dst)
+      for (int i = tid; i < kD * kD / 4; i += kSeqThreads) dst[i] = src ? src[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    write_conv_T();
+    return;
+  }
+  const int nch = (T + kC - 1) / kC;
+  auto item_of = [&](int n) -> long long { return (long long)slot_of(s, b, (int)bos, n) * d.Hv + h; };
+
+  if (tid == 0) {
+    bar_init(&V.full[0], 1);
+    bar_init(&V.full[1], 1);
+    bar_init(&V.bar_u, 1);
+    bar_init(&V.bar_z, 1);
+    bar_init(&V.bar_d, 1);
+    bar_init(&V.bar_o, 1);
+    bar_init(&V.bar_s, 1);
+    bar_init(&V.bar_ofree, 1);
+    bar_init(&V.bar_end, 1);
+    V.abort = 0;
+    V.req_full[0] = V.req_full[1] = V.req_u = V.req_z = 0;
+  }
+  if (warp == 0) tmem_alloc(&V.tmem, kSeqTmem);
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = V.tmem;
+
+  // One thread each: a chunk's stage; U^T of a chunk; z rows of a chunk.
+  auto request_stage = [&](int n) {
+    const int st = n & 1;
+    const uint32_t sb = sbase + st * kStage;
+    const long long it = item_of(n);
+    uint64_t *bar = &V.full[st];
+    bar_expect_tx(bar, kStageTx);
+#pragma unroll
+    for (int at = 0; at < 2; ++at) {
+      tma_load_3d(sb + Q_Q + at * 8192, &tm_qk, kh * kD + 64 * at, (int)(bos + kC * n), 0, bar);
+      tma_load_3d(sb + Q_KH + at * 8192, &tm_qk, kh * kD + 64 * at, (int)(bos + kC * n), 1, bar);
+      tma_load_3d(sb + Q_KL + at * 8192, &tm_qk, kh * kD + 64 * at, (int)(bos + kC * n), 2, bar);
+    }
+    tma_load_2d(sb + Q_NW, &tm_nw, 0, (int)(it * kD), bar);
+    tma_load_2d(sb + Q_M, &tm_m, 0, (int)(it * kC), bar);
+    bulk_load(sbase + S_VEC + st * 512, s.ws_vec + it * (2 * kC), 2 * kC * 4, bar);
+    V.req_full[st] += 1;
+  };
+  auto request_u = [&](int n) {
+    const long long it = item_of(n);
+    bar_expect_tx(&V.bar_u, 32768);
+    tma_load_2d(sbase + S_U, &tm_u, 0, (int)(it * kD), &V.bar_u);
+    tma_load_2d(sbase + S_U + 16384, &tm_u, 32, (int)(it * kD), &V.bar_u);
+    V.req_u += 1;
+  };
+  auto request_z = [&](int n) {
+    bar_expect_tx(&V.bar_z, kC * kD * 2);
+    tma_load_3d(sbase + S_Z, &tm_z, h * kD, (int)(bos + kC * n), 0, &V.bar_z);
+    V.req_z += 1;
+  };
+  if (tid == 0) {
+    request_stage(0);
+    if (nch > 1) request_stage(1);
+    request_u(0);
+    request_z(0);
+  }
+  const float *vec_d[2] = {reinterpret_cast<const float *>(sm + S_VEC), reinterpret_cast<const float *>(sm + S_VEC + 512)};
+
+  if (warp >= 8) {
+    // ------------------------------------------------ the chain (warps 8-11)
+    const int quad = warp - 8;
+    const int lrow = 32 * quad + lane;  // state row v of this thread
+    const uint32_t tl = tmem + ((uint32_t)(32 * quad) << 16);
+    const bool issuer = warp == 8;
+    const uint32_t id_kk = idesc(128, 64, 0, 0), id_km = idesc(128, 64, 0, 1), id_km128 = idesc(128, 128, 0, 1);
+    bool ok = true;
+    // e^{G_last} of chunk n (the decay the state takes at chunk n's start),
+    // read from the workspace two chunks ahead of its use.
+    auto dc_of = [&](int n) -> float { return n < nch ? s.ws_vec[item_of(n) * (2 * kC) + kC - 1] : 1.f; };
+    const float dc0 = dc_of(0);
+    float dc_n1 = dc_of(1), dc_n2 = dc_of(2);
+    {
+      // Initial state: TMEM fp32 <- d_C(chunk 0) S0, fp16 copy <- S0.
+#pragma unroll 1
+      for (int k0 = 0; k0 < kD; k0 += 32) {
+        float v[32];
+        if (a.S0) {
+          const float4 *src = reinterpret_cast<const float4 *>(a.S0 + unit_off + (long long)lrow * kD + k0);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 f = src[q];
+            v[4 * q] = f.x;
+            v[4 * q + 1] = f.y;
+            v[4 * q + 2] = f.z;
+            v[4 * q + 3] = f.w;
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < 32; ++q) v[q] = 0.f;
+        }
+        uint32_t w16[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) w16[q] = pack2_sat(v[2 * q], v[2 * q + 1]);
+        tmem_st16w_nw(tl + TS_S16 + k0 / 2, w16);
+#pragma unroll
+        for (int q = 0; q < 32; ++q) v[q] *= dc0;
+        tmem_st32(tl + TS_S + k0, v);
+      }
+      tmem_wait_st();
+      fence_before();
+      named_sync(kBarChain, 128);
+      for (int n = 0; n < nch; ++n) {
+        const int st = n & 1;
+        const uint32_t sb = sbase + st * kStage;
+        if (*reinterpret_cast<volatile int *>(&V.abort)) break;
+        // MMA4 D = S (-W^T), MMA5 O1 = S Q^T, once the chunk's tiles and U^T
+        // are in and the epilogue has read the previous chunk's O1, O2; the
+        // next chunk's stage is then requested into the previous chunk's buffer.
+        __syncwarp();
+        bool w = bar_wait(&V.full[st], (uint32_t)(n >> 1) & 1u);
+        w = bar_wait(&V.bar_u, (uint32_t)n & 1u) && w;
+        if (issuer && n > 0) w = bar_wait(&V.bar_ofree, (uint32_t)(n - 1) & 1u) && w;
+        ok = w;
+        if (named_sync_or(kBarChain, 128, !ok)) break;
+        if (issuer) {
+          if (lane == 0 && n > 0 && n + 1 < nch) request_stage(n + 1);
+          __syncwarp();
+          fence_after();
+          issue_ta_w(tmem + TS_D, tmem + TS_S16, id_km, 8, false, [&](int ks) { return desc_mn(sb + Q_NW, ks, kD); });
+          commit_w(&V.bar_d);
+          issue_ta_w(tmem + TS_O1, tmem + TS_S16, id_kk, 8, false, [&](int ks) { return desc_k(sb + Q_Q, ks, kC); });
+        }
+        // Delta^T = D + U^T -> fp16 hi (MMA6) and (Delta Gamma)^T hi / lo (MMA7)
+        __syncwarp();
+        ok = bar_wait(&V.bar_d, (uint32_t)n & 1u);
+        fence_after();
+        if (named_sync_or(kBarChain, 128, !ok)) break;
+        {
+          const float *gam = vec_d[st] + kC;
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            float dv[32];
+            tmem_ld32(tl + TS_D + 32 * hf, dv);
+            const uint8_t *ub = sm + S_U + hf * 16384 + lrow * 128;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const float4 u4 = *reinterpret_cast<const float4 *>(ub + ((q ^ (lrow & 7)) << 4));
+              dv[4 * q] += u4.x;
+              dv[4 * q + 1] += u4.y;
+              dv[4 * q + 2] += u4.z;
+              dv[4 * q + 3] += u4.w;
+            }
+            uint32_t wh[16], gh[16], gl[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) wh[q] = pack2_inrange(dv[2 * q], dv[2 * q + 1]);
+#pragma unroll
+            for (int q = 0; q < 32; q += 4) {  // times e^{G_last - G_j} <= 1
+              const float4 g = ld4(gam + 32 * hf + q);
+              const float2 p01 = __fmul2_rn(make_float2(dv[q], dv[q + 1]), make_float2(g.x, g.y));
+              const float2 p23 = __fmul2_rn(make_float2(dv[q + 2], dv[q + 3]), make_float2(g.z, g.w));
+              split2_inrange(p01.x, p01.y, gh[q / 2], gl[q / 2]);
+              split2_inrange(p23.x, p23.y, gh[q / 2 + 1], gl[q / 2 + 1]);
+            }
+            tmem_st16w_nw(tl + TS_DH + 16 * hf, wh);
+            tmem_st16w_nw(tl + TS_DG + 16 * hf, gh);
+            tmem_st16w_nw(tl + TS_DG + 32 + 16 * hf, gl);
+          }
+          tmem_wait_st();
+        }
+        fence_before();
+        named_sync(kBarChain, 128);
+        // U^T is read: the next chunk's may land.  MMA6, MMA7 (issuer).
+        if (warp == 9 && lane == 0 && n + 1 < nch) request_u(n + 1);
+        if (issuer) {
+          fence_after();
+          issue_ta_w(tmem + TS_O2, tmem + TS_DH, id_kk, 4, false, [&](int ks) { return desc_k(sb + Q_M, ks, kC); });
+          commit_w(&V.bar_o);
+          auto b_kh = [&](int ks) { return desc(sb + Q_KH + (uint32_t)(ks * 2048), 8192, 1024); };
+          issue_ta_w(tmem + TS_S, tmem + TS_DG, id_km128, 4, true, b_kh);
+          issue_ta_w(tmem + TS_S, tmem + TS_DG, id_km128, 4, true,
+                     [&](int ks) { return desc(sb + Q_KL + (uint32_t)(ks * 2048), 8192, 1024); });
+          issue_ta_w(tmem + TS_S, tmem + TS_DG + 32, id_km128, 4, true, b_kh);
+          commit_w(&V.bar_s);
+        }
+        // The state pass: the fp16 copy and the rescale by the next chunk's
+        // decay, or S_T after the last chunk.
+        const bool last = n + 1 == nch;
+        const float dcn = dc_n1;
+        dc_n1 = dc_n2;
+        dc_n2 = dc_of(n + 3);
+        __syncwarp();
+        ok = bar_wait(&V.bar_s, (uint32_t)n & 1u);
+        fence_after();
+        if (named_sync_or(kBarChain, 128, !ok)) break;
+#pragma unroll 1
+        for (int k0 = 0; k0 < kD; k0 += 64) {
+          uint32_t r0[32], r1[32];
+          tmem_ld32_nw(tl + TS_S + k0, r0);
+          tmem_ld32_nw(tl + TS_S + k0 + 32, r1);
+          tmem_wait_ld();
+          if (last) {
+            float4 *dst = reinterpret_cast<float4 *>(a.S_T + unit_off + (long long)lrow * kD + k0);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              dst[q] = make_float4(__uint_as_float(r0[4 * q]), __uint_as_float(r0[4 * q + 1]),
+                                   __uint_as_float(r0[4 * q + 2]), __uint_as_float(r0[4 * q + 3]));
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              dst[8 + q] = make_float4(__uint_as_float(r1[4 * q]), __uint_as_float(r1[4 * q + 1]),
+                                       __uint_as_float(r1[4 * q + 2]), __uint_as_float(r1[4 * q + 3]));
+          } else {
+            uint32_t w16[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) w16[q] = pack2_inrange(__uint_as_float(r0[2 * q]), __uint_as_float(r0[2 * q + 1]));
+            tmem_st16w_nw(tl + TS_S16 + k0 / 2, w16);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) w16[q] = pack2_inrange(__uint_as_float(r1[2 * q]), __uint_as_float(r1[2 * q + 1]));
+            tmem_st16w_nw(tl + TS_S16 + k0 / 2 + 16, w16);
+#pragma unroll
+            for (int q = 0; q < 32; q += 2) {
+              const float2 x0 = __fmul2_rn(make_float2(__uint_as_float(r0[q]), __uint_as_float(r0[q + 1])), make_float2(dcn, dcn));
+              const float2 x1 = __fmul2_rn(make_float2(__uint_as_float(r1[q]), __uint_as_float(r1[q + 1])), make_float2(dcn, dcn));
+              r0[q] = __float_as_uint(x0.x);
+              r0[q + 1] = __float_as_uint(x0.y);
+              r1[q] = __float_as_uint(x1.x);
+              r1[q + 1] = __float_as_uint(x1.y);
+            }
+            tmem_st32w_nw(tl + TS_S + k0, r0);
+            tmem_st32w_nw(tl + TS_S + k0 + 32, r1);
+            tmem_wait_st();
+          }
+        }
+        fence_before();
+        named_sync(kBarChain, 128);
+      }
+      if (!ok && tid == 256) {
+        atomicOr(a.err, kErrTimeout);
+        V.abort = 1;
+      }
+    }
+  } else {
+    // ------------------------------------------- the epilogue (warps 0-7)
+    const int quad = warp & 3, half = warp >> 2;
+    const int lrow = 32 * quad + lane;
+    const uint32_t tl = tmem + ((uint32_t)(32 * quad) << 16);
+    bool ok = true;
+    for (int n = 0; n < nch; ++n) {
+      const int st = n & 1;
+      if (*reinterpret_cast<volatile int *>(&V.abort)) break;
+      __syncwarp();
+      ok = bar_wait(&V.bar_o, (uint32_t)n & 1u);
+      ok = bar_wait(&V.full[st], (uint32_t)(n >> 1) & 1u) && ok;  // this stage's vectors (long landed)
+      fence_after();
+      if (named_sync_or(kBarEpi, 256, !ok)) break;
+      {  // O^T = d (S Q^T) + Delta^T M^T -> staging [i][v]
+        float *ost = reinterpret_cast<float *>(sm + S_OST);
+        uint32_t ra[32], rb[32];
+        tmem_ld32_nw(tl + TS_O1 + 32 * half, ra);
+        tmem_ld32_nw(tl + TS_O2 + 32 * half, rb);
+        tmem_wait_ld();
+        const float *dq = vec_d[st] + 32 * half;
+#pragma unroll
+        for (int q = 0; q < 32; q += 4) {
+          const float4 dd = ld4(dq + q);
+          const float2 o01 = __ffma2_rn(make_float2(dd.x, dd.y), make_float2(__uint_as_float(ra[q]), __uint_as_float(ra[q + 1])),
+                                        make_float2(__uint_as_float(rb[q]), __uint_as_float(rb[q + 1])));
+          const float2 o23 = __ffma2_rn(make_float2(dd.z, dd.w),
+                                        make_float2(__uint_as_float(ra[q + 2]), __uint_as_float(ra[q + 3])),
+                                        make_float2(__uint_as_float(rb[q + 2]), __uint_as_float(rb[q + 3])));
+          ost[(32 * half + q + 0) * kD + lrow] = o01.x;
+          ost[(32 * half + q + 1) * kD + lrow] = o01.y;
+          ost[(32 * half + q + 2) * kD + lrow] = o23.x;
+          ost[(32 * half + q + 3) * kD + lrow] = o23.y;
+        }
+      }
+      fence_before();
+      named_sync(kBarEpi, 256);
+      if (tid == 0) mbar_arrive(&V.bar_ofree);  // O1, O2 and this stage's vectors are read
+      __syncwarp();
+      ok = bar_wait(&V.bar_z, (uint32_t)n & 1u);
+      if (named_sync_or(kBarEpi, 256, !ok)) break;
+      gated_norm<4>(sm, static_cast<const bf16 *>(a.norm_w), static_cast<bf16 *>(a.o), d, bos, h, kC * n, T,
+                    2 * warp + (lane >> 4), 16, lane);
+      named_sync(kBarEpi, 256);  // z and the staging are read
+      if (tid == 0 && n + 1 < nch) request_z(n + 1);
+    }
+    if (!ok && tid == 0) {
+      atomicOr(a.err, kErrTimeout);
+      V.abort = 1;
+    }
+  }
+
+  write_conv_T();
+  // Before the CTA ends: no copy still landing in shared memory and no MMA
+  // still writing TMEM (after an early exit; on a normal exit every request
+  // was consumed and every MMA waited for).
+  fence_before();
+  __syncthreads();
+  if (tid == 256) {
+    for (int st = 0; st < 2; ++st)
+      if (V.req_full[st] > 0) bar_wait(&V.full[st], (uint32_t)(V.req_full[st] - 1) & 1u);
+    if (V.req_u > 0) bar_wait(&V.bar_u, (uint32_t)(V.req_u - 1) & 1u);
+    if (V.req_z > 0) bar_wait(&V.bar_z, (uint32_t)(V.req_z - 1) & 1u);
+    commit(&V.bar_end);
+    bar_wait(&V.bar_end, 0);
+  }
+  fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    fence_after();
+    tmem_dealloc(tmem, kSeqTmem);
+  }
+}
+
+// ---- tensor maps -------------------------------------------------------------
+bool encode_2d(CUtensorMap *m, void *base, CUtensorMapDataType dt, int esize, long long inner, long long rows,
+               int box_inner, int box_rows, CUtensorMapSwizzle sw) {
+  EncodeTiled enc = encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)(inner * esize)};
+  const cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, dt, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+// A token-major [rows][width] bf16 tensor with boxes of 128 columns x box_rows rows.
+bool encode_rows(CUtensorMap *m, const void *base, long long width, long long rows, int box_rows) {
+  EncodeTiled enc = encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)rows, 1};
+  const cuuint64_t strides[2] = {(cuuint64_t)width * 2, (cuuint64_t)width * 2 * rows};
+  const cuuint32_t box[3] = {(cuuint32_t)kD, (cuuint32_t)box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+// The staged q^ / k^ [3][rows][Hk*128] fp16 with 128-byte-swizzled 64 x 64 boxes.
+bool encode_qk(CUtensorMap *m, void *base, int Hk, long long rows) {
+  EncodeTiled enc = encoder();
+  if (!enc) return false;
+  const long long width = (long long)Hk * kD;
+  const cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)rows, 3};
+  const cuuint64_t strides[2] = {(cuuint64_t)width * 2, (cuuint64_t)width * 2 * rows};
+  const cuuint32_t box[3] = {64, (cuuint32_t)kC, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct SplitMaps {
+  CUtensorMap u, nw, m;
+};
+bool encode_split(SplitMaps *mp, const SplitArgs &s, long long nitems) {
+  return encode_2d(&mp->u, s.ws_u, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 2 * 32, nitems * kD, 32, kD,
+                   CU_TENSOR_MAP_SWIZZLE_128B) &&
+         encode_2d(&mp->nw, s.ws_nw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, 64, nitems * kD, 64, kD,
+                   CU_TENSOR_MAP_SWIZZLE_128B) &&
+         encode_2d(&mp->m, s.ws_m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, 64, nitems * kC, 64, kC,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+}  // namespace
+
+long long split_items(const Dims &d, long long tokens, bool packed, int *nslots, int *nch) {
+  const long long T = d.T;
+  const long long ch = (T + kC - 1) / kC;
+  const long long slots = packed ? (tokens >> 6) + d.B + 2 : (long long)d.B * ch;
+  *nch = (int)ch;
+  *nslots = (int)slots;
+  return slots * d.Hv;
+}
+
+cudaError_t launch_prefill_split(const PrefillArgs &a, const SplitArgs &s, cudaStream_t st) {
+  if (!a.qk_ws || !a.conv_w) return cudaErrorInvalidValue;
+  const long long rows = a.cu_seqlens ? (long long)a.d.T : (long long)a.d.B * a.d.T;
+  const long long nitems = (long long)s.nslots * a.d.Hv;
+  if (nitems * kD >= (1LL << 31) || rows > 0x7fffffffLL - 2 * kC) return cudaErrorInvalidValue;
+  CUtensorMap tm_qkv, tm_z, tm_qk;
+  SplitMaps mp;
+  if (!encode_rows(&tm_qkv, a.qkv_pre, a.d.C, rows, kRawRows) ||
+      !encode_rows(&tm_z, a.z, (long long)a.d.Hv * kD, rows, kC) || !encode_qk(&tm_qk, a.qk_ws, a.d.Hk, rows) ||
+      !encode_split(&mp, s, nitems))
+    return cudaErrorInvalidValue;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const bool raw = a.gate.g == nullptr;
+  auto prep = raw ? prefill_prep_kernel<true> : prefill_prep_kernel<false>;
+  e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem);
+  if (e != cudaSuccess) return e;
+  long long grid = 2LL * sms;
+  if (grid > nitems) grid = nitems;
+  if (grid < 1) grid = 1;
+  prep<<<(unsigned)grid, kPrepThreads, kPrepSmem, st>>>(a, s, tm_qkv, tm_qk, mp.u, mp.nw, mp.m);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(prefill_seq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSeqSmem);
+  if (e != cudaSuccess) return e;
+  prefill_seq_kernel<<<(unsigned)(a.d.B * a.d.Hv), kSeqThreads, kSeqSmem, st>>>(a, s, tm_qk, tm_z, mp.u, mp.nw, mp.m);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

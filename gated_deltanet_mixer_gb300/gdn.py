@@ -94,6 +94,8 @@ def lib():
         L.gdn_prefill_static.argtypes = [ctypes.POINTER(gdn_shape), ctypes.POINTER(gdn_prefill_io), vp]
         L.gdn_prefill_workspace_bytes.restype = ctypes.c_size_t
         L.gdn_prefill_workspace_bytes.argtypes = [ctypes.POINTER(gdn_shape), ctypes.c_int]
+        L.gdn_prefill_staged_bytes.restype = ctypes.c_size_t
+        L.gdn_prefill_staged_bytes.argtypes = [ctypes.POINTER(gdn_shape), ctypes.c_int]
         _lib = L
     return _lib
 
@@ -213,9 +215,15 @@ def gdn_prefill_static(qkv_pre, z, g, beta, conv_w, norm_w, S0, conv0, o, S_T, c
 
 
 def gdn_prefill_workspace_bytes(B, T, Hk, Hv, packed=False, D=128, io_dtype=None):
-    """Workspace bytes of the staged q^ / k^ path (gdn_prefill_workspace_bytes)."""
+    """Workspace bytes of the chunk-parallel prefill (gdn_prefill_workspace_bytes)."""
     sh = make_shape(B, T, Hk, Hv, D, GDN_BF16 if io_dtype is None else io_dtype)
     return lib().gdn_prefill_workspace_bytes(ctypes.byref(sh), 1 if packed else 0)
+
+
+def gdn_prefill_staged_bytes(B, T, Hk, Hv, packed=False, D=128, io_dtype=None):
+    """Workspace bytes of the staged q^ / k^ form alone (gdn_prefill_staged_bytes)."""
+    sh = make_shape(B, T, Hk, Hv, D, GDN_BF16 if io_dtype is None else io_dtype)
+    return lib().gdn_prefill_staged_bytes(ctypes.byref(sh), 1 if packed else 0)
 
 
 def gdn_decode_ex(qkv_pre, z, g, beta, conv_w, norm_w, S, conv_in, conv_out, o, *, Hk, Hv,

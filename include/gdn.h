@@ -67,7 +67,7 @@
 extern "C" {
 #endif
 
-#define GDN_ABI_VERSION 3
+#define GDN_ABI_VERSION 4
 
 typedef enum {
   GDN_OK = 0,
@@ -171,17 +171,31 @@ typedef struct {
  *               gdn_device_status.
  *   S_snap      [tokens][Hv][Dv][Dk] fp32 or NULL: the state after every
  *               token (for rollback; costs one state write per token).
- *   workspace   device scratch of at least gdn_prefill_workspace_bytes()
- *               bytes (workspace_bytes says how many were given), 256-byte
- *               aligned, overlapping no other argument; or NULL.  Owned by
- *               the caller; its contents are undefined after the call and
- *               it must not be shared by calls that may run concurrently.
- *               When given, and the call runs the chunked kernel, the
- *               normalised q and k of each key head are formed once by a
- *               separate kernel into the workspace and read back by TMA,
- *               instead of once per value head inside the chunked kernel.
+ *   workspace   device scratch, 256-byte aligned, overlapping no other
+ *               argument, or NULL; workspace_bytes says how large it is.
+ *               Owned by the caller; its contents are undefined after the
+ *               call and it must not be shared by calls that may run
+ *               concurrently.  The chunked prefill takes the fastest form
+ *               the workspace holds:
+ *                 >= gdn_prefill_workspace_bytes(): the chunk-parallel form.
+ *                    q^ and k^ are formed once per key head (first kernel);
+ *                    everything of a chunk that does not depend on the
+ *                    carried state (the inverse T, U, W, the decayed
+ *                    Q K^T) is formed for every chunk at once (second
+ *                    kernel); a third kernel walks the chunks of each
+ *                    (sequence, value head) with the state in TMEM, doing
+ *                    only the state-dependent products, the state update
+ *                    and the gated norm ("How Qwen3.5 works" section 9.11
+ *                    separates exactly these two parts).
+ *                 >= gdn_prefill_staged_bytes(): q^ and k^ once per key head
+ *                    into the workspace, then one kernel per (sequence,
+ *                    value head) for the rest.
+ *                 smaller: GDN_ERR_INVALID_ARG.
+ *               NULL: one kernel per (sequence, value head) does everything.
+ *               All forms compute the same chunked recurrence; they differ
+ *               in rounding order only.
  * bf16 io without snapshots (fixed length or packed) runs the chunked
- * tensor-core kernel; fp32 io and snapshots run the token-serial kernel,
+ * tensor-core kernels; fp32 io and snapshots run the token-serial kernel,
  * which ignores the workspace.
  */
 typedef struct {
@@ -200,27 +214,38 @@ typedef struct {
   size_t workspace_bytes;
 } gdn_prefill_io;
 
-/* Bytes of workspace the chunked prefill can use for this shape (packed: the
- * call passes cu_seqlens, so the token rows are shape->T, else B*T): the
- * staged q^ and k^ of every token row and key head, 3 fp16 values per
- * element (q^, and k^ as a hi/lo pair).  0 when the shape is invalid or
- * the call would not run the chunked kernel (fp32 io). */
+/* Bytes of workspace of the chunk-parallel prefill for this shape (packed:
+ * the call passes cu_seqlens, so the token rows are shape->T, else B*T):
+ * the staged q^ and k^ (gdn_prefill_staged_bytes, rounded up to 256) plus
+ * 57,856 bytes per (chunk slot, value head) -- U^T fp32 and -W^T fp16
+ * [128][64], M fp16 [64][64], and two fp32 vectors of 64 -- where the chunk
+ * slots are B * ceil(T/64) for fixed-length sequences and T/64 + B + 2 for
+ * packed ones.  Where the work items would exceed 2^24 it returns the staged
+ * size.  0 when the shape is invalid or the call would not run the chunked
+ * kernels (fp32 io). */
 size_t gdn_prefill_workspace_bytes(const gdn_shape *shape, int packed);
+
+/* Bytes of workspace of the staged form alone: the q^ and k^ of every token
+ * row and key head, 3 fp16 values per element (q^, and k^ as a hi/lo
+ * pair).  0 as above. */
+size_t gdn_prefill_staged_bytes(const gdn_shape *shape, int packed);
 
 /* Prefill with the options above; aliasing and alignment rules as for
  * gdn_prefill (raw gates, cu_seqlens and S_snap count as inputs / outputs). */
 gdn_status gdn_prefill_ex(const gdn_shape *shape, const gdn_prefill_io *io, void *stream);
 
 /*
- * gdn_prefill_ex with no caller workspace and no allocation: the staged
- * q^ / k^ path runs in a device scratch array that the library owns, one
- * per device, GDN_STATIC_SCRATCH_BYTES large.  The pages have no
- * counterpart; this is a serving convenience of the library.
+ * gdn_prefill_ex with no caller workspace and no allocation: the call runs
+ * in a device scratch array that the library owns, one per device,
+ * GDN_STATIC_SCRATCH_BYTES large, as gdn_prefill_ex would with a workspace
+ * of that size (the chunk-parallel form where it fits, else the staged
+ * form).  The pages have no counterpart; this is a serving convenience of
+ * the library.
  *   io->workspace must be NULL (GDN_ERR_INVALID_ARG otherwise).
- *   A call whose workspace need (gdn_prefill_workspace_bytes) exceeds the
- *   scratch returns GDN_ERR_UNSUPPORTED_SHAPE before any launch.
- *   Nothing in the scratch has to start at zero: every byte the chunked
- *   kernel reads is written first by the q/k kernel of the same call.
+ *   A call whose staged need (gdn_prefill_staged_bytes) exceeds the scratch
+ *   returns GDN_ERR_UNSUPPORTED_SHAPE before any launch.
+ *   Nothing in the scratch has to start at zero: every byte a kernel reads
+ *   there is written first by an earlier kernel of the same call.
  *   The scratch is shared by every call on the device: calls that overlap in
  *   time (different streams, or unordered host threads) race on it and give
  *   undefined results.  Issue them on one stream, or order them.

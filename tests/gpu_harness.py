@@ -96,23 +96,27 @@ def upload_prefill(p):
                 S0=dev(a["S0"]), conv0=dev(a["conv0"], t))
 
 
-def prefill_workspace(B, T, Hk, Hv, packed=False):
-    """A device workspace for the staged q^ / k^ path (256-byte aligned)."""
-    n = gdn.gdn_prefill_workspace_bytes(B, T, Hk, Hv, packed=packed)
+def prefill_workspace(B, T, Hk, Hv, packed=False, form="split"):
+    """A device workspace (256-byte aligned) sized for one form of the chunked
+    prefill: "split" (the chunk-parallel form, gdn_prefill_workspace_bytes)
+    or "staged" (q^ / k^ staged only, gdn_prefill_staged_bytes)."""
+    size = gdn.gdn_prefill_staged_bytes if form == "staged" else gdn.gdn_prefill_workspace_bytes
+    n = size(B, T, Hk, Hv, packed=packed)
     assert n > 0
     return torch.empty(n, dtype=torch.uint8, device="cuda")
 
 
-def gpu_prefill(p, inputs=None, in_place=False, staged=False):
-    """The GPU prefill; staged: through gdn_prefill_ex with a workspace (q^ and
-    k^ formed once per key head by their own kernel)."""
+def gpu_prefill(p, inputs=None, in_place=False, staged=False, split=False):
+    """The GPU prefill; staged: through gdn_prefill_ex with a workspace that
+    holds the staged q^ / k^ only (two kernels); split: with a workspace for
+    the chunk-parallel form (three kernels)."""
     x = inputs or upload_prefill(p)
     o, S_T, conv_T = gdn.alloc_prefill_outputs(p.B, p.T, p.Hk, p.Hv, torch_io(p.io))
     if in_place:
         assert x["S0"] is not None
         S_T = x["S0"]
-    if staged:
-        ws = prefill_workspace(p.B, p.T, p.Hk, p.Hv)
+    if staged or split:
+        ws = prefill_workspace(p.B, p.T, p.Hk, p.Hv, form="staged" if staged else "split")
         gdn.gdn_prefill_ex(x["qkv_pre"], x["z"], x["g"], x["beta"], x["conv_w"], x["norm_w"],
                            x["S0"], x["conv0"], o, S_T, conv_T, Hk=p.Hk, Hv=p.Hv, workspace=ws)
     else:

@@ -165,14 +165,19 @@ def test_extended_entry_points_check_on_host(L):
 
 def test_workspace_checked_on_host(L):
     sh = shape(B=2, T=8, Hk=2, Hv=4)
+    staged = L.gdn_prefill_staged_bytes(ctypes.byref(sh), 0)
+    assert staged == 3 * 2 * 8 * 2 * 128 * 2
+    assert L.gdn_prefill_staged_bytes(ctypes.byref(sh), 1) == 3 * 8 * 2 * 128 * 2   # packed: T rows
+    item = 32768 + 16384 + 8192 + 512   # U^T, -W^T, M, vectors of one (chunk slot, value head)
     need = L.gdn_prefill_workspace_bytes(ctypes.byref(sh), 0)
-    assert need == 3 * 2 * 8 * 2 * 128 * 2
-    assert L.gdn_prefill_workspace_bytes(ctypes.byref(sh), 1) == 3 * 8 * 2 * 128 * 2   # packed: T rows
+    assert need == staged + 2 * 1 * 4 * item                 # B * ceil(T/64) slots x Hv heads
+    assert L.gdn_prefill_workspace_bytes(ctypes.byref(sh), 1) == 3 * 8 * 2 * 128 * 2 + (0 + 2 + 2) * 4 * item
     assert L.gdn_prefill_workspace_bytes(ctypes.byref(shape(io=gdn.GDN_F32)), 0) == 0  # no chunked kernel
+    assert L.gdn_prefill_staged_bytes(ctypes.byref(shape(io=gdn.GDN_F32)), 0) == 0
     assert L.gdn_prefill_workspace_bytes(None, 0) == 0
     ws = fake(11)
     assert prefill_ex(L, sh, workspace=fake(11, 16), workspace_bytes=need) == 3     # not 256-byte aligned
-    assert prefill_ex(L, sh, workspace=ws, workspace_bytes=need - 1) == 1           # too small
+    assert prefill_ex(L, sh, workspace=ws, workspace_bytes=staged - 1) == 1         # too small
     assert prefill_ex(L, sh, workspace=fake(0), workspace_bytes=need) == 4          # over qkv_pre
     assert prefill_ex(L, sh, workspace=fake(8), workspace_bytes=need) == 4          # over o
 

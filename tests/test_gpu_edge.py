@@ -1,5 +1,6 @@
 """GPU parity on the method's edge cases, on every kernel that runs the
-recurrence: the chunked prefill (fused and staged q^/k^), the token-serial
+recurrence: the chunked prefill (fused, staged q^/k^, and the chunk-parallel
+split form), the token-serial
 prefill (fp32 io), the T-token decode and the single-token decode.
 
 The cases:
@@ -30,7 +31,7 @@ pytestmark = pytest.mark.gpu
 D = 128
 KINDS = ["reset", "deep_decay", "beta_runs", "frozen", "qkv_small", "qkv_large", "s0_small", "s0_large"]
 # path -> (io, tokens per sequence)
-PATHS = {"fused": ("bf16", 200), "staged": ("bf16", 200), "serial": ("f32", 90),
+PATHS = {"fused": ("bf16", 200), "staged": ("bf16", 200), "split": ("bf16", 200), "serial": ("f32", 90),
          "decode": ("bf16", 16), "decode_step": ("bf16", 12)}
 
 
@@ -99,9 +100,9 @@ def run_path(path, p):
     o, S_T, conv_T = gdn.alloc_prefill_outputs(p.B, p.T, p.Hk, p.Hv, t)
     if path in ("fused", "serial"):
         gdn.gdn_prefill(*x, S0, conv0, o, S_T, conv_T, Hk=p.Hk, Hv=p.Hv)
-    elif path == "staged":
+    elif path in ("staged", "split"):
         gdn.gdn_prefill_ex(*x, S0, conv0, o, S_T, conv_T, Hk=p.Hk, Hv=p.Hv,
-                           workspace=prefill_workspace(p.B, p.T, p.Hk, p.Hv))
+                           workspace=prefill_workspace(p.B, p.T, p.Hk, p.Hv, form=path))
     elif path == "decode":
         S_T = S0.clone()
         gdn.gdn_decode_ex(*x, S_T, conv0, conv_T, o, Hk=p.Hk, Hv=p.Hv)
@@ -139,7 +140,7 @@ def test_edge_case(kind, path):
         assert torch.equal(S_T, dev(a["S0"]))
 
 
-@pytest.mark.parametrize("path", ["fused", "staged"])
+@pytest.mark.parametrize("path", ["fused", "staged", "split"])
 def test_reset_at_every_chunk_boundary_and_3_heads_per_key(path):
     """g = -inf on the first token of every chunk of one head and the last
     token of every chunk of another, with three value heads per key head."""

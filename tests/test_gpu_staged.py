@@ -58,7 +58,7 @@ def test_staged_raw_gates():
                        dev(a["norm_w"], t), dev(a["S0"]), dev(a["conv0"], t), o, S_T, conv_T, Hk=Hk, Hv=Hv,
                        raw_gates=dict(a=dev(rg["a"], t), b=dev(rg["b"], t), A_log=dev(rg["A_log"]),
                                       dt_bias=dev(rg["dt_bias"])),
-                       workspace=prefill_workspace(B, T, Hk, Hv))
+                       workspace=prefill_workspace(B, T, Hk, Hv, form="staged"))
     torch.cuda.synchronize()
     assert gdn.gdn_device_status() == 0
     ref = O.gdn_prefill(a["qkv_pre"], a["z"], None, None, a["conv_w"], a["norm_w"], a["S0"], a["conv0"],
@@ -83,7 +83,7 @@ def test_staged_packed(lengths):
     cu = torch.from_numpy(p.cu_seqlens).to("cuda")
     gdn.gdn_prefill_ex(dev(a["qkv_pre"], t), dev(a["z"], t), dev(a["g"]), dev(a["beta"]), dev(a["conv_w"], t),
                        dev(a["norm_w"], t), dev(a["S0"]), dev(a["conv0"], t), o, S_T, conv_T, Hk=p.Hk, Hv=p.Hv,
-                       cu_seqlens=cu, workspace=prefill_workspace(B, N, p.Hk, p.Hv, packed=True))
+                       cu_seqlens=cu, workspace=prefill_workspace(B, N, p.Hk, p.Hv, packed=True, form="staged"))
     torch.cuda.synchronize()
     assert gdn.gdn_device_status() == 0
     keep = [s for s, n in enumerate(p.lengths) if n > 0]
