@@ -256,7 +256,8 @@ __device__ __forceinline__ void zero_T_upper(const SolveSmem &s, int first, int 
 // thread); the 32 x 32 halves by T_BA = -T_BB (L_BA T_AA); the whole by the
 // same identity on the halves.  Threads idle in a product convert finished
 // blocks to the fp16 tiles meanwhile.  With zero_upper, threads 128..255
-// re-zero the upper blocks of tiles 0 and 1 during the last product.
+// re-zero the upper blocks of all three tiles during the last product (for
+// callers that stage other data in the tiles' space between solves).
 __device__ __forceinline__ void solve_T(const SolveSmem &s, const ChunkVecs &V, int tid, int bar, bool zero_upper) {
   const float *L = s.L;
   float *Tf = s.Tf;
@@ -379,7 +380,7 @@ __device__ __forceinline__ void solve_T(const SolveSmem &s, const ChunkVecs &V, 
     store_T4(s, V, ra, col, make_float4(-acc0.x, -acc0.y, -acc0.z, -acc0.w));
     store_T4(s, V, rb, col, make_float4(-acc1.x, -acc1.y, -acc1.z, -acc1.w));
   } else if (zero_upper) {
-    zero_T_upper(s, tid - 128, 128, 0, 2 * 192);
+    zero_T_upper(s, tid - 128, 128, 0, 3 * 192);
   }
 }
 

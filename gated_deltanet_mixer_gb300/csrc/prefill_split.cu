@@ -107,21 +107,23 @@ constexpr uint32_t P_KQ = 0;        // [K;Q] K-major 128 x 128 fp16 (k^ hi rows 
 constexpr uint32_t P_TU = 32768;    // T diag(beta) hi  K-major [i][j]                                      8 KB
 constexpr uint32_t P_TUL = 40960;   // T diag(beta) lo                                                      8 KB
 constexpr uint32_t P_TW = 49152;    // -T diag(beta d)                                                      8 KB
-constexpr uint32_t P_NW = P_TU;     // after MMA U / W: -W^T fp16 MN-major [k][j] over TU + TUL            16 KB
 constexpr uint32_t P_M = 57344;     // M fp16 K-major [i][j]                                                8 KB
-constexpr uint32_t P_RAW = 65536;   // raw v rows bf16 [67][128]; then L fp32 [64][68]; then U^T box 0  17 KB
+constexpr uint32_t P_NW = P_TU;     // after MMA U / W: -W^T fp16 MN-major [k][j] over TU + TUL            16 KB
+constexpr uint32_t P_UB0 = P_TW;    // after MMA U / W: U^T box 0 over TW + M                              16 KB
+constexpr uint32_t P_RAW = 65536;   // raw v rows bf16 [67][128]; then L fp32 [64][68]                     17 KB
 constexpr uint32_t P_TF = P_RAW + 64 * kLs * 4;  // T fp32 [64][64] (tfi); then U^T box 1                16 KB
 constexpr uint32_t P_PB = P_TF + 16384;          // solve block products                                 4 KB
 constexpr uint32_t P_VEC = P_PB + 4096;
 struct PrepShared {
   ChunkVecs cv;
-  uint64_t bar_ld, bar_qk, bar_uw;
+  uint64_t bar_kq, bar_raw, bar_qk, bar_uw;
   uint32_t tmem;
   int abort;
 };
 constexpr uint32_t kPrepSmem = P_VEC + ((sizeof(PrepShared) + 127) / 128) * 128 + 1024;
-static_assert(64 * kLs * 4 >= kRawBlock && 64 * kLs * 4 >= 16384, "the raw v region holds L and U^T box 0");
-static_assert(P_TF % 1024 == 0 && P_PB % 16 == 0 && P_VEC % 16 == 0, "alignment (U^T boxes: 1024)");
+static_assert(64 * kLs * 4 >= kRawBlock, "the raw v region holds L");
+static_assert(P_UB0 % 1024 == 0 && P_M == P_UB0 + 8192 && P_TF % 1024 == 0 && P_PB % 16 == 0 && P_VEC % 16 == 0,
+              "alignment (U^T boxes: 1024)");
 static_assert(kPrepSmem <= 113 * 1024, "two CTAs per SM");
 // TMEM columns (256 allocated).
 constexpr uint32_t TP_KQ = 0;    // [K K^T; Q K^T]                    64
@@ -131,6 +133,9 @@ constexpr uint32_t TP_W = 192;   // -W^T [k][i]                       64
 constexpr uint32_t kPrepTmem = 256;
 constexpr int kBarSolve = 1;
 
+// Work items are taken in steps of the grid; the next one's tiles and gates
+// are requested while the current one is computed: its raw v rows once the
+// solve is done with L (their space), its [K;Q] once MMA W is done.
 template <bool kRawGates>
 __global__ void __launch_bounds__(kPrepThreads, 2)
     prefill_prep_kernel(const PrefillArgs a, const SplitArgs s, const __grid_constant__ CUtensorMap tm_qkv,
@@ -151,9 +156,11 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   const int r = d.Hv / d.Hk;
   const long long C = d.C;
   const long long nitems = (long long)s.nslots * d.Hv;
+  const long long cv0 = 2LL * d.Hk * kD;  // first v channel
 
   if (tid == 0) {
-    bar_init(&V.bar_ld, 1);
+    bar_init(&V.bar_kq, 1);
+    bar_init(&V.bar_raw, 1);
     bar_init(&V.bar_qk, 1);
     bar_init(&V.bar_uw, 1);
     V.abort = 0;
@@ -166,43 +173,68 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   const uint32_t tmem = V.tmem;
   const uint32_t tl = tmem + ((uint32_t)(32 * quad) << 16);
   const uint32_t id_kk = idesc(128, 64, 0, 0), id_mk = idesc(128, 64, 1, 0);
-  uint32_t ph_ld = 0, ph_qk = 0, ph_uw = 0;
-  bool ld_pending = false, stores = false;  // thread 0's bookkeeping
+  uint32_t ph_kq = 0, ph_raw = 0, ph_qk = 0, ph_uw = 0;
+  bool kq_pending = false, raw_pending = false, stores = false;  // thread 0's bookkeeping
 
-  for (long long item = blockIdx.x; item < nitems; item += gridDim.x) {
-    const int slot = (int)(item / d.Hv), h = (int)(item % d.Hv);
-    const ChunkLoc c = locate(s, slot);
-    if (!c.ok) continue;  // the same decision in every thread
-    const int kh = h / r, t0 = kC * c.n, T = c.len;
-    const long long bos = c.bos;
-    const long long cv = 2LL * d.Hk * kD + (long long)h * kD;
-    // The previous item's TMA stores must have read their shared-memory sources.
-    if (tid == 0 && stores) bulk_wait_read();
-    __syncthreads();
-    if (tid == 0) {
-      bar_expect_tx(&V.bar_ld, 2 * kC * kD * 2 + kRawBlock);
-#pragma unroll
-      for (int at = 0; at < 2; ++at) {
-        tma_load_3d(sbase + P_KQ + at * 16384 + 64 * 128, &tm_qk, kh * kD + 64 * at, (int)(bos + t0), 0, &V.bar_ld);
-        tma_load_3d(sbase + P_KQ + at * 16384, &tm_qk, kh * kD + 64 * at, (int)(bos + t0), 1, &V.bar_ld);
-      }
-      tma_load_3d(sbase + P_RAW, &tm_qkv, (int)cv, (int)(bos + t0 - 3), 0, &V.bar_ld);
-      ld_pending = true;
+  // The next valid item at or after `it` (every thread computes the same).
+  auto next_valid = [&](long long it, ChunkLoc &c) -> long long {
+    for (; it < nitems; it += gridDim.x) {
+      c = locate(s, (int)(it / d.Hv));
+      if (c.ok) return it;
     }
-    if (warp == 7) {  // the chunk's gates and vectors
-      float gv[2], bv[2];
-      load_gb<kRawGates>(a.gate, bos, d.Hv, h, t0, T, lane, gv, bv);
-      float nea = 0.f, dtb = 0.f;
-      if (kRawGates) {
-        nea = -expf(a.gate.A_log[h]);
-        dtb = a.gate.dt_bias[h];
-      }
-      finish_gb<kRawGates>(nea, dtb, t0, T, lane, gv, bv);
+    return nitems;
+  };
+  // Thread 0: an item's [K;Q] (q^ rows 64-127, k^ hi rows 0-63) and raw v rows.
+  auto request_kq = [&](long long it, const ChunkLoc &c) {
+    const int kh = (int)(it % d.Hv) / r;
+    bar_expect_tx(&V.bar_kq, 2 * kC * kD * 2);
+#pragma unroll
+    for (int at = 0; at < 2; ++at) {
+      tma_load_3d(sbase + P_KQ + at * 16384 + 64 * 128, &tm_qk, kh * kD + 64 * at, c.bos + kC * c.n, 0, &V.bar_kq);
+      tma_load_3d(sbase + P_KQ + at * 16384, &tm_qk, kh * kD + 64 * at, c.bos + kC * c.n, 1, &V.bar_kq);
+    }
+    kq_pending = true;
+  };
+  auto request_raw = [&](long long it, const ChunkLoc &c) {
+    bar_expect_tx(&V.bar_raw, kRawBlock);
+    tma_load_3d(sbase + P_RAW, &tm_qkv, (int)(cv0 + (it % d.Hv) * kD), c.bos + kC * c.n - 3, 0, &V.bar_raw);
+    raw_pending = true;
+  };
+  // Warp 7: an item's gates (raw bf16 bits for raw projections), a chunk ahead.
+  float gv[2] = {0.f, 0.f}, bv[2] = {0.f, 0.f}, nea = 0.f, dtb = 0.f;
+  auto load_gates = [&](long long it, const ChunkLoc &c) {
+    const int h = (int)(it % d.Hv);
+    load_gb<kRawGates>(a.gate, c.bos, d.Hv, h, kC * c.n, c.len, lane, gv, bv);
+    if (kRawGates) {
+      nea = a.gate.A_log[h];
+      dtb = a.gate.dt_bias[h];
+    }
+  };
+
+  ChunkLoc c{};
+  long long item = next_valid(blockIdx.x, c);
+  if (item < nitems) {
+    if (tid == 0) {
+      request_kq(item, c);
+      request_raw(item, c);
+    }
+    if (warp == 7) load_gates(item, c);
+  }
+  while (item < nitems) {
+    const int h = (int)(item % d.Hv);
+    const int t0 = kC * c.n, T = c.len;
+    const long long cv = cv0 + (long long)h * kD;
+    ChunkLoc cn{};
+    const long long next = next_valid(item + gridDim.x, cn);
+    if (warp == 7) {  // this item's chunk vectors, then the next item's gates requested
+      finish_gb<kRawGates>(kRawGates ? -expf(nea) : 0.f, dtb, t0, T, lane, gv, bv);
       chunk_vectors(V.cv, gv, bv, lane);
+      if (next < nitems) load_gates(next, cn);
     }
     __syncwarp();
-    bool ok = bar_wait(&V.bar_ld, ph_ld);
-    ph_ld ^= 1u;
+    bool ok = bar_wait(&V.bar_kq, ph_kq) && bar_wait(&V.bar_raw, ph_raw);
+    ph_kq ^= 1u;
+    ph_raw ^= 1u;
     if (__syncthreads_or(!ok)) {
       if (tid == 0) {
         atomicOr(a.err, kErrTimeout);
@@ -210,7 +242,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
       }
       break;
     }
-    if (tid == 0) ld_pending = false;
+    if (tid == 0) kq_pending = raw_pending = false;
     if (c.n == 0) {  // rows before the sequence's first token: the carried window, or zeros
       if (tid < 48) {
         const int rw = tid >> 4, g8 = tid & 15;
@@ -230,37 +262,42 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     }
     // The v tiles (every warp): row v = lrow, tokens 32 half .. 32 half + 31;
     // conv + SiLU, zero past the sequence, fp16 hi/lo pairs into TMEM (the A
-    // operand of MMA U: lane = v, column c = tokens 2c, 2c + 1).
+    // operand of MMA U: lane = v, column c = tokens 2c, 2c + 1).  Pairs of
+    // tokens on the paired fp32 pipes.
     {
-      const bf16 *raw = reinterpret_cast<const bf16 *>(sm + P_RAW);
+      const bf16 *raw = reinterpret_cast<const bf16 *>(sm + P_RAW) + lrow;
       const float4 w4 = ld_io4(conv_w + 4 * (cv + lrow));
+      const float2 w0 = make_float2(w4.x, w4.x), w1 = make_float2(w4.y, w4.y), w2 = make_float2(w4.z, w4.z),
+                   w3 = make_float2(w4.w, w4.w);
       const int j0 = 32 * half;
-      float x0 = __bfloat162float(raw[(j0 + 0) * kD + lrow]);
-      float x1 = __bfloat162float(raw[(j0 + 1) * kD + lrow]);
-      float x2 = __bfloat162float(raw[(j0 + 2) * kD + lrow]);
+      const bool tail = t0 + kC > T;  // the sequence ends inside this chunk
+      float2 xa = make_float2(__bfloat162float(raw[(j0 + 0) * kD]), __bfloat162float(raw[(j0 + 1) * kD]));
+      float2 xb = make_float2(__bfloat162float(raw[(j0 + 2) * kD]), __bfloat162float(raw[(j0 + 3) * kD]));
       uint32_t wh[16], wl[16];
 #pragma unroll
       for (int q = 0; q < 16; ++q) {
-        float u[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int j = j0 + 2 * q + e;
-          const float x3 = __bfloat162float(raw[(j + 3) * kD + lrow]);
-          float acc = w4.x * x0;
-          acc = fmaf(w4.y, x1, acc);
-          acc = fmaf(w4.z, x2, acc);
-          acc = fmaf(w4.w, x3, acc);
-          u[e] = t0 + j < T ? silu1(acc) : 0.f;
-          x0 = x1;
-          x1 = x2;
-          x2 = x3;
+        const int j = j0 + 2 * q;  // tokens j, j + 1 use rows j .. j + 4
+        const float2 xc = make_float2(__bfloat162float(raw[(j + 4) * kD]), __bfloat162float(raw[(j + 5 < kRawRows ? j + 5 : j + 4) * kD]));
+        float2 acc = __fmul2_rn(w0, xa);
+        acc = __ffma2_rn(w1, make_float2(xa.y, xb.x), acc);
+        acc = __ffma2_rn(w2, xb, acc);
+        acc = __ffma2_rn(w3, make_float2(xb.y, xc.x), acc);
+        float2 u = silu2(acc);
+        if (tail) {
+          if (t0 + j >= T) u.x = 0.f;
+          if (t0 + j + 1 >= T) u.y = 0.f;
         }
-        split2(u[0], u[1], wh[q], wl[q]);
+        split2(u.x, u.y, wh[q], wl[q]);
+        xa = xb;
+        xb = xc;
       }
       tmem_st16w_nw(tl + TP_V + 16 * half, wh);
       tmem_st16w_nw(tl + TP_V + 32 + 16 * half, wl);
       tmem_wait_st();
     }
+    // The previous item's stores must have read their sources (M, the T tiles
+    // and the T scratch are written next).
+    if (tid == 0 && stores) bulk_wait_read();
     fence_before();
     __syncthreads();  // the v rows are read: L may take their space
     ok = bar_wait(&V.bar_qk, ph_qk);
@@ -325,19 +362,21 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
       }
     }
     fence_smem_to_async();
-    __syncthreads();  // L and M written; MMA1 is done with [K;Q]'s q^ rows (the T scratch goes there)
+    __syncthreads();  // L and M written
     if (tid == 0) {
       tma_store_2d(&tm_m, sbase + P_M, 0, (int)(item * kC));
       bulk_commit();
       stores = true;
     }
-    // T = (I + L)^{-1} and the fp16 tiles (the upper blocks of T B hi / lo are
-    // zeroed again: the -W^T staging of the previous item used their space)
+    // T = (I + L)^{-1} and the fp16 tiles (their upper blocks are zeroed
+    // again: the previous item's -W^T and U^T staging used their space)
     solve_T(ss, V.cv, tid, kBarSolve, true);
     fence_smem_to_async();
     fence_before();
     __syncthreads();
-    // MMA U (hi*hi + lo*hi + hi*lo, A = V^T from TMEM) and MMA W (warp 0)
+    // L is done with: the next item's raw v rows may land.  MMA U (hi*hi +
+    // lo*hi + hi*lo, A = V^T from TMEM) and MMA W (warp 0).
+    if (tid == 0 && next < nitems) request_raw(next, cn);
     if (warp == 0) {
       fence_after();
       auto b_tu = [&](int ks) { return desc_k(sbase + P_TU, ks, kC); };
@@ -363,11 +402,18 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
       }
       break;
     }
+    // MMA W is done with [K;Q]: the next item's may land.  The M store is
+    // long complete (its space takes U^T box 0).
+    if (tid == 0) {
+      if (next < nitems) request_kq(next, cn);
+      bulk_wait_read();
+    }
+    __syncthreads();
     {
       // U^T [v][i] fp32 -> staging box `half` (rows v, 32 values of 4 bytes, 128-byte swizzle)
       float v[32];
       tmem_ld32(tl + TP_U + 32 * half, v);
-      uint8_t *box = sm + (half == 0 ? P_RAW : P_TF) + lrow * 128;
+      uint8_t *box = sm + (half == 0 ? P_UB0 : P_TF) + lrow * 128;
 #pragma unroll
       for (int q = 0; q < 8; ++q)
         *reinterpret_cast<float4 *>(box + ((q ^ (lrow & 7)) << 4)) =
@@ -381,17 +427,20 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     fence_before();
     __syncthreads();
     if (tid == 0) {
-      tma_store_2d(&tm_u, sbase + P_RAW, 0, (int)(item * kD));
+      tma_store_2d(&tm_u, sbase + P_UB0, 0, (int)(item * kD));
       tma_store_2d(&tm_u, sbase + P_TF, 32, (int)(item * kD));
       tma_store_2d(&tm_nw, sbase + P_NW, 0, (int)(item * kD));
       bulk_commit();
     }
+    item = next;
+    c = cn;
   }
   // Before the CTA ends: the stores complete, no load still lands, and no MMA
   // still writes TMEM (after an early exit).
   if (tid == 0) {
     bulk_wait_all();
-    if (ld_pending) bar_wait(&V.bar_ld, ph_ld);
+    if (kq_pending) bar_wait(&V.bar_kq, ph_kq);
+    if (raw_pending) bar_wait(&V.bar_raw, ph_raw);
   }
   fence_before();
   __syncthreads();
@@ -404,7 +453,13 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
 // =============================================================================
 // prefill_seq_kernel
 // =============================================================================
-constexpr int kSeqThreads = 384;
+// Warps 0-7: the epilogue (O staging, gated norm); warps 8-11: the chain (the
+// state-dependent MMAs, issued by warp 8, and the Delta and state passes);
+// warp 12: the TMA producer (lane 0 the U^T tiles, lane 1 the chunk stages,
+// lane 2 the z rows), each lane waiting for its buffer to be released.
+constexpr int kSeqThreads = 416;
+constexpr int kProducerWarp = 12;
+constexpr int kIssuerTid = 256;  // warp 8, lane 0
 // One stage (a chunk's tiles), offsets within the stage; fp16, 128-byte swizzle.
 constexpr uint32_t Q_Q = 0;         // q^ K-major [i][k] (64 rows, k halves 8 KB apart)   16 KB
 constexpr uint32_t Q_KH = 16384;    // k^ hi [j][k]                                       16 KB
@@ -419,13 +474,15 @@ constexpr uint32_t S_OST = S_Z + 16384;       // O staging fp32 [64 i][128 v]   
 constexpr uint32_t S_VEC = S_OST + 32768;     // d, Gamma of the two stages, fp32 [2][2][64]            1 KB
 constexpr uint32_t S_BAR = S_VEC + 1024;
 struct SeqShared {
-  uint64_t full[2];  // a stage's tiles and vectors landed
-  uint64_t bar_u;    // U^T landed
-  uint64_t bar_z;    // z rows landed
-  uint64_t bar_d;    // MMA4 done
-  uint64_t bar_o;    // MMA5 and MMA6 done
-  uint64_t bar_s;    // MMA7 done
-  uint64_t bar_ofree;  // the epilogue has read O1, O2 (one arrival per chunk)
+  uint64_t full[2];    // a stage's tiles and vectors landed
+  uint64_t bar_u;      // U^T landed
+  uint64_t bar_z;      // z rows landed
+  uint64_t bar_d;      // MMA4 done
+  uint64_t bar_o;      // MMA5 and MMA6 done
+  uint64_t bar_s;      // MMA7 done
+  uint64_t bar_ofree;  // the epilogue has read O1, O2 and the stage's vectors (one arrival per chunk)
+  uint64_t bar_ufree;  // the chain has read U^T (one arrival per chunk)
+  uint64_t bar_zfree;  // the epilogue has read the z rows (one arrival per chunk)
   uint64_t bar_end;
   uint32_t tmem;
   int abort;
@@ -445,6 +502,12 @@ constexpr uint32_t TS_S16 = 448;  // state fp16 pairs [v][k/2]           64
 constexpr uint32_t kSeqTmem = 512;
 constexpr int kBarChain = 2;  // warps 8-11
 constexpr int kBarEpi = 3;    // warps 0-7
+
+__device__ __forceinline__ bool seq_aborted(const SeqShared &V) { return *reinterpret_cast<const volatile int *>(&V.abort) != 0; }
+__device__ __forceinline__ void seq_fail(SeqShared &V, unsigned int *err) {
+  atomicOr(err, kErrTimeout);
+  *reinterpret_cast<volatile int *>(&V.abort) = 1;
+}
 
 // The gated RMSNorm (node gdn.norm) of NR tokens i0, i0 + di, ... of the chunk,
 // one half-warp per token (8 channels per lane), from the O staging and the
@@ -561,6 +624,8 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
     bar_init(&V.bar_o, 1);
     bar_init(&V.bar_s, 1);
     bar_init(&V.bar_ofree, 1);
+    bar_init(&V.bar_ufree, 1);
+    bar_init(&V.bar_zfree, 1);
     bar_init(&V.bar_end, 1);
     V.abort = 0;
     V.req_full[0] = V.req_full[1] = V.req_u = V.req_z = 0;
@@ -570,46 +635,59 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
   __syncthreads();
   fence_after();
   const uint32_t tmem = V.tmem;
+  auto vec_d = [&](int st) { return reinterpret_cast<const float *>(sm + S_VEC + 512 * st); };  // d [64], Gamma [64]
 
-  // One thread each: a chunk's stage; U^T of a chunk; z rows of a chunk.
-  auto request_stage = [&](int n) {
-    const int st = n & 1;
-    const uint32_t sb = sbase + st * kStage;
-    const long long it = item_of(n);
-    uint64_t *bar = &V.full[st];
-    bar_expect_tx(bar, kStageTx);
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------ the producer (warp 12)
+    // Lane 0: U^T of chunk n+1 once the chain has read chunk n's.  Lane 1: the
+    // stage of chunk n+2 into chunk n's buffer once MMA7(n) is done and the
+    // epilogue has read chunk n's vectors.  Lane 2: z of chunk n+1 once the
+    // epilogue has read chunk n's.  Every wait is bounded.
+    if (lane == 0) {
+      bar_expect_tx(&V.bar_u, 32768);
+      tma_load_2d(sbase + S_U, &tm_u, 0, (int)(item_of(0) * kD), &V.bar_u);
+      tma_load_2d(sbase + S_U + 16384, &tm_u, 32, (int)(item_of(0) * kD), &V.bar_u);
+      V.req_u = 1;
+      for (int n = 0; n + 1 < nch; ++n) {
+        if (!bar_wait(&V.bar_ufree, (uint32_t)n & 1u) || seq_aborted(V)) break;
+        const long long it = item_of(n + 1);
+        bar_expect_tx(&V.bar_u, 32768);
+        tma_load_2d(sbase + S_U, &tm_u, 0, (int)(it * kD), &V.bar_u);
+        tma_load_2d(sbase + S_U + 16384, &tm_u, 32, (int)(it * kD), &V.bar_u);
+        V.req_u = n + 2;
+      }
+    } else if (lane == 1) {
+      for (int n = 0; n < nch; ++n) {
+        if (n >= 2) {  // chunk n goes where chunk n-2 was
+          if (!bar_wait(&V.bar_s, (uint32_t)(n - 2) & 1u) || !bar_wait(&V.bar_ofree, (uint32_t)(n - 2) & 1u) ||
+              seq_aborted(V))
+            break;
+        }
+        const int st = n & 1;
+        const uint32_t sb = sbase + st * kStage;
+        const long long it = item_of(n);
+        uint64_t *bar = &V.full[st];
+        bar_expect_tx(bar, kStageTx);
 #pragma unroll
-    for (int at = 0; at < 2; ++at) {
-      tma_load_3d(sb + Q_Q + at * 8192, &tm_qk, kh * kD + 64 * at, (int)(bos + kC * n), 0, bar);
-      tma_load_3d(sb + Q_KH + at * 8192, &tm_qk, kh * kD + 64 * at, (int)(bos + kC * n), 1, bar);
-      tma_load_3d(sb + Q_KL + at * 8192, &tm_qk, kh * kD + 64 * at, (int)(bos + kC * n), 2, bar);
+        for (int at = 0; at < 2; ++at) {
+          tma_load_3d(sb + Q_Q + at * 8192, &tm_qk, kh * kD + 64 * at, (int)(bos + kC * n), 0, bar);
+          tma_load_3d(sb + Q_KH + at * 8192, &tm_qk, kh * kD + 64 * at, (int)(bos + kC * n), 1, bar);
+          tma_load_3d(sb + Q_KL + at * 8192, &tm_qk, kh * kD + 64 * at, (int)(bos + kC * n), 2, bar);
+        }
+        tma_load_2d(sb + Q_NW, &tm_nw, 0, (int)(it * kD), bar);
+        tma_load_2d(sb + Q_M, &tm_m, 0, (int)(it * kC), bar);
+        bulk_load(sbase + S_VEC + st * 512, s.ws_vec + it * (2 * kC), 2 * kC * 4, bar);
+        V.req_full[st] += 1;
+      }
+    } else if (lane == 2) {
+      for (int n = 0; n < nch; ++n) {
+        if (n >= 1 && (!bar_wait(&V.bar_zfree, (uint32_t)(n - 1) & 1u) || seq_aborted(V))) break;
+        bar_expect_tx(&V.bar_z, kC * kD * 2);
+        tma_load_3d(sbase + S_Z, &tm_z, h * kD, (int)(bos + kC * n), 0, &V.bar_z);
+        V.req_z = n + 1;
+      }
     }
-    tma_load_2d(sb + Q_NW, &tm_nw, 0, (int)(it * kD), bar);
-    tma_load_2d(sb + Q_M, &tm_m, 0, (int)(it * kC), bar);
-    bulk_load(sbase + S_VEC + st * 512, s.ws_vec + it * (2 * kC), 2 * kC * 4, bar);
-    V.req_full[st] += 1;
-  };
-  auto request_u = [&](int n) {
-    const long long it = item_of(n);
-    bar_expect_tx(&V.bar_u, 32768);
-    tma_load_2d(sbase + S_U, &tm_u, 0, (int)(it * kD), &V.bar_u);
-    tma_load_2d(sbase + S_U + 16384, &tm_u, 32, (int)(it * kD), &V.bar_u);
-    V.req_u += 1;
-  };
-  auto request_z = [&](int n) {
-    bar_expect_tx(&V.bar_z, kC * kD * 2);
-    tma_load_3d(sbase + S_Z, &tm_z, h * kD, (int)(bos + kC * n), 0, &V.bar_z);
-    V.req_z += 1;
-  };
-  if (tid == 0) {
-    request_stage(0);
-    if (nch > 1) request_stage(1);
-    request_u(0);
-    request_z(0);
-  }
-  const float *vec_d[2] = {reinterpret_cast<const float *>(sm + S_VEC), reinterpret_cast<const float *>(sm + S_VEC + 512)};
-
-  if (warp >= 8) {
+  } else if (warp >= 8) {
     // ------------------------------------------------ the chain (warps 8-11)
     const int quad = warp - 8;
     const int lrow = 32 * quad + lane;  // state row v of this thread
@@ -622,165 +700,171 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
     auto dc_of = [&](int n) -> float { return n < nch ? s.ws_vec[item_of(n) * (2 * kC) + kC - 1] : 1.f; };
     const float dc0 = dc_of(0);
     float dc_n1 = dc_of(1), dc_n2 = dc_of(2);
-    {
-      // Initial state: TMEM fp32 <- d_C(chunk 0) S0, fp16 copy <- S0.
+    // Initial state: TMEM fp32 <- d_C(chunk 0) S0, fp16 copy <- S0.
 #pragma unroll 1
-      for (int k0 = 0; k0 < kD; k0 += 32) {
-        float v[32];
-        if (a.S0) {
-          const float4 *src = reinterpret_cast<const float4 *>(a.S0 + unit_off + (long long)lrow * kD + k0);
+    for (int k0 = 0; k0 < kD; k0 += 32) {
+      float v[32];
+      if (a.S0) {
+        const float4 *src = reinterpret_cast<const float4 *>(a.S0 + unit_off + (long long)lrow * kD + k0);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float4 f = src[q];
+          v[4 * q] = f.x;
+          v[4 * q + 1] = f.y;
+          v[4 * q + 2] = f.z;
+          v[4 * q + 3] = f.w;
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 32; ++q) v[q] = 0.f;
+      }
+      uint32_t w16[16];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) w16[q] = pack2_sat(v[2 * q], v[2 * q + 1]);
+      tmem_st16w_nw(tl + TS_S16 + k0 / 2, w16);
+#pragma unroll
+      for (int q = 0; q < 32; ++q) v[q] *= dc0;
+      tmem_st32(tl + TS_S + k0, v);
+    }
+    tmem_wait_st();
+    fence_before();
+    named_sync(kBarChain, 128);
+    for (int n = 0; n < nch; ++n) {
+      const int st = n & 1;
+      const uint32_t sb = sbase + st * kStage;
+      if (seq_aborted(V)) break;
+      // MMA4 D = S (-W^T), MMA5 O1 = S Q^T, once the chunk's tiles and U^T are
+      // in and the epilogue has read the previous chunk's O1, O2.
+      __syncwarp();
+      bool w = bar_wait(&V.full[st], (uint32_t)(n >> 1) & 1u);
+      w = bar_wait(&V.bar_u, (uint32_t)n & 1u) && w;
+      if (issuer && n > 0) w = bar_wait(&V.bar_ofree, (uint32_t)(n - 1) & 1u) && w;
+      ok = w;
+      if (named_sync_or(kBarChain, 128, !ok)) break;
+      if (issuer) {
+        fence_after();
+        const uint64_t dnw = desc_mn(sb + Q_NW, 0, kD);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) mma_ta_w(tmem + TS_D, tmem + TS_S16 + 8 * ks, dnw + (uint64_t)(ks * 128), id_km, ks > 0);
+        commit_w(&V.bar_d);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          mma_ta_w(tmem + TS_O1, tmem + TS_S16 + 8 * ks, desc_k(sb + Q_Q, ks, kC), id_kk, ks > 0);
+      }
+      // Delta^T = D + U^T -> fp16 hi (MMA6) and (Delta Gamma)^T hi / lo (MMA7)
+      __syncwarp();
+      ok = bar_wait(&V.bar_d, (uint32_t)n & 1u);
+      fence_after();
+      if (named_sync_or(kBarChain, 128, !ok)) break;
+      {
+        const float *gam = vec_d(st) + kC;
+        const uint8_t *ub = sm + S_U + lrow * 128;  // U^T row v: box hf holds columns 32 hf .. 32 hf + 31
+        uint32_t r0[32], r1[32];
+        tmem_ld32_nw(tl + TS_D, r0);
+        tmem_ld32_nw(tl + TS_D + 32, r1);
+        tmem_wait_ld();
+        auto half_pass = [&](uint32_t(&rr)[32], const int hf) {
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
-            const float4 f = src[q];
-            v[4 * q] = f.x;
-            v[4 * q + 1] = f.y;
-            v[4 * q + 2] = f.z;
-            v[4 * q + 3] = f.w;
+            const float4 u4 = *reinterpret_cast<const float4 *>(ub + hf * 16384 + ((q ^ (lrow & 7)) << 4));
+            rr[4 * q] = __float_as_uint(__uint_as_float(rr[4 * q]) + u4.x);
+            rr[4 * q + 1] = __float_as_uint(__uint_as_float(rr[4 * q + 1]) + u4.y);
+            rr[4 * q + 2] = __float_as_uint(__uint_as_float(rr[4 * q + 2]) + u4.z);
+            rr[4 * q + 3] = __float_as_uint(__uint_as_float(rr[4 * q + 3]) + u4.w);
           }
-        } else {
+          {
+            uint32_t wh[16];
 #pragma unroll
-          for (int q = 0; q < 32; ++q) v[q] = 0.f;
-        }
-        uint32_t w16[16];
+            for (int q = 0; q < 16; ++q) wh[q] = pack2_inrange(__uint_as_float(rr[2 * q]), __uint_as_float(rr[2 * q + 1]));
+            tmem_st16w_nw(tl + TS_DH + 16 * hf, wh);
+          }
+          uint32_t gh[16], gl[16];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) w16[q] = pack2_sat(v[2 * q], v[2 * q + 1]);
-        tmem_st16w_nw(tl + TS_S16 + k0 / 2, w16);
-#pragma unroll
-        for (int q = 0; q < 32; ++q) v[q] *= dc0;
-        tmem_st32(tl + TS_S + k0, v);
+          for (int q = 0; q < 32; q += 4) {  // times e^{G_last - G_j} <= 1
+            const float4 g = ld4(gam + 32 * hf + q);
+            const float2 p01 = __fmul2_rn(make_float2(__uint_as_float(rr[q]), __uint_as_float(rr[q + 1])), make_float2(g.x, g.y));
+            const float2 p23 =
+                __fmul2_rn(make_float2(__uint_as_float(rr[q + 2]), __uint_as_float(rr[q + 3])), make_float2(g.z, g.w));
+            split2_inrange(p01.x, p01.y, gh[q / 2], gl[q / 2]);
+            split2_inrange(p23.x, p23.y, gh[q / 2 + 1], gl[q / 2 + 1]);
+          }
+          tmem_st16w_nw(tl + TS_DG + 16 * hf, gh);
+          tmem_st16w_nw(tl + TS_DG + 32 + 16 * hf, gl);
+        };
+        half_pass(r0, 0);
+        half_pass(r1, 1);
+        tmem_wait_st();
       }
-      tmem_wait_st();
       fence_before();
       named_sync(kBarChain, 128);
-      for (int n = 0; n < nch; ++n) {
-        const int st = n & 1;
-        const uint32_t sb = sbase + st * kStage;
-        if (*reinterpret_cast<volatile int *>(&V.abort)) break;
-        // MMA4 D = S (-W^T), MMA5 O1 = S Q^T, once the chunk's tiles and U^T
-        // are in and the epilogue has read the previous chunk's O1, O2; the
-        // next chunk's stage is then requested into the previous chunk's buffer.
+      // U^T is read (the producer may load the next); MMA6, MMA7 (issuer).
+      if (issuer) {
+        if (lane == 0) mbar_arrive(&V.bar_ufree);
         __syncwarp();
-        bool w = bar_wait(&V.full[st], (uint32_t)(n >> 1) & 1u);
-        w = bar_wait(&V.bar_u, (uint32_t)n & 1u) && w;
-        if (issuer && n > 0) w = bar_wait(&V.bar_ofree, (uint32_t)(n - 1) & 1u) && w;
-        ok = w;
-        if (named_sync_or(kBarChain, 128, !ok)) break;
-        if (issuer) {
-          if (lane == 0 && n > 0 && n + 1 < nch) request_stage(n + 1);
-          __syncwarp();
-          fence_after();
-          issue_ta_w(tmem + TS_D, tmem + TS_S16, id_km, 8, false, [&](int ks) { return desc_mn(sb + Q_NW, ks, kD); });
-          commit_w(&V.bar_d);
-          issue_ta_w(tmem + TS_O1, tmem + TS_S16, id_kk, 8, false, [&](int ks) { return desc_k(sb + Q_Q, ks, kC); });
-        }
-        // Delta^T = D + U^T -> fp16 hi (MMA6) and (Delta Gamma)^T hi / lo (MMA7)
-        __syncwarp();
-        ok = bar_wait(&V.bar_d, (uint32_t)n & 1u);
         fence_after();
-        if (named_sync_or(kBarChain, 128, !ok)) break;
-        {
-          const float *gam = vec_d[st] + kC;
 #pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            float dv[32];
-            tmem_ld32(tl + TS_D + 32 * hf, dv);
-            const uint8_t *ub = sm + S_U + hf * 16384 + lrow * 128;
+        for (int ks = 0; ks < 4; ++ks)
+          mma_ta_w(tmem + TS_O2, tmem + TS_DH + 8 * ks, desc_k(sb + Q_M, ks, kC), id_kk, ks > 0);
+        commit_w(&V.bar_o);
+        const uint64_t dkh = desc(sb + Q_KH, 8192, 1024), dkl = desc(sb + Q_KL, 8192, 1024);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const float4 u4 = *reinterpret_cast<const float4 *>(ub + ((q ^ (lrow & 7)) << 4));
-              dv[4 * q] += u4.x;
-              dv[4 * q + 1] += u4.y;
-              dv[4 * q + 2] += u4.z;
-              dv[4 * q + 3] += u4.w;
-            }
-            uint32_t wh[16], gh[16], gl[16];
+        for (int ks = 0; ks < 4; ++ks) mma_ta_w(tmem + TS_S, tmem + TS_DG + 8 * ks, dkh + (uint64_t)(ks * 128), id_km128, 1);
 #pragma unroll
-            for (int q = 0; q < 16; ++q) wh[q] = pack2_inrange(dv[2 * q], dv[2 * q + 1]);
+        for (int ks = 0; ks < 4; ++ks) mma_ta_w(tmem + TS_S, tmem + TS_DG + 8 * ks, dkl + (uint64_t)(ks * 128), id_km128, 1);
 #pragma unroll
-            for (int q = 0; q < 32; q += 4) {  // times e^{G_last - G_j} <= 1
-              const float4 g = ld4(gam + 32 * hf + q);
-              const float2 p01 = __fmul2_rn(make_float2(dv[q], dv[q + 1]), make_float2(g.x, g.y));
-              const float2 p23 = __fmul2_rn(make_float2(dv[q + 2], dv[q + 3]), make_float2(g.z, g.w));
-              split2_inrange(p01.x, p01.y, gh[q / 2], gl[q / 2]);
-              split2_inrange(p23.x, p23.y, gh[q / 2 + 1], gl[q / 2 + 1]);
-            }
-            tmem_st16w_nw(tl + TS_DH + 16 * hf, wh);
-            tmem_st16w_nw(tl + TS_DG + 16 * hf, gh);
-            tmem_st16w_nw(tl + TS_DG + 32 + 16 * hf, gl);
-          }
-          tmem_wait_st();
-        }
-        fence_before();
-        named_sync(kBarChain, 128);
-        // U^T is read: the next chunk's may land.  MMA6, MMA7 (issuer).
-        if (warp == 9 && lane == 0 && n + 1 < nch) request_u(n + 1);
-        if (issuer) {
-          fence_after();
-          issue_ta_w(tmem + TS_O2, tmem + TS_DH, id_kk, 4, false, [&](int ks) { return desc_k(sb + Q_M, ks, kC); });
-          commit_w(&V.bar_o);
-          auto b_kh = [&](int ks) { return desc(sb + Q_KH + (uint32_t)(ks * 2048), 8192, 1024); };
-          issue_ta_w(tmem + TS_S, tmem + TS_DG, id_km128, 4, true, b_kh);
-          issue_ta_w(tmem + TS_S, tmem + TS_DG, id_km128, 4, true,
-                     [&](int ks) { return desc(sb + Q_KL + (uint32_t)(ks * 2048), 8192, 1024); });
-          issue_ta_w(tmem + TS_S, tmem + TS_DG + 32, id_km128, 4, true, b_kh);
-          commit_w(&V.bar_s);
-        }
-        // The state pass: the fp16 copy and the rescale by the next chunk's
-        // decay, or S_T after the last chunk.
-        const bool last = n + 1 == nch;
-        const float dcn = dc_n1;
-        dc_n1 = dc_n2;
-        dc_n2 = dc_of(n + 3);
-        __syncwarp();
-        ok = bar_wait(&V.bar_s, (uint32_t)n & 1u);
-        fence_after();
-        if (named_sync_or(kBarChain, 128, !ok)) break;
-#pragma unroll 1
-        for (int k0 = 0; k0 < kD; k0 += 64) {
-          uint32_t r0[32], r1[32];
-          tmem_ld32_nw(tl + TS_S + k0, r0);
-          tmem_ld32_nw(tl + TS_S + k0 + 32, r1);
-          tmem_wait_ld();
+        for (int ks = 0; ks < 4; ++ks)
+          mma_ta_w(tmem + TS_S, tmem + TS_DG + 32 + 8 * ks, dkh + (uint64_t)(ks * 128), id_km128, 1);
+        commit_w(&V.bar_s);
+      }
+      // The state pass: the fp16 copy and the rescale by the next chunk's
+      // decay, or S_T after the last chunk.
+      const bool last = n + 1 == nch;
+      const float dcn = dc_n1;
+      dc_n1 = dc_n2;
+      dc_n2 = dc_of(n + 3);
+      __syncwarp();
+      ok = bar_wait(&V.bar_s, (uint32_t)n & 1u);
+      fence_after();
+      if (named_sync_or(kBarChain, 128, !ok)) break;
+      {
+        // two batches of 64 columns, each loaded with one wait
+        uint32_t ra[32], rb[32];
+        auto block = [&](uint32_t(&r0)[32], const int k0) {
           if (last) {
             float4 *dst = reinterpret_cast<float4 *>(a.S_T + unit_off + (long long)lrow * kD + k0);
 #pragma unroll
             for (int q = 0; q < 8; ++q)
               dst[q] = make_float4(__uint_as_float(r0[4 * q]), __uint_as_float(r0[4 * q + 1]),
                                    __uint_as_float(r0[4 * q + 2]), __uint_as_float(r0[4 * q + 3]));
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              dst[8 + q] = make_float4(__uint_as_float(r1[4 * q]), __uint_as_float(r1[4 * q + 1]),
-                                       __uint_as_float(r1[4 * q + 2]), __uint_as_float(r1[4 * q + 3]));
           } else {
             uint32_t w16[16];
 #pragma unroll
             for (int q = 0; q < 16; ++q) w16[q] = pack2_inrange(__uint_as_float(r0[2 * q]), __uint_as_float(r0[2 * q + 1]));
             tmem_st16w_nw(tl + TS_S16 + k0 / 2, w16);
 #pragma unroll
-            for (int q = 0; q < 16; ++q) w16[q] = pack2_inrange(__uint_as_float(r1[2 * q]), __uint_as_float(r1[2 * q + 1]));
-            tmem_st16w_nw(tl + TS_S16 + k0 / 2 + 16, w16);
-#pragma unroll
             for (int q = 0; q < 32; q += 2) {
-              const float2 x0 = __fmul2_rn(make_float2(__uint_as_float(r0[q]), __uint_as_float(r0[q + 1])), make_float2(dcn, dcn));
-              const float2 x1 = __fmul2_rn(make_float2(__uint_as_float(r1[q]), __uint_as_float(r1[q + 1])), make_float2(dcn, dcn));
+              const float2 x0 =
+                  __fmul2_rn(make_float2(__uint_as_float(r0[q]), __uint_as_float(r0[q + 1])), make_float2(dcn, dcn));
               r0[q] = __float_as_uint(x0.x);
               r0[q + 1] = __float_as_uint(x0.y);
-              r1[q] = __float_as_uint(x1.x);
-              r1[q + 1] = __float_as_uint(x1.y);
             }
             tmem_st32w_nw(tl + TS_S + k0, r0);
-            tmem_st32w_nw(tl + TS_S + k0 + 32, r1);
-            tmem_wait_st();
           }
+        };
+#pragma unroll 1
+        for (int k0 = 0; k0 < kD; k0 += 64) {
+          tmem_ld32_nw(tl + TS_S + k0, ra);
+          tmem_ld32_nw(tl + TS_S + k0 + 32, rb);
+          tmem_wait_ld();
+          block(ra, k0);
+          block(rb, k0 + 32);
         }
-        fence_before();
-        named_sync(kBarChain, 128);
       }
-      if (!ok && tid == 256) {
-        atomicOr(a.err, kErrTimeout);
-        V.abort = 1;
-      }
+      tmem_wait_st();
+      fence_before();
+      named_sync(kBarChain, 128);
     }
+    if (!ok && tid == kIssuerTid) seq_fail(V, a.err);
   } else {
     // ------------------------------------------- the epilogue (warps 0-7)
     const int quad = warp & 3, half = warp >> 2;
@@ -789,7 +873,7 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
     bool ok = true;
     for (int n = 0; n < nch; ++n) {
       const int st = n & 1;
-      if (*reinterpret_cast<volatile int *>(&V.abort)) break;
+      if (seq_aborted(V)) break;
       __syncwarp();
       ok = bar_wait(&V.bar_o, (uint32_t)n & 1u);
       ok = bar_wait(&V.full[st], (uint32_t)(n >> 1) & 1u) && ok;  // this stage's vectors (long landed)
@@ -801,7 +885,7 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
         tmem_ld32_nw(tl + TS_O1 + 32 * half, ra);
         tmem_ld32_nw(tl + TS_O2 + 32 * half, rb);
         tmem_wait_ld();
-        const float *dq = vec_d[st] + 32 * half;
+        const float *dq = vec_d(st) + 32 * half;
 #pragma unroll
         for (int q = 0; q < 32; q += 4) {
           const float4 dd = ld4(dq + q);
@@ -825,12 +909,9 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
       gated_norm<4>(sm, static_cast<const bf16 *>(a.norm_w), static_cast<bf16 *>(a.o), d, bos, h, kC * n, T,
                     2 * warp + (lane >> 4), 16, lane);
       named_sync(kBarEpi, 256);  // z and the staging are read
-      if (tid == 0 && n + 1 < nch) request_z(n + 1);
+      if (tid == 0) mbar_arrive(&V.bar_zfree);
     }
-    if (!ok && tid == 0) {
-      atomicOr(a.err, kErrTimeout);
-      V.abort = 1;
-    }
+    if (!ok && tid == 0) seq_fail(V, a.err);
   }
 
   write_conv_T();
@@ -839,7 +920,7 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
   // was consumed and every MMA waited for).
   fence_before();
   __syncthreads();
-  if (tid == 256) {
+  if (tid == kIssuerTid) {
     for (int st = 0; st < 2; ++st)
       if (V.req_full[st] > 0) bar_wait(&V.full[st], (uint32_t)(V.req_full[st] - 1) & 1u);
     if (V.req_u > 0) bar_wait(&V.bar_u, (uint32_t)(V.req_u - 1) & 1u);

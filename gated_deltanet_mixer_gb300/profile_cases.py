@@ -2,7 +2,7 @@
 
     python -m gated_deltanet_mixer_gb300.profile_cases decode --B 48 --calls 3
     python -m gated_deltanet_mixer_gb300.profile_cases prefill --B 1 --T 2048 --calls 2
-    python -m gated_deltanet_mixer_gb300.profile_cases prefill --B 4 --T 2048 --calls 2 --staged
+    python -m gated_deltanet_mixer_gb300.profile_cases prefill --B 4 --T 2048 --calls 2 --form split
     python -m gated_deltanet_mixer_gb300.profile_cases linear --T 2048 --K 5120 --N 16480 --calls 2
     python -m gated_deltanet_mixer_gb300.profile_cases decode_multi --B 64 --T 4 --calls 2 [--snap]
     python -m gated_deltanet_mixer_gb300.profile_cases serial --B 4 --T 1024 --Hv 32 --calls 2
@@ -35,18 +35,21 @@ def decode(B, Hk, Hv, calls):
         gdn.gdn_decode_step(q, z, g, b, cw, nw, S, conv[s % 2], conv[(s + 1) % 2], o, Hk=Hk, Hv=Hv)
 
 
-def prefill(B, T, Hk, Hv, calls, staged=False):
-    p = I.prefill_problem(B, T, Hk, Hv, io="bf16", case=201)
+def prefill(B, T, Hk, Hv, calls, form="fused", g_mu=3.0):
+    """form: "fused" (no workspace, one kernel), "staged" (q^ / k^ through a
+    workspace, two kernels) or "split" (the chunk-parallel form, three)."""
+    p = I.prefill_problem(B, T, Hk, Hv, io="bf16", case=201, g_mu=g_mu)
     t = torch.bfloat16
     a = p.arrays
     x = [_dev(a["qkv_pre"], t), _dev(a["z"], t), _dev(a["g"]), _dev(a["beta"]),
          _dev(a["conv_w"], t), _dev(a["norm_w"], t), _dev(a["S0"]), _dev(a["conv0"], t)]
     o, S_T, conv_T = gdn.alloc_prefill_outputs(B, T, Hk, Hv, t)
     ws = None
-    if staged:  # the two-kernel path: q^ / k^ through a workspace
-        ws = torch.empty(gdn.gdn_prefill_workspace_bytes(B, T, Hk, Hv), dtype=torch.uint8, device="cuda")
+    if form != "fused":
+        size = gdn.gdn_prefill_staged_bytes if form == "staged" else gdn.gdn_prefill_workspace_bytes
+        ws = torch.empty(size(B, T, Hk, Hv), dtype=torch.uint8, device="cuda")
     for _ in range(calls):
-        if staged:
+        if ws is not None:
             gdn.gdn_prefill_ex(*x, o, S_T, conv_T, Hk=Hk, Hv=Hv, workspace=ws)
         else:
             gdn.gdn_prefill(*x, o, S_T, conv_T, Hk=Hk, Hv=Hv)
@@ -97,7 +100,9 @@ def main():
     ap.add_argument("--K", type=int, default=5120)
     ap.add_argument("--N", type=int, default=16480)
     ap.add_argument("--calls", type=int, default=3)
-    ap.add_argument("--staged", action="store_true", help="prefill through a workspace (two kernels)")
+    ap.add_argument("--form", choices=["fused", "staged", "split"], default="fused",
+                    help="prefill: no workspace, the staged q^/k^ workspace, or the chunk-parallel workspace")
+    ap.add_argument("--g-mu", type=float, default=3.0, help="prefill: mean of the log-decay logits")
     ap.add_argument("--snap", action="store_true", help="decode_multi: a state snapshot after every token")
     a = ap.parse_args()
     gdn.lib()
@@ -110,7 +115,7 @@ def main():
     elif a.kernel == "serial":
         serial(a.B or 4, a.T, a.Hk, a.Hv or 32, a.calls)
     else:
-        prefill(a.B or 4, a.T, a.Hk, a.Hv or 32, a.calls, a.staged)
+        prefill(a.B or 4, a.T, a.Hk, a.Hv or 32, a.calls, a.form, a.g_mu)
     torch.cuda.synchronize()
     st = gdn.gdn_device_status()
     if st != 0:
