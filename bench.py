@@ -40,7 +40,7 @@ if ROOT not in sys.path:
 
 METRIC = "GDN prefill tokens/s (4B/27B shapes) + decode state GB/s vs HBM peak, 1×GB300"
 D = 128
-PREFILL_KERNELS_PER_CALL = 2   # gdn_prefill_ex with a workspace: the q^/k^ kernel, then the chunked kernel
+PREFILL_KERNELS_PER_CALL = 3   # gdn_prefill_ex with a full workspace: q^/k^, the chunk-parallel prep, the sequential pass
 DECODE_KERNELS_PER_CALL = 1    # gdn_decode_step launches one kernel
 DECODE_CALLS_PER_STEP = 64
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -292,9 +292,10 @@ def gdn_arm(args, world, rank, local):
     o, S_T, conv_T = gdn.alloc_prefill_outputs(p.B, p.T, p.Hk, p.Hv, t_io)
     stream = torch.cuda.current_stream()
 
-    # The staged q^ / k^ path: the workspace holds q^ and k^ of every token
-    # and key head between the call's two kernels (calls run one after another
-    # on the stream, so one workspace serves them all).
+    # The chunk-parallel path: the workspace holds q^ and k^ of every token and
+    # key head and every chunk's state-independent part between the call's
+    # three kernels (calls run one after another on the stream, so one
+    # workspace serves them all).
     ws = torch.empty(gdn.gdn_prefill_workspace_bytes(p.B, p.T, p.Hk, p.Hv), dtype=torch.uint8, device="cuda")
 
     def prefill_call(xx, oo, ss, cc):
@@ -468,11 +469,12 @@ def gdn_arm(args, world, rank, local):
                    "parallelism": "one GPU per rank, each rank its own batch (weak scaling)"},
         "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": ach / peaks["hbm_gbs"],
-                     "traffic": recorded_traffic("prefill_kernel", PREFILL_SOURCE),
+                     "traffic": recorded_traffic("prefill_call", PREFILL_SOURCE),
                      "algorithmic_bytes_per_launch": pbytes, "launch_ms": launch_ms,
-                     "scope": "one gdn_prefill_ex call: prefill_qk_kernel (q^, k^ once per key head) "
-                              "then prefill_chunked_kernel; the mixer's algorithmic bytes over the "
-                              "call's device time",
+                     "scope": "one gdn_prefill_ex call: prefill_qk_kernel (q^, k^ once per key head), "
+                              "prefill_prep_kernel (every chunk's T, U, W, M at once), prefill_seq_kernel "
+                              "(the state recurrence per sequence and value head); the mixer's algorithmic "
+                              "bytes over the call's device time; traffic counts the workspace round trip",
                      "peak_source": peak_src + " hbm_gbs (burst copy)"},
         "roofline_tensor": {"bound": "tensor", "achieved": tfl, "peak": peaks["bf16_tflops"],
                             "unit": "TFLOP/s", "frac": tfl / peaks["bf16_tflops"],
@@ -506,7 +508,7 @@ def gdn_arm(args, world, rank, local):
         dist.destroy_process_group()
 
 
-PREFILL_SOURCE = "gated_deltanet_mixer_gb300/csrc/prefill_chunked.cu"
+PREFILL_SOURCE = "gated_deltanet_mixer_gb300/csrc/prefill_split.cu"
 
 
 def time_launches(fn, steps, warmup, stream, barrier, world=1):

@@ -116,6 +116,16 @@ size_t qk_workspace_bytes(const gdn::Dims &d, long long tokens) {
   return 3 * (size_t)tokens * (size_t)d.Hk * gdn::kDHead * 2;
 }
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+// The chunk-parallel form pays where the sequential kernel alone (one CTA per
+// sequence and value head, one per SM) cannot fill the GPU twice over: there
+// the state-independent work moves onto the idle SMs.  With more units the
+// staged form keeps every SM busy and moves fewer bytes.
+bool split_pays(long long units) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return true;
+  return units < 2LL * sms;
+}
 // Workspace of the chunk-parallel / sequential prefill: the staged q^ / k^,
 // then kSplitItemBytes per (chunk slot, value head); 0 when the work items
 // exceed what the kernels index (TMA row coordinates in 31 bits).
@@ -188,7 +198,7 @@ gdn_status prefill_impl(const gdn_shape *shape, const gdn_prefill_io *io, void *
     const size_t need_split = split_workspace_bytes(d, tokens, packed, &sa);
     if ((reinterpret_cast<uintptr_t>(io->workspace) & 255u) != 0) return GDN_ERR_ALIGNMENT;
     if (io->workspace_bytes < need_qk) return GDN_ERR_INVALID_ARG;
-    split = need_split > 0 && io->workspace_bytes >= need_split;
+    split = need_split > 0 && io->workspace_bytes >= need_split && split_pays(d.B * d.Hv);
     const Range rw = range_of(io->workspace, split ? need_split : need_qk);
     for (int i = 0; i < n; ++i)
       if (overlap(rw, in[i])) return GDN_ERR_ALIAS;

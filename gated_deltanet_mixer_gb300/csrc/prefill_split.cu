@@ -453,12 +453,14 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
 // =============================================================================
 // prefill_seq_kernel
 // =============================================================================
-// Warps 0-7: the epilogue (O staging, gated norm); warps 8-11: the chain (the
-// state-dependent MMAs, issued by warp 8, and the Delta and state passes);
-// warp 12: the TMA producer (lane 0 the U^T tiles, lane 1 the chunk stages,
-// lane 2 the z rows), each lane waiting for its buffer to be released.
-constexpr int kSeqThreads = 416;
-constexpr int kProducerWarp = 12;
+// Warps 0-7: the epilogue (O staging, gated norm); warps 8-15: the chain (the
+// state-dependent MMAs, issued by warp 8, and the Delta and state passes, two
+// warps per TMEM lane quadrant, each on half of the columns); warp 16: the TMA
+// producer (lane 0 the U^T tiles, lane 1 the chunk stages, lane 2 the z rows),
+// each lane waiting for its buffer to be released.
+constexpr int kSeqThreads = 544;
+constexpr int kProducerWarp = 16;
+constexpr int kChainThreads = 256;
 constexpr int kIssuerTid = 256;  // warp 8, lane 0
 // One stage (a chunk's tiles), offsets within the stage; fp16, 128-byte swizzle.
 constexpr uint32_t Q_Q = 0;         // q^ K-major [i][k] (64 rows, k halves 8 KB apart)   16 KB
@@ -500,7 +502,7 @@ constexpr uint32_t TS_DG = 320;   // (Delta Gamma)^T fp16: hi 320..351, lo 352..
 constexpr uint32_t TS_DH = 384;   // Delta^T fp16 hi                     32
 constexpr uint32_t TS_S16 = 448;  // state fp16 pairs [v][k/2]           64
 constexpr uint32_t kSeqTmem = 512;
-constexpr int kBarChain = 2;  // warps 8-11
+constexpr int kBarChain = 2;  // warps 8-15
 constexpr int kBarEpi = 3;    // warps 0-7
 
 __device__ __forceinline__ bool seq_aborted(const SeqShared &V) { return *reinterpret_cast<const volatile int *>(&V.abort) != 0; }
@@ -688,9 +690,9 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
       }
     }
   } else if (warp >= 8) {
-    // ------------------------------------------------ the chain (warps 8-11)
-    const int quad = warp - 8;
-    const int lrow = 32 * quad + lane;  // state row v of this thread
+    // ------------------------------------------------ the chain (warps 8-15)
+    const int quad = warp & 3, ch = (warp - 8) >> 2;  // lane quadrant; column half
+    const int lrow = 32 * quad + lane;                // state row v of this thread
     const uint32_t tl = tmem + ((uint32_t)(32 * quad) << 16);
     const bool issuer = warp == 8;
     const uint32_t id_kk = idesc(128, 64, 0, 0), id_km = idesc(128, 64, 0, 1), id_km128 = idesc(128, 128, 0, 1);
@@ -700,9 +702,10 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
     auto dc_of = [&](int n) -> float { return n < nch ? s.ws_vec[item_of(n) * (2 * kC) + kC - 1] : 1.f; };
     const float dc0 = dc_of(0);
     float dc_n1 = dc_of(1), dc_n2 = dc_of(2);
-    // Initial state: TMEM fp32 <- d_C(chunk 0) S0, fp16 copy <- S0.
+    // Initial state: TMEM fp32 <- d_C(chunk 0) S0, fp16 copy <- S0 (this
+    // thread: row lrow, columns 64 ch .. 64 ch + 63).
 #pragma unroll 1
-    for (int k0 = 0; k0 < kD; k0 += 32) {
+    for (int k0 = 64 * ch; k0 < 64 * ch + 64; k0 += 32) {
       float v[32];
       if (a.S0) {
         const float4 *src = reinterpret_cast<const float4 *>(a.S0 + unit_off + (long long)lrow * kD + k0);
@@ -728,7 +731,7 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
     }
     tmem_wait_st();
     fence_before();
-    named_sync(kBarChain, 128);
+    named_sync(kBarChain, kChainThreads);
     for (int n = 0; n < nch; ++n) {
       const int st = n & 1;
       const uint32_t sb = sbase + st * kStage;
@@ -740,7 +743,7 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
       w = bar_wait(&V.bar_u, (uint32_t)n & 1u) && w;
       if (issuer && n > 0) w = bar_wait(&V.bar_ofree, (uint32_t)(n - 1) & 1u) && w;
       ok = w;
-      if (named_sync_or(kBarChain, 128, !ok)) break;
+      if (named_sync_or(kBarChain, kChainThreads, !ok)) break;
       if (issuer) {
         fence_after();
         const uint64_t dnw = desc_mn(sb + Q_NW, 0, kD);
@@ -755,48 +758,44 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
       __syncwarp();
       ok = bar_wait(&V.bar_d, (uint32_t)n & 1u);
       fence_after();
-      if (named_sync_or(kBarChain, 128, !ok)) break;
+      if (named_sync_or(kBarChain, kChainThreads, !ok)) break;
       {
-        const float *gam = vec_d(st) + kC;
-        const uint8_t *ub = sm + S_U + lrow * 128;  // U^T row v: box hf holds columns 32 hf .. 32 hf + 31
-        uint32_t r0[32], r1[32];
-        tmem_ld32_nw(tl + TS_D, r0);
-        tmem_ld32_nw(tl + TS_D + 32, r1);
+        // this thread: row lrow, token columns 32 ch .. 32 ch + 31 (U^T box ch)
+        const float *gam = vec_d(st) + kC + 32 * ch;
+        const uint8_t *ub = sm + S_U + ch * 16384 + lrow * 128;
+        uint32_t rr[32];
+        tmem_ld32_nw(tl + TS_D + 32 * ch, rr);
         tmem_wait_ld();
-        auto half_pass = [&](uint32_t(&rr)[32], const int hf) {
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const float4 u4 = *reinterpret_cast<const float4 *>(ub + hf * 16384 + ((q ^ (lrow & 7)) << 4));
-            rr[4 * q] = __float_as_uint(__uint_as_float(rr[4 * q]) + u4.x);
-            rr[4 * q + 1] = __float_as_uint(__uint_as_float(rr[4 * q + 1]) + u4.y);
-            rr[4 * q + 2] = __float_as_uint(__uint_as_float(rr[4 * q + 2]) + u4.z);
-            rr[4 * q + 3] = __float_as_uint(__uint_as_float(rr[4 * q + 3]) + u4.w);
-          }
-          {
-            uint32_t wh[16];
+        for (int q = 0; q < 8; ++q) {
+          const float4 u4 = *reinterpret_cast<const float4 *>(ub + ((q ^ (lrow & 7)) << 4));
+          rr[4 * q] = __float_as_uint(__uint_as_float(rr[4 * q]) + u4.x);
+          rr[4 * q + 1] = __float_as_uint(__uint_as_float(rr[4 * q + 1]) + u4.y);
+          rr[4 * q + 2] = __float_as_uint(__uint_as_float(rr[4 * q + 2]) + u4.z);
+          rr[4 * q + 3] = __float_as_uint(__uint_as_float(rr[4 * q + 3]) + u4.w);
+        }
+        {
+          uint32_t wh[16];
 #pragma unroll
-            for (int q = 0; q < 16; ++q) wh[q] = pack2_inrange(__uint_as_float(rr[2 * q]), __uint_as_float(rr[2 * q + 1]));
-            tmem_st16w_nw(tl + TS_DH + 16 * hf, wh);
-          }
-          uint32_t gh[16], gl[16];
+          for (int q = 0; q < 16; ++q) wh[q] = pack2_inrange(__uint_as_float(rr[2 * q]), __uint_as_float(rr[2 * q + 1]));
+          tmem_st16w_nw(tl + TS_DH + 16 * ch, wh);
+        }
+        uint32_t gh[16], gl[16];
 #pragma unroll
-          for (int q = 0; q < 32; q += 4) {  // times e^{G_last - G_j} <= 1
-            const float4 g = ld4(gam + 32 * hf + q);
-            const float2 p01 = __fmul2_rn(make_float2(__uint_as_float(rr[q]), __uint_as_float(rr[q + 1])), make_float2(g.x, g.y));
-            const float2 p23 =
-                __fmul2_rn(make_float2(__uint_as_float(rr[q + 2]), __uint_as_float(rr[q + 3])), make_float2(g.z, g.w));
-            split2_inrange(p01.x, p01.y, gh[q / 2], gl[q / 2]);
-            split2_inrange(p23.x, p23.y, gh[q / 2 + 1], gl[q / 2 + 1]);
-          }
-          tmem_st16w_nw(tl + TS_DG + 16 * hf, gh);
-          tmem_st16w_nw(tl + TS_DG + 32 + 16 * hf, gl);
-        };
-        half_pass(r0, 0);
-        half_pass(r1, 1);
+        for (int q = 0; q < 32; q += 4) {  // times e^{G_last - G_j} <= 1
+          const float4 g = ld4(gam + q);
+          const float2 p01 = __fmul2_rn(make_float2(__uint_as_float(rr[q]), __uint_as_float(rr[q + 1])), make_float2(g.x, g.y));
+          const float2 p23 =
+              __fmul2_rn(make_float2(__uint_as_float(rr[q + 2]), __uint_as_float(rr[q + 3])), make_float2(g.z, g.w));
+          split2_inrange(p01.x, p01.y, gh[q / 2], gl[q / 2]);
+          split2_inrange(p23.x, p23.y, gh[q / 2 + 1], gl[q / 2 + 1]);
+        }
+        tmem_st16w_nw(tl + TS_DG + 16 * ch, gh);
+        tmem_st16w_nw(tl + TS_DG + 32 + 16 * ch, gl);
         tmem_wait_st();
       }
       fence_before();
-      named_sync(kBarChain, 128);
+      named_sync(kBarChain, kChainThreads);
       // U^T is read (the producer may load the next); MMA6, MMA7 (issuer).
       if (issuer) {
         if (lane == 0) mbar_arrive(&V.bar_ufree);
@@ -825,10 +824,9 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
       __syncwarp();
       ok = bar_wait(&V.bar_s, (uint32_t)n & 1u);
       fence_after();
-      if (named_sync_or(kBarChain, 128, !ok)) break;
+      if (named_sync_or(kBarChain, kChainThreads, !ok)) break;
       {
-        // two batches of 64 columns, each loaded with one wait
-        uint32_t ra[32], rb[32];
+        uint32_t ra[32];
         auto block = [&](uint32_t(&r0)[32], const int k0) {
           if (last) {
             float4 *dst = reinterpret_cast<float4 *>(a.S_T + unit_off + (long long)lrow * kD + k0);
@@ -851,18 +849,17 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
             tmem_st32w_nw(tl + TS_S + k0, r0);
           }
         };
-#pragma unroll 1
-        for (int k0 = 0; k0 < kD; k0 += 64) {
-          tmem_ld32_nw(tl + TS_S + k0, ra);
-          tmem_ld32_nw(tl + TS_S + k0 + 32, rb);
-          tmem_wait_ld();
-          block(ra, k0);
-          block(rb, k0 + 32);
-        }
+        const int k0 = 64 * ch;  // this thread's 64 columns
+        tmem_ld32_nw(tl + TS_S + k0, ra);
+        tmem_wait_ld();
+        block(ra, k0);
+        tmem_ld32_nw(tl + TS_S + k0 + 32, ra);
+        tmem_wait_ld();
+        block(ra, k0 + 32);
       }
       tmem_wait_st();
       fence_before();
-      named_sync(kBarChain, 128);
+      named_sync(kBarChain, kChainThreads);
     }
     if (!ok && tid == kIssuerTid) seq_fail(V, a.err);
   } else {
@@ -879,25 +876,28 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
       ok = bar_wait(&V.full[st], (uint32_t)(n >> 1) & 1u) && ok;  // this stage's vectors (long landed)
       fence_after();
       if (named_sync_or(kBarEpi, 256, !ok)) break;
-      {  // O^T = d (S Q^T) + Delta^T M^T -> staging [i][v]
+      {  // O^T = d (S Q^T) + Delta^T M^T -> staging [i][v], 16 token columns at a time
         float *ost = reinterpret_cast<float *>(sm + S_OST);
-        uint32_t ra[32], rb[32];
-        tmem_ld32_nw(tl + TS_O1 + 32 * half, ra);
-        tmem_ld32_nw(tl + TS_O2 + 32 * half, rb);
-        tmem_wait_ld();
         const float *dq = vec_d(st) + 32 * half;
 #pragma unroll
-        for (int q = 0; q < 32; q += 4) {
-          const float4 dd = ld4(dq + q);
-          const float2 o01 = __ffma2_rn(make_float2(dd.x, dd.y), make_float2(__uint_as_float(ra[q]), __uint_as_float(ra[q + 1])),
-                                        make_float2(__uint_as_float(rb[q]), __uint_as_float(rb[q + 1])));
-          const float2 o23 = __ffma2_rn(make_float2(dd.z, dd.w),
-                                        make_float2(__uint_as_float(ra[q + 2]), __uint_as_float(ra[q + 3])),
-                                        make_float2(__uint_as_float(rb[q + 2]), __uint_as_float(rb[q + 3])));
-          ost[(32 * half + q + 0) * kD + lrow] = o01.x;
-          ost[(32 * half + q + 1) * kD + lrow] = o01.y;
-          ost[(32 * half + q + 2) * kD + lrow] = o23.x;
-          ost[(32 * half + q + 3) * kD + lrow] = o23.y;
+        for (int c0 = 0; c0 < 32; c0 += 16) {
+          uint32_t ra[16], rb[16];
+          tmem_ld16_nw(tl + TS_O1 + 32 * half + c0, ra);
+          tmem_ld16_nw(tl + TS_O2 + 32 * half + c0, rb);
+          tmem_wait_ld();
+#pragma unroll
+          for (int q = 0; q < 16; q += 4) {
+            const float4 dd = ld4(dq + c0 + q);
+            const float2 o01 = __ffma2_rn(make_float2(dd.x, dd.y), make_float2(__uint_as_float(ra[q]), __uint_as_float(ra[q + 1])),
+                                          make_float2(__uint_as_float(rb[q]), __uint_as_float(rb[q + 1])));
+            const float2 o23 = __ffma2_rn(make_float2(dd.z, dd.w),
+                                          make_float2(__uint_as_float(ra[q + 2]), __uint_as_float(ra[q + 3])),
+                                          make_float2(__uint_as_float(rb[q + 2]), __uint_as_float(rb[q + 3])));
+            ost[(32 * half + c0 + q + 0) * kD + lrow] = o01.x;
+            ost[(32 * half + c0 + q + 1) * kD + lrow] = o01.y;
+            ost[(32 * half + c0 + q + 2) * kD + lrow] = o23.x;
+            ost[(32 * half + c0 + q + 3) * kD + lrow] = o23.y;
+          }
         }
       }
       fence_before();

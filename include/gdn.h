@@ -177,7 +177,10 @@ typedef struct {
  *               call and it must not be shared by calls that may run
  *               concurrently.  The chunked prefill takes the fastest form
  *               the workspace holds:
- *                 >= gdn_prefill_workspace_bytes(): the chunk-parallel form.
+ *                 >= gdn_prefill_workspace_bytes(), and B * Hv (sequences x
+ *                    value heads) below twice the GPU's SM count: the
+ *                    chunk-parallel form (with more units the staged form
+ *                    below already fills every SM, and moves fewer bytes).
  *                    q^ and k^ are formed once per key head (first kernel);
  *                    everything of a chunk that does not depend on the
  *                    carried state (the inverse T, U, W, the decayed
