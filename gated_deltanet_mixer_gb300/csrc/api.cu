@@ -300,6 +300,7 @@ const char *gdn_status_str(int s) {
     case GDN_ERR_CUDA: return "CUDA runtime error";
     case GDN_ERR_TIMEOUT: return "device-side wait timed out";
     case GDN_ERR_NO_DEVICE: return "current device is not an sm_103 GPU";
+    case GDN_ERR_BOUNDS: return "device bounds check failed";
     default: return "unknown status";
   }
 }
@@ -439,6 +440,7 @@ gdn_status gdn_device_status(void *stream, int reset) {
       return GDN_ERR_CUDA;
   }
   if (word & gdn::kErrTimeout) return GDN_ERR_TIMEOUT;
+  if (word & gdn::kErrBounds) return GDN_ERR_BOUNDS;
   if (word & gdn::kErrSeqlens) return GDN_ERR_INVALID_ARG;
   return GDN_OK;
 }

@@ -30,7 +30,8 @@ constexpr int kRowsPerWarp = 16;
 // into conv_out when `write_window` is set.
 template <typename IO>
 __device__ __forceinline__ float conv_token(const IO *win, const IO *x, const IO *conv_w, IO *wout,
-                                            long long C, long long c, bool write_window) {
+                                            long long C, long long c, bool write_window, long long wout_end,
+                                            long long win_size, unsigned int *err) {
   float x0 = ld_io(win + c), x1 = ld_io(win + C + c), x2 = ld_io(win + 2 * C + c);
   float x3 = ld_io(x + c);
   float4 w = ld_io4(conv_w + 4 * c);
@@ -38,7 +39,7 @@ __device__ __forceinline__ float conv_token(const IO *win, const IO *x, const IO
   acc = fmaf(w.y, x1, acc);
   acc = fmaf(w.z, x2, acc);
   acc = fmaf(w.w, x3, acc);
-  if (write_window) {
+  if (write_window && in_bounds(wout_end + 2 * C + c + 1, win_size, err)) {
     // raw values are copied bit-exactly (same io type)
     wout[c] = win[C + c];
     wout[C + c] = win[2 * C + c];
@@ -85,6 +86,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode1_kernel(DecodeArgs a) {
   const IO *win = static_cast<const IO *>(a.conv_in) + (long long)b * 3 * C;
   IO *wout = static_cast<IO *>(a.conv_out) + (long long)b * 3 * C;
   const IO *cw = static_cast<const IO *>(a.conv_w);
+  const long long wbase = (long long)b * 3 * C, wsize = (long long)d.B * 3 * C;  // window offset, elements
+  const long long S_size = (long long)d.B * d.Hv * kD * kD;
 
   // This warp's 16 state rows and this thread's z element, requested first:
   // their latency overlaps the front end's.  (Requesting the gates here too
@@ -101,11 +104,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode1_kernel(DecodeArgs a) {
   float qraw = 0.f, kraw = 0.f;
   if (tid < kD) {
     const bool owner = (h % r) == 0;  // one CTA per key head shifts its q/k window
-    qraw = conv_token(win, x, cw, wout, C, (long long)kh * kD + tid, owner);
-    kraw = conv_token(win, x, cw, wout, C, (long long)d.Hk * kD + (long long)kh * kD + tid, owner);
+    qraw = conv_token(win, x, cw, wout, C, (long long)kh * kD + tid, owner, wbase, wsize, a.err);
+    kraw = conv_token(win, x, cw, wout, C, (long long)d.Hk * kD + (long long)kh * kD + tid, owner, wbase, wsize, a.err);
   } else {
     const int i = tid - kD;
-    s_v[i] = conv_token(win, x, cw, wout, C, 2LL * d.Hk * kD + (long long)h * kD + i, true);
+    s_v[i] = conv_token(win, x, cw, wout, C, 2LL * d.Hk * kD + (long long)h * kD + i, true, wbase, wsize, a.err);
   }
   float sq = warp_sum(qraw * qraw), sk = warp_sum(kraw * kraw);
   if (lane == 0) {
@@ -163,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode1_kernel(DecodeArgs a) {
     n.y = fmaf(alpha, s[i].y, di * k4.y);
     n.z = fmaf(alpha, s[i].z, di * k4.z);
     n.w = fmaf(alpha, s[i].w, di * k4.w);
-    st_stream(S + (row0 + i) * kD + 4 * lane, n);
+    if (in_bounds(gi * (kD * kD) + (row0 + i) * kD + 4 * lane + 4, S_size, a.err)) st_stream(S + (row0 + i) * kD + 4 * lane, n);
   }
   __syncthreads();
 
@@ -178,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode1_kernel(DecodeArgs a) {
     float rstd = rsqrtf(tot * (1.0f / kD) + d.eps_norm);
     const long long oi = gi * kD + tid;  // [B][Hv*Dv]
     float wv = ld_io(static_cast<const IO *>(a.norm_w) + tid);
-    st_io(static_cast<IO *>(a.o) + oi, wv * (ov * rstd) * silu(zv));
+    if (in_bounds(oi + 1, (long long)d.B * d.Hv * kD, a.err)) st_io(static_cast<IO *>(a.o) + oi, wv * (ov * rstd) * silu(zv));
   }
 }
 
@@ -275,12 +278,15 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
       }
     }
     // the new window: the last three raw rows (one CTA per key head shifts q/k)
+    const long long wsize = (long long)d.B * 3 * C, wbase = (long long)b * 3 * C;
     if (!qk || (h % r) == 0) {
 #pragma unroll
-      for (int e = 0; e < 3; ++e) st_io(wout + e * C + c0, w0[e]);
+      for (int e = 0; e < 3; ++e)
+        if (in_bounds(wbase + e * C + c0 + 1, wsize, a.err)) st_io(wout + e * C + c0, w0[e]);
       if (qk) {
 #pragma unroll
-        for (int e = 0; e < 3; ++e) st_io(wout + e * C + c1, w1[e]);
+        for (int e = 0; e < 3; ++e)
+          if (in_bounds(wbase + e * C + c1 + 1, wsize, a.err)) st_io(wout + e * C + c1, w1[e]);
       }
     }
   }
@@ -331,13 +337,18 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
       s[i] = decay_update(s[i], alpha, di, k4);
     }
     if (a.S_snap) {
-      float *snap = a.S_snap + (((long long)b * T + t) * d.Hv + h) * (kD * kD);
+      const long long so = (((long long)b * T + t) * d.Hv + h) * (kD * kD);
+      float *snap = a.S_snap + so;
 #pragma unroll
-      for (int i = 0; i < kRowsPerWarp; ++i) st_stream(snap + (row0 + i) * kD + 4 * lane, s[i]);
+      for (int i = 0; i < kRowsPerWarp; ++i)
+        if (in_bounds(so + (row0 + i) * kD + 4 * lane + 4, (long long)d.B * T * d.Hv * kD * kD, a.err))
+          st_stream(snap + (row0 + i) * kD + 4 * lane, s[i]);
     }
   }
 #pragma unroll
-  for (int i = 0; i < kRowsPerWarp; ++i) st_stream(S + (row0 + i) * kD + 4 * lane, s[i]);
+  for (int i = 0; i < kRowsPerWarp; ++i)
+    if (in_bounds(gi * (kD * kD) + (row0 + i) * kD + 4 * lane + 4, (long long)d.B * d.Hv * kD * kD, a.err))
+      st_stream(S + (row0 + i) * kD + 4 * lane, s[i]);
   __syncthreads();
 
   // ---- gated RMSNorm over the head's 128 outputs, one warp per token
@@ -346,6 +357,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
     const float4 o4 = reinterpret_cast<const float4 *>(s_o[t])[lane];
     const float rstd = rsqrtf(warp_sum(dot4(o4, o4)) * (1.0f / kD) + d.eps_norm);
     const long long oi = (((long long)b * T + t) * d.Hv + h) * kD + 4 * lane;  // [B][T][Hv*Dv]
+    if (!in_bounds(oi + 4, (long long)d.B * T * d.Hv * kD, a.err)) continue;
     const float4 z4 = reinterpret_cast<const float4 *>(s_z[t])[lane];
     float4 y;
     y.x = w4.x * (o4.x * rstd) * silu(z4.x);

@@ -115,5 +115,25 @@ cudaError_t launch_wait_selftest(unsigned int *err, unsigned long long limit_ns,
 // Device error bits (the error word is OR-ed).
 constexpr unsigned int kErrTimeout = 1u;  // a bounded wait gave up
 constexpr unsigned int kErrSeqlens = 2u;  // packed-sequence offsets out of order or range
+constexpr unsigned int kErrBounds = 4u;   // a GDN_CHECKS bounds check failed
+
+// GDN_CHECKS builds check every thread-issued global store of the prefill
+// (q/k, prep and sequential kernels) and decode kernels against its buffer:
+// `end` is one past the last element the store writes, `size` the buffer's
+// element count.  A failed check sets kErrBounds in the error word and the
+// caller skips the store; there is no trap.  Other builds compile it away.
+__device__ __forceinline__ bool in_bounds(long long end, long long size, unsigned int *err) {
+#ifdef GDN_CHECKS
+  if (end > size || end <= 0) {
+    atomicOr(err, kErrBounds);
+    return false;
+  }
+#else
+  (void)end;
+  (void)size;
+  (void)err;
+#endif
+  return true;
+}
 
 }  // namespace gdn

@@ -1449,7 +1449,7 @@ __global__ void __launch_bounds__(kQkThreads, 2)
       const float f = rsqrtf(ss + d.eps_l2) * scale;
 #pragma unroll
       for (int i = 0; i < 4; ++i) u[i] = __fmul2_rn(u[i], make_float2(f, f));
-      if (valid) {
+      if (valid && in_bounds((dst - static_cast<const __half *>(a.qk_ws)) + (blk == 1 ? plane : 0) + 8, 3 * plane, a.err)) {
         uint32_t wh[4], wl[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) split2_inrange(u[i].x, u[i].y, wh[i], wl[i]);  // |k^|, |q^| <= 1

@@ -389,7 +389,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     }
     if (tid < 2 * kC) {  // the chunk vectors d and Gamma, fp32 [2][64]
       float *vec = s.ws_vec + item * (2 * kC);
-      vec[tid] = tid < kC ? V.cv.d[tid] : V.cv.gam[tid - kC];
+      if (in_bounds(item * (2 * kC) + tid + 1, nitems * (2 * kC), a.err)) vec[tid] = tid < kC ? V.cv.d[tid] : V.cv.gam[tid - kC];
     }
     __syncwarp();
     ok = bar_wait(&V.bar_uw, ph_uw);
@@ -516,7 +516,8 @@ __device__ __forceinline__ void seq_fail(SeqShared &V, unsigned int *err) {
 // staged z rows, to o (valid tokens only).
 template <int NR>
 __device__ __forceinline__ void gated_norm(const uint8_t *sm, const bf16 *norm_w, bf16 *o, const Dims &d, long long bos,
-                                           int h, int t0, int T, int i0, int di, int lane) {
+                                           int h, int t0, int T, int i0, int di, int lane, long long o_size,
+                                           unsigned int *err) {
   const float *ost = reinterpret_cast<const float *>(sm + S_OST);
   const int hl = lane & 15;
   float2 wn[4];
@@ -551,7 +552,8 @@ __device__ __forceinline__ void gated_norm(const uint8_t *sm, const bf16 *norm_w
       __nv_bfloat162 t = __floats2bfloat162_rn(y.x, y.y);
       yw[q] = *reinterpret_cast<uint32_t *>(&t);
     }
-    if (valid) *reinterpret_cast<uint4 *>(ob + i * ostride) = make_uint4(yw[0], yw[1], yw[2], yw[3]);
+    if (valid && in_bounds((ob + i * ostride - o) + 8, o_size, err))
+      *reinterpret_cast<uint4 *>(ob + i * ostride) = make_uint4(yw[0], yw[1], yw[2], yw[3]);
   }
 }
 
@@ -586,6 +588,8 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
     T = d.T;
   }
   const long long unit_off = ((long long)b * d.Hv + h) * kD * kD;
+  const long long S_size = (long long)d.B * d.Hv * kD * kD;                                        // S_T elements
+  const long long o_size = (a.cu_seqlens ? (long long)d.T : (long long)d.B * d.T) * d.Hv * kD;  // o elements
   const bf16 *x = static_cast<const bf16 *>(a.qkv_pre) + bos * C;
   const bf16 *conv0 = a.conv0 ? static_cast<const bf16 *>(a.conv0) + (long long)b * 3 * C : nullptr;
   const int cq = kh * kD, ck = d.Hk * kD + kh * kD, cvv = 2 * d.Hk * kD + h * kD;
@@ -603,14 +607,15 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
       if (t >= 0) val = x[(long long)t * C + cc];
       else if (conv0) val = conv0[(long long)(3 + t) * C + cc];
       else val = bf16(0.f);
-      cT[(long long)e * C + cc] = val;
+      if (in_bounds(((long long)b * 3 + e) * C + cc + 1, (long long)d.B * 3 * C, a.err)) cT[(long long)e * C + cc] = val;
     }
   };
   if (T == 0) {  // an empty packed sequence: state and window pass through
     float4 *dst = reinterpret_cast<float4 *>(a.S_T + unit_off);
     const float4 *src = a.S0 ? reinterpret_cast<const float4 *>(a.S0 + unit_off) : nullptr;
     if (src != dst)
-      for (int i = tid; i < kD * kD / 4; i += kSeqThreads) dst[i] = src ? src[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int i = tid; i < kD * kD / 4; i += kSeqThreads)
+        if (in_bounds(unit_off + 4 * i + 4, S_size, a.err)) dst[i] = src ? src[i] : make_float4(0.f, 0.f, 0.f, 0.f);
     write_conv_T();
     return;
   }
@@ -830,10 +835,11 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
         auto block = [&](uint32_t(&r0)[32], const int k0) {
           if (last) {
             float4 *dst = reinterpret_cast<float4 *>(a.S_T + unit_off + (long long)lrow * kD + k0);
+            if (in_bounds(unit_off + (long long)lrow * kD + k0 + 32, S_size, a.err))
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-              dst[q] = make_float4(__uint_as_float(r0[4 * q]), __uint_as_float(r0[4 * q + 1]),
-                                   __uint_as_float(r0[4 * q + 2]), __uint_as_float(r0[4 * q + 3]));
+              for (int q = 0; q < 8; ++q)
+                dst[q] = make_float4(__uint_as_float(r0[4 * q]), __uint_as_float(r0[4 * q + 1]),
+                                     __uint_as_float(r0[4 * q + 2]), __uint_as_float(r0[4 * q + 3]));
           } else {
             uint32_t w16[16];
 #pragma unroll
@@ -907,7 +913,7 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
       ok = bar_wait(&V.bar_z, (uint32_t)n & 1u);
       if (named_sync_or(kBarEpi, 256, !ok)) break;
       gated_norm<4>(sm, static_cast<const bf16 *>(a.norm_w), static_cast<bf16 *>(a.o), d, bos, h, kC * n, T,
-                    2 * warp + (lane >> 4), 16, lane);
+                    2 * warp + (lane >> 4), 16, lane, o_size, a.err);
       named_sync(kBarEpi, 256);  // z and the staging are read
       if (tid == 0) mbar_arrive(&V.bar_zfree);
     }

@@ -11,14 +11,16 @@ import os
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libgdn.so")
+# GDN_CHECKS=1: the bounds-checked build (python -m gated_deltanet_mixer_gb300.build --checks)
+LIB_PATH = os.path.join(_HERE, "libgdn_checks.so" if os.environ.get("GDN_CHECKS", "0") not in ("", "0")
+                        else "libgdn.so")
 
 GDN_OK = 0
 GDN_ERR_INVALID_ARG = 1
 GDN_ERR_TIMEOUT = 6
 STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED_SHAPE",
                 3: "GDN_ERR_ALIGNMENT", 4: "GDN_ERR_ALIAS", 5: "GDN_ERR_CUDA",
-                6: "GDN_ERR_TIMEOUT", 7: "GDN_ERR_NO_DEVICE"}
+                6: "GDN_ERR_TIMEOUT", 7: "GDN_ERR_NO_DEVICE", 8: "GDN_ERR_BOUNDS"}
 GDN_F32, GDN_BF16 = 0, 1
 GDN_STATIC_SCRATCH_BYTES = 512 << 20  # include/gdn.h: the scratch of gdn_prefill_static
 

@@ -77,7 +77,8 @@ typedef enum {
   GDN_ERR_ALIAS = 4,             /* two buffers overlap where that is forbidden */
   GDN_ERR_CUDA = 5,              /* a CUDA runtime call failed */
   GDN_ERR_TIMEOUT = 6,           /* a device-side wait gave up (see gdn_device_status) */
-  GDN_ERR_NO_DEVICE = 7          /* the current device is not an sm_103 GPU */
+  GDN_ERR_NO_DEVICE = 7,         /* the current device is not an sm_103 GPU */
+  GDN_ERR_BOUNDS = 8             /* a device bounds check failed (GDN_CHECKS builds only) */
 } gdn_status;
 
 typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
@@ -315,9 +316,12 @@ gdn_status gdn_linear(int M, int N, int K, const void *x, long long ldx, const v
 /*
  * Synchronise `stream` and report device-side failures recorded since the
  * last reset: GDN_ERR_TIMEOUT if a kernel's bounded wait gave up (the kernel
- * then returned early and its outputs are incomplete), GDN_ERR_INVALID_ARG
- * if a kernel met packed-sequence offsets it could not use, GDN_ERR_CUDA if
- * the synchronisation itself failed, GDN_OK otherwise.  reset != 0 clears the
+ * then returned early and its outputs are incomplete), GDN_ERR_BOUNDS if a
+ * store failed its bounds check (only in a library built with GDN_CHECKS,
+ * where every thread-issued global store of the prefill and decode kernels
+ * is checked against its buffer and skipped when outside it),
+ * GDN_ERR_INVALID_ARG if a kernel met packed-sequence offsets it could not
+ * use, GDN_ERR_CUDA if the synchronisation itself failed, GDN_OK otherwise.  reset != 0 clears the
  * record afterwards.  The record is one word per device, shared by all
  * streams.
  */

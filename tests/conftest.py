@@ -38,14 +38,29 @@ def golden():
     return read_golden
 
 
+@pytest.fixture(autouse=True)
+def _canaries(request, monkeypatch):
+    """GPU tests: guard bands around every buffer a libgdn call writes."""
+    if request.node.get_closest_marker("gpu") is None:
+        yield
+        return
+    import guards
+    guards.install(monkeypatch)
+    yield
+
+
 def pytest_terminal_summary(terminalreporter):
     """The o error yardsticks over every GPU comparison of the run (see
     gpu_harness.REPORT): the largest of each, relative to rms(o_ref)."""
+    tr = terminalreporter
+    g = sys.modules.get("guards")
+    if g and g.checked["calls"]:
+        tr.write_sep("-", "canaries: %d guarded calls, %d buffers, every guard band intact"
+                     % (g.checked["calls"], g.checked["buffers"]))
     h = sys.modules.get("gpu_harness")
     rep = getattr(h, "REPORT", None) if h else None
     if not rep:
         return
-    tr = terminalreporter
     tr.write_sep("-", "o error over %d comparisons (max, relative to rms(o_ref))" % len(rep))
     for key, label in (("excess", "asserted: |o_gpu - o_ref| - bf16 quantum"),
                        ("plain", "plain: |o_gpu - o_ref|"),
