@@ -512,38 +512,50 @@ __device__ __forceinline__ void seq_fail(SeqShared &V, unsigned int *err) {
 }
 
 // The gated RMSNorm (node gdn.norm) of NR tokens i0, i0 + di, ... of the chunk,
-// one half-warp per token (8 channels per lane), from the O staging and the
-// staged z rows, to o (valid tokens only).
+// one half-warp per token (8 channels per lane).  norm_load takes the staged O
+// and z rows into registers (after it the z buffer may be refilled);
+// norm_store forms y and writes o (valid tokens only).
 template <int NR>
-__device__ __forceinline__ void gated_norm(const uint8_t *sm, const bf16 *norm_w, bf16 *o, const Dims &d, long long bos,
-                                           int h, int t0, int T, int i0, int di, int lane, long long o_size,
-                                           unsigned int *err) {
+struct NormRegs {
+  float4 o0[NR], o1[NR];
+  uint4 z[NR];
+};
+template <int NR>
+__device__ __forceinline__ void norm_load(const uint8_t *sm, NormRegs<NR> &R, int nv, int i0, int di, int lane) {
   const float *ost = reinterpret_cast<const float *>(sm + S_OST);
+  const int hl = lane & 15;
+#pragma unroll
+  for (int m = 0; m < NR; ++m) {
+    const int i = i0 + di * m;
+    R.o0[m] = R.o1[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+    R.z[m] = make_uint4(0u, 0u, 0u, 0u);
+    if (i < nv) {
+      R.o0[m] = ld4(ost + i * kD + 8 * hl);
+      R.o1[m] = ld4(ost + i * kD + 8 * hl + 4);
+      R.z[m] = *reinterpret_cast<const uint4 *>(sm + S_Z + i * kD * 2 + 16 * hl);
+    }
+  }
+}
+template <int NR>
+__device__ __forceinline__ void norm_store(const NormRegs<NR> &R, const bf16 *norm_w, bf16 *o, const Dims &d,
+                                           long long bos, int h, int t0, int nv, int i0, int di, int lane,
+                                           long long o_size, unsigned int *err) {
   const int hl = lane & 15;
   float2 wn[4];
   widen(*reinterpret_cast<const uint4 *>(norm_w + 8 * hl), wn);
-  const int nv = min(kC, T - t0);
   bf16 *ob = o + ((bos + t0) * d.Hv + h) * kD + 8 * hl;
   const long long ostride = (long long)d.Hv * kD;
 #pragma unroll
   for (int m = 0; m < NR; ++m) {
     const int i = i0 + di * m;
-    const bool valid = i < nv;
-    float4 o0 = make_float4(0.f, 0.f, 0.f, 0.f), o1 = o0;
-    uint4 zr = make_uint4(0u, 0u, 0u, 0u);
-    if (valid) {
-      o0 = ld4(ost + i * kD + 8 * hl);
-      o1 = ld4(ost + i * kD + 8 * hl + 4);
-      zr = *reinterpret_cast<const uint4 *>(sm + S_Z + i * kD * 2 + 16 * hl);
-    }
-    float ss = dot4(o0, o0) + dot4(o1, o1);
+    float ss = dot4(R.o0[m], R.o0[m]) + dot4(R.o1[m], R.o1[m]);
 #pragma unroll
     for (int off = 1; off < 16; off <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
     const float rstd = rsqrtf(ss * (1.0f / kD) + d.eps_norm);
     float2 zz[4];
-    widen(zr, zz);
-    const float2 op[4] = {make_float2(o0.x, o0.y), make_float2(o0.z, o0.w), make_float2(o1.x, o1.y),
-                          make_float2(o1.z, o1.w)};
+    widen(R.z[m], zz);
+    const float2 op[4] = {make_float2(R.o0[m].x, R.o0[m].y), make_float2(R.o0[m].z, R.o0[m].w),
+                          make_float2(R.o1[m].x, R.o1[m].y), make_float2(R.o1[m].z, R.o1[m].w)};
     uint32_t yw[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -552,7 +564,7 @@ __device__ __forceinline__ void gated_norm(const uint8_t *sm, const bf16 *norm_w
       __nv_bfloat162 t = __floats2bfloat162_rn(y.x, y.y);
       yw[q] = *reinterpret_cast<uint32_t *>(&t);
     }
-    if (valid && in_bounds((ob + i * ostride - o) + 8, o_size, err))
+    if (i < nv && in_bounds((ob + i * ostride - o) + 8, o_size, err))
       *reinterpret_cast<uint4 *>(ob + i * ostride) = make_uint4(yw[0], yw[1], yw[2], yw[3]);
   }
 }
@@ -741,15 +753,16 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
       const int st = n & 1;
       const uint32_t sb = sbase + st * kStage;
       if (seq_aborted(V)) break;
-      // MMA4 D = S (-W^T), MMA5 O1 = S Q^T, once the chunk's tiles and U^T are
-      // in and the epilogue has read the previous chunk's O1, O2.
+      // MMA4 D = S (-W^T), MMA5 O1 = S Q^T (warp 8), once the chunk's tiles and
+      // U^T are in and the epilogue has read the previous chunk's O1, O2.  The
+      // other chain warps go on to wait for D.  A wait that times out is voted
+      // on once, at the chunk's closing barrier.
       __syncwarp();
       bool w = bar_wait(&V.full[st], (uint32_t)(n >> 1) & 1u);
       w = bar_wait(&V.bar_u, (uint32_t)n & 1u) && w;
       if (issuer && n > 0) w = bar_wait(&V.bar_ofree, (uint32_t)(n - 1) & 1u) && w;
-      ok = w;
-      if (named_sync_or(kBarChain, kChainThreads, !ok)) break;
-      if (issuer) {
+      ok = ok && w;
+      if (issuer && __all_sync(0xffffffffu, w)) {
         fence_after();
         const uint64_t dnw = desc_mn(sb + Q_NW, 0, kD);
 #pragma unroll
@@ -761,9 +774,8 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
       }
       // Delta^T = D + U^T -> fp16 hi (MMA6) and (Delta Gamma)^T hi / lo (MMA7)
       __syncwarp();
-      ok = bar_wait(&V.bar_d, (uint32_t)n & 1u);
+      ok = bar_wait(&V.bar_d, (uint32_t)n & 1u) && ok;
       fence_after();
-      if (named_sync_or(kBarChain, kChainThreads, !ok)) break;
       {
         // this thread: row lrow, token columns 32 ch .. 32 ch + 31 (U^T box ch)
         const float *gam = vec_d(st) + kC + 32 * ch;
@@ -827,15 +839,14 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
       dc_n1 = dc_n2;
       dc_n2 = dc_of(n + 3);
       __syncwarp();
-      ok = bar_wait(&V.bar_s, (uint32_t)n & 1u);
+      ok = bar_wait(&V.bar_s, (uint32_t)n & 1u) && ok;
       fence_after();
-      if (named_sync_or(kBarChain, kChainThreads, !ok)) break;
       {
         uint32_t ra[32];
         auto block = [&](uint32_t(&r0)[32], const int k0) {
           if (last) {
             float4 *dst = reinterpret_cast<float4 *>(a.S_T + unit_off + (long long)lrow * kD + k0);
-            if (in_bounds(unit_off + (long long)lrow * kD + k0 + 32, S_size, a.err))
+            if (ok && in_bounds(unit_off + (long long)lrow * kD + k0 + 32, S_size, a.err))
 #pragma unroll
               for (int q = 0; q < 8; ++q)
                 dst[q] = make_float4(__uint_as_float(r0[4 * q]), __uint_as_float(r0[4 * q + 1]),
@@ -865,7 +876,7 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
       }
       tmem_wait_st();
       fence_before();
-      named_sync(kBarChain, kChainThreads);
+      if (named_sync_or(kBarChain, kChainThreads, !ok)) break;
     }
     if (!ok && tid == kIssuerTid) seq_fail(V, a.err);
   } else {
@@ -878,10 +889,9 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
       const int st = n & 1;
       if (seq_aborted(V)) break;
       __syncwarp();
-      ok = bar_wait(&V.bar_o, (uint32_t)n & 1u);
+      ok = bar_wait(&V.bar_o, (uint32_t)n & 1u) && ok;
       ok = bar_wait(&V.full[st], (uint32_t)(n >> 1) & 1u) && ok;  // this stage's vectors (long landed)
       fence_after();
-      if (named_sync_or(kBarEpi, 256, !ok)) break;
       {  // O^T = d (S Q^T) + Delta^T M^T -> staging [i][v], 16 token columns at a time
         float *ost = reinterpret_cast<float *>(sm + S_OST);
         const float *dq = vec_d(st) + 32 * half;
@@ -909,13 +919,18 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
       fence_before();
       named_sync(kBarEpi, 256);
       if (tid == 0) mbar_arrive(&V.bar_ofree);  // O1, O2 and this stage's vectors are read
+      // The gated norm of the chunk's 64 tokens (4 per half-warp): staged O and
+      // z into registers, the z buffer released, then y formed and stored.
       __syncwarp();
-      ok = bar_wait(&V.bar_z, (uint32_t)n & 1u);
-      if (named_sync_or(kBarEpi, 256, !ok)) break;
-      gated_norm<4>(sm, static_cast<const bf16 *>(a.norm_w), static_cast<bf16 *>(a.o), d, bos, h, kC * n, T,
-                    2 * warp + (lane >> 4), 16, lane, o_size, a.err);
-      named_sync(kBarEpi, 256);  // z and the staging are read
+      ok = bar_wait(&V.bar_z, (uint32_t)n & 1u) && ok;
+      const int nv = min(kC, T - kC * n), i0 = 2 * warp + (lane >> 4);
+      NormRegs<4> R;
+      norm_load<4>(sm, R, nv, i0, 16, lane);
+      named_sync(kBarEpi, 256);
       if (tid == 0) mbar_arrive(&V.bar_zfree);
+      if (ok) norm_store<4>(R, static_cast<const bf16 *>(a.norm_w), static_cast<bf16 *>(a.o), d, bos, h, kC * n, nv, i0,
+                            16, lane, o_size, a.err);
+      if (named_sync_or(kBarEpi, 256, !ok)) break;  // the staging is read; a timeout is voted on here
     }
     if (!ok && tid == 0) seq_fail(V, a.err);
   }
