@@ -212,6 +212,7 @@ gdn_status prefill_impl(const gdn_shape *shape, const gdn_prefill_io *io, void *
       sa.ws_nw = base + (size_t)items * 32768;
       sa.ws_m = base + (size_t)items * (32768 + 16384);
       sa.ws_vec = reinterpret_cast<float *>(base + (size_t)items * (32768 + 16384 + 8192));
+      sa.flags = reinterpret_cast<int *>(base + (size_t)items * (32768 + 16384 + 8192 + 512));
     }
   }
   unsigned int *err = nullptr;
@@ -223,7 +224,8 @@ gdn_status prefill_impl(const gdn_shape *shape, const gdn_prefill_io *io, void *
   if (!chunked) {
     e = gdn::launch_prefill(a, bf16, (cudaStream_t)stream);
   } else {
-    e = ws ? gdn::launch_prefill_qk(a, (cudaStream_t)stream) : cudaSuccess;
+    e = ws ? gdn::launch_prefill_qk(a, (cudaStream_t)stream, sa.flags, split ? (long long)sa.nslots * d.Hv : 0)
+           : cudaSuccess;
     if (e == cudaSuccess)
       e = split ? gdn::launch_prefill_split(a, sa, (cudaStream_t)stream)
                 : gdn::launch_prefill_chunked(a, true, (cudaStream_t)stream);

@@ -82,7 +82,8 @@ struct GemmArgs {
 cudaError_t launch_decode(const DecodeArgs &a, bool bf16, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillArgs &a, bool bf16, cudaStream_t s);          // token-serial
 cudaError_t launch_prefill_chunked(const PrefillArgs &a, bool bf16, cudaStream_t s);  // chunked WY, tcgen05
-cudaError_t launch_prefill_qk(const PrefillArgs &a, cudaStream_t s);  // q^ / k^ into a.qk_ws (bf16 io)
+// q^ / k^ into a.qk_ws (bf16 io); also zeroes nzero ints at `zero` (may be null).
+cudaError_t launch_prefill_qk(const PrefillArgs &a, cudaStream_t s, int *zero = nullptr, long long nzero = 0);
 
 // The chunk-parallel / sequential prefill (prefill_split.cu).  Chunk slots
 // index the workspace: fixed length, slot = b * nch + n; packed sequences,
@@ -92,6 +93,9 @@ cudaError_t launch_prefill_qk(const PrefillArgs &a, cudaStream_t s);  // q^ / k^
 //   ws_nw  [items][128 k][64 j]  fp16   -W^T
 //   ws_m   [items][64 i][64 j]   fp16   M = (Q K^T) o R (lower, diagonal included)
 //   ws_vec [items][2][64]        fp32   d_i = e^{G_i}, Gamma_j = e^{G_last - G_j}
+//   flags  [items]               int32  0, then 1 once the item's outputs are written
+//                                       (zeroed by launch_prefill_qk; read when both
+//                                       parts run in one launch)
 // The staged q^ / k^ (qk_ws, from launch_prefill_qk) must be in place first.
 struct SplitArgs {
   int B, T;        // sequences; tokens per sequence (fixed length) or in total (packed)
@@ -100,8 +104,9 @@ struct SplitArgs {
   float *ws_u;
   void *ws_nw, *ws_m;
   float *ws_vec;
+  int *flags;
 };
-constexpr size_t kSplitItemBytes = 32768 + 16384 + 8192 + 512;
+constexpr size_t kSplitItemBytes = 32768 + 16384 + 8192 + 512 + 4;
 // Work items of a call (tokens: B*T fixed length, T packed); sets nslots, nch.
 long long split_items(const Dims &d, long long tokens, bool packed, int *nslots, int *nch);
 cudaError_t launch_prefill_split(const PrefillArgs &a, const SplitArgs &s, cudaStream_t st);

@@ -1321,7 +1321,7 @@ constexpr uint32_t kQkSmem = kQkStages * kQkStage + 64 + 128;  // stages, mbarri
 static_assert(kQkStage % 128 == 0, "TMA stage alignment");
 
 __global__ void __launch_bounds__(kQkThreads, 2)
-    prefill_qk_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tm_qkv) {
+    prefill_qk_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tm_qkv, int *zero, long long nzero) {
   extern __shared__ uint8_t qk_smem_raw[];
   uint8_t *sm = qk_smem_raw + ((128 - (smem_u32(qk_smem_raw) & 127)) & 127);
   const uint32_t sbase = smem_u32(sm);
@@ -1339,6 +1339,8 @@ __global__ void __launch_bounds__(kQkThreads, 2)
   const float scale = blk == 0 ? d.q_scale : 1.0f;
   const bf16 *conv_w = static_cast<const bf16 *>(a.conv_w);
   const bf16 *conv0 = static_cast<const bf16 *>(a.conv0);
+  for (long long i = (long long)blockIdx.x * kQkThreads + tid; i < nzero; i += (long long)gridDim.x * kQkThreads)
+    zero[i] = 0;  // the chunk-parallel prefill's item flags
   if (tid == 0)
     for (int st = 0; st < kQkStages; ++st) bar_init(&full[st], 1);
   __syncthreads();
@@ -1520,7 +1522,7 @@ cudaError_t launch_prefill_chunked(const PrefillArgs &a, bool bf16_io, cudaStrea
   return cudaGetLastError();
 }
 
-cudaError_t launch_prefill_qk(const PrefillArgs &a, cudaStream_t s) {
+cudaError_t launch_prefill_qk(const PrefillArgs &a, cudaStream_t s, int *zero, long long nzero) {
   if (!a.qk_ws) return cudaErrorInvalidValue;
   const long long rows = a.cu_seqlens ? (long long)a.d.T : (long long)a.d.B * a.d.T;
   if (rows <= 0) return cudaSuccess;
@@ -1538,7 +1540,7 @@ cudaError_t launch_prefill_qk(const PrefillArgs &a, cudaStream_t s) {
   if (nslots < 1) nslots = 1;
   e = cudaFuncSetAttribute(prefill_qk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kQkSmem);
   if (e != cudaSuccess) return e;
-  prefill_qk_kernel<<<(unsigned)(nslots * a.d.Hk), kQkThreads, kQkSmem, s>>>(a, tm_qkv);
+  prefill_qk_kernel<<<(unsigned)(nslots * a.d.Hk), kQkThreads, kQkSmem, s>>>(a, tm_qkv, zero, nzero);
   return cudaGetLastError();
 }
 

@@ -91,6 +91,7 @@ __device__ __forceinline__ int slot_of(const SplitArgs &s, int b, int bos, int n
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
+
 // A plain bulk copy global -> shared completing on `bar` (16-byte aligned, size a multiple of 16).
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint64_t *bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
@@ -131,21 +132,47 @@ constexpr uint32_t TP_V = 64;    // V^T fp16 pairs: hi 64..95, lo 96..127
 constexpr uint32_t TP_U = 128;   // U^T [v][i]                        64
 constexpr uint32_t TP_W = 192;   // -W^T [k][i]                       64
 constexpr uint32_t kPrepTmem = 256;
-constexpr int kBarSolve = 1;
+constexpr int kBarSolve = 1;  // a prep group's solve barrier (the second group: 3)
+constexpr int kBarPrep = 2;   // a prep group's own barrier (the second group: 4)
 
-// Work items are taken in steps of the grid; the next one's tiles and gates
-// are requested while the current one is computed: its raw v rows once the
-// solve is done with L (their space), its [K;Q] once MMA W is done.
+// A prep group: 256 threads (8 warps) with their own kPrepSmem of shared
+// memory, 256 TMEM columns and named barriers, taking work items first,
+// first + step, ...  Without flags (prefill_prep_kernel) the items are the
+// workspace's own order (slot * Hv + h, packed slots skipped where no chunk
+// lies); with flags (prefill_overlap_kernel, fixed length only) they are
+// walked chunk by chunk, (n, b, h), so that the sequential CTAs of the same
+// launch find their next chunk early, and each item's flag is set once its
+// outputs have landed in the workspace.
+struct PrepGroup {
+  uint8_t *sm;       // 1024-aligned
+  uint32_t tmem;     // first of the group's 256 columns
+  int tid;           // 0..255
+  int bar, bar_solve;
+  long long first, step;
+  int *flags;
+};
+__device__ __forceinline__ void group_sync(const PrepGroup &G) { named_sync(G.bar, kPrepThreads); }
+__device__ __forceinline__ bool group_sync_or(const PrepGroup &G, bool p) {
+  return named_sync_or(G.bar, kPrepThreads, p);
+}
+// Release of an item's flag: its stores (TMA and plain) are complete and
+// visible at GPU scope before the flag is.
+__device__ __forceinline__ void st_release_gpu(int *p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_all() { asm volatile("fence.proxy.async;" ::: "memory"); }
+
+// The next item's tiles and gates are requested while the current one is
+// computed: its raw v rows once the solve is done with L (their space), its
+// [K;Q] once MMA W is done.
 template <bool kRawGates>
-__global__ void __launch_bounds__(kPrepThreads, 2)
-    prefill_prep_kernel(const PrefillArgs a, const SplitArgs s, const __grid_constant__ CUtensorMap tm_qkv,
-                        const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ CUtensorMap tm_u,
-                        const __grid_constant__ CUtensorMap tm_nw, const __grid_constant__ CUtensorMap tm_m) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+__device__ __forceinline__ void prep_role(const PrefillArgs &a, const SplitArgs &s, const CUtensorMap *tm_qkv,
+                                          const CUtensorMap *tm_qk, const CUtensorMap *tm_u, const CUtensorMap *tm_nw,
+                                          const CUtensorMap *tm_m, const PrepGroup &G) {
+  uint8_t *sm = G.sm;
   PrepShared &V = *reinterpret_cast<PrepShared *>(sm + P_VEC);
   const Dims d = a.d;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = G.tid, lane = threadIdx.x & 31, warp = tid >> 5;
   const int quad = warp & 3, half = warp >> 2;
   const int lrow = 32 * quad + lane;  // TMEM lane of this thread
   const uint32_t sbase = smem_u32(sm);
@@ -165,24 +192,44 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     bar_init(&V.bar_uw, 1);
     V.abort = 0;
   }
-  if (warp == 0) tmem_alloc(&V.tmem, kPrepTmem);
   zero_T_upper(ss, tid, kPrepThreads, 0, 3 * 192);
   fence_before();
-  __syncthreads();
+  group_sync(G);
   fence_after();
-  const uint32_t tmem = V.tmem;
+  const uint32_t tmem = G.tmem;
   const uint32_t tl = tmem + ((uint32_t)(32 * quad) << 16);
   const uint32_t id_kk = idesc(128, 64, 0, 0), id_mk = idesc(128, 64, 1, 0);
   uint32_t ph_kq = 0, ph_raw = 0, ph_qk = 0, ph_uw = 0;
   bool kq_pending = false, raw_pending = false, stores = false;  // thread 0's bookkeeping
+  long long pub = -1;  // thread 0: the item whose outputs are in flight, flagged once they land
 
-  // The next valid item at or after `it` (every thread computes the same).
-  auto next_valid = [&](long long it, ChunkLoc &c) -> long long {
-    for (; it < nitems; it += gridDim.x) {
+  // Step `it` of the walk: its workspace item and chunk.
+  auto resolve = [&](long long it, ChunkLoc &c) -> long long {
+    if (!G.flags) {
       c = locate(s, (int)(it / d.Hv));
+      return it;
+    }
+    const long long bh = (long long)s.B * d.Hv;
+    const int n = (int)(it / bh), b = (int)((it % bh) / d.Hv), h = (int)(it % d.Hv);
+    c = ChunkLoc{b, n, b * s.T, s.T, true};
+    return ((long long)b * s.nch + n) * d.Hv + h;
+  };
+  // The next step at or after `it` with a valid chunk (every thread computes the same).
+  auto next_valid = [&](long long it, ChunkLoc &c, long long &itm) -> long long {
+    for (; it < nitems; it += G.step) {
+      itm = resolve(it, c);
       if (c.ok) return it;
     }
     return nitems;
+  };
+  auto publish = [&]() {
+    if (pub >= 0) {
+      bulk_wait_all();
+      fence_proxy_async_all();
+      __threadfence();
+      st_release_gpu(G.flags + pub, 1);
+      pub = -1;
+    }
   };
   // Thread 0: an item's [K;Q] (q^ rows 64-127, k^ hi rows 0-63) and raw v rows.
   auto request_kq = [&](long long it, const ChunkLoc &c) {
@@ -190,14 +237,14 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     bar_expect_tx(&V.bar_kq, 2 * kC * kD * 2);
 #pragma unroll
     for (int at = 0; at < 2; ++at) {
-      tma_load_3d(sbase + P_KQ + at * 16384 + 64 * 128, &tm_qk, kh * kD + 64 * at, c.bos + kC * c.n, 0, &V.bar_kq);
-      tma_load_3d(sbase + P_KQ + at * 16384, &tm_qk, kh * kD + 64 * at, c.bos + kC * c.n, 1, &V.bar_kq);
+      tma_load_3d(sbase + P_KQ + at * 16384 + 64 * 128, tm_qk, kh * kD + 64 * at, c.bos + kC * c.n, 0, &V.bar_kq);
+      tma_load_3d(sbase + P_KQ + at * 16384, tm_qk, kh * kD + 64 * at, c.bos + kC * c.n, 1, &V.bar_kq);
     }
     kq_pending = true;
   };
   auto request_raw = [&](long long it, const ChunkLoc &c) {
     bar_expect_tx(&V.bar_raw, kRawBlock);
-    tma_load_3d(sbase + P_RAW, &tm_qkv, (int)(cv0 + (it % d.Hv) * kD), c.bos + kC * c.n - 3, 0, &V.bar_raw);
+    tma_load_3d(sbase + P_RAW, tm_qkv, (int)(cv0 + (it % d.Hv) * kD), c.bos + kC * c.n - 3, 0, &V.bar_raw);
     raw_pending = true;
   };
   // Warp 7: an item's gates (raw bf16 bits for raw projections), a chunk ahead.
@@ -212,30 +259,33 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   };
 
   ChunkLoc c{};
-  long long item = next_valid(blockIdx.x, c);
-  if (item < nitems) {
+  long long item = 0;
+  long long it = next_valid(G.first, c, item);
+  if (it < nitems) {
     if (tid == 0) {
       request_kq(item, c);
       request_raw(item, c);
     }
     if (warp == 7) load_gates(item, c);
   }
-  while (item < nitems) {
+  while (it < nitems) {
     const int h = (int)(item % d.Hv);
     const int t0 = kC * c.n, T = c.len;
     const long long cv = cv0 + (long long)h * kD;
     ChunkLoc cn{};
-    const long long next = next_valid(item + gridDim.x, cn);
+    long long next = 0;
+    const long long it_next = next_valid(it + G.step, cn, next);
+    const bool more = it_next < nitems;
     if (warp == 7) {  // this item's chunk vectors, then the next item's gates requested
       finish_gb<kRawGates>(kRawGates ? -expf(nea) : 0.f, dtb, t0, T, lane, gv, bv);
       chunk_vectors(V.cv, gv, bv, lane);
-      if (next < nitems) load_gates(next, cn);
+      if (more) load_gates(next, cn);
     }
     __syncwarp();
     bool ok = bar_wait(&V.bar_kq, ph_kq) && bar_wait(&V.bar_raw, ph_raw);
     ph_kq ^= 1u;
     ph_raw ^= 1u;
-    if (__syncthreads_or(!ok)) {
+    if (group_sync_or(G, !ok)) {
       if (tid == 0) {
         atomicOr(a.err, kErrTimeout);
         V.abort = 1;
@@ -250,7 +300,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
             conv0 ? *reinterpret_cast<const uint4 *>(conv0 + ((long long)c.b * 3 + rw) * C + cv + 8 * g8)
                   : make_uint4(0u, 0u, 0u, 0u);
       }
-      __syncthreads();
+      group_sync(G);
     }
     // MMA1 (warp 0): [K;Q] K^T -> K K^T (lanes 0-63), Q K^T (lanes 64-127)
     const uint32_t kq = sbase + P_KQ;
@@ -296,14 +346,18 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
       tmem_wait_st();
     }
     // The previous item's stores must have read their sources (M, the T tiles
-    // and the T scratch are written next).
-    if (tid == 0 && stores) bulk_wait_read();
+    // and the T scratch are written next); with flags they must have landed,
+    // and the item's flag is set.
+    if (tid == 0 && stores) {
+      if (G.flags) publish();
+      else bulk_wait_read();
+    }
     fence_before();
-    __syncthreads();  // the v rows are read: L may take their space
+    group_sync(G);  // the v rows are read: L may take their space
     ok = bar_wait(&V.bar_qk, ph_qk);
     ph_qk ^= 1u;
     fence_after();
-    if (__syncthreads_or(!ok)) {
+    if (group_sync_or(G, !ok)) {
       if (tid == 0) {
         atomicOr(a.err, kErrTimeout);
         V.abort = 1;
@@ -362,21 +416,21 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
       }
     }
     fence_smem_to_async();
-    __syncthreads();  // L and M written
+    group_sync(G);  // L and M written
     if (tid == 0) {
-      tma_store_2d(&tm_m, sbase + P_M, 0, (int)(item * kC));
+      tma_store_2d(tm_m, sbase + P_M, 0, (int)(item * kC));
       bulk_commit();
       stores = true;
     }
     // T = (I + L)^{-1} and the fp16 tiles (their upper blocks are zeroed
     // again: the previous item's -W^T and U^T staging used their space)
-    solve_T(ss, V.cv, tid, kBarSolve, true);
+    solve_T(ss, V.cv, tid, G.bar_solve, true);
     fence_smem_to_async();
     fence_before();
-    __syncthreads();
+    group_sync(G);
     // L is done with: the next item's raw v rows may land.  MMA U (hi*hi +
     // lo*hi + hi*lo, A = V^T from TMEM) and MMA W (warp 0).
-    if (tid == 0 && next < nitems) request_raw(next, cn);
+    if (tid == 0 && more) request_raw(next, cn);
     if (warp == 0) {
       fence_after();
       auto b_tu = [&](int ks) { return desc_k(sbase + P_TU, ks, kC); };
@@ -390,12 +444,13 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     if (tid < 2 * kC) {  // the chunk vectors d and Gamma, fp32 [2][64]
       float *vec = s.ws_vec + item * (2 * kC);
       if (in_bounds(item * (2 * kC) + tid + 1, nitems * (2 * kC), a.err)) vec[tid] = tid < kC ? V.cv.d[tid] : V.cv.gam[tid - kC];
+      if (G.flags) __threadfence();  // ordered before the item's flag
     }
     __syncwarp();
     ok = bar_wait(&V.bar_uw, ph_uw);
     ph_uw ^= 1u;
     fence_after();
-    if (__syncthreads_or(!ok)) {
+    if (group_sync_or(G, !ok)) {
       if (tid == 0) {
         atomicOr(a.err, kErrTimeout);
         V.abort = 1;
@@ -405,10 +460,10 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     // MMA W is done with [K;Q]: the next item's may land.  The M store is
     // long complete (its space takes U^T box 0).
     if (tid == 0) {
-      if (next < nitems) request_kq(next, cn);
+      if (more) request_kq(next, cn);
       bulk_wait_read();
     }
-    __syncthreads();
+    group_sync(G);
     {
       // U^T [v][i] fp32 -> staging box `half` (rows v, 32 values of 4 bytes, 128-byte swizzle)
       float v[32];
@@ -425,26 +480,49 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     }
     fence_smem_to_async();
     fence_before();
-    __syncthreads();
+    group_sync(G);
     if (tid == 0) {
-      tma_store_2d(&tm_u, sbase + P_UB0, 0, (int)(item * kD));
-      tma_store_2d(&tm_u, sbase + P_TF, 32, (int)(item * kD));
-      tma_store_2d(&tm_nw, sbase + P_NW, 0, (int)(item * kD));
+      tma_store_2d(tm_u, sbase + P_UB0, 0, (int)(item * kD));
+      tma_store_2d(tm_u, sbase + P_TF, 32, (int)(item * kD));
+      tma_store_2d(tm_nw, sbase + P_NW, 0, (int)(item * kD));
       bulk_commit();
+      if (G.flags) pub = item;
     }
+    it = it_next;
     item = next;
     c = cn;
   }
-  // Before the CTA ends: the stores complete, no load still lands, and no MMA
-  // still writes TMEM (after an early exit).
+  // Before the group ends: the stores complete (the last item flagged), no
+  // load still lands, and no MMA still writes TMEM (after an early exit).
   if (tid == 0) {
     bulk_wait_all();
+    if (G.flags) publish();
     if (kq_pending) bar_wait(&V.bar_kq, ph_kq);
     if (raw_pending) bar_wait(&V.bar_raw, ph_raw);
   }
   fence_before();
+  group_sync(G);
+}
+
+template <bool kRawGates>
+__global__ void __launch_bounds__(kPrepThreads, 2)
+    prefill_prep_kernel(const PrefillArgs a, const SplitArgs s, const __grid_constant__ CUtensorMap tm_qkv,
+                        const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ CUtensorMap tm_u,
+                        const __grid_constant__ CUtensorMap tm_nw, const __grid_constant__ CUtensorMap tm_m) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  PrepShared &V = *reinterpret_cast<PrepShared *>(sm + P_VEC);
+  if (threadIdx.x < 32) tmem_alloc(&V.tmem, kPrepTmem);
+  fence_before();
   __syncthreads();
-  if (warp == 0) {
+  fence_after();
+  const uint32_t tmem = V.tmem;
+  const PrepGroup G{sm, tmem, (int)threadIdx.x, kBarPrep, kBarSolve, (long long)blockIdx.x, (long long)gridDim.x,
+                    nullptr};
+  prep_role<kRawGates>(a, s, &tm_qkv, &tm_qk, &tm_u, &tm_nw, &tm_m, G);
+  fence_before();
+  __syncthreads();
+  if (threadIdx.x < 32) {
     fence_after();
     tmem_dealloc(tmem, kPrepTmem);
   }
@@ -453,13 +531,14 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
 // =============================================================================
 // prefill_seq_kernel
 // =============================================================================
-// Warps 0-7: the epilogue (O staging, gated norm); warps 8-15: the chain (the
+// Warps 0-6: the epilogue (O staging, gated norm); warp 7: the TMA producer
+// (lane 0 the U^T tiles, lane 1 the chunk stages, lane 2 the z rows), each lane
+// waiting for its buffer to be released; warps 8-15: the chain (the
 // state-dependent MMAs, issued by warp 8, and the Delta and state passes, two
-// warps per TMEM lane quadrant, each on half of the columns); warp 16: the TMA
-// producer (lane 0 the U^T tiles, lane 1 the chunk stages, lane 2 the z rows),
-// each lane waiting for its buffer to be released.
-constexpr int kSeqThreads = 544;
-constexpr int kProducerWarp = 16;
+// warps per TMEM lane quadrant, each on half of the columns).
+constexpr int kSeqThreads = 512;
+constexpr int kProducerWarp = 7;
+constexpr int kEpiThreads = 224;
 constexpr int kChainThreads = 256;
 constexpr int kIssuerTid = 256;  // warp 8, lane 0
 // One stage (a chunk's tiles), offsets within the stage; fp16, 128-byte swizzle.
@@ -483,12 +562,12 @@ struct SeqShared {
   uint64_t bar_o;      // MMA5 and MMA6 done
   uint64_t bar_s;      // MMA7 done
   uint64_t bar_ofree;  // the epilogue has read O1, O2 and the stage's vectors (one arrival per chunk)
-  uint64_t bar_ufree;  // the chain has read U^T (one arrival per chunk)
-  uint64_t bar_zfree;  // the epilogue has read the z rows (one arrival per chunk)
   uint64_t bar_end;
   uint32_t tmem;
   int abort;
   int req_full[2], req_u, req_z;  // requests issued (each completes one phase)
+  int ahead;                      // chunks 0 .. ahead-1: flags seen (when given) and decays in dcr
+  float dcr[4];                   // e^{G_last} of chunk m at m % 4
 };
 constexpr uint32_t kSeqSmem = S_BAR + ((sizeof(SeqShared) + 127) / 128) * 128 + 1024;
 static_assert(kSeqSmem <= 232448, "shared memory per CTA");
@@ -503,9 +582,40 @@ constexpr uint32_t TS_DH = 384;   // Delta^T fp16 hi                     32
 constexpr uint32_t TS_S16 = 448;  // state fp16 pairs [v][k/2]           64
 constexpr uint32_t kSeqTmem = 512;
 constexpr int kBarChain = 2;  // warps 8-15
-constexpr int kBarEpi = 3;    // warps 0-7
+constexpr int kBarEpi = 3;    // warps 0-6
 
 __device__ __forceinline__ bool seq_aborted(const SeqShared &V) { return *reinterpret_cast<const volatile int *>(&V.abort) != 0; }
+// Bounded wait (about one second) for the stage producer to have covered
+// `m` chunks (V.ahead >= m), then ordered before what follows.
+__device__ __forceinline__ bool ahead_wait(SeqShared &V, int m) {
+  const volatile int *v = &V.ahead;
+  if (*v < m) {
+    const uint64_t t0 = global_ns();
+    while (*v < m) {
+      if (global_ns() - t0 > 1000000000ull) return false;
+      __nanosleep(32);
+    }
+  }
+  __threadfence_block();
+  return true;
+}
+// Bounded wait (about one second) for a prep group of the same launch to set
+// an item's flag; the item's outputs may then be read, by TMA after a proxy
+// fence.
+__device__ __forceinline__ bool flag_wait(const int *f) {
+  auto get = [&]() {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    return v;
+  };
+  if (get() != 0) return true;
+  const uint64_t t0 = global_ns();
+  while (get() == 0) {
+    if (global_ns() - t0 > 1000000000ull) return false;
+    __nanosleep(256);
+  }
+  return true;
+}
 __device__ __forceinline__ void seq_fail(SeqShared &V, unsigned int *err) {
   atomicOr(err, kErrTimeout);
   *reinterpret_cast<volatile int *>(&V.abort) = 1;
@@ -569,12 +679,12 @@ __device__ __forceinline__ void norm_store(const NormRegs<NR> &R, const bf16 *no
   }
 }
 
-__global__ void __launch_bounds__(kSeqThreads, 1)
-    prefill_seq_kernel(const PrefillArgs a, const SplitArgs s, const __grid_constant__ CUtensorMap tm_qk,
-                       const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_u,
-                       const __grid_constant__ CUtensorMap tm_nw, const __grid_constant__ CUtensorMap tm_m) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+// The sequential part for the CTA's (sequence, value head), run by the whole
+// CTA (kSeqThreads threads).  With flags (prefill_overlap_kernel) a chunk's
+// workspace outputs are used only once its flag is set.
+__device__ __forceinline__ void seq_role(const PrefillArgs &a, const SplitArgs &s, const CUtensorMap *tm_qk,
+                                         const CUtensorMap *tm_z, const CUtensorMap *tm_u, const CUtensorMap *tm_nw,
+                                         const CUtensorMap *tm_m, uint8_t *sm, const int *flags) {
   SeqShared &V = *reinterpret_cast<SeqShared *>(sm + S_BAR);
   const Dims d = a.d;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -643,11 +753,10 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
     bar_init(&V.bar_o, 1);
     bar_init(&V.bar_s, 1);
     bar_init(&V.bar_ofree, 1);
-    bar_init(&V.bar_ufree, 1);
-    bar_init(&V.bar_zfree, 1);
     bar_init(&V.bar_end, 1);
     V.abort = 0;
     V.req_full[0] = V.req_full[1] = V.req_u = V.req_z = 0;
+    V.ahead = 0;
   }
   if (warp == 0) tmem_alloc(&V.tmem, kSeqTmem);
   fence_before();
@@ -656,55 +765,81 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
   const uint32_t tmem = V.tmem;
   auto vec_d = [&](int st) { return reinterpret_cast<const float *>(sm + S_VEC + 512 * st); };  // d [64], Gamma [64]
 
-  if (warp == kProducerWarp) {
-    // ------------------------------------------------ the producer (warp 12)
-    // Lane 0: U^T of chunk n+1 once the chain has read chunk n's.  Lane 1: the
-    // stage of chunk n+2 into chunk n's buffer once MMA7(n) is done and the
-    // epilogue has read chunk n's vectors.  Lane 2: z of chunk n+1 once the
-    // epilogue has read chunk n's.  Every wait is bounded.
+  // The U^T tile and the z rows are reloaded by the warps that free them (the
+  // chain's issuer after the Delta pass, the epilogue after it takes z into
+  // registers); the stages, the flags and the decays by the producer warp.
+  // No warp runs diverged waits.
+  auto load_u = [&](int n) {  // whole warp 8; chunk n's flag seen (V.ahead > n)
+    const long long it = item_of(n);
+    if (flags) fence_proxy_async_all();  // the outputs, released by a prep group, read by TMA
     if (lane == 0) {
       bar_expect_tx(&V.bar_u, 32768);
-      tma_load_2d(sbase + S_U, &tm_u, 0, (int)(item_of(0) * kD), &V.bar_u);
-      tma_load_2d(sbase + S_U + 16384, &tm_u, 32, (int)(item_of(0) * kD), &V.bar_u);
-      V.req_u = 1;
-      for (int n = 0; n + 1 < nch; ++n) {
-        if (!bar_wait(&V.bar_ufree, (uint32_t)n & 1u) || seq_aborted(V)) break;
-        const long long it = item_of(n + 1);
-        bar_expect_tx(&V.bar_u, 32768);
-        tma_load_2d(sbase + S_U, &tm_u, 0, (int)(it * kD), &V.bar_u);
-        tma_load_2d(sbase + S_U + 16384, &tm_u, 32, (int)(it * kD), &V.bar_u);
-        V.req_u = n + 2;
+      tma_load_2d(sbase + S_U, tm_u, 0, (int)(it * kD), &V.bar_u);
+      tma_load_2d(sbase + S_U + 16384, tm_u, 32, (int)(it * kD), &V.bar_u);
+      V.req_u = n + 1;
+    }
+    __syncwarp();
+  };
+  auto load_z = [&](int n) {  // one thread
+    bar_expect_tx(&V.bar_z, kC * kD * 2);
+    tma_load_3d(sbase + S_Z, tm_z, h * kD, (int)(bos + kC * n), 0, &V.bar_z);
+    V.req_z = n + 1;
+  };
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------ the producer (warp 7)
+    // The stage of chunk n+2 into chunk n's buffer once MMA7(n) is done and
+    // the epilogue has read chunk n's vectors (with flags, once chunk n+2's
+    // flag is set); then chunk n+3's flag and the decay of chunk n+3 into
+    // the ring, announced by V.ahead.  Lane 0 issues; every wait is bounded.
+    for (int n = 0; n < nch; ++n) {
+      if (n >= 2) {  // chunk n goes where chunk n-2 was
+        const bool w = bar_wait(&V.bar_s, (uint32_t)(n - 2) & 1u) && bar_wait(&V.bar_ofree, (uint32_t)(n - 2) & 1u);
+        if (!__all_sync(0xffffffffu, w) || seq_aborted(V)) break;
       }
-    } else if (lane == 1) {
-      for (int n = 0; n < nch; ++n) {
-        if (n >= 2) {  // chunk n goes where chunk n-2 was
-          if (!bar_wait(&V.bar_s, (uint32_t)(n - 2) & 1u) || !bar_wait(&V.bar_ofree, (uint32_t)(n - 2) & 1u) ||
-              seq_aborted(V))
-            break;
+      const long long it = item_of(n);
+      if (flags) {  // chunk n's flag: seen here for chunk 0, below (a stage earlier) for the rest
+        if (n == 0 && !__all_sync(0xffffffffu, lane != 0 || flag_wait(flags + it))) {
+          if (lane == 0) seq_fail(V, a.err);
+          break;
         }
-        const int st = n & 1;
+        fence_proxy_async_all();
+      }
+      const int st = n & 1;
+      if (lane == 0) {
         const uint32_t sb = sbase + st * kStage;
-        const long long it = item_of(n);
         uint64_t *bar = &V.full[st];
         bar_expect_tx(bar, kStageTx);
 #pragma unroll
         for (int at = 0; at < 2; ++at) {
-          tma_load_3d(sb + Q_Q + at * 8192, &tm_qk, kh * kD + 64 * at, (int)(bos + kC * n), 0, bar);
-          tma_load_3d(sb + Q_KH + at * 8192, &tm_qk, kh * kD + 64 * at, (int)(bos + kC * n), 1, bar);
-          tma_load_3d(sb + Q_KL + at * 8192, &tm_qk, kh * kD + 64 * at, (int)(bos + kC * n), 2, bar);
+          tma_load_3d(sb + Q_Q + at * 8192, tm_qk, kh * kD + 64 * at, (int)(bos + kC * n), 0, bar);
+          tma_load_3d(sb + Q_KH + at * 8192, tm_qk, kh * kD + 64 * at, (int)(bos + kC * n), 1, bar);
+          tma_load_3d(sb + Q_KL + at * 8192, tm_qk, kh * kD + 64 * at, (int)(bos + kC * n), 2, bar);
         }
-        tma_load_2d(sb + Q_NW, &tm_nw, 0, (int)(it * kD), bar);
-        tma_load_2d(sb + Q_M, &tm_m, 0, (int)(it * kC), bar);
+        tma_load_2d(sb + Q_NW, tm_nw, 0, (int)(it * kD), bar);
+        tma_load_2d(sb + Q_M, tm_m, 0, (int)(it * kC), bar);
         bulk_load(sbase + S_VEC + st * 512, s.ws_vec + it * (2 * kC), 2 * kC * 4, bar);
         V.req_full[st] += 1;
       }
-    } else if (lane == 2) {
-      for (int n = 0; n < nch; ++n) {
-        if (n >= 1 && (!bar_wait(&V.bar_zfree, (uint32_t)(n - 1) & 1u) || seq_aborted(V))) break;
-        bar_expect_tx(&V.bar_z, kC * kD * 2);
-        tma_load_3d(sbase + S_Z, &tm_z, h * kD, (int)(bos + kC * n), 0, &V.bar_z);
-        V.req_z = n + 1;
+      // Then the decays the chain's state passes take (chunk n + 1's in
+      // chunk n's; chunk 0's before the first), chunk n + 1's flag seen
+      // first, and V.ahead covering both.
+      bool got = true;
+      if (lane == 0) {
+        if (n == 0) V.dcr[0] = s.ws_vec[it * (2 * kC) + kC - 1];
+        if (n + 1 < nch) {
+          const long long it1 = item_of(n + 1);
+          got = !flags || flag_wait(flags + it1);
+          if (got) V.dcr[(n + 1) & 3] = s.ws_vec[it1 * (2 * kC) + kC - 1];
+        }
+        if (got) {
+          __threadfence_block();
+          *reinterpret_cast<volatile int *>(&V.ahead) = min(n + 2, nch);
+        } else {
+          seq_fail(V, a.err);
+        }
       }
+      if (!__all_sync(0xffffffffu, got)) break;
     }
   } else if (warp >= 8) {
     // ------------------------------------------------ the chain (warps 8-15)
@@ -714,11 +849,14 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
     const bool issuer = warp == 8;
     const uint32_t id_kk = idesc(128, 64, 0, 0), id_km = idesc(128, 64, 0, 1), id_km128 = idesc(128, 128, 0, 1);
     bool ok = true;
-    // e^{G_last} of chunk n (the decay the state takes at chunk n's start),
-    // read from the workspace two chunks ahead of its use.
-    auto dc_of = [&](int n) -> float { return n < nch ? s.ws_vec[item_of(n) * (2 * kC) + kC - 1] : 1.f; };
+    // e^{G_last} of chunk m (the decay the state takes at its start): in the
+    // ring once V.ahead > m, in practice a chunk or more before it is needed.
+    auto dc_of = [&](int m) -> float {
+      if (!ahead_wait(V, m + 1)) ok = false;
+      return *reinterpret_cast<volatile const float *>(&V.dcr[m & 3]);
+    };
     const float dc0 = dc_of(0);
-    float dc_n1 = dc_of(1), dc_n2 = dc_of(2);
+    if (issuer) load_u(0);  // chunk 0's flag seen by now
     // Initial state: TMEM fp32 <- d_C(chunk 0) S0, fp16 copy <- S0 (this
     // thread: row lrow, columns 64 ch .. 64 ch + 63).
 #pragma unroll 1
@@ -753,24 +891,33 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
       const int st = n & 1;
       const uint32_t sb = sbase + st * kStage;
       if (seq_aborted(V)) break;
-      // MMA4 D = S (-W^T), MMA5 O1 = S Q^T (warp 8), once the chunk's tiles and
-      // U^T are in and the epilogue has read the previous chunk's O1, O2.  The
-      // other chain warps go on to wait for D.  A wait that times out is voted
-      // on once, at the chunk's closing barrier.
+      // MMA4 D = S (-W^T) (warp 8) once the chunk's tiles and U^T are in;
+      // MMA5 O1 = S Q^T right after it if the epilogue has read the previous
+      // chunk's O1, O2 by then, else after the Delta pass, before MMA7 (so
+      // that MMA7's barrier covers MMA5's reads of the fp16 state).  The other
+      // chain warps go on to wait for D.  A wait that times out is voted on
+      // once, at the chunk's closing barrier.
       __syncwarp();
       bool w = bar_wait(&V.full[st], (uint32_t)(n >> 1) & 1u);
       w = bar_wait(&V.bar_u, (uint32_t)n & 1u) && w;
-      if (issuer && n > 0) w = bar_wait(&V.bar_ofree, (uint32_t)(n - 1) & 1u) && w;
       ok = ok && w;
+      bool o1_done = false;
+      auto mma5 = [&]() {
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          mma_ta_w(tmem + TS_O1, tmem + TS_S16 + 8 * ks, desc_k(sb + Q_Q, ks, kC), id_kk, ks > 0);
+      };
       if (issuer && __all_sync(0xffffffffu, w)) {
         fence_after();
         const uint64_t dnw = desc_mn(sb + Q_NW, 0, kD);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) mma_ta_w(tmem + TS_D, tmem + TS_S16 + 8 * ks, dnw + (uint64_t)(ks * 128), id_km, ks > 0);
         commit_w(&V.bar_d);
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          mma_ta_w(tmem + TS_O1, tmem + TS_S16 + 8 * ks, desc_k(sb + Q_Q, ks, kC), id_kk, ks > 0);
+        o1_done = __all_sync(0xffffffffu, n == 0 || bar_try_wait(&V.bar_ofree, (uint32_t)(n - 1) & 1u));
+        if (o1_done) {
+          fence_after();
+          mma5();
+        }
       }
       // Delta^T = D + U^T -> fp16 hi (MMA6) and (Delta Gamma)^T hi / lo (MMA7)
       __syncwarp();
@@ -813,15 +960,16 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
       }
       fence_before();
       named_sync(kBarChain, kChainThreads);
-      // U^T is read (the producer may load the next); MMA6, MMA7 (issuer).
+      // The deferred MMA5, MMA7 (the state update, first: the chain waits for
+      // it), MMA6, then U^T of the next chunk into the buffer just read
+      // (issuer).
       if (issuer) {
-        if (lane == 0) mbar_arrive(&V.bar_ufree);
-        __syncwarp();
+        if (!o1_done) {
+          ok = bar_wait(&V.bar_ofree, (uint32_t)(n - 1) & 1u) && ok;
+          fence_after();
+          mma5();
+        }
         fence_after();
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          mma_ta_w(tmem + TS_O2, tmem + TS_DH + 8 * ks, desc_k(sb + Q_M, ks, kC), id_kk, ks > 0);
-        commit_w(&V.bar_o);
         const uint64_t dkh = desc(sb + Q_KH, 8192, 1024), dkl = desc(sb + Q_KL, 8192, 1024);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) mma_ta_w(tmem + TS_S, tmem + TS_DG + 8 * ks, dkh + (uint64_t)(ks * 128), id_km128, 1);
@@ -831,13 +979,19 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
         for (int ks = 0; ks < 4; ++ks)
           mma_ta_w(tmem + TS_S, tmem + TS_DG + 32 + 8 * ks, dkh + (uint64_t)(ks * 128), id_km128, 1);
         commit_w(&V.bar_s);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          mma_ta_w(tmem + TS_O2, tmem + TS_DH + 8 * ks, desc_k(sb + Q_M, ks, kC), id_kk, ks > 0);
+        commit_w(&V.bar_o);
+        if (n + 1 < nch) {
+          ok = ahead_wait(V, n + 2) && ok;  // chunk n + 1's flag seen
+          load_u(n + 1);
+        }
       }
       // The state pass: the fp16 copy and the rescale by the next chunk's
       // decay, or S_T after the last chunk.
       const bool last = n + 1 == nch;
-      const float dcn = dc_n1;
-      dc_n1 = dc_n2;
-      dc_n2 = dc_of(n + 3);
+      const float dcn = last ? 1.f : dc_of(n + 1);
       __syncwarp();
       ok = bar_wait(&V.bar_s, (uint32_t)n & 1u) && ok;
       fence_after();
@@ -880,11 +1034,15 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
     }
     if (!ok && tid == kIssuerTid) seq_fail(V, a.err);
   } else {
-    // ------------------------------------------- the epilogue (warps 0-7)
-    const int quad = warp & 3, half = warp >> 2;
+    // ------------------------------------------- the epilogue (warps 0-6)
+    // O staging: warp w takes lane quadrant w & 3, column half w >> 2; lane
+    // quadrant 3 has one epilogue warp (3), which takes both halves.
+    const int quad = warp & 3;
     const int lrow = 32 * quad + lane;
     const uint32_t tl = tmem + ((uint32_t)(32 * quad) << 16);
+    const int h_lo = warp < 4 ? 0 : 1, h_hi = warp < 3 ? 1 : 2;
     bool ok = true;
+    if (tid == 0) load_z(0);
     for (int n = 0; n < nch; ++n) {
       const int st = n & 1;
       if (seq_aborted(V)) break;
@@ -892,7 +1050,7 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
       ok = bar_wait(&V.bar_o, (uint32_t)n & 1u) && ok;
       ok = bar_wait(&V.full[st], (uint32_t)(n >> 1) & 1u) && ok;  // this stage's vectors (long landed)
       fence_after();
-      {  // O^T = d (S Q^T) + Delta^T M^T -> staging [i][v], 16 token columns at a time
+      for (int half = h_lo; half < h_hi; ++half) {  // O^T = d (S Q^T) + Delta^T M^T -> staging [i][v]
         float *ost = reinterpret_cast<float *>(sm + S_OST);
         const float *dq = vec_d(st) + 32 * half;
 #pragma unroll
@@ -917,20 +1075,20 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
         }
       }
       fence_before();
-      named_sync(kBarEpi, 256);
+      named_sync(kBarEpi, kEpiThreads);
       if (tid == 0) mbar_arrive(&V.bar_ofree);  // O1, O2 and this stage's vectors are read
-      // The gated norm of the chunk's 64 tokens (4 per half-warp): staged O and
+      // The gated norm of the chunk's 64 tokens over 14 half-warps: staged O and
       // z into registers, the z buffer released, then y formed and stored.
       __syncwarp();
       ok = bar_wait(&V.bar_z, (uint32_t)n & 1u) && ok;
       const int nv = min(kC, T - kC * n), i0 = 2 * warp + (lane >> 4);
-      NormRegs<4> R;
-      norm_load<4>(sm, R, nv, i0, 16, lane);
-      named_sync(kBarEpi, 256);
-      if (tid == 0) mbar_arrive(&V.bar_zfree);
-      if (ok) norm_store<4>(R, static_cast<const bf16 *>(a.norm_w), static_cast<bf16 *>(a.o), d, bos, h, kC * n, nv, i0,
-                            16, lane, o_size, a.err);
-      if (named_sync_or(kBarEpi, 256, !ok)) break;  // the staging is read; a timeout is voted on here
+      NormRegs<5> R;
+      norm_load<5>(sm, R, nv, i0, 14, lane);
+      named_sync(kBarEpi, kEpiThreads);
+      if (tid == 0 && n + 1 < nch) load_z(n + 1);  // the z rows are in registers: the next chunk's may land
+      if (ok) norm_store<5>(R, static_cast<const bf16 *>(a.norm_w), static_cast<bf16 *>(a.o), d, bos, h, kC * n, nv, i0,
+                            14, lane, o_size, a.err);
+      if (named_sync_or(kBarEpi, kEpiThreads, !ok)) break;  // the staging is read; a timeout is voted on here
     }
     if (!ok && tid == 0) seq_fail(V, a.err);
   }
@@ -954,6 +1112,67 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
   if (warp == 0) {
     fence_after();
     tmem_dealloc(tmem, kSeqTmem);
+  }
+}
+
+__global__ void __launch_bounds__(kSeqThreads, 1)
+    prefill_seq_kernel(const PrefillArgs a, const SplitArgs s, const __grid_constant__ CUtensorMap tm_qk,
+                       const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_u,
+                       const __grid_constant__ CUtensorMap tm_nw, const __grid_constant__ CUtensorMap tm_m) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  seq_role(a, s, &tm_qk, &tm_z, &tm_u, &tm_nw, &tm_m, sm, nullptr);
+}
+
+// =============================================================================
+// prefill_overlap_kernel
+// =============================================================================
+// Both parts in one cooperative launch, for a fixed-length batch with few
+// (sequence, value head) units: CTAs 0 .. B*Hv - 1 run the sequential part,
+// every other CTA runs two prep groups, which walk the items chunk by chunk
+// and flag each item once its outputs have landed; a sequential CTA reads a
+// chunk's outputs once its flag is set.  Every CTA is resident at once (the
+// launch is cooperative) and the prep groups wait on nothing the sequential
+// CTAs do, so each flag wait ends; a wait that runs past its bound reports
+// GDN_ERR_TIMEOUT instead.
+constexpr uint32_t kPrepGroupBytes = ((P_VEC + (uint32_t)sizeof(PrepShared) + 1023) / 1024) * 1024;
+constexpr uint32_t kOverlapSmem = kSeqSmem > 2 * kPrepGroupBytes + 1024 ? kSeqSmem : 2 * kPrepGroupBytes + 1024;
+static_assert(kSeqThreads == 2 * kPrepThreads && kOverlapSmem <= 232448, "two prep groups in a sequential CTA's place");
+
+template <bool kRawGates>
+__global__ void __launch_bounds__(kSeqThreads, 1)
+    prefill_overlap_kernel(const PrefillArgs a, const SplitArgs s, int *flags,
+                           const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_qk,
+                           const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_u,
+                           const __grid_constant__ CUtensorMap tm_nw, const __grid_constant__ CUtensorMap tm_m) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  const int nseq = a.d.B * a.d.Hv;
+  if ((int)blockIdx.x < nseq) {
+    seq_role(a, s, &tm_qk, &tm_z, &tm_u, &tm_nw, &tm_m, sm, flags);
+    return;
+  }
+  PrepShared &V0 = *reinterpret_cast<PrepShared *>(sm + P_VEC);
+  if (threadIdx.x < 32) tmem_alloc(&V0.tmem, 2 * kPrepTmem);
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = V0.tmem;
+  const int g = (int)threadIdx.x / kPrepThreads;
+  const PrepGroup G{sm + g * kPrepGroupBytes,
+                    tmem + (uint32_t)(g * kPrepTmem),
+                    (int)threadIdx.x % kPrepThreads,
+                    kBarPrep + 2 * g,
+                    kBarSolve + 2 * g,
+                    2LL * ((int)blockIdx.x - nseq) + g,
+                    2LL * ((int)gridDim.x - nseq),
+                    flags};
+  prep_role<kRawGates>(a, s, &tm_qkv, &tm_qk, &tm_u, &tm_nw, &tm_m, G);
+  fence_before();
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    fence_after();
+    tmem_dealloc(tmem, 2 * kPrepTmem);
   }
 }
 
@@ -1029,11 +1248,36 @@ cudaError_t launch_prefill_split(const PrefillArgs &a, const SplitArgs &s, cudaS
       !encode_rows(&tm_z, a.z, (long long)a.d.Hv * kD, rows, kC) || !encode_qk(&tm_qk, a.qk_ws, a.d.Hk, rows) ||
       !encode_split(&mp, s, nitems))
     return cudaErrorInvalidValue;
-  int dev = 0, sms = 0;
+  int dev = 0, sms = 0, coop = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
   if (e != cudaSuccess) return e;
   const bool raw = a.gate.g == nullptr;
+  // Few units of a fixed-length batch: both parts in one launch, the prep
+  // groups on the SMs the sequential CTAs leave (at least half of them).
+  const long long nseq = (long long)a.d.B * a.d.Hv;
+  if (!s.cu && s.flags && coop && 2 * nseq <= sms) {
+    auto ov = raw ? prefill_overlap_kernel<true> : prefill_overlap_kernel<false>;
+    e = cudaFuncSetAttribute(ov, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kOverlapSmem);
+    int per_sm = 0;
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ov, kSeqThreads, kOverlapSmem);
+    if (e != cudaSuccess) return e;
+    if (per_sm >= 1) {
+      cudaLaunchConfig_t cfg{};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeCooperative;
+      attr[0].val.cooperative = 1;
+      cfg.gridDim = dim3((unsigned)sms);
+      cfg.blockDim = dim3(kSeqThreads);
+      cfg.dynamicSmemBytes = kOverlapSmem;
+      cfg.stream = st;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      return cudaLaunchKernelEx(&cfg, ov, a, s, s.flags, tm_qkv, tm_qk, tm_z, mp.u, mp.nw, mp.m);
+    }
+  }
   auto prep = raw ? prefill_prep_kernel<true> : prefill_prep_kernel<false>;
   e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem);
   if (e != cudaSuccess) return e;

@@ -221,8 +221,9 @@ typedef struct {
 /* Bytes of workspace of the chunk-parallel prefill for this shape (packed:
  * the call passes cu_seqlens, so the token rows are shape->T, else B*T):
  * the staged q^ and k^ (gdn_prefill_staged_bytes, rounded up to 256) plus
- * 57,856 bytes per (chunk slot, value head) -- U^T fp32 and -W^T fp16
- * [128][64], M fp16 [64][64], and two fp32 vectors of 64 -- where the chunk
+ * 57,860 bytes per (chunk slot, value head) -- U^T fp32 and -W^T fp16
+ * [128][64], M fp16 [64][64], two fp32 vectors of 64 and a ready flag (the
+ * two parts may run in one launch) -- where the chunk
  * slots are B * ceil(T/64) for fixed-length sequences and T/64 + B + 2 for
  * packed ones.  Where the work items would exceed 2^24 it returns the staged
  * size.  0 when the shape is invalid or the call would not run the chunked

@@ -123,7 +123,8 @@ def gpu_prefill(p, inputs=None, in_place=False, staged=False, split=False):
         gdn.gdn_prefill(x["qkv_pre"], x["z"], x["g"], x["beta"], x["conv_w"], x["norm_w"],
                         x["S0"], x["conv0"], o, S_T, conv_T, Hk=p.Hk, Hv=p.Hv)
     torch.cuda.synchronize()
-    assert gdn.gdn_device_status() == 0
+    st = gdn.gdn_device_status()
+    assert st == 0, "device status %s" % gdn.STATUS_NAMES.get(st, st)
     return o, S_T, conv_T
 
 

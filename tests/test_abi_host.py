@@ -168,7 +168,7 @@ def test_workspace_checked_on_host(L):
     staged = L.gdn_prefill_staged_bytes(ctypes.byref(sh), 0)
     assert staged == 3 * 2 * 8 * 2 * 128 * 2
     assert L.gdn_prefill_staged_bytes(ctypes.byref(sh), 1) == 3 * 8 * 2 * 128 * 2   # packed: T rows
-    item = 32768 + 16384 + 8192 + 512   # U^T, -W^T, M, vectors of one (chunk slot, value head)
+    item = 32768 + 16384 + 8192 + 512 + 4  # U^T, -W^T, M, vectors, flag of one (chunk slot, value head)
     need = L.gdn_prefill_workspace_bytes(ctypes.byref(sh), 0)
     assert need == staged + 2 * 1 * 4 * item                 # B * ceil(T/64) slots x Hv heads
     assert L.gdn_prefill_workspace_bytes(ctypes.byref(sh), 1) == 3 * 8 * 2 * 128 * 2 + (0 + 2 + 2) * 4 * item

@@ -1,7 +1,8 @@
 """GPU parity of the chunk-parallel form of gdn_prefill_ex (a workspace of
 gdn_prefill_workspace_bytes: q^ / k^ staged once per key head, every chunk's
 state-independent part -- T, U, W, the decayed Q K^T -- formed at once, then
-one sequential pass per (sequence, value head) with the state in TMEM)
+one sequential pass per (sequence, value head) with the state in TMEM; for
+few units of a fixed-length batch both parts share one cooperative launch)
 against the fp64 oracle: ragged lengths, head ratios 1 to 3, raw gates,
 packed sequences with empty and short ones, unusable offsets, in-place state,
 continuation, and the model-shaped workloads."""
@@ -34,6 +35,13 @@ def _lib():
     (1, 65, 1, 3, True), (2, 130, 2, 6, True), (3, 200, 1, 3, False), (1, 257, 4, 4, True), (2, 129, 4, 8, True)])
 def test_split_prefill(B, T, Hk, Hv, state):
     p = I.prefill_problem(B, T, Hk, Hv, io="bf16", case=600 + T, s0_std=0.02 if state else 0.0, conv0=state)
+    compare_prefill(p, gpu_prefill(p, split=True))
+
+
+def test_split_many_units_two_launches():
+    """More (sequence, value head) units than half the SMs: the two parts run
+    as separate launches (with fewer, both run in one cooperative launch)."""
+    p = I.prefill_problem(20, 130, 2, 4, io="bf16", case=629, s0_std=0.02, conv0=True)
     compare_prefill(p, gpu_prefill(p, split=True))
 
 
