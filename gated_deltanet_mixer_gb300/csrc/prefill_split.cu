@@ -88,6 +88,17 @@ __device__ __forceinline__ int slot_of(const SplitArgs &s, int b, int bos, int n
   return s.cu ? (bos >> 6) + b + n : b * s.nch + n;
 }
 
+// Non-blocking probe of an mbarrier phase.
+__device__ __forceinline__ bool bar_test_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
@@ -561,15 +572,20 @@ struct SeqShared {
   uint64_t bar_d;      // MMA4 done
   uint64_t bar_o;      // MMA5 and MMA6 done
   uint64_t bar_s;      // MMA7 done
+  uint64_t bar_ufree;  // the chain has read U^T (one arrival per chunk)
   uint64_t bar_ofree;  // the epilogue has read O1, O2 and the stage's vectors (one arrival per chunk)
   uint64_t bar_end;
   uint32_t tmem;
   int abort;
   int req_full[2], req_u, req_z;  // requests issued (each completes one phase)
   int ahead;                      // chunks 0 .. ahead-1: flags seen (when given) and decays in dcr
+  int s_seen;                     // chunks whose MMA7 (and the MMAs issued before it) are done
+  int epi_seen;                   // chunks whose MMA6 is done and whose vectors the epilogue has read
+  alignas(16) float de[2][64];    // the epilogue's copy of chunk n's d at n & 1 (read as float4)
   float dcr[4];                   // e^{G_last} of chunk m at m % 4
 };
 constexpr uint32_t kSeqSmem = S_BAR + ((sizeof(SeqShared) + 127) / 128) * 128 + 1024;
+static_assert(offsetof(SeqShared, de) % 16 == 0 && S_BAR % 16 == 0, "16-byte loads of the d copy");
 static_assert(kSeqSmem <= 232448, "shared memory per CTA");
 static_assert(S_U % 1024 == 0 && S_Z % 128 == 0 && kStage % 1024 == 0, "TMA destinations");
 // TMEM columns (512 allocated).
@@ -585,10 +601,10 @@ constexpr int kBarChain = 2;  // warps 8-15
 constexpr int kBarEpi = 3;    // warps 0-6
 
 __device__ __forceinline__ bool seq_aborted(const SeqShared &V) { return *reinterpret_cast<const volatile int *>(&V.abort) != 0; }
-// Bounded wait (about one second) for the stage producer to have covered
-// `m` chunks (V.ahead >= m), then ordered before what follows.
-__device__ __forceinline__ bool ahead_wait(SeqShared &V, int m) {
-  const volatile int *v = &V.ahead;
+// Bounded wait (about one second) for a shared counter to reach `m`, then
+// ordered before what follows.
+__device__ __forceinline__ bool count_wait(int *p, int m) {
+  const volatile int *v = p;
   if (*v < m) {
     const uint64_t t0 = global_ns();
     while (*v < m) {
@@ -599,6 +615,8 @@ __device__ __forceinline__ bool ahead_wait(SeqShared &V, int m) {
   __threadfence_block();
   return true;
 }
+// The stage producer has covered `m` chunks (V.ahead >= m).
+__device__ __forceinline__ bool ahead_wait(SeqShared &V, int m) { return count_wait(&V.ahead, m); }
 // Bounded wait (about one second) for a prep group of the same launch to set
 // an item's flag; the item's outputs may then be read, by TMA after a proxy
 // fence.
@@ -752,11 +770,12 @@ __device__ __forceinline__ void seq_role(const PrefillArgs &a, const SplitArgs &
     bar_init(&V.bar_d, 1);
     bar_init(&V.bar_o, 1);
     bar_init(&V.bar_s, 1);
+    bar_init(&V.bar_ufree, 1);
     bar_init(&V.bar_ofree, 1);
     bar_init(&V.bar_end, 1);
     V.abort = 0;
     V.req_full[0] = V.req_full[1] = V.req_u = V.req_z = 0;
-    V.ahead = 0;
+    V.ahead = V.s_seen = V.epi_seen = 0;
   }
   if (warp == 0) tmem_alloc(&V.tmem, kSeqTmem);
   fence_before();
@@ -765,21 +784,9 @@ __device__ __forceinline__ void seq_role(const PrefillArgs &a, const SplitArgs &
   const uint32_t tmem = V.tmem;
   auto vec_d = [&](int st) { return reinterpret_cast<const float *>(sm + S_VEC + 512 * st); };  // d [64], Gamma [64]
 
-  // The U^T tile and the z rows are reloaded by the warps that free them (the
-  // chain's issuer after the Delta pass, the epilogue after it takes z into
-  // registers); the stages, the flags and the decays by the producer warp.
-  // No warp runs diverged waits.
-  auto load_u = [&](int n) {  // whole warp 8; chunk n's flag seen (V.ahead > n)
-    const long long it = item_of(n);
-    if (flags) fence_proxy_async_all();  // the outputs, released by a prep group, read by TMA
-    if (lane == 0) {
-      bar_expect_tx(&V.bar_u, 32768);
-      tma_load_2d(sbase + S_U, tm_u, 0, (int)(it * kD), &V.bar_u);
-      tma_load_2d(sbase + S_U + 16384, tm_u, 32, (int)(it * kD), &V.bar_u);
-      V.req_u = n + 1;
-    }
-    __syncwarp();
-  };
+  // The z rows are reloaded by the epilogue once it has taken them into
+  // registers; the stages, the U^T tiles, the flags and the decays by the
+  // producer warp, in one ordered loop (no warp runs diverged waits).
   auto load_z = [&](int n) {  // one thread
     bar_expect_tx(&V.bar_z, kC * kD * 2);
     tma_load_3d(sbase + S_Z, tm_z, h * kD, (int)(bos + kC * n), 0, &V.bar_z);
@@ -788,59 +795,82 @@ __device__ __forceinline__ void seq_role(const PrefillArgs &a, const SplitArgs &
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------ the producer (warp 7)
-    // The stage of chunk n+2 into chunk n's buffer once MMA7(n) is done and
-    // the epilogue has read chunk n's vectors (with flags, once chunk n+2's
-    // flag is set); then chunk n+3's flag and the decay of chunk n+3 into
-    // the ring, announced by V.ahead.  Lane 0 issues; every wait is bounded.
-    for (int n = 0; n < nch; ++n) {
-      if (n >= 2) {  // chunk n goes where chunk n-2 was
-        const bool w = bar_wait(&V.bar_s, (uint32_t)(n - 2) & 1u) && bar_wait(&V.bar_ofree, (uint32_t)(n - 2) & 1u);
-        if (!__all_sync(0xffffffffu, w) || seq_aborted(V)) break;
-      }
-      const long long it = item_of(n);
-      if (flags) {  // chunk n's flag: seen here for chunk 0, below (a stage earlier) for the rest
-        if (n == 0 && !__all_sync(0xffffffffu, lane != 0 || flag_wait(flags + it))) {
-          if (lane == 0) seq_fail(V, a.err);
-          break;
-        }
-        fence_proxy_async_all();
-      }
-      const int st = n & 1;
+    // Step n: U^T of chunk n once the chain has read chunk n-1's; chunk
+    // n+2's flag (with flags) and decay, announced by V.ahead; the stage of
+    // chunk n+1 into chunk n-1's buffer once MMA7(n-1) and MMA6(n-1) are
+    // done and the epilogue has read chunk n-1's vectors.  Those two are
+    // counters, not barrier phases: while this warp waits for a flag the
+    // chain may finish another chunk, and a phase two ahead would read as
+    // not yet complete.  A chunk's workspace outputs
+    // are loaded only after its flag was seen.  Lane 0 issues; every wait is
+    // bounded.
+    auto see_flag = [&](int m) -> bool {  // chunk m's flag (lane 0 polls)
+      return !flags || __all_sync(0xffffffffu, lane != 0 || flag_wait(flags + item_of(m)));
+    };
+    auto announce = [&](int m) {  // chunk m's decay into the ring; chunks <= m covered
       if (lane == 0) {
+        V.dcr[m & 3] = s.ws_vec[item_of(m) * (2 * kC) + kC - 1];
+        __threadfence_block();
+        *reinterpret_cast<volatile int *>(&V.ahead) = m + 1;
+      }
+      __syncwarp();
+    };
+    auto load_stage = [&](int m) {
+      if (flags) fence_proxy_async_all();  // the outputs, released by a prep group, read by TMA
+      if (lane == 0) {
+        const int st = m & 1;
         const uint32_t sb = sbase + st * kStage;
+        const long long it = item_of(m);
         uint64_t *bar = &V.full[st];
         bar_expect_tx(bar, kStageTx);
 #pragma unroll
         for (int at = 0; at < 2; ++at) {
-          tma_load_3d(sb + Q_Q + at * 8192, tm_qk, kh * kD + 64 * at, (int)(bos + kC * n), 0, bar);
-          tma_load_3d(sb + Q_KH + at * 8192, tm_qk, kh * kD + 64 * at, (int)(bos + kC * n), 1, bar);
-          tma_load_3d(sb + Q_KL + at * 8192, tm_qk, kh * kD + 64 * at, (int)(bos + kC * n), 2, bar);
+          tma_load_3d(sb + Q_Q + at * 8192, tm_qk, kh * kD + 64 * at, (int)(bos + kC * m), 0, bar);
+          tma_load_3d(sb + Q_KH + at * 8192, tm_qk, kh * kD + 64 * at, (int)(bos + kC * m), 1, bar);
+          tma_load_3d(sb + Q_KL + at * 8192, tm_qk, kh * kD + 64 * at, (int)(bos + kC * m), 2, bar);
         }
         tma_load_2d(sb + Q_NW, tm_nw, 0, (int)(it * kD), bar);
         tma_load_2d(sb + Q_M, tm_m, 0, (int)(it * kC), bar);
         bulk_load(sbase + S_VEC + st * 512, s.ws_vec + it * (2 * kC), 2 * kC * 4, bar);
         V.req_full[st] += 1;
       }
-      // Then the decays the chain's state passes take (chunk n + 1's in
-      // chunk n's; chunk 0's before the first), chunk n + 1's flag seen
-      // first, and V.ahead covering both.
-      bool got = true;
+      __syncwarp();
+    };
+    auto load_u = [&](int m) {
+      if (flags) fence_proxy_async_all();
       if (lane == 0) {
-        if (n == 0) V.dcr[0] = s.ws_vec[it * (2 * kC) + kC - 1];
-        if (n + 1 < nch) {
-          const long long it1 = item_of(n + 1);
-          got = !flags || flag_wait(flags + it1);
-          if (got) V.dcr[(n + 1) & 3] = s.ws_vec[it1 * (2 * kC) + kC - 1];
-        }
-        if (got) {
-          __threadfence_block();
-          *reinterpret_cast<volatile int *>(&V.ahead) = min(n + 2, nch);
-        } else {
-          seq_fail(V, a.err);
-        }
+        const long long it = item_of(m);
+        bar_expect_tx(&V.bar_u, 32768);
+        tma_load_2d(sbase + S_U, tm_u, 0, (int)(it * kD), &V.bar_u);
+        tma_load_2d(sbase + S_U + 16384, tm_u, 32, (int)(it * kD), &V.bar_u);
+        V.req_u = m + 1;
       }
-      if (!__all_sync(0xffffffffu, got)) break;
+      __syncwarp();
+    };
+    bool good = see_flag(0);
+    if (good) {
+      load_stage(0);
+      announce(0);
+      if (nch > 1 && (good = see_flag(1))) announce(1);
     }
+    if (good) load_u(0);
+    if (good && nch > 1) {
+      load_stage(1);
+      if (nch > 2 && (good = see_flag(2))) announce(2);
+    }
+    for (int n = 1; good && n < nch; ++n) {
+      good = __all_sync(0xffffffffu, bar_wait(&V.bar_ufree, (uint32_t)(n - 1) & 1u));
+      if (!good || seq_aborted(V)) break;
+      load_u(n);
+      if (n + 2 < nch && !(good = see_flag(n + 2))) break;  // meanwhile MMA7(n-1) and the epilogue go on
+      if (n + 2 < nch) announce(n + 2);
+      if (n + 1 < nch) {  // chunk n+1 goes where chunk n-1 was, once that is done with
+        good = __all_sync(0xffffffffu, count_wait(&V.s_seen, n) && count_wait(&V.epi_seen, n));
+        if (!good || seq_aborted(V)) break;
+        load_stage(n + 1);
+      }
+    }
+    if (!good && lane == 0) seq_fail(V, a.err);
   } else if (warp >= 8) {
     // ------------------------------------------------ the chain (warps 8-15)
     const int quad = warp & 3, ch = (warp - 8) >> 2;  // lane quadrant; column half
@@ -856,7 +886,6 @@ __device__ __forceinline__ void seq_role(const PrefillArgs &a, const SplitArgs &
       return *reinterpret_cast<volatile const float *>(&V.dcr[m & 3]);
     };
     const float dc0 = dc_of(0);
-    if (issuer) load_u(0);  // chunk 0's flag seen by now
     // Initial state: TMEM fp32 <- d_C(chunk 0) S0, fp16 copy <- S0 (this
     // thread: row lrow, columns 64 ch .. 64 ch + 63).
 #pragma unroll 1
@@ -890,16 +919,14 @@ __device__ __forceinline__ void seq_role(const PrefillArgs &a, const SplitArgs &
     for (int n = 0; n < nch; ++n) {
       const int st = n & 1;
       const uint32_t sb = sbase + st * kStage;
-      if (seq_aborted(V)) break;
-      // MMA4 D = S (-W^T) (warp 8) once the chunk's tiles and U^T are in;
+      // MMA4 D = S (-W^T) (warp 8) once the chunk's tiles are in;
       // MMA5 O1 = S Q^T right after it if the epilogue has read the previous
       // chunk's O1, O2 by then, else after the Delta pass, before MMA7 (so
       // that MMA7's barrier covers MMA5's reads of the fp16 state).  The other
       // chain warps go on to wait for D.  A wait that times out is voted on
       // once, at the chunk's closing barrier.
       __syncwarp();
-      bool w = bar_wait(&V.full[st], (uint32_t)(n >> 1) & 1u);
-      w = bar_wait(&V.bar_u, (uint32_t)n & 1u) && w;
+      const bool w = bar_wait(&V.full[st], (uint32_t)(n >> 1) & 1u);
       ok = ok && w;
       bool o1_done = false;
       auto mma5 = [&]() {
@@ -913,15 +940,17 @@ __device__ __forceinline__ void seq_role(const PrefillArgs &a, const SplitArgs &
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) mma_ta_w(tmem + TS_D, tmem + TS_S16 + 8 * ks, dnw + (uint64_t)(ks * 128), id_km, ks > 0);
         commit_w(&V.bar_d);
-        o1_done = __all_sync(0xffffffffu, n == 0 || bar_try_wait(&V.bar_ofree, (uint32_t)(n - 1) & 1u));
+        o1_done = __all_sync(0xffffffffu, n == 0 || bar_test_wait(&V.bar_ofree, (uint32_t)(n - 1) & 1u));
         if (o1_done) {
           fence_after();
           mma5();
         }
       }
-      // Delta^T = D + U^T -> fp16 hi (MMA6) and (Delta Gamma)^T hi / lo (MMA7)
+      // Delta^T = D + U^T -> fp16 hi (MMA6) and (Delta Gamma)^T hi / lo (MMA7),
+      // once D and U^T are in
       __syncwarp();
       ok = bar_wait(&V.bar_d, (uint32_t)n & 1u) && ok;
+      ok = bar_wait(&V.bar_u, (uint32_t)n & 1u) && ok;
       fence_after();
       {
         // this thread: row lrow, token columns 32 ch .. 32 ch + 31 (U^T box ch)
@@ -960,10 +989,11 @@ __device__ __forceinline__ void seq_role(const PrefillArgs &a, const SplitArgs &
       }
       fence_before();
       named_sync(kBarChain, kChainThreads);
-      // The deferred MMA5, MMA7 (the state update, first: the chain waits for
-      // it), MMA6, then U^T of the next chunk into the buffer just read
-      // (issuer).
+      // U^T is read (the producer may load the next); the deferred MMA5,
+      // MMA7 (the state update, first: the chain waits for it), MMA6 (issuer).
       if (issuer) {
+        if (lane == 0) mbar_arrive(&V.bar_ufree);
+        __syncwarp();
         if (!o1_done) {
           ok = bar_wait(&V.bar_ofree, (uint32_t)(n - 1) & 1u) && ok;
           fence_after();
@@ -983,10 +1013,6 @@ __device__ __forceinline__ void seq_role(const PrefillArgs &a, const SplitArgs &
         for (int ks = 0; ks < 4; ++ks)
           mma_ta_w(tmem + TS_O2, tmem + TS_DH + 8 * ks, desc_k(sb + Q_M, ks, kC), id_kk, ks > 0);
         commit_w(&V.bar_o);
-        if (n + 1 < nch) {
-          ok = ahead_wait(V, n + 2) && ok;  // chunk n + 1's flag seen
-          load_u(n + 1);
-        }
       }
       // The state pass: the fp16 copy and the rescale by the next chunk's
       // decay, or S_T after the last chunk.
@@ -994,6 +1020,7 @@ __device__ __forceinline__ void seq_role(const PrefillArgs &a, const SplitArgs &
       const float dcn = last ? 1.f : dc_of(n + 1);
       __syncwarp();
       ok = bar_wait(&V.bar_s, (uint32_t)n & 1u) && ok;
+      if (tid == kIssuerTid) *reinterpret_cast<volatile int *>(&V.s_seen) = n + 1;
       fence_after();
       {
         uint32_t ra[32];
@@ -1030,13 +1057,17 @@ __device__ __forceinline__ void seq_role(const PrefillArgs &a, const SplitArgs &
       }
       tmem_wait_st();
       fence_before();
-      if (named_sync_or(kBarChain, kChainThreads, !ok)) break;
+      // A timeout here or an abort elsewhere ends the loop for all chain warps
+      // at once (a warp leaving alone would strand the others at a barrier).
+      if (named_sync_or(kBarChain, kChainThreads, !ok || seq_aborted(V))) break;
     }
     if (!ok && tid == kIssuerTid) seq_fail(V, a.err);
   } else {
     // ------------------------------------------- the epilogue (warps 0-6)
     // O staging: warp w takes lane quadrant w & 3, column half w >> 2; lane
-    // quadrant 3 has one epilogue warp (3), which takes both halves.
+    // quadrant 3 has one epilogue warp (3), which takes both halves.  The
+    // chunk's d values are copied out first, so that the stage buffer is
+    // free for the next load once MMA6 is done (V.epi_seen).
     const int quad = warp & 3;
     const int lrow = 32 * quad + lane;
     const uint32_t tl = tmem + ((uint32_t)(32 * quad) << 16);
@@ -1045,14 +1076,16 @@ __device__ __forceinline__ void seq_role(const PrefillArgs &a, const SplitArgs &
     if (tid == 0) load_z(0);
     for (int n = 0; n < nch; ++n) {
       const int st = n & 1;
-      if (seq_aborted(V)) break;
       __syncwarp();
       ok = bar_wait(&V.bar_o, (uint32_t)n & 1u) && ok;
       ok = bar_wait(&V.full[st], (uint32_t)(n >> 1) & 1u) && ok;  // this stage's vectors (long landed)
       fence_after();
+      if (tid < kC) V.de[n & 1][tid] = vec_d(st)[tid];
+      named_sync(kBarEpi, kEpiThreads);
+      if (tid == 0) *reinterpret_cast<volatile int *>(&V.epi_seen) = n + 1;  // MMA6 done, the vectors read
       for (int half = h_lo; half < h_hi; ++half) {  // O^T = d (S Q^T) + Delta^T M^T -> staging [i][v]
         float *ost = reinterpret_cast<float *>(sm + S_OST);
-        const float *dq = vec_d(st) + 32 * half;
+        const float *dq = V.de[n & 1] + 32 * half;
 #pragma unroll
         for (int c0 = 0; c0 < 32; c0 += 16) {
           uint32_t ra[16], rb[16];
@@ -1076,9 +1109,9 @@ __device__ __forceinline__ void seq_role(const PrefillArgs &a, const SplitArgs &
       }
       fence_before();
       named_sync(kBarEpi, kEpiThreads);
-      if (tid == 0) mbar_arrive(&V.bar_ofree);  // O1, O2 and this stage's vectors are read
+      if (tid == 0) mbar_arrive(&V.bar_ofree);  // O1 and O2 are read
       // The gated norm of the chunk's 64 tokens over 14 half-warps: staged O and
-      // z into registers, the z buffer released, then y formed and stored.
+      // z into registers, the z buffer refilled, then y formed and stored.
       __syncwarp();
       ok = bar_wait(&V.bar_z, (uint32_t)n & 1u) && ok;
       const int nv = min(kC, T - kC * n), i0 = 2 * warp + (lane >> 4);
@@ -1088,7 +1121,9 @@ __device__ __forceinline__ void seq_role(const PrefillArgs &a, const SplitArgs &
       if (tid == 0 && n + 1 < nch) load_z(n + 1);  // the z rows are in registers: the next chunk's may land
       if (ok) norm_store<5>(R, static_cast<const bf16 *>(a.norm_w), static_cast<bf16 *>(a.o), d, bos, h, kC * n, nv, i0,
                             14, lane, o_size, a.err);
-      if (named_sync_or(kBarEpi, kEpiThreads, !ok)) break;  // the staging is read; a timeout is voted on here
+      // The staging is read; a timeout here or an abort elsewhere ends the
+      // loop for all epilogue warps at once.
+      if (named_sync_or(kBarEpi, kEpiThreads, !ok || seq_aborted(V))) break;
     }
     if (!ok && tid == 0) seq_fail(V, a.err);
   }
