@@ -213,6 +213,7 @@ __device__ __forceinline__ void prep_role(const PrefillArgs &a, const SplitArgs 
   uint32_t ph_kq = 0, ph_raw = 0, ph_qk = 0, ph_uw = 0;
   bool kq_pending = false, raw_pending = false, stores = false;  // thread 0's bookkeeping
   long long pub = -1;  // thread 0: the item whose outputs are in flight, flagged once they land
+  bool first = true;
 
   // Step `it` of the walk: its workspace item and chunk.
   auto resolve = [&](long long it, ChunkLoc &c) -> long long {
@@ -497,8 +498,12 @@ __device__ __forceinline__ void prep_role(const PrefillArgs &a, const SplitArgs 
       tma_store_2d(tm_u, sbase + P_TF, 32, (int)(item * kD));
       tma_store_2d(tm_nw, sbase + P_NW, 0, (int)(item * kD));
       bulk_commit();
-      if (G.flags) pub = item;
+      if (G.flags) {
+        pub = item;
+        if (first) publish();  // the first items are the launch's first chunks: flag them without delay
+      }
     }
+    first = false;
     it = it_next;
     item = next;
     c = cn;
@@ -640,13 +645,15 @@ __device__ __forceinline__ void seq_fail(SeqShared &V, unsigned int *err) {
 }
 
 // The gated RMSNorm (node gdn.norm) of NR tokens i0, i0 + di, ... of the chunk,
-// one half-warp per token (8 channels per lane).  norm_load takes the staged O
-// and z rows into registers (after it the z buffer may be refilled);
-// norm_store forms y and writes o (valid tokens only).
+// one half-warp per token; lane hl of the half-warp takes channels 4 hl .. 4 hl
+// + 3 and 64 + 4 hl .. 64 + 4 hl + 3 (16-byte reads of the staged rows without
+// bank conflicts).  norm_load takes the staged O and z rows into registers
+// (after it the z buffer may be refilled); norm_store forms y and writes o
+// (valid tokens only).
 template <int NR>
 struct NormRegs {
   float4 o0[NR], o1[NR];
-  uint4 z[NR];
+  uint2 z0[NR], z1[NR];
 };
 template <int NR>
 __device__ __forceinline__ void norm_load(const uint8_t *sm, NormRegs<NR> &R, int nv, int i0, int di, int lane) {
@@ -656,13 +663,18 @@ __device__ __forceinline__ void norm_load(const uint8_t *sm, NormRegs<NR> &R, in
   for (int m = 0; m < NR; ++m) {
     const int i = i0 + di * m;
     R.o0[m] = R.o1[m] = make_float4(0.f, 0.f, 0.f, 0.f);
-    R.z[m] = make_uint4(0u, 0u, 0u, 0u);
+    R.z0[m] = R.z1[m] = make_uint2(0u, 0u);
     if (i < nv) {
-      R.o0[m] = ld4(ost + i * kD + 8 * hl);
-      R.o1[m] = ld4(ost + i * kD + 8 * hl + 4);
-      R.z[m] = *reinterpret_cast<const uint4 *>(sm + S_Z + i * kD * 2 + 16 * hl);
+      R.o0[m] = ld4(ost + i * kD + 4 * hl);
+      R.o1[m] = ld4(ost + i * kD + 64 + 4 * hl);
+      R.z0[m] = *reinterpret_cast<const uint2 *>(sm + S_Z + i * kD * 2 + 8 * hl);
+      R.z1[m] = *reinterpret_cast<const uint2 *>(sm + S_Z + i * kD * 2 + 128 + 8 * hl);
     }
   }
+}
+__device__ __forceinline__ void widen2(uint2 u, float2 (&v)[2]) {
+  v[0] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+  v[1] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
 }
 template <int NR>
 __device__ __forceinline__ void norm_store(const NormRegs<NR> &R, const bf16 *norm_w, bf16 *o, const Dims &d,
@@ -670,18 +682,21 @@ __device__ __forceinline__ void norm_store(const NormRegs<NR> &R, const bf16 *no
                                            long long o_size, unsigned int *err) {
   const int hl = lane & 15;
   float2 wn[4];
-  widen(*reinterpret_cast<const uint4 *>(norm_w + 8 * hl), wn);
-  bf16 *ob = o + ((bos + t0) * d.Hv + h) * kD + 8 * hl;
+  widen2(*reinterpret_cast<const uint2 *>(norm_w + 4 * hl), *reinterpret_cast<float2(*)[2]>(&wn[0]));
+  widen2(*reinterpret_cast<const uint2 *>(norm_w + 64 + 4 * hl), *reinterpret_cast<float2(*)[2]>(&wn[2]));
+  bf16 *ob = o + ((bos + t0) * d.Hv + h) * kD + 4 * hl;
   const long long ostride = (long long)d.Hv * kD;
 #pragma unroll
   for (int m = 0; m < NR; ++m) {
     const int i = i0 + di * m;
+    if (!__any_sync(0xffffffffu, i < nv)) continue;  // no token of this warp (uniform: the shuffles stay converged)
     float ss = dot4(R.o0[m], R.o0[m]) + dot4(R.o1[m], R.o1[m]);
 #pragma unroll
     for (int off = 1; off < 16; off <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
     const float rstd = rsqrtf(ss * (1.0f / kD) + d.eps_norm);
     float2 zz[4];
-    widen(R.z[m], zz);
+    widen2(R.z0[m], *reinterpret_cast<float2(*)[2]>(&zz[0]));
+    widen2(R.z1[m], *reinterpret_cast<float2(*)[2]>(&zz[2]));
     const float2 op[4] = {make_float2(R.o0[m].x, R.o0[m].y), make_float2(R.o0[m].z, R.o0[m].w),
                           make_float2(R.o1[m].x, R.o1[m].y), make_float2(R.o1[m].z, R.o1[m].w)};
     uint32_t yw[4];
@@ -692,8 +707,11 @@ __device__ __forceinline__ void norm_store(const NormRegs<NR> &R, const bf16 *no
       __nv_bfloat162 t = __floats2bfloat162_rn(y.x, y.y);
       yw[q] = *reinterpret_cast<uint32_t *>(&t);
     }
-    if (i < nv && in_bounds((ob + i * ostride - o) + 8, o_size, err))
-      *reinterpret_cast<uint4 *>(ob + i * ostride) = make_uint4(yw[0], yw[1], yw[2], yw[3]);
+    bf16 *orow = ob + i * ostride;
+    if (i < nv && in_bounds((orow - o) + 68, o_size, err)) {
+      *reinterpret_cast<uint2 *>(orow) = make_uint2(yw[0], yw[1]);
+      *reinterpret_cast<uint2 *>(orow + 64) = make_uint2(yw[2], yw[3]);
+    }
   }
 }
 
@@ -1119,8 +1137,9 @@ __device__ __forceinline__ void seq_role(const PrefillArgs &a, const SplitArgs &
       norm_load<5>(sm, R, nv, i0, 14, lane);
       named_sync(kBarEpi, kEpiThreads);
       if (tid == 0 && n + 1 < nch) load_z(n + 1);  // the z rows are in registers: the next chunk's may land
-      if (ok) norm_store<5>(R, static_cast<const bf16 *>(a.norm_w), static_cast<bf16 *>(a.o), d, bos, h, kC * n, nv, i0,
-                            14, lane, o_size, a.err);
+      if (__all_sync(0xffffffffu, ok))  // warp-uniform: the norm's shuffles need the whole warp
+        norm_store<5>(R, static_cast<const bf16 *>(a.norm_w), static_cast<bf16 *>(a.o), d, bos, h, kC * n, nv, i0, 14,
+                      lane, o_size, a.err);
       // The staging is read; a timeout here or an abort elsewhere ends the
       // loop for all epilogue warps at once.
       if (named_sync_or(kBarEpi, kEpiThreads, !ok || seq_aborted(V))) break;

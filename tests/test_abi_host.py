@@ -203,3 +203,4 @@ def test_linear_checked_on_host(L):
     assert L.gdn_linear(4, 16, 64, fake(0), 64, fake(1), 64, 5, out, None) == 1   # too many outputs
     bad = (gdn.gdn_linear_out * 1)(gdn.gdn_linear_out(0, 8, fake(0, 64), 8))
     assert L.gdn_linear(4, 16, 64, fake(0), 64, fake(1), 64, 1, bad, None) == 4  # output over x
+

@@ -47,7 +47,8 @@ def test_split_many_units_two_launches():
 
 def test_split_and_staged_agree():
     """The split and staged forms compute the same chunked recurrence with the
-    same operand roundings; they differ in summation order only."""
+    same operand roundings; they differ in summation order only, so a bf16
+    output may round one unit apart."""
     p = I.prefill_problem(2, 300, 2, 4, io="bf16", case=630)
     so, sS, sc = gpu_prefill(p, staged=True)
     po, pS, pc = gpu_prefill(p, split=True)
@@ -55,7 +56,8 @@ def test_split_and_staged_agree():
     rms = sS.pow(2).mean().sqrt()
     assert (pS - sS).abs().max() <= 1e-3 * rms
     orms = so.float().pow(2).mean().sqrt()
-    assert (po.float() - so.float()).abs().max() <= 2e-2 * orms
+    ulp = torch.exp2(torch.floor(torch.log2(so.float().abs().clamp_min(1e-30))) - 7)  # one bf16 unit of |so|
+    assert ((po.float() - so.float()).abs() - ulp).max() <= 2e-2 * orms
 
 
 def test_split_in_place_state_and_continuation():
