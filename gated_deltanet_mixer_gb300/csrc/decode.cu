@@ -3,21 +3,29 @@
 // decode_kernel takes T <= kDecodeMaxT tokens and can keep the state after
 // every token.
 //
-// One CTA per (sequence b, value head h), 8 warps.  The 128 x 128 fp32 state
-// of the pair is streamed through registers exactly once: each warp owns 16
-// state rows (row = value index i, key index j contiguous), loads them as
-// float4 per lane, and per token forms both S k^ and S q^ in the same pass
-// and updates the rows in registers; the final rows (and, when asked, the
-// rows after every token) are written straight back.  Row i of the update
-// only needs v[i], so no block-wide barrier sits inside the state pass.
+// 8 warps per CTA.  The 128 x 128 fp32 state of a (sequence b, value head h)
+// pair is streamed through registers exactly once: each warp owns 16 state
+// rows (row = value index i, key index j contiguous), per token forms both
+// S k^ and S q^ in the same pass and updates the rows in registers; the
+// final rows (and, when asked, the rows after every token) are written
+// straight back.  Row i of the update only needs v[i], so no block-wide
+// barrier sits inside the state pass.  decode1_kernel: one CTA per pair,
+// lane L holding columns 4L .. 4L + 3 of the warp's rows.  decode_kernel:
+// persistent (two CTAs per SM walking the pairs), the next pair's state
+// copied into shared memory while the current pair's T serial token steps
+// run, and lane (rg, cg) holding 4 rows x 16 columns, so that a token's dot
+// products reduce over 8 lanes.
 //
 // Per token ("How Qwen3.5 works" section 9.6, decay -> predict -> correct ->
 // read; node gdn.core of the Qwen3.8-27B spec for the v x k orientation):
 //   alpha = e^g,  p = alpha S k^,  delta = beta (v - p),
 //   S' = alpha S + delta k^^T,  o = S' q^ = alpha S q^ + delta (k^ . q^)
 // followed by the per-head gated RMSNorm (node gdn.norm).
+#include <cstddef>
+
 #include "gdn_device.cuh"
 #include "launch.h"
+#include "umma.cuh"
 
 namespace gdn {
 namespace {
@@ -185,187 +193,283 @@ __global__ void __launch_bounds__(kThreads, 2) decode1_kernel(DecodeArgs a) {
   }
 }
 
+// The T-token kernel's shared memory: the next unit's state (filled by bulk
+// copies while the current unit is computed from registers) and the current
+// unit's token vectors.
+struct DecodeSmem {
+  float S[kD * kD];  // 64 KB
+  float q[kDecodeMaxT][kD], k[kDecodeMaxT][kD], v[kDecodeMaxT][kD], o[kDecodeMaxT][kD], z[kDecodeMaxT][kD];
+  float kq[kDecodeMaxT], g[kDecodeMaxT], b[kDecodeMaxT];
+  uint64_t bar;  // the state copy landed
+  int stop;
+};
+constexpr uint32_t kStateBytes = kD * kD * 4;
+constexpr size_t kDecodeSmem = sizeof(DecodeSmem) + 128;  // + alignment slack
+static_assert(offsetof(DecodeSmem, S) == 0 && offsetof(DecodeSmem, q) % 16 == 0 && offsetof(DecodeSmem, bar) % 8 == 0,
+              "layout");
+
+__device__ __forceinline__ void bulk_load_state(DecodeSmem &M, const float *src) {
+  umma::bar_expect_tx(&M.bar, kStateBytes);
+#pragma unroll
+  for (int p = 0; p < 4; ++p)
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     umma::smem_u32(M.S + p * (kD * kD / 4))),
+                 "l"(src + p * (kD * kD / 4)), "r"(kStateBytes / 4), "r"(umma::smem_u32(&M.bar))
+                 : "memory");
+}
+
+// Persistent: CTA c takes the (sequence, value head) units c, c + grid, ...
+// While a unit's T token steps run on its state in registers, the bulk copy
+// of the CTA's next unit's state lands in shared memory, so that the state
+// stream does not stop for the serial token steps.  Two CTAs per SM.
 template <typename IO, bool kRawGates>
 __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
+  extern __shared__ uint8_t decode_smem_raw[];
+  DecodeSmem &M = *reinterpret_cast<DecodeSmem *>(decode_smem_raw + ((128 - (umma::smem_u32(decode_smem_raw) & 127)) & 127));
   const Dims d = a.d;
   const int T = d.T;
-  const int unit = blockIdx.x;
-  const int b = unit / d.Hv, h = unit % d.Hv;
-  const int r = d.Hv / d.Hk, kh = h / r;
+  const int nunits = d.B * d.Hv;
+  const int r = d.Hv / d.Hk;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const long long C = d.C;
-
-  __shared__ __align__(16) float s_q[kDecodeMaxT][kD];
-  __shared__ __align__(16) float s_k[kDecodeMaxT][kD];
-  __shared__ float s_v[kDecodeMaxT][kD];
-  __shared__ __align__(16) float s_o[kDecodeMaxT][kD];
-  __shared__ __align__(16) float s_z[kDecodeMaxT][kD];
-  __shared__ float s_kq[kDecodeMaxT];
-  __shared__ float s_g[kDecodeMaxT], s_b[kDecodeMaxT];
-
-  const IO *x = static_cast<const IO *>(a.qkv_pre) + (long long)b * T * C;
-  const IO *win = static_cast<const IO *>(a.conv_in) + (long long)b * 3 * C;
-  IO *wout = static_cast<IO *>(a.conv_out) + (long long)b * 3 * C;
   const IO *cw = static_cast<const IO *>(a.conv_w);
+  const int row0 = warp * kRowsPerWarp;
 
-  // The gates of every token and the z rows of the gated norm, fetched now so
-  // that their loads overlap the front end's instead of sitting one after
-  // another inside the token steps.
-  if (tid < T) {
-    const long long i = ((long long)b * T + tid) * d.Hv + h;
-    float gt, bt;
-    if (kRawGates) {
-      gate_at<IO>(a.gate, i, h, gt, bt);
-    } else {
-      gt = a.gate.g[i];
-      bt = a.gate.beta[i];
-    }
-    s_g[tid] = gt;
-    s_b[tid] = bt;
+  if (tid == 0) {
+    umma::bar_init(&M.bar, 1);
+    M.stop = 0;
   }
-  for (int e = tid; e < T * (kD / 4); e += kThreads) {  // four channels per load
-    const int t = e / (kD / 4), c = 4 * (e % (kD / 4));
-    reinterpret_cast<float4 *>(s_z[t])[c / 4] =
-        ld_io4(static_cast<const IO *>(a.z) + (((long long)b * T + t) * d.Hv + h) * kD + c);
+  umma::fence_smem_to_async();
+  __syncthreads();
+  int unit = blockIdx.x;
+  uint32_t phase = 0;
+  bool pending = false;  // thread 0: a state copy is in flight
+  if (tid == 0 && unit < nunits) {
+    bulk_load_state(M, a.S + (long long)unit * (kD * kD));
+    pending = true;
   }
+  for (; unit < nunits; unit += gridDim.x) {
+    const int b = unit / d.Hv, h = unit % d.Hv, kh = h / r;
+    const IO *x = static_cast<const IO *>(a.qkv_pre) + (long long)b * T * C;
+    const IO *win = static_cast<const IO *>(a.conv_in) + (long long)b * 3 * C;
+    IO *wout = static_cast<IO *>(a.conv_out) + (long long)b * 3 * C;
 
-  // ---- front end: conv + SiLU of the T tokens, sliding the window of the
-  // channel(s) this thread owns (q and k of key head kh, or v of head h)
-  {
-    const bool qk = tid < kD;
-    const long long c0 = qk ? (long long)kh * kD + tid : 2LL * d.Hk * kD + (long long)h * kD + (tid - kD);
-    const long long c1 = (long long)d.Hk * kD + (long long)kh * kD + tid;  // k channel (qk threads)
-    float w0[3] = {ld_io(win + c0), ld_io(win + C + c0), ld_io(win + 2 * C + c0)};
-    float w1[3] = {0.f, 0.f, 0.f};
-    const float4 t0 = ld_io4(cw + 4 * c0);
-    float4 t1 = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (qk) {
-      w1[0] = ld_io(win + c1);
-      w1[1] = ld_io(win + C + c1);
-      w1[2] = ld_io(win + 2 * C + c1);
-      t1 = ld_io4(cw + 4 * c1);
-    }
-    // Tokens in batches of 8: the batch's loads are all issued before the
-    // first is used, so the T tokens cost about T / 8 load latencies.
-    for (int tb = 0; tb < T; tb += 8) {
-      float xa[8], xb[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const bool in = tb + u < T;
-        xa[u] = in ? ld_io(x + (long long)(tb + u) * C + c0) : 0.f;
-        xb[u] = (in && qk) ? ld_io(x + (long long)(tb + u) * C + c1) : 0.f;
+    // The gates of every token and the z rows of the gated norm.
+    if (tid < T) {
+      const long long i = ((long long)b * T + tid) * d.Hv + h;
+      float gt, bt;
+      if (kRawGates) {
+        gate_at<IO>(a.gate, i, h, gt, bt);
+      } else {
+        gt = a.gate.g[i];
+        bt = a.gate.beta[i];
       }
+      M.g[tid] = gt;
+      M.b[tid] = bt;
+    }
+    for (int e = tid; e < T * (kD / 4); e += kThreads) {  // four channels per load
+      const int t = e / (kD / 4), c = 4 * (e % (kD / 4));
+      reinterpret_cast<float4 *>(M.z[t])[c / 4] =
+          ld_io4(static_cast<const IO *>(a.z) + (((long long)b * T + t) * d.Hv + h) * kD + c);
+    }
+
+    // ---- front end: conv + SiLU of the T tokens, sliding the window of the
+    // channel(s) this thread owns (q and k of key head kh, or v of head h)
+    {
+      const bool qk = tid < kD;
+      const long long c0 = qk ? (long long)kh * kD + tid : 2LL * d.Hk * kD + (long long)h * kD + (tid - kD);
+      const long long c1 = (long long)d.Hk * kD + (long long)kh * kD + tid;  // k channel (qk threads)
+      float w0[3] = {ld_io(win + c0), ld_io(win + C + c0), ld_io(win + 2 * C + c0)};
+      float w1[3] = {0.f, 0.f, 0.f};
+      const float4 t0 = ld_io4(cw + 4 * c0);
+      float4 t1 = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (qk) {
+        w1[0] = ld_io(win + c1);
+        w1[1] = ld_io(win + C + c1);
+        w1[2] = ld_io(win + 2 * C + c1);
+        t1 = ld_io4(cw + 4 * c1);
+      }
+      // Tokens in batches of 8: the batch's loads are all issued before the
+      // first is used, so the T tokens cost about T / 8 load latencies.
+      for (int tb = 0; tb < T; tb += 8) {
+        float xa[8], xb[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        if (tb + u >= T) break;
-        const int t = tb + u;
-        const float x0 = xa[u];
-        float acc = fmaf(t0.w, x0, fmaf(t0.z, w0[2], fmaf(t0.y, w0[1], t0.x * w0[0])));
-        w0[0] = w0[1];
-        w0[1] = w0[2];
-        w0[2] = x0;
+        for (int u = 0; u < 8; ++u) {
+          const bool in = tb + u < T;
+          xa[u] = in ? ld_io(x + (long long)(tb + u) * C + c0) : 0.f;
+          xb[u] = (in && qk) ? ld_io(x + (long long)(tb + u) * C + c1) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          if (tb + u >= T) break;
+          const int t = tb + u;
+          const float x0 = xa[u];
+          float acc = fmaf(t0.w, x0, fmaf(t0.z, w0[2], fmaf(t0.y, w0[1], t0.x * w0[0])));
+          w0[0] = w0[1];
+          w0[1] = w0[2];
+          w0[2] = x0;
+          if (qk) {
+            M.q[t][tid] = silu(acc);
+            const float x1 = xb[u];
+            const float acc1 = fmaf(t1.w, x1, fmaf(t1.z, w1[2], fmaf(t1.y, w1[1], t1.x * w1[0])));
+            w1[0] = w1[1];
+            w1[1] = w1[2];
+            w1[2] = x1;
+            M.k[t][tid] = silu(acc1);
+          } else {
+            M.v[t][tid - kD] = silu(acc);
+          }
+        }
+      }
+      // the new window: the last three raw rows (one CTA per key head shifts q/k)
+      const long long wsize = (long long)d.B * 3 * C, wbase = (long long)b * 3 * C;
+      if (!qk || (h % r) == 0) {
+#pragma unroll
+        for (int e = 0; e < 3; ++e)
+          if (in_bounds(wbase + e * C + c0 + 1, wsize, a.err)) st_io(wout + e * C + c0, w0[e]);
         if (qk) {
-          s_q[t][tid] = silu(acc);
-          const float x1 = xb[u];
-          const float acc1 = fmaf(t1.w, x1, fmaf(t1.z, w1[2], fmaf(t1.y, w1[1], t1.x * w1[0])));
-          w1[0] = w1[1];
-          w1[1] = w1[2];
-          w1[2] = x1;
-          s_k[t][tid] = silu(acc1);
-        } else {
-          s_v[t][tid - kD] = silu(acc);
+#pragma unroll
+          for (int e = 0; e < 3; ++e)
+            if (in_bounds(wbase + e * C + c1 + 1, wsize, a.err)) st_io(wout + e * C + c1, w1[e]);
         }
       }
     }
-    // the new window: the last three raw rows (one CTA per key head shifts q/k)
-    const long long wsize = (long long)d.B * 3 * C, wbase = (long long)b * 3 * C;
-    if (!qk || (h % r) == 0) {
+    __syncthreads();
+    // ---- L2 norms of q and k, and k^ . q^, one warp per token
+    for (int t = warp; t < T; t += kWarps) {
+      float4 q4 = reinterpret_cast<const float4 *>(M.q[t])[lane];
+      float4 k4 = reinterpret_cast<const float4 *>(M.k[t])[lane];
+      const float fq = rsqrtf(warp_sum(dot4(q4, q4)) + d.eps_l2) * d.q_scale;
+      const float fk = rsqrtf(warp_sum(dot4(k4, k4)) + d.eps_l2);
+      q4.x *= fq; q4.y *= fq; q4.z *= fq; q4.w *= fq;
+      k4.x *= fk; k4.y *= fk; k4.z *= fk; k4.w *= fk;
+      reinterpret_cast<float4 *>(M.q[t])[lane] = q4;
+      reinterpret_cast<float4 *>(M.k[t])[lane] = k4;
+      const float kq = warp_sum(dot4(q4, k4));
+      if (lane == 0) M.kq[t] = kq;
+    }
+
+    // ---- the state: this unit's copy landed; into registers (each warp its
+    // 16 rows), then the buffer takes the next unit's
+    if (tid == 0) {
+      if (!umma::bar_wait(&M.bar, phase)) {
+        atomicOr(a.err, kErrTimeout);
+        umma::bar_wait(&M.bar, phase);  // once more (bounded): no copy may land after the CTA ends
+        M.stop = 1;
+      }
+      pending = false;
+    }
+    phase ^= 1u;
+    __syncthreads();
+    if (M.stop) break;
+    // Lane (rg, cg) = (lane >> 3, lane & 7) of a warp holds rows row0 + 4 rg
+    // + i (i < 4) at columns 4 cg + 32 m + e (m, e < 4): a token's dot
+    // products then reduce over the 8 lanes of a row group only, and every
+    // shared-memory read of the state or of k^, q^ is conflict-free.
+    const int rg = lane >> 3, cg = lane & 7;
+    const int rbase = row0 + 4 * rg;
+    float4 s[4][4];
 #pragma unroll
-      for (int e = 0; e < 3; ++e)
-        if (in_bounds(wbase + e * C + c0 + 1, wsize, a.err)) st_io(wout + e * C + c0, w0[e]);
-      if (qk) {
+    for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int e = 0; e < 3; ++e)
-          if (in_bounds(wbase + e * C + c1 + 1, wsize, a.err)) st_io(wout + e * C + c1, w1[e]);
+      for (int m = 0; m < 4; ++m) s[i][m] = *reinterpret_cast<const float4 *>(M.S + (rbase + i) * kD + 4 * cg + 32 * m);
+    __syncthreads();
+    if (tid == 0 && unit + (int)gridDim.x < nunits) {
+      bulk_load_state(M, a.S + (long long)(unit + gridDim.x) * (kD * kD));
+      pending = true;
+    }
+
+    // ---- the token steps on the registers
+    const long long gi = (long long)b * d.Hv + h;
+    float *S = a.S + gi * (kD * kD);
+    for (int t = 0; t < T; ++t) {
+      const float alpha = expf(M.g[t]), beta = M.b[t], kq = M.kq[t];
+      float4 k4[4], q4[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        k4[m] = *reinterpret_cast<const float4 *>(M.k[t] + 4 * cg + 32 * m);
+        q4[m] = *reinterpret_cast<const float4 *>(M.q[t] + 4 * cg + 32 * m);
+      }
+      // partial (S k^) and (S q^) of the lane's 4 rows over its 16 columns
+      float part[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float2 ak = __fmul2_rn(make_float2(s[i][0].x, s[i][0].y), make_float2(k4[0].x, k4[0].y));
+        float2 aq = __fmul2_rn(make_float2(s[i][0].x, s[i][0].y), make_float2(q4[0].x, q4[0].y));
+        ak = __ffma2_rn(make_float2(s[i][0].z, s[i][0].w), make_float2(k4[0].z, k4[0].w), ak);
+        aq = __ffma2_rn(make_float2(s[i][0].z, s[i][0].w), make_float2(q4[0].z, q4[0].w), aq);
+#pragma unroll
+        for (int m = 1; m < 4; ++m) {
+          ak = __ffma2_rn(make_float2(s[i][m].x, s[i][m].y), make_float2(k4[m].x, k4[m].y), ak);
+          aq = __ffma2_rn(make_float2(s[i][m].x, s[i][m].y), make_float2(q4[m].x, q4[m].y), aq);
+          ak = __ffma2_rn(make_float2(s[i][m].z, s[i][m].w), make_float2(k4[m].z, k4[m].w), ak);
+          aq = __ffma2_rn(make_float2(s[i][m].z, s[i][m].w), make_float2(q4[m].z, q4[m].w), aq);
+        }
+        part[i] = ak.x + ak.y;
+        part[4 + i] = aq.x + aq.y;
+      }
+      // Sums over the row group's 8 lanes: lane cg ends with value cg,
+      // i.e. (S k^)[rbase + cg] for cg < 4 and (S q^)[rbase + cg - 4] above.
+#pragma unroll
+      for (int o = 4; o >= 1; o >>= 1) {
+        const bool up = (cg & o) != 0;
+#pragma unroll
+        for (int v = 0; v < o; ++v) {
+          const float keep = up ? part[v + o] : part[v], send = up ? part[v] : part[v + o];
+          part[v] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+      }
+      const float Sq = __shfl_down_sync(0xffffffffu, part[0], 4);  // lanes cg < 4: their row's S q^
+      const float delta = beta * (M.v[t][rbase + (cg & 3)] - alpha * part[0]);
+      if (cg < 4) M.o[t][rbase + cg] = fmaf(alpha, Sq, delta * kq);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float di = __shfl_sync(0xffffffffu, delta, (lane & ~7) + i);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) s[i][m] = decay_update(s[i][m], alpha, di, k4[m]);
+      }
+      if (a.S_snap) {
+        const long long so = (((long long)b * T + t) * d.Hv + h) * (kD * kD);
+        float *snap = a.S_snap + so;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const long long off = (long long)(rbase + i) * kD + 4 * cg + 32 * m;
+            if (in_bounds(so + off + 4, (long long)d.B * T * d.Hv * kD * kD, a.err)) st_stream(snap + off, s[i][m]);
+          }
       }
     }
-  }
-  __syncthreads();
-  // ---- L2 norms of q and k, and k^ . q^, one warp per token
-  for (int t = warp; t < T; t += kWarps) {
-    float4 q4 = reinterpret_cast<const float4 *>(s_q[t])[lane];
-    float4 k4 = reinterpret_cast<const float4 *>(s_k[t])[lane];
-    const float fq = rsqrtf(warp_sum(dot4(q4, q4)) + d.eps_l2) * d.q_scale;
-    const float fk = rsqrtf(warp_sum(dot4(k4, k4)) + d.eps_l2);
-    q4.x *= fq; q4.y *= fq; q4.z *= fq; q4.w *= fq;
-    k4.x *= fk; k4.y *= fk; k4.z *= fk; k4.w *= fk;
-    reinterpret_cast<float4 *>(s_q[t])[lane] = q4;
-    reinterpret_cast<float4 *>(s_k[t])[lane] = k4;
-    const float kq = warp_sum(dot4(q4, k4));
-    if (lane == 0) s_kq[t] = kq;
-  }
-  __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const long long off = (long long)(rbase + i) * kD + 4 * cg + 32 * m;
+        if (in_bounds(gi * (kD * kD) + off + 4, (long long)d.B * d.Hv * kD * kD, a.err)) st_stream(S + off, s[i][m]);
+      }
+    __syncthreads();
 
-  // ---- state pass: each warp streams its 16 rows once
-  const long long gi = (long long)b * d.Hv + h;
-  float *S = a.S + gi * (kD * kD);
-  const int row0 = warp * kRowsPerWarp;
-  float4 s[kRowsPerWarp];
-#pragma unroll
-  for (int i = 0; i < kRowsPerWarp; ++i) s[i] = ld_stream(S + (row0 + i) * kD + 4 * lane);
-
-  for (int t = 0; t < T; ++t) {
-    const float alpha = expf(s_g[t]), beta = s_b[t], kq = s_kq[t];
-    const float4 k4 = reinterpret_cast<const float4 *>(s_k[t])[lane];
-    const float4 q4 = reinterpret_cast<const float4 *>(s_q[t])[lane];
-    float part[32];
-#pragma unroll
-    for (int i = 0; i < kRowsPerWarp; ++i) {
-      part[i] = dot4p(s[i], k4);
-      part[16 + i] = dot4p(s[i], q4);
+    // ---- gated RMSNorm over the head's 128 outputs, one warp per token
+    const float4 w4 = ld_io4(static_cast<const IO *>(a.norm_w) + 4 * lane);
+    for (int t = warp; t < T; t += kWarps) {
+      const float4 o4 = reinterpret_cast<const float4 *>(M.o[t])[lane];
+      const float rstd = rsqrtf(warp_sum(dot4(o4, o4)) * (1.0f / kD) + d.eps_norm);
+      const long long oi = (((long long)b * T + t) * d.Hv + h) * kD + 4 * lane;  // [B][T][Hv*Dv]
+      if (!in_bounds(oi + 4, (long long)d.B * T * d.Hv * kD, a.err)) continue;
+      const float4 z4 = reinterpret_cast<const float4 *>(M.z[t])[lane];
+      float4 y;
+      y.x = w4.x * (o4.x * rstd) * silu(z4.x);
+      y.y = w4.y * (o4.y * rstd) * silu(z4.y);
+      y.z = w4.z * (o4.z * rstd) * silu(z4.z);
+      y.w = w4.w * (o4.w * rstd) * silu(z4.w);
+      st_io4(static_cast<IO *>(a.o) + oi, y);
     }
-    // lane L < 16: (S k^)[row0 + L];  lane L >= 16: (S q^)[row0 + L - 16]
-    const float red = transpose_reduce32(part, lane);
-    const int myrow = lane & 15;
-    const float Sk = __shfl_sync(0xffffffffu, red, myrow);
-    const float Sq = __shfl_sync(0xffffffffu, red, myrow + 16);
-    const float delta = beta * (s_v[t][row0 + myrow] - alpha * Sk);
-    if (lane < 16) s_o[t][row0 + myrow] = fmaf(alpha, Sq, delta * kq);
-#pragma unroll
-    for (int i = 0; i < kRowsPerWarp; ++i) {
-      const float di = __shfl_sync(0xffffffffu, delta, i);
-      s[i] = decay_update(s[i], alpha, di, k4);
-    }
-    if (a.S_snap) {
-      const long long so = (((long long)b * T + t) * d.Hv + h) * (kD * kD);
-      float *snap = a.S_snap + so;
-#pragma unroll
-      for (int i = 0; i < kRowsPerWarp; ++i)
-        if (in_bounds(so + (row0 + i) * kD + 4 * lane + 4, (long long)d.B * T * d.Hv * kD * kD, a.err))
-          st_stream(snap + (row0 + i) * kD + 4 * lane, s[i]);
-    }
+    __syncthreads();  // the token vectors are reused by the next unit
   }
-#pragma unroll
-  for (int i = 0; i < kRowsPerWarp; ++i)
-    if (in_bounds(gi * (kD * kD) + (row0 + i) * kD + 4 * lane + 4, (long long)d.B * d.Hv * kD * kD, a.err))
-      st_stream(S + (row0 + i) * kD + 4 * lane, s[i]);
+  // No copy may still land in shared memory when the CTA ends (after a
+  // timeout: one more bounded wait).
+  if (tid == 0 && pending) umma::bar_wait(&M.bar, phase);
   __syncthreads();
-
-  // ---- gated RMSNorm over the head's 128 outputs, one warp per token
-  const float4 w4 = ld_io4(static_cast<const IO *>(a.norm_w) + 4 * lane);
-  for (int t = warp; t < T; t += kWarps) {
-    const float4 o4 = reinterpret_cast<const float4 *>(s_o[t])[lane];
-    const float rstd = rsqrtf(warp_sum(dot4(o4, o4)) * (1.0f / kD) + d.eps_norm);
-    const long long oi = (((long long)b * T + t) * d.Hv + h) * kD + 4 * lane;  // [B][T][Hv*Dv]
-    if (!in_bounds(oi + 4, (long long)d.B * T * d.Hv * kD, a.err)) continue;
-    const float4 z4 = reinterpret_cast<const float4 *>(s_z[t])[lane];
-    float4 y;
-    y.x = w4.x * (o4.x * rstd) * silu(z4.x);
-    y.y = w4.y * (o4.y * rstd) * silu(z4.y);
-    y.z = w4.z * (o4.z * rstd) * silu(z4.z);
-    y.w = w4.w * (o4.w * rstd) * silu(z4.w);
-    st_io4(static_cast<IO *>(a.o) + oi, y);
-  }
 }
 
 }  // namespace
@@ -379,10 +483,17 @@ cudaError_t launch_decode(const DecodeArgs &a, bool bf16, cudaStream_t s) {
       (raw ? decode1_kernel<__nv_bfloat16, true> : decode1_kernel<__nv_bfloat16, false>)<<<grid, block, 0, s>>>(a);
     else
       (raw ? decode1_kernel<float, true> : decode1_kernel<float, false>)<<<grid, block, 0, s>>>(a);
-  } else if (bf16) {
-    (raw ? decode_kernel<__nv_bfloat16, true> : decode_kernel<__nv_bfloat16, false>)<<<grid, block, 0, s>>>(a);
   } else {
-    (raw ? decode_kernel<float, true> : decode_kernel<float, false>)<<<grid, block, 0, s>>>(a);
+    auto kern = bf16 ? (raw ? decode_kernel<__nv_bfloat16, true> : decode_kernel<__nv_bfloat16, false>)
+                     : (raw ? decode_kernel<float, true> : decode_kernel<float, false>);
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecodeSmem);
+    if (e != cudaSuccess) return e;
+    const long long units = (long long)a.d.B * a.d.Hv;
+    const unsigned g = (unsigned)(units < 2LL * sms ? units : 2LL * sms);  // two resident CTAs per SM
+    kern<<<g, block, kDecodeSmem, s>>>(a);
   }
   return cudaGetLastError();
 }
