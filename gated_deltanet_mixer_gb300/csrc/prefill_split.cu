@@ -587,7 +587,7 @@ struct SeqShared {
   int s_seen;                     // chunks whose MMA7 (and the MMAs issued before it) are done
   int epi_seen;                   // chunks whose MMA6 is done and whose vectors the epilogue has read
   alignas(16) float de[2][64];    // the epilogue's copy of chunk n's d at n & 1 (read as float4)
-  float dcr[4];                   // e^{G_last} of chunk m at m % 4
+  float dcr[16];                  // e^{G_last} of chunk m at m % 16
 };
 constexpr uint32_t kSeqSmem = S_BAR + ((sizeof(SeqShared) + 127) / 128) * 128 + 1024;
 static_assert(offsetof(SeqShared, de) % 16 == 0 && S_BAR % 16 == 0, "16-byte loads of the d copy");
@@ -622,23 +622,6 @@ __device__ __forceinline__ bool count_wait(int *p, int m) {
 }
 // The stage producer has covered `m` chunks (V.ahead >= m).
 __device__ __forceinline__ bool ahead_wait(SeqShared &V, int m) { return count_wait(&V.ahead, m); }
-// Bounded wait (about one second) for a prep group of the same launch to set
-// an item's flag; the item's outputs may then be read, by TMA after a proxy
-// fence.
-__device__ __forceinline__ bool flag_wait(const int *f) {
-  auto get = [&]() {
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
-    return v;
-  };
-  if (get() != 0) return true;
-  const uint64_t t0 = global_ns();
-  while (get() == 0) {
-    if (global_ns() - t0 > 1000000000ull) return false;
-    __nanosleep(256);
-  }
-  return true;
-}
 __device__ __forceinline__ void seq_fail(SeqShared &V, unsigned int *err) {
   atomicOr(err, kErrTimeout);
   *reinterpret_cast<volatile int *>(&V.abort) = 1;
@@ -813,8 +796,9 @@ __device__ __forceinline__ void seq_role(const PrefillArgs &a, const SplitArgs &
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------ the producer (warp 7)
-    // Step n: U^T of chunk n once the chain has read chunk n-1's; chunk
-    // n+2's flag (with flags) and decay, announced by V.ahead; the stage of
+    // Step n: U^T of chunk n once the chain has read chunk n-1's; V.ahead
+    // past chunk n+2 (its flag seen, with flags, and its decay in the ring);
+    // the stage of
     // chunk n+1 into chunk n-1's buffer once MMA7(n-1) and MMA6(n-1) are
     // done and the epilogue has read chunk n-1's vectors.  Those two are
     // counters, not barrier phases: while this warp waits for a flag the
@@ -822,16 +806,40 @@ __device__ __forceinline__ void seq_role(const PrefillArgs &a, const SplitArgs &
     // not yet complete.  A chunk's workspace outputs
     // are loaded only after its flag was seen.  Lane 0 issues; every wait is
     // bounded.
-    auto see_flag = [&](int m) -> bool {  // chunk m's flag (lane 0 polls)
-      return !flags || __all_sync(0xffffffffu, lane != 0 || flag_wait(flags + item_of(m)));
-    };
-    auto announce = [&](int m) {  // chunk m's decay into the ring; chunks <= m covered
-      if (lane == 0) {
-        V.dcr[m & 3] = s.ws_vec[item_of(m) * (2 * kC) + kC - 1];
-        __threadfence_block();
-        *reinterpret_cast<volatile int *>(&V.ahead) = m + 1;
+    // V.ahead up to `need`: lanes 0-7 look at the next 8 chunks' flags at
+    // once (with flags), and the leading run that is set is announced with
+    // its decays, one round trip for up to 8 chunks.  The ring holds 16
+    // decays and at most 10 are ahead of the chain's reads.
+    auto advance = [&](int need) -> bool {
+      int have = *reinterpret_cast<volatile int *>(&V.ahead);
+      uint64_t t0 = 0;
+      while (have < need) {
+        const int m = have + lane;
+        const bool mine = lane < 8 && m < nch;
+        bool set = true;
+        if (mine && flags) {
+          int v;
+          asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flags + item_of(m)) : "memory");
+          set = v != 0;
+        }
+        const unsigned run = __ballot_sync(0xffffffffu, !mine || set);
+        const int cnt = min(min(__ffs(~run | 0x100u) - 1, 8), nch - have);
+        if (cnt == 0) {
+          if (t0 == 0) t0 = global_ns();
+          else if (global_ns() - t0 > 1000000000ull) return false;
+          __nanosleep(256);
+          continue;
+        }
+        if (lane < cnt) V.dcr[m & 15] = s.ws_vec[item_of(m) * (2 * kC) + kC - 1];
+        __syncwarp();
+        have += cnt;
+        if (lane == 0) {
+          __threadfence_block();
+          *reinterpret_cast<volatile int *>(&V.ahead) = have;
+        }
+        __syncwarp();
       }
-      __syncwarp();
+      return true;
     };
     auto load_stage = [&](int m) {
       if (flags) fence_proxy_async_all();  // the outputs, released by a prep group, read by TMA
@@ -865,23 +873,17 @@ __device__ __forceinline__ void seq_role(const PrefillArgs &a, const SplitArgs &
       }
       __syncwarp();
     };
-    bool good = see_flag(0);
+    bool good = advance(min(3, nch));
     if (good) {
       load_stage(0);
-      announce(0);
-      if (nch > 1 && (good = see_flag(1))) announce(1);
-    }
-    if (good) load_u(0);
-    if (good && nch > 1) {
-      load_stage(1);
-      if (nch > 2 && (good = see_flag(2))) announce(2);
+      load_u(0);
+      if (nch > 1) load_stage(1);
     }
     for (int n = 1; good && n < nch; ++n) {
       good = __all_sync(0xffffffffu, bar_wait(&V.bar_ufree, (uint32_t)(n - 1) & 1u));
       if (!good || seq_aborted(V)) break;
       load_u(n);
-      if (n + 2 < nch && !(good = see_flag(n + 2))) break;  // meanwhile MMA7(n-1) and the epilogue go on
-      if (n + 2 < nch) announce(n + 2);
+      if (!(good = advance(min(n + 3, nch)))) break;  // meanwhile MMA7(n-1) and the epilogue go on
       if (n + 1 < nch) {  // chunk n+1 goes where chunk n-1 was, once that is done with
         good = __all_sync(0xffffffffu, count_wait(&V.s_seen, n) && count_wait(&V.epi_seen, n));
         if (!good || seq_aborted(V)) break;
@@ -901,7 +903,7 @@ __device__ __forceinline__ void seq_role(const PrefillArgs &a, const SplitArgs &
     // ring once V.ahead > m, in practice a chunk or more before it is needed.
     auto dc_of = [&](int m) -> float {
       if (!ahead_wait(V, m + 1)) ok = false;
-      return *reinterpret_cast<volatile const float *>(&V.dcr[m & 3]);
+      return *reinterpret_cast<volatile const float *>(&V.dcr[m & 15]);
     };
     const float dc0 = dc_of(0);
     // Initial state: TMEM fp32 <- d_C(chunk 0) S0, fp16 copy <- S0 (this
