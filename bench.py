@@ -137,16 +137,19 @@ def source_sha(relpath):
         return hashlib.sha256(f.read()).hexdigest()
 
 
-def recorded_traffic(kernel_key, source_relpath):
-    """DRAM bytes per launch recorded from an ncu capture, if the kernel's
-    source is unchanged since; otherwise None."""
+def recorded_traffic(kernel_key, source_relpaths):
+    """DRAM bytes per launch recorded from an ncu capture, if every source it
+    depends on is unchanged since; otherwise None."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f).get(kernel_key)
     except (OSError, ValueError):
         return None
-    if not rec or rec.get("source_sha256") != source_sha(source_relpath):
+    if not rec:
+        return None
+    shas = rec.get("sources_sha256", {})
+    if sorted(shas) != sorted(source_relpaths) or any(shas[p] != source_sha(p) for p in source_relpaths):
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -385,8 +388,7 @@ def gdn_arm(args, world, rank, local):
             "gpu_launches": args.steps * DECODE_CALLS_PER_STEP * DECODE_KERNELS_PER_CALL,
             "roofline": {"bound": "hbm", "achieved": dach, "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": dach / peaks["hbm_gbs"],
-                         "traffic": recorded_traffic("decode_kernel",
-                                                     "gated_deltanet_mixer_gb300/csrc/decode.cu"),
+                         "traffic": recorded_traffic("decode_kernel", DECODE_SOURCES),
                          "algorithmic_bytes_per_launch": dbytes,
                          "peak_source": peak_src + " hbm_gbs (burst copy)"},
         }
@@ -469,7 +471,7 @@ def gdn_arm(args, world, rank, local):
                    "parallelism": "one GPU per rank, each rank its own batch (weak scaling)"},
         "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": ach / peaks["hbm_gbs"],
-                     "traffic": recorded_traffic("prefill_call", PREFILL_SOURCE),
+                     "traffic": recorded_traffic("prefill_call_4b", PREFILL_SOURCES),
                      "algorithmic_bytes_per_launch": pbytes, "launch_ms": launch_ms,
                      "scope": "one gdn_prefill_ex call: prefill_qk_kernel (q^, k^ once per key head), "
                               "prefill_prep_kernel (every chunk's T, U, W, M at once), prefill_seq_kernel "
@@ -508,7 +510,11 @@ def gdn_arm(args, world, rank, local):
         dist.destroy_process_group()
 
 
-PREFILL_SOURCE = "gated_deltanet_mixer_gb300/csrc/prefill_split.cu"
+# The sources a recorded prefill / decode traffic figure depends on.
+PREFILL_SOURCES = ["gated_deltanet_mixer_gb300/csrc/prefill_split.cu",
+                   "gated_deltanet_mixer_gb300/csrc/prefill_chunked.cu",
+                   "gated_deltanet_mixer_gb300/csrc/chunk_math.cuh"]
+DECODE_SOURCES = ["gated_deltanet_mixer_gb300/csrc/decode.cu"]
 
 
 def time_launches(fn, steps, warmup, stream, barrier, world=1):
@@ -526,6 +532,15 @@ def time_launches(fn, steps, warmup, stream, barrier, world=1):
         ev[k][1].record(stream)
     barrier()
     return max_over_ranks(float(np.mean([s.elapsed_time(e) for s, e in ev])), world)
+
+
+def split_overlaps(B, Hv):
+    """Whether a fixed-length call with a full workspace runs both parts of
+    the chunk-parallel prefill in one cooperative launch (prefill_qk_kernel +
+    prefill_overlap_kernel) rather than three kernels: at most half as many
+    (sequence, value head) units as SMs."""
+    import torch
+    return 2 * B * Hv <= torch.cuda.get_device_properties(0).multi_processor_count
 
 
 def shape_rows(args, peaks, peak_src, stream, barrier, world, rank):
@@ -568,8 +583,10 @@ def shape_rows(args, peaks, peak_src, stream, barrier, world, rank):
         out[name] = {
             "workload": workload_name(name, q), "value": world * q.B * q.T / (ms * 1e-3),
             "unit": "tokens/s", "ms_per_launch": ms, "launches_timed": steps,
+            "kernels_per_launch": 2 if split_overlaps(q.B, q.Hv) else 3,
             "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": ach / peaks["hbm_gbs"], "algorithmic_bytes_per_launch": nb,
+                         "traffic": recorded_traffic("prefill_call_" + name.split("_")[0], PREFILL_SOURCES),
                          "peak_source": peak_src + " hbm_gbs (burst copy)"},
             "roofline_tensor": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"],
                                 "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"],
@@ -663,6 +680,7 @@ def next_rows(args, x, o, S_T, conv_T, p, peaks, peak_src, stream, barrier, worl
             "value": world * dp.B * T / (ms * 1e-3), "unit": "tokens/s", "ms_per_launch": ms,
             "roofline": {"bound": "hbm", "achieved": nb / (ms * 1e-3) / 1e9, "peak": hbm,
                          "unit": "GB/s", "frac": nb / (ms * 1e-3) / 1e9 / hbm,
+                         "traffic": None if with_snap else recorded_traffic("decode_multi_kernel", DECODE_SOURCES),
                          "peak_source": peak_src}}
     del S, snap, conv_in, conv_out, tq, tz, tg, tb, od
 
