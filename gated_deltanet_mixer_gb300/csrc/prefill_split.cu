@@ -586,6 +586,8 @@ struct SeqShared {
   int ahead;                      // chunks 0 .. ahead-1: flags seen (when given) and decays in dcr
   int s_seen;                     // chunks whose MMA7 (and the MMAs issued before it) are done
   int epi_seen;                   // chunks whose MMA6 is done and whose vectors the epilogue has read
+  int epi_zread;                  // chunks whose staged O and z rows 0-31 the epilogue has read
+  int help_loaded;                // chunks whose staged O and z rows 32-63 the chain warps have read
   alignas(16) float de[2][64];    // the epilogue's copy of chunk n's d at n & 1 (read as float4)
   float dcr[16];                  // e^{G_last} of chunk m at m % 16
 };
@@ -604,6 +606,9 @@ constexpr uint32_t TS_S16 = 448;  // state fp16 pairs [v][k/2]           64
 constexpr uint32_t kSeqTmem = 512;
 constexpr int kBarChain = 2;  // warps 8-15
 constexpr int kBarEpi = 3;    // warps 0-6
+constexpr int kBarHelp = 4;   // warps 9-15 (the chain warps that do not issue MMAs)
+constexpr int kHelpThreads = 224;
+constexpr int kHelpLeadTid = 288;  // warp 9, lane 0
 
 __device__ __forceinline__ bool seq_aborted(const SeqShared &V) { return *reinterpret_cast<const volatile int *>(&V.abort) != 0; }
 // Bounded wait (about one second) for a shared counter to reach `m`, then
@@ -776,7 +781,7 @@ __device__ __forceinline__ void seq_role(const PrefillArgs &a, const SplitArgs &
     bar_init(&V.bar_end, 1);
     V.abort = 0;
     V.req_full[0] = V.req_full[1] = V.req_u = V.req_z = 0;
-    V.ahead = V.s_seen = V.epi_seen = 0;
+    V.ahead = V.s_seen = V.epi_seen = V.epi_zread = V.help_loaded = 0;
   }
   if (warp == 0) tmem_alloc(&V.tmem, kSeqTmem);
   fence_before();
@@ -936,6 +941,33 @@ __device__ __forceinline__ void seq_role(const PrefillArgs &a, const SplitArgs &
     tmem_wait_st();
     fence_before();
     named_sync(kBarChain, kChainThreads);
+    // Warps 9-15, while MMA7 runs: the gated norm of chunk m's tokens 32-63
+    // (the epilogue takes 0-31), from the epilogue's staging, over 14
+    // half-warps; the z rows of chunk m+1 are requested once both halves
+    // have read chunk m's.
+    auto help_norm = [&](int m) {
+      const int hw = 2 * (warp - 9) + (lane >> 4);
+      __syncwarp();
+      bool hok = bar_wait(&V.bar_ofree, (uint32_t)m & 1u);
+      hok = bar_wait(&V.bar_z, (uint32_t)m & 1u) && hok;
+      const int nv = min(kC, T - kC * m);
+      NormRegs<3> R;
+      norm_load<3>(sm, R, nv, 32 + hw, 14, lane);
+      named_sync(kBarHelp, kHelpThreads);
+      if (tid == kHelpLeadTid) {
+        if (m + 1 < nch) {
+          hok = count_wait(&V.epi_zread, m + 1) && hok;
+          load_z(m + 1);
+        }
+        __threadfence_block();
+        *reinterpret_cast<volatile int *>(&V.help_loaded) = m + 1;
+      }
+      if (__all_sync(0xffffffffu, hok && ok))
+        norm_store<3>(R, static_cast<const bf16 *>(a.norm_w), static_cast<bf16 *>(a.o), d, bos, h, kC * m, nv, 32 + hw,
+                      14, lane, o_size, a.err);
+      ok = ok && hok;
+    };
+    bool finished = true;
     for (int n = 0; n < nch; ++n) {
       const int st = n & 1;
       const uint32_t sb = sbase + st * kStage;
@@ -1033,6 +1065,8 @@ __device__ __forceinline__ void seq_role(const PrefillArgs &a, const SplitArgs &
         for (int ks = 0; ks < 4; ++ks)
           mma_ta_w(tmem + TS_O2, tmem + TS_DH + 8 * ks, desc_k(sb + Q_M, ks, kC), id_kk, ks > 0);
         commit_w(&V.bar_o);
+      } else if (n > 0) {
+        help_norm(n - 1);
       }
       // The state pass: the fp16 copy and the rescale by the next chunk's
       // decay, or S_T after the last chunk.
@@ -1079,9 +1113,13 @@ __device__ __forceinline__ void seq_role(const PrefillArgs &a, const SplitArgs &
       fence_before();
       // A timeout here or an abort elsewhere ends the loop for all chain warps
       // at once (a warp leaving alone would strand the others at a barrier).
-      if (named_sync_or(kBarChain, kChainThreads, !ok || seq_aborted(V))) break;
+      if (named_sync_or(kBarChain, kChainThreads, !ok || seq_aborted(V))) {
+        finished = false;
+        break;
+      }
     }
-    if (!ok && tid == kIssuerTid) seq_fail(V, a.err);
+    if (finished && !issuer) help_norm(nch - 1);
+    if (!ok && (tid == kIssuerTid || tid == kHelpLeadTid)) seq_fail(V, a.err);
   } else {
     // ------------------------------------------- the epilogue (warps 0-6)
     // O staging: warp w takes lane quadrant w & 3, column half w >> 2; lane
@@ -1101,6 +1139,8 @@ __device__ __forceinline__ void seq_role(const PrefillArgs &a, const SplitArgs &
       ok = bar_wait(&V.full[st], (uint32_t)(n >> 1) & 1u) && ok;  // this stage's vectors (long landed)
       fence_after();
       if (tid < kC) V.de[n & 1][tid] = vec_d(st)[tid];
+      // The chain warps have read chunk n-1's staging (its tokens 32-63).
+      if (n > 0) ok = count_wait(&V.help_loaded, n) && ok;
       named_sync(kBarEpi, kEpiThreads);
       if (tid == 0) *reinterpret_cast<volatile int *>(&V.epi_seen) = n + 1;  // MMA6 done, the vectors read
       for (int half = h_lo; half < h_hi; ++half) {  // O^T = d (S Q^T) + Delta^T M^T -> staging [i][v]
@@ -1130,17 +1170,21 @@ __device__ __forceinline__ void seq_role(const PrefillArgs &a, const SplitArgs &
       fence_before();
       named_sync(kBarEpi, kEpiThreads);
       if (tid == 0) mbar_arrive(&V.bar_ofree);  // O1 and O2 are read
-      // The gated norm of the chunk's 64 tokens over 14 half-warps: staged O and
-      // z into registers, the z buffer refilled, then y formed and stored.
+      // The gated norm of the chunk's tokens 0-31 over 14 half-warps (the
+      // chain warps take 32-63 during the next chunk's MMA7): staged O and z
+      // into registers, then y formed and stored.
       __syncwarp();
       ok = bar_wait(&V.bar_z, (uint32_t)n & 1u) && ok;
-      const int nv = min(kC, T - kC * n), i0 = 2 * warp + (lane >> 4);
-      NormRegs<5> R;
-      norm_load<5>(sm, R, nv, i0, 14, lane);
+      const int nv = min(kC, T - kC * n), nv0 = min(nv, 32), i0 = 2 * warp + (lane >> 4);
+      NormRegs<3> R;
+      norm_load<3>(sm, R, nv0, i0, 14, lane);
       named_sync(kBarEpi, kEpiThreads);
-      if (tid == 0 && n + 1 < nch) load_z(n + 1);  // the z rows are in registers: the next chunk's may land
+      if (tid == 0) {  // this role's z rows are in registers (the chain warps reload z)
+        __threadfence_block();
+        *reinterpret_cast<volatile int *>(&V.epi_zread) = n + 1;
+      }
       if (__all_sync(0xffffffffu, ok))  // warp-uniform: the norm's shuffles need the whole warp
-        norm_store<5>(R, static_cast<const bf16 *>(a.norm_w), static_cast<bf16 *>(a.o), d, bos, h, kC * n, nv, i0, 14,
+        norm_store<3>(R, static_cast<const bf16 *>(a.norm_w), static_cast<bf16 *>(a.o), d, bos, h, kC * n, nv0, i0, 14,
                       lane, o_size, a.err);
       // The staging is read; a timeout here or an abort elsewhere ends the
       // loop for all epilogue warps at once.
