@@ -586,8 +586,8 @@ struct SeqShared {
   int ahead;                      // chunks 0 .. ahead-1: flags seen (when given) and decays in dcr
   int s_seen;                     // chunks whose MMA7 (and the MMAs issued before it) are done
   int epi_seen;                   // chunks whose MMA6 is done and whose vectors the epilogue has read
-  int epi_zread;                  // chunks whose staged O and z rows 0-31 the epilogue has read
-  int help_loaded;                // chunks whose staged O and z rows 32-63 the chain warps have read
+  int epi_zread;                  // chunks whose staged O and z rows 0..kEpiTokens-1 the epilogue has read
+  int help_loaded;                // chunks whose staged O and z rows kEpiTokens.. the chain warps have read
   alignas(16) float de[2][64];    // the epilogue's copy of chunk n's d at n & 1 (read as float4)
   float dcr[16];                  // e^{G_last} of chunk m at m % 16
 };
@@ -609,6 +609,10 @@ constexpr int kBarEpi = 3;    // warps 0-6
 constexpr int kBarHelp = 4;   // warps 9-15 (the chain warps that do not issue MMAs)
 constexpr int kHelpThreads = 224;
 constexpr int kHelpLeadTid = 288;  // warp 9, lane 0
+// The gated norm's tokens: 0 .. kEpiTokens-1 by the epilogue's 14 half-warps,
+// the rest by the 14 half-warps of chain warps 9-15.
+constexpr int kEpiTokens = 40;
+constexpr int kEpiNR = (kEpiTokens + 13) / 14, kHelpNR = (kC - kEpiTokens + 13) / 14;
 
 __device__ __forceinline__ bool seq_aborted(const SeqShared &V) { return *reinterpret_cast<const volatile int *>(&V.abort) != 0; }
 // Bounded wait (about one second) for a shared counter to reach `m`, then
@@ -941,18 +945,18 @@ __device__ __forceinline__ void seq_role(const PrefillArgs &a, const SplitArgs &
     tmem_wait_st();
     fence_before();
     named_sync(kBarChain, kChainThreads);
-    // Warps 9-15, while MMA7 runs: the gated norm of chunk m's tokens 32-63
-    // (the epilogue takes 0-31), from the epilogue's staging, over 14
-    // half-warps; the z rows of chunk m+1 are requested once both halves
-    // have read chunk m's.
+    // Warps 9-15, while MMA7 runs: the gated norm of chunk m's tokens
+    // kEpiTokens .. 63 (the epilogue takes the others), from the epilogue's
+    // staging, over 14 half-warps; the z rows of chunk m+1 are requested once
+    // both parts have read chunk m's.
     auto help_norm = [&](int m) {
       const int hw = 2 * (warp - 9) + (lane >> 4);
       __syncwarp();
       bool hok = bar_wait(&V.bar_ofree, (uint32_t)m & 1u);
       hok = bar_wait(&V.bar_z, (uint32_t)m & 1u) && hok;
       const int nv = min(kC, T - kC * m);
-      NormRegs<3> R;
-      norm_load<3>(sm, R, nv, 32 + hw, 14, lane);
+      NormRegs<kHelpNR> R;
+      norm_load<kHelpNR>(sm, R, nv, kEpiTokens + hw, 14, lane);
       named_sync(kBarHelp, kHelpThreads);
       if (tid == kHelpLeadTid) {
         if (m + 1 < nch) {
@@ -963,8 +967,8 @@ __device__ __forceinline__ void seq_role(const PrefillArgs &a, const SplitArgs &
         *reinterpret_cast<volatile int *>(&V.help_loaded) = m + 1;
       }
       if (__all_sync(0xffffffffu, hok && ok))
-        norm_store<3>(R, static_cast<const bf16 *>(a.norm_w), static_cast<bf16 *>(a.o), d, bos, h, kC * m, nv, 32 + hw,
-                      14, lane, o_size, a.err);
+        norm_store<kHelpNR>(R, static_cast<const bf16 *>(a.norm_w), static_cast<bf16 *>(a.o), d, bos, h, kC * m, nv,
+                            kEpiTokens + hw, 14, lane, o_size, a.err);
       ok = ok && hok;
     };
     bool finished = true;
@@ -1170,22 +1174,22 @@ __device__ __forceinline__ void seq_role(const PrefillArgs &a, const SplitArgs &
       fence_before();
       named_sync(kBarEpi, kEpiThreads);
       if (tid == 0) mbar_arrive(&V.bar_ofree);  // O1 and O2 are read
-      // The gated norm of the chunk's tokens 0-31 over 14 half-warps (the
-      // chain warps take 32-63 during the next chunk's MMA7): staged O and z
-      // into registers, then y formed and stored.
+      // The gated norm of the chunk's tokens 0 .. kEpiTokens-1 over 14
+      // half-warps (the chain warps take the rest during the next chunk's
+      // MMA7): staged O and z into registers, then y formed and stored.
       __syncwarp();
       ok = bar_wait(&V.bar_z, (uint32_t)n & 1u) && ok;
-      const int nv = min(kC, T - kC * n), nv0 = min(nv, 32), i0 = 2 * warp + (lane >> 4);
-      NormRegs<3> R;
-      norm_load<3>(sm, R, nv0, i0, 14, lane);
+      const int nv = min(kC, T - kC * n), nv0 = min(nv, kEpiTokens), i0 = 2 * warp + (lane >> 4);
+      NormRegs<kEpiNR> R;
+      norm_load<kEpiNR>(sm, R, nv0, i0, 14, lane);
       named_sync(kBarEpi, kEpiThreads);
       if (tid == 0) {  // this role's z rows are in registers (the chain warps reload z)
         __threadfence_block();
         *reinterpret_cast<volatile int *>(&V.epi_zread) = n + 1;
       }
       if (__all_sync(0xffffffffu, ok))  // warp-uniform: the norm's shuffles need the whole warp
-        norm_store<3>(R, static_cast<const bf16 *>(a.norm_w), static_cast<bf16 *>(a.o), d, bos, h, kC * n, nv0, i0, 14,
-                      lane, o_size, a.err);
+        norm_store<kEpiNR>(R, static_cast<const bf16 *>(a.norm_w), static_cast<bf16 *>(a.o), d, bos, h, kC * n, nv0, i0,
+                           14, lane, o_size, a.err);
       // The staging is read; a timeout here or an abort elsewhere ends the
       // loop for all epilogue warps at once.
       if (named_sync_or(kBarEpi, kEpiThreads, !ok || seq_aborted(V))) break;
