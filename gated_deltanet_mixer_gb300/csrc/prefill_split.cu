@@ -640,8 +640,9 @@ __device__ __forceinline__ void seq_fail(SeqShared &V, unsigned int *err) {
 // one half-warp per token; lane hl of the half-warp takes channels 4 hl .. 4 hl
 // + 3 and 64 + 4 hl .. 64 + 4 hl + 3 (16-byte reads of the staged rows without
 // bank conflicts).  norm_load takes the staged O and z rows into registers
-// (after it the z buffer may be refilled); norm_store forms y and writes o
-// (valid tokens only).
+// (after it the z buffer may be refilled); norm_store forms y for every slot
+// without branches (a slot past the chunk holds zeros and gives y = 0; the
+// tokens stay independent for the scheduler) and writes o for valid tokens.
 template <int NR>
 struct NormRegs {
   float4 o0[NR], o1[NR];
@@ -681,7 +682,6 @@ __device__ __forceinline__ void norm_store(const NormRegs<NR> &R, const bf16 *no
 #pragma unroll
   for (int m = 0; m < NR; ++m) {
     const int i = i0 + di * m;
-    if (!__any_sync(0xffffffffu, i < nv)) continue;  // no token of this warp (uniform: the shuffles stay converged)
     float ss = dot4(R.o0[m], R.o0[m]) + dot4(R.o1[m], R.o1[m]);
 #pragma unroll
     for (int off = 1; off < 16; off <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
