@@ -25,9 +25,14 @@
 //   MMA6  O2 = Delta^T M^T    MMA7  S += (Delta Gamma)^T K (hi/lo split)
 // and three passes on the CUDA cores: Delta = D + U^T to fp16 (hi, and
 // Gamma-scaled hi/lo); the state pass (fp16 copy, rescale by the next chunk's
-// decay); the epilogue O = d O1 + O2 and the gated RMSNorm (node gdn.norm)
-// on other warps, overlapping the next chunk's chain.  The chunk tiles arrive
-// by TMA two chunks ahead.
+// decay); the epilogue O = d O1 + O2 and the gated RMSNorm (node gdn.norm),
+// on other warps and, for part of the tokens, on the chain warps while MMA7
+// runs, overlapping the next chunk's chain.  The chunk tiles arrive by TMA a
+// chunk or more ahead.
+//
+// prefill_overlap_kernel: both parts in one cooperative launch, for few
+// (sequence, value head) units; the sequential CTAs read a chunk's workspace
+// outputs once the prep group that made them has set the item's flag.
 //
 // Rows of a chunk past its sequence's end carry beta = 0 and g = 0, so their
 // columns of T B, T B D are zero: they add nothing to U, W, Delta or the state,
@@ -547,11 +552,12 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
 // =============================================================================
 // prefill_seq_kernel
 // =============================================================================
-// Warps 0-6: the epilogue (O staging, gated norm); warp 7: the TMA producer
-// (lane 0 the U^T tiles, lane 1 the chunk stages, lane 2 the z rows), each lane
-// waiting for its buffer to be released; warps 8-15: the chain (the
-// state-dependent MMAs, issued by warp 8, and the Delta and state passes, two
-// warps per TMEM lane quadrant, each on half of the columns).
+// Warps 0-6: the epilogue (O staging, the gated norm of most tokens); warp 7:
+// the TMA producer (the U^T tiles and chunk stages, the flags and decays), in
+// one converged loop; warps 8-15: the chain (the state-dependent MMAs, issued
+// by warp 8, and the Delta and state passes, two warps per TMEM lane quadrant,
+// each on half of the columns; warps 9-15 also form the gated norm of the
+// other tokens while MMA7 runs, and reload the z rows).
 constexpr int kSeqThreads = 512;
 constexpr int kProducerWarp = 7;
 constexpr int kEpiThreads = 224;
@@ -578,7 +584,7 @@ struct SeqShared {
   uint64_t bar_o;      // MMA5 and MMA6 done
   uint64_t bar_s;      // MMA7 done
   uint64_t bar_ufree;  // the chain has read U^T (one arrival per chunk)
-  uint64_t bar_ofree;  // the epilogue has read O1, O2 and the stage's vectors (one arrival per chunk)
+  uint64_t bar_ofree;  // the epilogue has staged O1, O2 (one arrival per chunk): TMEM's O is free
   uint64_t bar_end;
   uint32_t tmem;
   int abort;
@@ -794,9 +800,10 @@ __device__ __forceinline__ void seq_role(const PrefillArgs &a, const SplitArgs &
   const uint32_t tmem = V.tmem;
   auto vec_d = [&](int st) { return reinterpret_cast<const float *>(sm + S_VEC + 512 * st); };  // d [64], Gamma [64]
 
-  // The z rows are reloaded by the epilogue once it has taken them into
-  // registers; the stages, the U^T tiles, the flags and the decays by the
-  // producer warp, in one ordered loop (no warp runs diverged waits).
+  // The z rows are reloaded by the chain warps once both parts of the gated
+  // norm have read them (chunk 0's by the epilogue); the stages, the U^T
+  // tiles, the flags and the decays by the producer warp, in one ordered loop
+  // (no warp runs diverged waits).
   auto load_z = [&](int n) {  // one thread
     bar_expect_tx(&V.bar_z, kC * kD * 2);
     tma_load_3d(sbase + S_Z, tm_z, h * kD, (int)(bos + kC * n), 0, &V.bar_z);
@@ -805,16 +812,15 @@ __device__ __forceinline__ void seq_role(const PrefillArgs &a, const SplitArgs &
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------ the producer (warp 7)
-    // Step n: U^T of chunk n once the chain has read chunk n-1's; V.ahead
-    // past chunk n+2 (its flag seen, with flags, and its decay in the ring);
-    // the stage of
-    // chunk n+1 into chunk n-1's buffer once MMA7(n-1) and MMA6(n-1) are
-    // done and the epilogue has read chunk n-1's vectors.  Those two are
-    // counters, not barrier phases: while this warp waits for a flag the
-    // chain may finish another chunk, and a phase two ahead would read as
-    // not yet complete.  A chunk's workspace outputs
-    // are loaded only after its flag was seen.  Lane 0 issues; every wait is
-    // bounded.
+    // Step n: U^T of chunk n once the chain has read chunk n-1's; then
+    // V.ahead past chunk n+2 (its flag seen, with flags, and its decay in the
+    // ring); then the stage of chunk n+1 into chunk n-1's buffer once
+    // MMA7(n-1) and MMA6(n-1) are done and the epilogue has copied chunk
+    // n-1's vectors.  The stage's two conditions are counters, not barrier
+    // phases: while this warp waits for a flag the chain may finish another
+    // chunk, and a phase two ahead would read as not yet complete.  A chunk's
+    // workspace outputs are loaded only after its flag was seen.  Lane 0
+    // issues; every wait is bounded.
     // V.ahead up to `need`: lanes 0-7 look at the next 8 chunks' flags at
     // once (with flags), and the leading run that is set is announced with
     // its decays, one round trip for up to 8 chunks.  The ring holds 16
@@ -1143,7 +1149,7 @@ __device__ __forceinline__ void seq_role(const PrefillArgs &a, const SplitArgs &
       ok = bar_wait(&V.full[st], (uint32_t)(n >> 1) & 1u) && ok;  // this stage's vectors (long landed)
       fence_after();
       if (tid < kC) V.de[n & 1][tid] = vec_d(st)[tid];
-      // The chain warps have read chunk n-1's staging (its tokens 32-63).
+      // The chain warps have read chunk n-1's staging (its tokens kEpiTokens..63).
       if (n > 0) ok = count_wait(&V.help_loaded, n) && ok;
       named_sync(kBarEpi, kEpiThreads);
       if (tid == 0) *reinterpret_cast<volatile int *>(&V.epi_seen) = n + 1;  // MMA6 done, the vectors read
@@ -1173,7 +1179,7 @@ __device__ __forceinline__ void seq_role(const PrefillArgs &a, const SplitArgs &
       }
       fence_before();
       named_sync(kBarEpi, kEpiThreads);
-      if (tid == 0) mbar_arrive(&V.bar_ofree);  // O1 and O2 are read
+      if (tid == 0) mbar_arrive(&V.bar_ofree);  // O1 and O2 are read: MMA5, MMA6 of the next chunk may write them
       // The gated norm of the chunk's tokens 0 .. kEpiTokens-1 over 14
       // half-warps (the chain warps take the rest during the next chunk's
       // MMA7): staged O and z into registers, then y formed and stored.
