@@ -66,6 +66,8 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // This thread's committed stores are complete (visible in global memory).
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// ... all but the most recently committed group.
+__device__ __forceinline__ void bulk_wait_all_but_one() { asm volatile("cp.async.bulk.wait_group 1;" ::: "memory"); }
 
 // 16 consecutive 32-bit TMEM columns of this warp's 32 lanes (raw words), no
 // wait: tmem_wait_ld() before the registers are used.
@@ -263,12 +265,15 @@ __device__ __forceinline__ void zero_T_upper(const SolveSmem &s, int first, int 
 // T = (I + L)^{-1} (L strictly lower, 64 x 64) in fp32 by recursive doubling on
 // 16 x 16 blocks, by 256 threads (tid 0..255) that meet on named barrier
 // `bar`: the four diagonal blocks by forward substitution (one column per
-// thread); the 32 x 32 halves by T_BA = -T_BB (L_BA T_AA); the whole by the
-// same identity on the halves.  Threads idle in a product convert finished
-// blocks to the fp16 tiles meanwhile.  With zero_upper, threads 128..255
-// re-zero the upper blocks of all three tiles during the last product (for
-// callers that stage other data in the tiles' space between solves).
-__device__ __forceinline__ void solve_T(const SolveSmem &s, const ChunkVecs &V, int tid, int bar, bool zero_upper) {
+// thread, tid 0..63; the other threads call `idle` meanwhile); the 32 x 32
+// halves by T_BA = -T_BB (L_BA T_AA); the whole by the same identity on the
+// halves.  Threads idle in a product convert finished blocks to the fp16 tiles
+// meanwhile.  With zero_upper, threads 128..255 re-zero the upper blocks of
+// all three tiles during the last product (for callers that stage other data
+// in the tiles' space between solves).
+template <typename Idle>
+__device__ __forceinline__ void solve_T(const SolveSmem &s, const ChunkVecs &V, int tid, int bar, bool zero_upper,
+                                        Idle &&idle) {
   const float *L = s.L;
   float *Tf = s.Tf;
   float *P = s.P;
@@ -293,6 +298,8 @@ __device__ __forceinline__ void solve_T(const SolveSmem &s, const ChunkVecs &V, 
     }
 #pragma unroll
     for (int i = 0; i < 16; ++i) Tf[tfi(base + i, base + c)] = xv[i];
+  } else {
+    idle();
   }
   __syncwarp();
   named_sync(bar, 256);

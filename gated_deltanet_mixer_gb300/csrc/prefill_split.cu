@@ -132,7 +132,7 @@ constexpr uint32_t P_TF = P_RAW + 64 * kLs * 4;  // T fp32 [64][64] (tfi); then 
 constexpr uint32_t P_PB = P_TF + 16384;          // solve block products                                 4 KB
 constexpr uint32_t P_VEC = P_PB + 4096;
 struct PrepShared {
-  ChunkVecs cv;
+  ChunkVecs cv[2];  // the group's k-th item uses cv[k & 1]; the next item's are formed meanwhile
   uint64_t bar_kq, bar_raw, bar_qk, bar_uw;
   uint32_t tmem;
   int abort;
@@ -150,6 +150,8 @@ constexpr uint32_t TP_W = 192;   // -W^T [k][i]                       64
 constexpr uint32_t kPrepTmem = 256;
 constexpr int kBarSolve = 1;  // a prep group's solve barrier (the second group: 3)
 constexpr int kBarPrep = 2;   // a prep group's own barrier (the second group: 4)
+constexpr int kStoreTid = 192;  // warp 6, lane 0: a group's workspace stores and flags
+constexpr int kGateWarp = 7;    // a group's gates and chunk vectors
 
 // A prep group: 256 threads (8 warps) with their own kPrepSmem of shared
 // memory, 256 TMEM columns and named barriers, taking work items first,
@@ -179,8 +181,11 @@ __device__ __forceinline__ void st_release_gpu(int *p, int v) {
 __device__ __forceinline__ void fence_proxy_async_all() { asm volatile("fence.proxy.async;" ::: "memory"); }
 
 // The next item's tiles and gates are requested while the current one is
-// computed: its raw v rows once the solve is done with L (their space), its
-// [K;Q] once MMA W is done.
+// computed: its q^ rows once MMA1 is done with them, its raw v rows once the
+// solve is done with L (their space), its k^ rows once MMA W is done; its
+// chunk vectors are formed while MMA U / W runs.  The workspace stores (and,
+// with flags, their completion and the flag) belong to one thread of warp 6,
+// which has no part in the first step of the solve and waits there.
 template <bool kRawGates>
 __device__ __forceinline__ void prep_role(const PrefillArgs &a, const SplitArgs &s, const CUtensorMap *tm_qkv,
                                           const CUtensorMap *tm_qk, const CUtensorMap *tm_u, const CUtensorMap *tm_nw,
@@ -216,8 +221,9 @@ __device__ __forceinline__ void prep_role(const PrefillArgs &a, const SplitArgs 
   const uint32_t tl = tmem + ((uint32_t)(32 * quad) << 16);
   const uint32_t id_kk = idesc(128, 64, 0, 0), id_mk = idesc(128, 64, 1, 0);
   uint32_t ph_kq = 0, ph_raw = 0, ph_qk = 0, ph_uw = 0;
-  bool kq_pending = false, raw_pending = false, stores = false;  // thread 0's bookkeeping
-  long long pub = -1;  // thread 0: the item whose outputs are in flight, flagged once they land
+  bool q_req = false, k_req = false, raw_pending = false;  // thread 0: loads in flight
+  bool stores = false;  // kStoreTid: stores issued
+  long long pub = -1;   // kStoreTid: the item whose outputs are in flight, flagged once they land
   bool first = true;
 
   // Step `it` of the walk: its workspace item and chunk.
@@ -239,32 +245,45 @@ __device__ __forceinline__ void prep_role(const PrefillArgs &a, const SplitArgs 
     }
     return nitems;
   };
-  auto publish = [&]() {
+  // kStoreTid: the flag of the item in flight once its outputs have landed
+  // (keep_newest: the most recent store group may still be in flight).
+  auto publish = [&](bool keep_newest) {
     if (pub >= 0) {
-      bulk_wait_all();
+      if (keep_newest) bulk_wait_all_but_one();
+      else bulk_wait_all();
       fence_proxy_async_all();
       __threadfence();
       st_release_gpu(G.flags + pub, 1);
       pub = -1;
     }
   };
-  // Thread 0: an item's [K;Q] (q^ rows 64-127, k^ hi rows 0-63) and raw v rows.
-  auto request_kq = [&](long long it, const ChunkLoc &c) {
+  // Thread 0: an item's q^ rows (rows 64-127 of [K;Q]) and k^ hi rows (rows
+  // 0-63) complete one phase of bar_kq: the first part only announces its
+  // bytes, the second arrives.  The raw v rows complete bar_raw.
+  auto load_kq_part = [&](long long it, const ChunkLoc &c, int plane) {
     const int kh = (int)(it % d.Hv) / r;
-    bar_expect_tx(&V.bar_kq, 2 * kC * kD * 2);
 #pragma unroll
-    for (int at = 0; at < 2; ++at) {
-      tma_load_3d(sbase + P_KQ + at * 16384 + 64 * 128, tm_qk, kh * kD + 64 * at, c.bos + kC * c.n, 0, &V.bar_kq);
-      tma_load_3d(sbase + P_KQ + at * 16384, tm_qk, kh * kD + 64 * at, c.bos + kC * c.n, 1, &V.bar_kq);
-    }
-    kq_pending = true;
+    for (int at = 0; at < 2; ++at)
+      tma_load_3d(sbase + P_KQ + at * 16384 + (plane == 0 ? 64 * 128 : 0), tm_qk, kh * kD + 64 * at, c.bos + kC * c.n,
+                  plane, &V.bar_kq);
+  };
+  auto request_q = [&](long long it, const ChunkLoc &c) {
+    bar_expect_tx_only(&V.bar_kq, kC * kD * 2);
+    load_kq_part(it, c, 0);
+    q_req = true;
+  };
+  auto request_k = [&](long long it, const ChunkLoc &c) {
+    bar_expect_tx(&V.bar_kq, kC * kD * 2);
+    load_kq_part(it, c, 1);
+    k_req = true;
   };
   auto request_raw = [&](long long it, const ChunkLoc &c) {
     bar_expect_tx(&V.bar_raw, kRawBlock);
     tma_load_3d(sbase + P_RAW, tm_qkv, (int)(cv0 + (it % d.Hv) * kD), c.bos + kC * c.n - 3, 0, &V.bar_raw);
     raw_pending = true;
   };
-  // Warp 7: an item's gates (raw bf16 bits for raw projections), a chunk ahead.
+  // kGateWarp: an item's gates (raw bf16 bits for raw projections), requested
+  // an item before its chunk vectors are formed.
   float gv[2] = {0.f, 0.f}, bv[2] = {0.f, 0.f}, nea = 0.f, dtb = 0.f;
   auto load_gates = [&](long long it, const ChunkLoc &c) {
     const int h = (int)(it % d.Hv);
@@ -274,18 +293,30 @@ __device__ __forceinline__ void prep_role(const PrefillArgs &a, const SplitArgs 
       dtb = a.gate.dt_bias[h];
     }
   };
+  auto form_vectors = [&](const ChunkLoc &c, ChunkVecs &cvd) {
+    finish_gb<kRawGates>(kRawGates ? -expf(nea) : 0.f, dtb, kC * c.n, c.len, lane, gv, bv);
+    chunk_vectors(cvd, gv, bv, lane);
+  };
 
   ChunkLoc c{};
   long long item = 0;
   long long it = next_valid(G.first, c, item);
   if (it < nitems) {
     if (tid == 0) {
-      request_kq(item, c);
+      request_q(item, c);
+      request_k(item, c);
       request_raw(item, c);
     }
-    if (warp == 7) load_gates(item, c);
+    if (warp == kGateWarp) {  // the first item's chunk vectors; the second item's gates
+      load_gates(item, c);
+      form_vectors(c, V.cv[0]);
+      ChunkLoc c2{};
+      long long item2 = 0;
+      if (next_valid(it + G.step, c2, item2) < nitems) load_gates(item2, c2);
+    }
   }
-  while (it < nitems) {
+  for (int k = 0; it < nitems; ++k) {
+    const ChunkVecs &CV = V.cv[k & 1];
     const int h = (int)(item % d.Hv);
     const int t0 = kC * c.n, T = c.len;
     const long long cv = cv0 + (long long)h * kD;
@@ -293,15 +324,18 @@ __device__ __forceinline__ void prep_role(const PrefillArgs &a, const SplitArgs 
     long long next = 0;
     const long long it_next = next_valid(it + G.step, cn, next);
     const bool more = it_next < nitems;
-    if (warp == 7) {  // this item's chunk vectors, then the next item's gates requested
-      finish_gb<kRawGates>(kRawGates ? -expf(nea) : 0.f, dtb, t0, T, lane, gv, bv);
-      chunk_vectors(V.cv, gv, bv, lane);
-      if (more) load_gates(next, cn);
-    }
     __syncwarp();
-    bool ok = bar_wait(&V.bar_kq, ph_kq) && bar_wait(&V.bar_raw, ph_raw);
-    ph_kq ^= 1u;
-    ph_raw ^= 1u;
+    const bool kq_ok = bar_wait(&V.bar_kq, ph_kq);
+    const bool raw_ok = kq_ok && bar_wait(&V.bar_raw, ph_raw);
+    if (kq_ok) {
+      ph_kq ^= 1u;
+      if (tid == 0) q_req = k_req = false;
+    }
+    if (raw_ok) {
+      ph_raw ^= 1u;
+      if (tid == 0) raw_pending = false;
+    }
+    bool ok = raw_ok;
     if (group_sync_or(G, !ok)) {
       if (tid == 0) {
         atomicOr(a.err, kErrTimeout);
@@ -309,7 +343,6 @@ __device__ __forceinline__ void prep_role(const PrefillArgs &a, const SplitArgs 
       }
       break;
     }
-    if (tid == 0) kq_pending = raw_pending = false;
     if (c.n == 0) {  // rows before the sequence's first token: the carried window, or zeros
       if (tid < 48) {
         const int rw = tid >> 4, g8 = tid & 15;
@@ -363,12 +396,8 @@ __device__ __forceinline__ void prep_role(const PrefillArgs &a, const SplitArgs 
       tmem_wait_st();
     }
     // The previous item's stores must have read their sources (M, the T tiles
-    // and the T scratch are written next); with flags they must have landed,
-    // and the item's flag is set.
-    if (tid == 0 && stores) {
-      if (G.flags) publish();
-      else bulk_wait_read();
-    }
+    // and the T scratch are written next).
+    if (tid == kStoreTid && stores) bulk_wait_read();
     fence_before();
     group_sync(G);  // the v rows are read: L may take their space
     ok = bar_wait(&V.bar_qk, ph_qk);
@@ -381,9 +410,10 @@ __device__ __forceinline__ void prep_role(const PrefillArgs &a, const SplitArgs 
       }
       break;
     }
+    // MMA1 is done with the q^ rows: the next item's may land.
+    if (tid == 0 && more) request_q(next, cn);
     // L (fp32, strictly lower, decayed beta K K^T) and M (fp16, decayed Q K^T incl. the diagonal)
     {
-      const ChunkVecs &CV = V.cv;
       float v[32], rr[32];
       tmem_ld32(tl + TP_KQ + 32 * half, v);
       const int j0 = 32 * half;
@@ -434,14 +464,18 @@ __device__ __forceinline__ void prep_role(const PrefillArgs &a, const SplitArgs 
     }
     fence_smem_to_async();
     group_sync(G);  // L and M written
-    if (tid == 0) {
+    if (tid == kStoreTid) {
       tma_store_2d(tm_m, sbase + P_M, 0, (int)(item * kC));
       bulk_commit();
       stores = true;
     }
     // T = (I + L)^{-1} and the fp16 tiles (their upper blocks are zeroed
-    // again: the previous item's -W^T and U^T staging used their space)
-    solve_T(ss, V.cv, tid, G.bar_solve, true);
+    // again: the previous item's -W^T and U^T staging used their space).
+    // With flags, the store thread sets the previous item's flag once its
+    // outputs have landed while the diagonal blocks are solved.
+    solve_T(ss, CV, tid, G.bar_solve, true, [&]() {
+      if (tid == kStoreTid && G.flags) publish(true);
+    });
     fence_smem_to_async();
     fence_before();
     group_sync(G);
@@ -460,8 +494,14 @@ __device__ __forceinline__ void prep_role(const PrefillArgs &a, const SplitArgs 
     }
     if (tid < 2 * kC) {  // the chunk vectors d and Gamma, fp32 [2][64]
       float *vec = s.ws_vec + item * (2 * kC);
-      if (in_bounds(item * (2 * kC) + tid + 1, nitems * (2 * kC), a.err)) vec[tid] = tid < kC ? V.cv.d[tid] : V.cv.gam[tid - kC];
+      if (in_bounds(item * (2 * kC) + tid + 1, nitems * (2 * kC), a.err)) vec[tid] = tid < kC ? CV.d[tid] : CV.gam[tid - kC];
       if (G.flags) __threadfence();  // ordered before the item's flag
+    }
+    if (warp == kGateWarp && more) {  // the next item's chunk vectors; the gates of the one after it
+      form_vectors(cn, V.cv[(k + 1) & 1]);
+      ChunkLoc c2{};
+      long long item2 = 0;
+      if (next_valid(it_next + G.step, c2, item2) < nitems) load_gates(item2, c2);
     }
     __syncwarp();
     ok = bar_wait(&V.bar_uw, ph_uw);
@@ -474,12 +514,10 @@ __device__ __forceinline__ void prep_role(const PrefillArgs &a, const SplitArgs 
       }
       break;
     }
-    // MMA W is done with [K;Q]: the next item's may land.  The M store is
-    // long complete (its space takes U^T box 0).
-    if (tid == 0) {
-      if (more) request_kq(next, cn);
-      bulk_wait_read();
-    }
+    // MMA W is done with the k^ rows: the next item's may land.  The M store
+    // has long read its source (whose space takes U^T box 0).
+    if (tid == 0 && more) request_k(next, cn);
+    if (tid == kStoreTid) bulk_wait_read();
     group_sync(G);
     {
       // U^T [v][i] fp32 -> staging box `half` (rows v, 32 values of 4 bytes, 128-byte swizzle)
@@ -498,14 +536,14 @@ __device__ __forceinline__ void prep_role(const PrefillArgs &a, const SplitArgs 
     fence_smem_to_async();
     fence_before();
     group_sync(G);
-    if (tid == 0) {
+    if (tid == kStoreTid) {
       tma_store_2d(tm_u, sbase + P_UB0, 0, (int)(item * kD));
       tma_store_2d(tm_u, sbase + P_TF, 32, (int)(item * kD));
       tma_store_2d(tm_nw, sbase + P_NW, 0, (int)(item * kD));
       bulk_commit();
       if (G.flags) {
         pub = item;
-        if (first) publish();  // the first items are the launch's first chunks: flag them without delay
+        if (first) publish(false);  // the first items are the launch's first chunks: flag them without delay
       }
     }
     first = false;
@@ -514,11 +552,15 @@ __device__ __forceinline__ void prep_role(const PrefillArgs &a, const SplitArgs 
     c = cn;
   }
   // Before the group ends: the stores complete (the last item flagged), no
-  // load still lands, and no MMA still writes TMEM (after an early exit).
-  if (tid == 0) {
+  // load still lands (a q^ request alone completes its phase with an
+  // arrival), and no MMA still writes TMEM (after an early exit).
+  if (tid == kStoreTid) {
     bulk_wait_all();
-    if (G.flags) publish();
-    if (kq_pending) bar_wait(&V.bar_kq, ph_kq);
+    if (G.flags) publish(false);
+  }
+  if (tid == 0) {
+    if (q_req && !k_req) mbar_arrive(&V.bar_kq);
+    if (q_req || k_req) bar_wait(&V.bar_kq, ph_kq);
     if (raw_pending) bar_wait(&V.bar_raw, ph_raw);
   }
   fence_before();
