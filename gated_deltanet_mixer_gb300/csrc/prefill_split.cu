@@ -226,15 +226,18 @@ __device__ __forceinline__ void prep_role(const PrefillArgs &a, const SplitArgs 
   long long pub = -1;   // kStoreTid: the item whose outputs are in flight, flagged once they land
   bool first = true;
 
-  // Step `it` of the walk: its workspace item and chunk.
+  // Step `it` of the walk: its workspace item and chunk.  Steps and items
+  // are below 2^24 (the host's limit), so the divisions are 32-bit.
+  const unsigned hv = (unsigned)d.Hv;
+  auto head_of = [&](long long it) -> int { return (int)((unsigned)it % hv); };
   auto resolve = [&](long long it, ChunkLoc &c) -> long long {
     if (!G.flags) {
-      c = locate(s, (int)(it / d.Hv));
+      c = locate(s, (int)((unsigned)it / hv));
       return it;
     }
-    const long long bh = (long long)s.B * d.Hv;
-    const int n = (int)(it / bh), b = (int)((it % bh) / d.Hv), h = (int)(it % d.Hv);
-    c = ChunkLoc{b, n, b * s.T, s.T, true};
+    const unsigned bh = (unsigned)s.B * hv;
+    const unsigned n = (unsigned)it / bh, rem = (unsigned)it - n * bh, b = rem / hv, h = rem - b * hv;
+    c = ChunkLoc{(int)b, (int)n, (int)b * s.T, s.T, true};
     return ((long long)b * s.nch + n) * d.Hv + h;
   };
   // The next step at or after `it` with a valid chunk (every thread computes the same).
@@ -261,7 +264,7 @@ __device__ __forceinline__ void prep_role(const PrefillArgs &a, const SplitArgs 
   // 0-63) complete one phase of bar_kq: the first part only announces its
   // bytes, the second arrives.  The raw v rows complete bar_raw.
   auto load_kq_part = [&](long long it, const ChunkLoc &c, int plane) {
-    const int kh = (int)(it % d.Hv) / r;
+    const int kh = head_of(it) / r;
 #pragma unroll
     for (int at = 0; at < 2; ++at)
       tma_load_3d(sbase + P_KQ + at * 16384 + (plane == 0 ? 64 * 128 : 0), tm_qk, kh * kD + 64 * at, c.bos + kC * c.n,
@@ -279,14 +282,14 @@ __device__ __forceinline__ void prep_role(const PrefillArgs &a, const SplitArgs 
   };
   auto request_raw = [&](long long it, const ChunkLoc &c) {
     bar_expect_tx(&V.bar_raw, kRawBlock);
-    tma_load_3d(sbase + P_RAW, tm_qkv, (int)(cv0 + (it % d.Hv) * kD), c.bos + kC * c.n - 3, 0, &V.bar_raw);
+    tma_load_3d(sbase + P_RAW, tm_qkv, (int)(cv0 + head_of(it) * kD), c.bos + kC * c.n - 3, 0, &V.bar_raw);
     raw_pending = true;
   };
   // kGateWarp: an item's gates (raw bf16 bits for raw projections), requested
   // an item before its chunk vectors are formed.
   float gv[2] = {0.f, 0.f}, bv[2] = {0.f, 0.f}, nea = 0.f, dtb = 0.f;
   auto load_gates = [&](long long it, const ChunkLoc &c) {
-    const int h = (int)(it % d.Hv);
+    const int h = head_of(it);
     load_gb<kRawGates>(a.gate, c.bos, d.Hv, h, kC * c.n, c.len, lane, gv, bv);
     if (kRawGates) {
       nea = a.gate.A_log[h];
@@ -317,7 +320,7 @@ __device__ __forceinline__ void prep_role(const PrefillArgs &a, const SplitArgs 
   }
   for (int k = 0; it < nitems; ++k) {
     const ChunkVecs &CV = V.cv[k & 1];
-    const int h = (int)(item % d.Hv);
+    const int h = head_of(item);
     const int t0 = kC * c.n, T = c.len;
     const long long cv = cv0 + (long long)h * kD;
     ChunkLoc cn{};
