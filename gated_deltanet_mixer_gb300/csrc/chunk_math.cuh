@@ -225,11 +225,12 @@ struct SolveSmem {
 __device__ __forceinline__ int tfi(int row, int col) {
   return row * kC + ((((col >> 2) ^ (row & 15)) << 2) | (col & 3));
 }
+// acc += s t, on the paired fp32 pipes.
 __device__ __forceinline__ void fma4(float4 &acc, float s, const float4 t) {
-  acc.x = fmaf(s, t.x, acc.x);
-  acc.y = fmaf(s, t.y, acc.y);
-  acc.z = fmaf(s, t.z, acc.z);
-  acc.w = fmaf(s, t.w, acc.w);
+  const float2 ss = make_float2(s, s);
+  const float2 lo = __ffma2_rn(ss, make_float2(t.x, t.y), make_float2(acc.x, acc.y));
+  const float2 hi = __ffma2_rn(ss, make_float2(t.z, t.w), make_float2(acc.z, acc.w));
+  acc = make_float4(lo.x, lo.y, hi.x, hi.y);
 }
 
 // Row i, columns j .. j+3 of T -> T diag(beta) (hi, lo) and -T diag(beta d)
@@ -265,7 +266,8 @@ __device__ __forceinline__ void zero_T_upper(const SolveSmem &s, int first, int 
 // T = (I + L)^{-1} (L strictly lower, 64 x 64) in fp32 by recursive doubling on
 // 16 x 16 blocks, by 256 threads (tid 0..255) that meet on named barrier
 // `bar`: the four diagonal blocks by forward substitution (one column per
-// thread, tid 0..63; the other threads call `idle` meanwhile); the 32 x 32
+// thread, tid 0..63, column-oriented over 4-wide column blocks so that the
+// dependent chain is short; the other threads call `idle` meanwhile); the 32 x 32
 // halves by T_BA = -T_BB (L_BA T_AA); the whole by the same identity on the
 // halves.  Threads idle in a product convert finished blocks to the fp16 tiles
 // meanwhile.  With zero_upper, threads 128..255 re-zero the upper blocks of
@@ -278,23 +280,24 @@ __device__ __forceinline__ void solve_T(const SolveSmem &s, const ChunkVecs &V, 
   float *Tf = s.Tf;
   float *P = s.P;
   if (tid < kC) {
+    // x = (I + L_bb)^{-1} e_c: once x_j .. x_j+3 are final, their terms
+    // leave every later row at once.
     const int base = 16 * (tid >> 4), c = tid & 15;
     const float *Lb = L + base * kLs + base;
     float xv[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) xv[i] = (i == c) ? 1.f : 0.f;
 #pragma unroll
-    for (int i = 1; i < 16; ++i) {
-      float a0 = 0.f, a1 = 0.f;
+    for (int j = 0; j < 16; j += 4) {
+      const float4 l1 = ld4(Lb + (j + 1) * kLs + j), l2 = ld4(Lb + (j + 2) * kLs + j), l3 = ld4(Lb + (j + 3) * kLs + j);
+      xv[j + 1] = fmaf(-l1.x, xv[j], xv[j + 1]);
+      xv[j + 2] = fmaf(-l2.y, xv[j + 1], fmaf(-l2.x, xv[j], xv[j + 2]));
+      xv[j + 3] = fmaf(-l3.z, xv[j + 2], fmaf(-l3.y, xv[j + 1], fmaf(-l3.x, xv[j], xv[j + 3])));
 #pragma unroll
-      for (int j4 = 0; j4 < i; j4 += 4) {
-        const float4 l = ld4(Lb + i * kLs + j4);
-        a0 = fmaf(l.x, xv[j4], a0);
-        if (j4 + 1 < i) a1 = fmaf(l.y, xv[j4 + 1], a1);
-        if (j4 + 2 < i) a0 = fmaf(l.z, xv[j4 + 2], a0);
-        if (j4 + 3 < i) a1 = fmaf(l.w, xv[j4 + 3], a1);
+      for (int i = j + 4; i < 16; ++i) {
+        const float4 l = ld4(Lb + i * kLs + j);
+        xv[i] -= fmaf(l.w, xv[j + 3], fmaf(l.z, xv[j + 2], fmaf(l.y, xv[j + 1], l.x * xv[j])));
       }
-      xv[i] -= a0 + a1;
     }
 #pragma unroll
     for (int i = 0; i < 16; ++i) Tf[tfi(base + i, base + c)] = xv[i];
@@ -346,8 +349,9 @@ __device__ __forceinline__ void solve_T(const SolveSmem &s, const ChunkVecs &V, 
   if (tid < 128) {
     const float *La = L + (32 + r16b) * kLs, *Lb = L + (48 + r16b) * kLs;
     float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
-#pragma unroll 2
-    for (int k4 = col >= 16 ? 16 : 0; k4 < 32; k4 += 4) {  // T[0:16][16:32] is zero
+#pragma unroll
+    for (int k4 = 0; k4 < 32; k4 += 4) {
+      if (k4 < 16 && col >= 16) continue;  // T[0:16][16:32] is zero
       const float4 la = ld4(La + k4), lb = ld4(Lb + k4);
       const float4 t0 = ld4(Tf + tfi(k4 + 0, col)), t1 = ld4(Tf + tfi(k4 + 1, col));
       const float4 t2 = ld4(Tf + tfi(k4 + 2, col)), t3 = ld4(Tf + tfi(k4 + 3, col));
@@ -372,7 +376,7 @@ __device__ __forceinline__ void solve_T(const SolveSmem &s, const ChunkVecs &V, 
   if (tid < 128) {  // rows 32 + r (16 terms) and 48 + r (32 terms); T[32:48][48:64] is zero
     const int ra = 32 + r16b, rb = 48 + r16b;
     float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
-#pragma unroll 2
+#pragma unroll
     for (int k4 = 0; k4 < 16; k4 += 4) {
       const float4 ta = ld4(Tf + tfi(ra, 32 + k4)), tb = ld4(Tf + tfi(rb, 32 + k4));
       const float4 p0 = ld4(P + (k4 + 0) * 32 + col), p1 = ld4(P + (k4 + 1) * 32 + col);
@@ -386,7 +390,7 @@ __device__ __forceinline__ void solve_T(const SolveSmem &s, const ChunkVecs &V, 
       fma4(acc0, ta.w, p3);
       fma4(acc1, tb.w, p3);
     }
-#pragma unroll 2
+#pragma unroll
     for (int k4 = 16; k4 < 32; k4 += 4) {
       const float4 tb = ld4(Tf + tfi(rb, 32 + k4));
       fma4(acc1, tb.x, ld4(P + (k4 + 0) * 32 + col));

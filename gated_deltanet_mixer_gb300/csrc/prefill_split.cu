@@ -174,7 +174,9 @@ __device__ __forceinline__ bool group_sync_or(const PrepGroup &G, bool p) {
   return named_sync_or(G.bar, kPrepThreads, p);
 }
 // Release of an item's flag: its stores (TMA and plain) are complete and
-// visible at GPU scope before the flag is.
+// visible at GPU scope before the flag is.  The plain stores of the group's
+// other threads precede it through the group barriers they passed, which the
+// release (cumulative) covers.
 __device__ __forceinline__ void st_release_gpu(int *p, int v) {
   asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -497,8 +499,9 @@ __device__ __forceinline__ void prep_role(const PrefillArgs &a, const SplitArgs 
     }
     if (tid < 2 * kC) {  // the chunk vectors d and Gamma, fp32 [2][64]
       float *vec = s.ws_vec + item * (2 * kC);
+      // (ordered before the item's flag by the group barriers that precede
+      // the store thread's release; no fence of its own)
       if (in_bounds(item * (2 * kC) + tid + 1, nitems * (2 * kC), a.err)) vec[tid] = tid < kC ? CV.d[tid] : CV.gam[tid - kC];
-      if (G.flags) __threadfence();  // ordered before the item's flag
     }
     if (warp == kGateWarp && more) {  // the next item's chunk vectors; the gates of the one after it
       form_vectors(cn, V.cv[(k + 1) & 1]);
