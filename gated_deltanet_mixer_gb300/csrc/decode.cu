@@ -56,15 +56,6 @@ __device__ __forceinline__ float conv_token(const IO *win, const IO *x, const IO
   return silu(acc);
 }
 
-// s . k for one state row, on the paired fp32 pipes: (x, y) and (z, w) lanes
-// in parallel, then one add.  Used by the T-token kernel, whose serial token
-// steps are arithmetic-bound; the single-token kernel, bound by the state
-// stream, measured faster with the scalar form.
-__device__ __forceinline__ float dot4p(float4 s, float4 k) {
-  const float2 acc = __ffma2_rn(make_float2(s.x, s.y), make_float2(k.x, k.y),
-                                __fmul2_rn(make_float2(s.z, s.w), make_float2(k.z, k.w)));
-  return acc.x + acc.y;
-}
 // alpha s + di k for one state row (fmaf(alpha, s, di * k) per element), paired.
 __device__ __forceinline__ float4 decay_update(float4 s, float alpha, float di, float4 k) {
   const float2 n01 = __ffma2_rn(make_float2(alpha, alpha), make_float2(s.x, s.y),
@@ -194,36 +185,54 @@ __global__ void __launch_bounds__(kThreads, 2) decode1_kernel(DecodeArgs a) {
 }
 
 // The T-token kernel's shared memory: the next unit's state (filled by bulk
-// copies while the current unit is computed from registers) and the current
-// unit's token vectors.
+// copies while the current unit is computed from registers), the current
+// unit's token vectors, and (bf16 io) the raw inputs of the unit whose turn
+// is next, also by bulk copy: its new rows' and window's q, k, v channels,
+// their conv weights and its z rows.
 struct DecodeSmem {
   float S[kD * kD];  // 64 KB
-  float q[kDecodeMaxT][kD], k[kDecodeMaxT][kD], v[kDecodeMaxT][kD], o[kDecodeMaxT][kD], z[kDecodeMaxT][kD];
+  // q^, k^ and v of each token; o is written over v (each warp over its own rows)
+  float q[kDecodeMaxT][kD], k[kDecodeMaxT][kD], v[kDecodeMaxT][kD];
   float kq[kDecodeMaxT], g[kDecodeMaxT], b[kDecodeMaxT];
-  uint64_t bar;  // the state copy landed
+  uint16_t xr[kDecodeMaxT][3 * kD];  // raw rows: q | k | v channels (bf16 io; fp32 io keeps z here)
+  uint16_t wr[3][3 * kD];            // the carried window, same channels
+  uint16_t cwr[3 * kD * 4];          // conv weights of those channels
+  uint16_t zr[kDecodeMaxT][kD];      // z rows
+  uint64_t bar;     // the state copy landed
+  uint64_t bar_in;  // raw rows, window and conv weights landed
+  uint64_t bar_z;   // z rows landed
   int stop;
 };
 constexpr uint32_t kStateBytes = kD * kD * 4;
 constexpr size_t kDecodeSmem = sizeof(DecodeSmem) + 128;  // + alignment slack
-static_assert(offsetof(DecodeSmem, S) == 0 && offsetof(DecodeSmem, q) % 16 == 0 && offsetof(DecodeSmem, bar) % 8 == 0,
+static_assert(offsetof(DecodeSmem, S) == 0 && offsetof(DecodeSmem, q) % 16 == 0 && offsetof(DecodeSmem, xr) % 16 == 0 &&
+                  offsetof(DecodeSmem, wr) % 16 == 0 && offsetof(DecodeSmem, cwr) % 16 == 0 &&
+                  offsetof(DecodeSmem, zr) % 16 == 0 && offsetof(DecodeSmem, bar) % 8 == 0,
               "layout");
+static_assert(sizeof(float) * kDecodeMaxT * kD <= sizeof(uint16_t) * kDecodeMaxT * 3 * kD, "fp32 z fits the raw rows");
+static_assert(2 * (kDecodeSmem + 1024) <= 233472, "two CTAs per SM");
 
+__device__ __forceinline__ void bulk_copy(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   umma::smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(umma::smem_u32(bar))
+               : "memory");
+}
 __device__ __forceinline__ void bulk_load_state(DecodeSmem &M, const float *src) {
   umma::bar_expect_tx(&M.bar, kStateBytes);
 #pragma unroll
-  for (int p = 0; p < 4; ++p)
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     umma::smem_u32(M.S + p * (kD * kD / 4))),
-                 "l"(src + p * (kD * kD / 4)), "r"(kStateBytes / 4), "r"(umma::smem_u32(&M.bar))
-                 : "memory");
+  for (int p = 0; p < 4; ++p) bulk_copy(M.S + p * (kD * kD / 4), src + p * (kD * kD / 4), kStateBytes / 4, &M.bar);
 }
 
 // Persistent: CTA c takes the (sequence, value head) units c, c + grid, ...
 // While a unit's T token steps run on its state in registers, the bulk copy
 // of the CTA's next unit's state lands in shared memory, so that the state
-// stream does not stop for the serial token steps.  Two CTAs per SM.
+// stream does not stop for the serial token steps; with bf16 io the next
+// unit's raw inputs arrive the same way, and its gates in registers.  Two
+// CTAs per SM.
 template <typename IO, bool kRawGates>
 __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
+  constexpr bool kPre = sizeof(IO) == 2;  // inputs by bulk copy (bf16 io)
   extern __shared__ uint8_t decode_smem_raw[];
   DecodeSmem &M = *reinterpret_cast<DecodeSmem *>(decode_smem_raw + ((128 - (umma::smem_u32(decode_smem_raw) & 127)) & 127));
   const Dims d = a.d;
@@ -234,60 +243,151 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
   const long long C = d.C;
   const IO *cw = static_cast<const IO *>(a.conv_w);
   const int row0 = warp * kRowsPerWarp;
+  // fp32 io: the z rows as fp32, in the raw rows' space
+  float(*zf)[kD] = reinterpret_cast<float(*)[kD]>(&M.xr[0][0]);
 
   if (tid == 0) {
     umma::bar_init(&M.bar, 1);
+    umma::bar_init(&M.bar_in, 1);
+    umma::bar_init(&M.bar_z, 1);
     M.stop = 0;
   }
   umma::fence_smem_to_async();
   __syncthreads();
+
+  // The first channel of each of a unit's three channel blocks (q, k of its
+  // key head; v of its head).
+  auto chan0 = [&](int h, int seg) -> long long {
+    return seg == 0 ? (long long)(h / r) * kD : seg == 1 ? (long long)(d.Hk + h / r) * kD : (long long)(2 * d.Hk + h) * kD;
+  };
+  // One warp: unit u's raw rows, window and conv weights (bf16 io).
+  auto request_inputs = [&](int u) {
+    const int ub = u / d.Hv, uh = u % d.Hv;
+    if (lane == 0) umma::bar_expect_tx(&M.bar_in, (uint32_t)(3 * T + 9) * (kD * 2) + 3 * (kD * 8));
+    __syncwarp();
+    const IO *x = static_cast<const IO *>(a.qkv_pre) + (long long)ub * T * C;
+    const IO *win = static_cast<const IO *>(a.conv_in) + (long long)ub * 3 * C;
+    for (int i = lane; i < 3 * T + 12; i += 32) {
+      if (i < 3 * T) {
+        const int t = i / 3, seg = i % 3;
+        bulk_copy(&M.xr[t][seg * kD], x + (long long)t * C + chan0(uh, seg), kD * 2, &M.bar_in);
+      } else if (i < 3 * T + 9) {
+        const int e = (i - 3 * T) / 3, seg = (i - 3 * T) % 3;
+        bulk_copy(&M.wr[e][seg * kD], win + (long long)e * C + chan0(uh, seg), kD * 2, &M.bar_in);
+      } else {
+        const int seg = i - 3 * T - 9;
+        bulk_copy(&M.cwr[seg * kD * 4], cw + 4 * chan0(uh, seg), kD * 8, &M.bar_in);
+      }
+    }
+  };
+  // One warp: unit u's z rows (bf16 io).
+  auto request_z = [&](int u) {
+    const int ub = u / d.Hv, uh = u % d.Hv;
+    if (lane == 0) umma::bar_expect_tx(&M.bar_z, (uint32_t)T * (kD * 2));
+    __syncwarp();
+    if (lane < T)
+      bulk_copy(&M.zr[lane][0], static_cast<const IO *>(a.z) + (((long long)ub * T + lane) * d.Hv + uh) * kD, kD * 2,
+                &M.bar_z);
+  };
+  // Threads t < T: unit u's gates of token t.
+  auto gates = [&](int u, float &gt, float &bt) {
+    const int ub = u / d.Hv, uh = u % d.Hv;
+    const long long i = ((long long)ub * T + tid) * d.Hv + uh;
+    if (kRawGates) {
+      gate_at<IO>(a.gate, i, uh, gt, bt);
+    } else {
+      gt = a.gate.g[i];
+      bt = a.gate.beta[i];
+    }
+  };
+  // Thread 0: a bounded wait; after a timeout the CTA stops at the next
+  // barrier (a second bounded wait first: no copy may land after the CTA ends).
+  auto wait_or_stop = [&](uint64_t *bar, uint32_t ph) {
+    if (!umma::bar_wait(bar, ph)) {
+      atomicOr(a.err, kErrTimeout);
+      umma::bar_wait(bar, ph);
+      M.stop = 1;
+    }
+  };
+
   int unit = blockIdx.x;
-  uint32_t phase = 0;
-  bool pending = false;  // thread 0: a state copy is in flight
-  if (tid == 0 && unit < nunits) {
-    bulk_load_state(M, a.S + (long long)unit * (kD * kD));
-    pending = true;
+  uint32_t phase = 0, ph_in = 0, ph_z = 0;
+  bool pending = false, pending_in = false, pending_z = false;  // copies in flight (thread 0's view)
+  float ng = 0.f, nb = 0.f;  // threads t < T: the gates of the CTA's next unit (bf16 io)
+  if (unit < nunits) {
+    if (tid == 0) {
+      bulk_load_state(M, a.S + (long long)unit * (kD * kD));
+      pending = true;
+    }
+    if (kPre) {
+      if (warp == 0) {
+        request_inputs(unit);
+        request_z(unit);
+      }
+      pending_in = pending_z = true;
+      if (tid < T) gates(unit, ng, nb);
+      if (tid == 0) {
+        wait_or_stop(&M.bar_in, ph_in);
+        pending_in = false;
+      }
+      ph_in ^= 1u;
+      if (tid < T) {
+        M.g[tid] = ng;
+        M.b[tid] = nb;
+      }
+      __syncthreads();
+    }
   }
-  for (; unit < nunits; unit += gridDim.x) {
+  for (; unit < nunits && !M.stop; unit += gridDim.x) {
     const int b = unit / d.Hv, h = unit % d.Hv, kh = h / r;
+    const int next = unit + (int)gridDim.x;
     const IO *x = static_cast<const IO *>(a.qkv_pre) + (long long)b * T * C;
     const IO *win = static_cast<const IO *>(a.conv_in) + (long long)b * 3 * C;
     IO *wout = static_cast<IO *>(a.conv_out) + (long long)b * 3 * C;
 
-    // The gates of every token and the z rows of the gated norm.
-    if (tid < T) {
-      const long long i = ((long long)b * T + tid) * d.Hv + h;
-      float gt, bt;
-      if (kRawGates) {
-        gate_at<IO>(a.gate, i, h, gt, bt);
-      } else {
-        gt = a.gate.g[i];
-        bt = a.gate.beta[i];
+    if (!kPre) {  // the gates of every token and the z rows of the gated norm
+      if (tid < T) gates(unit, M.g[tid], M.b[tid]);
+      for (int e = tid; e < T * (kD / 4); e += kThreads) {  // four channels per load
+        const int t = e / (kD / 4), c = 4 * (e % (kD / 4));
+        reinterpret_cast<float4 *>(zf[t])[c / 4] =
+            ld_io4(static_cast<const IO *>(a.z) + (((long long)b * T + t) * d.Hv + h) * kD + c);
       }
-      M.g[tid] = gt;
-      M.b[tid] = bt;
-    }
-    for (int e = tid; e < T * (kD / 4); e += kThreads) {  // four channels per load
-      const int t = e / (kD / 4), c = 4 * (e % (kD / 4));
-      reinterpret_cast<float4 *>(M.z[t])[c / 4] =
-          ld_io4(static_cast<const IO *>(a.z) + (((long long)b * T + t) * d.Hv + h) * kD + c);
     }
 
     // ---- front end: conv + SiLU of the T tokens, sliding the window of the
-    // channel(s) this thread owns (q and k of key head kh, or v of head h)
+    // channel(s) this thread owns (q and k of key head kh, or v of head h);
+    // with bf16 io from the raw rows in shared memory
     {
       const bool qk = tid < kD;
+      const int j0 = qk ? tid : 2 * kD + (tid - kD);  // the channel's index in the raw rows
+      const int j1 = kD + tid;                       // k channel (qk threads)
       const long long c0 = qk ? (long long)kh * kD + tid : 2LL * d.Hk * kD + (long long)h * kD + (tid - kD);
-      const long long c1 = (long long)d.Hk * kD + (long long)kh * kD + tid;  // k channel (qk threads)
-      float w0[3] = {ld_io(win + c0), ld_io(win + C + c0), ld_io(win + 2 * C + c0)};
-      float w1[3] = {0.f, 0.f, 0.f};
-      const float4 t0 = ld_io4(cw + 4 * c0);
-      float4 t1 = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (qk) {
-        w1[0] = ld_io(win + c1);
-        w1[1] = ld_io(win + C + c1);
-        w1[2] = ld_io(win + 2 * C + c1);
-        t1 = ld_io4(cw + 4 * c1);
+      const long long c1 = (long long)d.Hk * kD + (long long)kh * kD + tid;
+      auto raw = [&](const uint16_t *p) { return __uint_as_float((uint32_t)*p << 16); };  // bf16 bits -> fp32
+      float w0[3], w1[3] = {0.f, 0.f, 0.f};
+      float4 t0, t1 = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (kPre) {
+        const uint2 u0 = *reinterpret_cast<const uint2 *>(&M.cwr[4 * j0]);
+        t0 = make_float4(__uint_as_float(u0.x << 16), __uint_as_float(u0.x & 0xffff0000u), __uint_as_float(u0.y << 16),
+                         __uint_as_float(u0.y & 0xffff0000u));
+#pragma unroll
+        for (int e = 0; e < 3; ++e) w0[e] = raw(&M.wr[e][j0]);
+        if (qk) {
+          const uint2 u1 = *reinterpret_cast<const uint2 *>(&M.cwr[4 * j1]);
+          t1 = make_float4(__uint_as_float(u1.x << 16), __uint_as_float(u1.x & 0xffff0000u),
+                           __uint_as_float(u1.y << 16), __uint_as_float(u1.y & 0xffff0000u));
+#pragma unroll
+          for (int e = 0; e < 3; ++e) w1[e] = raw(&M.wr[e][j1]);
+        }
+      } else {
+        t0 = ld_io4(cw + 4 * c0);
+#pragma unroll
+        for (int e = 0; e < 3; ++e) w0[e] = ld_io(win + e * C + c0);
+        if (qk) {
+          t1 = ld_io4(cw + 4 * c1);
+#pragma unroll
+          for (int e = 0; e < 3; ++e) w1[e] = ld_io(win + e * C + c1);
+        }
       }
       // Tokens in batches of 8: the batch's loads are all issued before the
       // first is used, so the T tokens cost about T / 8 load latencies.
@@ -296,8 +396,13 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           const bool in = tb + u < T;
-          xa[u] = in ? ld_io(x + (long long)(tb + u) * C + c0) : 0.f;
-          xb[u] = (in && qk) ? ld_io(x + (long long)(tb + u) * C + c1) : 0.f;
+          if (kPre) {
+            xa[u] = in ? raw(&M.xr[tb + u][j0]) : 0.f;
+            xb[u] = (in && qk) ? raw(&M.xr[tb + u][j1]) : 0.f;
+          } else {
+            xa[u] = in ? ld_io(x + (long long)(tb + u) * C + c0) : 0.f;
+            xb[u] = (in && qk) ? ld_io(x + (long long)(tb + u) * C + c1) : 0.f;
+          }
         }
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
@@ -335,6 +440,13 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
       }
     }
     __syncthreads();
+    // The raw rows are read: the next unit's may land (and its gates arrive).
+    // The last warp issues the copies: it has no token's norm below when T < 8.
+    if (kPre && next < nunits) {
+      if (warp == kWarps - 1) request_inputs(next);
+      pending_in = true;
+      if (tid < T) gates(next, ng, nb);
+    }
     // ---- L2 norms of q and k, and k^ . q^, one warp per token
     for (int t = warp; t < T; t += kWarps) {
       float4 q4 = reinterpret_cast<const float4 *>(M.q[t])[lane];
@@ -352,11 +464,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
     // ---- the state: this unit's copy landed; into registers (each warp its
     // 16 rows), then the buffer takes the next unit's
     if (tid == 0) {
-      if (!umma::bar_wait(&M.bar, phase)) {
-        atomicOr(a.err, kErrTimeout);
-        umma::bar_wait(&M.bar, phase);  // once more (bounded): no copy may land after the CTA ends
-        M.stop = 1;
-      }
+      wait_or_stop(&M.bar, phase);
       pending = false;
     }
     phase ^= 1u;
@@ -374,8 +482,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
 #pragma unroll
       for (int m = 0; m < 4; ++m) s[i][m] = *reinterpret_cast<const float4 *>(M.S + (rbase + i) * kD + 4 * cg + 32 * m);
     __syncthreads();
-    if (tid == 0 && unit + (int)gridDim.x < nunits) {
-      bulk_load_state(M, a.S + (long long)(unit + gridDim.x) * (kD * kD));
+    if (tid == 0 && next < nunits) {
+      bulk_load_state(M, a.S + (long long)next * (kD * kD));
       pending = true;
     }
 
@@ -421,7 +529,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
       }
       const float Sq = __shfl_down_sync(0xffffffffu, part[0], 4);  // lanes cg < 4: their row's S q^
       const float delta = beta * (M.v[t][rbase + (cg & 3)] - alpha * part[0]);
-      if (cg < 4) M.o[t][rbase + cg] = fmaf(alpha, Sq, delta * kq);
+      __syncwarp();  // every lane has read its v before o takes its place (this warp's rows only)
+      if (cg < 4) M.v[t][rbase + cg] = fmaf(alpha, Sq, delta * kq);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const float di = __shfl_sync(0xffffffffu, delta, (lane & ~7) + i);
@@ -447,16 +556,28 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
         const long long off = (long long)(rbase + i) * kD + 4 * cg + 32 * m;
         if (in_bounds(gi * (kD * kD) + off + 4, (long long)d.B * d.Hv * kD * kD, a.err)) st_stream(S + off, s[i][m]);
       }
+    if (kPre && tid == 0) {
+      wait_or_stop(&M.bar_z, ph_z);
+      pending_z = false;
+    }
+    ph_z ^= 1u;
     __syncthreads();
 
-    // ---- gated RMSNorm over the head's 128 outputs, one warp per token
+    // ---- gated RMSNorm over the head's 128 outputs (o in v's place), one warp per token
     const float4 w4 = ld_io4(static_cast<const IO *>(a.norm_w) + 4 * lane);
     for (int t = warp; t < T; t += kWarps) {
-      const float4 o4 = reinterpret_cast<const float4 *>(M.o[t])[lane];
+      const float4 o4 = reinterpret_cast<const float4 *>(M.v[t])[lane];
       const float rstd = rsqrtf(warp_sum(dot4(o4, o4)) * (1.0f / kD) + d.eps_norm);
       const long long oi = (((long long)b * T + t) * d.Hv + h) * kD + 4 * lane;  // [B][T][Hv*Dv]
       if (!in_bounds(oi + 4, (long long)d.B * T * d.Hv * kD, a.err)) continue;
-      const float4 z4 = reinterpret_cast<const float4 *>(M.z[t])[lane];
+      float4 z4;
+      if (kPre) {
+        const uint2 u = *reinterpret_cast<const uint2 *>(&M.zr[t][4 * lane]);
+        z4 = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u), __uint_as_float(u.y << 16),
+                         __uint_as_float(u.y & 0xffff0000u));
+      } else {
+        z4 = reinterpret_cast<const float4 *>(zf[t])[lane];
+      }
       float4 y;
       y.x = w4.x * (o4.x * rstd) * silu(z4.x);
       y.y = w4.y * (o4.y * rstd) * silu(z4.y);
@@ -464,11 +585,33 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
       y.w = w4.w * (o4.w * rstd) * silu(z4.w);
       st_io4(static_cast<IO *>(a.o) + oi, y);
     }
-    __syncthreads();  // the token vectors are reused by the next unit
+    // The next unit: its raw inputs landed (requested a unit ago) and its
+    // gates take the place of this unit's; after the barrier its z rows may
+    // replace these.
+    if (kPre && next < nunits) {
+      if (tid == 0) {
+        wait_or_stop(&M.bar_in, ph_in);
+        pending_in = false;
+      }
+      ph_in ^= 1u;
+      if (tid < T) {
+        M.g[tid] = ng;
+        M.b[tid] = nb;
+      }
+    }
+    __syncthreads();  // the token vectors and z rows are reused by the next unit
+    if (kPre && next < nunits) {
+      if (warp == kWarps - 1) request_z(next);
+      pending_z = true;
+    }
   }
   // No copy may still land in shared memory when the CTA ends (after a
-  // timeout: one more bounded wait).
-  if (tid == 0 && pending) umma::bar_wait(&M.bar, phase);
+  // timeout or a stop: one more bounded wait each).
+  if (tid == 0) {
+    if (pending) umma::bar_wait(&M.bar, phase);
+    if (pending_in) umma::bar_wait(&M.bar_in, ph_in);
+    if (pending_z) umma::bar_wait(&M.bar_z, ph_z);
+  }
   __syncthreads();
 }
 
