@@ -218,6 +218,14 @@ __device__ __forceinline__ void bulk_copy(void *dst, const void *src, uint32_t b
                "l"(src), "r"(bytes), "r"(umma::smem_u32(bar))
                : "memory");
 }
+// silu(x) = x / (1 + 2^(-x log2 e)) on the MUFU ex2 and rcp approximations
+// (relative error about 1e-6; the inputs and outputs are bf16 here).
+__device__ __forceinline__ float silu_mufu(float x) {
+  float e, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x * -1.4426950408889634f));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
+  return x * r;
+}
 __device__ __forceinline__ void bulk_load_state(DecodeSmem &M, const float *src) {
   umma::bar_expect_tx(&M.bar, kStateBytes);
 #pragma unroll
@@ -260,14 +268,19 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
   auto chan0 = [&](int h, int seg) -> long long {
     return seg == 0 ? (long long)(h / r) * kD : seg == 1 ? (long long)(d.Hk + h / r) * kD : (long long)(2 * d.Hk + h) * kD;
   };
-  // One warp: unit u's raw rows, window and conv weights (bf16 io).
+  // bf16 io.  Thread 0 announces a unit's copies on their barrier before a
+  // block barrier; after it the copies are issued one per thread (a warp
+  // issues its lanes' copies one after another, so they are spread over
+  // warps): unit u's raw rows, window and conv weights by the warps that have
+  // no token's L2 norm (warps min(T, 7) .. 7), its z rows by all warps.
+  const uint32_t in_bytes = (uint32_t)(3 * T + 9) * (kD * 2) + 3 * (kD * 8), z_bytes = (uint32_t)T * (kD * 2);
+  const int cw0 = T < kWarps - 1 ? T : kWarps - 1, ncw = kWarps - cw0;  // the warps issuing the input copies
   auto request_inputs = [&](int u) {
+    if (warp < cw0) return;
     const int ub = u / d.Hv, uh = u % d.Hv;
-    if (lane == 0) umma::bar_expect_tx(&M.bar_in, (uint32_t)(3 * T + 9) * (kD * 2) + 3 * (kD * 8));
-    __syncwarp();
     const IO *x = static_cast<const IO *>(a.qkv_pre) + (long long)ub * T * C;
     const IO *win = static_cast<const IO *>(a.conv_in) + (long long)ub * 3 * C;
-    for (int i = lane; i < 3 * T + 12; i += 32) {
+    for (int i = (warp - cw0) + ncw * lane; i < 3 * T + 12; i += ncw * 32) {
       if (i < 3 * T) {
         const int t = i / 3, seg = i % 3;
         bulk_copy(&M.xr[t][seg * kD], x + (long long)t * C + chan0(uh, seg), kD * 2, &M.bar_in);
@@ -280,14 +293,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
       }
     }
   };
-  // One warp: unit u's z rows (bf16 io).
   auto request_z = [&](int u) {
-    const int ub = u / d.Hv, uh = u % d.Hv;
-    if (lane == 0) umma::bar_expect_tx(&M.bar_z, (uint32_t)T * (kD * 2));
-    __syncwarp();
-    if (lane < T)
-      bulk_copy(&M.zr[lane][0], static_cast<const IO *>(a.z) + (((long long)ub * T + lane) * d.Hv + uh) * kD, kD * 2,
-                &M.bar_z);
+    const int ub = u / d.Hv, uh = u % d.Hv, t = warp + kWarps * lane;
+    if (t < T)
+      bulk_copy(&M.zr[t][0], static_cast<const IO *>(a.z) + (((long long)ub * T + t) * d.Hv + uh) * kD, kD * 2, &M.bar_z);
   };
   // Threads t < T: unit u's gates of token t.
   auto gates = [&](int u, float &gt, float &bt) {
@@ -320,10 +329,13 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
       pending = true;
     }
     if (kPre) {
-      if (warp == 0) {
-        request_inputs(unit);
-        request_z(unit);
+      if (tid == 0) {
+        umma::bar_expect_tx(&M.bar_in, in_bytes);
+        umma::bar_expect_tx(&M.bar_z, z_bytes);
       }
+      __syncthreads();
+      request_inputs(unit);
+      request_z(unit);
       pending_in = pending_z = true;
       if (tid < T) gates(unit, ng, nb);
       if (tid == 0) {
@@ -414,15 +426,15 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
           w0[1] = w0[2];
           w0[2] = x0;
           if (qk) {
-            M.q[t][tid] = silu(acc);
+            M.q[t][tid] = silu_mufu(acc);
             const float x1 = xb[u];
             const float acc1 = fmaf(t1.w, x1, fmaf(t1.z, w1[2], fmaf(t1.y, w1[1], t1.x * w1[0])));
             w1[0] = w1[1];
             w1[1] = w1[2];
             w1[2] = x1;
-            M.k[t][tid] = silu(acc1);
+            M.k[t][tid] = silu_mufu(acc1);
           } else {
-            M.v[t][tid - kD] = silu(acc);
+            M.v[t][tid - kD] = silu_mufu(acc);
           }
         }
       }
@@ -439,11 +451,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
         }
       }
     }
+    if (kPre && tid == 0 && next < nunits) umma::bar_expect_tx(&M.bar_in, in_bytes);
     __syncthreads();
     // The raw rows are read: the next unit's may land (and its gates arrive).
-    // The last warp issues the copies: it has no token's norm below when T < 8.
     if (kPre && next < nunits) {
-      if (warp == kWarps - 1) request_inputs(next);
+      request_inputs(next);
       pending_in = true;
       if (tid < T) gates(next, ng, nb);
     }
@@ -579,10 +591,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
         z4 = reinterpret_cast<const float4 *>(zf[t])[lane];
       }
       float4 y;
-      y.x = w4.x * (o4.x * rstd) * silu(z4.x);
-      y.y = w4.y * (o4.y * rstd) * silu(z4.y);
-      y.z = w4.z * (o4.z * rstd) * silu(z4.z);
-      y.w = w4.w * (o4.w * rstd) * silu(z4.w);
+      y.x = w4.x * (o4.x * rstd) * silu_mufu(z4.x);
+      y.y = w4.y * (o4.y * rstd) * silu_mufu(z4.y);
+      y.z = w4.z * (o4.z * rstd) * silu_mufu(z4.z);
+      y.w = w4.w * (o4.w * rstd) * silu_mufu(z4.w);
       st_io4(static_cast<IO *>(a.o) + oi, y);
     }
     // The next unit: its raw inputs landed (requested a unit ago) and its
@@ -598,10 +610,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
         M.g[tid] = ng;
         M.b[tid] = nb;
       }
+      if (tid == 0) umma::bar_expect_tx(&M.bar_z, z_bytes);
     }
     __syncthreads();  // the token vectors and z rows are reused by the next unit
     if (kPre && next < nunits) {
-      if (warp == kWarps - 1) request_z(next);
+      request_z(next);
       pending_z = true;
     }
   }
