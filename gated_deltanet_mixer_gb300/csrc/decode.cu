@@ -25,6 +25,7 @@
 
 #include "gdn_device.cuh"
 #include "launch.h"
+#include "tma_host.h"
 #include "umma.cuh"
 
 namespace gdn {
@@ -187,17 +188,17 @@ __global__ void __launch_bounds__(kThreads, 2) decode1_kernel(DecodeArgs a) {
 // The T-token kernel's shared memory: the next unit's state (filled by bulk
 // copies while the current unit is computed from registers), the current
 // unit's token vectors, and (bf16 io) the raw inputs of the unit whose turn
-// is next, also by bulk copy: its new rows' and window's q, k, v channels,
-// their conv weights and its z rows.
+// is next, also by asynchronous copy: its new rows' and window's q, k, v
+// channel blocks (one TMA box each), their conv weights and its z rows.
 struct DecodeSmem {
   float S[kD * kD];  // 64 KB
   // q^, k^ and v of each token; o is written over v (each warp over its own rows)
   float q[kDecodeMaxT][kD], k[kDecodeMaxT][kD], v[kDecodeMaxT][kD];
   float kq[kDecodeMaxT], g[kDecodeMaxT], b[kDecodeMaxT];
-  uint16_t xr[kDecodeMaxT][3 * kD];  // raw rows: q | k | v channels (bf16 io; fp32 io keeps z here)
-  uint16_t wr[3][3 * kD];            // the carried window, same channels
-  uint16_t cwr[3 * kD * 4];          // conv weights of those channels
-  uint16_t zr[kDecodeMaxT][kD];      // z rows
+  alignas(128) uint16_t xr[3][kDecodeMaxT][kD];  // raw rows of the q, k, v blocks (bf16 io; fp32 io keeps z here)
+  alignas(128) uint16_t wr[3][3][kD];            // the carried window, same blocks
+  alignas(128) uint16_t cwr[3 * kD * 4];         // conv weights of those channels
+  alignas(128) uint16_t zr[kDecodeMaxT][kD];     // z rows
   uint64_t bar;     // the state copy landed
   uint64_t bar_in;  // raw rows, window and conv weights landed
   uint64_t bar_z;   // z rows landed
@@ -205,11 +206,11 @@ struct DecodeSmem {
 };
 constexpr uint32_t kStateBytes = kD * kD * 4;
 constexpr size_t kDecodeSmem = sizeof(DecodeSmem) + 128;  // + alignment slack
-static_assert(offsetof(DecodeSmem, S) == 0 && offsetof(DecodeSmem, q) % 16 == 0 && offsetof(DecodeSmem, xr) % 16 == 0 &&
-                  offsetof(DecodeSmem, wr) % 16 == 0 && offsetof(DecodeSmem, cwr) % 16 == 0 &&
-                  offsetof(DecodeSmem, zr) % 16 == 0 && offsetof(DecodeSmem, bar) % 8 == 0,
-              "layout");
-static_assert(sizeof(float) * kDecodeMaxT * kD <= sizeof(uint16_t) * kDecodeMaxT * 3 * kD, "fp32 z fits the raw rows");
+static_assert(offsetof(DecodeSmem, S) == 0 && offsetof(DecodeSmem, q) % 16 == 0 && offsetof(DecodeSmem, xr) % 128 == 0 &&
+                  offsetof(DecodeSmem, wr) % 128 == 0 && offsetof(DecodeSmem, cwr) % 128 == 0 &&
+                  offsetof(DecodeSmem, zr) % 128 == 0 && offsetof(DecodeSmem, bar) % 8 == 0,
+              "layout (TMA destinations 128-byte aligned)");
+static_assert(sizeof(float) * kDecodeMaxT * kD <= sizeof(uint16_t) * 3 * kDecodeMaxT * kD, "fp32 z fits the raw rows");
 static_assert(2 * (kDecodeSmem + 1024) <= 233472, "two CTAs per SM");
 
 __device__ __forceinline__ void bulk_copy(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
@@ -238,8 +239,14 @@ __device__ __forceinline__ void bulk_load_state(DecodeSmem &M, const float *src)
 // stream does not stop for the serial token steps; with bf16 io the next
 // unit's raw inputs arrive the same way, and its gates in registers.  Two
 // CTAs per SM.
+//
+// The tensor maps (bf16 io): tm_x over qkv_pre as rows of C (box 128 x T),
+// tm_w over the carried windows as rows of C (box 128 x 3), tm_z over z as
+// rows of Hv*128 (box 128 x T).  Unused (and not encoded) for fp32 io.
 template <typename IO, bool kRawGates>
-__global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap tm_x,
+                                                             const __grid_constant__ CUtensorMap tm_w,
+                                                             const __grid_constant__ CUtensorMap tm_z) {
   constexpr bool kPre = sizeof(IO) == 2;  // inputs by bulk copy (bf16 io)
   extern __shared__ uint8_t decode_smem_raw[];
   DecodeSmem &M = *reinterpret_cast<DecodeSmem *>(decode_smem_raw + ((128 - (umma::smem_u32(decode_smem_raw) & 127)) & 127));
@@ -269,34 +276,29 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
     return seg == 0 ? (long long)(h / r) * kD : seg == 1 ? (long long)(d.Hk + h / r) * kD : (long long)(2 * d.Hk + h) * kD;
   };
   // bf16 io.  Thread 0 announces a unit's copies on their barrier before a
-  // block barrier; after it the copies are issued one per thread (a warp
-  // issues its lanes' copies one after another, so they are spread over
-  // warps): unit u's raw rows, window and conv weights by the warps that have
-  // no token's L2 norm (warps min(T, 7) .. 7), its z rows by all warps.
+  // block barrier; after it the copies are issued (a warp issues its lanes'
+  // copies one after another, so they are spread over warps): unit u's nine
+  // (raw rows and window of each channel block by TMA, conv weights by bulk
+  // copy) by the warps that have no token's L2 norm (warps min(T, 7) .. 7),
+  // its z rows (one TMA box) by the last warp.
   const uint32_t in_bytes = (uint32_t)(3 * T + 9) * (kD * 2) + 3 * (kD * 8), z_bytes = (uint32_t)T * (kD * 2);
   const int cw0 = T < kWarps - 1 ? T : kWarps - 1, ncw = kWarps - cw0;  // the warps issuing the input copies
   auto request_inputs = [&](int u) {
     if (warp < cw0) return;
     const int ub = u / d.Hv, uh = u % d.Hv;
-    const IO *x = static_cast<const IO *>(a.qkv_pre) + (long long)ub * T * C;
-    const IO *win = static_cast<const IO *>(a.conv_in) + (long long)ub * 3 * C;
-    for (int i = (warp - cw0) + ncw * lane; i < 3 * T + 12; i += ncw * 32) {
-      if (i < 3 * T) {
-        const int t = i / 3, seg = i % 3;
-        bulk_copy(&M.xr[t][seg * kD], x + (long long)t * C + chan0(uh, seg), kD * 2, &M.bar_in);
-      } else if (i < 3 * T + 9) {
-        const int e = (i - 3 * T) / 3, seg = (i - 3 * T) % 3;
-        bulk_copy(&M.wr[e][seg * kD], win + (long long)e * C + chan0(uh, seg), kD * 2, &M.bar_in);
-      } else {
-        const int seg = i - 3 * T - 9;
+    for (int i = (warp - cw0) + ncw * lane; i < 9; i += ncw * 32) {
+      const int seg = i % 3;
+      if (i < 3)
+        umma::tma_load_3d(umma::smem_u32(&M.xr[seg][0][0]), &tm_x, (int)chan0(uh, seg), ub * T, 0, &M.bar_in);
+      else if (i < 6)
+        umma::tma_load_3d(umma::smem_u32(&M.wr[seg][0][0]), &tm_w, (int)chan0(uh, seg), ub * 3, 0, &M.bar_in);
+      else
         bulk_copy(&M.cwr[seg * kD * 4], cw + 4 * chan0(uh, seg), kD * 8, &M.bar_in);
-      }
     }
   };
   auto request_z = [&](int u) {
-    const int ub = u / d.Hv, uh = u % d.Hv, t = warp + kWarps * lane;
-    if (t < T)
-      bulk_copy(&M.zr[t][0], static_cast<const IO *>(a.z) + (((long long)ub * T + t) * d.Hv + uh) * kD, kD * 2, &M.bar_z);
+    if (warp == kWarps - 1 && lane == 0)
+      umma::tma_load_3d(umma::smem_u32(&M.zr[0][0]), &tm_z, (u % d.Hv) * kD, (u / d.Hv) * T, 0, &M.bar_z);
   };
   // Threads t < T: unit u's gates of token t.
   auto gates = [&](int u, float &gt, float &bt) {
@@ -371,25 +373,24 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
     // with bf16 io from the raw rows in shared memory
     {
       const bool qk = tid < kD;
-      const int j0 = qk ? tid : 2 * kD + (tid - kD);  // the channel's index in the raw rows
-      const int j1 = kD + tid;                       // k channel (qk threads)
+      const int s0 = qk ? 0 : 2, j = tid & (kD - 1);  // the channel's block and index in the raw rows (k: block 1)
       const long long c0 = qk ? (long long)kh * kD + tid : 2LL * d.Hk * kD + (long long)h * kD + (tid - kD);
       const long long c1 = (long long)d.Hk * kD + (long long)kh * kD + tid;
       auto raw = [&](const uint16_t *p) { return __uint_as_float((uint32_t)*p << 16); };  // bf16 bits -> fp32
       float w0[3], w1[3] = {0.f, 0.f, 0.f};
       float4 t0, t1 = make_float4(0.f, 0.f, 0.f, 0.f);
       if (kPre) {
-        const uint2 u0 = *reinterpret_cast<const uint2 *>(&M.cwr[4 * j0]);
+        const uint2 u0 = *reinterpret_cast<const uint2 *>(&M.cwr[4 * (s0 * kD + j)]);
         t0 = make_float4(__uint_as_float(u0.x << 16), __uint_as_float(u0.x & 0xffff0000u), __uint_as_float(u0.y << 16),
                          __uint_as_float(u0.y & 0xffff0000u));
 #pragma unroll
-        for (int e = 0; e < 3; ++e) w0[e] = raw(&M.wr[e][j0]);
+        for (int e = 0; e < 3; ++e) w0[e] = raw(&M.wr[s0][e][j]);
         if (qk) {
-          const uint2 u1 = *reinterpret_cast<const uint2 *>(&M.cwr[4 * j1]);
+          const uint2 u1 = *reinterpret_cast<const uint2 *>(&M.cwr[4 * (kD + j)]);
           t1 = make_float4(__uint_as_float(u1.x << 16), __uint_as_float(u1.x & 0xffff0000u),
                            __uint_as_float(u1.y << 16), __uint_as_float(u1.y & 0xffff0000u));
 #pragma unroll
-          for (int e = 0; e < 3; ++e) w1[e] = raw(&M.wr[e][j1]);
+          for (int e = 0; e < 3; ++e) w1[e] = raw(&M.wr[1][e][j]);
         }
       } else {
         t0 = ld_io4(cw + 4 * c0);
@@ -409,8 +410,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
         for (int u = 0; u < 8; ++u) {
           const bool in = tb + u < T;
           if (kPre) {
-            xa[u] = in ? raw(&M.xr[tb + u][j0]) : 0.f;
-            xb[u] = (in && qk) ? raw(&M.xr[tb + u][j1]) : 0.f;
+            xa[u] = in ? raw(&M.xr[s0][tb + u][j]) : 0.f;
+            xb[u] = (in && qk) ? raw(&M.xr[1][tb + u][j]) : 0.f;
           } else {
             xa[u] = in ? ld_io(x + (long long)(tb + u) * C + c0) : 0.f;
             xb[u] = (in && qk) ? ld_io(x + (long long)(tb + u) * C + c1) : 0.f;
@@ -628,6 +629,19 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
   __syncthreads();
 }
 
+// A bf16 [rows][width] tensor read in boxes of 128 columns x box_rows rows.
+bool encode_rows128(CUtensorMap *m, const void *base, long long width, long long rows, int box_rows) {
+  EncodeTiled enc = encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)rows, 1};
+  const cuuint64_t strides[2] = {(cuuint64_t)width * 2, (cuuint64_t)width * 2 * rows};
+  const cuuint32_t box[3] = {(cuuint32_t)kD, (cuuint32_t)box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 cudaError_t launch_decode(const DecodeArgs &a, bool bf16, cudaStream_t s) {
@@ -649,7 +663,14 @@ cudaError_t launch_decode(const DecodeArgs &a, bool bf16, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     const long long units = (long long)a.d.B * a.d.Hv;
     const unsigned g = (unsigned)(units < 2LL * sms ? units : 2LL * sms);  // two resident CTAs per SM
-    kern<<<g, block, kDecodeSmem, s>>>(a);
+    CUtensorMap tm_x{}, tm_w{}, tm_z{};
+    if (bf16) {
+      const long long C = a.d.C, rows = (long long)a.d.B * a.d.T;
+      if (!encode_rows128(&tm_x, a.qkv_pre, C, rows, a.d.T) || !encode_rows128(&tm_w, a.conv_in, C, 3LL * a.d.B, 3) ||
+          !encode_rows128(&tm_z, a.z, (long long)a.d.Hv * kD, rows, a.d.T))
+        return cudaErrorInvalidValue;
+    }
+    kern<<<g, block, kDecodeSmem, s>>>(a, tm_x, tm_w, tm_z);
   }
   return cudaGetLastError();
 }
