@@ -154,6 +154,32 @@ def recorded_traffic(kernel_key, source_relpaths):
     return rec.get("dram_bytes_per_launch")
 
 
+def bind_gpu_local_cpus(uuid):
+    """Run this process on the CPUs the GPU's PCI device reports as local (its
+    NUMA node), where they are among those allowed, so that the pinned host
+    buffers of the end-to-end measurement are allocated next to the GPU, as a
+    serving process would place them.  Returns the CPUs used, or None where
+    the topology is not readable (nothing is changed then)."""
+    try:
+        cmd = ["nvidia-smi", "--query-gpu=pci.bus_id", "--format=csv,noheader"] + (["-i", uuid] if uuid else [])
+        bus = subprocess.check_output(cmd, text=True, stderr=subprocess.DEVNULL).strip().splitlines()[0]
+        dom, rest = bus.split(":", 1)  # "00000009:01:00.0" -> "0009:01:00.0"
+        with open("/sys/bus/pci/devices/%04x:%s/local_cpulist" % (int(dom, 16), rest.lower())) as f:
+            text = f.read().strip()
+        local = set()
+        for part in text.split(","):
+            lo, _, hi = part.partition("-")
+            local.update(range(int(lo), int(hi or lo) + 1))
+        use = local & os.sched_getaffinity(0)
+        if not use:
+            return None
+        if use != os.sched_getaffinity(0):
+            os.sched_setaffinity(0, use)
+        return sorted(use)
+    except Exception:
+        return None
+
+
 class ClockSampler:
     """nvidia-smi clocks / throttle reasons sampled every 50 ms."""
     QUERY = ("index,uuid,utilization.gpu,clocks.sm,clocks.max.sm,power.draw,"
@@ -311,6 +337,7 @@ def gdn_arm(args, world, rank, local):
         uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
     except Exception:
         uuid = None
+    host_cpus = bind_gpu_local_cpus(uuid)
     clocks = ClockSampler(uuid)
     clocks.start()
 
@@ -445,14 +472,17 @@ def gdn_arm(args, world, rank, local):
     for k in range(2):
         e2e_step(k)
     barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(s_in)
-    for k in range(e2e_steps):
-        e2e_step(k)
-    e1.record(s_out)
-    barrier()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    e2e_ms = max_over_ranks(e2e_ms, world)
+    # three repetitions of e2e_steps steps each; the median is reported
+    e2e_reps = []
+    for _ in range(3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s_in)
+        for k in range(e2e_steps):
+            e2e_step(k)
+        e1.record(s_out)
+        barrier()
+        e2e_reps.append(max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world))
+    e2e_ms = statistics.median(e2e_reps)
 
     # ---- roofline of the prefill kernel
     pbytes = prefill_bytes(p.B, p.T, p.Hk, p.Hv, 2 if p.io == "bf16" else 4)
@@ -484,6 +514,8 @@ def gdn_arm(args, world, rank, local):
                             "peak_source": peak_src + " bf16_tflops (burst)"},
         "e2e": {"value": world * tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "ms_per_step_reps": e2e_reps, "steps_per_rep": e2e_steps,
+                "host_cpus": ("%d GPU-local CPUs" % len(host_cpus)) if host_cpus else "as scheduled",
                 "pipelined": "two buffer sets: a step's copies overlap the neighbouring steps' calls"},
         "gpu_launches": args.steps * PREFILL_KERNELS_PER_CALL,
         "clocks": clk,
