@@ -150,6 +150,7 @@ constexpr uint32_t TP_W = 192;   // -W^T [k][i]                       64
 constexpr uint32_t kPrepTmem = 256;
 constexpr int kBarSolve = 1;  // a prep group's solve barrier (the second group: 3)
 constexpr int kBarPrep = 2;   // a prep group's own barrier (the second group: 4)
+constexpr int kLoadTid = 160;   // warp 5, lane 0: a group's TMA loads
 constexpr int kStoreTid = 192;  // warp 6, lane 0: a group's workspace stores and flags
 constexpr int kGateWarp = 7;    // a group's gates and chunk vectors
 
@@ -183,11 +184,13 @@ __device__ __forceinline__ void st_release_gpu(int *p, int v) {
 __device__ __forceinline__ void fence_proxy_async_all() { asm volatile("fence.proxy.async;" ::: "memory"); }
 
 // The next item's tiles and gates are requested while the current one is
-// computed: its q^ rows once MMA1 is done with them, its raw v rows once the
-// solve is done with L (their space), its k^ rows once MMA W is done; its
-// chunk vectors are formed while MMA U / W runs.  The workspace stores (and,
-// with flags, their completion and the flag) belong to one thread of warp 6,
-// which has no part in the first step of the solve and waits there.
+// computed: its q^ rows during the solve (MMA1 is done with them), its raw v
+// rows once the solve is done with L (their space), its k^ rows once MMA W is
+// done; its chunk vectors are formed while MMA U / W runs.  The loads belong
+// to one thread of warp 5, the workspace stores (and, with flags, their
+// completion and the flag) to one of warp 6: issuing a copy holds its warp a
+// while, and neither warp has a part in the first step of the solve, nor
+// warp 5 in writing the chunk vectors, where they issue.
 template <bool kRawGates>
 __device__ __forceinline__ void prep_role(const PrefillArgs &a, const SplitArgs &s, const CUtensorMap *tm_qkv,
                                           const CUtensorMap *tm_qk, const CUtensorMap *tm_u, const CUtensorMap *tm_nw,
@@ -223,7 +226,7 @@ __device__ __forceinline__ void prep_role(const PrefillArgs &a, const SplitArgs 
   const uint32_t tl = tmem + ((uint32_t)(32 * quad) << 16);
   const uint32_t id_kk = idesc(128, 64, 0, 0), id_mk = idesc(128, 64, 1, 0);
   uint32_t ph_kq = 0, ph_raw = 0, ph_qk = 0, ph_uw = 0;
-  bool q_req = false, k_req = false, raw_pending = false;  // thread 0: loads in flight
+  bool q_req = false, k_req = false, raw_pending = false;  // kLoadTid: loads in flight
   bool stores = false;  // kStoreTid: stores issued
   long long pub = -1;   // kStoreTid: the item whose outputs are in flight, flagged once they land
   bool first = true;
@@ -262,7 +265,7 @@ __device__ __forceinline__ void prep_role(const PrefillArgs &a, const SplitArgs 
       pub = -1;
     }
   };
-  // Thread 0: an item's q^ rows (rows 64-127 of [K;Q]) and k^ hi rows (rows
+  // kLoadTid: an item's q^ rows (rows 64-127 of [K;Q]) and k^ hi rows (rows
   // 0-63) complete one phase of bar_kq: the first part only announces its
   // bytes, the second arrives.  The raw v rows complete bar_raw.
   auto load_kq_part = [&](long long it, const ChunkLoc &c, int plane) {
@@ -307,7 +310,7 @@ __device__ __forceinline__ void prep_role(const PrefillArgs &a, const SplitArgs 
   long long item = 0;
   long long it = next_valid(G.first, c, item);
   if (it < nitems) {
-    if (tid == 0) {
+    if (tid == kLoadTid) {
       request_q(item, c);
       request_k(item, c);
       request_raw(item, c);
@@ -334,11 +337,11 @@ __device__ __forceinline__ void prep_role(const PrefillArgs &a, const SplitArgs 
     const bool raw_ok = kq_ok && bar_wait(&V.bar_raw, ph_raw);
     if (kq_ok) {
       ph_kq ^= 1u;
-      if (tid == 0) q_req = k_req = false;
+      if (tid == kLoadTid) q_req = k_req = false;
     }
     if (raw_ok) {
       ph_raw ^= 1u;
-      if (tid == 0) raw_pending = false;
+      if (tid == kLoadTid) raw_pending = false;
     }
     bool ok = raw_ok;
     if (group_sync_or(G, !ok)) {
@@ -415,8 +418,6 @@ __device__ __forceinline__ void prep_role(const PrefillArgs &a, const SplitArgs 
       }
       break;
     }
-    // MMA1 is done with the q^ rows: the next item's may land.
-    if (tid == 0 && more) request_q(next, cn);
     // L (fp32, strictly lower, decayed beta K K^T) and M (fp16, decayed Q K^T incl. the diagonal)
     {
       float v[32], rr[32];
@@ -476,17 +477,17 @@ __device__ __forceinline__ void prep_role(const PrefillArgs &a, const SplitArgs 
     }
     // T = (I + L)^{-1} and the fp16 tiles (their upper blocks are zeroed
     // again: the previous item's -W^T and U^T staging used their space).
-    // With flags, the store thread sets the previous item's flag once its
-    // outputs have landed while the diagonal blocks are solved.
+    // Meanwhile (the diagonal blocks) the store thread sets the previous
+    // item's flag once its outputs have landed (with flags), and the next
+    // item's q^ rows are requested (MMA1 is long done with them).
     solve_T(ss, CV, tid, G.bar_solve, true, [&]() {
       if (tid == kStoreTid && G.flags) publish(true);
+      if (tid == kLoadTid && more) request_q(next, cn);
     });
     fence_smem_to_async();
     fence_before();
     group_sync(G);
-    // L is done with: the next item's raw v rows may land.  MMA U (hi*hi +
-    // lo*hi + hi*lo, A = V^T from TMEM) and MMA W (warp 0).
-    if (tid == 0 && more) request_raw(next, cn);
+    // MMA U (hi*hi + lo*hi + hi*lo, A = V^T from TMEM) and MMA W (warp 0).
     if (warp == 0) {
       fence_after();
       auto b_tu = [&](int ks) { return desc_k(sbase + P_TU, ks, kC); };
@@ -503,6 +504,7 @@ __device__ __forceinline__ void prep_role(const PrefillArgs &a, const SplitArgs 
       // the store thread's release; no fence of its own)
       if (in_bounds(item * (2 * kC) + tid + 1, nitems * (2 * kC), a.err)) vec[tid] = tid < kC ? CV.d[tid] : CV.gam[tid - kC];
     }
+    if (tid == kLoadTid && more) request_raw(next, cn);  // L is done with: the next item's raw v rows may land
     if (warp == kGateWarp && more) {  // the next item's chunk vectors; the gates of the one after it
       form_vectors(cn, V.cv[(k + 1) & 1]);
       ChunkLoc c2{};
@@ -522,7 +524,7 @@ __device__ __forceinline__ void prep_role(const PrefillArgs &a, const SplitArgs 
     }
     // MMA W is done with the k^ rows: the next item's may land.  The M store
     // has long read its source (whose space takes U^T box 0).
-    if (tid == 0 && more) request_k(next, cn);
+    if (tid == kLoadTid && more) request_k(next, cn);
     if (tid == kStoreTid) bulk_wait_read();
     group_sync(G);
     {
@@ -564,7 +566,7 @@ __device__ __forceinline__ void prep_role(const PrefillArgs &a, const SplitArgs 
     bulk_wait_all();
     if (G.flags) publish(false);
   }
-  if (tid == 0) {
+  if (tid == kLoadTid) {
     if (q_req && !k_req) mbar_arrive(&V.bar_kq);
     if (q_req || k_req) bar_wait(&V.bar_kq, ph_kq);
     if (raw_pending) bar_wait(&V.bar_raw, ph_raw);
