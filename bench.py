@@ -469,10 +469,12 @@ def gdn_arm(args, world, rank, local):
         ev_out[bsel].record(s_out)
         used[bsel] = True
 
-    for k in range(2):
+    # two untimed repetitions (on some hosts the first passes over freshly
+    # pinned buffers run several times slower), then three timed ones; the
+    # median is reported
+    for k in range(2 * e2e_steps):
         e2e_step(k)
     barrier()
-    # three repetitions of e2e_steps steps each; the median is reported
     e2e_reps = []
     for _ in range(3):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
