@@ -12,9 +12,10 @@
 // barrier sits inside the state pass.  decode1_kernel: one CTA per pair,
 // lane L holding columns 4L .. 4L + 3 of the warp's rows.  decode_kernel:
 // persistent (two CTAs per SM walking the pairs), the next pair's state
-// copied into shared memory while the current pair's T serial token steps
-// run, and lane (rg, cg) holding 4 rows x 16 columns, so that a token's dot
-// products reduce over 8 lanes.
+// (and, with bf16 io, its raw rows, window, conv weights and z) copied into
+// shared memory while the current pair's T serial token steps run, and lane
+// (rg, cg) holding 4 rows x 16 columns, so that a token's dot products reduce
+// over 8 lanes.
 //
 // Per token ("How Qwen3.5 works" section 9.6, decay -> predict -> correct ->
 // read; node gdn.core of the Qwen3.8-27B spec for the v x k orientation):
@@ -247,7 +248,7 @@ template <typename IO, bool kRawGates>
 __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap tm_x,
                                                              const __grid_constant__ CUtensorMap tm_w,
                                                              const __grid_constant__ CUtensorMap tm_z) {
-  constexpr bool kPre = sizeof(IO) == 2;  // inputs by bulk copy (bf16 io)
+  constexpr bool kPre = sizeof(IO) == 2;  // inputs by asynchronous copy (bf16 io)
   extern __shared__ uint8_t decode_smem_raw[];
   DecodeSmem &M = *reinterpret_cast<DecodeSmem *>(decode_smem_raw + ((128 - (umma::smem_u32(decode_smem_raw) & 127)) & 127));
   const Dims d = a.d;
