@@ -141,6 +141,27 @@ def test_split_packed(lengths):
         assert torch.equal(S_T[s], dev(a["S0"][s]))
 
 
+def test_split_packed_many_items_per_group():
+    """A packed batch at the 4B head shape (about 8k tokens, 16/32 heads): each
+    prep group walks a dozen work items or more across sequences of unequal
+    length (the next item's loads, gates and chunk vectors prepared during the
+    current one), then every output against the oracle."""
+    lengths = (1500, 37, 2048, 700, 1000, 0, 2690)
+    p = I.packed_problem(lengths, 16, 32, io="bf16", case=646)
+    cu = torch.from_numpy(p.cu_seqlens).to("cuda")
+    o, S_T, conv_T = _packed_run(p, cu)
+    assert gdn.gdn_device_status() == 0
+    a = p.arrays
+    keep = [s for s, n in enumerate(p.lengths) if n > 0]
+    sub = I.PackedProblem(tuple(p.lengths[s] for s in keep), p.Hk, p.Hv, p.io)
+    ref = O.gdn_prefill_varlen(a["qkv_pre"], a["z"], a["g"], a["beta"], a["conv_w"], a["norm_w"],
+                               sub.cu_seqlens, a["S0"][keep], a["conv0"][keep], Hk=p.Hk, Hv=p.Hv,
+                               threads=O.default_threads())
+    check_o(to_np(o), ref["o"], p.io)
+    check_S(to_np(S_T)[keep], ref["S_T"])
+    np.testing.assert_array_equal(to_np(conv_T)[keep], ref["conv_T"])
+
+
 def test_split_packed_equal_lengths_match_fixed_length():
     """A packed batch of equal lengths uses other chunk slots than the
     fixed-length call but the same arithmetic: bit-identical outputs."""
