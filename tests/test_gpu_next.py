@@ -221,20 +221,23 @@ def test_multi_token_decode(io, T, raw):
     np.testing.assert_array_equal(to_np(conv_out), ref["conv_out"])
 
 
-@pytest.mark.parametrize("T,snap,raw", [(2, False, False), (5, True, False), (8, False, True), (13, False, False)])
-def test_multi_token_decode_many_units(T, snap, raw):
+@pytest.mark.parametrize("io,T,snap,raw", [("bf16", 2, False, False), ("bf16", 5, True, False),
+                                           ("bf16", 8, False, True), ("bf16", 13, False, False),
+                                           ("f32", 3, True, False)])
+def test_multi_token_decode_many_units(io, T, snap, raw):
     """More (sequence, value head) pairs than the persistent T-token kernel has
     CTAs (768 against two per SM), so that each CTA walks two or three pairs
     and every pair after its first arrives by the prefetch (state, raw rows,
-    window, conv weights and z by asynchronous copy, gates in registers)."""
+    window, conv weights and z by asynchronous copy with bf16 io, gates in
+    registers; with fp32 io the state alone)."""
     B, Hk, Hv = 128, 2, 6
-    dp = I.decode_problem(B=B, Hk=Hk, Hv=Hv, io="bf16", steps=T, case=160 + T)
-    t = torch.bfloat16
+    dp = I.decode_problem(B=B, Hk=Hk, Hv=Hv, io=io, steps=T, case=160 + T)
+    t = torch_io(io)
     qkv = np.ascontiguousarray(dp.qkv_pre.transpose(1, 0, 2))
     z = np.ascontiguousarray(dp.z.transpose(1, 0, 2))
     g = np.ascontiguousarray(dp.g.transpose(1, 0, 2))
     beta = np.ascontiguousarray(dp.beta.transpose(1, 0, 2))
-    rg = I.raw_gate_arrays(160 + T, (B, T), Hv, "bf16") if raw else None
+    rg = I.raw_gate_arrays(160 + T, (B, T), Hv, io) if raw else None
     S = dev(dp.S)
     snaps = torch.empty(B, T, Hv, D, D, device="cuda") if snap else None
     conv_out = torch.empty(B, 3, dp.C, device="cuda", dtype=t)
@@ -247,7 +250,7 @@ def test_multi_token_decode_many_units(T, snap, raw):
     ref = O.gdn_decode_multi(qkv, z, None if raw else g, None if raw else beta, dp.conv_w,
                              dp.norm_w, dp.S, dp.conv, Hk=Hk, Hv=Hv,
                              raw_gates=_raw_np(rg) if raw else None)
-    check_o(to_np(o), ref["o"], "bf16")
+    check_o(to_np(o), ref["o"], io)
     check_S(to_np(S), ref["S"])
     if snap:
         for k in range(T):
